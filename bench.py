@@ -1,0 +1,428 @@
+#!/usr/bin/env python3
+"""Benchmark of the KDA decode state update on GB300.
+
+Headline workload: one decode step, N=64 requests x HV=12 value heads,
+K=V=128, fp32 state pool [256, 12, 128, 128], bf16 q/k/v, fp32 gates and
+output (the N=64, HV=12, K=V=128 shape the pages time their gating kernel on:
+ROCm/ATOM pull request 2130, What).  A "step" is one call of kda_decode_step.
+
+Metric: state GB/s = (state bytes read + written + q/k/v/o bytes) / step time.
+
+Timing:
+  * device ("value"): inputs resident in HBM; K steps are launched back to
+    back from a CUDA graph, each on a different one of R state pools whose
+    combined footprint is > 4x the L2, so every step streams its state from
+    HBM and also pays the write-back of earlier steps' dirty lines (the
+    steady state of a model that updates a different layer's pool each step).
+    CUDA events on the launching stream bracket exactly the K steps.
+  * end to end ("e2e"): the same steps through the same C ABI call, but each
+    step copies its inputs (q, k, v, a, b, slot ids) from pinned host memory
+    and reads the output o back; the pools stay resident.
+  * clocks are sampled with nvidia-smi while the timed work runs.
+
+--impl reference times the fp64 CPU oracle (the only reference this method
+has: the pages ship no code) on the host cores, on a bounded sample of the
+same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+REPO = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, REPO)
+
+N, HV, K, V, SLOTS = 64, 12, 128, 128, 256
+METRIC = "KDA decode state GB/s (% of HBM peak) and us/step at N=64, HV=12, K=V=128"
+PEAK_FALLBACK_GBS = 6800.0
+
+
+def algorithmic_bytes(n, hv, k, v, t, state_bytes, qkv_bytes, reads=1, writes=1):
+    """State read + written plus q, k, v (qkv_bytes each) and fp32 o."""
+    state = (reads + writes * t) * n * hv * k * v * state_bytes
+    io = n * t * hv * (2 * k + v) * qkv_bytes + n * t * hv * v * 4
+    return state + io
+
+
+def peaks():
+    path = os.path.join(REPO, "MEASURED_PEAKS.json")
+    try:
+        d = json.load(open(path))
+        return float(d["hbm_gbs"]), "measured", d
+    except Exception:
+        return PEAK_FALLBACK_GBS, "fallback", {}
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason sampling around the timed work."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_id: str | None):
+        self.proc = None
+        self.out = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+               "-lms", "50"]
+        if device_id:
+            cmd += ["-i", device_id]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=self.out, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.out.flush()
+        rows = []
+        for line in open(self.out.name):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append(dict(sm=float(parts[1]), max=float(parts[2]),
+                                 hw=parts[5], hwt=parts[6], swt=parts[7], pcap=parts[8]))
+            except ValueError:
+                continue
+        os.unlink(self.out.name)
+        if not rows:
+            return None
+        reasons = set()
+        for r in rows:
+            for key, name in (("hw", "hw_slowdown"), ("hwt", "hw_thermal_slowdown"),
+                              ("swt", "sw_thermal_slowdown"), ("pcap", "sw_power_cap")):
+                if r[key].lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(r["sm"] for r in rows),
+                "sm_max_mhz": max(r["max"] for r in rows), "reasons": sorted(reasons),
+                "samples": len(rows)}
+
+
+def chunk_size(k, limit=512):
+    for c in range(min(k, limit), 0, -1):
+        if k % c == 0:
+            return c
+    return 1
+
+
+def cpu_oracle_sample(target_s=12.0, nthreads=None):
+    """Time the fp64 oracle on the headline workload: whole decode steps of
+    N=64 x HV=12 on a 256-slot fp32 pool, repeated until about target_s."""
+    import numpy as np
+    import torch
+    import oracle
+    from kda_linear_attention_gated_gb300 import workloads
+    nthreads = nthreads or os.cpu_count() or 1
+    inp = workloads.make_decode(n=N, hv=HV, k=K, v=V, num_slots=SLOTS, state_dtype=torch.float32,
+                                qkv_dtype=torch.bfloat16, seed=0)
+    pool = inp.pool.numpy().copy()
+    args = [x.double().numpy() for x in (inp.q, inp.k, inp.v, inp.a, inp.b)]
+    slots = inp.init_slot.numpy()
+    oracle.decode_step(pool, slots, *args, nthreads=nthreads)  # load + warm
+    steps, t0 = 0, time.perf_counter()
+    while True:
+        oracle.decode_step(pool, slots, *args, nthreads=nthreads)
+        steps += 1
+        el = time.perf_counter() - t0
+        if el >= target_s:
+            break
+    per_step = el / steps
+    gbs = algorithmic_bytes(N, HV, K, V, 1, 4, 2) / per_step / 1e9
+    return dict(value=round(gbs, 4), unit="GB/s", cores=nthreads, kind="oracle",
+                sample=f"{steps} full decode steps (N=64 x HV=12, K=V=128, fp32 pool, bf16 q/k/v) "
+                       f"in {el:.1f} s; {per_step * 1e3:.1f} ms/step",
+                ms_per_step=per_step * 1e3), steps, el
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return 0
+    base, steps_done, el = cpu_oracle_sample(target_s=min(30.0, max(4.0, 0.5 * args.steps)))
+    per_step_ms = base["ms_per_step"]
+    line = {
+        "impl": "reference", "metric": METRIC, "value": base["value"], "unit": "GB/s",
+        "n_gpus": args.gpus, "steps": steps_done, "warmup": 1, "ms_per_step": round(per_step_ms, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": "decode N=64 HV=12 K=V=128 fp32 pool bf16 qkv",
+                                         "l2": "n/a (host)"},
+        "cpu_baseline": {k: base[k] for k in ("value", "unit", "cores", "kind", "sample")},
+        "e2e": {"value": base["value"], "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=2000)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extra", action="store_true", help="skip the fp16 / verify lines")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer measurement")
+    ap.add_argument("--soak-seconds", type=float, default=1.0,
+                    help="minimum untimed load before timing (clocks ramp; 0 under a profiler)")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if args.impl == "reference":
+        return run_reference(args, rank, world)
+
+    import torch
+    import kda_linear_attention_gated_gb300 as kda
+    from kda_linear_attention_gated_gb300 import workloads
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+
+    kda.build()
+    lib32 = kda.KdaLibrary(torch.float32)
+    props = torch.cuda.get_device_properties(local)
+    l2 = getattr(props, "L2_cache_size", 0) or 126 * 2**20
+    dev_uuid = None
+    try:
+        dev_uuid = "GPU-" + str(props.uuid)
+    except Exception:
+        pass
+
+    def make_pools(inp, count):
+        base = inp.pool.to("cuda")
+        return [base] + [base.clone() for _ in range(count - 1)]
+
+    def bench_decode(state_dtype, qkv_dtype, seed, steps, warmup, sample_clocks):
+        lib = kda.KdaLibrary(state_dtype)
+        inp = workloads.make_decode(n=N, hv=HV, k=K, v=V, num_slots=SLOTS, state_dtype=state_dtype,
+                                    qkv_dtype=qkv_dtype, seed=seed)
+        es = 4 if state_dtype == torch.float32 else 2
+        active = N * HV * K * V * es
+        R = max(4, math.ceil(4 * l2 / active) + 1)
+        pools = make_pools(inp, R)
+        d = inp.to("cuda")
+        o = torch.empty(N, HV, V, device="cuda")
+        status = torch.zeros(1, dtype=torch.int32, device="cuda")
+        stream = torch.cuda.Stream()
+        chunk = chunk_size(steps)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            # eager warm-up launch (module load) before capture
+            lib.kda_decode_step(pools[0], d.init_slot, d.q, d.k, d.v, d.a, d.b, o, status)
+            stream.synchronize()
+            with torch.cuda.graph(g, stream=stream):
+                for i in range(chunk):
+                    lib.kda_decode_step(pools[i % R], d.init_slot, d.q, d.k, d.v, d.a, d.b, o, status)
+        # warm-up: at least `warmup` steps and at least ~1 s of load
+        t_w = time.perf_counter()
+        done = 0
+        with torch.cuda.stream(stream):
+            while done < warmup or time.perf_counter() - t_w < args.soak_seconds:
+                g.replay()
+                done += chunk
+                if done % (chunk * 8) == 0:
+                    stream.synchronize()
+        sampler = ClockSampler(dev_uuid) if sample_clocks else None
+        if sample_clocks and args.soak_seconds > 0:
+            with torch.cuda.stream(stream):
+                # keep the GPU loaded while the sampler starts
+                for _ in range(max(1, int(0.3 / max(chunk * 20e-6, 1e-6)))):
+                    g.replay()
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for _ in range(steps // chunk):
+                g.replay()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        if dist is not None:
+            dist.barrier()
+        clocks = sampler.stop() if sampler else None
+        ms = e0.elapsed_time(e1)
+        st = int(status.item())
+        if st != 0:
+            raise RuntimeError(f"device status {st}: {lib.kda_strerror(st)}")
+        return dict(ms_total=ms, us_per_step=ms * 1e3 / steps, pools=R, chunk=chunk,
+                    bytes=algorithmic_bytes(N, HV, K, V, 1, es, 2), clocks=clocks,
+                    pool_bytes=R * pools[0].numel() * es)
+
+    def bench_e2e(steps):
+        """Through the C ABI with host buffers: H2D inputs, kernel, D2H output, per step."""
+        inp = workloads.make_decode(n=N, hv=HV, k=K, v=V, num_slots=SLOTS, state_dtype=torch.float32,
+                                    qkv_dtype=torch.bfloat16, seed=0)
+        R = max(4, math.ceil(4 * l2 / (N * HV * K * V * 4)) + 1)
+        pools = make_pools(inp, R)
+        host = {n: getattr(inp, n).pin_memory() for n in ("init_slot", "q", "k", "v", "a", "b")}
+        dev = {n: torch.empty_like(t, device="cuda") for n, t in host.items()}
+        o = torch.empty(N, HV, V, device="cuda")
+        o_host = torch.empty(N, HV, V).pin_memory()
+        status = torch.zeros(1, dtype=torch.int32, device="cuda")
+        stream = torch.cuda.Stream()
+        h2d = sum(t.numel() * t.element_size() for t in host.values())
+        d2h = o.numel() * 4
+
+        def one(i):
+            for n_, t in host.items():
+                dev[n_].copy_(t, non_blocking=True)
+            lib32.kda_decode_step(pools[i % R], dev["init_slot"], dev["q"], dev["k"], dev["v"],
+                                  dev["a"], dev["b"], o, status, stream=stream)
+            o_host.copy_(o, non_blocking=True)
+
+        with torch.cuda.stream(stream):
+            for i in range(max(3, args.warmup // 10)):
+                one(i)
+        torch.cuda.synchronize()
+        if dist is not None:
+            dist.barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        n_e2e = min(steps, 2000)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for i in range(n_e2e):
+                one(i)
+            e1.record(stream)
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1)
+        return dict(us_per_step=ms * 1e3 / n_e2e, steps=n_e2e, h2d=h2d, d2h=d2h)
+
+    def max_over_ranks(x):
+        if dist is None:
+            return x
+        t = torch.tensor([x], dtype=torch.float64, device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    peak, peak_kind, _ = peaks()
+    head = bench_decode(torch.float32, torch.bfloat16, 0, args.steps, args.warmup, True)
+    us = max_over_ranks(head["us_per_step"])
+    gbs_per_gpu = head["bytes"] / (us * 1e-6) / 1e9
+    value = gbs_per_gpu * world
+    e2e, e2e_us, e2e_gbs = None, None, None
+    if not args.no_e2e:
+        e2e = bench_e2e(args.steps)
+        e2e_us = max_over_ranks(e2e["us_per_step"])
+        e2e_gbs = head["bytes"] / (e2e_us * 1e-6) / 1e9 * world
+
+    extra = {}
+    if not args.no_extra:
+        h16 = bench_decode(torch.float16, torch.bfloat16, 1, min(args.steps, 20000), args.warmup, False)
+        extra["decode_fp16_pool"] = {
+            "us_per_step": round(h16["us_per_step"], 3),
+            "gbs": round(h16["bytes"] / (h16["us_per_step"] * 1e-6) / 1e9, 1),
+            "frac_of_peak": round(h16["bytes"] / (h16["us_per_step"] * 1e-6) / 1e9 / peak, 4),
+            "bytes_per_step": h16["bytes"], "pools": h16["pools"]}
+        extra["verify"] = bench_verify(kda, workloads, torch, args, l2, peak)
+
+    traffic = None
+    tpath = os.path.join(REPO, "profiles", "decode_f32_n64_traffic.json")
+    if os.path.exists(tpath):
+        try:
+            t = json.load(open(tpath))
+            if t.get("source_hash") == kda.source_hash():
+                traffic = t["dram_bytes_per_launch"]
+        except Exception:
+            traffic = None
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        cpu, _, _ = cpu_oracle_sample(target_s=12.0)
+        cpu = {k: cpu[k] for k in ("value", "unit", "cores", "kind", "sample")}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(us / 1e3, 6), "us_per_step": round(us, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic",
+            "config": {"workload": "decode step, N=64 x HV=12, K=V=128, fp32 pool [256,12,128,128], "
+                                   "bf16 q/k/v, fp32 a/b/o", "global_batch": N * world,
+                       "parallelism": f"replicas x{world}",
+                       "l2": f"inputs larger than L2: {head['pools']} rotating pools, "
+                             f"{head['pool_bytes'] / 1e9:.2f} GB > 4 x {l2 / 2**20:.0f} MiB L2",
+                       "launch": f"CUDA graph of {head['chunk']} launches, replayed"},
+            "roofline": {"bound": "hbm", "achieved": round(gbs_per_gpu, 1), "peak": peak,
+                         "unit": "GB/s", "frac": round(gbs_per_gpu / peak, 4),
+                         "traffic": traffic, "peak_kind": peak_kind,
+                         "bytes_per_launch": head["bytes"]},
+            "cpu_baseline": cpu,
+            "e2e": None if e2e is None else {
+                "value": round(e2e_gbs, 2), "unit": "GB/s", "us_per_step": round(e2e_us, 3),
+                "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"],
+                "steps": e2e["steps"]},
+            "gpu_launches": args.steps,
+            "clocks": head["clocks"],
+            "extra": extra,
+        }
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+def bench_verify(kda, workloads, torch, args, l2, peak):
+    """Speculative verify, fp16 pool, N=8 x T=8, HV=12, K=V=128, fp32 inputs."""
+    lib = kda.KdaLibrary(torch.float16)
+    n, t = 8, 8
+    inp = workloads.make_verify(n=n, t=t, hv=HV, k=K, v=V, num_slots=SLOTS,
+                                state_dtype=torch.float16, qkv_dtype=torch.float32, seed=2)
+    per = n * (1 + t) * HV * K * V * 2
+    R = max(4, math.ceil(4 * l2 / per) + 1)
+    base = inp.pool.to("cuda")
+    pools = [base] + [base.clone() for _ in range(R - 1)]
+    d = inp.to("cuda")
+    o = torch.empty(n, t, HV, V, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    stream = torch.cuda.Stream()
+    steps = min(args.steps, 10000)
+    chunk = chunk_size(steps)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        lib.kda_spec_verify(pools[0], d.init_slot, d.snap_slot, d.q, d.k, d.v, d.a, d.b, o, status)
+        stream.synchronize()
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(chunk):
+                lib.kda_spec_verify(pools[i % R], d.init_slot, d.snap_slot, d.q, d.k, d.v, d.a,
+                                    d.b, o, status)
+        for _ in range(max(1, args.warmup // chunk)):
+            g.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(steps // chunk):
+            g.replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    us = e0.elapsed_time(e1) * 1e3 / steps
+    byt = algorithmic_bytes(n, HV, K, V, t, 2, 4)
+    return {"workload": "spec verify, fp16 pool, N=8 x T=8, HV=12, K=V=128, fp32 q/k/v",
+            "us_per_step": round(us, 3), "gbs": round(byt / (us * 1e-6) / 1e9, 1),
+            "frac_of_peak": round(byt / (us * 1e-6) / 1e9 / peak, 4), "bytes_per_step": byt,
+            "pools": R}
+
+
+if __name__ == "__main__":
+    sys.exit(main())

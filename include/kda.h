@@ -1,0 +1,160 @@
+/*
+ * kda.h -- C ABI of the GB300 (sm_103a) KDA recurrent-state library.
+ *
+ * Kimi Delta Attention (KDA) keeps, per layer, request slot and value head, a
+ * recurrent state S of shape [K][V] (V innermost).  At decode and at
+ * speculative verify each token applies the fused sigmoid-gated delta rule
+ *
+ *     khat = k / sqrt(sum k^2 + 1e-6),  qhat = q / sqrt(sum q^2 + 1e-6)
+ *     beta = sigmoid(b),                alpha_i = exp(-softplus(a_i))
+ *     S <- diag(alpha) S;   u = S^T khat;   S <- S + beta khat (v - u)^T
+ *     o = S^T qhat / sqrt(K)
+ *
+ * (ROCm/ATOM pull request 2130, "perf(kimi-k3): make the KDA temporal state
+ * dtype configurable", What: the [12,128,128] state, q and k normalised in the
+ * kernel, fused sigmoid gating; ROCm/ATOM pull request 2945, Summary and
+ * Changes: the state pool's dtype is a build constant, a loaded fp16 state is
+ * widened to fp32, the recurrence runs in fp32, a stored state is rounded to
+ * fp16 to nearest even, and every state access goes through one address
+ * function state_at(c, slot).)
+ *
+ * One library file is built per pool dtype: libkda_h0.so (fp32 pool) and
+ * libkda_h1.so (fp16 pool), after the _h0/_h1 kernel names of pull request
+ * 2945 (Changes).  A pool of the other dtype is refused at call time.
+ *
+ * Conventions for every entry point:
+ *  - Return value: KDA_OK (0) or a kda_status code; argument errors are
+ *    detected on the host, synchronously, before anything is launched.
+ *  - Memory: the caller owns every buffer and the stream; the library
+ *    allocates nothing, keeps no state between calls and never synchronises.
+ *    Pointers marked "device" must be device-accessible (cudaMalloc'd);
+ *    pointers marked "host" are read on the host during the call.
+ *  - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
+ *    stream) and runs asynchronously; outputs are valid once it completes.
+ *  - Device-side errors (a slot id outside [0, num_slots)) do not trap: the
+ *    affected (request, head) tiles are skipped and the first such error code
+ *    is written to *dev_status, which the caller zeroes before the call and
+ *    reads after synchronising.
+ *  - Preconditions not checked on the hot path: the slot ids of different
+ *    requests (and the snapshot slots of one call) are pairwise distinct, and
+ *    no other work touches those slots while the call runs.
+ */
+#ifndef KDA_H_
+#define KDA_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum kda_dtype {
+    KDA_F32 = 0,   /* IEEE binary32 */
+    KDA_F16 = 1,   /* IEEE binary16 */
+    KDA_BF16 = 2   /* bfloat16: accepted for q/k/v, refused for a state pool */
+} kda_dtype;
+
+typedef enum kda_status {
+    KDA_OK = 0,
+    KDA_ERR_NULL = 1,              /* a required pointer is NULL */
+    KDA_ERR_DTYPE_MISMATCH = 2,    /* pool dtype is not this library's build dtype */
+    KDA_ERR_DTYPE_UNSUPPORTED = 3, /* pool dtype other than fp32/fp16 (bf16 included), or a bad q/k/v dtype */
+    KDA_ERR_LAYERS_DISAGREE = 4,   /* kda_pool_check: layers differ in dtype or shape */
+    KDA_ERR_SHAPE = 5,             /* K or V outside 16..128 or not a multiple of 16; bad counts or strides */
+    KDA_ERR_ALIGN = 6,             /* pool base or slot stride not 16-byte aligned; an input not naturally aligned */
+    KDA_ERR_LAUNCH = 7,            /* the CUDA launch itself failed */
+    KDA_ERR_SLOT_RANGE = 8,        /* device: a slot id outside [0, num_slots); its tiles were skipped */
+    KDA_ERR_ARG = 9                /* any other bad argument (negative counts, n_layers < 1) */
+} kda_status;
+
+/*
+ * One layer's state pool: num_slots slots, each holding hv heads of a [k][v]
+ * state (v innermost, row-major), all in device memory.
+ *   state_at(slot, h) = base + (slot * slot_stride + h * k * v) elements.
+ * slot_stride is in elements and must be >= hv * k * v (pass hv * k * v for a
+ * dense pool); slot_stride * element size must be a multiple of 16 bytes and
+ * base must be 16-byte aligned (the kernels move the state in 16-byte vectors).
+ */
+typedef struct kda_pool {
+    void* base;           /* device */
+    int32_t dtype;        /* kda_dtype: KDA_F32 or KDA_F16 */
+    int32_t hv;           /* value heads per slot */
+    int32_t k;            /* key dimension K: 16..128, multiple of 16 */
+    int32_t v;            /* value dimension V: 16..128, multiple of 16 */
+    int64_t num_slots;    /* slots in the pool */
+    int64_t slot_stride;  /* elements from one slot to the next */
+} kda_pool;
+
+/* The pool dtype this library was built for: KDA_F32 (libkda_h0) or KDA_F16
+ * (libkda_h1).  (Pull request 2945, Changes: the dtype is a build-key field.) */
+int kda_build_state_dtype(void);
+
+/*
+ * Host-only check of the pools of n_layers layers (no device access): every
+ * pool is fp32 or fp16 (else KDA_ERR_DTYPE_UNSUPPORTED), all layers share one
+ * dtype, hv, k and v (else KDA_ERR_LAYERS_DISAGREE), that dtype is this
+ * build's (else KDA_ERR_DTYPE_MISMATCH), and each pool's shape and alignment
+ * are valid (KDA_ERR_SHAPE / KDA_ERR_ALIGN / KDA_ERR_NULL).
+ * (Pull request 2945, Changes: one recurrent dtype across every layer; a step
+ * refuses a pool of the other dtype; only fp32 or fp16 are accepted because
+ * anything else would be reinterpreted rather than converted.)
+ * pools: host array [n_layers].
+ */
+int kda_pool_check(const kda_pool* pools, int32_t n_layers);
+
+/*
+ * Host-only: the bytes of state one slot of `pool` holds (hv * k * v * element
+ * size) in *bytes_per_slot (host).  Returns KDA_ERR_DTYPE_UNSUPPORTED for a
+ * dtype other than fp32/fp16.  (Pull request 2130, Memory: the per-slot state
+ * size scales with the element size.)
+ */
+int kda_state_bytes(const kda_pool* pool, int64_t* bytes_per_slot);
+
+/*
+ * One decode token for each of n requests, all value heads.  The state of
+ * request r is read from slot slot_ids[r] (or taken as zero when reset[r] is
+ * nonzero), updated, and written back in place to the same slot.
+ *   pool      host pointer to the descriptor; the pool memory is device.
+ *   slot_ids  device int32 [n].
+ *   reset     device uint8 [n], or NULL for "no request resets".
+ *   q, k      device [n][hv][k] of qkv_dtype (KDA_F32, KDA_F16 or KDA_BF16).
+ *   v         device [n][hv][v] of qkv_dtype.
+ *   a         device fp32 [n][hv][k]: decay logits; alpha = exp(-softplus(a)).
+ *   b         device fp32 [n][hv]: beta logits; beta = sigmoid(b).
+ *   o         device fp32 [n][hv][v] (output).
+ *   dev_status device int32 [1]; the caller zeroes it; see conventions.
+ * n == 0 is a no-op returning KDA_OK after the pool checks (buffers may then be NULL).
+ */
+int kda_decode_step(const kda_pool* pool, const int32_t* slot_ids, const uint8_t* reset,
+                    int32_t n, const void* q, const void* k, const void* v,
+                    int32_t qkv_dtype, const float* a, const float* b, float* o,
+                    int32_t* dev_status, void* stream);
+
+/*
+ * Speculative verify: t tokens per request (the accepted token and the draft
+ * tokens), applied one after another.  The state of request r is read once
+ * from init_slot[r] (or zero when reset[r] is nonzero), carried in fp32
+ * between tokens without rounding, and after token j it is stored (rounded to
+ * the pool's dtype) to snapshot slot snap_slot[r][j].  init_slot[r] itself is
+ * not written unless it is also one of the snapshot slots.
+ * (Pull request 2945, Changes: state_at serves each token's snapshot slot.)
+ *   init_slot device int32 [n];  snap_slot device int32 [n][t].
+ *   q, k      device [n][t][hv][k] of qkv_dtype;  v device [n][t][hv][v].
+ *   a         device fp32 [n][t][hv][k];  b device fp32 [n][t][hv].
+ *   o         device fp32 [n][t][hv][v] (output).
+ * Other arguments as for kda_decode_step.  n == 0 or t == 0 is a no-op
+ * returning KDA_OK after the pool checks (buffers may then be NULL).
+ */
+int kda_spec_verify(const kda_pool* pool, const int32_t* init_slot, const int32_t* snap_slot,
+                    const uint8_t* reset, int32_t n, int32_t t, const void* q,
+                    const void* k, const void* v, int32_t qkv_dtype, const float* a,
+                    const float* b, float* o, int32_t* dev_status, void* stream);
+
+/* A static, human-readable string for a kda_status code. */
+const char* kda_strerror(int32_t code);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KDA_H_ */

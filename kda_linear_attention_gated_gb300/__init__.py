@@ -1,0 +1,227 @@
+"""Python binding of the GB300 KDA recurrent-state library (include/kda.h).
+
+Argument marshalling only: every step of the state update runs in the CUDA
+kernels of ``libkda_h0.so`` (fp32 pool) / ``libkda_h1.so`` (fp16 pool).  There
+is no CPU fallback: if the library is missing, ``KdaLibrary`` raises.
+
+    import torch, kda_linear_attention_gated_gb300 as kda
+    lib = kda.KdaLibrary(torch.float16)          # loads libkda_h1.so
+    pool = torch.zeros(256, 12, 128, 128, dtype=torch.float16, device="cuda")
+    lib.kda_decode_step(pool, slot_ids, q, k, v, a, b, o, status)
+
+Tensors are PyTorch CUDA tensors (PyTorch supplies device memory and the
+stream); the calls are asynchronous on ``stream`` (default: the current
+PyTorch stream).  Names follow the C ABI one to one.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+from ._build import LIB_DIR, SOURCES, build, lib_path  # noqa: F401  (re-exported)
+
+__all__ = ["KdaError", "KdaLibrary", "PoolDesc", "build", "lib_path",
+           "KDA_F32", "KDA_F16", "KDA_BF16", "KDA_OK", "KDA_ERR_NULL",
+           "KDA_ERR_DTYPE_MISMATCH", "KDA_ERR_DTYPE_UNSUPPORTED", "KDA_ERR_LAYERS_DISAGREE",
+           "KDA_ERR_SHAPE", "KDA_ERR_ALIGN", "KDA_ERR_LAUNCH", "KDA_ERR_SLOT_RANGE",
+           "KDA_ERR_ARG", "EXPORTED_SYMBOLS"]
+
+KDA_F32, KDA_F16, KDA_BF16 = 0, 1, 2
+(KDA_OK, KDA_ERR_NULL, KDA_ERR_DTYPE_MISMATCH, KDA_ERR_DTYPE_UNSUPPORTED,
+ KDA_ERR_LAYERS_DISAGREE, KDA_ERR_SHAPE, KDA_ERR_ALIGN, KDA_ERR_LAUNCH,
+ KDA_ERR_SLOT_RANGE, KDA_ERR_ARG) = range(10)
+
+EXPORTED_SYMBOLS = ("kda_build_state_dtype", "kda_pool_check", "kda_state_bytes",
+                    "kda_decode_step", "kda_spec_verify", "kda_strerror")
+
+
+class KdaError(RuntimeError):
+    def __init__(self, code: int, what: str, msg: str):
+        super().__init__(f"{what}: {msg} (status {code})")
+        self.code = code
+
+
+class PoolDesc(ctypes.Structure):
+    """Mirror of ``struct kda_pool`` (include/kda.h)."""
+    _fields_ = [("base", ctypes.c_void_p), ("dtype", ctypes.c_int32), ("hv", ctypes.c_int32),
+                ("k", ctypes.c_int32), ("v", ctypes.c_int32), ("num_slots", ctypes.c_int64),
+                ("slot_stride", ctypes.c_int64)]
+
+
+def source_hash() -> str:
+    """Short hash of the CUDA sources: profile summaries record it, so a number
+    measured on an older kernel is recognised as stale."""
+    import hashlib
+    h = hashlib.sha256()
+    for path in SOURCES:
+        with open(path, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def _dtype_code(dt) -> int:
+    import torch
+    table = {torch.float32: KDA_F32, torch.float16: KDA_F16, torch.bfloat16: KDA_BF16}
+    if dt not in table:
+        raise ValueError(f"dtype {dt} has no kda_dtype code")
+    return table[dt]
+
+
+def pool_desc(pool) -> PoolDesc:
+    """Descriptor of a [num_slots, hv, k, v] tensor whose inner three dims are dense."""
+    if pool.dim() != 4:
+        raise ValueError("a state pool is a [num_slots, hv, k, v] tensor")
+    ns, hv, k, v = pool.shape
+    if pool.stride(3) != 1 or pool.stride(2) != v or pool.stride(1) != k * v:
+        raise ValueError("the [hv, k, v] part of a state pool must be dense (v innermost)")
+    return PoolDesc(pool.data_ptr(), _dtype_code(pool.dtype), hv, k, v, ns, pool.stride(0))
+
+
+def _ptr(t) -> int | None:
+    return None if t is None else t.data_ptr()
+
+
+def _expect(name, t, shape, dtypes) -> None:
+    """Shape/dtype/contiguity/device check, so that no kernel indexes past a buffer."""
+    if t is None:
+        raise ValueError(f"{name} is required")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+    if t.dtype not in dtypes:
+        raise ValueError(f"{name} has dtype {t.dtype}, expected one of {dtypes}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+
+
+_libs: dict[bool, ctypes.CDLL] = {}
+_lock = threading.Lock()
+
+
+def _load(state16: bool) -> ctypes.CDLL:
+    with _lock:
+        if state16 in _libs:
+            return _libs[state16]
+        path = lib_path(state16)
+        if not os.path.exists(path):
+            raise RuntimeError(
+                f"KDA CUDA library {path} is missing; build it with "
+                "kda_linear_attention_gated_gb300.build() (there is no CPU fallback)")
+        import torch  # noqa: F401  -- loads the CUDA runtime the library shares
+        lib = ctypes.CDLL(path)
+        P = ctypes.POINTER(PoolDesc)
+        vp, i32 = ctypes.c_void_p, ctypes.c_int32
+        lib.kda_build_state_dtype.restype = ctypes.c_int
+        lib.kda_build_state_dtype.argtypes = []
+        lib.kda_pool_check.restype = ctypes.c_int
+        lib.kda_pool_check.argtypes = [P, i32]
+        lib.kda_state_bytes.restype = ctypes.c_int
+        lib.kda_state_bytes.argtypes = [P, ctypes.POINTER(ctypes.c_int64)]
+        lib.kda_decode_step.restype = ctypes.c_int
+        lib.kda_decode_step.argtypes = [P, vp, vp, i32, vp, vp, vp, i32, vp, vp, vp, vp, vp]
+        lib.kda_spec_verify.restype = ctypes.c_int
+        lib.kda_spec_verify.argtypes = [P, vp, vp, vp, i32, i32, vp, vp, vp, i32, vp, vp, vp, vp, vp]
+        lib.kda_strerror.restype = ctypes.c_char_p
+        lib.kda_strerror.argtypes = [i32]
+        _libs[state16] = lib
+        return lib
+
+
+class KdaLibrary:
+    """One build of the library: ``state_dtype`` torch.float32 -> libkda_h0, float16 -> libkda_h1."""
+
+    def __init__(self, state_dtype):
+        import torch
+        if state_dtype not in (torch.float32, torch.float16):
+            raise ValueError("the state pool dtype of a build is fp32 or fp16")
+        self.state_dtype = state_dtype
+        self.lib = _load(state_dtype == torch.float16)
+        self.path = lib_path(state_dtype == torch.float16)
+
+    # -- helpers ------------------------------------------------------------
+    def _check(self, rc: int, what: str) -> None:
+        if rc != KDA_OK:
+            raise KdaError(rc, what, self.kda_strerror(rc))
+
+    @staticmethod
+    def _stream(stream) -> int | None:
+        import torch
+        if stream is None:
+            stream = torch.cuda.current_stream()
+        return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+    # -- the C ABI, one to one ---------------------------------------------
+    def kda_build_state_dtype(self) -> int:
+        return self.lib.kda_build_state_dtype()
+
+    def kda_strerror(self, code: int) -> str:
+        return self.lib.kda_strerror(int(code)).decode()
+
+    def kda_pool_check_raw(self, descs) -> int:
+        arr = (PoolDesc * len(descs))(*descs)
+        return self.lib.kda_pool_check(arr, len(descs))
+
+    def kda_pool_check(self, pools) -> None:
+        """Raise KdaError unless every layer's pool is valid for this build."""
+        self._check(self.kda_pool_check_raw([pool_desc(p) for p in pools]), "kda_pool_check")
+
+    def kda_state_bytes(self, pool) -> int:
+        desc = pool if isinstance(pool, PoolDesc) else pool_desc(pool)
+        out = ctypes.c_int64(0)
+        self._check(self.lib.kda_state_bytes(ctypes.byref(desc), ctypes.byref(out)), "kda_state_bytes")
+        return out.value
+
+    def kda_decode_step_raw(self, desc: PoolDesc, slot_ids, reset, n, q, k, v, qkv_dtype,
+                            a, b, o, status, stream) -> int:
+        return self.lib.kda_decode_step(ctypes.byref(desc), slot_ids, reset, n, q, k, v,
+                                        qkv_dtype, a, b, o, status, stream)
+
+    def kda_decode_step(self, pool, slot_ids, q, k, v, a, b, o, status, reset=None,
+                        stream=None) -> None:
+        """One decode token per request; ``pool`` is updated in place (see include/kda.h)."""
+        import torch
+        desc = pool_desc(pool)
+        n, hv, kd, vd = int(slot_ids.shape[0]), desc.hv, desc.k, desc.v
+        qkv_types = (torch.float32, torch.float16, torch.bfloat16)
+        _expect("slot_ids", slot_ids, (n,), (torch.int32,))
+        for name, t in (("q", q), ("k", k)):
+            _expect(name, t, (n, hv, kd), (q.dtype,) if name == "k" else qkv_types)
+        _expect("v", v, (n, hv, vd), (q.dtype,))
+        _expect("a", a, (n, hv, kd), (torch.float32,))
+        _expect("b", b, (n, hv), (torch.float32,))
+        _expect("o", o, (n, hv, vd), (torch.float32,))
+        _expect("status", status, (1,), (torch.int32,))
+        if reset is not None:
+            _expect("reset", reset, (n,), (torch.uint8,))
+        rc = self.kda_decode_step_raw(
+            desc, _ptr(slot_ids), _ptr(reset), int(slot_ids.shape[0]), _ptr(q), _ptr(k),
+            _ptr(v), _dtype_code(q.dtype), _ptr(a), _ptr(b), _ptr(o), _ptr(status),
+            self._stream(stream))
+        self._check(rc, "kda_decode_step")
+
+    def kda_spec_verify(self, pool, init_slot, snap_slot, q, k, v, a, b, o, status,
+                        reset=None, stream=None) -> None:
+        """T tokens per request; the state after token t goes to snap_slot[n, t]."""
+        import torch
+        desc = pool_desc(pool)
+        n, t = int(snap_slot.shape[0]), int(snap_slot.shape[1])
+        hv, kd, vd = desc.hv, desc.k, desc.v
+        qkv_types = (torch.float32, torch.float16, torch.bfloat16)
+        _expect("init_slot", init_slot, (n,), (torch.int32,))
+        _expect("snap_slot", snap_slot, (n, t), (torch.int32,))
+        _expect("q", q, (n, t, hv, kd), qkv_types)
+        _expect("k", k, (n, t, hv, kd), (q.dtype,))
+        _expect("v", v, (n, t, hv, vd), (q.dtype,))
+        _expect("a", a, (n, t, hv, kd), (torch.float32,))
+        _expect("b", b, (n, t, hv), (torch.float32,))
+        _expect("o", o, (n, t, hv, vd), (torch.float32,))
+        _expect("status", status, (1,), (torch.int32,))
+        if reset is not None:
+            _expect("reset", reset, (n,), (torch.uint8,))
+        rc = self.lib.kda_spec_verify(
+            ctypes.byref(desc), _ptr(init_slot), _ptr(snap_slot), _ptr(reset), n, t,
+            _ptr(q), _ptr(k), _ptr(v), _dtype_code(q.dtype), _ptr(a), _ptr(b), _ptr(o),
+            _ptr(status), self._stream(stream))
+        self._check(rc, "kda_spec_verify")

@@ -1,0 +1,138 @@
+"""Seeded synthetic inputs for the KDA state update (no KDA arithmetic here).
+
+Every tensor is drawn on the CPU from ``torch.Generator().manual_seed(seed)``
+so that the CUDA path and the CPU oracle see identical bits; callers copy to
+the device.  The shapes and distributions follow the workloads the method is
+measured on (ROCm/ATOM pull request 2130, What and Memory: 69 KDA layers,
+a [12, 128, 128] state per layer and slot, N = 64 requests; pull request 2945,
+Method: 7 draft tokens + 1 under speculative decoding):
+
+  tiny    N=1, HV=2, K=V=16, T=8 decode tokens, fp32 pool of 1 slot; q,k,v fp32
+          N(0,1); a,b N(0,1); S0 N(0, 0.1^2); seed 0
+  decode  N=64, HV=12, K=V=128, pool [256,12,128,128] ~ N(0, 0.1^2); q,k,v bf16
+          N(0,1); a,b fp32 N(0,1); 64 distinct active slots, a seeded random
+          subset (fp32 pool: seed 0; fp16 pool = fp32 draw rounded to nearest
+          even: seed 1)
+  verify  N=8 requests x T=8 tokens, HV=12, K=V=128, fp16 pool of 256 slots;
+          fp32 inputs as in tiny; distinct init slots and 8 distinct snapshot
+          slots per request (all 72 distinct); seed 2
+  sweep   69 layers x N in {1,16,64,128}, own 256-slot pool per layer; slot ids
+          the first N of a seeded permutation; reset ~ Bernoulli(0.05); fp32
+          inputs; seed 3
+
+"N(0, 0.1)" for the state is read as standard deviation 0.1.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass, field
+
+import torch
+
+
+@dataclass
+class StepInputs:
+    """CPU tensors of one call.  For decode, the token axis is absent (T = 1)."""
+    pool: torch.Tensor          # [num_slots, HV, K, V] fp32 or fp16
+    init_slot: torch.Tensor     # int32 [N]
+    q: torch.Tensor             # [N(,T), HV, K]
+    k: torch.Tensor
+    v: torch.Tensor             # [N(,T), HV, V]
+    a: torch.Tensor             # fp32 [N(,T), HV, K]
+    b: torch.Tensor             # fp32 [N(,T), HV]
+    snap_slot: torch.Tensor | None = None  # int32 [N, T] (verify only)
+    reset: torch.Tensor | None = None      # uint8 [N]
+    meta: dict = field(default_factory=dict)
+
+    def to(self, device) -> "StepInputs":
+        mv = lambda t: None if t is None else t.to(device)  # noqa: E731
+        return StepInputs(mv(self.pool), mv(self.init_slot), mv(self.q), mv(self.k), mv(self.v),
+                          mv(self.a), mv(self.b), mv(self.snap_slot), mv(self.reset), dict(self.meta))
+
+
+def _randn(g, shape, dtype=torch.float32, std=1.0):
+    x = torch.randn(shape, generator=g, dtype=torch.float32)
+    if std != 1.0:
+        x = x * std
+    return x.to(dtype)
+
+
+def make_pool(g, num_slots, hv, k, v, state_dtype, std=0.1):
+    """fp32 N(0, std^2), then (fp16 pool) rounded to nearest even by the dtype cast."""
+    return _randn(g, (num_slots, hv, k, v), std=std).to(state_dtype)
+
+
+def make_decode(n=64, hv=12, k=128, v=128, num_slots=256, state_dtype=torch.float32,
+                qkv_dtype=torch.bfloat16, seed=0, reset_p=0.0, pool=True) -> StepInputs:
+    """One decode token for n requests (n distinct slots of a num_slots pool)."""
+    g = torch.Generator().manual_seed(seed)
+    P = make_pool(g, num_slots, hv, k, v, state_dtype) if pool else None
+    slots = torch.randperm(num_slots, generator=g)[:n].to(torch.int32)
+    q = _randn(g, (n, hv, k), qkv_dtype)
+    kk = _randn(g, (n, hv, k), qkv_dtype)
+    vv = _randn(g, (n, hv, v), qkv_dtype)
+    a = _randn(g, (n, hv, k))
+    b = _randn(g, (n, hv))
+    reset = None
+    if reset_p > 0:
+        reset = (torch.rand((n,), generator=g) < reset_p).to(torch.uint8)
+    return StepInputs(P, slots, q, kk, vv, a, b, None, reset,
+                      dict(kind="decode", n=n, hv=hv, k=k, v=v, num_slots=num_slots, seed=seed))
+
+
+def make_verify(n=8, t=8, hv=12, k=128, v=128, num_slots=256, state_dtype=torch.float16,
+                qkv_dtype=torch.float32, seed=2, reset_p=0.0) -> StepInputs:
+    """t tokens for each of n requests; init slots and snapshot slots all distinct."""
+    if n * (t + 1) > num_slots:
+        raise ValueError("not enough slots for distinct init and snapshot slots")
+    g = torch.Generator().manual_seed(seed)
+    P = make_pool(g, num_slots, hv, k, v, state_dtype)
+    perm = torch.randperm(num_slots, generator=g).to(torch.int32)
+    init = perm[:n].clone()
+    snap = perm[n:n + n * t].reshape(n, t).clone()
+    q = _randn(g, (n, t, hv, k), qkv_dtype)
+    kk = _randn(g, (n, t, hv, k), qkv_dtype)
+    vv = _randn(g, (n, t, hv, v), qkv_dtype)
+    a = _randn(g, (n, t, hv, k))
+    b = _randn(g, (n, t, hv))
+    reset = None
+    if reset_p > 0:
+        reset = (torch.rand((n,), generator=g) < reset_p).to(torch.uint8)
+    return StepInputs(P, init, q, kk, vv, a, b, snap, reset,
+                      dict(kind="verify", n=n, t=t, hv=hv, k=k, v=v, num_slots=num_slots, seed=seed))
+
+
+def make_tiny(seed=0):
+    """Config 'tiny': a 1-slot fp32 pool and T=8 decode tokens (returned stacked [T, ...])."""
+    g = torch.Generator().manual_seed(seed)
+    hv, k, v, t = 2, 16, 16, 8
+    P = make_pool(g, 1, hv, k, v, torch.float32)
+    q = _randn(g, (t, 1, hv, k))
+    kk = _randn(g, (t, 1, hv, k))
+    vv = _randn(g, (t, 1, hv, v))
+    a = _randn(g, (t, 1, hv, k))
+    b = _randn(g, (t, 1, hv))
+    return dict(pool=P, slot=torch.zeros(1, dtype=torch.int32), q=q, k=kk, v=vv, a=a, b=b)
+
+
+def make_sweep_layer(layer: int, n: int, state_dtype, hv=12, k=128, v=128, num_slots=256,
+                     seed=3, reset_p=0.05, sentinel=None) -> StepInputs:
+    """One layer of the 69-layer sweep.  Active slots get N(0, 0.1^2) states;
+    the other slots are filled with ``sentinel`` when given (a value no update
+    produces, so stray writes show), else drawn like the active ones."""
+    g = torch.Generator().manual_seed(seed * 1_000_003 + layer * 1009 + n)
+    perm = torch.randperm(num_slots, generator=g)
+    slots = perm[:n].to(torch.int32)
+    if sentinel is None:
+        P = make_pool(g, num_slots, hv, k, v, state_dtype)
+    else:
+        P = torch.full((num_slots, hv, k, v), sentinel, dtype=state_dtype)
+        P[slots.long()] = make_pool(g, n, hv, k, v, state_dtype)
+    q = _randn(g, (n, hv, k))
+    kk = _randn(g, (n, hv, k))
+    vv = _randn(g, (n, hv, v))
+    a = _randn(g, (n, hv, k))
+    b = _randn(g, (n, hv))
+    reset = (torch.rand((n,), generator=g) < reset_p).to(torch.uint8)
+    return StepInputs(P, slots, q, kk, vv, a, b, None, reset,
+                      dict(kind="decode", layer=layer, n=n, hv=hv, k=k, v=v,
+                           num_slots=num_slots, seed=seed))

@@ -1,0 +1,276 @@
+/*
+ * KDA recurrent-state oracle: TEST INFRASTRUCTURE ONLY.
+ *
+ * A plain, slow, fp64 CPU restatement of the Kimi Delta Attention (KDA) gated
+ * delta-rule recurrent-state update at decode and speculative-verify time.
+ * Only the test-suite, the smoke check and the benchmark's CPU-baseline leg
+ * may load this file's library; the product path never does, and this file
+ * shares no code, header or table with the CUDA library.
+ *
+ * Sources (three ROCm/ATOM pull-request pages; cited by number and section):
+ *  - ATOM pull request 2945 (the mono decode kernel K1 takes an fp16 state
+ *    pool), Summary and Changes: a loaded state is widened to fp32, the
+ *    recurrence runs in fp32, a stored state is rounded to fp16 to nearest
+ *    even; one address function state_at(c, slot) serves the initial state
+ *    and each token's snapshot slot.  Limitations: the norm bound -- with a
+ *    unit-norm k, 0 < beta < 1 and alpha <= 1, one token can grow the squared
+ *    norm of state column j by no more than v_j^2.
+ *  - ATOM pull request 2130, "perf(kimi-k3): make the KDA temporal state dtype
+ *    configurable", What: the state of one layer and slot is [HV=12, K=128,
+ *    V=128]; q and k are L2-normalised inside the kernel; the kernel is a
+ *    fused sigmoid-gating delta-rule update.
+ *  - The order of operations (decay, then u = S^T k, then the delta update,
+ *    then o = S^T q / sqrt(K)) and the gate form g = -softplus(a), alpha =
+ *    exp(g), beta = sigmoid(b) are the plainest reading of the method's
+ *    statement; the pages never print the recurrence as an equation.
+ *
+ * Readings where the pages are silent (each one is listed with its reason in
+ * the design notes): L2 norm x / sqrt(sum x^2 + 1e-6); softplus written in
+ * its overflow-free form; the fp64 carry across speculative tokens is never
+ * rounded, only each stored snapshot is; an fp32 pool is stored with the
+ * ordinary fp64 -> fp32 conversion (round to nearest even).
+ *
+ * Everything here is fp64.  The one rounding it performs is the store into the
+ * pool's own element type.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define ORACLE_L2_EPS 1e-6
+
+enum { ORACLE_F32 = 0, ORACLE_F16 = 1 };
+
+/* ------------------------------------------------------------------------ */
+/* IEEE-754 binary16, written from the format's definition:                  */
+/* 1 sign bit, 5 exponent bits (bias 15), 10 fraction bits; subnormal        */
+/* quantum 2^-24; largest finite value 65504.                                */
+/* ------------------------------------------------------------------------ */
+
+double oracle_f16_to_f64(uint16_t h)
+{
+    int sign = (h >> 15) & 1;
+    int expo = (h >> 10) & 0x1f;
+    int frac = h & 0x3ff;
+    double mag;
+    if (expo == 0x1f) {
+        mag = frac ? NAN : INFINITY;
+    } else if (expo == 0) {
+        mag = ldexp((double)frac, -24);                 /* subnormal or zero */
+    } else {
+        mag = ldexp((double)(1024 + frac), expo - 25);  /* (1 + f/1024) 2^(e-15) */
+    }
+    return sign ? -mag : mag;
+}
+
+/* Round an fp64 value to binary16, to nearest, ties to even.  The quantum of
+ * the binade |x| falls in is a power of two, so |x| / quantum is exact, and
+ * rint() (the default rounding mode is nearest-even) does the one rounding. */
+uint16_t oracle_f64_to_f16_rne(double x)
+{
+    uint16_t sign = signbit(x) ? 0x8000 : 0;
+    double ax = fabs(x);
+    if (isnan(x)) return (uint16_t)(sign | 0x7e00);
+    /* Halfway between 65504 and 65536 (the first value past the format)
+     * ties to 65536, whose significand is even: that, and above, is inf. */
+    if (ax >= 65520.0) return (uint16_t)(sign | 0x7c00);
+
+    double quantum;
+    if (ax < ldexp(1.0, -14)) {
+        quantum = ldexp(1.0, -24);
+    } else {
+        int e2;
+        frexp(ax, &e2);                     /* ax = f 2^e2, f in [0.5, 1) */
+        quantum = ldexp(1.0, (e2 - 1) - 10);
+    }
+    double r = rint(ax / quantum) * quantum;  /* the rounded magnitude, exact */
+
+    if (r < ldexp(1.0, -14)) {
+        /* subnormal (or zero): the integer count of 2^-24 quanta */
+        return (uint16_t)(sign | (uint16_t)(r / ldexp(1.0, -24)));
+    }
+    int e2;
+    frexp(r, &e2);
+    int E = e2 - 1;                                   /* r in [2^E, 2^(E+1)) */
+    uint16_t frac = (uint16_t)(r / ldexp(1.0, E - 10) - 1024.0);
+    return (uint16_t)(sign | (uint16_t)((E + 15) << 10) | frac);
+}
+
+void oracle_f64_to_f16_rne_array(const double* x, uint16_t* out, int64_t n)
+{
+    for (int64_t i = 0; i < n; ++i) out[i] = oracle_f64_to_f16_rne(x[i]);
+}
+
+void oracle_f16_to_f64_array(const uint16_t* h, double* out, int64_t n)
+{
+    for (int64_t i = 0; i < n; ++i) out[i] = oracle_f16_to_f64(h[i]);
+}
+
+/* ------------------------------------------------------------------------ */
+/* The pool and its one address function                                     */
+/* ------------------------------------------------------------------------ */
+
+typedef struct {
+    void* base;           /* element 0 of slot 0 */
+    int dtype;            /* ORACLE_F32 or ORACLE_F16 */
+    int64_t num_slots;
+    int hv, k, v;
+    int64_t slot_stride;  /* elements from one slot to the next */
+} oracle_pool;
+
+/* state_at(slot, head): element offset of S[0][0] of one head's [K][V] state
+ * (ATOM PR 2945, Changes: one address function for every state access). */
+static int64_t state_at(const oracle_pool* p, int64_t slot, int h)
+{
+    return slot * p->slot_stride + (int64_t)h * p->k * p->v;
+}
+
+static void load_state(const oracle_pool* p, int64_t slot, int h, double* S)
+{
+    int64_t off = state_at(p, slot, h);
+    int64_t kv = (int64_t)p->k * p->v;
+    if (p->dtype == ORACLE_F32) {
+        const float* src = (const float*)p->base + off;
+        for (int64_t e = 0; e < kv; ++e) S[e] = (double)src[e];
+    } else {
+        const uint16_t* src = (const uint16_t*)p->base + off;
+        for (int64_t e = 0; e < kv; ++e) S[e] = oracle_f16_to_f64(src[e]);
+    }
+}
+
+static void store_state(const oracle_pool* p, int64_t slot, int h, const double* S)
+{
+    int64_t off = state_at(p, slot, h);
+    int64_t kv = (int64_t)p->k * p->v;
+    if (p->dtype == ORACLE_F32) {
+        float* dst = (float*)p->base + off;
+        for (int64_t e = 0; e < kv; ++e) dst[e] = (float)S[e];
+    } else {
+        uint16_t* dst = (uint16_t*)p->base + off;
+        for (int64_t e = 0; e < kv; ++e) dst[e] = oracle_f64_to_f16_rne(S[e]);
+    }
+}
+
+/* ------------------------------------------------------------------------ */
+/* One token of the recurrence on one head's fp64 state S[K][V]              */
+/* ------------------------------------------------------------------------ */
+
+static double softplus(double a)
+{
+    /* log(1 + e^a), in the form that never overflows */
+    return a > 0 ? a + log1p(exp(-a)) : log1p(exp(a));
+}
+
+/*
+ * q, k, a: [K]; v: [V]; b: scalar; o: [V] (out).  Work arrays qh, kh, u: [K or V].
+ *   khat = k / sqrt(sum k^2 + eps), qhat likewise        (L2 norm, in-kernel)
+ *   beta = sigmoid(b); alpha_i = exp(-softplus(a_i))      (fused gating)
+ *   S <- diag(alpha) S                                    (per-key-channel decay)
+ *   u  = S^T khat                                         (what S recalls for k)
+ *   S <- S + beta khat (v - u)^T                          (delta update)
+ *   o  = S^T qhat / sqrt(K)                               (read-out, updated S)
+ */
+static void recur_token(int K, int V, double* S,
+                        const double* q, const double* k, const double* v,
+                        const double* a, double b, double* o,
+                        double* qh, double* kh, double* u)
+{
+    double qq = 0.0, kk = 0.0;
+    for (int i = 0; i < K; ++i) { qq += q[i] * q[i]; kk += k[i] * k[i]; }
+    double qn = sqrt(qq + ORACLE_L2_EPS), kn = sqrt(kk + ORACLE_L2_EPS);
+    for (int i = 0; i < K; ++i) { qh[i] = q[i] / qn; kh[i] = k[i] / kn; }
+
+    double beta = 1.0 / (1.0 + exp(-b));
+
+    for (int i = 0; i < K; ++i) {
+        double alpha = exp(-softplus(a[i]));
+        for (int j = 0; j < V; ++j) S[(int64_t)i * V + j] *= alpha;
+    }
+    for (int j = 0; j < V; ++j) {
+        double s = 0.0;
+        for (int i = 0; i < K; ++i) s += S[(int64_t)i * V + j] * kh[i];
+        u[j] = s;
+    }
+    for (int i = 0; i < K; ++i)
+        for (int j = 0; j < V; ++j)
+            S[(int64_t)i * V + j] += beta * kh[i] * (v[j] - u[j]);
+    double inv_sqrt_k = 1.0 / sqrt((double)K);
+    for (int j = 0; j < V; ++j) {
+        double s = 0.0;
+        for (int i = 0; i < K; ++i) s += S[(int64_t)i * V + j] * qh[i];
+        o[j] = s * inv_sqrt_k;
+    }
+}
+
+/*
+ * The whole step for requests n = 0..N-1, heads h = 0..HV-1, tokens t = 0..T-1.
+ * Inputs are fp64, already widened exactly from whatever type the caller used:
+ *   q, k, a: [N][T][HV][K];  v: [N][T][HV][V];  b: [N][T][HV];  o: [N][T][HV][V].
+ * init_slot[n]: the slot the request's state is read from (unless reset[n]).
+ * snap_slot == NULL (decode, T must be 1): the state is written back in place
+ *   to init_slot[n].
+ * snap_slot != NULL ([N][T], speculative verify): the state after token t is
+ *   written to snap_slot[n*T + t]; init_slot[n] is not written.
+ * reset (may be NULL): reset[n] != 0 starts request n from a zero state.
+ * Returns 0, or -1 when a slot id lies outside [0, num_slots).
+ */
+static int run(const oracle_pool* p, int n_req, int T,
+               const int32_t* init_slot, const int32_t* snap_slot, const uint8_t* reset,
+               const double* q, const double* k, const double* v,
+               const double* a, const double* b, double* o, int nthreads)
+{
+    const int HV = p->hv, K = p->k, V = p->v;
+    for (int n = 0; n < n_req; ++n) {
+        if (init_slot[n] < 0 || init_slot[n] >= p->num_slots) return -1;
+        if (snap_slot)
+            for (int t = 0; t < T; ++t)
+                if (snap_slot[(int64_t)n * T + t] < 0 ||
+                    snap_slot[(int64_t)n * T + t] >= p->num_slots) return -1;
+    }
+    int64_t pairs = (int64_t)n_req * HV;
+    int bad = 0;
+#if defined(_OPENMP)
+#pragma omp parallel for schedule(dynamic, 1) num_threads(nthreads) if (nthreads > 1)
+#endif
+    for (int64_t nh = 0; nh < pairs; ++nh) {
+        int n = (int)(nh / HV), h = (int)(nh % HV);
+        double* S = (double*)malloc(sizeof(double) * ((size_t)K * V + 2 * (size_t)K + (size_t)V));
+        if (!S) { bad = 1; continue; }
+        double* qh = S + (int64_t)K * V;
+        double* kh = qh + K;
+        double* u = kh + K;
+        if (reset && reset[n]) memset(S, 0, sizeof(double) * (size_t)K * V);
+        else load_state(p, init_slot[n], h, S);
+        for (int t = 0; t < T; ++t) {
+            int64_t row = ((int64_t)n * T + t) * HV + h;
+            recur_token(K, V, S, q + row * K, k + row * K, v + row * V,
+                        a + row * K, b[row], o + row * V, qh, kh, u);
+            if (snap_slot) store_state(p, snap_slot[(int64_t)n * T + t], h, S);
+        }
+        if (!snap_slot) store_state(p, init_slot[n], h, S);
+        free(S);
+    }
+    (void)nthreads;
+    return bad ? -2 : 0;
+}
+
+int oracle_decode_step(void* base, int dtype, int64_t num_slots, int hv, int k, int v,
+                       int64_t slot_stride, int n_req, const int32_t* slot_ids,
+                       const uint8_t* reset, const double* q, const double* kk,
+                       const double* vv, const double* a, const double* b, double* o,
+                       int nthreads)
+{
+    oracle_pool p = {base, dtype, num_slots, hv, k, v, slot_stride};
+    return run(&p, n_req, 1, slot_ids, NULL, reset, q, kk, vv, a, b, o, nthreads);
+}
+
+int oracle_spec_verify(void* base, int dtype, int64_t num_slots, int hv, int k, int v,
+                       int64_t slot_stride, int n_req, int T, const int32_t* init_slot,
+                       const int32_t* snap_slot, const uint8_t* reset, const double* q,
+                       const double* kk, const double* vv, const double* a, const double* b,
+                       double* o, int nthreads)
+{
+    oracle_pool p = {base, dtype, num_slots, hv, k, v, slot_stride};
+    return run(&p, n_req, T, init_slot, snap_slot, reset, q, kk, vv, a, b, o, nthreads);
+}

@@ -1,0 +1,160 @@
+"""Host-side tests of the C ABI (no GPU): the libraries build, load, export
+every symbol include/kda.h declares, and refuse bad pools on the host.
+
+kda_pool_check and kda_state_bytes touch no device memory, so they run here
+on fake (never dereferenced) base addresses.  The refusal rules are those of
+ROCm/ATOM pull request 2945 (Changes, Testing): layers must agree on the
+dtype, a pool of the other dtype is refused, and only fp32/fp16 are accepted.
+"""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+import torch
+
+import kda_linear_attention_gated_gb300 as kda
+from kda_linear_attention_gated_gb300 import PoolDesc
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "kda.h")
+FAKE_BASE = 0x7F0000000000  # 16-byte aligned, never dereferenced
+
+
+@pytest.fixture(scope="module")
+def libs(built_libs):
+    return {torch.float32: kda.KdaLibrary(torch.float32), torch.float16: kda.KdaLibrary(torch.float16)}
+
+
+def desc(dtype=kda.KDA_F32, hv=12, k=128, v=128, num_slots=256, slot_stride=None, base=FAKE_BASE):
+    return PoolDesc(base, dtype, hv, k, v, num_slots, hv * k * v if slot_stride is None else slot_stride)
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"^\s*(?:int|const char\*)\s+(kda_\w+)\s*\(", text, re.M)))
+
+
+def test_header_declarations_match_binding():
+    assert declared_functions() == sorted(kda.EXPORTED_SYMBOLS)
+
+
+@pytest.mark.parametrize("state16", [False, True])
+def test_library_exports_every_declared_symbol(built_libs, state16):
+    path = kda.lib_path(state16)
+    out = subprocess.run(["nm", "-D", "--defined-only", path], capture_output=True, text=True,
+                         check=True).stdout
+    exported = set(re.findall(r"\sT\s(\w+)$", out, re.M))
+    for sym in declared_functions():
+        assert sym in exported, f"{sym} missing from {os.path.basename(path)}"
+    lib = ctypes.CDLL(path)
+    for sym in declared_functions():
+        assert getattr(lib, sym) is not None
+
+
+def test_build_dtype(libs):
+    assert libs[torch.float32].kda_build_state_dtype() == kda.KDA_F32
+    assert libs[torch.float16].kda_build_state_dtype() == kda.KDA_F16
+
+
+@pytest.mark.parametrize("sd", [torch.float32, torch.float16])
+def test_pool_check_accepts_agreeing_layers(libs, sd):
+    code = kda.KDA_F32 if sd == torch.float32 else kda.KDA_F16
+    pools = [desc(code, base=FAKE_BASE + i * (1 << 32)) for i in range(69)]
+    assert libs[sd].kda_pool_check_raw(pools) == kda.KDA_OK
+
+
+def test_pool_check_refusals(libs):
+    L32, L16 = libs[torch.float32], libs[torch.float16]
+    # a pool of the other dtype
+    assert L32.kda_pool_check_raw([desc(kda.KDA_F16)]) == kda.KDA_ERR_DTYPE_MISMATCH
+    assert L16.kda_pool_check_raw([desc(kda.KDA_F32)]) == kda.KDA_ERR_DTYPE_MISMATCH
+    # bf16 refused by both builds
+    for L in (L32, L16):
+        assert L.kda_pool_check_raw([desc(kda.KDA_BF16)]) == kda.KDA_ERR_DTYPE_UNSUPPORTED
+        assert L.kda_pool_check_raw([desc(7)]) == kda.KDA_ERR_DTYPE_UNSUPPORTED
+    # layers that disagree on dtype or shape
+    assert L32.kda_pool_check_raw([desc(), desc(kda.KDA_F16)]) == kda.KDA_ERR_LAYERS_DISAGREE
+    assert L16.kda_pool_check_raw([desc(kda.KDA_F16), desc(kda.KDA_F32)]) == kda.KDA_ERR_LAYERS_DISAGREE
+    assert L32.kda_pool_check_raw([desc(), desc(hv=8)]) == kda.KDA_ERR_LAYERS_DISAGREE
+    assert L32.kda_pool_check_raw([desc(), desc(k=64)]) == kda.KDA_ERR_LAYERS_DISAGREE
+    # shapes
+    for bad in (dict(k=8), dict(k=136), dict(v=24), dict(v=0), dict(hv=0), dict(num_slots=0),
+                dict(slot_stride=12 * 128 * 128 - 4)):
+        assert L32.kda_pool_check_raw([desc(**bad)]) == kda.KDA_ERR_SHAPE, bad
+    # alignment
+    assert L32.kda_pool_check_raw([desc(base=FAKE_BASE + 4)]) == kda.KDA_ERR_ALIGN
+    assert L16.kda_pool_check_raw([desc(kda.KDA_F16, slot_stride=12 * 128 * 128 + 2)]) == kda.KDA_ERR_ALIGN
+    assert L16.kda_pool_check_raw([desc(kda.KDA_F16, slot_stride=12 * 128 * 128 + 8)]) == kda.KDA_OK
+    # nulls and counts
+    assert L32.kda_pool_check_raw([desc(base=0)]) == kda.KDA_ERR_NULL
+    assert L32.lib.kda_pool_check(None, 1) == kda.KDA_ERR_NULL
+    arr = (PoolDesc * 1)(desc())
+    assert L32.lib.kda_pool_check(arr, 0) == kda.KDA_ERR_ARG
+
+
+def test_state_bytes(libs):
+    L = libs[torch.float32]
+    assert L.kda_state_bytes(desc()) == 12 * 128 * 128 * 4
+    assert L.kda_state_bytes(desc(kda.KDA_F16)) == 12 * 128 * 128 * 2
+    with pytest.raises(kda.KdaError) as e:
+        L.kda_state_bytes(desc(kda.KDA_BF16))
+    assert e.value.code == kda.KDA_ERR_DTYPE_UNSUPPORTED
+
+
+def test_step_refusals_before_any_launch(libs):
+    """Argument errors come back synchronously from the host checks; the
+    pointers below are never dereferenced because every call is refused."""
+    L32 = libs[torch.float32]
+    P = 0x7F0000100000
+    args = lambda d, **kw: dict(dict(desc=d, slot_ids=P, reset=None, n=4, q=P, k=P, v=P,  # noqa: E731
+                                     qkv_dtype=kda.KDA_BF16, a=P, b=P, o=P, status=P, stream=None), **kw)
+    call = lambda **kw: L32.kda_decode_step_raw(**kw)  # noqa: E731
+    assert call(**args(desc(kda.KDA_F16))) == kda.KDA_ERR_DTYPE_MISMATCH
+    assert call(**args(desc(kda.KDA_BF16))) == kda.KDA_ERR_DTYPE_UNSUPPORTED
+    assert call(**args(desc(), qkv_dtype=9)) == kda.KDA_ERR_DTYPE_UNSUPPORTED
+    assert call(**args(desc(), n=-1)) == kda.KDA_ERR_ARG
+    assert call(**args(desc(), q=None)) == kda.KDA_ERR_NULL
+    assert call(**args(desc(), status=None)) == kda.KDA_ERR_NULL
+    assert call(**args(desc(), a=P + 2)) == kda.KDA_ERR_ALIGN
+    assert call(**args(desc(), q=P + 1)) == kda.KDA_ERR_ALIGN
+    assert call(**args(desc(k=100))) == kda.KDA_ERR_SHAPE
+    # n == 0 is a no-op that succeeds without touching the GPU
+    assert call(**args(desc(), n=0)) == kda.KDA_OK
+    # verify: snapshot ids are required
+    rc = L32.lib.kda_spec_verify(ctypes.byref(desc()), P, None, None, 4, 8, P, P, P,
+                                 kda.KDA_F32, P, P, P, P, None)
+    assert rc == kda.KDA_ERR_NULL
+    rc = L32.lib.kda_spec_verify(ctypes.byref(desc()), P, P, None, 4, 0, P, P, P,
+                                 kda.KDA_F32, P, P, P, P, None)
+    assert rc == kda.KDA_OK
+
+
+def test_strerror_covers_every_code(libs):
+    L = libs[torch.float32]
+    msgs = {c: L.kda_strerror(c) for c in range(10)}
+    assert msgs[0] == "ok"
+    assert len(set(msgs.values())) == 10
+    assert L.kda_strerror(99) == "unknown kda status code"
+
+
+def test_binding_rejects_cpu_and_misshapen_tensors(libs):
+    L = libs[torch.float32]
+    pool = torch.zeros(4, 2, 16, 16)
+    z = lambda *s, dt=torch.float32: torch.zeros(*s, dtype=dt)  # noqa: E731
+    with pytest.raises(ValueError):  # CPU tensors never reach the library
+        L.kda_decode_step(pool, z(2, dt=torch.int32), z(2, 2, 16), z(2, 2, 16), z(2, 2, 16),
+                          z(2, 2, 16), z(2, 2), z(2, 2, 16), z(1, dt=torch.int32))
+    with pytest.raises(ValueError):  # wrong shape
+        L.kda_decode_step(pool, z(2, dt=torch.int32), z(2, 2, 8), z(2, 2, 16), z(2, 2, 16),
+                          z(2, 2, 16), z(2, 2), z(2, 2, 16), z(1, dt=torch.int32))
+    with pytest.raises(ValueError):  # pool whose head part is not dense
+        kda.pool_desc(torch.zeros(4, 2, 16, 32)[..., :16])
+
+
+def test_library_missing_fails_loudly(monkeypatch, tmp_path):
+    import kda_linear_attention_gated_gb300 as pkg
+    monkeypatch.setattr(pkg, "lib_path", lambda s: str(tmp_path / "nope.so"))
+    monkeypatch.setattr(pkg, "_libs", {})
+    with pytest.raises(RuntimeError, match="no CPU fallback"):
+        pkg.KdaLibrary(torch.float32)
