@@ -210,7 +210,7 @@ def main():
         base = inp.pool.to("cuda")
         return [base] + [base.clone() for _ in range(count - 1)]
 
-    def bench_decode(state_dtype, qkv_dtype, seed, steps, warmup, sample_clocks):
+    def bench_decode(state_dtype, qkv_dtype, seed, steps, warmup, sample_clocks, flags):
         lib = kda.KdaLibrary(state_dtype)
         inp = workloads.make_decode(n=N, hv=HV, k=K, v=V, num_slots=SLOTS, state_dtype=state_dtype,
                                     qkv_dtype=qkv_dtype, seed=seed)
@@ -230,7 +230,8 @@ def main():
             stream.synchronize()
             with torch.cuda.graph(g, stream=stream):
                 for i in range(chunk):
-                    lib.kda_decode_step(pools[i % R], d.init_slot, d.q, d.k, d.v, d.a, d.b, o, status)
+                    lib.kda_decode_step(pools[i % R], d.init_slot, d.q, d.k, d.v, d.a, d.b, o, status,
+                                        flags=flags)
         # warm-up: at least `warmup` steps and at least ~1 s of load
         t_w = time.perf_counter()
         done = 0
@@ -314,7 +315,10 @@ def main():
         return float(t.item())
 
     peak, peak_kind, _ = peaks()
-    head = bench_decode(torch.float32, torch.bfloat16, 0, args.steps, args.warmup, True)
+    # Consecutive steps update different pools (as consecutive layers do), so
+    # each launch may start streaming its state while the previous one drains.
+    pdl = kda.KDA_LAUNCH_PDL | kda.KDA_LAUNCH_PDL_EARLY_STATE
+    head = bench_decode(torch.float32, torch.bfloat16, 0, args.steps, args.warmup, True, pdl)
     us = max_over_ranks(head["us_per_step"])
     gbs_per_gpu = head["bytes"] / (us * 1e-6) / 1e9
     value = gbs_per_gpu * world
@@ -326,7 +330,12 @@ def main():
 
     extra = {}
     if not args.no_extra:
-        h16 = bench_decode(torch.float16, torch.bfloat16, 1, min(args.steps, 20000), args.warmup, False)
+        plain = bench_decode(torch.float32, torch.bfloat16, 0, min(args.steps, 20000), args.warmup, False, 0)
+        extra["decode_fp32_pool_no_pdl"] = {
+            "us_per_step": round(plain["us_per_step"], 3),
+            "gbs": round(plain["bytes"] / (plain["us_per_step"] * 1e-6) / 1e9, 1),
+            "frac_of_peak": round(plain["bytes"] / (plain["us_per_step"] * 1e-6) / 1e9 / peak, 4)}
+        h16 = bench_decode(torch.float16, torch.bfloat16, 1, min(args.steps, 20000), args.warmup, False, pdl)
         extra["decode_fp16_pool"] = {
             "us_per_step": round(h16["us_per_step"], 3),
             "gbs": round(h16["bytes"] / (h16["us_per_step"] * 1e-6) / 1e9, 1),
@@ -361,7 +370,8 @@ def main():
                        "parallelism": f"replicas x{world}",
                        "l2": f"inputs larger than L2: {head['pools']} rotating pools, "
                              f"{head['pool_bytes'] / 1e9:.2f} GB > 4 x {l2 / 2**20:.0f} MiB L2",
-                       "launch": f"CUDA graph of {head['chunk']} launches, replayed"},
+                       "launch": f"CUDA graph of {head['chunk']} launches, replayed; "
+                      "flags KDA_LAUNCH_PDL|KDA_LAUNCH_PDL_EARLY_STATE"},
             "roofline": {"bound": "hbm", "achieved": round(gbs_per_gpu, 1), "peak": peak,
                          "unit": "GB/s", "frac": round(gbs_per_gpu / peak, 4),
                          "traffic": traffic, "peak_kind": peak_kind,
@@ -405,7 +415,8 @@ def bench_verify(kda, workloads, torch, args, l2, peak):
         with torch.cuda.graph(g, stream=stream):
             for i in range(chunk):
                 lib.kda_spec_verify(pools[i % R], d.init_slot, d.snap_slot, d.q, d.k, d.v, d.a,
-                                    d.b, o, status)
+                                    d.b, o, status,
+                                    flags=kda.KDA_LAUNCH_PDL | kda.KDA_LAUNCH_PDL_EARLY_STATE)
         for _ in range(max(1, args.warmup // chunk)):
             g.replay()
     torch.cuda.synchronize()

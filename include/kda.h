@@ -31,10 +31,12 @@
  *    pointers marked "host" are read on the host during the call.
  *  - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
  *    stream) and runs asynchronously; outputs are valid once it completes.
- *  - Device-side errors (a slot id outside [0, num_slots)) do not trap: the
- *    affected (request, head) tiles are skipped and the first such error code
- *    is written to *dev_status, which the caller zeroes before the call and
- *    reads after synchronising.
+ *  - Device-side errors do not trap.  A slot id outside [0, num_slots): the
+ *    affected (request, head) tiles are skipped and KDA_ERR_SLOT_RANGE is
+ *    written to *dev_status (first error wins).  A pipeline wait inside the
+ *    kernel that has not completed after 1 s: KDA_ERR_TIMEOUT is written and
+ *    the kernel drains its copies and exits.  The caller zeroes *dev_status
+ *    before the call and reads it after synchronising.
  *  - Preconditions not checked on the hot path: the slot ids of different
  *    requests (and the snapshot slots of one call) are pairwise distinct, and
  *    no other work touches those slots while the call runs.
@@ -61,11 +63,30 @@ typedef enum kda_status {
     KDA_ERR_DTYPE_UNSUPPORTED = 3, /* pool dtype other than fp32/fp16 (bf16 included), or a bad q/k/v dtype */
     KDA_ERR_LAYERS_DISAGREE = 4,   /* kda_pool_check: layers differ in dtype or shape */
     KDA_ERR_SHAPE = 5,             /* K or V outside 16..128 or not a multiple of 16; bad counts or strides */
-    KDA_ERR_ALIGN = 6,             /* pool base or slot stride not 16-byte aligned; an input not naturally aligned */
+    KDA_ERR_ALIGN = 6,             /* pool base, slot stride, q, k, v or a not 16-byte aligned; b, o, ids not 4-byte */
     KDA_ERR_LAUNCH = 7,            /* the CUDA launch itself failed */
     KDA_ERR_SLOT_RANGE = 8,        /* device: a slot id outside [0, num_slots); its tiles were skipped */
-    KDA_ERR_ARG = 9                /* any other bad argument (negative counts, n_layers < 1) */
+    KDA_ERR_ARG = 9,               /* any other bad argument (negative counts, n_layers < 1) */
+    KDA_ERR_TIMEOUT = 10           /* device: a pipeline wait gave up after 1 s; results incomplete */
 } kda_status;
+
+/*
+ * Launch options of kda_decode_step and kda_spec_verify (bitwise OR; 0 = none).
+ *
+ * KDA_LAUNCH_PDL: launch with programmatic stream serialization, so the kernel
+ *   may be scheduled while the previous kernel on the stream is still running
+ *   (it starts its set-up there).  It reads and writes nothing the previous
+ *   kernel may write until that kernel has completed.  Without a previous
+ *   kernel on the stream this has no effect.
+ * KDA_LAUNCH_PDL_EARLY_STATE: with KDA_LAUNCH_PDL, the kernel also reads the
+ *   slot ids, reset flags and its first state tiles before the previous kernel
+ *   has completed, so the state stream overlaps that kernel's tail.  Only valid
+ *   when the previous kernel on the stream writes none of those: e.g. it is a
+ *   projection producing q/k/v/a/b, or a step on another layer's pool.  Two
+ *   back-to-back calls on the same pool must not use it.
+ */
+#define KDA_LAUNCH_PDL 1u
+#define KDA_LAUNCH_PDL_EARLY_STATE 2u
 
 /*
  * One layer's state pool: num_slots slots, each holding hv heads of a [k][v]
@@ -120,15 +141,18 @@ int kda_state_bytes(const kda_pool* pool, int64_t* bytes_per_slot);
  *   q, k      device [n][hv][k] of qkv_dtype (KDA_F32, KDA_F16 or KDA_BF16).
  *   v         device [n][hv][v] of qkv_dtype.
  *   a         device fp32 [n][hv][k]: decay logits; alpha = exp(-softplus(a)).
+ *             q, k, v and a must be 16-byte aligned (they move by bulk copy).
  *   b         device fp32 [n][hv]: beta logits; beta = sigmoid(b).
  *   o         device fp32 [n][hv][v] (output).
  *   dev_status device int32 [1]; the caller zeroes it; see conventions.
+ *   flags     KDA_LAUNCH_* bits (unknown bits: KDA_ERR_ARG).
+ *   stream    cudaStream_t to enqueue on (NULL: the legacy default stream).
  * n == 0 is a no-op returning KDA_OK after the pool checks (buffers may then be NULL).
  */
 int kda_decode_step(const kda_pool* pool, const int32_t* slot_ids, const uint8_t* reset,
                     int32_t n, const void* q, const void* k, const void* v,
                     int32_t qkv_dtype, const float* a, const float* b, float* o,
-                    int32_t* dev_status, void* stream);
+                    int32_t* dev_status, uint32_t flags, void* stream);
 
 /*
  * Speculative verify: t tokens per request (the accepted token and the draft
@@ -148,7 +172,8 @@ int kda_decode_step(const kda_pool* pool, const int32_t* slot_ids, const uint8_t
 int kda_spec_verify(const kda_pool* pool, const int32_t* init_slot, const int32_t* snap_slot,
                     const uint8_t* reset, int32_t n, int32_t t, const void* q,
                     const void* k, const void* v, int32_t qkv_dtype, const float* a,
-                    const float* b, float* o, int32_t* dev_status, void* stream);
+                    const float* b, float* o, int32_t* dev_status, uint32_t flags,
+                    void* stream);
 
 /* A static, human-readable string for a kda_status code. */
 const char* kda_strerror(int32_t code);

@@ -25,12 +25,14 @@ __all__ = ["KdaError", "KdaLibrary", "PoolDesc", "build", "lib_path",
            "KDA_F32", "KDA_F16", "KDA_BF16", "KDA_OK", "KDA_ERR_NULL",
            "KDA_ERR_DTYPE_MISMATCH", "KDA_ERR_DTYPE_UNSUPPORTED", "KDA_ERR_LAYERS_DISAGREE",
            "KDA_ERR_SHAPE", "KDA_ERR_ALIGN", "KDA_ERR_LAUNCH", "KDA_ERR_SLOT_RANGE",
-           "KDA_ERR_ARG", "EXPORTED_SYMBOLS"]
+           "KDA_ERR_ARG", "KDA_ERR_TIMEOUT", "KDA_LAUNCH_PDL", "KDA_LAUNCH_PDL_EARLY_STATE",
+           "EXPORTED_SYMBOLS"]
 
 KDA_F32, KDA_F16, KDA_BF16 = 0, 1, 2
+KDA_LAUNCH_PDL, KDA_LAUNCH_PDL_EARLY_STATE = 1, 2
 (KDA_OK, KDA_ERR_NULL, KDA_ERR_DTYPE_MISMATCH, KDA_ERR_DTYPE_UNSUPPORTED,
  KDA_ERR_LAYERS_DISAGREE, KDA_ERR_SHAPE, KDA_ERR_ALIGN, KDA_ERR_LAUNCH,
- KDA_ERR_SLOT_RANGE, KDA_ERR_ARG) = range(10)
+ KDA_ERR_SLOT_RANGE, KDA_ERR_ARG, KDA_ERR_TIMEOUT) = range(11)
 
 EXPORTED_SYMBOLS = ("kda_build_state_dtype", "kda_pool_check", "kda_state_bytes",
                     "kda_decode_step", "kda_spec_verify", "kda_strerror")
@@ -120,9 +122,10 @@ def _load(state16: bool) -> ctypes.CDLL:
         lib.kda_state_bytes.restype = ctypes.c_int
         lib.kda_state_bytes.argtypes = [P, ctypes.POINTER(ctypes.c_int64)]
         lib.kda_decode_step.restype = ctypes.c_int
-        lib.kda_decode_step.argtypes = [P, vp, vp, i32, vp, vp, vp, i32, vp, vp, vp, vp, vp]
+        u32 = ctypes.c_uint32
+        lib.kda_decode_step.argtypes = [P, vp, vp, i32, vp, vp, vp, i32, vp, vp, vp, vp, u32, vp]
         lib.kda_spec_verify.restype = ctypes.c_int
-        lib.kda_spec_verify.argtypes = [P, vp, vp, vp, i32, i32, vp, vp, vp, i32, vp, vp, vp, vp, vp]
+        lib.kda_spec_verify.argtypes = [P, vp, vp, vp, i32, i32, vp, vp, vp, i32, vp, vp, vp, vp, u32, vp]
         lib.kda_strerror.restype = ctypes.c_char_p
         lib.kda_strerror.argtypes = [i32]
         _libs[state16] = lib
@@ -174,12 +177,12 @@ class KdaLibrary:
         return out.value
 
     def kda_decode_step_raw(self, desc: PoolDesc, slot_ids, reset, n, q, k, v, qkv_dtype,
-                            a, b, o, status, stream) -> int:
+                            a, b, o, status, stream, flags=0) -> int:
         return self.lib.kda_decode_step(ctypes.byref(desc), slot_ids, reset, n, q, k, v,
-                                        qkv_dtype, a, b, o, status, stream)
+                                        qkv_dtype, a, b, o, status, flags, stream)
 
     def kda_decode_step(self, pool, slot_ids, q, k, v, a, b, o, status, reset=None,
-                        stream=None) -> None:
+                        stream=None, flags=0) -> None:
         """One decode token per request; ``pool`` is updated in place (see include/kda.h)."""
         import torch
         desc = pool_desc(pool)
@@ -198,11 +201,11 @@ class KdaLibrary:
         rc = self.kda_decode_step_raw(
             desc, _ptr(slot_ids), _ptr(reset), int(slot_ids.shape[0]), _ptr(q), _ptr(k),
             _ptr(v), _dtype_code(q.dtype), _ptr(a), _ptr(b), _ptr(o), _ptr(status),
-            self._stream(stream))
+            self._stream(stream), flags)
         self._check(rc, "kda_decode_step")
 
     def kda_spec_verify(self, pool, init_slot, snap_slot, q, k, v, a, b, o, status,
-                        reset=None, stream=None) -> None:
+                        reset=None, stream=None, flags=0) -> None:
         """T tokens per request; the state after token t goes to snap_slot[n, t]."""
         import torch
         desc = pool_desc(pool)
@@ -223,5 +226,5 @@ class KdaLibrary:
         rc = self.lib.kda_spec_verify(
             ctypes.byref(desc), _ptr(init_slot), _ptr(snap_slot), _ptr(reset), n, t,
             _ptr(q), _ptr(k), _ptr(v), _dtype_code(q.dtype), _ptr(a), _ptr(b), _ptr(o),
-            _ptr(status), self._stream(stream))
+            _ptr(status), flags, self._stream(stream))
         self._check(rc, "kda_spec_verify")

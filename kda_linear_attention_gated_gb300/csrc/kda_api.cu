@@ -6,36 +6,40 @@
 // following ROCm/ATOM pull request 2945 (Changes): the pool's dtype is a build
 // constant, and a pool of the other dtype is refused at call time.
 //
-// Host side: validate every argument synchronously, pick the column tile by
-// element size, and enqueue exactly one kernel on the caller's stream.
+// Host side: validate every argument synchronously, encode the pool's TMA
+// tensor map, and enqueue exactly one kernel on the caller's stream.
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cstdint>
+#include <map>
+#include <mutex>
+#include <utility>
 
 #include "kda.h"
-#include "kda_kernels.cuh"
+#include "kda_decode_tma.cuh"
+#include "kda_verify_tma.cuh"
 
 #ifndef KDA_STATE16
 #error "build with -DKDA_STATE16=0 (fp32 pool) or -DKDA_STATE16=1 (fp16 pool)"
 #endif
 
-// Column tile (BV) and threads per CTA.  A 2-byte state takes twice the
-// columns of a 4-byte one so that a CTA moves the same bytes (the element-size
-// rule of ROCm/ATOM pull request 2130, What); the values are tuned on GB300.
+// Tile shapes.  A tile is BV state columns x all K rows; BV * element size is
+// 128 bytes, one TMA box row and one swizzle span, so a 2-byte state takes
+// twice the columns of a 4-byte one and a tile moves the same bytes (the
+// element-size rule of ROCm/ATOM pull request 2130, What).  Decode runs one
+// CTA of DEC_NT threads per tile, at least DEC_MINB resident per SM; the values
+// are tuned on GB300.
 #if KDA_STATE16
 using state_t = __half;
 static constexpr int kBuildDtype = KDA_F16;
 #ifndef KDA_DEC_BV
 #define KDA_DEC_BV 64
 #endif
-#ifndef KDA_DEC_NT
-#define KDA_DEC_NT 256
-#endif
 #ifndef KDA_VER_BV
 #define KDA_VER_BV 32
-#endif
-#ifndef KDA_VER_NT
-#define KDA_VER_NT 128
 #endif
 #else
 using state_t = float;
@@ -43,15 +47,15 @@ static constexpr int kBuildDtype = KDA_F32;
 #ifndef KDA_DEC_BV
 #define KDA_DEC_BV 32
 #endif
-#ifndef KDA_DEC_NT
-#define KDA_DEC_NT 128
-#endif
 #ifndef KDA_VER_BV
 #define KDA_VER_BV 32
 #endif
-#ifndef KDA_VER_NT
-#define KDA_VER_NT 128
 #endif
+#ifndef KDA_DEC_NT
+#define KDA_DEC_NT 128
+#endif
+#ifndef KDA_DEC_MINB
+#define KDA_DEC_MINB 8
 #endif
 
 namespace {
@@ -77,6 +81,7 @@ int check_pool_self(const kda_pool* p) {
     if (p->v < 16 || p->v > kda::KMAX || p->v % 16 != 0) return KDA_ERR_SHAPE;
     const int64_t per_slot = (int64_t)p->hv * p->k * p->v;
     if (p->slot_stride < per_slot) return KDA_ERR_SHAPE;
+    if (p->num_slots > 0x7fffffffLL) return KDA_ERR_SHAPE;  // slot ids are int32
     const int es = elem_size(p->dtype);
     if (!aligned(p->base, 16) || (p->slot_stride * es) % 16 != 0) return KDA_ERR_ALIGN;
     return KDA_OK;
@@ -89,26 +94,135 @@ int check_pool_for_build(const kda_pool* p) {
     return KDA_OK;
 }
 
-template <int BV, int NT, bool VERIFY, typename QT>
-int launch_typed(const kda::StepParams& prm, cudaStream_t stream) {
-    const int64_t vt = (prm.v + BV - 1) / BV;
-    const int64_t blocks = (int64_t)prm.n * prm.hv * vt;
-    if (blocks > 0x7fffffffLL) return KDA_ERR_SHAPE;
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    });
+    return fn;
+}
+
+// Tensor map of the pool as a 3-D tensor [num_slots][hv * k][v] (v innermost),
+// box [1][k][bv]: one tile of one head of one slot.  Out-of-range columns of a
+// partial last tile load as zeros and are not stored.
+int make_pool_map(const kda_pool* pool, int bv, CUtensorMap* map) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
+    if (enc == nullptr) return KDA_ERR_LAUNCH;
+    const int es = elem_size(pool->dtype);
+    const cuuint64_t dims[3] = {(cuuint64_t)pool->v, (cuuint64_t)pool->hv * (cuuint64_t)pool->k,
+                                (cuuint64_t)pool->num_slots};
+    const cuuint64_t strides[2] = {(cuuint64_t)pool->v * es, (cuuint64_t)pool->slot_stride * es};
+    const cuuint32_t box[3] = {(cuuint32_t)bv, (cuuint32_t)pool->k, 1u};
+    const cuuint32_t estr[3] = {1u, 1u, 1u};
+    const int rowbytes = bv * es;
+    const CUtensorMapSwizzle sw = rowbytes == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
+                                  : rowbytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                                   : CU_TENSOR_MAP_SWIZZLE_32B;
+    const CUresult r = enc(map, es == 4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                           3, pool->base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? KDA_OK : KDA_ERR_LAUNCH;
+}
+
+// Resident CTAs per SM of `kernel` with `smem` dynamic bytes (also raises the
+// kernel's dynamic shared-memory limit); cached per (kernel, device).
+int occupancy(const void* kernel, int threads, size_t smem, int* blocks_per_sm, int* sms) {
+    static std::mutex mu;
+    static std::map<std::pair<const void*, int>, std::pair<int, int>> cache;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return KDA_ERR_LAUNCH;
+    std::lock_guard<std::mutex> lock(mu);
+    auto it = cache.find({kernel, dev});
+    if (it == cache.end()) {
+        int occ = 0, count = 0;
+        if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+                cudaSuccess ||
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kernel, threads, smem) != cudaSuccess ||
+            cudaDeviceGetAttribute(&count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+            occ < 1)
+            return KDA_ERR_LAUNCH;
+        it = cache.emplace(std::make_pair(kernel, dev), std::make_pair(occ, count)).first;
+    }
+    *blocks_per_sm = it->second.first;
+    *sms = it->second.second;
+    return KDA_OK;
+}
+
+// Programmatic dependent launch attribute when the caller asked for it.
+void set_pdl(cudaLaunchConfig_t& cfg, cudaLaunchAttribute* attr, uint32_t flags) {
+    if (flags & KDA_LAUNCH_PDL) {
+        attr->id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr->val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    }
+}
+
+template <typename QT>
+int launch_decode(const kda_pool* pool, const kda::StepParams& prm, cudaStream_t stream) {
+    constexpr int BV = KDA_DEC_BV, NT = KDA_DEC_NT;
+    constexpr size_t smem = kda::decode_smem_bytes<state_t, BV, NT>();
+    auto kernel = kda::kda_decode_kernel<state_t, QT, BV, NT, KDA_DEC_MINB>;
+    const int64_t tiles = (int64_t)prm.n * prm.hv * ((prm.v + BV - 1) / BV);
+    if (tiles > 0x7fffffffLL) return KDA_ERR_SHAPE;
+    CUtensorMap map;
+    int rc = make_pool_map(pool, BV, &map);
+    if (rc != KDA_OK) return rc;
+    int occ = 0, sms = 0;
+    rc = occupancy(reinterpret_cast<const void*>(kernel), NT, smem, &occ, &sms);
+    if (rc != KDA_OK) return rc;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)blocks, 1, 1);
+    cfg.gridDim = dim3((unsigned)tiles, 1, 1);
     cfg.blockDim = dim3(NT, 1, 1);
-    cfg.dynamicSmemBytes = 0;
+    cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
-    cudaError_t err = cudaLaunchKernelEx(&cfg, kda::kda_step_kernel<state_t, QT, BV, NT, VERIFY>, prm);
+    cudaLaunchAttribute attr;
+    set_pdl(cfg, &attr, prm.flags);
+    const cudaError_t err = cudaLaunchKernelEx(&cfg, kernel, map, prm);
     return err == cudaSuccess ? KDA_OK : KDA_ERR_LAUNCH;
 }
 
-template <int BV, int NT, bool VERIFY>
-int launch(const kda::StepParams& prm, int32_t qkv_dtype, cudaStream_t stream) {
+template <typename QT>
+int launch_verify(const kda_pool* pool, const kda::StepParams& prm, cudaStream_t stream) {
+    constexpr int BV = KDA_VER_BV;
+    using SH = kda::VerifyTmaShape<state_t, BV>;
+    constexpr size_t smem = kda::verify_tma_smem_bytes<state_t, BV>();
+    auto kernel = kda::kda_verify_tma_kernel<state_t, QT, BV>;
+    const int64_t tiles = (int64_t)prm.n * prm.hv * ((prm.v + BV - 1) / BV);
+    if (tiles > 0x7fffffffLL) return KDA_ERR_SHAPE;
+    CUtensorMap map;
+    int rc = make_pool_map(pool, BV, &map);
+    if (rc != KDA_OK) return rc;
+    int occ = 0, sms = 0;
+    rc = occupancy(reinterpret_cast<const void*>(kernel), SH::THREADS, smem, &occ, &sms);
+    if (rc != KDA_OK) return rc;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)tiles, 1, 1);
+    cfg.blockDim = dim3(SH::THREADS, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr;
+    set_pdl(cfg, &attr, prm.flags);
+    const cudaError_t err = cudaLaunchKernelEx(&cfg, kernel, map, prm);
+    return err == cudaSuccess ? KDA_OK : KDA_ERR_LAUNCH;
+}
+
+template <bool VERIFY>
+int launch(const kda_pool* pool, const kda::StepParams& prm, int32_t qkv_dtype, cudaStream_t stream) {
     switch (qkv_dtype) {
-        case KDA_F32: return launch_typed<BV, NT, VERIFY, float>(prm, stream);
-        case KDA_F16: return launch_typed<BV, NT, VERIFY, __half>(prm, stream);
-        case KDA_BF16: return launch_typed<BV, NT, VERIFY, __nv_bfloat16>(prm, stream);
+        case KDA_F32:
+            return VERIFY ? launch_verify<float>(pool, prm, stream) : launch_decode<float>(pool, prm, stream);
+        case KDA_F16:
+            return VERIFY ? launch_verify<__half>(pool, prm, stream) : launch_decode<__half>(pool, prm, stream);
+        case KDA_BF16:
+            return VERIFY ? launch_verify<__nv_bfloat16>(pool, prm, stream)
+                          : launch_decode<__nv_bfloat16>(pool, prm, stream);
         default: return KDA_ERR_DTYPE_UNSUPPORTED;
     }
 }
@@ -116,16 +230,19 @@ int launch(const kda::StepParams& prm, int32_t qkv_dtype, cudaStream_t stream) {
 // Shared argument checks of the two step entry points.
 int check_step_args(const kda_pool* pool, const int32_t* init_slot, int32_t n, int32_t t,
                     const void* q, const void* k, const void* v, int32_t qkv_dtype,
-                    const float* a, const float* b, const float* o, const int32_t* dev_status) {
+                    const float* a, const float* b, const float* o, const int32_t* dev_status,
+                    uint32_t flags) {
     int rc = check_pool_for_build(pool);
     if (rc != KDA_OK) return rc;
     if (n < 0 || t < 0) return KDA_ERR_ARG;
+    if (flags & ~(uint32_t)(KDA_LAUNCH_PDL | KDA_LAUNCH_PDL_EARLY_STATE)) return KDA_ERR_ARG;
     const int qs = elem_size(qkv_dtype);
     if (qs == 0) return KDA_ERR_DTYPE_UNSUPPORTED;
     if (n == 0 || t == 0) return KDA_OK;  // nothing to do; empty buffers may be NULL
     if (!init_slot || !q || !k || !v || !a || !b || !o || !dev_status) return KDA_ERR_NULL;
-    if (!aligned(init_slot, 4) || !aligned(dev_status, 4) || !aligned(a, 4) || !aligned(b, 4) ||
-        !aligned(o, 4) || !aligned(q, qs) || !aligned(k, qs) || !aligned(v, qs))
+    // q, k, v and a rows are moved by 16-byte bulk copies
+    if (!aligned(init_slot, 4) || !aligned(dev_status, 4) || !aligned(b, 4) || !aligned(o, 4) ||
+        !aligned(a, 16) || !aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16))
         return KDA_ERR_ALIGN;
     return KDA_OK;
 }
@@ -133,7 +250,8 @@ int check_step_args(const kda_pool* pool, const int32_t* init_slot, int32_t n, i
 kda::StepParams make_params(const kda_pool* pool, const int32_t* init_slot,
                             const int32_t* snap_slot, const uint8_t* reset, int32_t n,
                             int32_t t, const void* q, const void* k, const void* v,
-                            const float* a, const float* b, float* o, int32_t* dev_status) {
+                            const float* a, const float* b, float* o, int32_t* dev_status,
+                            uint32_t flags) {
     kda::StepParams prm;
     prm.pool = pool->base;
     prm.num_slots = pool->num_slots;
@@ -154,6 +272,7 @@ kda::StepParams make_params(const kda_pool* pool, const int32_t* init_slot,
     prm.o = o;
     prm.status = dev_status;
     prm.inv_sqrt_k = 1.0f / sqrtf((float)pool->k);
+    prm.flags = flags;
     return prm;
 }
 
@@ -191,27 +310,27 @@ int kda_state_bytes(const kda_pool* pool, int64_t* bytes_per_slot) {
 int kda_decode_step(const kda_pool* pool, const int32_t* slot_ids, const uint8_t* reset,
                     int32_t n, const void* q, const void* k, const void* v, int32_t qkv_dtype,
                     const float* a, const float* b, float* o, int32_t* dev_status,
-                    void* stream) {
-    const int rc = check_step_args(pool, slot_ids, n, 1, q, k, v, qkv_dtype, a, b, o, dev_status);
+                    uint32_t flags, void* stream) {
+    const int rc = check_step_args(pool, slot_ids, n, 1, q, k, v, qkv_dtype, a, b, o, dev_status, flags);
     if (rc != KDA_OK) return rc;
     if (n == 0) return KDA_OK;
     const kda::StepParams prm =
-        make_params(pool, slot_ids, nullptr, reset, n, 1, q, k, v, a, b, o, dev_status);
-    return launch<KDA_DEC_BV, KDA_DEC_NT, false>(prm, qkv_dtype, static_cast<cudaStream_t>(stream));
+        make_params(pool, slot_ids, nullptr, reset, n, 1, q, k, v, a, b, o, dev_status, flags);
+    return launch<false>(pool, prm, qkv_dtype, static_cast<cudaStream_t>(stream));
 }
 
 int kda_spec_verify(const kda_pool* pool, const int32_t* init_slot, const int32_t* snap_slot,
                     const uint8_t* reset, int32_t n, int32_t t, const void* q, const void* k,
                     const void* v, int32_t qkv_dtype, const float* a, const float* b,
-                    float* o, int32_t* dev_status, void* stream) {
-    const int rc = check_step_args(pool, init_slot, n, t, q, k, v, qkv_dtype, a, b, o, dev_status);
+                    float* o, int32_t* dev_status, uint32_t flags, void* stream) {
+    const int rc = check_step_args(pool, init_slot, n, t, q, k, v, qkv_dtype, a, b, o, dev_status, flags);
     if (rc != KDA_OK) return rc;
     if (n == 0 || t == 0) return KDA_OK;
     if (snap_slot == nullptr) return KDA_ERR_NULL;
     if (!aligned(snap_slot, 4)) return KDA_ERR_ALIGN;
     const kda::StepParams prm =
-        make_params(pool, init_slot, snap_slot, reset, n, t, q, k, v, a, b, o, dev_status);
-    return launch<KDA_VER_BV, KDA_VER_NT, true>(prm, qkv_dtype, static_cast<cudaStream_t>(stream));
+        make_params(pool, init_slot, snap_slot, reset, n, t, q, k, v, a, b, o, dev_status, flags);
+    return launch<true>(pool, prm, qkv_dtype, static_cast<cudaStream_t>(stream));
 }
 
 const char* kda_strerror(int32_t code) {
@@ -222,10 +341,11 @@ const char* kda_strerror(int32_t code) {
         case KDA_ERR_DTYPE_UNSUPPORTED: return "unsupported dtype (state pools are fp32 or fp16 only; q/k/v fp32, fp16 or bf16)";
         case KDA_ERR_LAYERS_DISAGREE: return "layers disagree on the state dtype or head shape";
         case KDA_ERR_SHAPE: return "bad shape (K and V must be multiples of 16 in 16..128; slot stride >= hv*k*v)";
-        case KDA_ERR_ALIGN: return "misaligned pointer or stride (pool 16-byte aligned; inputs naturally aligned)";
+        case KDA_ERR_ALIGN: return "misaligned pointer or stride (pool, q, k, v, a 16-byte aligned; b, o, ids 4-byte)";
         case KDA_ERR_LAUNCH: return "CUDA kernel launch failed";
         case KDA_ERR_SLOT_RANGE: return "a slot id lies outside [0, num_slots); its tiles were skipped";
         case KDA_ERR_ARG: return "bad argument";
+        case KDA_ERR_TIMEOUT: return "a device-side pipeline wait ran out (1 s); the call's results are incomplete";
         default: return "unknown kda status code";
     }
 }

@@ -1,0 +1,235 @@
+// Shared device helpers of the KDA kernels: parameters, element conversion,
+// the state address function, and the PTX wrappers for TMA (cp.async.bulk),
+// mbarriers and proxy fences used by the pipelined kernels (sm_90+ PTX, valid
+// on sm_103a).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+namespace kda {
+
+constexpr int KMAX = 128;        // largest K (and V) a launch accepts
+constexpr float L2_EPS = 1e-6f;  // L2-norm epsilon: x / sqrt(sum x^2 + eps)
+constexpr int32_t STATUS_SLOT_RANGE = 8;   // KDA_ERR_SLOT_RANGE in kda.h
+constexpr int32_t STATUS_TIMEOUT = 10;     // KDA_ERR_TIMEOUT in kda.h
+constexpr uint64_t WAIT_LIMIT_NS = 1000000000ull;  // a pipeline wait gives up after 1 s
+
+struct StepParams {
+    void* pool;               // state pool base (fp32 or fp16 by build)
+    int64_t num_slots;
+    int64_t slot_stride;      // elements
+    int hv, k, v;
+    int n, t;                 // requests, tokens per request (1 for decode)
+    const int32_t* init_slot; // [n]
+    const int32_t* snap_slot; // [n][t], or nullptr: write back in place
+    const uint8_t* reset;     // [n] or nullptr
+    const void* q;            // [n][t][hv][k]
+    const void* kk;           // [n][t][hv][k]
+    const void* vv;           // [n][t][hv][v]
+    const float* a;           // [n][t][hv][k]
+    const float* b;           // [n][t][hv]
+    float* o;                 // [n][t][hv][v]
+    int32_t* status;
+    float inv_sqrt_k;
+    uint32_t flags;           // KDA_LAUNCH_* bits
+};
+
+constexpr uint32_t LAUNCH_PDL = 1u;               // KDA_LAUNCH_PDL in kda.h
+constexpr uint32_t LAUNCH_PDL_EARLY_STATE = 2u;   // KDA_LAUNCH_PDL_EARLY_STATE in kda.h
+
+__device__ __forceinline__ float to_f32(float x) { return x; }
+__device__ __forceinline__ float to_f32(__half x) { return __half2float(x); }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
+
+// A 16-byte vector of state elements <-> fp32 registers.
+template <typename ST> struct StateVec;
+
+template <> struct StateVec<float> {
+    static constexpr int VEC = 4;
+    static __device__ __forceinline__ void widen(const uint4& r, float (&x)[VEC]) {
+        x[0] = __uint_as_float(r.x); x[1] = __uint_as_float(r.y);
+        x[2] = __uint_as_float(r.z); x[3] = __uint_as_float(r.w);
+    }
+    static __device__ __forceinline__ uint4 narrow(const float (&x)[VEC]) {
+        return make_uint4(__float_as_uint(x[0]), __float_as_uint(x[1]),
+                          __float_as_uint(x[2]), __float_as_uint(x[3]));
+    }
+};
+
+template <> struct StateVec<__half> {
+    static constexpr int VEC = 8;
+    static __device__ __forceinline__ float2 w2(uint32_t u) {
+        __half2 h = *reinterpret_cast<const __half2*>(&u);
+        return __half22float2(h);  // exact: every fp16 value is an fp32 value
+    }
+    static __device__ __forceinline__ uint32_t n2(float lo, float hi) {
+        __half2 h = __floats2half2_rn(lo, hi);  // round to nearest even
+        return *reinterpret_cast<const uint32_t*>(&h);
+    }
+    static __device__ __forceinline__ void widen(const uint4& r, float (&x)[VEC]) {
+        float2 f;
+        f = w2(r.x); x[0] = f.x; x[1] = f.y;
+        f = w2(r.y); x[2] = f.x; x[3] = f.y;
+        f = w2(r.z); x[4] = f.x; x[5] = f.y;
+        f = w2(r.w); x[6] = f.x; x[7] = f.y;
+    }
+    static __device__ __forceinline__ uint4 narrow(const float (&x)[VEC]) {
+        return make_uint4(n2(x[0], x[1]), n2(x[2], x[3]), n2(x[4], x[5]), n2(x[6], x[7]));
+    }
+};
+
+// state_at(slot, h): the one address function for every state access
+// (ROCm/ATOM pull request 2945, Changes), in elements from the pool base.
+__device__ __forceinline__ int64_t state_at(const StepParams& p, int64_t slot, int h) {
+    return slot * p.slot_stride + (int64_t)h * p.k * p.v;
+}
+
+// ---------------------------------------------------------------------------
+// PTX: shared-memory addresses, mbarriers, TMA, proxy fences
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+// Make barrier initialisation visible to the async (TMA) proxy.
+__device__ __forceinline__ void fence_mbar_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;"
+                 ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
+}
+
+// Add `bytes` to the phase's expected transaction count without arriving.
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.expect_tx.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+// One bounded test of a phase.  With the suspend-time hint the waiting warp is
+// parked by the hardware until the phase completes or about 1 ms passes, so
+// waiting warps do not take issue slots from the warps doing the work.
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(1000000u)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ uint64_t global_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Wait for the phase of `bar` with the given parity to complete; false if it
+// has not completed within WAIT_LIMIT_NS (the caller reports a timeout).
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_ns();
+    while (!mbar_try_wait(bar, parity)) {
+        if (global_ns() - t0 > WAIT_LIMIT_NS) return false;
+    }
+    return true;
+}
+
+__device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(map) : "memory");
+}
+
+// 3-D tiled TMA load global -> shared, completing `bytes` on `bar`.
+__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, uint64_t* bar,
+                                            int c0, int c1, int c2) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5}], [%2];"
+        ::"r"(smem_u32(dst)), "l"(map), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2)
+        : "memory");
+}
+
+// 1-D bulk copy global -> shared of `bytes` (a multiple of 16; both addresses
+// 16-byte aligned), completing on `bar`.
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+        ::"r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+
+// 3-D tiled TMA store shared -> global (bulk-group completion).
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, const void* src,
+                                             int c0, int c1, int c2) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4}], [%1];"
+        ::"l"(map), "r"(smem_u32(src)), "r"(c0), "r"(c1), "r"(c2)
+        : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit() {
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+
+// All but the N most recent bulk groups have finished reading shared memory.
+template <int N> __device__ __forceinline__ void bulk_wait_read() {
+    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+
+// All but the N most recent bulk groups have completed (writes performed).
+template <int N> __device__ __forceinline__ void bulk_wait() {
+    asm volatile("cp.async.bulk.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// Order this thread's generic-proxy shared-memory writes before later
+// async-proxy (TMA) accesses.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+    uint4 r;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "r"(addr) : "memory");
+    return r;
+}
+
+__device__ __forceinline__ void sts128(uint32_t addr, const uint4& r) {
+    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};"
+                 ::"r"(addr), "r"(r.x), "r"(r.y), "r"(r.z), "r"(r.w) : "memory");
+}
+
+// Byte offset of (row, 16-byte chunk) inside a tile that TMA wrote with the
+// swizzle mode matching ROWBYTES (128 B -> SWIZZLE_128B, 64 B -> SWIZZLE_64B,
+// 32 B -> SWIZZLE_32B): the chunk index is XORed with address bits 7.. of the
+// row, which spreads the 8 rows a quarter-warp reads over all 32 banks.  The
+// tile base must be aligned to the pattern's period (1024 B suffices).
+template <int ROWBYTES>
+__device__ __forceinline__ uint32_t swz(int row, int chunk) {
+    static_assert(ROWBYTES == 128 || ROWBYTES == 64 || ROWBYTES == 32, "row bytes");
+    if constexpr (ROWBYTES == 128) return row * 128 + ((chunk ^ (row & 7)) << 4);
+    else if constexpr (ROWBYTES == 64) return row * 64 + ((chunk ^ ((row >> 1) & 3)) << 4);
+    else return row * 32 + ((chunk ^ ((row >> 2) & 1)) << 4);
+}
+
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) x += __shfl_xor_sync(0xffffffffu, x, off);
+    return x;
+}
+
+}  // namespace kda

@@ -184,7 +184,8 @@ def test_identity_step_is_bit_exact(state_dtype):
 
 def test_verify_equals_chained_decode_on_fp32_pool():
     """An fp32 pool stores the fp32 carry exactly, so T decode calls and one
-    T-token verify produce the same bits (same tile shape, same reduction order)."""
+    T-token verify agree up to the order of the fp32 sums over K (the two
+    kernels split that reduction differently): within a few fp32 ulps."""
     inp = workloads.make_verify(n=4, t=6, hv=12, k=128, v=128, num_slots=64,
                                 state_dtype=torch.float32, seed=61)
     gpool_v, o_v, st = gpu_verify(inp)
@@ -195,9 +196,10 @@ def test_verify_equals_chained_decode_on_fp32_pool():
                                     inp.a[:, t], inp.b[:, t])
         pool, o_d, st = gpu_decode(step)
         assert st == 0
-        assert torch.equal(o_d, o_v[:, t])
+        np.testing.assert_allclose(o_d.numpy(), o_v[:, t].numpy(), rtol=0, atol=2e-6)
         for r in range(4):
-            assert torch.equal(pool[inp.init_slot[r]], gpool_v[inp.snap_slot[r, t]])
+            np.testing.assert_allclose(pool[inp.init_slot[r]].numpy(),
+                                       gpool_v[inp.snap_slot[r, t]].numpy(), rtol=0, atol=2e-6)
 
 
 def test_fp16_build_against_fp32_twin():
@@ -226,3 +228,55 @@ def test_results_do_not_depend_on_the_stream():
         p1, o1, st1 = gpu_decode(inp, stream=s)
     p2, o2, st2 = gpu_decode(inp)
     assert st1 == st2 == 0 and torch.equal(p1, p2) and torch.equal(o1, o2)
+
+
+@pytest.mark.parametrize("state_dtype", [torch.float32, torch.float16])
+def test_launch_flags_do_not_change_results(state_dtype):
+    """Programmatic dependent launch (with and without early state loads) gives
+    the same bits as a plain launch, also when captured in a CUDA graph of
+    back-to-back steps on different pools."""
+    inp = workloads.make_decode(n=24, hv=12, k=128, v=128, num_slots=64, state_dtype=state_dtype,
+                                seed=81, reset_p=0.2)
+    lib = lib_for(state_dtype)
+    d = inp.to("cuda")
+    pools = [d.pool.clone() for _ in range(3)]
+    outs = [torch.empty(24, 12, 128, device="cuda") for _ in range(3)]
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    flags = [0, kda.KDA_LAUNCH_PDL, kda.KDA_LAUNCH_PDL | kda.KDA_LAUNCH_PDL_EARLY_STATE]
+    s = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            for i in range(3):
+                lib.kda_decode_step(pools[i], d.init_slot, d.q, d.k, d.v, d.a, d.b, outs[i], status,
+                                    reset=d.reset, flags=flags[i])
+        g.replay()
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    for i in (1, 2):
+        assert torch.equal(pools[i], pools[0]) and torch.equal(outs[i], outs[0])
+    ref, o_ref = oracle_decode(inp)
+    assert_out_match(outs[2].cpu(), o_ref, state_dtype, "o")
+    assert_pool_match(pools[2].cpu(), ref, inp.init_slot.numpy(), "pool")
+
+
+def test_pdl_chain_on_one_pool_without_early_state():
+    """Back-to-back steps on the same pool with KDA_LAUNCH_PDL alone (the state
+    is read only after the previous step completed) equal the plain chain."""
+    inp = workloads.make_verify(n=4, t=5, hv=12, k=128, v=128, num_slots=64,
+                                state_dtype=torch.float32, seed=82)
+    lib = lib_for(torch.float32)
+    d = inp.to("cuda")
+    results = []
+    for flags in (0, kda.KDA_LAUNCH_PDL):
+        pool = d.pool.clone()
+        o = torch.empty(5, 4, 12, 128, device="cuda")
+        status = torch.zeros(1, dtype=torch.int32, device="cuda")
+        for t in range(5):
+            lib.kda_decode_step(pool, d.init_slot, d.q[:, t].contiguous(), d.k[:, t].contiguous(),
+                                d.v[:, t].contiguous(), d.a[:, t].contiguous(), d.b[:, t].contiguous(),
+                                o[t], status, flags=flags)
+        torch.cuda.synchronize()
+        assert int(status.item()) == 0
+        results.append((pool.cpu(), o.cpu()))
+    assert torch.equal(results[0][0], results[1][0]) and torch.equal(results[0][1], results[1][1])

@@ -117,24 +117,30 @@ def test_step_refusals_before_any_launch(libs):
     assert call(**args(desc(), q=None)) == kda.KDA_ERR_NULL
     assert call(**args(desc(), status=None)) == kda.KDA_ERR_NULL
     assert call(**args(desc(), a=P + 2)) == kda.KDA_ERR_ALIGN
+    assert call(**args(desc(), a=P + 4)) == kda.KDA_ERR_ALIGN
+    assert call(**args(desc(), v=P + 8)) == kda.KDA_ERR_ALIGN
+    assert call(**args(desc(), b=P + 2)) == kda.KDA_ERR_ALIGN
     assert call(**args(desc(), q=P + 1)) == kda.KDA_ERR_ALIGN
     assert call(**args(desc(k=100))) == kda.KDA_ERR_SHAPE
     # n == 0 is a no-op that succeeds without touching the GPU
     assert call(**args(desc(), n=0)) == kda.KDA_OK
     # verify: snapshot ids are required
     rc = L32.lib.kda_spec_verify(ctypes.byref(desc()), P, None, None, 4, 8, P, P, P,
-                                 kda.KDA_F32, P, P, P, P, None)
+                                 kda.KDA_F32, P, P, P, P, 0, None)
     assert rc == kda.KDA_ERR_NULL
     rc = L32.lib.kda_spec_verify(ctypes.byref(desc()), P, P, None, 4, 0, P, P, P,
-                                 kda.KDA_F32, P, P, P, P, None)
+                                 kda.KDA_F32, P, P, P, P, 0, None)
     assert rc == kda.KDA_OK
+    # unknown launch flags
+    assert call(**args(desc(), flags=4)) == kda.KDA_ERR_ARG
+    assert call(**args(desc(), n=0, flags=kda.KDA_LAUNCH_PDL | kda.KDA_LAUNCH_PDL_EARLY_STATE)) == kda.KDA_OK
 
 
 def test_strerror_covers_every_code(libs):
     L = libs[torch.float32]
-    msgs = {c: L.kda_strerror(c) for c in range(10)}
+    msgs = {c: L.kda_strerror(c) for c in range(11)}
     assert msgs[0] == "ok"
-    assert len(set(msgs.values())) == 10
+    assert len(set(msgs.values())) == 11
     assert L.kda_strerror(99) == "unknown kda status code"
 
 
