@@ -175,6 +175,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extra", action="store_true", help="skip the fp16 / verify lines")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer measurement")
+    ap.add_argument("--workload", choices=("decode_f32", "decode_f16"), default="decode_f32",
+                    help="headline workload: the decode step on an fp32 pool (the metric's) or fp16 pool")
     ap.add_argument("--soak-seconds", type=float, default=1.0,
                     help="minimum untimed load before timing (clocks ramp; 0 under a profiler)")
     args = ap.parse_args()
@@ -318,12 +320,14 @@ def main():
     # Consecutive steps update different pools (as consecutive layers do), so
     # each launch may start streaming its state while the previous one drains.
     pdl = kda.KDA_LAUNCH_PDL | kda.KDA_LAUNCH_PDL_EARLY_STATE
-    head = bench_decode(torch.float32, torch.bfloat16, 0, args.steps, args.warmup, True, pdl)
+    f16_head = args.workload == "decode_f16"
+    head_dtype = torch.float16 if f16_head else torch.float32
+    head = bench_decode(head_dtype, torch.bfloat16, 1 if f16_head else 0, args.steps, args.warmup, True, pdl)
     us = max_over_ranks(head["us_per_step"])
     gbs_per_gpu = head["bytes"] / (us * 1e-6) / 1e9
     value = gbs_per_gpu * world
     e2e, e2e_us, e2e_gbs = None, None, None
-    if not args.no_e2e:
+    if not args.no_e2e and not f16_head:
         e2e = bench_e2e(args.steps)
         e2e_us = max_over_ranks(e2e["us_per_step"])
         e2e_gbs = head["bytes"] / (e2e_us * 1e-6) / 1e9 * world
@@ -335,7 +339,8 @@ def main():
             "us_per_step": round(plain["us_per_step"], 3),
             "gbs": round(plain["bytes"] / (plain["us_per_step"] * 1e-6) / 1e9, 1),
             "frac_of_peak": round(plain["bytes"] / (plain["us_per_step"] * 1e-6) / 1e9 / peak, 4)}
-        h16 = bench_decode(torch.float16, torch.bfloat16, 1, min(args.steps, 20000), args.warmup, False, pdl)
+        h16 = head if f16_head else bench_decode(torch.float16, torch.bfloat16, 1, min(args.steps, 20000),
+                                                  args.warmup, False, pdl)
         extra["decode_fp16_pool"] = {
             "us_per_step": round(h16["us_per_step"], 3),
             "gbs": round(h16["bytes"] / (h16["us_per_step"] * 1e-6) / 1e9, 1),
@@ -363,10 +368,11 @@ def main():
             "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(us / 1e3, 6), "us_per_step": round(us, 3),
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f16 state, f32 math" if f16_head else "f32",
             "data": "synthetic",
-            "config": {"workload": "decode step, N=64 x HV=12, K=V=128, fp32 pool [256,12,128,128], "
-                                   "bf16 q/k/v, fp32 a/b/o", "global_batch": N * world,
+            "config": {"workload": f"decode step, N=64 x HV=12, K=V=128, {'fp16' if f16_head else 'fp32'} "
+                                   "pool [256,12,128,128], bf16 q/k/v, fp32 a/b/o", "global_batch": N * world,
                        "parallelism": f"replicas x{world}",
                        "l2": f"inputs larger than L2: {head['pools']} rotating pools, "
                              f"{head['pool_bytes'] / 1e9:.2f} GB > 4 x {l2 / 2**20:.0f} MiB L2",

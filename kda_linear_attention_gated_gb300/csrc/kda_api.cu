@@ -55,7 +55,14 @@ static constexpr int kBuildDtype = KDA_F32;
 #define KDA_DEC_NT 128
 #endif
 #ifndef KDA_DEC_MINB
+#if KDA_STATE16
 #define KDA_DEC_MINB 8
+#else
+#define KDA_DEC_MINB 11
+#endif
+#endif
+#ifndef KDA_DEC_KEEP
+#define KDA_DEC_KEEP 0
 #endif
 
 namespace {
@@ -164,11 +171,11 @@ void set_pdl(cudaLaunchConfig_t& cfg, cudaLaunchAttribute* attr, uint32_t flags)
     }
 }
 
-template <typename QT>
-int launch_decode(const kda_pool* pool, const kda::StepParams& prm, cudaStream_t stream) {
+template <typename QT, bool FULLK>
+int launch_decode_k(const kda_pool* pool, const kda::StepParams& prm, cudaStream_t stream) {
     constexpr int BV = KDA_DEC_BV, NT = KDA_DEC_NT;
-    constexpr size_t smem = kda::decode_smem_bytes<state_t, BV, NT>();
-    auto kernel = kda::kda_decode_kernel<state_t, QT, BV, NT, KDA_DEC_MINB>;
+    constexpr size_t smem = kda::decode_smem_bytes<state_t, BV, NT, (int)sizeof(QT)>();
+    auto kernel = kda::kda_decode_kernel<state_t, QT, BV, NT, KDA_DEC_MINB, KDA_DEC_KEEP != 0, FULLK>;
     const int64_t tiles = (int64_t)prm.n * prm.hv * ((prm.v + BV - 1) / BV);
     if (tiles > 0x7fffffffLL) return KDA_ERR_SHAPE;
     CUtensorMap map;
@@ -186,6 +193,14 @@ int launch_decode(const kda_pool* pool, const kda::StepParams& prm, cudaStream_t
     set_pdl(cfg, &attr, prm.flags);
     const cudaError_t err = cudaLaunchKernelEx(&cfg, kernel, map, prm);
     return err == cudaSuccess ? KDA_OK : KDA_ERR_LAUNCH;
+}
+
+// K = 128 (the configured models' key dimension) gets a build without the
+// per-row bound checks.
+template <typename QT>
+int launch_decode(const kda_pool* pool, const kda::StepParams& prm, cudaStream_t stream) {
+    return prm.k == kda::KMAX ? launch_decode_k<QT, true>(pool, prm, stream)
+                              : launch_decode_k<QT, false>(pool, prm, stream);
 }
 
 template <typename QT>

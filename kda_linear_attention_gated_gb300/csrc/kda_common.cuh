@@ -15,6 +15,7 @@ constexpr int KMAX = 128;        // largest K (and V) a launch accepts
 constexpr float L2_EPS = 1e-6f;  // L2-norm epsilon: x / sqrt(sum x^2 + eps)
 constexpr int32_t STATUS_SLOT_RANGE = 8;   // KDA_ERR_SLOT_RANGE in kda.h
 constexpr int32_t STATUS_TIMEOUT = 10;     // KDA_ERR_TIMEOUT in kda.h
+constexpr int32_t STATUS_SMEM_ALIGN = 6;   // KDA_ERR_ALIGN in kda.h (shared-memory base)
 constexpr uint64_t WAIT_LIMIT_NS = 1000000000ull;  // a pipeline wait gives up after 1 s
 
 struct StepParams {

@@ -15,19 +15,22 @@
 //   (1) gates: thread i < K turns row i's inputs into khat_i, qhat_i, alpha_i
 //       (the norms of k and q are a block reduction);
 //   (2) thread (row group rg, 16-byte column chunk cl) reads rows rg, rg + RG,
-//       ... of its chunk from shared memory, decays them and accumulates
-//       u = S^T khat and p = S^T qhat; warp shuffles and one shared-memory pass
-//       finish the sums over K;
-//   (3) it reads its rows again, applies the delta update and writes them back
-//       to the slot with coalesced 16-byte stores.
-// The stage barrier wait is bounded (1 s); a wait that runs out makes the whole
-// CTA record KDA_ERR_TIMEOUT, wait once more (bounded) for its copies, and exit.
+//       ... of its chunk from shared memory and accumulates u = S^T (alpha khat)
+//       and p = S^T (alpha qhat) (the decay folded into the gates); warp
+//       shuffles and one shared-memory pass finish the sums over K;
+//   (3) it reads its rows again (or keeps them in registers), applies the
+//       delta update and writes them back to the slot with coalesced 16-byte
+//       stores.
+// The inputs and the state tile complete on separate barriers, so the gates
+// are computed while the state is still in flight.  Each barrier wait is
+// bounded (1 s); a wait that runs out makes the whole CTA record
+// KDA_ERR_TIMEOUT, wait once more (bounded) for its copies, and exit.
 //
 // Math per tile (ROCm/ATOM pull requests 2130 "What", 2945 "Summary"):
 //   khat = k / sqrt(|k|^2 + eps), qhat likewise; beta = 1 / (1 + e^-b)
 //   alpha_i = exp(-softplus(a_i)) = 1 / (1 + e^{a_i})
-//   x_ij = alpha_i S_ij;  u_j = sum_i x_ij khat_i;  p_j = sum_i x_ij qhat_i
-//   S'_ij = x_ij + beta khat_i (v_j - u_j)
+//   u_j = sum_i S_ij (alpha_i khat_i);  p_j = sum_i S_ij (alpha_i qhat_i)
+//   S'_ij = alpha_i S_ij + (beta khat_i) (v_j - u_j)
 //   o_j = (p_j + beta (qhat . khat)(v_j - u_j)) / sqrt(K)   (= sum_i S'_ij qhat_i / sqrt(K))
 #pragma once
 
@@ -35,7 +38,7 @@
 
 namespace kda {
 
-template <typename ST, int BV, int NT>
+template <typename ST, int BV, int NT, int QES>
 struct DecodeShape {
     static constexpr int VEC = StateVec<ST>::VEC;
     static constexpr int ROWBYTES = BV * (int)sizeof(ST);
@@ -44,53 +47,65 @@ struct DecodeShape {
     static constexpr int ROWS = KMAX / RG;       // rows per thread
     static constexpr int NWARP = NT / 32;
     static constexpr uint32_t TILE_BYTES = (KMAX * ROWBYTES + 1023u) & ~1023u;
-    // input area: q row, k row (any q/k/v type, <= 4 bytes), a row (fp32), v slice
-    static constexpr uint32_t IN_Q = 0, IN_K = KMAX * 4, IN_A = 2 * KMAX * 4, IN_V = 3 * KMAX * 4;
-    static constexpr uint32_t IN_BYTES = (IN_V + BV * 4 + 127u) & ~127u;
-    // gates: float4 {khat, qhat, alpha, 0} per row, then v (fp32)
+    // input area: q row, k row (QES-byte elements), a row (fp32), v slice
+    static constexpr uint32_t IN_Q = 0, IN_K = KMAX * QES, IN_A = 2 * KMAX * QES;
+    static constexpr uint32_t IN_V = IN_A + KMAX * 4, IN_END = IN_V + BV * QES;
+    // gates: float4 {alpha khat, alpha qhat, alpha, beta khat} per row, then v
+    // (fp32); they overlay the input area, which is read into registers first
     static constexpr uint32_t GATE_BYTES = KMAX * 16 + BV * 4;
+    static constexpr uint32_t WORK_BYTES = ((IN_END > GATE_BYTES ? IN_END : GATE_BYTES) + 15u) & ~15u;
     static constexpr uint32_t RED_BYTES = NWARP * 4 * 4 + NWARP * CL * 2 * VEC * 4;
     static_assert(ROWBYTES == 128 || ROWBYTES == 64 || ROWBYTES == 32, "tile row bytes");
     static_assert(NT % 32 == 0 && NT >= KMAX && RG * CL == NT && KMAX % RG == 0, "thread shape");
     static_assert(32 % CL == 0, "a warp holds whole rows");
-    static_assert(IN_BYTES % 128 == 0 && GATE_BYTES % 16 == 0 && RED_BYTES % 16 == 0, "layout");
+    static_assert(IN_K % 16 == 0 && IN_A % 16 == 0 && IN_V % 16 == 0 && RED_BYTES % 16 == 0, "layout");
+    // rows rg + RG * i share the swizzle XOR term of row rg (patterns repeat every 8 rows of 128 B,
+    // 8 rows of 64 B read as pairs, 8 rows of 32 B read as quads: 1024 B in each case)
+    static_assert((RG * ROWBYTES) % 1024 == 0, "row stride must span whole swizzle periods");
 };
 
-template <typename ST, int BV, int NT>
+template <typename ST, int BV, int NT, int QES>
 constexpr size_t decode_smem_bytes() {
-    using SH = DecodeShape<ST, BV, NT>;
-    // alignment slack, the tile, inputs, gates, reductions, one barrier
-    return 1024 + SH::TILE_BYTES + SH::IN_BYTES + SH::GATE_BYTES + SH::RED_BYTES + 16;
+    using SH = DecodeShape<ST, BV, NT, QES>;
+    // the tile, inputs/gates, reductions, two barriers (no alignment slack: the
+    // dynamic shared memory base is 1024-byte aligned, which the kernel checks)
+    return SH::TILE_BYTES + SH::WORK_BYTES + SH::RED_BYTES + 16;
 }
 
-template <typename ST, typename QT, int BV, int NT, int MINB>
+template <typename ST, typename QT, int BV, int NT, int MINB, bool KEEP, bool FULLK>
 __global__ void __launch_bounds__(NT, MINB)
 kda_decode_kernel(const __grid_constant__ CUtensorMap tmap, const StepParams p) {
-    using SH = DecodeShape<ST, BV, NT>;
+    using SH = DecodeShape<ST, BV, NT, (int)sizeof(QT)>;
     using SV = StateVec<ST>;
     constexpr int VEC = SH::VEC, CL = SH::CL, RG = SH::RG, ROWS = SH::ROWS, NWARP = SH::NWARP;
 
-    extern __shared__ uint8_t smem_raw[];
-    const uint32_t raw_u32 = smem_u32(smem_raw);
-    uint8_t* smem = smem_raw + (((raw_u32 + 1023u) & ~1023u) - raw_u32);  // swizzle period
+    extern __shared__ __align__(1024) uint8_t smem[];
     uint8_t* in = smem + SH::TILE_BYTES;
-    float4* gates = reinterpret_cast<float4*>(in + SH::IN_BYTES);
+    float4* gates = reinterpret_cast<float4*>(in);  // overlays the inputs once they are read
     float* gv = reinterpret_cast<float*>(gates + KMAX);
-    float* red = gv + BV;          // [NWARP][4]
-    float* red2 = red + NWARP * 4;  // [NWARP][CL][2 VEC]
-    uint64_t* full = reinterpret_cast<uint64_t*>(red2 + NWARP * CL * 2 * VEC);
+    float* red = reinterpret_cast<float*>(in + SH::WORK_BYTES);  // [NWARP][4]
+    float* red2 = red + NWARP * 4;                               // [NWARP][CL][2 VEC]
+    uint64_t* bar_st = reinterpret_cast<uint64_t*>(red2 + NWARP * CL * 2 * VEC);  // state tile landed
+    uint64_t* bar_in = bar_st + 1;                                                 // inputs landed
     const uint32_t tile_base = smem_u32(smem);
     const uint32_t gate_base = smem_u32(gates);
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int cl = tid % CL, rg = tid / CL;
+    // 32-bit index arithmetic: the host guarantees n * hv * ceil(v / BV) < 2^31
     const int vt = (p.v + BV - 1) / BV;
-    const int cb = blockIdx.x % vt;
-    const int64_t r = blockIdx.x / vt;  // n * hv + h
-    const int h = (int)(r % p.hv);
-    const int n = (int)(r / p.hv);
+    const int tile = (int)blockIdx.x;
+    const int r = tile / vt;  // n * hv + h
+    const int cb = tile - r * vt;
+    const int n = r / p.hv;
+    const int h = r - n * p.hv;
     const int col0 = cb * BV + cl * VEC;
     const int qes = (int)sizeof(QT);
+    // The swizzled tile needs a 1024-byte aligned base; report, never guess.
+    if ((tile_base & 1023u) != 0) {
+        if (tid == 0) atomicCAS(p.status, 0, STATUS_SMEM_ALIGN);
+        return;
+    }
 
     // The next kernel on the stream may be scheduled now.  Nothing the previous
     // kernel may write is read before it completes, except -- when the caller
@@ -104,12 +119,13 @@ kda_decode_kernel(const __grid_constant__ CUtensorMap tmap, const StepParams p) 
     const bool valid = slot >= 0 && slot < p.num_slots;
     const bool rst = valid && p.reset != nullptr && p.reset[n] != 0;
     if (tid == 0) {
-        mbar_init(full, 1);
+        mbar_init(bar_st, 1);
+        mbar_init(bar_in, 1);
         fence_mbar_init();
         if (valid && !rst) {
             prefetch_tmap(&tmap);
-            mbar_expect_tx(full, (uint32_t)p.k * SH::ROWBYTES);
-            tma_load_3d(smem, &tmap, full, cb * BV, h * p.k, slot);
+            mbar_arrive_expect_tx(bar_st, (uint32_t)p.k * SH::ROWBYTES);
+            tma_load_3d(smem, &tmap, bar_st, cb * BV, h * p.k, slot);
         }
     }
     if (early) cudaGridDependencySynchronize();
@@ -120,23 +136,28 @@ kda_decode_kernel(const __grid_constant__ CUtensorMap tmap, const StepParams p) 
     if (tid == 0) {
         const uint32_t qk_bytes = (uint32_t)p.k * qes;
         const uint32_t v_bytes = (uint32_t)min(BV, p.v - cb * BV) * qes;
-        mbar_arrive_expect_tx(full, 2 * qk_bytes + (uint32_t)p.k * 4 + v_bytes);
-        bulk_load(in + SH::IN_Q, static_cast<const char*>(p.q) + r * qk_bytes, qk_bytes, full);
-        bulk_load(in + SH::IN_K, static_cast<const char*>(p.kk) + r * qk_bytes, qk_bytes, full);
-        bulk_load(in + SH::IN_A, p.a + r * p.k, (uint32_t)p.k * 4, full);
-        bulk_load(in + SH::IN_V, static_cast<const char*>(p.vv) + (r * p.v + (int64_t)cb * BV) * qes,
-                  v_bytes, full);
+        mbar_arrive_expect_tx(bar_in, 2 * qk_bytes + (uint32_t)p.k * 4 + v_bytes);
+        const int64_t r64 = r;
+        bulk_load(in + SH::IN_Q, static_cast<const char*>(p.q) + r64 * qk_bytes, qk_bytes, bar_in);
+        bulk_load(in + SH::IN_K, static_cast<const char*>(p.kk) + r64 * qk_bytes, qk_bytes, bar_in);
+        bulk_load(in + SH::IN_A, p.a + r64 * p.k, (uint32_t)p.k * 4, bar_in);
+        bulk_load(in + SH::IN_V, static_cast<const char*>(p.vv) + (r64 * p.v + (int64_t)cb * BV) * qes,
+                  v_bytes, bar_in);
     }
     const float b = __ldg(p.b + r);
-    __syncthreads();  // the barrier is initialised before anyone waits on it
-    const bool ok = mbar_wait(full, 0);
+    __syncthreads();  // the barriers are initialised before anyone waits on them
+    // The gates need only the small inputs, so they are worked out while the
+    // state tile is still in flight.
+    const bool ok = mbar_wait(bar_in, 0);
 
     // (1) gates: thread tid < K owns row tid.
-    float kt = 0.f, qt = 0.f, alpha = 0.f;
+    float kt = 0.f, qt = 0.f, alpha = 0.f, vt_ = 0.f;
+    if (ok && tid < BV && tid < min(BV, p.v - cb * BV))
+        vt_ = to_f32(reinterpret_cast<const QT*>(in + SH::IN_V)[tid]);
     if (ok && tid < p.k) {
         kt = to_f32(reinterpret_cast<const QT*>(in + SH::IN_K)[tid]);
         qt = to_f32(reinterpret_cast<const QT*>(in + SH::IN_Q)[tid]);
-        alpha = 1.0f / (1.0f + expf(reinterpret_cast<const float*>(in + SH::IN_A)[tid]));  // exp(-softplus(a))
+        alpha = __frcp_rn(1.0f + expf(reinterpret_cast<const float*>(in + SH::IN_A)[tid]));  // exp(-softplus(a))
     }
     float kk2 = warp_sum(kt * kt), qq2 = warp_sum(qt * qt), kq = warp_sum(kt * qt);
     if (lane == 0) {
@@ -147,7 +168,8 @@ kda_decode_kernel(const __grid_constant__ CUtensorMap tmap, const StepParams p) 
     if (__syncthreads_or(ok ? 0 : 1)) {  // the copies did not land in time: give up
         if (tid == 0) {
             atomicExch(p.status, STATUS_TIMEOUT);
-            mbar_wait(full, 0);  // bounded: no copy may still target this CTA's memory
+            mbar_wait(bar_in, 0);  // bounded: no copy may still target this CTA's memory
+            if (!rst) mbar_wait(bar_st, 0);
         }
         return;
     }
@@ -160,35 +182,47 @@ kda_decode_kernel(const __grid_constant__ CUtensorMap tmap, const StepParams p) 
         qq2 += red[w * 4 + 1];
         kq += red[w * 4 + 2];
     }
-    const float rk = 1.0f / sqrtf(kk2 + L2_EPS);
-    const float rq = 1.0f / sqrtf(qq2 + L2_EPS);
-    const float beta = 1.0f / (1.0f + expf(-b));  // sigmoid(b)
-    const float bqk = beta * (kq * rk * rq);       // beta (qhat . khat)
-    if (tid < p.k) gates[tid] = make_float4(kt * rk, qt * rq, alpha, 0.f);
-    if (tid < BV) {
-        const int vcols = min(BV, p.v - cb * BV);
-        gv[tid] = tid < vcols ? to_f32(reinterpret_cast<const QT*>(in + SH::IN_V)[tid]) : 0.f;
+    const float rk = __frsqrt_rn(kk2 + L2_EPS);
+    const float rq = __frsqrt_rn(qq2 + L2_EPS);
+    const float beta = __frcp_rn(1.0f + expf(-b));  // sigmoid(b)
+    const float bqk = beta * (kq * rk * rq);         // beta (qhat . khat)
+    // Per row: w = alpha khat and z = alpha qhat fold the decay into the two
+    // reductions (u = sum_i S_ij w_i, p = sum_i S_ij z_i); alpha and beta khat
+    // serve the update S' = alpha S + (beta khat) d.
+    if (tid < p.k) {
+        const float kh = kt * rk, qh = qt * rq;
+        gates[tid] = make_float4(alpha * kh, alpha * qh, alpha, beta * kh);
     }
+    if (tid < BV) gv[tid] = vt_;
     __syncthreads();
 
-    // (2) decay and the partial sums over this thread's rows.
+    // This thread's rows are rg + RG * rr.  RG rows span whole swizzle periods,
+    // so the XOR term of every row equals that of row rg: one base address,
+    // then a constant stride.
+    const int nrows = FULLK ? ROWS : min(ROWS, (p.k - rg + RG - 1) / RG);
+    const uint32_t srow0 = tile_base + swz<SH::ROWBYTES>(rg, cl);
+    const uint32_t grow0 = gate_base + rg * 16;
+    constexpr uint32_t SSTRIDE = RG * SH::ROWBYTES, GSTRIDE = RG * 16;
+
+    // (2) the two partial sums over this thread's rows, once the tile is in.
+    const bool ok_st = rst || mbar_wait(bar_st, 0);
     float u[VEC], pp[VEC];
+    float xs[KEEP ? ROWS : 1][VEC];
 #pragma unroll
     for (int c = 0; c < VEC; ++c) { u[c] = 0.f; pp[c] = 0.f; }
-    if (!rst) {
+    if (!rst && ok_st) {
 #pragma unroll
         for (int rr = 0; rr < ROWS; ++rr) {
-            const int row = rg + RG * rr;
-            if (row < p.k) {
+            if (FULLK || rr < nrows) {
                 float x[VEC];
-                SV::widen(lds128(tile_base + swz<SH::ROWBYTES>(row, cl)), x);
-                const uint4 g = lds128(gate_base + row * 16);
-                const float kh = __uint_as_float(g.x), qh = __uint_as_float(g.y), al = __uint_as_float(g.z);
+                SV::widen(lds128(srow0 + rr * SSTRIDE), x);
+                const uint4 g = lds128(grow0 + rr * GSTRIDE);
+                const float w = __uint_as_float(g.x), z = __uint_as_float(g.y);
 #pragma unroll
                 for (int c = 0; c < VEC; ++c) {
-                    x[c] *= al;
-                    u[c] = fmaf(x[c], kh, u[c]);
-                    pp[c] = fmaf(x[c], qh, pp[c]);
+                    u[c] = fmaf(x[c], w, u[c]);
+                    pp[c] = fmaf(x[c], z, pp[c]);
+                    if (KEEP) xs[KEEP ? rr : 0][c] = x[c];
                 }
             }
         }
@@ -203,50 +237,72 @@ kda_decode_kernel(const __grid_constant__ CUtensorMap tmap, const StepParams p) 
         }
     }
     if (lane < CL) {
+        float4* dst4 = reinterpret_cast<float4*>(red2 + (warp * CL + cl) * 2 * VEC);
 #pragma unroll
-        for (int c = 0; c < VEC; ++c) {
-            red2[(warp * CL + cl) * 2 * VEC + c] = u[c];
-            red2[(warp * CL + cl) * 2 * VEC + VEC + c] = pp[c];
+        for (int c = 0; c < VEC; c += 4) {
+            dst4[c / 4] = make_float4(u[c], u[c + 1], u[c + 2], u[c + 3]);
+            dst4[(VEC + c) / 4] = make_float4(pp[c], pp[c + 1], pp[c + 2], pp[c + 3]);
         }
     }
-    __syncthreads();
-    // ... then over the warps.
-#pragma unroll
-    for (int c = 0; c < VEC; ++c) {
-        float su = 0.f, sp = 0.f;
-#pragma unroll
-        for (int w = 0; w < NWARP; ++w) {
-            su += red2[(w * CL + cl) * 2 * VEC + c];
-            sp += red2[(w * CL + cl) * 2 * VEC + VEC + c];
+    if (__syncthreads_or(ok_st ? 0 : 1)) {  // the state tile did not land in time
+        if (tid == 0) {
+            atomicExch(p.status, STATUS_TIMEOUT);
+            mbar_wait(bar_st, 0);  // bounded, as above
         }
-        u[c] = gv[cl * VEC + c] - su;  // d_j = v_j - u_j
-        pp[c] = sp;
+        return;
+    }
+    // ... then over the warps (16-byte reads: lanes with the same cl share them).
+    float su[VEC], sp[VEC];
+#pragma unroll
+    for (int c = 0; c < VEC; ++c) { su[c] = 0.f; sp[c] = 0.f; }
+#pragma unroll
+    for (int w = 0; w < NWARP; ++w) {
+        const float4* src4 = reinterpret_cast<const float4*>(red2 + (w * CL + cl) * 2 * VEC);
+#pragma unroll
+        for (int c = 0; c < VEC; c += 4) {
+            const float4 a4 = src4[c / 4], b4 = src4[(VEC + c) / 4];
+            su[c] += a4.x; su[c + 1] += a4.y; su[c + 2] += a4.z; su[c + 3] += a4.w;
+            sp[c] += b4.x; sp[c + 1] += b4.y; sp[c + 2] += b4.z; sp[c + 3] += b4.w;
+        }
+    }
+    float d[VEC];
+#pragma unroll
+    for (int c = 0; c < VEC; c += 4) {
+        const float4 v4 = *reinterpret_cast<const float4*>(gv + cl * VEC + c);
+        d[c] = v4.x - su[c];  // d_j = v_j - u_j
+        d[c + 1] = v4.y - su[c + 1];
+        d[c + 2] = v4.z - su[c + 2];
+        d[c + 3] = v4.w - su[c + 3];
     }
     if (col0 >= p.v) return;
     if (rg == 0) {
-        float* o = p.o + r * p.v + col0;
+        float* o = p.o + (int64_t)r * p.v + col0;
 #pragma unroll
-        for (int c = 0; c < VEC; ++c) o[c] = fmaf(bqk, u[c], pp[c]) * p.inv_sqrt_k;
+        for (int c = 0; c < VEC; ++c) o[c] = fmaf(bqk, d[c], sp[c]) * p.inv_sqrt_k;
     }
 
-    // (3) the delta update, stored in place with coalesced 16-byte stores.
-    ST* dst = static_cast<ST*>(p.pool) + state_at(p, slot, h) + col0;
+    // (3) the delta update S' = alpha S + (beta khat) d, stored in place with
+    // coalesced 16-byte stores.
+    ST* dst = static_cast<ST*>(p.pool) + state_at(p, slot, h) + (int64_t)rg * p.v + col0;
+    const int64_t gstride = (int64_t)RG * p.v;
 #pragma unroll
     for (int rr = 0; rr < ROWS; ++rr) {
-        const int row = rg + RG * rr;
-        if (row < p.k) {
+        if (FULLK || rr < nrows) {
             float x[VEC];
-            if (!rst) {
-                SV::widen(lds128(tile_base + swz<SH::ROWBYTES>(row, cl)), x);
-            } else {
+            if (rst) {
 #pragma unroll
                 for (int c = 0; c < VEC; ++c) x[c] = 0.f;
-            }
-            const uint4 g = lds128(gate_base + row * 16);
-            const float bk = beta * __uint_as_float(g.x), al = __uint_as_float(g.z);
+            } else if (KEEP) {
 #pragma unroll
-            for (int c = 0; c < VEC; ++c) x[c] = fmaf(bk, u[c], x[c] * al);
-            __stcs(reinterpret_cast<uint4*>(dst + (int64_t)row * p.v), SV::narrow(x));
+                for (int c = 0; c < VEC; ++c) x[c] = xs[KEEP ? rr : 0][c];
+            } else {
+                SV::widen(lds128(srow0 + rr * SSTRIDE), x);
+            }
+            const uint4 g = lds128(grow0 + rr * GSTRIDE);
+            const float al = __uint_as_float(g.z), bk = __uint_as_float(g.w);
+#pragma unroll
+            for (int c = 0; c < VEC; ++c) x[c] = fmaf(al, x[c], bk * d[c]);
+            __stcs(reinterpret_cast<uint4*>(dst + rr * gstride), SV::narrow(x));
         }
     }
 }
