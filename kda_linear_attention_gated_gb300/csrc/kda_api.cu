@@ -32,6 +32,9 @@
 // element-size rule of ROCm/ATOM pull request 2130, What).  Decode runs one
 // CTA of DEC_NT threads per tile, at least DEC_MINB resident per SM; the values
 // are tuned on GB300.
+// Verify carries the state in registers across tokens and runs its tokens in
+// sequence, so its tiles are 32 columns wide (128-byte rows for fp32, 64-byte
+// rows for fp16), for registers and for parallelism.
 #if KDA_STATE16
 using state_t = __half;
 static constexpr int kBuildDtype = KDA_F16;
@@ -51,6 +54,7 @@ static constexpr int kBuildDtype = KDA_F32;
 #define KDA_VER_BV 32
 #endif
 #endif
+
 #ifndef KDA_DEC_NT
 #define KDA_DEC_NT 128
 #endif
@@ -206,20 +210,20 @@ int launch_decode(const kda_pool* pool, const kda::StepParams& prm, cudaStream_t
 template <typename QT>
 int launch_verify(const kda_pool* pool, const kda::StepParams& prm, cudaStream_t stream) {
     constexpr int BV = KDA_VER_BV;
-    using SH = kda::VerifyTmaShape<state_t, BV>;
-    constexpr size_t smem = kda::verify_tma_smem_bytes<state_t, BV>();
-    auto kernel = kda::kda_verify_tma_kernel<state_t, QT, BV>;
+    using SH = kda::VerifyShape<state_t, BV, (int)sizeof(QT)>;
+    constexpr size_t smem = kda::verify_smem_bytes<state_t, BV, (int)sizeof(QT)>();
+    auto kernel = kda::kda_verify_kernel<state_t, QT, BV>;
     const int64_t tiles = (int64_t)prm.n * prm.hv * ((prm.v + BV - 1) / BV);
     if (tiles > 0x7fffffffLL) return KDA_ERR_SHAPE;
     CUtensorMap map;
     int rc = make_pool_map(pool, BV, &map);
     if (rc != KDA_OK) return rc;
     int occ = 0, sms = 0;
-    rc = occupancy(reinterpret_cast<const void*>(kernel), SH::THREADS, smem, &occ, &sms);
+    rc = occupancy(reinterpret_cast<const void*>(kernel), SH::NT, smem, &occ, &sms);
     if (rc != KDA_OK) return rc;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)tiles, 1, 1);
-    cfg.blockDim = dim3(SH::THREADS, 1, 1);
+    cfg.blockDim = dim3(SH::NT, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     cudaLaunchAttribute attr;

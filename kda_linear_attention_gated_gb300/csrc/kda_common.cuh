@@ -227,6 +227,32 @@ __device__ __forceinline__ uint32_t swz(int row, int chunk) {
     else return row * 32 + ((chunk ^ ((row >> 2) & 1)) << 4);
 }
 
+// Reduce NV values per lane over the 32 lanes of a warp, scattering the
+// results: afterwards lane l holds the full sum of value (l >> (5 - log2 NV))
+// (lanes sharing that index hold the same sum).  Each step sends the half of
+// the values the lane does not keep, so the whole reduction costs
+// NV/2 + NV/4 + ... + 1 shuffles plus one per remaining lane bit, instead of
+// 5 NV for NV separate butterflies.
+template <int NV>
+__device__ __forceinline__ float warp_reduce_scatter(float (&v)[NV], int lane) {
+    static_assert(NV >= 1 && NV <= 32 && (NV & (NV - 1)) == 0, "power of two");
+    int m = 16;
+#pragma unroll
+    for (int cnt = NV; cnt > 1; cnt >>= 1, m >>= 1) {
+        const bool upper = (lane & m) != 0;
+#pragma unroll
+        for (int k = 0; k < cnt / 2; ++k) {
+            const float send = upper ? v[k] : v[k + cnt / 2];
+            const float keep = upper ? v[k + cnt / 2] : v[k];
+            v[k] = keep + __shfl_xor_sync(0xffffffffu, send, m);
+        }
+    }
+    float s = v[0];
+#pragma unroll
+    for (; m >= 1; m >>= 1) s += __shfl_xor_sync(0xffffffffu, s, m);
+    return s;
+}
+
 __device__ __forceinline__ float warp_sum(float x) {
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) x += __shfl_xor_sync(0xffffffffu, x, off);
