@@ -111,6 +111,21 @@ class ClockSampler:
                 "samples": len(rows)}
 
 
+def reduce_max(x, dist, device):
+    """The largest of every rank's x (x itself on one rank)."""
+    if dist is None or not dist.is_initialized() or dist.get_world_size() == 1:
+        return float(x)
+    import torch
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_gbs(bytes_per_step_per_rank, us_per_step_max, world):
+    """Whole-job throughput: every rank's bytes over the slowest rank's time."""
+    return bytes_per_step_per_rank * world / (us_per_step_max * 1e-6) / 1e9
+
+
 def chunk_size(k, limit=512):
     for c in range(min(k, limit), 0, -1):
         if k % c == 0:
@@ -177,6 +192,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer measurement")
     ap.add_argument("--workload", choices=("decode_f32", "decode_f16"), default="decode_f32",
                     help="headline workload: the decode step on an fp32 pool (the metric's) or fp16 pool")
+    ap.add_argument("--case", choices=("verify_f16", "sweep"), default=None,
+                    help="time one secondary case alone and print its line (profiling runs)")
     ap.add_argument("--soak-seconds", type=float, default=1.0,
                     help="minimum untimed load before timing (clocks ramp; 0 under a profiler)")
     args = ap.parse_args()
@@ -310,13 +327,19 @@ def main():
         return dict(us_per_step=ms * 1e3 / n_e2e, steps=n_e2e, h2d=h2d, d2h=d2h)
 
     def max_over_ranks(x):
-        if dist is None:
-            return x
-        t = torch.tensor([x], dtype=torch.float64, device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
+        return reduce_max(x, dist, "cuda")
 
     peak, peak_kind, _ = peaks()
+    if args.case is not None:
+        if args.case == "verify_f16":
+            res = {"verify_f16": bench_verify(kda, workloads, torch, args, l2, peak)}
+        else:
+            res = {f"sweep_69_layers_n{n}_{nm}": bench_sweep(kda, workloads, torch, sd, n, peak)
+                   for nm, sd in (("fp32", torch.float32), ("fp16", torch.float16))
+                   for n in (1, 16, 64, 128)}
+        if rank == 0:
+            print(json.dumps({"case": args.case, "peak": peak, "peak_kind": peak_kind, **res}), flush=True)
+        return 0
     # Consecutive steps update different pools (as consecutive layers do), so
     # each launch may start streaming its state while the previous one drains.
     pdl = kda.KDA_LAUNCH_PDL | kda.KDA_LAUNCH_PDL_EARLY_STATE
@@ -325,7 +348,7 @@ def main():
     head = bench_decode(head_dtype, torch.bfloat16, 1 if f16_head else 0, args.steps, args.warmup, True, pdl)
     us = max_over_ranks(head["us_per_step"])
     gbs_per_gpu = head["bytes"] / (us * 1e-6) / 1e9
-    value = gbs_per_gpu * world
+    value = whole_job_gbs(head["bytes"], us, world)
     e2e, e2e_us, e2e_gbs = None, None, None
     if not args.no_e2e and not f16_head:
         e2e = bench_e2e(args.steps)
@@ -347,6 +370,8 @@ def main():
             "frac_of_peak": round(h16["bytes"] / (h16["us_per_step"] * 1e-6) / 1e9 / peak, 4),
             "bytes_per_step": h16["bytes"], "pools": h16["pools"]}
         extra["verify"] = bench_verify(kda, workloads, torch, args, l2, peak)
+        for sd_name, sd in (("fp32", torch.float32), ("fp16", torch.float16)):
+            extra[f"sweep_69_layers_n128_{sd_name}"] = bench_sweep(kda, workloads, torch, sd, 128, peak)
 
     traffic = None
     tpath = os.path.join(REPO, "profiles", "decode_f32_n64_traffic.json")
@@ -398,6 +423,52 @@ def main():
     return 0
 
 
+def bench_sweep(kda, workloads, torch, state_dtype, n, peak, layers=69, replays=30):
+    """The full-depth decode: one CUDA graph of `layers` decode steps, each on
+    its own 256-slot pool (N requests, HV=12, K=V=128, fp32 inputs, resets ~
+    Bernoulli(0.05)); 69 distinct pools, far larger than L2."""
+    lib = kda.KdaLibrary(state_dtype)
+    es = 4 if state_dtype == torch.float32 else 2
+    dev = [workloads.make_sweep_layer(l, n, state_dtype, sentinel=0.0).to("cuda") for l in range(layers)]
+    outs = [torch.empty(n, HV, V, device="cuda") for _ in range(layers)]
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    flags = kda.KDA_LAUNCH_PDL | kda.KDA_LAUNCH_PDL_EARLY_STATE
+    stream = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        d = dev[0]
+        lib.kda_decode_step(d.pool, d.init_slot, d.q, d.k, d.v, d.a, d.b, outs[0], status, reset=d.reset)
+        stream.synchronize()
+        with torch.cuda.graph(g, stream=stream):
+            for l in range(layers):
+                d = dev[l]
+                lib.kda_decode_step(d.pool, d.init_slot, d.q, d.k, d.v, d.a, d.b, outs[l], status,
+                                    reset=d.reset, flags=flags)
+        for _ in range(3):
+            g.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(replays):
+            g.replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    us_fwd = e0.elapsed_time(e1) * 1e3 / replays
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item())}")
+    resets = sum(int(d.reset.sum().item()) for d in dev)
+    state = HV * K * V * es
+    byt = (layers * n - resets) * state + layers * n * state + layers * n * HV * (2 * K + V) * 4 + layers * n * HV * V * 4
+    del dev, outs
+    torch.cuda.empty_cache()
+    return {"workload": f"{layers} layers x N={n}, HV=12, K=V=128, {'fp32' if es == 4 else 'fp16'} pools, "
+                        "fp32 inputs, resets ~ Bernoulli(0.05), one CUDA graph",
+            "us_per_forward": round(us_fwd, 2), "us_per_layer": round(us_fwd / layers, 3),
+            "gbs": round(byt / (us_fwd * 1e-6) / 1e9, 1),
+            "frac_of_peak": round(byt / (us_fwd * 1e-6) / 1e9 / peak, 4), "bytes_per_forward": byt}
+
+
 def bench_verify(kda, workloads, torch, args, l2, peak):
     """Speculative verify, fp16 pool, N=8 x T=8, HV=12, K=V=128, fp32 inputs."""
     lib = kda.KdaLibrary(torch.float16)
@@ -421,8 +492,7 @@ def bench_verify(kda, workloads, torch, args, l2, peak):
         with torch.cuda.graph(g, stream=stream):
             for i in range(chunk):
                 lib.kda_spec_verify(pools[i % R], d.init_slot, d.snap_slot, d.q, d.k, d.v, d.a,
-                                    d.b, o, status,
-                                    flags=kda.KDA_LAUNCH_PDL | kda.KDA_LAUNCH_PDL_EARLY_STATE)
+                                    d.b, o, status)
         for _ in range(max(1, args.warmup // chunk)):
             g.replay()
     torch.cuda.synchronize()
@@ -435,10 +505,12 @@ def bench_verify(kda, workloads, torch, args, l2, peak):
     torch.cuda.synchronize()
     us = e0.elapsed_time(e1) * 1e3 / steps
     byt = algorithmic_bytes(n, HV, K, V, t, 2, 4)
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item())}")
     return {"workload": "spec verify, fp16 pool, N=8 x T=8, HV=12, K=V=128, fp32 q/k/v",
             "us_per_step": round(us, 3), "gbs": round(byt / (us * 1e-6) / 1e9, 1),
             "frac_of_peak": round(byt / (us * 1e-6) / 1e9 / peak, 4), "bytes_per_step": byt,
-            "pools": R}
+            "pools": R, "launch": f"CUDA graph of {chunk} plain launches, replayed"}
 
 
 if __name__ == "__main__":
