@@ -55,3 +55,10 @@ def test_reference_arm_other_ranks_do_nothing(capsys):
         steps, gpus = 2, 2
     assert bench.run_reference(Args(), rank=1, world=2) == 0
     assert capsys.readouterr().out == ""
+
+
+def test_reference_sample_size_bounds():
+    assert bench.reference_sample_size(20000, 2.7e-3) == 64      # 54 s for whole steps
+    assert bench.reference_sample_size(20000, 27e-3) == 7        # 64 * 60 / 540
+    assert bench.reference_sample_size(10, 2.7e-3) == 64
+    assert bench.reference_sample_size(10**9, 1.0) == 1
