@@ -54,10 +54,16 @@ struct DecodeShape {
     // (fp32); they overlay the input area, which is read into registers first
     static constexpr uint32_t GATE_BYTES = KMAX * 16 + BV * 4;
     static constexpr uint32_t WORK_BYTES = ((IN_END > GATE_BYTES ? IN_END : GATE_BYTES) + 15u) & ~15u;
-    static constexpr uint32_t RED_BYTES = NWARP * 4 * 4 + NWARP * CL * 2 * VEC * 4;
+    // lanes of a warp that share a column chunk, and the values each keeps
+    // after the in-warp reduce-scatter of its 2 VEC partial sums
+    static constexpr int NL = 32 / CL, KEEPV = 2 * VEC / NL;
+    // norms [NWARP][4], partial sums [NWARP][CL][2 VEC], d [BV]
+    static constexpr uint32_t RED_BYTES = NWARP * 4 * 4 + NWARP * CL * 2 * VEC * 4 + BV * 4;
     static_assert(ROWBYTES == 128 || ROWBYTES == 64 || ROWBYTES == 32, "tile row bytes");
     static_assert(NT % 32 == 0 && NT >= KMAX && RG * CL == NT && KMAX % RG == 0, "thread shape");
     static_assert(32 % CL == 0, "a warp holds whole rows");
+    static_assert(KEEPV >= 1 && (KEEPV == 1 || KEEPV == 2 || KEEPV == 4), "reduce-scatter split");
+    static_assert(BV <= NT, "one thread per column in the finishing step");
     static_assert(IN_K % 16 == 0 && IN_A % 16 == 0 && IN_V % 16 == 0 && RED_BYTES % 16 == 0, "layout");
     // rows rg + RG * i share the swizzle XOR term of row rg (patterns repeat every 8 rows of 128 B,
     // 8 rows of 64 B read as pairs, 8 rows of 32 B read as quads: 1024 B in each case)
@@ -78,6 +84,7 @@ kda_decode_kernel(const __grid_constant__ CUtensorMap tmap, const StepParams p) 
     using SH = DecodeShape<ST, BV, NT, (int)sizeof(QT)>;
     using SV = StateVec<ST>;
     constexpr int VEC = SH::VEC, CL = SH::CL, RG = SH::RG, ROWS = SH::ROWS, NWARP = SH::NWARP;
+    constexpr int KEEPV = SH::KEEPV;
 
     extern __shared__ __align__(1024) uint8_t smem[];
     uint8_t* in = smem + SH::TILE_BYTES;
@@ -85,7 +92,8 @@ kda_decode_kernel(const __grid_constant__ CUtensorMap tmap, const StepParams p) 
     float* gv = reinterpret_cast<float*>(gates + KMAX);
     float* red = reinterpret_cast<float*>(in + SH::WORK_BYTES);  // [NWARP][4]
     float* red2 = red + NWARP * 4;                               // [NWARP][CL][2 VEC]
-    uint64_t* bar_st = reinterpret_cast<uint64_t*>(red2 + NWARP * CL * 2 * VEC);  // state tile landed
+    float* dsm = red2 + NWARP * CL * 2 * VEC;                    // [BV]: d = v - u
+    uint64_t* bar_st = reinterpret_cast<uint64_t*>(dsm + BV);    // state tile landed
     uint64_t* bar_in = bar_st + 1;                                                 // inputs landed
     const uint32_t tile_base = smem_u32(smem);
     const uint32_t gate_base = smem_u32(gates);
@@ -227,22 +235,30 @@ kda_decode_kernel(const __grid_constant__ CUtensorMap tmap, const StepParams p) 
             }
         }
     }
-    // sum over the row groups of this warp (lanes that share cl) ...
+    // Sum over the row groups of this warp (the lanes that share cl) as a
+    // reduce-scatter: each step hands the partner lane the half of the values
+    // this lane will not keep, so the lane ends with KEEPV finished sums of
+    // the 2 VEC values {u[0..VEC), p[0..VEC)} of chunk cl, at index kbase.
+    float vals[2 * VEC];
 #pragma unroll
-    for (int off = CL; off < 32; off <<= 1) {
+    for (int c = 0; c < VEC; ++c) { vals[c] = u[c]; vals[VEC + c] = pp[c]; }
+    int kbase = 0;
 #pragma unroll
-        for (int c = 0; c < VEC; ++c) {
-            u[c] += __shfl_xor_sync(0xffffffffu, u[c], off);
-            pp[c] += __shfl_xor_sync(0xffffffffu, pp[c], off);
+    for (int m = 16, cnt = 2 * VEC; m >= CL; m >>= 1, cnt >>= 1) {
+        const bool upper = (lane & m) != 0;
+#pragma unroll
+        for (int j = 0; j < cnt / 2; ++j) {
+            const float send = upper ? vals[j] : vals[j + cnt / 2];
+            const float keep = upper ? vals[j + cnt / 2] : vals[j];
+            vals[j] = keep + __shfl_xor_sync(0xffffffffu, send, m);
         }
+        kbase += upper ? cnt / 2 : 0;
     }
-    if (lane < CL) {
-        float4* dst4 = reinterpret_cast<float4*>(red2 + (warp * CL + cl) * 2 * VEC);
-#pragma unroll
-        for (int c = 0; c < VEC; c += 4) {
-            dst4[c / 4] = make_float4(u[c], u[c + 1], u[c + 2], u[c + 3]);
-            dst4[(VEC + c) / 4] = make_float4(pp[c], pp[c + 1], pp[c + 2], pp[c + 3]);
-        }
+    {
+        float* dst = red2 + (warp * CL + cl) * 2 * VEC + kbase;
+        if (KEEPV == 4) *reinterpret_cast<float4*>(dst) = make_float4(vals[0], vals[1], vals[2], vals[3]);
+        else if (KEEPV == 2) *reinterpret_cast<float2*>(dst) = make_float2(vals[0], vals[1]);
+        else dst[0] = vals[0];
     }
     if (__syncthreads_or(ok_st ? 0 : 1)) {  // the state tile did not land in time
         if (tid == 0) {
@@ -251,34 +267,28 @@ kda_decode_kernel(const __grid_constant__ CUtensorMap tmap, const StepParams p) 
         }
         return;
     }
-    // ... then over the warps (16-byte reads: lanes with the same cl share them).
-    float su[VEC], sp[VEC];
+    // ... then over the warps: thread j < BV finishes column j, writes its
+    // output and leaves d_j = v_j - u_j for the update.
+    const int ncols = min(BV, p.v - cb * BV);
+    if (tid < ncols) {
+        const int jc = tid / VEC, jv = tid - jc * VEC;
+        float su = 0.f, sp = 0.f;
 #pragma unroll
-    for (int c = 0; c < VEC; ++c) { su[c] = 0.f; sp[c] = 0.f; }
-#pragma unroll
-    for (int w = 0; w < NWARP; ++w) {
-        const float4* src4 = reinterpret_cast<const float4*>(red2 + (w * CL + cl) * 2 * VEC);
-#pragma unroll
-        for (int c = 0; c < VEC; c += 4) {
-            const float4 a4 = src4[c / 4], b4 = src4[(VEC + c) / 4];
-            su[c] += a4.x; su[c + 1] += a4.y; su[c + 2] += a4.z; su[c + 3] += a4.w;
-            sp[c] += b4.x; sp[c + 1] += b4.y; sp[c + 2] += b4.z; sp[c + 3] += b4.w;
+        for (int w = 0; w < NWARP; ++w) {
+            su += red2[(w * CL + jc) * 2 * VEC + jv];
+            sp += red2[(w * CL + jc) * 2 * VEC + VEC + jv];
         }
+        const float dj = gv[tid] - su;
+        dsm[tid] = dj;
+        p.o[(int64_t)r * p.v + cb * BV + tid] = fmaf(bqk, dj, sp) * p.inv_sqrt_k;
     }
+    __syncthreads();
+    if (col0 >= p.v) return;
     float d[VEC];
 #pragma unroll
     for (int c = 0; c < VEC; c += 4) {
-        const float4 v4 = *reinterpret_cast<const float4*>(gv + cl * VEC + c);
-        d[c] = v4.x - su[c];  // d_j = v_j - u_j
-        d[c + 1] = v4.y - su[c + 1];
-        d[c + 2] = v4.z - su[c + 2];
-        d[c + 3] = v4.w - su[c + 3];
-    }
-    if (col0 >= p.v) return;
-    if (rg == 0) {
-        float* o = p.o + (int64_t)r * p.v + col0;
-#pragma unroll
-        for (int c = 0; c < VEC; ++c) o[c] = fmaf(bqk, d[c], sp[c]) * p.inv_sqrt_k;
+        const float4 d4 = *reinterpret_cast<const float4*>(dsm + cl * VEC + c);
+        d[c] = d4.x; d[c + 1] = d4.y; d[c + 2] = d4.z; d[c + 3] = d4.w;
     }
 
     // (3) the delta update S' = alpha S + (beta khat) d, stored in place with
