@@ -120,8 +120,9 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 // Tensor map of the pool as a 3-D tensor [num_slots][hv * k][v] (v innermost),
-// box [1][k][bv]: one tile of one head of one slot.  Out-of-range columns of a
-// partial last tile load as zeros and are not stored.
+// box [1][k][bv]: one tile of one head of one slot, swizzled to match the row
+// bytes.  Out-of-range columns of a partial last tile load as zeros and are
+// not stored.
 int make_pool_map(const kda_pool* pool, int bv, CUtensorMap* map) {
     PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
     if (enc == nullptr) return KDA_ERR_LAUNCH;

@@ -5,27 +5,45 @@
 // chunk.  The state tile is TMA-loaded once from init_slot[n] (or taken as
 // zero on reset); lane l of warp w then carries rows l, l+32, l+64, l+96 of
 // chunk w in fp32 registers through the T tokens without rounding.  After each
-// token the state, rounded to the pool's dtype, is written to a shared-memory
-// staging buffer (three in turn) and TMA-stored, as one coalesced box, to that
-// token's snapshot slot snap_slot[n][t] (ROCm/ATOM pull request 2945, Changes:
-// the state after each token goes to the token's snapshot slot through
-// state_at).
+// token the state, rounded to the pool's dtype, is written to a swizzled
+// shared-memory staging tile and from there to that token's snapshot slot
+// snap_slot[n][t] (ROCm/ATOM pull request 2945, Changes: the state after each
+// token goes to the token's snapshot slot through state_at): either as one TMA
+// box store (KDA_VER_TMA_STORE, NSTAGE buffers in turn) or by every thread
+// reading back whole 16-byte row pieces and storing them coalesced (two
+// buffers in turn).
 //
-// The gates do not depend on the state, so they are worked out for a chunk of
-// up to TC tokens at once, from inputs bulk-copied into shared memory together
-// (q, k, a rows and the tile's v slice of every token): the per-token norms
-// and beta by one warp (a lane per token), then per row
-//   w_i = alpha_i khat_i,  z_i = alpha_i qhat_i,  alpha_i,  beta khat_i.
-// Each token then costs each warp one pass over its registers:
-// u_j = sum_i S_ij w_i and p_j = sum_i S_ij z_i reduce over the lanes by
-// shuffles; d_j = v_j - u_j; o_j = (p_j + beta (qhat . khat) d_j) / sqrt(K);
-// S_ij <- alpha_i S_ij + (beta khat_i) d_j; and one CTA barrier before thread 0
-// issues the snapshot's TMA store.
+// Tokens are taken in chunks of up to TC.  Within a chunk the recurrence
+//   S_t = D_t S_{t-1} + beta_t khat_t d_t^T,   D_t = diag(alpha_t),
+//   d_t = v_t - (D_t S_{t-1})^T khat_t,        o_t = S_t^T qhat_t / sqrt(K)
+// unrolls from the chunk's initial state S_0.  With P_ts = D_{s+1} ... D_t
+// (P_tt = I) and c_t = alpha_1 ... alpha_t (elementwise):
+//   (D_t S_{t-1})^T khat_t = S_0^T (c_t khat_t) + sum_{s<t}  A_ts d_s,
+//   S_t^T qhat_t           = S_0^T (c_t qhat_t) + sum_{s<=t} B_ts d_s,
+//   A_ts = beta_s sum_i khat_s,i P_ts,ii khat_t,i,
+//   B_ts = beta_s sum_i khat_s,i P_ts,ii qhat_t,i.
+// So one pass over S_0 gives the 2 TC column sums of every token at once (no
+// reduction waits on the previous token), each column solves its T x T
+// lower-triangular system for d by forward substitution, and the snapshots
+// then need only S_t = alpha_t S_{t-1} + (beta_t khat_t) d_t^T per element.
+// It is the token-by-token recurrence with its sums taken in another order;
+// the products P are formed by multiplication, never division, so alpha = 0
+// stays exact.
 // Barrier waits are bounded (1 s); one that runs out makes the CTA record
 // KDA_ERR_TIMEOUT, wait once more (bounded) for its copies, and exit.
 #pragma once
 
 #include "kda_common.cuh"
+
+#ifndef KDA_VER_TMA_STORE
+#define KDA_VER_TMA_STORE 1
+#endif
+#ifndef KDA_VER_MINB
+#define KDA_VER_MINB 3
+#endif
+#ifndef KDA_VER_NSTAGE
+#define KDA_VER_NSTAGE 3
+#endif
 
 namespace kda {
 
@@ -35,25 +53,39 @@ struct VerifyShape {
     static constexpr int ROWBYTES = BV * (int)sizeof(ST);
     static constexpr int NW = ROWBYTES / 16;  // warps, one per 16-byte column chunk
     static constexpr int NT = 32 * NW;
+    // resident CTAs per SM the register budget must allow: at the configured
+    // shapes a launch is about 2.5 CTAs per SM, so 3 keep it in one wave
+    static constexpr int MINB = KDA_VER_MINB;
     static constexpr int ROWS = KMAX / 32;    // rows per lane
-    static constexpr int TC = 8;              // tokens per chunk of inputs and gates
+    static constexpr int TC = 8;              // tokens per chunk
+    static constexpr int NA = TC * (TC - 1) / 2, NB = TC * (TC + 1) / 2;  // 28 + 36 = 64 sums
+    static constexpr int G = 16 / VEC;        // tokens per group of column sums (2 G VEC = 32 values)
     static constexpr uint32_t TILE_BYTES = (KMAX * ROWBYTES + 1023u) & ~1023u;
     // per token inputs: q row, k row (QES-byte elements), a row (fp32), v slice
     static constexpr uint32_t IN_Q = 0, IN_K = KMAX * QES, IN_A = 2 * KMAX * QES;
     static constexpr uint32_t IN_V = IN_A + KMAX * 4, IN_TOK = (IN_V + BV * QES + 15u) & ~15u;
-    // per token gates: float4 per row, then v (fp32)
+    // per token gates: float4 {c khat, c qhat, alpha, beta khat} per row, then v (fp32)
     static constexpr uint32_t G_V = KMAX * 16, G_TOK = G_V + BV * 4;
     static constexpr uint32_t IN_BYTES = TC * IN_TOK, GATE_BYTES = TC * G_TOK;
     // the gates overlay the inputs, which are all read into registers first
     static constexpr uint32_t WORK_BYTES = IN_BYTES > GATE_BYTES ? IN_BYTES : GATE_BYTES;
     // staging buffers for the snapshot stores (the state tile's area is the first)
-    static constexpr int NSTAGE = 3;
-    // norms [TC][NW][4], per-token scalars [TC] float4, snapshot ids [TC]
-    static constexpr uint32_t RED_BYTES = TC * NW * 16 + TC * 16 + TC * 4;
+    static constexpr bool TMA_STORE = KDA_VER_TMA_STORE != 0;
+    static constexpr int NSTAGE = TMA_STORE ? KDA_VER_NSTAGE : 2;
+    // norms [TC][NW][2] and b [TC], scalars [TC] float4, A and B per warp
+    // [NW][64] then summed [64], column sums [TC][2][BV], d [TC][BV], snapshot ids [TC]
+    static constexpr uint32_t RED_NORM = 0, RED_B = RED_NORM + TC * NW * 8;
+    static constexpr uint32_t RED_SCAL = (RED_B + TC * 4 + 15u) & ~15u, RED_ABW = RED_SCAL + TC * 16;
+    static constexpr uint32_t RED_AB = RED_ABW + NW * 64 * 4, RED_RES = RED_AB + 64 * 4;
+    static constexpr uint32_t RED_D = RED_RES + TC * 2 * BV * 4, RED_SNAP = RED_D + TC * BV * 4;
+    static constexpr uint32_t RED_BYTES = (RED_SNAP + TC * 4 + 15u) & ~15u;
     static_assert(ROWBYTES == 128 || ROWBYTES == 64, "tile row bytes");
     static_assert(NT >= KMAX, "one thread per key row in the gate phase");
+    static_assert(NA + NB == 64 && 2 * G * VEC == 32 && TC % G == 0 && TC == 8, "chunk shape");
+    static_assert(BV <= NT, "one thread per column in the solve");
+    static_assert(NSTAGE >= 2, "staging buffers");
     static_assert(IN_K % 16 == 0 && IN_A % 16 == 0 && IN_V % 16 == 0 && G_TOK % 16 == 0 &&
-                  WORK_BYTES % 16 == 0 && RED_BYTES % 16 == 0, "layout");
+                  WORK_BYTES % 16 == 0 && RED_RES % 16 == 0 && RED_D % 16 == 0, "layout");
 };
 
 template <typename ST, int BV, int QES>
@@ -62,20 +94,51 @@ constexpr size_t verify_smem_bytes() {
     return SH::NSTAGE * SH::TILE_BYTES + SH::WORK_BYTES + SH::RED_BYTES + 16;
 }
 
+// Position of A_ts (s < t) and of B_ts (s <= t) among a chunk's 64 row sums.
+__host__ __device__ constexpr int idx_a(int t, int s) { return t * (t - 1) / 2 + s; }
+__host__ __device__ constexpr int idx_b(int t, int s) { return 28 + t * (t + 1) / 2 + s; }
+
+// This row's terms of the row sums LO .. LO + 31 (A and B above): e runs
+// through beta_s khat_s,i P_ts,ii for t = s, s + 1, ...  Every index is a
+// compile-time constant, so only the 32 requested terms are formed.
+template <int LO, int TC>
+__device__ __forceinline__ void ab_terms(float (&out)[32], const float (&bk)[TC], const float (&kh)[TC],
+                                         const float (&qh)[TC], const float (&al)[TC]) {
+#pragma unroll
+    for (int i = 0; i < 32; ++i) out[i] = 0.f;
+#pragma unroll
+    for (int s = 0; s < TC; ++s) {
+        float e = bk[s];
+        if (idx_b(s, s) >= LO && idx_b(s, s) < LO + 32) out[idx_b(s, s) - LO] = e * qh[s];
+#pragma unroll
+        for (int t = s + 1; t < TC; ++t) {
+            e *= al[t];
+            if (idx_a(t, s) >= LO && idx_a(t, s) < LO + 32) out[idx_a(t, s) - LO] = e * kh[t];
+            if (idx_b(t, s) >= LO && idx_b(t, s) < LO + 32) out[idx_b(t, s) - LO] = e * qh[t];
+        }
+    }
+}
+
 template <typename ST, typename QT, int BV>
-__global__ void __launch_bounds__(VerifyShape<ST, BV, (int)sizeof(QT)>::NT)
+__global__ void __launch_bounds__(VerifyShape<ST, BV, (int)sizeof(QT)>::NT, VerifyShape<ST, BV, (int)sizeof(QT)>::MINB)
 kda_verify_kernel(const __grid_constant__ CUtensorMap tmap, const StepParams p) {
     using SH = VerifyShape<ST, BV, (int)sizeof(QT)>;
     using SV = StateVec<ST>;
-    constexpr int VEC = SH::VEC, NW = SH::NW, ROWS = SH::ROWS, TC = SH::TC;
+    constexpr int VEC = SH::VEC, NW = SH::NW, ROWS = SH::ROWS, TC = SH::TC, G = SH::G;
 
     extern __shared__ __align__(1024) uint8_t smem[];
     uint8_t* ins = smem + SH::NSTAGE * SH::TILE_BYTES;
     uint8_t* gts = ins;  // overlays the inputs once they are in registers
-    float* red = reinterpret_cast<float*>(ins + SH::WORK_BYTES);  // [TC][NW][4]
-    float4* scal = reinterpret_cast<float4*>(red + TC * NW * 4);  // [TC] {beta, bqk, rk, rq}
-    int32_t* snaps = reinterpret_cast<int32_t*>(scal + TC);       // [TC]
-    uint64_t* bar_st = reinterpret_cast<uint64_t*>(snaps + TC);
+    uint8_t* redb = ins + SH::WORK_BYTES;
+    float* nrm = reinterpret_cast<float*>(redb + SH::RED_NORM);    // [TC][NW][2]
+    float* bsm = reinterpret_cast<float*>(redb + SH::RED_B);       // [TC]
+    float4* scal = reinterpret_cast<float4*>(redb + SH::RED_SCAL); // [TC] {beta, rk, rq, -}
+    float* abw = reinterpret_cast<float*>(redb + SH::RED_ABW);     // [NW][64]
+    float* ab = reinterpret_cast<float*>(redb + SH::RED_AB);       // [64]
+    float* res = reinterpret_cast<float*>(redb + SH::RED_RES);     // [TC][2][BV]
+    float* dsm = reinterpret_cast<float*>(redb + SH::RED_D);       // [TC][BV]
+    int32_t* snaps = reinterpret_cast<int32_t*>(redb + SH::RED_SNAP);  // [TC]
+    uint64_t* bar_st = reinterpret_cast<uint64_t*>(redb + SH::RED_BYTES);
     uint64_t* bar_in = bar_st + 1;
     const uint32_t tile_base = smem_u32(smem);
     const uint32_t gate_base = smem_u32(gts);
@@ -88,7 +151,6 @@ kda_verify_kernel(const __grid_constant__ CUtensorMap tmap, const StepParams p) 
     const int cb = tile - r * vt;
     const int n = r / p.hv;
     const int h = r - n * p.hv;
-    const int col0 = cb * BV + chunk * VEC;
     const int T = p.t;
     const int qes = (int)sizeof(QT);
     const int vcols = min(BV, p.v - cb * BV);
@@ -97,77 +159,89 @@ kda_verify_kernel(const __grid_constant__ CUtensorMap tmap, const StepParams p) 
         return;
     }
 
+    const uint32_t qk_bytes = (uint32_t)p.k * qes;
+    const uint32_t v_bytes = (uint32_t)vcols * qes;
+    // inputs of tokens t0 .. t0 + tc - 1 into the work area: lane 0 of warp 0
+    // arms the barrier with the whole byte count, then warp 0 issues the 4 tc
+    // copies (none of them depends on a slot id)
+    auto issue_inputs = [&](int t0, int tc) {
+        if (lane == 0)
+            mbar_arrive_expect_tx(bar_in, (uint32_t)tc * (2 * qk_bytes + (uint32_t)p.k * 4 + v_bytes));
+        __syncwarp();
+        for (int c = lane; c < 4 * tc; c += 32) {
+            const int j = c >> 2, kind = c & 3;
+            const int64_t rt = ((int64_t)n * T + t0 + j) * p.hv + h;
+            uint8_t* in = ins + j * SH::IN_TOK;
+            if (kind == 0)
+                bulk_load(in + SH::IN_Q, static_cast<const char*>(p.q) + rt * qk_bytes, qk_bytes, bar_in);
+            else if (kind == 1)
+                bulk_load(in + SH::IN_K, static_cast<const char*>(p.kk) + rt * qk_bytes, qk_bytes, bar_in);
+            else if (kind == 2)
+                bulk_load(in + SH::IN_A, p.a + rt * p.k, (uint32_t)p.k * 4, bar_in);
+            else
+                bulk_load(in + SH::IN_V, static_cast<const char*>(p.vv) + (rt * p.v + (int64_t)cb * BV) * qes,
+                          v_bytes, bar_in);
+        }
+    };
+
     // Programmatic dependent launch: as in the decode kernel, only the slot ids
     // and the state may be read before the previous kernel completes, and only
-    // when the caller vouches for it (KDA_LAUNCH_PDL_EARLY_STATE).
+    // when the caller vouches for it (KDA_LAUNCH_PDL_EARLY_STATE).  The first
+    // chunk's inputs are requested as soon as that allows, before the slot ids
+    // are even read.
     cudaTriggerProgrammaticLaunchCompletion();
     const bool early = (p.flags & LAUNCH_PDL_EARLY_STATE) != 0;
+    if (tid == 0) {
+        mbar_init(bar_st, 1);
+        mbar_init(bar_in, 1);
+        fence_mbar_init();
+    }
     if (!early) cudaGridDependencySynchronize();
-
+    // the slot ids are requested first, the inputs while they are in flight
     const int32_t slot = p.init_slot[n];
-    bool bad = slot < 0 || slot >= p.num_slots;
-    for (int t = lane; t < T; t += 32) {
+    const int32_t snap0 = lane < T ? p.snap_slot[(int64_t)n * T + lane] : 0;
+    if (!early && warp == 0) issue_inputs(0, min(TC, T));
+    bool bad = slot < 0 || slot >= p.num_slots || snap0 < 0 || snap0 >= p.num_slots;
+    for (int t = lane + 32; t < T; t += 32) {
         const int32_t s = p.snap_slot[(int64_t)n * T + t];
         bad |= (s < 0 || s >= p.num_slots);
     }
     bad = __any_sync(0xffffffffu, bad);  // the same answer in every warp
     const bool rst = !bad && p.reset != nullptr && p.reset[n] != 0;
-    if (tid == 0) {
-        mbar_init(bar_st, 1);
-        mbar_init(bar_in, 1);
-        fence_mbar_init();
-        if (!bad && !rst) {
-            prefetch_tmap(&tmap);
-            mbar_arrive_expect_tx(bar_st, (uint32_t)p.k * SH::ROWBYTES);
-            tma_load_3d(smem, &tmap, bar_st, cb * BV, h * p.k, slot);
-        }
+    if (tid == 0 && !bad && !rst) {
+        prefetch_tmap(&tmap);
+        mbar_arrive_expect_tx(bar_st, (uint32_t)p.k * SH::ROWBYTES);
+        tma_load_3d(smem, &tmap, bar_st, cb * BV, h * p.k, slot);
     }
-    if (early) cudaGridDependencySynchronize();
+    if (early) {
+        cudaGridDependencySynchronize();
+        if (warp == 0) issue_inputs(0, min(TC, T));
+    }
     if (bad) {
-        if (tid == 0) atomicCAS(p.status, 0, STATUS_SLOT_RANGE);
-        return;  // uniform; nothing was issued
+        if (tid == 0) {
+            atomicCAS(p.status, 0, STATUS_SLOT_RANGE);
+            mbar_wait(bar_in, 0);  // bounded: the input copies land before the CTA exits
+        }
+        return;  // uniform; no state copy was issued
     }
     __syncthreads();  // barriers initialised
 
-    const uint32_t qk_bytes = (uint32_t)p.k * qes;
-    const uint32_t v_bytes = (uint32_t)vcols * qes;
     float x[ROWS][VEC];
     bool state_in = false;
     bool alive = true;
     int in_phase = 0;
     for (int t0 = 0; t0 < T; t0 += TC) {
         const int tc = min(TC, T - t0);
-        // inputs of tokens t0 .. t0 + tc - 1: lane 0 of warp 0 arms the barrier
-        // with the whole byte count, then warp 0 issues the 4 tc copies
-        if (warp == 0) {
-            if (lane == 0)
-                mbar_arrive_expect_tx(bar_in, (uint32_t)tc * (2 * qk_bytes + (uint32_t)p.k * 4 + v_bytes));
-            __syncwarp();
-            for (int c = lane; c < 4 * tc; c += 32) {
-                const int j = c >> 2, kind = c & 3;
-                const int64_t rt = ((int64_t)n * T + t0 + j) * p.hv + h;
-                uint8_t* in = ins + j * SH::IN_TOK;
-                if (kind == 0)
-                    bulk_load(in + SH::IN_Q, static_cast<const char*>(p.q) + rt * qk_bytes, qk_bytes, bar_in);
-                else if (kind == 1)
-                    bulk_load(in + SH::IN_K, static_cast<const char*>(p.kk) + rt * qk_bytes, qk_bytes, bar_in);
-                else if (kind == 2)
-                    bulk_load(in + SH::IN_A, p.a + rt * p.k, (uint32_t)p.k * 4, bar_in);
-                else
-                    bulk_load(in + SH::IN_V,
-                              static_cast<const char*>(p.vv) + (rt * p.v + (int64_t)cb * BV) * qes, v_bytes,
-                              bar_in);
-            }
-        }
-        float bt = 0.f;
+        if (t0 > 0 && warp == 0) issue_inputs(t0, tc);
         if (tid < tc) {
-            bt = __ldg(p.b + ((int64_t)n * T + t0 + tid) * p.hv + h);
+            bsm[tid] = __ldg(p.b + ((int64_t)n * T + t0 + tid) * p.hv + h);
             snaps[tid] = p.snap_slot[(int64_t)n * T + t0 + tid];
         }
         const bool ok_in = mbar_wait(bar_in, in_phase);
         in_phase ^= 1;
 
-        // (1) row tid of every token: k, q, alpha; partial norms per warp
+        // (1) row tid of every token: k, q, alpha; the squared norms of k and q
+        // per warp (one reduce-scatter of 16 values: lane pair 2m holds value m)
         float kt[TC], qt[TC], at[TC], vv[TC];
 #pragma unroll
         for (int j = 0; j < TC; ++j) {
@@ -182,47 +256,56 @@ kda_verify_kernel(const __grid_constant__ CUtensorMap tmap, const StepParams p) 
                 if (tid < vcols) vv[j] = to_f32(reinterpret_cast<const QT*>(in + SH::IN_V)[tid]);
             }
         }
+        {
+            float sq[2 * TC];
 #pragma unroll
-        for (int j = 0; j < TC; ++j) {
-            const float s1 = warp_sum(kt[j] * kt[j]), s2 = warp_sum(qt[j] * qt[j]), s3 = warp_sum(kt[j] * qt[j]);
-            if (lane == 0) {
-                float* rj = red + (j * NW + warp) * 4;
-                rj[0] = s1;
-                rj[1] = s2;
-                rj[2] = s3;
+            for (int j = 0; j < TC; ++j) { sq[2 * j] = kt[j] * kt[j]; sq[2 * j + 1] = qt[j] * qt[j]; }
+            const float s = warp_reduce_scatter<2 * TC>(sq, lane);
+            if ((lane & 1) == 0) {
+                const int m = lane >> 1;  // token m >> 1, k (even) or q (odd)
+                nrm[((m >> 1) * NW + warp) * 2 + (m & 1)] = s;
             }
         }
-        if (tid < TC) red[(tid * NW) * 4 + 3] = bt;
         if (__syncthreads_or(ok_in ? 0 : 1)) {
             alive = false;
             break;
         }
         // (2) per-token scalars, a lane per token
         if (warp == 0 && lane < tc) {
-            float kk2 = 0.f, qq2 = 0.f, kq = 0.f;
+            float kk2 = 0.f, qq2 = 0.f;
 #pragma unroll
             for (int w = 0; w < NW; ++w) {
-                kk2 += red[(lane * NW + w) * 4 + 0];
-                qq2 += red[(lane * NW + w) * 4 + 1];
-                kq += red[(lane * NW + w) * 4 + 2];
+                kk2 += nrm[(lane * NW + w) * 2 + 0];
+                qq2 += nrm[(lane * NW + w) * 2 + 1];
             }
-            const float rk = __frsqrt_rn(kk2 + L2_EPS), rq = __frsqrt_rn(qq2 + L2_EPS);
-            const float beta = __frcp_rn(1.0f + expf(-red[(lane * NW) * 4 + 3]));  // sigmoid(b)
-            scal[lane] = make_float4(beta, beta * (kq * rk * rq), rk, rq);
+            const float beta = __frcp_rn(1.0f + expf(-bsm[lane]));  // sigmoid(b)
+            scal[lane] = make_float4(beta, __frsqrt_rn(kk2 + L2_EPS), __frsqrt_rn(qq2 + L2_EPS), 0.f);
         }
         __syncthreads();
-        // (3) gates of row tid for every token (the inputs are dead now)
+        // (3) row tid: the gates of every token, then this row's terms of the
+        // 64 sums A and B, summed over the warp's rows (two reduce-scatters of
+        // 32: lane L holds sum L of each half) and stored per warp
+        {
+            float kh[TC], qh[TC], bk[TC], cdec = 1.f;
 #pragma unroll
-        for (int j = 0; j < TC; ++j) {
-            if (j < tc) {
+            for (int j = 0; j < TC; ++j) {
                 const float4 sc = scal[j];
-                uint8_t* g = gts + j * SH::G_TOK;
-                if (tid < p.k) {
-                    const float kh = kt[j] * sc.z, qh = qt[j] * sc.w;
-                    reinterpret_cast<float4*>(g)[tid] = make_float4(at[j] * kh, at[j] * qh, at[j], sc.x * kh);
+                kh[j] = j < tc ? kt[j] * sc.y : 0.f;
+                qh[j] = j < tc ? qt[j] * sc.z : 0.f;
+                bk[j] = j < tc ? sc.x * kh[j] : 0.f;
+                cdec *= at[j];  // c_j: alpha of tokens 0 .. j
+                if (j < tc) {
+                    uint8_t* g = gts + j * SH::G_TOK;
+                    if (tid < p.k)
+                        reinterpret_cast<float4*>(g)[tid] = make_float4(cdec * kh[j], cdec * qh[j], at[j], bk[j]);
+                    if (tid < BV) reinterpret_cast<float*>(g + SH::G_V)[tid] = vv[j];
                 }
-                if (tid < BV) reinterpret_cast<float*>(g + SH::G_V)[tid] = vv[j];
             }
+            float part[32];
+            ab_terms<0, TC>(part, bk, kh, qh, at);
+            abw[warp * 64 + lane] = warp_reduce_scatter<32>(part, lane);
+            ab_terms<32, TC>(part, bk, kh, qh, at);
+            abw[warp * 64 + 32 + lane] = warp_reduce_scatter<32>(part, lane);
         }
         if (!state_in) {  // the initial state, once, while the gates are written
             const bool ok_st = rst || mbar_wait(bar_st, 0);
@@ -242,72 +325,119 @@ kda_verify_kernel(const __grid_constant__ CUtensorMap tmap, const StepParams p) 
         } else {
             __syncthreads();
         }
+        if (tid < 64) {
+            float s = 0.f;
+#pragma unroll
+            for (int w = 0; w < NW; ++w) s += abw[w * 64 + tid];
+            ab[tid] = s;
+        }
 
-        // (4) the tokens, each warp on its own: no CTA barrier in this loop
-        for (int j = 0; j < tc; ++j) {
-            const int t = t0 + j;
-            const uint32_t gb = gate_base + j * SH::G_TOK;
-            const uint8_t* g = gts + j * SH::G_TOK;
-            float u[VEC], pp[VEC];
+        // (4) the column sums of the chunk's initial state against c khat and
+        // c qhat of every token, G tokens (32 values per lane) at a time
 #pragma unroll
-            for (int c = 0; c < VEC; ++c) { u[c] = 0.f; pp[c] = 0.f; }
-            float al[ROWS], bk[ROWS];
+        for (int g0 = 0; g0 < TC; g0 += G) {
+            if (g0 < tc) {
+                float acc[2 * G * VEC];
 #pragma unroll
-            for (int rr = 0; rr < ROWS; ++rr) {
-                const int row = lane + 32 * rr;
-                al[rr] = 0.f;
-                bk[rr] = 0.f;
-                if (row < p.k) {
-                    const uint4 gq = lds128(gb + row * 16);
-                    const float w = __uint_as_float(gq.x), z = __uint_as_float(gq.y);
-                    al[rr] = __uint_as_float(gq.z);
-                    bk[rr] = __uint_as_float(gq.w);
+                for (int i = 0; i < 2 * G * VEC; ++i) acc[i] = 0.f;
 #pragma unroll
-                    for (int c = 0; c < VEC; ++c) {
-                        u[c] = fmaf(x[rr][c], w, u[c]);
-                        pp[c] = fmaf(x[rr][c], z, pp[c]);
+                for (int jj = 0; jj < G; ++jj) {
+                    if (g0 + jj < tc) {
+                        const uint32_t gb = gate_base + (g0 + jj) * SH::G_TOK;
+#pragma unroll
+                        for (int rr = 0; rr < ROWS; ++rr) {
+                            const int row = lane + 32 * rr;
+                            if (row < p.k) {
+                                const uint4 gq = lds128(gb + row * 16);
+                                const float w = __uint_as_float(gq.x), z = __uint_as_float(gq.y);
+#pragma unroll
+                                for (int c = 0; c < VEC; ++c) {
+                                    acc[jj * 2 * VEC + c] = fmaf(x[rr][c], w, acc[jj * 2 * VEC + c]);
+                                    acc[jj * 2 * VEC + VEC + c] = fmaf(x[rr][c], z, acc[jj * 2 * VEC + VEC + c]);
+                                }
+                            }
+                        }
                     }
                 }
+                const float sum = warp_reduce_scatter<2 * G * VEC>(acc, lane);  // entry `lane`
+                const int jj = lane / (2 * VEC), kind = (lane / VEC) & 1, c = lane % VEC;
+                res[((g0 + jj) * 2 + kind) * BV + chunk * VEC + c] = sum;
             }
-            // u and p over the 32 lanes: reduce-scatter, then broadcast d
-            constexpr int NV = 2 * VEC, SHIFT = (NV == 16) ? 1 : 2;  // lanes per value: 1 << SHIFT
-            float rv[NV];
+        }
+        __syncthreads();
+
+        // (5) per column: forward substitution for d, and the outputs; the
+        // columns past V get d = 0
+        if (tid < BV) {
+            const int j = tid;
+            const bool col_ok = j < vcols;
+            float d[TC];
 #pragma unroll
-            for (int c = 0; c < VEC; ++c) { rv[c] = u[c]; rv[VEC + c] = pp[c]; }
-            const float sum = warp_reduce_scatter<NV>(rv, lane);
-            const int idx = lane >> SHIFT;  // value this lane holds: u_idx, or p_(idx - VEC)
-            const float* gv = reinterpret_cast<const float*>(g + SH::G_V) + chunk * VEC;
-            const float dmine = idx < VEC ? gv[idx] - sum : 0.f;  // d_j = v_j - u_j
+            for (int t = 0; t < TC; ++t) {
+                d[t] = 0.f;
+                if (t < tc) {
+                    if (col_ok) {
+                        const float* g = reinterpret_cast<const float*>(gts + t * SH::G_TOK + SH::G_V);
+                        float u = res[(t * 2 + 0) * BV + j];
+#pragma unroll
+                        for (int s = 0; s < t; ++s) u = fmaf(ab[idx_a(t, s)], d[s], u);
+                        d[t] = g[j] - u;  // d_t = v_t - (D_t S_(t-1))^T khat_t
+                        float o = res[(t * 2 + 1) * BV + j];
+#pragma unroll
+                        for (int s = 0; s <= t; ++s) o = fmaf(ab[idx_b(t, s)], d[s], o);
+                        p.o[(((int64_t)n * T + t0 + t) * p.hv + h) * p.v + cb * BV + j] = o * p.inv_sqrt_k;
+                    }
+                    dsm[t * BV + j] = d[t];
+                }
+            }
+        }
+        __syncthreads();
+
+        // (6) the snapshots: S_t = alpha_t S_(t-1) + (beta_t khat_t) d_t^T,
+        // staged rounded in a swizzled tile, then stored
+        for (int j = 0; j < tc; ++j) {
             float d[VEC];
 #pragma unroll
-            for (int c = 0; c < VEC; ++c) d[c] = __shfl_sync(0xffffffffu, dmine, c << SHIFT);
-            const bool col_ok = col0 < p.v;
-            if (idx >= VEC && (lane & ((1 << SHIFT) - 1)) == 0 && col_ok) {
-                const int c = idx - VEC;
-                float dc = d[0];
-#pragma unroll
-                for (int e = 1; e < VEC; ++e) dc = (c == e) ? d[e] : dc;
-                p.o[(((int64_t)n * T + t) * p.hv + h) * p.v + col0 + c] = fmaf(scal[j].y, dc, sum) * p.inv_sqrt_k;
+            for (int c = 0; c < VEC; c += 4) {
+                const float4 d4 = *reinterpret_cast<const float4*>(dsm + j * BV + chunk * VEC + c);
+                d[c] = d4.x; d[c + 1] = d4.y; d[c + 2] = d4.z; d[c + 3] = d4.w;
             }
-            // snapshot: stage the rounded rows, then one TMA store of the box
-            const int b = t % SH::NSTAGE;
+            const uint32_t gb = gate_base + j * SH::G_TOK;
+            const int b = (t0 + j) % SH::NSTAGE;
             const uint32_t stage = tile_base + b * SH::TILE_BYTES;
 #pragma unroll
             for (int rr = 0; rr < ROWS; ++rr) {
                 const int row = lane + 32 * rr;
                 if (row < p.k) {
+                    const uint4 gq = lds128(gb + row * 16);
+                    const float al = __uint_as_float(gq.z), bkr = __uint_as_float(gq.w);
 #pragma unroll
-                    for (int c = 0; c < VEC; ++c) x[rr][c] = fmaf(al[rr], x[rr][c], bk[rr] * d[c]);
+                    for (int c = 0; c < VEC; ++c) x[rr][c] = fmaf(al, x[rr][c], bkr * d[c]);
                     sts128(stage + swz<SH::ROWBYTES>(row, chunk), SV::narrow(x[rr]));
                 }
             }
-            fence_proxy_async_smem();
-            __syncthreads();
-            if (tid == 0) {
-                tma_store_3d(&tmap, smem + b * SH::TILE_BYTES, cb * BV, h * p.k, snaps[j]);
-                bulk_commit();
-                // the store of token t - 1 has read its buffer, which token t + 2 rewrites
-                bulk_wait_read<1>();
+            if constexpr (SH::TMA_STORE) {
+                fence_proxy_async_smem();
+                __syncthreads();
+                if (tid == 0) {
+                    tma_store_3d(&tmap, smem + b * SH::TILE_BYTES, cb * BV, h * p.k, snaps[j]);
+                    bulk_commit();
+                    // the stores of the last NSTAGE - 2 tokens may still read their
+                    // buffers; the one token t + 1 rewrites is free
+                    bulk_wait_read<SH::NSTAGE - 2>();
+                }
+            } else {
+                // Every thread stores whole 16-byte pieces of rows, consecutive
+                // threads along a row: coalesced.  The barrier also frees the
+                // other buffer, which the next token writes.
+                __syncthreads();
+                ST* dst = static_cast<ST*>(p.pool) + state_at(p, snaps[j], h) + cb * BV;
+                for (int pc = tid; pc < p.k * NW; pc += SH::NT) {
+                    const int row = pc / NW, ch = pc - row * NW;
+                    if (ch * VEC < vcols)
+                        __stcs(reinterpret_cast<uint4*>(dst + (int64_t)row * p.v + ch * VEC),
+                               lds128(stage + swz<SH::ROWBYTES>(row, ch)));
+                }
             }
         }
         // The next chunk's bulk copies (async proxy) overwrite this chunk's
@@ -315,7 +445,7 @@ kda_verify_kernel(const __grid_constant__ CUtensorMap tmap, const StepParams p) 
         fence_proxy_async_smem();
         __syncthreads();
     }
-    if (tid == 0) bulk_wait<0>();
+    if (SH::TMA_STORE && tid == 0) bulk_wait<0>();  // the snapshot stores are complete
     if (!alive) {
         if (tid == 0) {
             atomicExch(p.status, STATUS_TIMEOUT);
