@@ -533,7 +533,8 @@ def bench_verify(kda, workloads, torch, args, l2, peak):
         with torch.cuda.graph(g, stream=stream):
             for i in range(chunk):
                 lib.kda_spec_verify(pools[i % R], d.init_slot, d.snap_slot, d.q, d.k, d.v, d.a,
-                                    d.b, o, status)
+                                    d.b, o, status,
+                                    flags=kda.KDA_LAUNCH_PDL | kda.KDA_LAUNCH_PDL_EARLY_STATE)
         for _ in range(max(1, args.warmup // chunk)):
             g.replay()
     torch.cuda.synchronize()
@@ -551,7 +552,7 @@ def bench_verify(kda, workloads, torch, args, l2, peak):
     return {"workload": "spec verify, fp16 pool, N=8 x T=8, HV=12, K=V=128, fp32 q/k/v",
             "us_per_step": round(us, 3), "gbs": round(byt / (us * 1e-6) / 1e9, 1),
             "frac_of_peak": round(byt / (us * 1e-6) / 1e9 / peak, 4), "bytes_per_step": byt,
-            "pools": R, "launch": f"CUDA graph of {chunk} plain launches, replayed"}
+            "pools": R, "launch": f"CUDA graph of {chunk} launches, replayed; flags KDA_LAUNCH_PDL|KDA_LAUNCH_PDL_EARLY_STATE"}
 
 
 if __name__ == "__main__":

@@ -136,3 +136,86 @@ def make_sweep_layer(layer: int, n: int, state_dtype, hv=12, k=128, v=128, num_s
     return StepInputs(P, slots, q, kk, vv, a, b, None, reset,
                       dict(kind="decode", layer=layer, n=n, hv=hv, k=k, v=v,
                            num_slots=num_slots, seed=seed))
+
+
+@dataclass
+class GeneralInputs:
+    """CPU tensors of one general step (packed tokens, slot table)."""
+    pool: torch.Tensor                 # [num_slots, HV, K, V] fp32 or fp16
+    slot_table: torch.Tensor           # int32 [N, C]
+    q: torch.Tensor                    # [total, H, K]
+    k: torch.Tensor
+    v: torch.Tensor                    # [total, HV, V]
+    a: torch.Tensor                    # fp32 [total, HV, K]
+    b: torch.Tensor                    # fp32 [total, HV]
+    cu_seqlens: torch.Tensor | None = None   # int32 [N + 1]
+    accepted: torch.Tensor | None = None     # int32 [N], in 1 .. C
+    reset: torch.Tensor | None = None        # uint8 [N]
+    a_log: torch.Tensor | None = None        # fp32 [HV]
+    dt_bias: torch.Tensor | None = None      # fp32 [HV, K]
+    in_place: bool = False
+    max_t: int = 0
+    meta: dict = field(default_factory=dict)
+
+    def to(self, device) -> "GeneralInputs":
+        mv = lambda t: None if t is None else t.to(device)  # noqa: E731
+        return GeneralInputs(mv(self.pool), mv(self.slot_table), mv(self.q), mv(self.k), mv(self.v),
+                             mv(self.a), mv(self.b), mv(self.cu_seqlens), mv(self.accepted), mv(self.reset),
+                             mv(self.a_log), mv(self.dt_bias), self.in_place, self.max_t, dict(self.meta))
+
+
+def make_general(n=8, t_lens=None, t=8, num_cols=None, h_qk=None, hv=12, k=128, v=128, num_slots=256,
+                 state_dtype=torch.float16, qkv_dtype=torch.float32, seed=4, reset_p=0.0, pad_p=0.0,
+                 drop_p=0.0, accepted=True, gate_scale=False, in_place=False) -> GeneralInputs:
+    """A general step: requests of t_lens[r] tokens (packed; None: t each),
+    a slot table of num_cols distinct slots per request, the initial column
+    accepted[r] - 1 drawn uniformly, padding requests (whole row -1) with
+    probability pad_p, kept-snapshot entries dropped (-1) with probability
+    drop_p (never the initial column), grouped q/k heads (h_qk), and the
+    learned gate scale (A_log = log U(1, 16), dt_bias = log(expm1(dt)),
+    dt = exp U(log 1e-3, log 1e-1)).  in_place: one token per request, stored
+    back to the initial slot."""
+    g = torch.Generator().manual_seed(seed)
+    h_qk = hv if h_qk is None else h_qk
+    if in_place:
+        t_lens, t = None, 1
+    lens = [t] * n if t_lens is None else list(t_lens)
+    max_t = max(lens) if lens else 0
+    num_cols = max(max_t, 1) if num_cols is None else num_cols
+    if n * num_cols > num_slots:
+        raise ValueError("not enough slots for a table of distinct slots")
+    P = make_pool(g, num_slots, hv, k, v, state_dtype)
+    table = torch.randperm(num_slots, generator=g)[:n * num_cols].to(torch.int32).reshape(n, num_cols).clone()
+    total = sum(lens)
+    q = _randn(g, (total, h_qk, k), qkv_dtype)
+    kk = _randn(g, (total, h_qk, k), qkv_dtype)
+    vv = _randn(g, (total, hv, v), qkv_dtype)
+    a = _randn(g, (total, hv, k))
+    b = _randn(g, (total, hv))
+    acc = None
+    if accepted:
+        acc = (torch.randint(0, num_cols, (n,), generator=g) + 1).to(torch.int32)
+    c0 = acc.long() - 1 if acc is not None else torch.zeros(n, dtype=torch.long)
+    if drop_p > 0:
+        drop = torch.rand((n, num_cols), generator=g) < drop_p
+        drop[torch.arange(n), c0] = False
+        table[drop] = -1
+    if pad_p > 0:
+        pad = torch.rand((n,), generator=g) < pad_p
+        table[pad] = -1
+    reset = None
+    if reset_p > 0:
+        reset = (torch.rand((n,), generator=g) < reset_p).to(torch.uint8)
+    a_log = dt_bias = None
+    if gate_scale:
+        a_log = torch.log(1.0 + 15.0 * torch.rand((hv,), generator=g))
+        lo, hi = torch.log(torch.tensor(1e-3)), torch.log(torch.tensor(1e-1))
+        dt = torch.exp(lo + (hi - lo) * torch.rand((hv, k), generator=g))
+        dt_bias = torch.log(torch.expm1(dt))
+    cu = None
+    if t_lens is not None:
+        cu = torch.zeros(n + 1, dtype=torch.int32)
+        cu[1:] = torch.cumsum(torch.tensor(lens, dtype=torch.int64), 0).to(torch.int32)
+    return GeneralInputs(P, table, q, kk, vv, a, b, cu, acc, reset, a_log, dt_bias, in_place, max_t,
+                         dict(kind="general", n=n, hv=hv, h_qk=h_qk, k=k, v=v, num_slots=num_slots,
+                              seed=seed, lens=lens))

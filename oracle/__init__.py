@@ -80,6 +80,10 @@ def _load():
             lib.oracle_spec_verify.restype = ctypes.c_int
             lib.oracle_spec_verify.argtypes = common + [ctypes.c_int, i32p, i32p, u8p,
                                                         dp, dp, dp, dp, dp, dp, ctypes.c_int]
+            lib.oracle_step.restype = ctypes.c_int
+            lib.oracle_step.argtypes = common + [ctypes.c_int, i32p, ctypes.c_int, i32p, ctypes.c_int, i32p,
+                                                 ctypes.c_int, u8p, dp, dp, dp, dp, dp, dp, dp, dp,
+                                                 ctypes.c_int]
             _lib = lib
     return _lib
 
@@ -176,4 +180,39 @@ def spec_verify(pool: np.ndarray, init_slot, snap_slot, q, k, v, a, b, reset=Non
         int(nthreads))
     if rc != 0:
         raise ValueError(f"oracle_spec_verify failed ({rc}): slot id out of range")
+    return o
+
+
+def step(pool: np.ndarray, slot_table, q, k, v, a, b, cu_seqlens=None, accepted=None, reset=None,
+         a_log=None, dt_bias=None, in_place=False, slot_stride=None, nthreads: int = 1) -> np.ndarray:
+    """The general step: packed variable-length requests, a [N, C] slot table
+    (initial state at column accepted[r] - 1, token j's state to column j),
+    padding requests (negative initial slot), grouped q/k heads and the learned
+    gate scale.  Returns o fp64 [total, HV, V].
+
+    q, k: [total, H, K]; v: [total, HV, V]; a: [total, HV, K]; b: [total, HV];
+    without cu_seqlens every request has total / N tokens.
+    """
+    slot_table = np.ascontiguousarray(np.asarray(slot_table, dtype=np.int32))
+    n, ncols = slot_table.shape
+    args = _pool_args(pool, slot_stride)
+    hv, vdim = args[3], args[5]
+    q64, k64, v64, a64, b64 = (_f64(x) for x in (q, k, v, a, b))
+    total, h_qk = q64.shape[0], q64.shape[1]
+    cu = None if cu_seqlens is None else np.ascontiguousarray(np.asarray(cu_seqlens, dtype=np.int32))
+    t_uniform = 0 if cu is not None else (total // n if n else 0)
+    acc = None if accepted is None else np.ascontiguousarray(np.asarray(accepted, dtype=np.int32))
+    rs = None if reset is None else np.ascontiguousarray(np.asarray(reset, dtype=np.uint8))
+    al = None if a_log is None else _f64(a_log)
+    db = None if dt_bias is None else _f64(dt_bias)
+    o = np.zeros((total, hv, vdim), dtype=np.float64)
+    opt = lambda x, t: None if x is None else _ptr(x, t)
+    rc = _load().oracle_step(
+        *args, n, h_qk, opt(cu, ctypes.c_int32), t_uniform, _ptr(slot_table, ctypes.c_int32), ncols,
+        opt(acc, ctypes.c_int32), int(bool(in_place)), opt(rs, ctypes.c_uint8),
+        _ptr(q64, ctypes.c_double), _ptr(k64, ctypes.c_double), _ptr(v64, ctypes.c_double),
+        _ptr(a64, ctypes.c_double), _ptr(b64, ctypes.c_double), opt(al, ctypes.c_double),
+        opt(db, ctypes.c_double), _ptr(o, ctypes.c_double), int(nthreads))
+    if rc != 0:
+        raise ValueError(f"oracle_step failed ({rc}): " + ("slot id out of range" if rc == -1 else "layout"))
     return o

@@ -171,10 +171,28 @@ static double softplus(double a)
  *   S <- S + beta khat (v - u)^T                          (delta update)
  *   o  = S^T qhat / sqrt(K)                               (read-out, updated S)
  */
+static void recur_token_gated(int K, int V, double* S,
+                              const double* q, const double* k, const double* v,
+                              const double* a, double b, double scale, const double* bias,
+                              double* o, double* qh, double* kh, double* u);
+
 static void recur_token(int K, int V, double* S,
                         const double* q, const double* k, const double* v,
                         const double* a, double b, double* o,
                         double* qh, double* kh, double* u)
+{
+    recur_token_gated(K, V, S, q, k, v, a, b, 1.0, NULL, o, qh, kh, u);
+}
+
+/*
+ * The same token with the learned gate scale of the KDA layer:
+ *   alpha_i = exp(-scale * softplus(a_i + bias_i)),  scale = exp(A_log) of the head.
+ * scale = 1 and bias = NULL is the plain gate exp(-softplus(a_i)) above, to the bit.
+ */
+static void recur_token_gated(int K, int V, double* S,
+                              const double* q, const double* k, const double* v,
+                              const double* a, double b, double scale, const double* bias,
+                              double* o, double* qh, double* kh, double* u)
 {
     double qq = 0.0, kk = 0.0;
     for (int i = 0; i < K; ++i) { qq += q[i] * q[i]; kk += k[i] * k[i]; }
@@ -184,7 +202,7 @@ static void recur_token(int K, int V, double* S,
     double beta = 1.0 / (1.0 + exp(-b));
 
     for (int i = 0; i < K; ++i) {
-        double alpha = exp(-softplus(a[i]));
+        double alpha = exp(-(scale * softplus(bias ? a[i] + bias[i] : a[i])));
         for (int j = 0; j < V; ++j) S[(int64_t)i * V + j] *= alpha;
     }
     for (int j = 0; j < V; ++j) {
@@ -273,4 +291,93 @@ int oracle_spec_verify(void* base, int dtype, int64_t num_slots, int hv, int k, 
 {
     oracle_pool p = {base, dtype, num_slots, hv, k, v, slot_stride};
     return run(&p, n_req, T, init_slot, snap_slot, reset, q, kk, vv, a, b, o, nthreads);
+}
+
+/*
+ * The general step: accepted-length speculative decode over packed,
+ * variable-length requests (the address function state_at(c, slot) of ATOM
+ * pull request 2945, Changes, serving a request's initial state and each of
+ * its tokens' snapshot slots; the number of tokens a step keeps varies with
+ * the drafts accepted, ATOM pull request 2945, Performance).
+ *
+ *   tokens are packed: request r owns tokens cu[r] .. cu[r+1]-1 (T_r of them);
+ *     cu == NULL means T_r = t_uniform and request r owns r*t_uniform ..
+ *   q, k: [total][H][K] (value head h reads q/k head h / (HV / H));
+ *   v: [total][HV][V];  a: [total][HV][K];  b: [total][HV];  o: [total][HV][V]
+ *   slot_table[r][c], c < num_cols: the request's slots, column c = token c
+ *   initial column c0 = accepted ? accepted[r] - 1 : 0, which must lie in
+ *     [0, num_cols); the initial slot is slot_table[r][c0]
+ *   a negative initial slot marks a padding request: nothing is read or
+ *     stored and its output rows are zero
+ *   in_place (decode): T_r must be 1 and the state goes back to the initial
+ *     slot; otherwise the state after token j goes to slot_table[r][j], and a
+ *     negative entry there means that snapshot is not kept
+ *   reset[r] != 0 starts request r from a zero state
+ *   a_log ([HV]) and dt_bias ([HV][K]) may be NULL: scale 1, bias 0
+ * Returns 0; -1 for a slot id >= num_slots; -3 for an inconsistent layout
+ * (initial column outside the table, T_r > num_cols, T_r != 1 in place,
+ * H not dividing HV, cu not non-decreasing).
+ */
+int oracle_step(void* base, int dtype, int64_t num_slots, int hv, int k, int v,
+                int64_t slot_stride, int n_req, int h_qk, const int32_t* cu, int t_uniform,
+                const int32_t* slot_table, int num_cols, const int32_t* accepted, int in_place,
+                const uint8_t* reset, const double* q, const double* kk, const double* vv,
+                const double* a, const double* b, const double* a_log, const double* dt_bias,
+                double* o, int nthreads)
+{
+    oracle_pool p = {base, dtype, num_slots, hv, k, v, slot_stride};
+    const int HV = hv, K = k, V = v;
+    if (h_qk <= 0 || HV % h_qk != 0) return -3;
+    const int group = HV / h_qk;
+    for (int r = 0; r < n_req; ++r) {
+        int64_t t0 = cu ? cu[r] : (int64_t)r * t_uniform;
+        int64_t tr = cu ? (int64_t)cu[r + 1] - cu[r] : t_uniform;
+        if (tr < 0 || tr > num_cols || (in_place && tr != 1) || t0 < 0) return -3;
+        int c0 = accepted ? accepted[r] - 1 : 0;
+        if (c0 < 0 || c0 >= num_cols) return -3;
+        const int32_t* row = slot_table + (int64_t)r * num_cols;
+        if (row[c0] >= num_slots) return -1;
+        if (row[c0] < 0) continue;
+        if (!in_place)
+            for (int64_t j = 0; j < tr; ++j)
+                if (row[j] >= num_slots) return -1;
+    }
+    int64_t pairs = (int64_t)n_req * HV;
+    int bad = 0;
+#if defined(_OPENMP)
+#pragma omp parallel for schedule(dynamic, 1) num_threads(nthreads) if (nthreads > 1)
+#endif
+    for (int64_t nh = 0; nh < pairs; ++nh) {
+        int r = (int)(nh / HV), h = (int)(nh % HV);
+        int64_t t0 = cu ? cu[r] : (int64_t)r * t_uniform;
+        int64_t tr = cu ? (int64_t)cu[r + 1] - cu[r] : t_uniform;
+        const int32_t* row = slot_table + (int64_t)r * num_cols;
+        int32_t s0 = row[accepted ? accepted[r] - 1 : 0];
+        if (s0 < 0) {  /* padding request */
+            for (int64_t j = 0; j < tr; ++j)
+                memset(o + ((t0 + j) * HV + h) * V, 0, sizeof(double) * (size_t)V);
+            continue;
+        }
+        double* S = (double*)malloc(sizeof(double) * ((size_t)K * V + 2 * (size_t)K + (size_t)V));
+        if (!S) { bad = 1; continue; }
+        double* qh = S + (int64_t)K * V;
+        double* kh = qh + K;
+        double* u = kh + K;
+        if (reset && reset[r]) memset(S, 0, sizeof(double) * (size_t)K * V);
+        else load_state(&p, s0, h, S);
+        double scale = a_log ? exp(a_log[h]) : 1.0;
+        const double* bias = dt_bias ? dt_bias + (int64_t)h * K : NULL;
+        int hq = h / group;
+        for (int64_t j = 0; j < tr; ++j) {
+            int64_t tok = t0 + j;
+            int64_t vrow = tok * HV + h, qrow = tok * h_qk + hq;
+            recur_token_gated(K, V, S, q + qrow * K, kk + qrow * K, vv + vrow * V, a + vrow * K,
+                              b[vrow], scale, bias, o + vrow * V, qh, kh, u);
+            if (!in_place && row[j] >= 0) store_state(&p, row[j], h, S);
+        }
+        if (in_place) store_state(&p, s0, h, S);
+        free(S);
+    }
+    (void)nthreads;
+    return bad ? -2 : 0;
 }

@@ -20,6 +20,7 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 from kda_linear_attention_gated_gb300 import workloads
 
 EPS = 1e-6
@@ -360,3 +361,164 @@ def test_state_bytes_match_printed_memory_table():
     assert round(68 * (per_layer["fp32"] - per_layer["fp16"]) / 1e6, 2) != pytest.approx(printed)
     for dt in ("fp32", "fp16"):
         assert round(g["state_per_slot_MB"][dt] * 1e6 * 64 / 2**30, 2) == g["state_pool_64_slots_GB"][dt]
+
+
+# ---------------------------------------------------------------------------
+# The general step (accepted-length speculative decode, packed variable-length
+# requests, padding, grouped q/k heads, learned gate scale): each feature is
+# pinned to the plain forms above or to a closed form.
+# ---------------------------------------------------------------------------
+def _pool64(pool):
+    return pool.numpy().copy() if pool.dtype == torch.float32 else pool.view(torch.int16).numpy().view(np.uint16).copy()
+
+
+def _general(inp, **over):
+    pool = _pool64(inp.pool)
+    kw = dict(cu_seqlens=inp.cu_seqlens, accepted=inp.accepted, reset=inp.reset, a_log=inp.a_log,
+              dt_bias=inp.dt_bias, in_place=inp.in_place)
+    kw.update(over)
+    o = oracle.step(pool, inp.slot_table, inp.q, inp.k, inp.v, inp.a, inp.b, **kw)
+    return pool, o
+
+
+@pytest.mark.parametrize("state_dtype", [torch.float32, torch.float16])
+def test_general_step_is_verify_from_the_accepted_column(state_dtype):
+    inp = workloads.make_general(n=5, t=4, num_cols=6, hv=3, k=16, v=32, num_slots=40,
+                                 state_dtype=state_dtype, seed=21, reset_p=0.3)
+    pool, o = _general(inp)
+    n, t = 5, 4
+    ref = _pool64(inp.pool)
+    init = inp.slot_table[torch.arange(n), inp.accepted.long() - 1]
+    o_ref = oracle.spec_verify(ref, init, inp.slot_table[:, :t], inp.q.reshape(n, t, 3, 16),
+                               inp.k.reshape(n, t, 3, 16), inp.v.reshape(n, t, 3, 32),
+                               inp.a.reshape(n, t, 3, 16), inp.b.reshape(n, t, 3), reset=inp.reset)
+    assert np.array_equal(pool, ref)
+    assert np.array_equal(o.reshape(n, t, 3, 32), o_ref)
+
+
+@pytest.mark.parametrize("h_qk", [1, 2])
+def test_grouped_heads_equal_repeated_q_and_k(h_qk):
+    inp = workloads.make_general(n=3, t=3, hv=4, h_qk=h_qk, k=16, v=16, num_slots=20,
+                                 state_dtype=torch.float32, seed=22)
+    pool, o = _general(inp)
+    rep = 4 // h_qk
+    pool2, o2 = _general(inp, accepted=inp.accepted)  # same call, to show it is deterministic
+    q = inp.q.repeat_interleave(rep, dim=1)
+    k = inp.k.repeat_interleave(rep, dim=1)
+    ref = _pool64(inp.pool)
+    o_ref = oracle.step(ref, inp.slot_table, q, k, inp.v, inp.a, inp.b, accepted=inp.accepted)
+    assert np.array_equal(pool, ref) and np.array_equal(o, o_ref)
+    assert np.array_equal(pool2, pool) and np.array_equal(o2, o)
+    # a wrong head map (h % H instead of h / (HV / H)) would differ
+    q_bad = inp.q.repeat(1, rep, 1)
+    if h_qk > 1:
+        o_bad = oracle.step(_pool64(inp.pool), inp.slot_table, q_bad, inp.k.repeat(1, rep, 1), inp.v, inp.a,
+                            inp.b, accepted=inp.accepted)
+        assert not np.allclose(o_bad, o)
+
+
+def test_gate_scale_closed_forms():
+    """exp(-s softplus(a + d)) = (1 + e^(a+d))^(-s).  s = 1, d = 0 is the plain
+    gate to the bit; s = 2 equals the plain gate at a' = log((1 + e^(a+d))^2 - 1)."""
+    inp = workloads.make_general(n=3, t=2, hv=2, k=16, v=16, num_slots=12, state_dtype=torch.float32,
+                                 seed=23)
+    zero_log, zero_bias = torch.zeros(2), torch.zeros(2, 16)
+    p1, o1 = _general(inp, a_log=zero_log, dt_bias=zero_bias)
+    p0, o0 = _general(inp)
+    assert np.array_equal(p1, p0) and np.array_equal(o1, o0)
+    d = torch.linspace(-1.0, 1.0, 32, dtype=torch.float64).reshape(2, 16)
+    p2, o2 = _general(inp, a_log=torch.full((2,), np.log(2.0), dtype=torch.float64), dt_bias=d)
+    x = inp.a.double() + d[None]
+    a_eq = torch.log(torch.square(1.0 + torch.exp(x)) - 1.0)
+    ref = _pool64(inp.pool)
+    o_ref = oracle.step(ref, inp.slot_table, inp.q, inp.k, inp.v, a_eq, inp.b, accepted=inp.accepted)
+    np.testing.assert_allclose(o2, o_ref, rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(p2, ref, rtol=0, atol=2e-7)  # fp32 pool: at most an ulp of rounding apart
+
+
+def test_varlen_equals_each_request_alone():
+    lens = [3, 0, 1, 5, 2]
+    inp = workloads.make_general(n=5, t_lens=lens, num_cols=6, hv=2, k=16, v=16, num_slots=40,
+                                 state_dtype=torch.float16, seed=24, reset_p=0.4)
+    pool, o = _general(inp)
+    ref = _pool64(inp.pool)
+    cu = inp.cu_seqlens.long()
+    for r, tr in enumerate(lens):
+        if tr == 0:
+            continue
+        sl = slice(int(cu[r]), int(cu[r + 1]))
+        init = inp.slot_table[r:r + 1, int(inp.accepted[r]) - 1]
+        o_r = oracle.spec_verify(ref, init, inp.slot_table[r:r + 1, :tr], inp.q[sl][None], inp.k[sl][None],
+                                 inp.v[sl][None], inp.a[sl][None], inp.b[sl][None],
+                                 reset=None if inp.reset is None else inp.reset[r:r + 1])
+        assert np.array_equal(o[sl], o_r[0])
+    assert np.array_equal(pool, ref)
+
+
+def test_padding_request_touches_nothing():
+    inp = workloads.make_general(n=6, t=3, hv=2, k=16, v=16, num_slots=30, state_dtype=torch.float32,
+                                 seed=25, pad_p=0.5)
+    pad = (inp.slot_table < 0).all(dim=1)
+    assert 0 < int(pad.sum()) < 6
+    before = _pool64(inp.pool)
+    pool, o = _general(inp)
+    o = o.reshape(6, 3, 2, 16)
+    assert (o[pad.numpy()] == 0).all() and (o[~pad.numpy()] != 0).any()
+    # the padded requests' inputs do not matter
+    q2 = inp.q.clone().reshape(6, 3, 2, 16)
+    q2[pad] = 7.0
+    ref = _pool64(inp.pool)
+    o_ref = oracle.step(ref, inp.slot_table, q2.reshape(18, 2, 16), inp.k, inp.v, inp.a, inp.b,
+                        accepted=inp.accepted)
+    assert np.array_equal(pool, ref) and np.array_equal(o.reshape(18, 2, 16), o_ref)
+    # slots of padded rows are all -1, so nothing outside the real rows' slots changed
+    real = inp.slot_table[~pad].reshape(-1)
+    real = real[real >= 0].long().numpy()
+    untouched = np.setdiff1d(np.arange(30), real)
+    assert np.array_equal(pool[untouched], before[untouched])
+
+
+def test_dropped_snapshot_is_not_stored():
+    inp = workloads.make_general(n=4, t=4, hv=2, k=16, v=16, num_slots=24, state_dtype=torch.float16,
+                                 seed=26)
+    full_pool, full_o = _general(inp)
+    table = inp.slot_table.clone()
+    c0 = inp.accepted.long() - 1
+    # drop one snapshot column that is not the initial one, per request
+    drop_col = (c0 + 1) % 4
+    dropped = table[torch.arange(4), drop_col].clone()
+    table[torch.arange(4), drop_col] = -1
+    pool = _pool64(inp.pool)
+    o = oracle.step(pool, table, inp.q, inp.k, inp.v, inp.a, inp.b, accepted=inp.accepted)
+    assert np.array_equal(o, full_o)  # the recurrence does not depend on what is kept
+    before = _pool64(inp.pool)
+    for r in range(4):
+        s = int(dropped[r])
+        assert np.array_equal(pool[s], before[s])          # not stored
+        assert not np.array_equal(full_pool[s], before[s])  # the full run stored it
+    keep = np.setdiff1d(np.arange(24), dropped.numpy())
+    assert np.array_equal(pool[keep], full_pool[keep])
+
+
+@pytest.mark.parametrize("state_dtype", [torch.float32, torch.float16])
+def test_in_place_step_is_decode_on_the_accepted_slot(state_dtype):
+    inp = workloads.make_general(n=6, num_cols=3, hv=2, k=16, v=32, num_slots=30, state_dtype=state_dtype,
+                                 seed=27, in_place=True, reset_p=0.3)
+    pool, o = _general(inp)
+    ref = _pool64(inp.pool)
+    slots = inp.slot_table[torch.arange(6), inp.accepted.long() - 1]
+    o_ref = oracle.decode_step(ref, slots, inp.q, inp.k, inp.v, inp.a, inp.b, reset=inp.reset)
+    assert np.array_equal(pool, ref) and np.array_equal(o, o_ref)
+
+
+def test_general_layout_errors():
+    inp = workloads.make_general(n=2, t=2, num_cols=2, hv=2, k=16, v=16, num_slots=10,
+                                 state_dtype=torch.float32, seed=28)
+    with pytest.raises(ValueError):
+        _general(inp, accepted=torch.tensor([3, 1], dtype=torch.int32))   # column 2 of 2
+    with pytest.raises(ValueError):
+        _general(inp, accepted=torch.tensor([0, 1], dtype=torch.int32))   # column -1
+    bad = inp.slot_table.clone()
+    bad[0, 1] = 10
+    with pytest.raises(ValueError):
+        oracle.step(_pool64(inp.pool), bad, inp.q, inp.k, inp.v, inp.a, inp.b, accepted=inp.accepted)
