@@ -175,6 +175,68 @@ int kda_spec_verify(const kda_pool* pool, const int32_t* init_slot, const int32_
                     const float* b, float* o, int32_t* dev_status, uint32_t flags,
                     void* stream);
 
+/*
+ * Arguments of kda_step, the general step.  Pointers are device pointers
+ * unless noted; the optional ones may be NULL.
+ *
+ * Request r owns tokens cu_seqlens[r] .. cu_seqlens[r+1] - 1 of the packed
+ * inputs (T_r of them, 0 <= T_r <= max_t), or, with cu_seqlens NULL, tokens
+ * r * max_t .. r * max_t + max_t - 1.  Its row of slot_table holds num_cols
+ * slots: state_at(c, slot) of pull request 2945, Changes -- one address
+ * function for a request's initial state and for each token's snapshot.  The
+ * initial state is read from column accepted[r] - 1 (column 0 when accepted
+ * is NULL), so a step starts from the snapshot of the last token the previous
+ * step accepted; the state after token j is stored to column j.  A negative
+ * initial slot marks a padding request: nothing is read or stored and its
+ * output rows are zero.  A negative snapshot slot means that token's state is
+ * not kept (the recurrence still runs through it).
+ * in_place != 0 is decode: one token per request (cu_seqlens NULL, total == n,
+ * max_t == 1), the state stored back to the initial slot (the decode kernel).
+ *
+ * Heads: q and k have h_qk heads and value head h reads q/k head
+ * h / (hv / h_qk) (hv % h_qk == 0; h_qk == hv is one q/k per value head).
+ * Gate: alpha = exp(-softplus(a)) without a_log; with a_log,
+ * alpha = exp(-exp(a_log[h]) * softplus(a + dt_bias[h])) (dt_bias NULL: 0).
+ */
+typedef struct kda_step_args {
+    int32_t n;                  /* requests */
+    int32_t total;              /* packed tokens: rows of q, k, v, a, b, o */
+    int32_t max_t;              /* most tokens of any request; <= num_cols unless in_place */
+    int32_t h_qk;               /* q/k heads */
+    int32_t num_cols;           /* columns of slot_table (>= 1) */
+    int32_t in_place;           /* 0: speculative step; nonzero: decode in place */
+    int32_t qkv_dtype;          /* KDA_F32, KDA_F16 or KDA_BF16 */
+    int32_t reserved;           /* 0 */
+    const int32_t* cu_seqlens;  /* [n + 1] or NULL */
+    const int32_t* slot_table;  /* [n][num_cols] */
+    const int32_t* accepted;    /* [n], values 1 .. num_cols, or NULL */
+    const uint8_t* reset;       /* [n] or NULL: nonzero starts request r from a zero state */
+    const void* q;              /* [total][h_qk][k], 16-byte aligned */
+    const void* k;              /* [total][h_qk][k], 16-byte aligned */
+    const void* v;              /* [total][hv][v], 16-byte aligned */
+    const float* a;             /* [total][hv][k], 16-byte aligned */
+    const float* b;             /* [total][hv] */
+    const float* a_log;         /* [hv] or NULL */
+    const float* dt_bias;       /* [hv][k] or NULL */
+    float* o;                   /* [total][hv][v] (output) */
+} kda_step_args;
+
+/*
+ * The general step (accepted-length speculative decode, variable-length
+ * requests, padding, grouped heads, learned gate scale) on one pool; see
+ * kda_step_args.  args is a host pointer.  Host checks (before any launch):
+ * KDA_ERR_NULL, _DTYPE_*, _SHAPE (h_qk not dividing hv, num_cols < 1, max_t >
+ * num_cols, total inconsistent with n and max_t, in_place with cu_seqlens or
+ * max_t != 1), _ALIGN, _ARG (negative counts, reserved != 0, unknown flags).
+ * Device checks (in *dev_status, the tile skipped): KDA_ERR_ARG for an
+ * accepted column outside 1 .. num_cols or token offsets outside 0 .. max_t;
+ * KDA_ERR_SLOT_RANGE for a slot id >= num_slots.  KDA_LAUNCH_PDL_EARLY_STATE
+ * also lets the kernel read cu_seqlens, accepted and slot_table early.
+ * n == 0 or total == 0 is a no-op after the pool checks.
+ */
+int kda_step(const kda_pool* pool, const kda_step_args* args, int32_t* dev_status, uint32_t flags,
+             void* stream);
+
 /* A static, human-readable string for a kda_status code. */
 const char* kda_strerror(int32_t code);
 

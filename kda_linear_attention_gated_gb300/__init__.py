@@ -35,7 +35,7 @@ KDA_LAUNCH_PDL, KDA_LAUNCH_PDL_EARLY_STATE = 1, 2
  KDA_ERR_SLOT_RANGE, KDA_ERR_ARG, KDA_ERR_TIMEOUT) = range(11)
 
 EXPORTED_SYMBOLS = ("kda_build_state_dtype", "kda_pool_check", "kda_state_bytes",
-                    "kda_decode_step", "kda_spec_verify", "kda_strerror")
+                    "kda_decode_step", "kda_spec_verify", "kda_step", "kda_strerror")
 
 
 class KdaError(RuntimeError):
@@ -49,6 +49,18 @@ class PoolDesc(ctypes.Structure):
     _fields_ = [("base", ctypes.c_void_p), ("dtype", ctypes.c_int32), ("hv", ctypes.c_int32),
                 ("k", ctypes.c_int32), ("v", ctypes.c_int32), ("num_slots", ctypes.c_int64),
                 ("slot_stride", ctypes.c_int64)]
+
+
+class StepArgs(ctypes.Structure):
+    """Mirror of ``struct kda_step_args`` (include/kda.h)."""
+    _fields_ = [("n", ctypes.c_int32), ("total", ctypes.c_int32), ("max_t", ctypes.c_int32),
+                ("h_qk", ctypes.c_int32), ("num_cols", ctypes.c_int32), ("in_place", ctypes.c_int32),
+                ("qkv_dtype", ctypes.c_int32), ("reserved", ctypes.c_int32),
+                ("cu_seqlens", ctypes.c_void_p), ("slot_table", ctypes.c_void_p),
+                ("accepted", ctypes.c_void_p), ("reset", ctypes.c_void_p), ("q", ctypes.c_void_p),
+                ("k", ctypes.c_void_p), ("v", ctypes.c_void_p), ("a", ctypes.c_void_p),
+                ("b", ctypes.c_void_p), ("a_log", ctypes.c_void_p), ("dt_bias", ctypes.c_void_p),
+                ("o", ctypes.c_void_p)]
 
 
 def source_hash() -> str:
@@ -126,6 +138,8 @@ def _load(state16: bool) -> ctypes.CDLL:
         lib.kda_decode_step.argtypes = [P, vp, vp, i32, vp, vp, vp, i32, vp, vp, vp, vp, u32, vp]
         lib.kda_spec_verify.restype = ctypes.c_int
         lib.kda_spec_verify.argtypes = [P, vp, vp, vp, i32, i32, vp, vp, vp, i32, vp, vp, vp, vp, u32, vp]
+        lib.kda_step.restype = ctypes.c_int
+        lib.kda_step.argtypes = [P, ctypes.POINTER(StepArgs), vp, u32, vp]
         lib.kda_strerror.restype = ctypes.c_char_p
         lib.kda_strerror.argtypes = [i32]
         _libs[state16] = lib
@@ -228,3 +242,46 @@ class KdaLibrary:
             _ptr(q), _ptr(k), _ptr(v), _dtype_code(q.dtype), _ptr(a), _ptr(b), _ptr(o),
             _ptr(status), flags, self._stream(stream))
         self._check(rc, "kda_spec_verify")
+
+    def kda_step_raw(self, desc: PoolDesc, args: StepArgs, status, stream, flags=0) -> int:
+        return self.lib.kda_step(ctypes.byref(desc), ctypes.byref(args), status, flags, stream)
+
+    def kda_step(self, pool, slot_table, q, k, v, a, b, o, status, cu_seqlens=None, max_t=None,
+                 accepted=None, reset=None, a_log=None, dt_bias=None, in_place=False, stream=None,
+                 flags=0) -> None:
+        """The general step (see kda_step_args in include/kda.h): packed tokens
+        q, k [total, H, K], v [total, HV, V], a [total, HV, K], b [total, HV],
+        o [total, HV, V]; slot_table [N, C]; cu_seqlens [N + 1] (then max_t is
+        required) or None (every request has total / N tokens)."""
+        import torch
+        desc = pool_desc(pool)
+        hv, kd, vd = desc.hv, desc.k, desc.v
+        n, ncols = int(slot_table.shape[0]), int(slot_table.shape[1])
+        total, h_qk = int(q.shape[0]), int(q.shape[1])
+        qkv_types = (torch.float32, torch.float16, torch.bfloat16)
+        _expect("slot_table", slot_table, (n, ncols), (torch.int32,))
+        _expect("q", q, (total, h_qk, kd), qkv_types)
+        _expect("k", k, (total, h_qk, kd), (q.dtype,))
+        _expect("v", v, (total, hv, vd), (q.dtype,))
+        _expect("a", a, (total, hv, kd), (torch.float32,))
+        _expect("b", b, (total, hv), (torch.float32,))
+        _expect("o", o, (total, hv, vd), (torch.float32,))
+        _expect("status", status, (1,), (torch.int32,))
+        if cu_seqlens is not None:
+            _expect("cu_seqlens", cu_seqlens, (n + 1,), (torch.int32,))
+            if max_t is None:
+                raise ValueError("max_t is required with cu_seqlens")
+        elif max_t is None:
+            max_t = total // n if n else 0
+        if accepted is not None:
+            _expect("accepted", accepted, (n,), (torch.int32,))
+        if reset is not None:
+            _expect("reset", reset, (n,), (torch.uint8,))
+        if a_log is not None:
+            _expect("a_log", a_log, (hv,), (torch.float32,))
+        if dt_bias is not None:
+            _expect("dt_bias", dt_bias, (hv, kd), (torch.float32,))
+        args = StepArgs(n, total, int(max_t), h_qk, ncols, int(bool(in_place)), _dtype_code(q.dtype), 0,
+                        _ptr(cu_seqlens), _ptr(slot_table), _ptr(accepted), _ptr(reset), _ptr(q), _ptr(k),
+                        _ptr(v), _ptr(a), _ptr(b), _ptr(a_log), _ptr(dt_bias), _ptr(o))
+        self._check(self.kda_step_raw(desc, args, _ptr(status), self._stream(stream), flags), "kda_step")

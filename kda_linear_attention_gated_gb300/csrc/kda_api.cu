@@ -293,6 +293,17 @@ kda::StepParams make_params(const kda_pool* pool, const int32_t* init_slot,
     prm.status = dev_status;
     prm.inv_sqrt_k = 1.0f / sqrtf((float)pool->k);
     prm.flags = flags;
+    // plain decode / verify: one q/k head per value head, one slot per request
+    // row (init), t snapshot columns, no accepted column, no offsets, plain gate
+    prm.hqk = pool->hv;
+    prm.init_stride = 1;
+    prm.snap_stride = t;
+    prm.num_cols = 1;
+    prm.accepted = nullptr;
+    prm.cu = nullptr;
+    prm.a_log = nullptr;
+    prm.dt_bias = nullptr;
+    prm.mode = 0;
     return prm;
 }
 
@@ -353,6 +364,44 @@ int kda_spec_verify(const kda_pool* pool, const int32_t* init_slot, const int32_
     return launch<true>(pool, prm, qkv_dtype, static_cast<cudaStream_t>(stream));
 }
 
+int kda_step(const kda_pool* pool, const kda_step_args* args, int32_t* dev_status, uint32_t flags,
+             void* stream) {
+    if (args == nullptr) return KDA_ERR_NULL;
+    const kda_step_args& g = *args;
+    int rc = check_pool_for_build(pool);
+    if (rc != KDA_OK) return rc;
+    if (g.n < 0 || g.total < 0 || g.max_t < 0 || g.reserved != 0) return KDA_ERR_ARG;
+    if (flags & ~(uint32_t)(KDA_LAUNCH_PDL | KDA_LAUNCH_PDL_EARLY_STATE)) return KDA_ERR_ARG;
+    if (elem_size(g.qkv_dtype) == 0) return KDA_ERR_DTYPE_UNSUPPORTED;
+    if (g.h_qk < 1 || pool->hv % g.h_qk != 0 || g.num_cols < 1) return KDA_ERR_SHAPE;
+    if (g.in_place) {
+        if (g.cu_seqlens != nullptr || g.total != g.n || (g.n > 0 && g.max_t != 1)) return KDA_ERR_SHAPE;
+    } else {
+        if (g.max_t > g.num_cols) return KDA_ERR_SHAPE;
+        if (g.cu_seqlens == nullptr && (int64_t)g.total != (int64_t)g.n * g.max_t) return KDA_ERR_SHAPE;
+    }
+    if (g.n == 0 || g.total == 0 || g.max_t == 0) return KDA_OK;
+    if (!g.slot_table || !g.q || !g.k || !g.v || !g.a || !g.b || !g.o || !dev_status) return KDA_ERR_NULL;
+    if (!aligned(g.slot_table, 4) || !aligned(dev_status, 4) || !aligned(g.b, 4) || !aligned(g.o, 4) ||
+        !aligned(g.a, 16) || !aligned(g.q, 16) || !aligned(g.k, 16) || !aligned(g.v, 16) ||
+        (g.cu_seqlens && !aligned(g.cu_seqlens, 4)) || (g.accepted && !aligned(g.accepted, 4)) ||
+        (g.a_log && !aligned(g.a_log, 4)) || (g.dt_bias && !aligned(g.dt_bias, 4)))
+        return KDA_ERR_ALIGN;
+    kda::StepParams prm = make_params(pool, g.slot_table, g.in_place ? nullptr : g.slot_table, g.reset, g.n,
+                                      g.in_place ? 1 : g.max_t, g.q, g.k, g.v, g.a, g.b, g.o, dev_status, flags);
+    prm.hqk = g.h_qk;
+    prm.init_stride = g.num_cols;
+    prm.snap_stride = g.num_cols;
+    prm.num_cols = g.num_cols;
+    prm.accepted = g.accepted;
+    prm.cu = g.in_place ? nullptr : g.cu_seqlens;
+    prm.a_log = g.a_log;
+    prm.dt_bias = g.dt_bias;
+    prm.mode = kda::MODE_PADDING;
+    const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    return g.in_place ? launch<false>(pool, prm, g.qkv_dtype, st) : launch<true>(pool, prm, g.qkv_dtype, st);
+}
+
 const char* kda_strerror(int32_t code) {
     switch (code) {
         case KDA_OK: return "ok";
@@ -364,7 +413,7 @@ const char* kda_strerror(int32_t code) {
         case KDA_ERR_ALIGN: return "misaligned pointer or stride (pool, q, k, v, a 16-byte aligned; b, o, ids 4-byte)";
         case KDA_ERR_LAUNCH: return "CUDA kernel launch failed";
         case KDA_ERR_SLOT_RANGE: return "a slot id lies outside [0, num_slots); its tiles were skipped";
-        case KDA_ERR_ARG: return "bad argument";
+        case KDA_ERR_ARG: return "bad argument (on the device: an accepted column or token offsets out of range)";
         case KDA_ERR_TIMEOUT: return "a device-side pipeline wait ran out (1 s); the call's results are incomplete";
         default: return "unknown kda status code";
     }

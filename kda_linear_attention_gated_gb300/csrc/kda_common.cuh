@@ -16,6 +16,7 @@ constexpr float L2_EPS = 1e-6f;  // L2-norm epsilon: x / sqrt(sum x^2 + eps)
 constexpr int32_t STATUS_SLOT_RANGE = 8;   // KDA_ERR_SLOT_RANGE in kda.h
 constexpr int32_t STATUS_TIMEOUT = 10;     // KDA_ERR_TIMEOUT in kda.h
 constexpr int32_t STATUS_SMEM_ALIGN = 6;   // KDA_ERR_ALIGN in kda.h (shared-memory base)
+constexpr int32_t STATUS_ARG = 9;          // KDA_ERR_ARG in kda.h (bad accepted column or token offsets)
 constexpr uint64_t WAIT_LIMIT_NS = 1000000000ull;  // a pipeline wait gives up after 1 s
 
 struct StepParams {
@@ -36,7 +37,34 @@ struct StepParams {
     int32_t* status;
     float inv_sqrt_k;
     uint32_t flags;           // KDA_LAUNCH_* bits
+    // The general step; the values make_params sets reproduce plain decode and verify.
+    int hqk;                  // q/k heads: value head h reads q/k head h / (hv / hqk)
+    int init_stride;          // elements between two requests' rows of init_slot
+    int snap_stride;          // ... of snap_slot
+    int num_cols;             // columns of a slot-table row (bounds the accepted column)
+    const int32_t* accepted;  // [n] or nullptr: request n's initial slot is column accepted[n] - 1
+    const int32_t* cu;        // [n + 1] or nullptr: request n owns tokens cu[n] .. cu[n+1] - 1
+                              // (else n t .. n t + t - 1); t bounds cu[n+1] - cu[n]
+    const float* a_log;       // [hv] or nullptr: gate scale exp(a_log[h])
+    const float* dt_bias;     // [hv][k] or nullptr: gate bias
+    uint32_t mode;            // MODE_* bits
 };
+
+// A negative initial slot marks a padding request (nothing read or stored,
+// output rows zero); a negative snapshot slot marks a snapshot not kept.
+// Without this bit a negative slot is out of range.
+constexpr uint32_t MODE_PADDING = 1u;
+
+__device__ __forceinline__ float softplus_f(float x) {
+    return x > 0.f ? x + log1pf(expf(-x)) : log1pf(expf(x));
+}
+
+// The per-key-channel decay alpha_i of one row.  Plain gate: exp(-softplus(a))
+// = 1 / (1 + e^a) (one exponential, no logarithm).  Learned scale (the KDA
+// layer's A_log, dt_bias): exp(-exp(A_log) softplus(a + dt_bias)).
+__device__ __forceinline__ float gate_alpha(float a, bool scaled, float scale, float bias) {
+    return scaled ? expf(-scale * softplus_f(a + bias)) : __frcp_rn(1.0f + expf(a));
+}
 
 constexpr uint32_t LAUNCH_PDL = 1u;               // KDA_LAUNCH_PDL in kda.h
 constexpr uint32_t LAUNCH_PDL_EARLY_STATE = 2u;   // KDA_LAUNCH_PDL_EARLY_STATE in kda.h

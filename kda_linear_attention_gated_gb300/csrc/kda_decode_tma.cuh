@@ -26,9 +26,15 @@
 // bounded (1 s); a wait that runs out makes the whole CTA record
 // KDA_ERR_TIMEOUT, wait once more (bounded) for its copies, and exit.
 //
+// The request's slot is column accepted[n] - 1 (or 0) of its row of the slot
+// table (init_slot, init_stride); q and k may be shared by groups of value
+// heads (hqk heads); with MODE_PADDING a negative slot is a padding request
+// whose outputs are zeroed and whose state is left alone.
+//
 // Math per tile (ROCm/ATOM pull requests 2130 "What", 2945 "Summary"):
 //   khat = k / sqrt(|k|^2 + eps), qhat likewise; beta = 1 / (1 + e^-b)
-//   alpha_i = exp(-softplus(a_i)) = 1 / (1 + e^{a_i})
+//   alpha_i = exp(-softplus(a_i)) = 1 / (1 + e^{a_i}), or with the layer's
+//             learned scale exp(-exp(A_log_h) softplus(a_i + dt_bias_h,i))
 //   u_j = sum_i S_ij (alpha_i khat_i);  p_j = sum_i S_ij (alpha_i qhat_i)
 //   S'_ij = alpha_i S_ij + (beta khat_i) (v_j - u_j)
 //   o_j = (p_j + beta (qhat . khat)(v_j - u_j)) / sqrt(K)   (= sum_i S'_ij qhat_i / sqrt(K))
@@ -123,8 +129,14 @@ kda_decode_kernel(const __grid_constant__ CUtensorMap tmap, const StepParams p) 
     const bool early = (p.flags & LAUNCH_PDL_EARLY_STATE) != 0;
     if (!early) cudaGridDependencySynchronize();
 
-    const int32_t slot = p.init_slot[n];
-    const bool valid = slot >= 0 && slot < p.num_slots;
+    // The request's slot: column accepted[n] - 1 (or 0) of its row of the
+    // slot table; a negative slot is padding when the caller says so.
+    int col = 0;
+    if (p.accepted != nullptr) col = p.accepted[n] - 1;
+    const bool col_ok = col >= 0 && col < p.num_cols;
+    const int32_t slot = col_ok ? p.init_slot[(int64_t)n * p.init_stride + col] : -1;
+    const bool pad = col_ok && slot < 0 && (p.mode & MODE_PADDING) != 0;
+    const bool valid = col_ok && slot >= 0 && slot < p.num_slots;
     const bool rst = valid && p.reset != nullptr && p.reset[n] != 0;
     if (tid == 0) {
         mbar_init(bar_st, 1);
@@ -138,7 +150,11 @@ kda_decode_kernel(const __grid_constant__ CUtensorMap tmap, const StepParams p) 
     }
     if (early) cudaGridDependencySynchronize();
     if (!valid) {
-        if (tid == 0) atomicCAS(p.status, 0, STATUS_SLOT_RANGE);
+        if (pad) {  // padding: this tile's outputs are zero
+            if (tid < min(BV, p.v - cb * BV)) p.o[(int64_t)r * p.v + cb * BV + tid] = 0.f;
+        } else if (tid == 0) {
+            atomicCAS(p.status, 0, col_ok ? STATUS_SLOT_RANGE : STATUS_ARG);
+        }
         return;  // uniform over the CTA; nothing was issued
     }
     if (tid == 0) {
@@ -146,8 +162,9 @@ kda_decode_kernel(const __grid_constant__ CUtensorMap tmap, const StepParams p) 
         const uint32_t v_bytes = (uint32_t)min(BV, p.v - cb * BV) * qes;
         mbar_arrive_expect_tx(bar_in, 2 * qk_bytes + (uint32_t)p.k * 4 + v_bytes);
         const int64_t r64 = r;
-        bulk_load(in + SH::IN_Q, static_cast<const char*>(p.q) + r64 * qk_bytes, qk_bytes, bar_in);
-        bulk_load(in + SH::IN_K, static_cast<const char*>(p.kk) + r64 * qk_bytes, qk_bytes, bar_in);
+        const int64_t rqk = (int64_t)n * p.hqk + h / (p.hv / p.hqk);  // grouped q/k heads
+        bulk_load(in + SH::IN_Q, static_cast<const char*>(p.q) + rqk * qk_bytes, qk_bytes, bar_in);
+        bulk_load(in + SH::IN_K, static_cast<const char*>(p.kk) + rqk * qk_bytes, qk_bytes, bar_in);
         bulk_load(in + SH::IN_A, p.a + r64 * p.k, (uint32_t)p.k * 4, bar_in);
         bulk_load(in + SH::IN_V, static_cast<const char*>(p.vv) + (r64 * p.v + (int64_t)cb * BV) * qes,
                   v_bytes, bar_in);
@@ -165,7 +182,10 @@ kda_decode_kernel(const __grid_constant__ CUtensorMap tmap, const StepParams p) 
     if (ok && tid < p.k) {
         kt = to_f32(reinterpret_cast<const QT*>(in + SH::IN_K)[tid]);
         qt = to_f32(reinterpret_cast<const QT*>(in + SH::IN_Q)[tid]);
-        alpha = __frcp_rn(1.0f + expf(reinterpret_cast<const float*>(in + SH::IN_A)[tid]));  // exp(-softplus(a))
+        const bool scaled = p.a_log != nullptr;
+        alpha = gate_alpha(reinterpret_cast<const float*>(in + SH::IN_A)[tid], scaled,
+                           scaled ? expf(__ldg(p.a_log + h)) : 1.f,
+                           p.dt_bias != nullptr ? __ldg(p.dt_bias + (int64_t)h * p.k + tid) : 0.f);
     }
     float kk2 = warp_sum(kt * kt), qq2 = warp_sum(qt * qt), kq = warp_sum(kt * qt);
     if (lane == 0) {

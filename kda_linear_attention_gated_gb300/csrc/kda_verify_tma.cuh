@@ -13,6 +13,13 @@
 // reading back whole 16-byte row pieces and storing them coalesced (two
 // buffers in turn).
 //
+// The general step: request n owns tokens cu[n] .. cu[n+1] - 1 of packed
+// inputs (or n T .. n T + T - 1), reads its initial state from column
+// accepted[n] - 1 (or 0) of its row of the slot table and stores token j's
+// state to column j; value head h reads q/k head h / (hv / hqk); with
+// MODE_PADDING a negative initial slot is a padding request (outputs zero,
+// no state read or stored) and a negative snapshot slot is not kept.
+//
 // Tokens are taken in chunks of up to TC.  Within a chunk the recurrence
 //   S_t = D_t S_{t-1} + beta_t khat_t d_t^T,   D_t = diag(alpha_t),
 //   d_t = v_t - (D_t S_{t-1})^T khat_t,        o_t = S_t^T qhat_t / sqrt(K)
@@ -151,8 +158,9 @@ kda_verify_kernel(const __grid_constant__ CUtensorMap tmap, const StepParams p) 
     const int cb = tile - r * vt;
     const int n = r / p.hv;
     const int h = r - n * p.hv;
-    const int T = p.t;
+    const int T = p.t;  // most tokens a request may have
     const int qes = (int)sizeof(QT);
+    const int hq = h / (p.hv / p.hqk);  // q/k head of value head h
     const int vcols = min(BV, p.v - cb * BV);
     if ((tile_base & 1023u) != 0) {  // the swizzled tile needs a 1024-byte aligned base
         if (tid == 0) atomicCAS(p.status, 0, STATUS_SMEM_ALIGN);
@@ -161,6 +169,7 @@ kda_verify_kernel(const __grid_constant__ CUtensorMap tmap, const StepParams p) 
 
     const uint32_t qk_bytes = (uint32_t)p.k * qes;
     const uint32_t v_bytes = (uint32_t)vcols * qes;
+    int tb = n * T, Tn = T;  // request n's packed tokens tb .. tb + Tn - 1 (set below)
     // inputs of tokens t0 .. t0 + tc - 1 into the work area: lane 0 of warp 0
     // arms the barrier with the whole byte count, then warp 0 issues the 4 tc
     // copies (none of them depends on a slot id)
@@ -170,12 +179,13 @@ kda_verify_kernel(const __grid_constant__ CUtensorMap tmap, const StepParams p) 
         __syncwarp();
         for (int c = lane; c < 4 * tc; c += 32) {
             const int j = c >> 2, kind = c & 3;
-            const int64_t rt = ((int64_t)n * T + t0 + j) * p.hv + h;
+            const int64_t tok = (int64_t)tb + t0 + j;
+            const int64_t rt = tok * p.hv + h, rq = tok * p.hqk + hq;
             uint8_t* in = ins + j * SH::IN_TOK;
             if (kind == 0)
-                bulk_load(in + SH::IN_Q, static_cast<const char*>(p.q) + rt * qk_bytes, qk_bytes, bar_in);
+                bulk_load(in + SH::IN_Q, static_cast<const char*>(p.q) + rq * qk_bytes, qk_bytes, bar_in);
             else if (kind == 1)
-                bulk_load(in + SH::IN_K, static_cast<const char*>(p.kk) + rt * qk_bytes, qk_bytes, bar_in);
+                bulk_load(in + SH::IN_K, static_cast<const char*>(p.kk) + rq * qk_bytes, qk_bytes, bar_in);
             else if (kind == 2)
                 bulk_load(in + SH::IN_A, p.a + rt * p.k, (uint32_t)p.k * 4, bar_in);
             else
@@ -197,30 +207,46 @@ kda_verify_kernel(const __grid_constant__ CUtensorMap tmap, const StepParams p) 
         fence_mbar_init();
     }
     if (!early) cudaGridDependencySynchronize();
-    // the slot ids are requested first, the inputs while they are in flight
-    const int32_t slot = p.init_slot[n];
-    const int32_t snap0 = lane < T ? p.snap_slot[(int64_t)n * T + lane] : 0;
-    if (!early && warp == 0) issue_inputs(0, min(TC, T));
-    bool bad = slot < 0 || slot >= p.num_slots || snap0 < 0 || snap0 >= p.num_slots;
-    for (int t = lane + 32; t < T; t += 32) {
-        const int32_t s = p.snap_slot[(int64_t)n * T + t];
-        bad |= (s < 0 || s >= p.num_slots);
+    // The index metadata (token range, accepted column, slot ids) is requested
+    // first, the inputs while it is in flight.  Request n owns tokens
+    // tb .. tb + Tn - 1; its initial slot is column accepted[n] - 1 (or 0) of
+    // its row of init_slot, and token j's snapshot goes to column j of its row
+    // of snap_slot.
+    if (p.cu != nullptr) {
+        tb = p.cu[n];
+        Tn = p.cu[n + 1] - tb;
     }
+    const bool range_ok = tb >= 0 && Tn >= 0 && Tn <= T;
+    int col = 0;
+    if (p.accepted != nullptr) col = p.accepted[n] - 1;
+    const bool arg_ok = range_ok && col >= 0 && col < p.num_cols;
+    const int32_t slot = arg_ok ? p.init_slot[(int64_t)n * p.init_stride + col] : 0;
+    const int32_t snap0 = arg_ok && lane < Tn ? p.snap_slot[(int64_t)n * p.snap_stride + lane] : 0;
+    const bool issued = arg_ok && Tn > 0;  // the first chunk's inputs are requested
+    if (!early && warp == 0 && issued) issue_inputs(0, min(TC, Tn));
+    const bool padding = (p.mode & MODE_PADDING) != 0;
+    auto slot_bad = [&](int32_t s) { return s >= p.num_slots || (s < 0 && !padding); };
+    bool bad = !arg_ok || slot_bad(slot) || slot_bad(snap0);
+    for (int t = lane + 32; arg_ok && t < Tn; t += 32) bad |= slot_bad(p.snap_slot[(int64_t)n * p.snap_stride + t]);
     bad = __any_sync(0xffffffffu, bad);  // the same answer in every warp
+    const bool pad = !bad && slot < 0;     // a padding request
     const bool rst = !bad && p.reset != nullptr && p.reset[n] != 0;
-    if (tid == 0 && !bad && !rst) {
+    if (tid == 0 && !bad && !pad && !rst && Tn > 0) {
         prefetch_tmap(&tmap);
         mbar_arrive_expect_tx(bar_st, (uint32_t)p.k * SH::ROWBYTES);
         tma_load_3d(smem, &tmap, bar_st, cb * BV, h * p.k, slot);
     }
     if (early) {
         cudaGridDependencySynchronize();
-        if (warp == 0) issue_inputs(0, min(TC, T));
+        if (warp == 0 && issued) issue_inputs(0, min(TC, Tn));
     }
-    if (bad) {
+    if (bad || pad || Tn == 0) {
+        if (pad)  // padding: this tile's outputs of every token are zero
+            for (int e = tid; e < Tn * vcols; e += SH::NT)
+                p.o[((int64_t)(tb + e / vcols) * p.hv + h) * p.v + cb * BV + e % vcols] = 0.f;
         if (tid == 0) {
-            atomicCAS(p.status, 0, STATUS_SLOT_RANGE);
-            mbar_wait(bar_in, 0);  // bounded: the input copies land before the CTA exits
+            if (bad) atomicCAS(p.status, 0, arg_ok ? STATUS_SLOT_RANGE : STATUS_ARG);
+            if (issued) mbar_wait(bar_in, 0);  // bounded: the input copies land before the CTA exits
         }
         return;  // uniform; no state copy was issued
     }
@@ -230,12 +256,15 @@ kda_verify_kernel(const __grid_constant__ CUtensorMap tmap, const StepParams p) 
     bool state_in = false;
     bool alive = true;
     int in_phase = 0;
-    for (int t0 = 0; t0 < T; t0 += TC) {
-        const int tc = min(TC, T - t0);
+    const bool scaled = p.a_log != nullptr;
+    const float gscale = scaled ? expf(__ldg(p.a_log + h)) : 1.f;
+    const float gbias = p.dt_bias != nullptr && tid < p.k ? __ldg(p.dt_bias + (int64_t)h * p.k + tid) : 0.f;
+    for (int t0 = 0; t0 < Tn; t0 += TC) {
+        const int tc = min(TC, Tn - t0);
         if (t0 > 0 && warp == 0) issue_inputs(t0, tc);
         if (tid < tc) {
-            bsm[tid] = __ldg(p.b + ((int64_t)n * T + t0 + tid) * p.hv + h);
-            snaps[tid] = p.snap_slot[(int64_t)n * T + t0 + tid];
+            bsm[tid] = __ldg(p.b + ((int64_t)tb + t0 + tid) * p.hv + h);
+            snaps[tid] = p.snap_slot[(int64_t)n * p.snap_stride + t0 + tid];
         }
         const bool ok_in = mbar_wait(bar_in, in_phase);
         in_phase ^= 1;
@@ -251,7 +280,7 @@ kda_verify_kernel(const __grid_constant__ CUtensorMap tmap, const StepParams p) 
                 if (tid < p.k) {
                     kt[j] = to_f32(reinterpret_cast<const QT*>(in + SH::IN_K)[tid]);
                     qt[j] = to_f32(reinterpret_cast<const QT*>(in + SH::IN_Q)[tid]);
-                    at[j] = __frcp_rn(1.0f + expf(reinterpret_cast<const float*>(in + SH::IN_A)[tid]));
+                    at[j] = gate_alpha(reinterpret_cast<const float*>(in + SH::IN_A)[tid], scaled, gscale, gbias);
                 }
                 if (tid < vcols) vv[j] = to_f32(reinterpret_cast<const QT*>(in + SH::IN_V)[tid]);
             }
@@ -385,7 +414,7 @@ kda_verify_kernel(const __grid_constant__ CUtensorMap tmap, const StepParams p) 
                         float o = res[(t * 2 + 1) * BV + j];
 #pragma unroll
                         for (int s = 0; s <= t; ++s) o = fmaf(ab[idx_b(t, s)], d[s], o);
-                        p.o[(((int64_t)n * T + t0 + t) * p.hv + h) * p.v + cb * BV + j] = o * p.inv_sqrt_k;
+                        p.o[(((int64_t)tb + t0 + t) * p.hv + h) * p.v + cb * BV + j] = o * p.inv_sqrt_k;
                     }
                     dsm[t * BV + j] = d[t];
                 }
@@ -419,7 +448,7 @@ kda_verify_kernel(const __grid_constant__ CUtensorMap tmap, const StepParams p) 
             if constexpr (SH::TMA_STORE) {
                 fence_proxy_async_smem();
                 __syncthreads();
-                if (tid == 0) {
+                if (tid == 0 && snaps[j] >= 0) {  // a negative slot: this snapshot is not kept
                     tma_store_3d(&tmap, smem + b * SH::TILE_BYTES, cb * BV, h * p.k, snaps[j]);
                     bulk_commit();
                     // the stores of the last NSTAGE - 2 tokens may still read their
@@ -432,7 +461,7 @@ kda_verify_kernel(const __grid_constant__ CUtensorMap tmap, const StepParams p) 
                 // other buffer, which the next token writes.
                 __syncthreads();
                 ST* dst = static_cast<ST*>(p.pool) + state_at(p, snaps[j], h) + cb * BV;
-                for (int pc = tid; pc < p.k * NW; pc += SH::NT) {
+                for (int pc = tid; snaps[j] >= 0 && pc < p.k * NW; pc += SH::NT) {
                     const int row = pc / NW, ch = pc - row * NW;
                     if (ch * VEC < vcols)
                         __stcs(reinterpret_cast<uint4*>(dst + (int64_t)row * p.v + ch * VEC),

@@ -136,6 +136,43 @@ def test_step_refusals_before_any_launch(libs):
     assert call(**args(desc(), n=0, flags=kda.KDA_LAUNCH_PDL | kda.KDA_LAUNCH_PDL_EARLY_STATE)) == kda.KDA_OK
 
 
+def test_general_step_refusals_before_any_launch(libs):
+    """kda_step's host checks (include/kda.h, kda_step_args): every call below
+    is refused before a launch, so the fake pointers are never dereferenced."""
+    L32 = libs[torch.float32]
+    P = 0x7F0000100000
+
+    def args(**kw):
+        f = dict(n=4, total=32, max_t=8, h_qk=12, num_cols=8, in_place=0, qkv_dtype=kda.KDA_F32,
+                 reserved=0, cu_seqlens=None, slot_table=P, accepted=None, reset=None, q=P, k=P, v=P,
+                 a=P, b=P, a_log=None, dt_bias=None, o=P)
+        f.update(kw)
+        return kda.StepArgs(**f)
+
+    call = lambda a, d=None, status=P, flags=0: L32.kda_step_raw(d or desc(), a, status, None, flags)  # noqa
+    assert L32.lib.kda_step(ctypes.byref(desc()), None, P, 0, None) == kda.KDA_ERR_NULL
+    assert call(args(), d=desc(kda.KDA_F16)) == kda.KDA_ERR_DTYPE_MISMATCH
+    assert call(args(qkv_dtype=7)) == kda.KDA_ERR_DTYPE_UNSUPPORTED
+    assert call(args(h_qk=5)) == kda.KDA_ERR_SHAPE          # 12 % 5 != 0
+    assert call(args(h_qk=0)) == kda.KDA_ERR_SHAPE
+    assert call(args(num_cols=0)) == kda.KDA_ERR_SHAPE
+    assert call(args(max_t=9, total=36)) == kda.KDA_ERR_SHAPE  # more tokens than columns
+    assert call(args(total=31)) == kda.KDA_ERR_SHAPE         # not n * max_t without offsets
+    assert call(args(in_place=1, total=4, max_t=1, cu_seqlens=P)) == kda.KDA_ERR_SHAPE
+    assert call(args(in_place=1, total=5, max_t=1)) == kda.KDA_ERR_SHAPE
+    assert call(args(reserved=1)) == kda.KDA_ERR_ARG
+    assert call(args(n=-1)) == kda.KDA_ERR_ARG
+    assert call(args(), flags=8) == kda.KDA_ERR_ARG
+    assert call(args(slot_table=None)) == kda.KDA_ERR_NULL
+    assert call(args(), status=None) == kda.KDA_ERR_NULL
+    assert call(args(a=P + 4)) == kda.KDA_ERR_ALIGN
+    assert call(args(cu_seqlens=P + 2, total=20)) == kda.KDA_ERR_ALIGN
+    assert call(args(dt_bias=P + 1)) == kda.KDA_ERR_ALIGN
+    # nothing to do: succeeds without touching the GPU
+    assert call(args(n=0, total=0)) == kda.KDA_OK
+    assert call(args(total=0, cu_seqlens=P)) == kda.KDA_OK
+
+
 def test_strerror_covers_every_code(libs):
     L = libs[torch.float32]
     msgs = {c: L.kda_strerror(c) for c in range(11)}
