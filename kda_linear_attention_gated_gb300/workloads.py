@@ -219,3 +219,52 @@ def make_general(n=8, t_lens=None, t=8, num_cols=None, h_qk=None, hv=12, k=128, 
     return GeneralInputs(P, table, q, kk, vv, a, b, cu, acc, reset, a_log, dt_bias, in_place, max_t,
                          dict(kind="general", n=n, hv=hv, h_qk=h_qk, k=k, v=v, num_slots=num_slots,
                               seed=seed, lens=lens))
+
+
+@dataclass
+class ConvInputs:
+    """CPU tensors of one causal short-convolution step with its paged window."""
+    window: torch.Tensor               # [num_slots, L, C] fp32, fp16 or bf16
+    conv_slot: torch.Tensor            # int32 [N]
+    x: torch.Tensor                    # [total, C], the window's dtype
+    weight: torch.Tensor               # fp32 [C, KW]
+    bias: torch.Tensor | None = None   # fp32 [C]
+    cu_seqlens: torch.Tensor | None = None
+    accepted: torch.Tensor | None = None  # int32 [N], 1 .. L - KW + 2
+    reset: torch.Tensor | None = None
+    max_t: int = 0
+    meta: dict = field(default_factory=dict)
+
+    def to(self, device) -> "ConvInputs":
+        mv = lambda t: None if t is None else t.to(device)  # noqa: E731
+        return ConvInputs(mv(self.window), mv(self.conv_slot), mv(self.x), mv(self.weight), mv(self.bias),
+                          mv(self.cu_seqlens), mv(self.accepted), mv(self.reset), self.max_t, dict(self.meta))
+
+
+def make_conv(n=8, t=5, t_lens=None, channels=4608, kw=4, num_spec=4, num_slots=64, dtype=torch.bfloat16,
+              seed=5, accepted=True, reset_p=0.0, pad_p=0.0, bias=True) -> ConvInputs:
+    """The short convolution in front of the recurrence: window length
+    L = kw - 1 + num_spec (the conv pool's kernel - 1 + num_spec), qlen =
+    num_spec + 1 tokens per request (or t_lens), channels = 2 * 12 * 128 +
+    12 * 128 by default (q, k and v of one layer); window and x ~ N(0, 1) in
+    dtype, weight ~ N(0, 1 / kw), bias ~ N(0, 0.1^2); accepted[r] uniform in
+    1 .. num_spec + 1."""
+    g = torch.Generator().manual_seed(seed)
+    L = kw - 1 + num_spec
+    lens = [t] * n if t_lens is None else list(t_lens)
+    total = sum(lens)
+    W = _randn(g, (num_slots, L, channels), dtype)
+    slots = torch.randperm(num_slots, generator=g)[:n].to(torch.int32)
+    x = _randn(g, (total, channels), dtype)
+    w = _randn(g, (channels, kw), std=1.0 / kw ** 0.5)
+    b = _randn(g, (channels,), std=0.1) if bias else None
+    acc = (torch.randint(0, num_spec + 1, (n,), generator=g) + 1).to(torch.int32) if accepted else None
+    if pad_p > 0:
+        slots[torch.rand((n,), generator=g) < pad_p] = -1
+    reset = (torch.rand((n,), generator=g) < reset_p).to(torch.uint8) if reset_p > 0 else None
+    cu = None
+    if t_lens is not None:
+        cu = torch.zeros(n + 1, dtype=torch.int32)
+        cu[1:] = torch.cumsum(torch.tensor(lens, dtype=torch.int64), 0).to(torch.int32)
+    return ConvInputs(W, slots, x, w, b, cu, acc, reset, max(lens) if lens else 0,
+                      dict(kind="conv", n=n, kw=kw, L=L, channels=channels, seed=seed, lens=lens))

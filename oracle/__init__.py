@@ -84,6 +84,16 @@ def _load():
             lib.oracle_step.argtypes = common + [ctypes.c_int, i32p, ctypes.c_int, i32p, ctypes.c_int, i32p,
                                                  ctypes.c_int, u8p, dp, dp, dp, dp, dp, dp, dp, dp,
                                                  ctypes.c_int]
+            lib.oracle_bf16_to_f64.restype = ctypes.c_double
+            lib.oracle_bf16_to_f64.argtypes = [ctypes.c_uint16]
+            lib.oracle_f64_to_bf16_rne.restype = ctypes.c_uint16
+            lib.oracle_f64_to_bf16_rne.argtypes = [ctypes.c_double]
+            lib.oracle_f64_to_bf16_rne_array.argtypes = [dp, ctypes.POINTER(ctypes.c_uint16), ctypes.c_int64]
+            lib.oracle_conv_step.restype = ctypes.c_int
+            lib.oracle_conv_step.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_int,
+                                             ctypes.c_int, ctypes.c_int64, ctypes.c_int, i32p, ctypes.c_int,
+                                             i32p, i32p, u8p, ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
+                                             dp, dp, ctypes.c_void_p]
             _lib = lib
     return _lib
 
@@ -216,3 +226,50 @@ def step(pool: np.ndarray, slot_table, q, k, v, a, b, cu_seqlens=None, accepted=
     if rc != 0:
         raise ValueError(f"oracle_step failed ({rc}): " + ("slot id out of range" if rc == -1 else "layout"))
     return o
+
+
+def f64_to_bf16_rne(x) -> np.ndarray:
+    """Round fp64 values to bfloat16 (nearest, ties to even, one rounding); returns uint16 bits."""
+    x = _f64(x)
+    out = np.empty(x.shape, dtype=np.uint16)
+    _load().oracle_f64_to_bf16_rne_array(_ptr(x.reshape(-1), ctypes.c_double),
+                                         _ptr(out.reshape(-1), ctypes.c_uint16), x.size)
+    return out
+
+
+CONV_DTYPES = {"float32": 0, "float16": 1, "bfloat16": 2}
+
+
+def conv_step(window: np.ndarray, dtype: str, conv_slot, x: np.ndarray, weight, bias=None, cu_seqlens=None,
+              accepted=None, reset=None, silu=True) -> np.ndarray:
+    """The causal short convolution with its paged window (see oracle_conv_step).
+
+    window: [num_slots, L, C] as float32, or uint16 bit patterns for fp16/bf16
+    (``dtype`` names which); x: [total, C] of the same storage; weight fp64
+    [C, KW]; bias [C] or None.  Updates ``window`` in place and returns y with
+    x's storage type, [total, C]."""
+    code = CONV_DTYPES[dtype]
+    window = window if window.flags.c_contiguous else None
+    if window is None:
+        raise ValueError("window must be C-contiguous")
+    num_slots, L, C = window.shape
+    x = np.ascontiguousarray(x)
+    total = x.shape[0]
+    conv_slot = np.ascontiguousarray(np.asarray(conv_slot, dtype=np.int32))
+    n = conv_slot.shape[0]
+    w = _f64(weight)
+    kw = w.shape[1]
+    b = None if bias is None else _f64(bias)
+    cu = None if cu_seqlens is None else np.ascontiguousarray(np.asarray(cu_seqlens, dtype=np.int32))
+    acc = None if accepted is None else np.ascontiguousarray(np.asarray(accepted, dtype=np.int32))
+    rs = None if reset is None else np.ascontiguousarray(np.asarray(reset, dtype=np.uint8))
+    y = np.zeros_like(x)
+    opt = lambda a, t: None if a is None else _ptr(a, t)  # noqa: E731
+    rc = _load().oracle_conv_step(window.ctypes.data, code, num_slots, C, L, L * C, n,
+                                  opt(cu, ctypes.c_int32), 0 if cu is not None else (total // n if n else 0),
+                                  _ptr(conv_slot, ctypes.c_int32), opt(acc, ctypes.c_int32),
+                                  opt(rs, ctypes.c_uint8), kw, int(bool(silu)), x.ctypes.data,
+                                  _ptr(w, ctypes.c_double), opt(b, ctypes.c_double), y.ctypes.data)
+    if rc != 0:
+        raise ValueError(f"oracle_conv_step failed ({rc})")
+    return y

@@ -381,3 +381,137 @@ int oracle_step(void* base, int dtype, int64_t num_slots, int hv, int k, int v,
     (void)nthreads;
     return bad ? -2 : 0;
 }
+
+/* ------------------------------------------------------------------------ */
+/* bfloat16 (1 sign, 8 exponent bits with bias 127, 7 fraction bits): the    */
+/* fp32 exponent range with a 7-bit fraction.                                 */
+/* ------------------------------------------------------------------------ */
+
+double oracle_bf16_to_f64(uint16_t h)
+{
+    uint32_t bits = (uint32_t)h << 16;
+    float f;
+    memcpy(&f, &bits, sizeof f);  /* the bf16 value is the fp32 value with these top bits */
+    return (double)f;
+}
+
+/* fp64 -> bf16, to nearest, ties to even, in one rounding: the quantum of the
+ * binade is 2^(e - 7); below 2^-126 the quantum is the subnormal one, 2^-133. */
+uint16_t oracle_f64_to_bf16_rne(double x)
+{
+    uint16_t sign = signbit(x) ? 0x8000 : 0;
+    double ax = fabs(x);
+    if (isnan(x)) return (uint16_t)(sign | 0x7fc0);
+    /* the largest finite bf16 is (2 - 2^-7) 2^127; halfway to 2^128 rounds up */
+    if (ax >= ldexp(2.0 - ldexp(1.0, -8), 127)) return (uint16_t)(sign | 0x7f80);
+    double quantum;
+    if (ax < ldexp(1.0, -126)) {
+        quantum = ldexp(1.0, -133);
+    } else {
+        int e2;
+        frexp(ax, &e2);
+        quantum = ldexp(1.0, (e2 - 1) - 7);
+    }
+    double r = rint(ax / quantum) * quantum;
+    float f = (float)r;  /* exact: r has at most 8 significant bits inside the fp32 range */
+    uint32_t bits;
+    memcpy(&bits, &f, sizeof bits);
+    return (uint16_t)(sign | (uint16_t)(bits >> 16));
+}
+
+void oracle_f64_to_bf16_rne_array(const double* x, uint16_t* out, int64_t n)
+{
+    for (int64_t i = 0; i < n; ++i) out[i] = oracle_f64_to_bf16_rne(x[i]);
+}
+
+/*
+ * The causal short convolution in front of the recurrence, with its paged
+ * window (ATOM pull request 2894, review thread: the conv pool keeps the last
+ * kernel - 1 + num_spec inputs of a request; a step reads its kernel - 1
+ * history entries starting at the accepted index acc_idx, and writes back the
+ * kept old entries followed by the step's inputs).
+ *
+ * Window of slot s: W[s][e][c], e = 0 .. L-1 oldest first, c < C channels
+ * (channel innermost).  Request r: tokens cu[r] .. cu[r+1]-1 (or r*t_uniform ..),
+ * window slot conv_slot[r] (negative: padding, nothing read or stored, output
+ * rows zero), acc = accepted ? accepted[r] - 1 : 0.
+ *   history h_i = W[acc + i], i < KW - 1 (zero when reset[r]);
+ *   z = h ++ x;  y_t[c] = act(bias[c] + sum_{i<KW} w[c][i] z[t + i])
+ *   (w[c][KW-1] weighs the newest input; act = SiLU x sigmoid(x), or none);
+ *   with m = acc + KW - 1 valid entries and kept = max(0, L - T) old ones,
+ *   the new window is W[m - kept .. m - 1] (zero when reset) followed by the
+ *   last min(T, L) inputs.  T = 0 leaves the window alone.
+ * x, y and the window share dtype (0 fp32, 1 fp16, 2 bf16); y is rounded to it.
+ * Returns 0; -1 slot >= num_slots; -3 layout (m > L, m < kept, acc < 0).
+ */
+static double conv_load(int dtype, const void* p, int64_t i)
+{
+    if (dtype == 0) return (double)((const float*)p)[i];
+    uint16_t h = ((const uint16_t*)p)[i];
+    return dtype == 1 ? oracle_f16_to_f64(h) : oracle_bf16_to_f64(h);
+}
+
+static void conv_store(int dtype, void* p, int64_t i, double v)
+{
+    if (dtype == 0) ((float*)p)[i] = (float)v;
+    else ((uint16_t*)p)[i] = dtype == 1 ? oracle_f64_to_f16_rne(v) : oracle_f64_to_bf16_rne(v);
+}
+
+int oracle_conv_step(void* wbase, int dtype, int64_t num_slots, int C, int L, int64_t slot_stride,
+                     int n_req, const int32_t* cu, int t_uniform, const int32_t* conv_slot,
+                     const int32_t* accepted, const uint8_t* reset, int KW, int silu,
+                     const void* x, const double* w, const double* bias, void* y)
+{
+    for (int r = 0; r < n_req; ++r) {
+        int64_t T = cu ? (int64_t)cu[r + 1] - cu[r] : t_uniform;
+        int acc = accepted ? accepted[r] - 1 : 0;
+        if (conv_slot[r] >= num_slots) return -1;
+        if (conv_slot[r] < 0 || T == 0) continue;
+        int m = acc + KW - 1;
+        int64_t kept = L - T > 0 ? L - T : 0;
+        if (acc < 0 || m > L || m < kept || T < 0) return -3;
+    }
+    double* old = (double*)malloc(sizeof(double) * (size_t)(L > 0 ? L : 1));
+    double* z = (double*)malloc(sizeof(double) * (size_t)(KW + 1));
+    if (!old || !z) { free(old); free(z); return -2; }
+    for (int r = 0; r < n_req; ++r) {
+        int64_t t0 = cu ? cu[r] : (int64_t)r * t_uniform;
+        int64_t T = cu ? (int64_t)cu[r + 1] - cu[r] : t_uniform;
+        int32_t s = conv_slot[r];
+        if (s < 0) {
+            for (int64_t t = 0; t < T; ++t)
+                for (int c = 0; c < C; ++c) conv_store(dtype, y, (t0 + t) * C + c, 0.0);
+            continue;
+        }
+        if (T == 0) continue;
+        int acc = accepted ? accepted[r] - 1 : 0;
+        int m = acc + KW - 1;
+        int64_t kept = L - T > 0 ? L - T : 0;
+        int rst = reset && reset[r];
+        int64_t wofs = (int64_t)s * slot_stride;
+        for (int c = 0; c < C; ++c) {
+            /* history and kept entries, read before anything is written */
+            for (int i = 0; i < KW - 1; ++i)
+                z[i] = rst ? 0.0 : conv_load(dtype, wbase, wofs + (int64_t)(acc + i) * C + c);
+            for (int64_t e = 0; e < kept; ++e)
+                old[e] = rst ? 0.0 : conv_load(dtype, wbase, wofs + (m - kept + e) * C + c);
+            for (int64_t t = 0; t < T; ++t) {
+                z[KW - 1] = conv_load(dtype, x, (t0 + t) * C + c);
+                double s_ = bias ? bias[c] : 0.0;
+                for (int i = 0; i < KW; ++i) s_ += w[(int64_t)c * KW + i] * z[i];
+                double out = silu ? s_ / (1.0 + exp(-s_)) : s_;
+                conv_store(dtype, y, (t0 + t) * C + c, out);
+                for (int i = 0; i < KW - 1; ++i) z[i] = z[i + 1];
+            }
+            for (int64_t e = 0; e < kept; ++e)
+                conv_store(dtype, wbase, wofs + e * C + c, old[e]);
+            int64_t nin = T < L ? T : L;
+            for (int64_t e = 0; e < nin; ++e)
+                conv_store(dtype, wbase, wofs + (kept + e) * C + c,
+                           conv_load(dtype, x, (t0 + T - nin + e) * C + c));
+        }
+    }
+    free(old);
+    free(z);
+    return 0;
+}
