@@ -237,6 +237,72 @@ typedef struct kda_step_args {
 int kda_step(const kda_pool* pool, const kda_step_args* args, int32_t* dev_status, uint32_t flags,
              void* stream);
 
+/*
+ * The causal short convolution in front of the recurrence, with its paged
+ * window (pull request 2894, review thread on the conv window: the conv pool
+ * keeps kernel - 1 + num_spec inputs per request; a step reads its kernel - 1
+ * history entries at the accepted index and writes back the kept old entries
+ * followed by its inputs).  One window per slot: [state_len][channels] of
+ * `dtype`, oldest entry first, channel innermost:
+ *   entry e, channel c of slot s = base + s * slot_stride + e * channels + c.
+ */
+typedef struct kda_conv_window {
+    void* base;           /* device */
+    int32_t dtype;        /* KDA_F32, KDA_F16 or KDA_BF16: also the dtype of x and y */
+    int32_t channels;     /* C >= 1 */
+    int32_t state_len;    /* L: kernel_width - 1 .. 32 */
+    int32_t reserved;     /* 0 */
+    int64_t num_slots;
+    int64_t slot_stride;  /* elements from one slot to the next, >= state_len * channels */
+} kda_conv_window;
+
+/*
+ * Arguments of kda_conv_step (device pointers unless noted; optional ones may
+ * be NULL).  Request r owns tokens cu_seqlens[r] .. cu_seqlens[r+1] - 1 of x
+ * and y (or r * max_t .. with cu_seqlens NULL; T_r <= max_t) and the window
+ * of slot conv_slot[r] (negative: a padding request, nothing read or stored,
+ * its y rows zero).  With acc = accepted[r] - 1 (0 when accepted is NULL),
+ * m = acc + kernel_width - 1 and kept = max(0, state_len - T_r):
+ *   history h_i = W[acc + i], i < kernel_width - 1 (zeros when reset[r]);
+ *   y_t = act(bias + sum_i weight[i] z[t + i]) with z = h ++ x (weight[kernel_width - 1]
+ *   weighs x_t); act = SiLU (x sigmoid(x)) when activation == 1, none when 0;
+ *   the window becomes W[m - kept .. m - 1] (zeros when reset[r]) followed by
+ *   the last min(T_r, state_len) inputs.  T_r == 0 leaves the window alone.
+ * Arithmetic is fp32; y is rounded to nearest even; the window keeps exact
+ * copies of x.  Device checks (in *dev_status, that request skipped):
+ * KDA_ERR_ARG unless 0 <= acc, m <= state_len and kept <= m, and for offsets
+ * outside 0 .. max_t; KDA_ERR_SLOT_RANGE for conv_slot[r] >= num_slots.
+ */
+typedef struct kda_conv_args {
+    int32_t n;                  /* requests */
+    int32_t total;              /* packed tokens: rows of x and y */
+    int32_t max_t;              /* most tokens of any request */
+    int32_t kernel_width;       /* 1 .. 8 */
+    int32_t activation;         /* 0 none, 1 SiLU */
+    int32_t reserved;           /* 0 */
+    const int32_t* cu_seqlens;  /* [n + 1] or NULL */
+    const int32_t* conv_slot;   /* [n] */
+    const int32_t* accepted;    /* [n] or NULL */
+    const uint8_t* reset;       /* [n] or NULL */
+    const void* x;              /* [total][channels] of the window's dtype */
+    const float* weight;        /* [channels][kernel_width] */
+    const float* bias;          /* [channels] or NULL */
+    void* y;                    /* [total][channels] of the window's dtype (output) */
+} kda_conv_args;
+
+/*
+ * One step of the short convolution (see kda_conv_args); win and args are host
+ * pointers.  Host checks: KDA_ERR_NULL, _DTYPE_UNSUPPORTED (window dtype),
+ * _SHAPE (channels < 1, kernel_width outside 1..8, state_len outside
+ * kernel_width - 1 .. 32, slot_stride too small, total inconsistent with n and
+ * max_t), _ALIGN (x, y, base to their element size; ids, weight, bias 4-byte),
+ * _ARG (negative counts, activation not 0/1, reserved fields, unknown flags).
+ * Works in either library build (the window dtype is independent of the pool's).
+ * n == 0 or total == 0 is a no-op.
+ */
+int kda_conv_step(const kda_conv_window* win, const kda_conv_args* args, int32_t* dev_status,
+                  uint32_t flags, void* stream);
+
 /* A static, human-readable string for a kda_status code. */
 const char* kda_strerror(int32_t code);
 

@@ -35,7 +35,7 @@ KDA_LAUNCH_PDL, KDA_LAUNCH_PDL_EARLY_STATE = 1, 2
  KDA_ERR_SLOT_RANGE, KDA_ERR_ARG, KDA_ERR_TIMEOUT) = range(11)
 
 EXPORTED_SYMBOLS = ("kda_build_state_dtype", "kda_pool_check", "kda_state_bytes",
-                    "kda_decode_step", "kda_spec_verify", "kda_step", "kda_strerror")
+                    "kda_decode_step", "kda_spec_verify", "kda_step", "kda_conv_step", "kda_strerror")
 
 
 class KdaError(RuntimeError):
@@ -61,6 +61,22 @@ class StepArgs(ctypes.Structure):
                 ("k", ctypes.c_void_p), ("v", ctypes.c_void_p), ("a", ctypes.c_void_p),
                 ("b", ctypes.c_void_p), ("a_log", ctypes.c_void_p), ("dt_bias", ctypes.c_void_p),
                 ("o", ctypes.c_void_p)]
+
+
+class ConvWindowDesc(ctypes.Structure):
+    """Mirror of ``struct kda_conv_window`` (include/kda.h)."""
+    _fields_ = [("base", ctypes.c_void_p), ("dtype", ctypes.c_int32), ("channels", ctypes.c_int32),
+                ("state_len", ctypes.c_int32), ("reserved", ctypes.c_int32), ("num_slots", ctypes.c_int64),
+                ("slot_stride", ctypes.c_int64)]
+
+
+class ConvArgs(ctypes.Structure):
+    """Mirror of ``struct kda_conv_args`` (include/kda.h)."""
+    _fields_ = [("n", ctypes.c_int32), ("total", ctypes.c_int32), ("max_t", ctypes.c_int32),
+                ("kernel_width", ctypes.c_int32), ("activation", ctypes.c_int32), ("reserved", ctypes.c_int32),
+                ("cu_seqlens", ctypes.c_void_p), ("conv_slot", ctypes.c_void_p), ("accepted", ctypes.c_void_p),
+                ("reset", ctypes.c_void_p), ("x", ctypes.c_void_p), ("weight", ctypes.c_void_p),
+                ("bias", ctypes.c_void_p), ("y", ctypes.c_void_p)]
 
 
 def source_hash() -> str:
@@ -140,6 +156,8 @@ def _load(state16: bool) -> ctypes.CDLL:
         lib.kda_spec_verify.argtypes = [P, vp, vp, vp, i32, i32, vp, vp, vp, i32, vp, vp, vp, vp, u32, vp]
         lib.kda_step.restype = ctypes.c_int
         lib.kda_step.argtypes = [P, ctypes.POINTER(StepArgs), vp, u32, vp]
+        lib.kda_conv_step.restype = ctypes.c_int
+        lib.kda_conv_step.argtypes = [ctypes.POINTER(ConvWindowDesc), ctypes.POINTER(ConvArgs), vp, u32, vp]
         lib.kda_strerror.restype = ctypes.c_char_p
         lib.kda_strerror.argtypes = [i32]
         _libs[state16] = lib
@@ -285,3 +303,38 @@ class KdaLibrary:
                         _ptr(cu_seqlens), _ptr(slot_table), _ptr(accepted), _ptr(reset), _ptr(q), _ptr(k),
                         _ptr(v), _ptr(a), _ptr(b), _ptr(a_log), _ptr(dt_bias), _ptr(o))
         self._check(self.kda_step_raw(desc, args, _ptr(status), self._stream(stream), flags), "kda_step")
+
+    def kda_conv_step_raw(self, win: ConvWindowDesc, args: ConvArgs, status, stream, flags=0) -> int:
+        return self.lib.kda_conv_step(ctypes.byref(win), ctypes.byref(args), status, flags, stream)
+
+    def kda_conv_step(self, window, conv_slot, x, weight, y, status, bias=None, cu_seqlens=None, max_t=None,
+                      accepted=None, reset=None, silu=True, stream=None, flags=0) -> None:
+        """The short convolution with its paged window (see kda_conv_args in
+        include/kda.h): window [num_slots, L, C] (C innermost), x and y
+        [total, C] of the window's dtype, weight fp32 [C, KW], bias [C]."""
+        import torch
+        if window.dim() != 3 or window.stride(2) != 1 or window.stride(1) != window.shape[2]:
+            raise ValueError("a conv window pool is a [num_slots, L, C] tensor, dense in [L, C]")
+        ns, L, C = window.shape
+        n, total, kw = int(conv_slot.shape[0]), int(x.shape[0]), int(weight.shape[1])
+        _expect("conv_slot", conv_slot, (n,), (torch.int32,))
+        _expect("x", x, (total, C), (window.dtype,))
+        _expect("y", y, (total, C), (window.dtype,))
+        _expect("weight", weight, (C, kw), (torch.float32,))
+        _expect("status", status, (1,), (torch.int32,))
+        if bias is not None:
+            _expect("bias", bias, (C,), (torch.float32,))
+        if cu_seqlens is not None:
+            _expect("cu_seqlens", cu_seqlens, (n + 1,), (torch.int32,))
+            if max_t is None:
+                raise ValueError("max_t is required with cu_seqlens")
+        elif max_t is None:
+            max_t = total // n if n else 0
+        if accepted is not None:
+            _expect("accepted", accepted, (n,), (torch.int32,))
+        if reset is not None:
+            _expect("reset", reset, (n,), (torch.uint8,))
+        win = ConvWindowDesc(window.data_ptr(), _dtype_code(window.dtype), C, L, 0, ns, window.stride(0))
+        args = ConvArgs(n, total, int(max_t), kw, int(bool(silu)), 0, _ptr(cu_seqlens), _ptr(conv_slot),
+                        _ptr(accepted), _ptr(reset), _ptr(x), _ptr(weight), _ptr(bias), _ptr(y))
+        self._check(self.kda_conv_step_raw(win, args, _ptr(status), self._stream(stream), flags), "kda_conv_step")

@@ -21,6 +21,7 @@
 #include "kda.h"
 #include "kda_decode_tma.cuh"
 #include "kda_verify_tma.cuh"
+#include "kda_conv.cuh"
 
 #ifndef KDA_STATE16
 #error "build with -DKDA_STATE16=0 (fp32 pool) or -DKDA_STATE16=1 (fp16 pool)"
@@ -304,6 +305,7 @@ kda::StepParams make_params(const kda_pool* pool, const int32_t* init_slot,
     prm.a_log = nullptr;
     prm.dt_bias = nullptr;
     prm.mode = 0;
+    prm.total = n * t;
     return prm;
 }
 
@@ -395,11 +397,71 @@ int kda_step(const kda_pool* pool, const kda_step_args* args, int32_t* dev_statu
     prm.num_cols = g.num_cols;
     prm.accepted = g.accepted;
     prm.cu = g.in_place ? nullptr : g.cu_seqlens;
+    prm.total = g.total;
     prm.a_log = g.a_log;
     prm.dt_bias = g.dt_bias;
     prm.mode = kda::MODE_PADDING;
     const cudaStream_t st = static_cast<cudaStream_t>(stream);
     return g.in_place ? launch<false>(pool, prm, g.qkv_dtype, st) : launch<true>(pool, prm, g.qkv_dtype, st);
+}
+
+int kda_conv_step(const kda_conv_window* win, const kda_conv_args* args, int32_t* dev_status,
+                  uint32_t flags, void* stream) {
+    if (win == nullptr || args == nullptr) return KDA_ERR_NULL;
+    const kda_conv_args& g = *args;
+    const int es = elem_size(win->dtype);
+    if (es == 0) return KDA_ERR_DTYPE_UNSUPPORTED;
+    if (win->reserved != 0 || g.reserved != 0 || g.n < 0 || g.total < 0 || g.max_t < 0 ||
+        (g.activation != 0 && g.activation != 1))
+        return KDA_ERR_ARG;
+    if (flags & ~(uint32_t)(KDA_LAUNCH_PDL | KDA_LAUNCH_PDL_EARLY_STATE)) return KDA_ERR_ARG;
+    if (win->channels < 1 || g.kernel_width < 1 || g.kernel_width > kda::CONV_KW_MAX ||
+        win->state_len < g.kernel_width - 1 || win->state_len > kda::CONV_L_MAX || win->num_slots < 1 ||
+        win->slot_stride < (int64_t)win->state_len * win->channels)
+        return KDA_ERR_SHAPE;
+    if (g.cu_seqlens == nullptr && (int64_t)g.total != (int64_t)g.n * g.max_t) return KDA_ERR_SHAPE;
+    if (g.n == 0 || g.total == 0 || g.max_t == 0) return KDA_OK;
+    if (!win->base || !g.conv_slot || !g.x || !g.weight || !g.y || !dev_status) return KDA_ERR_NULL;
+    if (!aligned(win->base, es) || !aligned(g.x, es) || !aligned(g.y, es) || !aligned(g.conv_slot, 4) ||
+        !aligned(g.weight, 4) || !aligned(dev_status, 4) || (g.bias && !aligned(g.bias, 4)) ||
+        (g.cu_seqlens && !aligned(g.cu_seqlens, 4)) || (g.accepted && !aligned(g.accepted, 4)))
+        return KDA_ERR_ALIGN;
+    const int64_t cblocks = (win->channels + kda::CONV_THREADS - 1) / kda::CONV_THREADS;
+    if (cblocks * g.n > 0x7fffffffLL) return KDA_ERR_SHAPE;
+    kda::ConvParams prm;
+    prm.window = win->base;
+    prm.num_slots = win->num_slots;
+    prm.slot_stride = win->slot_stride;
+    prm.C = win->channels;
+    prm.L = win->state_len;
+    prm.KW = g.kernel_width;
+    prm.n = g.n;
+    prm.t = g.max_t;
+    prm.total = g.total;
+    prm.cu = g.cu_seqlens;
+    prm.conv_slot = g.conv_slot;
+    prm.accepted = g.accepted;
+    prm.reset = g.reset;
+    prm.x = g.x;
+    prm.w = g.weight;
+    prm.bias = g.bias;
+    prm.y = g.y;
+    prm.silu = g.activation;
+    prm.status = dev_status;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(cblocks * g.n), 1, 1);
+    cfg.blockDim = dim3(kda::CONV_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = static_cast<cudaStream_t>(stream);
+    cudaLaunchAttribute attr;
+    set_pdl(cfg, &attr, flags);
+    cudaError_t err;
+    switch (win->dtype) {
+        case KDA_F32: err = cudaLaunchKernelEx(&cfg, kda::kda_conv_kernel<float>, prm); break;
+        case KDA_F16: err = cudaLaunchKernelEx(&cfg, kda::kda_conv_kernel<__half>, prm); break;
+        default: err = cudaLaunchKernelEx(&cfg, kda::kda_conv_kernel<__nv_bfloat16>, prm); break;
+    }
+    return err == cudaSuccess ? KDA_OK : KDA_ERR_LAUNCH;
 }
 
 const char* kda_strerror(int32_t code) {

@@ -48,6 +48,7 @@ struct StepParams {
     const float* a_log;       // [hv] or nullptr: gate scale exp(a_log[h])
     const float* dt_bias;     // [hv][k] or nullptr: gate bias
     uint32_t mode;            // MODE_* bits
+    int total;                // rows of the packed token arrays (bounds cu)
 };
 
 // A negative initial slot marks a padding request (nothing read or stored,

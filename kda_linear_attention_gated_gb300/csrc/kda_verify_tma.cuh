@@ -216,7 +216,7 @@ kda_verify_kernel(const __grid_constant__ CUtensorMap tmap, const StepParams p) 
         tb = p.cu[n];
         Tn = p.cu[n + 1] - tb;
     }
-    const bool range_ok = tb >= 0 && Tn >= 0 && Tn <= T;
+    const bool range_ok = tb >= 0 && Tn >= 0 && Tn <= T && (int64_t)tb + Tn <= p.total;
     int col = 0;
     if (p.accepted != nullptr) col = p.accepted[n] - 1;
     const bool arg_ok = range_ok && col >= 0 && col < p.num_cols;

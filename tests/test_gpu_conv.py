@@ -1,0 +1,115 @@
+"""GPU parity of the short convolution with its paged window (kda_conv_step)
+against the fp64 oracle.
+
+y: fp32 within max-abs 1e-5; fp16 / bf16 within one step of the oracle's
+value rounded once from fp64 (the GPU rounds from its fp32 sum).  The window
+holds copies of inputs and old entries, so it must match bit for bit, and
+windows of slots no request uses must not change.
+"""
+import numpy as np
+import pytest
+import torch
+
+import kda_linear_attention_gated_gb300 as kda
+from kda_linear_attention_gated_gb300 import workloads
+
+import oracle
+from _harness import lib_for
+
+pytestmark = [pytest.mark.gpu, pytest.mark.usefixtures("built_libs", "oracle_mod")]
+
+DT = [torch.float32, torch.float16, torch.bfloat16]
+
+
+def storage(t):
+    name = str(t.dtype).split(".")[1]
+    if t.dtype == torch.float32:
+        return t.numpy().copy(), name
+    return t.contiguous().view(torch.int16).numpy().view(np.uint16).copy(), name
+
+
+def gpu_conv(inp, silu=True, flags=0):
+    d = inp.to("cuda")
+    y = torch.full_like(d.x, float("nan"))
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    lib_for(torch.float32).kda_conv_step(d.window, d.conv_slot, d.x, d.weight, y, status, bias=d.bias,
+                                         cu_seqlens=d.cu_seqlens, max_t=inp.max_t, accepted=d.accepted,
+                                         reset=d.reset, silu=silu, flags=flags)
+    torch.cuda.synchronize()
+    return d.window.cpu(), y.cpu(), int(status.item())
+
+
+def oracle_conv(inp, silu=True):
+    W, name = storage(inp.window)
+    x, _ = storage(inp.x)
+    y = oracle.conv_step(W, name, inp.conv_slot.numpy(), x, inp.weight, inp.bias,
+                         cu_seqlens=None if inp.cu_seqlens is None else inp.cu_seqlens.numpy(),
+                         accepted=None if inp.accepted is None else inp.accepted.numpy(),
+                         reset=None if inp.reset is None else inp.reset.numpy(), silu=silu)
+    return W, y
+
+
+def compare(inp, silu=True, flags=0):
+    gw, gy, st = gpu_conv(inp, silu, flags)
+    rw, ry = oracle_conv(inp, silu)
+    assert st == 0, lib_for(torch.float32).kda_strerror(st)
+    gws, _ = storage(gw)
+    assert np.array_equal(gws, rw), "window differs"
+    gys, _ = storage(gy)
+    if inp.x.dtype == torch.float32:
+        assert np.isfinite(gys).all()
+        assert np.abs(gys.astype(np.float64) - ry.astype(np.float64)).max() <= 1e-5
+    else:
+        assert np.abs(gys.astype(np.int32) - ry.astype(np.int32)).max() <= 1, "y more than one step off"
+
+
+@pytest.mark.parametrize("dtype", DT)
+def test_conv_layer_shape(dtype):
+    """8 requests x 5 tokens (4 drafts), 4608 channels (q, k and v of one layer),
+    kernel 4, window 7, accepted index per request, resets and padding."""
+    compare(workloads.make_conv(n=8, t=5, dtype=dtype, seed=60, reset_p=0.25, pad_p=0.2))
+
+
+@pytest.mark.parametrize("dtype", DT)
+def test_conv_variable_lengths(dtype):
+    inp = workloads.make_conv(n=5, t_lens=[5, 0, 3, 5, 1], channels=300, dtype=dtype, seed=61)
+    inp.accepted[:] = 5  # the whole window is history: every token count is valid
+    compare(inp)
+
+
+@pytest.mark.parametrize("kw", [1, 2, 3, 4, 8])
+def test_conv_kernel_widths_and_no_activation(kw):
+    inp = workloads.make_conv(n=4, t=3, channels=200, kw=kw, num_spec=2, dtype=torch.float32, seed=62 + kw)
+    compare(inp, silu=(kw % 2 == 0))
+
+
+def test_conv_decode_rolling_window_chain():
+    """Plain decode (qlen 1, window kernel - 1) over 6 calls equals conv1d over
+    the 6 tokens from a zero start."""
+    n, C, kw = 3, 64, 4
+    g = torch.Generator().manual_seed(63)
+    W = torch.zeros(4, kw - 1, C, device="cuda")
+    w = torch.randn(C, kw, generator=g)
+    xs = torch.randn(6, n, C, generator=g)
+    slots = torch.tensor([2, 0, 3], dtype=torch.int32, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    lib = lib_for(torch.float32)
+    ys = []
+    for t in range(6):
+        y = torch.empty(n, C, device="cuda")
+        lib.kda_conv_step(W, slots, xs[t].cuda(), w.cuda(), y, status, silu=False)
+        ys.append(y.cpu())
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    ref = torch.nn.functional.conv1d(torch.nn.functional.pad(xs.permute(1, 2, 0).double(), (kw - 1, 0)),
+                                     w.double()[:, None, :], groups=C).permute(2, 0, 1)
+    assert (torch.stack(ys).double() - ref).abs().max() <= 1e-5
+
+
+def test_conv_bad_accepted_index_sets_status():
+    inp = workloads.make_conv(n=3, t=5, channels=64, dtype=torch.float32, seed=64)
+    inp.accepted[1] = 6  # history would run past the 7-entry window
+    gw, gy, st = gpu_conv(inp)
+    assert st == kda.KDA_ERR_ARG
+    s = int(inp.conv_slot[1])
+    assert torch.equal(gw[s], inp.window[s])  # that request was skipped

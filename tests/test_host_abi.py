@@ -173,6 +173,41 @@ def test_general_step_refusals_before_any_launch(libs):
     assert call(args(total=0, cu_seqlens=P)) == kda.KDA_OK
 
 
+def test_conv_step_refusals_before_any_launch(libs):
+    """kda_conv_step's host checks (include/kda.h, kda_conv_args)."""
+    L = libs[torch.float16]  # the conv window's dtype is independent of the pool build
+    P = 0x7F0000100000
+
+    def win(**kw):
+        f = dict(base=P, dtype=kda.KDA_BF16, channels=4608, state_len=7, reserved=0, num_slots=64,
+                 slot_stride=7 * 4608)
+        f.update(kw)
+        return kda.ConvWindowDesc(**f)
+
+    def args(**kw):
+        f = dict(n=8, total=40, max_t=5, kernel_width=4, activation=1, reserved=0, cu_seqlens=None,
+                 conv_slot=P, accepted=None, reset=None, x=P, weight=P, bias=None, y=P)
+        f.update(kw)
+        return kda.ConvArgs(**f)
+
+    call = lambda w, a, status=P, flags=0: L.kda_conv_step_raw(w, a, status, None, flags)  # noqa: E731
+    assert L.lib.kda_conv_step(None, ctypes.byref(args()), P, 0, None) == kda.KDA_ERR_NULL
+    assert call(win(dtype=7), args()) == kda.KDA_ERR_DTYPE_UNSUPPORTED
+    assert call(win(channels=0), args()) == kda.KDA_ERR_SHAPE
+    assert call(win(), args(kernel_width=9)) == kda.KDA_ERR_SHAPE
+    assert call(win(state_len=2), args()) == kda.KDA_ERR_SHAPE      # fewer than kernel - 1 entries
+    assert call(win(state_len=33, slot_stride=33 * 4608), args()) == kda.KDA_ERR_SHAPE
+    assert call(win(slot_stride=7 * 4608 - 1), args()) == kda.KDA_ERR_SHAPE
+    assert call(win(), args(total=39)) == kda.KDA_ERR_SHAPE
+    assert call(win(), args(activation=2)) == kda.KDA_ERR_ARG
+    assert call(win(reserved=1), args()) == kda.KDA_ERR_ARG
+    assert call(win(), args(), flags=16) == kda.KDA_ERR_ARG
+    assert call(win(), args(conv_slot=None)) == kda.KDA_ERR_NULL
+    assert call(win(), args(x=P + 1)) == kda.KDA_ERR_ALIGN
+    assert call(win(), args(weight=P + 2)) == kda.KDA_ERR_ALIGN
+    assert call(win(), args(n=0, total=0)) == kda.KDA_OK
+
+
 def test_strerror_covers_every_code(libs):
     L = libs[torch.float32]
     msgs = {c: L.kda_strerror(c) for c in range(11)}
