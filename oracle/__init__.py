@@ -94,6 +94,10 @@ def _load():
                                              ctypes.c_int, ctypes.c_int64, ctypes.c_int, i32p, ctypes.c_int,
                                              i32p, i32p, u8p, ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
                                              dp, dp, ctypes.c_void_p]
+            lib.oracle_ckpt_transfer.restype = ctypes.c_int
+            lib.oracle_ckpt_transfer.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p,
+                                                 ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int,
+                                                 ctypes.c_int, i32p, i32p, ctypes.c_int]
             _lib = lib
     return _lib
 
@@ -273,3 +277,22 @@ def conv_step(window: np.ndarray, dtype: str, conv_slot, x: np.ndarray, weight, 
     if rc != 0:
         raise ValueError(f"oracle_conv_step failed ({rc})")
     return y
+
+
+def ckpt_transfer(pool: np.ndarray, plane: np.ndarray, slots, entries, load: bool) -> None:
+    """Checkpoint flush (load=False: plane[entries] <- pool[slots]) or load
+    (pool[slots] <- plane[entries]) of whole slot states; negative indices
+    skip.  pool [num_slots, HV, K, V] and plane [num_entries, HV, K, V] share
+    an element type (float32, or uint16 fp16 bits)."""
+    if pool.dtype != plane.dtype or pool.shape[1:] != plane.shape[1:]:
+        raise ValueError("pool and plane differ in element type or state shape")
+    if not (pool.flags.c_contiguous and plane.flags.c_contiguous):
+        raise ValueError("pool and plane must be C-contiguous")
+    slots = np.ascontiguousarray(np.asarray(slots, dtype=np.int32))
+    entries = np.ascontiguousarray(np.asarray(entries, dtype=np.int32))
+    state = int(np.prod(pool.shape[1:]))
+    rc = _load().oracle_ckpt_transfer(pool.ctypes.data, pool.shape[0], state, plane.ctypes.data, plane.shape[0],
+                                      state, state, pool.itemsize, slots.shape[0], _ptr(slots, ctypes.c_int32),
+                                      _ptr(entries, ctypes.c_int32), int(bool(load)))
+    if rc != 0:
+        raise ValueError("oracle_ckpt_transfer: index out of range")

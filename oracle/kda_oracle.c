@@ -515,3 +515,31 @@ int oracle_conv_step(void* wbase, int dtype, int64_t num_slots, int C, int L, in
     free(z);
     return 0;
 }
+
+/*
+ * Checkpoint flush and load through the address function (ATOM pull request
+ * 2945, Changes: under ReplaySSM the checkpoint load and the flush go through
+ * state_at; pull request 2130, What: the checkpoint plane shapes and layout id
+ * derive from the state dtype).  A plane holds entries of one slot's state
+ * ([HV][K][V], the pool's element type).  flush: plane[entry[i]] <- pool[slot[i]];
+ * load: pool[slot[i]] <- plane[entry[i]].  A negative slot or entry skips i.
+ * Element copies only: nothing is converted.  Returns 0, or -1 for an index
+ * past its buffer.
+ */
+int oracle_ckpt_transfer(void* pool_base, int64_t num_slots, int64_t slot_stride,
+                         void* plane_base, int64_t num_entries, int64_t entry_stride,
+                         int64_t state_elems, int elem_bytes, int n, const int32_t* slot,
+                         const int32_t* entry, int load)
+{
+    for (int i = 0; i < n; ++i) {
+        if (slot[i] >= num_slots || entry[i] >= num_entries) return -1;
+    }
+    for (int i = 0; i < n; ++i) {
+        if (slot[i] < 0 || entry[i] < 0) continue;
+        char* p = (char*)pool_base + (int64_t)slot[i] * slot_stride * elem_bytes;
+        char* c = (char*)plane_base + (int64_t)entry[i] * entry_stride * elem_bytes;
+        if (load) memcpy(p, c, (size_t)(state_elems * elem_bytes));
+        else memcpy(c, p, (size_t)(state_elems * elem_bytes));
+    }
+    return 0;
+}
