@@ -412,6 +412,7 @@ def main():
         extra["verify"] = bench_verify(kda, workloads, torch, args, l2, peak)
         for sd_name, sd in (("fp32", torch.float32), ("fp16", torch.float16)):
             extra[f"sweep_69_layers_n128_{sd_name}"] = bench_sweep(kda, workloads, torch, sd, 128, peak)
+        extra["ckpt_flush_fp32_n64"] = bench_ckpt(kda, workloads, torch, peak)
 
     traffic = None
     tpath = os.path.join(REPO, "profiles", "decode_f32_n64_traffic.json")
@@ -508,6 +509,47 @@ def bench_sweep(kda, workloads, torch, state_dtype, n, peak, layers=69, replays=
             "us_per_forward": round(us_fwd, 2), "us_per_layer": round(us_fwd / layers, 3),
             "gbs": round(byt / (us_fwd * 1e-6) / 1e9, 1),
             "frac_of_peak": round(byt / (us_fwd * 1e-6) / 1e9 / peak, 4), "bytes_per_forward": byt}
+
+
+def bench_ckpt(kda, workloads, torch, peak, replays=200):
+    """Checkpoint flush of 64 fp32 states (12 x 128 x 128) from a 256-slot pool
+    to a 128-entry plane; 24 pool/plane pairs rotate (4.8 GB, far past L2)."""
+    lib = kda.KdaLibrary(torch.float32)
+    g = torch.Generator().manual_seed(9)
+    R = 24
+    pools = [workloads.make_pool(g, 256, HV, K, V, torch.float32).to("cuda") for _ in range(R)]
+    planes = [torch.empty(128, HV, K, V, device="cuda") for _ in range(R)]
+    slots = torch.randperm(256, generator=g)[:64].to(torch.int32).to("cuda")
+    entries = torch.randperm(128, generator=g)[:64].to(torch.int32).to("cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    stream = torch.cuda.Stream()
+    g_ = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        lib.kda_ckpt_flush(pools[0], planes[0], slots, entries, status)
+        stream.synchronize()
+        with torch.cuda.graph(g_, stream=stream):
+            for i in range(R):
+                lib.kda_ckpt_flush(pools[i], planes[i], slots, entries, status)
+        for _ in range(3):
+            g_.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    reps = max(1, replays // R)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(reps):
+            g_.replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item())}")
+    us = e0.elapsed_time(e1) * 1e3 / (reps * R)
+    byt = 2 * 64 * HV * K * V * 4
+    del pools, planes
+    torch.cuda.empty_cache()
+    return {"workload": "checkpoint flush, 64 fp32 states [12,128,128], 256-slot pool -> 128-entry plane",
+            "us_per_call": round(us, 3), "gbs": round(byt / (us * 1e-6) / 1e9, 1),
+            "frac_of_peak": round(byt / (us * 1e-6) / 1e9 / peak, 4), "bytes_per_call": byt}
 
 
 def bench_verify(kda, workloads, torch, args, l2, peak):

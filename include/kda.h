@@ -67,7 +67,8 @@ typedef enum kda_status {
     KDA_ERR_LAUNCH = 7,            /* the CUDA launch itself failed */
     KDA_ERR_SLOT_RANGE = 8,        /* device: a slot id outside [0, num_slots); its tiles were skipped */
     KDA_ERR_ARG = 9,               /* any other bad argument (negative counts, n_layers < 1) */
-    KDA_ERR_TIMEOUT = 10           /* device: a pipeline wait gave up after 1 s; results incomplete */
+    KDA_ERR_TIMEOUT = 10,          /* device: a pipeline wait gave up after 1 s; results incomplete */
+    KDA_ERR_LAYOUT = 11            /* a checkpoint plane written under another state layout (dtype or shape) */
 } kda_status;
 
 /*
@@ -302,6 +303,46 @@ typedef struct kda_conv_args {
  */
 int kda_conv_step(const kda_conv_window* win, const kda_conv_args* args, int32_t* dev_status,
                   uint32_t flags, void* stream);
+
+/*
+ * Checkpoint planes (ReplaySSM in pull request 2945, Changes: the checkpoint
+ * load and the flush go through state_at; pull request 2130, What: the plane
+ * shapes and the checkpoint layout id derive from the state dtype, so a build
+ * that flips the dtype cannot read another's checkpoint images).
+ *
+ * kda_layout_id: the layout id of `pool`'s states, a 32-bit FNV-1a digest of
+ * the five int32 values (1, dtype, hv, k, v); two pools share it exactly when
+ * their states are interchangeable byte for byte.  0 for a NULL pool.
+ */
+uint32_t kda_layout_id(const kda_pool* pool);
+
+/*
+ * A plane of checkpoint entries, each one slot's state in the pool's layout:
+ * entry e = base + e * entry_stride elements.  layout_id is the
+ * kda_layout_id of the pool the plane serves (it travels with the image).
+ */
+typedef struct kda_ckpt_plane {
+    void* base;            /* device, 16-byte aligned */
+    uint32_t layout_id;
+    int32_t reserved;      /* 0 */
+    int64_t num_entries;
+    int64_t entry_stride;  /* elements, >= hv * k * v, a multiple of 16 bytes */
+} kda_ckpt_plane;
+
+/*
+ * kda_ckpt_flush: plane entry entries[i] <- pool slot slots[i];
+ * kda_ckpt_load:  pool slot slots[i] <- plane entry entries[i]; i < n.
+ * Whole states, bit for bit (no conversion).  A negative slot or entry skips
+ * that pair; one past its buffer sets KDA_ERR_SLOT_RANGE in *dev_status and
+ * skips it.  Host checks: KDA_ERR_NULL, the pool checks of kda_decode_step,
+ * KDA_ERR_LAYOUT when plane->layout_id != kda_layout_id(pool), KDA_ERR_SHAPE
+ * for a short entry_stride, KDA_ERR_ALIGN, KDA_ERR_ARG (n < 0, reserved,
+ * flags).  slots and entries: device int32 [n].  n == 0 is a no-op.
+ */
+int kda_ckpt_flush(const kda_pool* pool, const kda_ckpt_plane* plane, const int32_t* slots,
+                   const int32_t* entries, int32_t n, int32_t* dev_status, uint32_t flags, void* stream);
+int kda_ckpt_load(const kda_pool* pool, const kda_ckpt_plane* plane, const int32_t* slots,
+                  const int32_t* entries, int32_t n, int32_t* dev_status, uint32_t flags, void* stream);
 
 /* A static, human-readable string for a kda_status code. */
 const char* kda_strerror(int32_t code);

@@ -25,17 +25,18 @@ __all__ = ["KdaError", "KdaLibrary", "PoolDesc", "build", "lib_path",
            "KDA_F32", "KDA_F16", "KDA_BF16", "KDA_OK", "KDA_ERR_NULL",
            "KDA_ERR_DTYPE_MISMATCH", "KDA_ERR_DTYPE_UNSUPPORTED", "KDA_ERR_LAYERS_DISAGREE",
            "KDA_ERR_SHAPE", "KDA_ERR_ALIGN", "KDA_ERR_LAUNCH", "KDA_ERR_SLOT_RANGE",
-           "KDA_ERR_ARG", "KDA_ERR_TIMEOUT", "KDA_LAUNCH_PDL", "KDA_LAUNCH_PDL_EARLY_STATE",
+           "KDA_ERR_ARG", "KDA_ERR_TIMEOUT", "KDA_ERR_LAYOUT", "KDA_LAUNCH_PDL", "KDA_LAUNCH_PDL_EARLY_STATE",
            "EXPORTED_SYMBOLS"]
 
 KDA_F32, KDA_F16, KDA_BF16 = 0, 1, 2
 KDA_LAUNCH_PDL, KDA_LAUNCH_PDL_EARLY_STATE = 1, 2
 (KDA_OK, KDA_ERR_NULL, KDA_ERR_DTYPE_MISMATCH, KDA_ERR_DTYPE_UNSUPPORTED,
  KDA_ERR_LAYERS_DISAGREE, KDA_ERR_SHAPE, KDA_ERR_ALIGN, KDA_ERR_LAUNCH,
- KDA_ERR_SLOT_RANGE, KDA_ERR_ARG, KDA_ERR_TIMEOUT) = range(11)
+ KDA_ERR_SLOT_RANGE, KDA_ERR_ARG, KDA_ERR_TIMEOUT, KDA_ERR_LAYOUT) = range(12)
 
 EXPORTED_SYMBOLS = ("kda_build_state_dtype", "kda_pool_check", "kda_state_bytes",
-                    "kda_decode_step", "kda_spec_verify", "kda_step", "kda_conv_step", "kda_strerror")
+                    "kda_decode_step", "kda_spec_verify", "kda_step", "kda_conv_step",
+                    "kda_layout_id", "kda_ckpt_flush", "kda_ckpt_load", "kda_strerror")
 
 
 class KdaError(RuntimeError):
@@ -77,6 +78,12 @@ class ConvArgs(ctypes.Structure):
                 ("cu_seqlens", ctypes.c_void_p), ("conv_slot", ctypes.c_void_p), ("accepted", ctypes.c_void_p),
                 ("reset", ctypes.c_void_p), ("x", ctypes.c_void_p), ("weight", ctypes.c_void_p),
                 ("bias", ctypes.c_void_p), ("y", ctypes.c_void_p)]
+
+
+class CkptPlaneDesc(ctypes.Structure):
+    """Mirror of ``struct kda_ckpt_plane`` (include/kda.h)."""
+    _fields_ = [("base", ctypes.c_void_p), ("layout_id", ctypes.c_uint32), ("reserved", ctypes.c_int32),
+                ("num_entries", ctypes.c_int64), ("entry_stride", ctypes.c_int64)]
 
 
 def source_hash() -> str:
@@ -158,6 +165,11 @@ def _load(state16: bool) -> ctypes.CDLL:
         lib.kda_step.argtypes = [P, ctypes.POINTER(StepArgs), vp, u32, vp]
         lib.kda_conv_step.restype = ctypes.c_int
         lib.kda_conv_step.argtypes = [ctypes.POINTER(ConvWindowDesc), ctypes.POINTER(ConvArgs), vp, u32, vp]
+        lib.kda_layout_id.restype = ctypes.c_uint32
+        lib.kda_layout_id.argtypes = [P]
+        for fn in (lib.kda_ckpt_flush, lib.kda_ckpt_load):
+            fn.restype = ctypes.c_int
+            fn.argtypes = [P, ctypes.POINTER(CkptPlaneDesc), vp, vp, i32, vp, u32, vp]
         lib.kda_strerror.restype = ctypes.c_char_p
         lib.kda_strerror.argtypes = [i32]
         _libs[state16] = lib
@@ -338,3 +350,37 @@ class KdaLibrary:
         args = ConvArgs(n, total, int(max_t), kw, int(bool(silu)), 0, _ptr(cu_seqlens), _ptr(conv_slot),
                         _ptr(accepted), _ptr(reset), _ptr(x), _ptr(weight), _ptr(bias), _ptr(y))
         self._check(self.kda_conv_step_raw(win, args, _ptr(status), self._stream(stream), flags), "kda_conv_step")
+
+    def kda_layout_id(self, pool) -> int:
+        desc = pool if isinstance(pool, PoolDesc) else pool_desc(pool)
+        return int(self.lib.kda_layout_id(ctypes.byref(desc)))
+
+    def plane_desc(self, plane, pool, layout_id=None) -> CkptPlaneDesc:
+        """Descriptor of a [num_entries, hv, k, v] checkpoint plane serving ``pool``."""
+        if plane.dim() != 4 or tuple(plane.shape[1:]) != tuple(pool.shape[1:]) or plane.dtype != pool.dtype:
+            raise ValueError("a checkpoint plane is [num_entries, hv, k, v] of the pool's dtype")
+        if not plane[0].is_contiguous():
+            raise ValueError("each plane entry must be dense")
+        lid = self.kda_layout_id(pool) if layout_id is None else layout_id
+        return CkptPlaneDesc(plane.data_ptr(), lid, 0, plane.shape[0], plane.stride(0))
+
+    def _ckpt(self, fn, name, pool, plane, slots, entries, status, layout_id, stream, flags):
+        import torch
+        n = int(slots.shape[0])
+        _expect("slots", slots, (n,), (torch.int32,))
+        _expect("entries", entries, (n,), (torch.int32,))
+        _expect("status", status, (1,), (torch.int32,))
+        desc, pdesc = pool_desc(pool), self.plane_desc(plane, pool, layout_id)
+        self._check(fn(ctypes.byref(desc), ctypes.byref(pdesc), _ptr(slots), _ptr(entries), n, _ptr(status),
+                       flags, self._stream(stream)), name)
+
+    def kda_ckpt_flush(self, pool, plane, slots, entries, status, layout_id=None, stream=None, flags=0) -> None:
+        """plane[entries[i]] <- pool[slots[i]] (whole states, bit for bit)."""
+        self._ckpt(self.lib.kda_ckpt_flush, "kda_ckpt_flush", pool, plane, slots, entries, status, layout_id,
+                   stream, flags)
+
+    def kda_ckpt_load(self, pool, plane, slots, entries, status, layout_id=None, stream=None, flags=0) -> None:
+        """pool[slots[i]] <- plane[entries[i]] (whole states, bit for bit)."""
+        self._ckpt(self.lib.kda_ckpt_load, "kda_ckpt_load", pool, plane, slots, entries, status, layout_id,
+                   stream, flags)
+

@@ -22,6 +22,7 @@
 #include "kda_decode_tma.cuh"
 #include "kda_verify_tma.cuh"
 #include "kda_conv.cuh"
+#include "kda_ckpt.cuh"
 
 #ifndef KDA_STATE16
 #error "build with -DKDA_STATE16=0 (fp32 pool) or -DKDA_STATE16=1 (fp16 pool)"
@@ -464,6 +465,77 @@ int kda_conv_step(const kda_conv_window* win, const kda_conv_args* args, int32_t
     return err == cudaSuccess ? KDA_OK : KDA_ERR_LAUNCH;
 }
 
+uint32_t kda_layout_id(const kda_pool* pool) {
+    if (pool == nullptr) return 0u;
+    const int32_t words[5] = {1, pool->dtype, pool->hv, pool->k, pool->v};
+    uint32_t h = 2166136261u;  // FNV-1a, 32-bit
+    for (int32_t w : words)
+        for (int b = 0; b < 4; ++b) {
+            h ^= (uint32_t)((uint32_t)w >> (8 * b)) & 0xffu;
+            h *= 16777619u;
+        }
+    return h;
+}
+
+}  // extern "C"
+
+namespace {
+
+int ckpt_transfer(const kda_pool* pool, const kda_ckpt_plane* plane, const int32_t* slots,
+                  const int32_t* entries, int32_t n, int32_t* dev_status, uint32_t flags, void* stream,
+                  int load) {
+    int rc = check_pool_for_build(pool);
+    if (rc != KDA_OK) return rc;
+    if (plane == nullptr) return KDA_ERR_NULL;
+    if (n < 0 || plane->reserved != 0) return KDA_ERR_ARG;
+    if (flags & ~(uint32_t)(KDA_LAUNCH_PDL | KDA_LAUNCH_PDL_EARLY_STATE)) return KDA_ERR_ARG;
+    if (plane->layout_id != kda_layout_id(pool)) return KDA_ERR_LAYOUT;
+    const int es = elem_size(pool->dtype);
+    const int64_t state = (int64_t)pool->hv * pool->k * pool->v;
+    if (plane->num_entries < 1 || plane->entry_stride < state) return KDA_ERR_SHAPE;
+    if (n == 0) return KDA_OK;
+    if (!plane->base || !slots || !entries || !dev_status) return KDA_ERR_NULL;
+    if (!aligned(plane->base, 16) || (plane->entry_stride * es) % 16 != 0 || !aligned(slots, 4) ||
+        !aligned(entries, 4) || !aligned(dev_status, 4))
+        return KDA_ERR_ALIGN;
+    kda::CkptParams prm;
+    prm.pool = static_cast<char*>(pool->base);
+    prm.num_slots = pool->num_slots;
+    prm.slot_bytes = pool->slot_stride * es;
+    prm.plane = static_cast<char*>(plane->base);
+    prm.num_entries = plane->num_entries;
+    prm.entry_bytes = plane->entry_stride * es;
+    prm.state_bytes = state * es;
+    prm.n = n;
+    prm.slots = slots;
+    prm.entries = entries;
+    prm.load = load;
+    prm.status = dev_status;
+    const int64_t pieces = (prm.state_bytes + kda::CKPT_PIECE - 1) / kda::CKPT_PIECE;
+    if (pieces * n > 0x7fffffffLL) return KDA_ERR_SHAPE;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(pieces * n), 1, 1);
+    cfg.blockDim = dim3(kda::CKPT_THREADS, 1, 1);
+    cfg.stream = static_cast<cudaStream_t>(stream);
+    cudaLaunchAttribute attr;
+    set_pdl(cfg, &attr, flags);
+    return cudaLaunchKernelEx(&cfg, kda::kda_ckpt_kernel, prm) == cudaSuccess ? KDA_OK : KDA_ERR_LAUNCH;
+}
+
+}  // namespace
+
+extern "C" {
+
+int kda_ckpt_flush(const kda_pool* pool, const kda_ckpt_plane* plane, const int32_t* slots,
+                   const int32_t* entries, int32_t n, int32_t* dev_status, uint32_t flags, void* stream) {
+    return ckpt_transfer(pool, plane, slots, entries, n, dev_status, flags, stream, 0);
+}
+
+int kda_ckpt_load(const kda_pool* pool, const kda_ckpt_plane* plane, const int32_t* slots,
+                  const int32_t* entries, int32_t n, int32_t* dev_status, uint32_t flags, void* stream) {
+    return ckpt_transfer(pool, plane, slots, entries, n, dev_status, flags, stream, 1);
+}
+
 const char* kda_strerror(int32_t code) {
     switch (code) {
         case KDA_OK: return "ok";
@@ -477,6 +549,7 @@ const char* kda_strerror(int32_t code) {
         case KDA_ERR_SLOT_RANGE: return "a slot id lies outside [0, num_slots); its tiles were skipped";
         case KDA_ERR_ARG: return "bad argument (on the device: an accepted column or token offsets out of range)";
         case KDA_ERR_TIMEOUT: return "a device-side pipeline wait ran out (1 s); the call's results are incomplete";
+        case KDA_ERR_LAYOUT: return "the checkpoint plane was written under another state layout (dtype or shape)";
         default: return "unknown kda status code";
     }
 }

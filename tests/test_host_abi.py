@@ -32,7 +32,7 @@ def desc(dtype=kda.KDA_F32, hv=12, k=128, v=128, num_slots=256, slot_stride=None
 
 def declared_functions():
     text = open(HEADER).read()
-    return sorted(set(re.findall(r"^\s*(?:int|const char\*)\s+(kda_\w+)\s*\(", text, re.M)))
+    return sorted(set(re.findall(r"^\s*(?:int|uint32_t|const char\*)\s+(kda_\w+)\s*\(", text, re.M)))
 
 
 def test_header_declarations_match_binding():
@@ -208,11 +208,45 @@ def test_conv_step_refusals_before_any_launch(libs):
     assert call(win(), args(n=0, total=0)) == kda.KDA_OK
 
 
+def test_layout_id_names_dtype_and_shape(libs):
+    """Pull request 2130, What: the checkpoint layout id names the dtype, so an
+    fp16 build cannot read an fp32 build's checkpoint images."""
+    L = libs[torch.float32]
+    base = L.kda_layout_id(desc())
+    assert base != 0 and L.kda_layout_id(desc()) == base
+    others = {L.kda_layout_id(desc(kda.KDA_F16)), L.kda_layout_id(desc(hv=8)), L.kda_layout_id(desc(k=64)),
+              L.kda_layout_id(desc(v=64))}
+    assert base not in others and len(others) == 4
+    assert L.kda_layout_id(desc(num_slots=9, slot_stride=12 * 128 * 128 + 64)) == base  # slots do not matter
+    assert L.lib.kda_layout_id(None) == 0
+
+
+def test_ckpt_refusals_before_any_launch(libs):
+    L32, L16 = libs[torch.float32], libs[torch.float16]
+    P = 0x7F0000100000
+    d32, d16 = desc(), desc(kda.KDA_F16)
+    plane = lambda lid, **kw: kda.CkptPlaneDesc(**{**dict(base=P, layout_id=lid, reserved=0, num_entries=8,  # noqa
+                                                         entry_stride=12 * 128 * 128), **kw})
+    lid32, lid16 = L32.kda_layout_id(d32), L16.kda_layout_id(d16)
+    call = lambda L, d, pl, n=4, slots=P, status=P: L.lib.kda_ckpt_flush(  # noqa: E731
+        ctypes.byref(d), ctypes.byref(pl), slots, P, n, status, 0, None)
+    assert call(L32, d32, plane(lid16)) == kda.KDA_ERR_LAYOUT     # an fp16 image in the fp32 build
+    assert call(L16, d16, plane(lid32)) == kda.KDA_ERR_LAYOUT
+    assert call(L16, d32, plane(lid32)) == kda.KDA_ERR_DTYPE_MISMATCH
+    assert call(L32, d32, plane(lid32, entry_stride=100)) == kda.KDA_ERR_SHAPE
+    assert call(L32, d32, plane(lid32, reserved=1)) == kda.KDA_ERR_ARG
+    assert call(L32, d32, plane(lid32), n=-1) == kda.KDA_ERR_ARG
+    assert call(L32, d32, plane(lid32), slots=None) == kda.KDA_ERR_NULL
+    assert call(L32, d32, plane(lid32, base=P + 8)) == kda.KDA_ERR_ALIGN
+    assert call(L32, d32, plane(lid32), n=0) == kda.KDA_OK
+    assert L32.lib.kda_ckpt_load(ctypes.byref(d32), None, P, P, 1, P, 0, None) == kda.KDA_ERR_NULL
+
+
 def test_strerror_covers_every_code(libs):
     L = libs[torch.float32]
-    msgs = {c: L.kda_strerror(c) for c in range(11)}
+    msgs = {c: L.kda_strerror(c) for c in range(12)}
     assert msgs[0] == "ok"
-    assert len(set(msgs.values())) == 11
+    assert len(set(msgs.values())) == 12
     assert L.kda_strerror(99) == "unknown kda status code"
 
 
