@@ -268,3 +268,65 @@ def make_conv(n=8, t=5, t_lens=None, channels=4608, kw=4, num_spec=4, num_slots=
         cu[1:] = torch.cumsum(torch.tensor(lens, dtype=torch.int64), 0).to(torch.int32)
     return ConvInputs(W, slots, x, w, b, cu, acc, reset, max(lens) if lens else 0,
                       dict(kind="conv", n=n, kw=kw, L=L, channels=channels, seed=seed, lens=lens))
+
+
+@dataclass
+class PrefillInputs:
+    """CPU tensors of one prefill call over packed prompts."""
+    pool: torch.Tensor
+    init_slot: torch.Tensor            # int32 [N]
+    final_slot: torch.Tensor           # int32 [N]
+    q: torch.Tensor                    # [total, H, K]
+    k: torch.Tensor
+    v: torch.Tensor                    # [total, HV, V]
+    a: torch.Tensor                    # fp32 [total, HV, K]
+    b: torch.Tensor                    # fp32 [total, HV]
+    cu_seqlens: torch.Tensor | None = None
+    reset: torch.Tensor | None = None
+    a_log: torch.Tensor | None = None
+    dt_bias: torch.Tensor | None = None
+    max_t: int = 0
+    meta: dict = field(default_factory=dict)
+
+    def to(self, device) -> "PrefillInputs":
+        mv = lambda t: None if t is None else t.to(device)  # noqa: E731
+        return PrefillInputs(mv(self.pool), mv(self.init_slot), mv(self.final_slot), mv(self.q), mv(self.k),
+                             mv(self.v), mv(self.a), mv(self.b), mv(self.cu_seqlens), mv(self.reset),
+                             mv(self.a_log), mv(self.dt_bias), self.max_t, dict(self.meta))
+
+
+def make_prefill(lens=(200, 37), h_qk=None, hv=12, k=128, v=128, num_slots=16, state_dtype=torch.float16,
+                 qkv_dtype=torch.bfloat16, seed=6, reset_p=0.5, same_slot_p=0.5, gate_scale=False,
+                 pad_p=0.0) -> PrefillInputs:
+    """Prompts of the given lengths (packed; cu_seqlens always given), q/k/v
+    N(0, 1) in qkv_dtype, a, b N(0, 1); a request starts from zero (fresh
+    prompt, probability reset_p) or from a slot's state, and its final state
+    goes to its own slot or to a fresh one.  The gate-scale draws follow
+    make_general."""
+    g = torch.Generator().manual_seed(seed)
+    n = len(lens)
+    h_qk = hv if h_qk is None else h_qk
+    if 2 * n > num_slots:
+        raise ValueError("not enough slots")
+    P = make_pool(g, num_slots, hv, k, v, state_dtype)
+    perm = torch.randperm(num_slots, generator=g).to(torch.int32)
+    init = perm[:n].clone()
+    final = torch.where(torch.rand((n,), generator=g) < same_slot_p, init, perm[n:2 * n])
+    total = int(sum(lens))
+    q = _randn(g, (total, h_qk, k), qkv_dtype)
+    kk = _randn(g, (total, h_qk, k), qkv_dtype)
+    vv = _randn(g, (total, hv, v), qkv_dtype)
+    a = _randn(g, (total, hv, k))
+    b = _randn(g, (total, hv))
+    reset = (torch.rand((n,), generator=g) < reset_p).to(torch.uint8)
+    if pad_p > 0:
+        init[torch.rand((n,), generator=g) < pad_p] = -1
+    a_log = dt_bias = None
+    if gate_scale:
+        a_log = torch.log(1.0 + 15.0 * torch.rand((hv,), generator=g))
+        lo, hi = torch.log(torch.tensor(1e-3)), torch.log(torch.tensor(1e-1))
+        dt_bias = torch.log(torch.expm1(torch.exp(lo + (hi - lo) * torch.rand((hv, k), generator=g))))
+    cu = torch.zeros(n + 1, dtype=torch.int32)
+    cu[1:] = torch.cumsum(torch.tensor(list(lens), dtype=torch.int64), 0).to(torch.int32)
+    return PrefillInputs(P, init, final.to(torch.int32), q, kk, vv, a, b, cu, reset, a_log, dt_bias,
+                         max(lens) if lens else 0, dict(kind="prefill", lens=list(lens), seed=seed))

@@ -98,6 +98,9 @@ def _load():
             lib.oracle_ckpt_transfer.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p,
                                                  ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int,
                                                  ctypes.c_int, i32p, i32p, ctypes.c_int]
+            lib.oracle_prefill.restype = ctypes.c_int
+            lib.oracle_prefill.argtypes = common + [ctypes.c_int, i32p, ctypes.c_int, i32p, i32p, u8p,
+                                                    dp, dp, dp, dp, dp, dp, dp, dp, ctypes.c_int]
             _lib = lib
     return _lib
 
@@ -296,3 +299,34 @@ def ckpt_transfer(pool: np.ndarray, plane: np.ndarray, slots, entries, load: boo
                                       _ptr(entries, ctypes.c_int32), int(bool(load)))
     if rc != 0:
         raise ValueError("oracle_ckpt_transfer: index out of range")
+
+
+def prefill(pool: np.ndarray, init_slot, final_slot, q, k, v, a, b, cu_seqlens=None, reset=None,
+            a_log=None, dt_bias=None, slot_stride=None, nthreads: int = 1) -> np.ndarray:
+    """Prefill over packed prompts: the state from init_slot[r] (zero on reset;
+    negative: padding), the state after the last token to final_slot[r]
+    (negative: not stored).  q, k: [total, H, K]; v: [total, HV, V];
+    a: [total, HV, K]; b: [total, HV].  Returns o fp64 [total, HV, V]."""
+    init_slot = np.ascontiguousarray(np.asarray(init_slot, dtype=np.int32))
+    final_slot = np.ascontiguousarray(np.asarray(final_slot, dtype=np.int32))
+    n = init_slot.shape[0]
+    args = _pool_args(pool, slot_stride)
+    hv, vdim = args[3], args[5]
+    q64, k64, v64, a64, b64 = (_f64(x) for x in (q, k, v, a, b))
+    total, h_qk = q64.shape[0], q64.shape[1]
+    cu = None if cu_seqlens is None else np.ascontiguousarray(np.asarray(cu_seqlens, dtype=np.int32))
+    t_uniform = 0 if cu is not None else (total // n if n else 0)
+    rs = None if reset is None else np.ascontiguousarray(np.asarray(reset, dtype=np.uint8))
+    al = None if a_log is None else _f64(a_log)
+    db = None if dt_bias is None else _f64(dt_bias)
+    o = np.zeros((total, hv, vdim), dtype=np.float64)
+    opt = lambda x, t: None if x is None else _ptr(x, t)  # noqa: E731
+    rc = _load().oracle_prefill(
+        *args, n, h_qk, opt(cu, ctypes.c_int32), t_uniform, _ptr(init_slot, ctypes.c_int32),
+        _ptr(final_slot, ctypes.c_int32), opt(rs, ctypes.c_uint8), _ptr(q64, ctypes.c_double),
+        _ptr(k64, ctypes.c_double), _ptr(v64, ctypes.c_double), _ptr(a64, ctypes.c_double),
+        _ptr(b64, ctypes.c_double), opt(al, ctypes.c_double), opt(db, ctypes.c_double),
+        _ptr(o, ctypes.c_double), int(nthreads))
+    if rc != 0:
+        raise ValueError(f"oracle_prefill failed ({rc})")
+    return o

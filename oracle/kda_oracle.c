@@ -543,3 +543,68 @@ int oracle_ckpt_transfer(void* pool_base, int64_t num_slots, int64_t slot_stride
     }
     return 0;
 }
+
+/*
+ * Prefill: the same recurrence over each request's prompt (the second
+ * workload of ATOM pull request 2130, What: prefill reads and writes the state
+ * through the destination's element type like every other path).  Request r
+ * owns tokens cu[r] .. cu[r+1]-1 (or r*t_uniform ..); its state starts from
+ * init_slot[r] (zero when reset[r]; a negative init_slot is a padding request:
+ * nothing read or stored, outputs zero) and only the state after its last
+ * token is stored, to final_slot[r] (negative: not stored; may equal
+ * init_slot[r]).  A request with no tokens stores its initial state unchanged.
+ * Heads, gate and layouts as in oracle_step.  Returns 0, -1 slot out of range,
+ * -3 layout.
+ */
+int oracle_prefill(void* base, int dtype, int64_t num_slots, int hv, int k, int v,
+                   int64_t slot_stride, int n_req, int h_qk, const int32_t* cu, int t_uniform,
+                   const int32_t* init_slot, const int32_t* final_slot, const uint8_t* reset,
+                   const double* q, const double* kk, const double* vv, const double* a,
+                   const double* b, const double* a_log, const double* dt_bias, double* o,
+                   int nthreads)
+{
+    oracle_pool p = {base, dtype, num_slots, hv, k, v, slot_stride};
+    const int HV = hv, K = k, V = v;
+    if (h_qk <= 0 || HV % h_qk != 0) return -3;
+    const int group = HV / h_qk;
+    for (int r = 0; r < n_req; ++r) {
+        int64_t tr = cu ? (int64_t)cu[r + 1] - cu[r] : t_uniform;
+        if (tr < 0) return -3;
+        if (init_slot[r] >= num_slots || final_slot[r] >= num_slots) return -1;
+    }
+    int64_t pairs = (int64_t)n_req * HV;
+    int bad = 0;
+#if defined(_OPENMP)
+#pragma omp parallel for schedule(dynamic, 1) num_threads(nthreads) if (nthreads > 1)
+#endif
+    for (int64_t nh = 0; nh < pairs; ++nh) {
+        int r = (int)(nh / HV), h = (int)(nh % HV);
+        int64_t t0 = cu ? cu[r] : (int64_t)r * t_uniform;
+        int64_t tr = cu ? (int64_t)cu[r + 1] - cu[r] : t_uniform;
+        if (init_slot[r] < 0) {  /* padding request */
+            for (int64_t j = 0; j < tr; ++j)
+                memset(o + ((t0 + j) * HV + h) * V, 0, sizeof(double) * (size_t)V);
+            continue;
+        }
+        double* S = (double*)malloc(sizeof(double) * ((size_t)K * V + 2 * (size_t)K + (size_t)V));
+        if (!S) { bad = 1; continue; }
+        double* qh = S + (int64_t)K * V;
+        double* kh = qh + K;
+        double* u = kh + K;
+        if (reset && reset[r]) memset(S, 0, sizeof(double) * (size_t)K * V);
+        else load_state(&p, init_slot[r], h, S);
+        double scale = a_log ? exp(a_log[h]) : 1.0;
+        const double* bias = dt_bias ? dt_bias + (int64_t)h * K : NULL;
+        int hq = h / group;
+        for (int64_t j = 0; j < tr; ++j) {
+            int64_t tok = t0 + j;
+            int64_t vrow = tok * HV + h, qrow = tok * h_qk + hq;
+            recur_token_gated(K, V, S, q + qrow * K, kk + qrow * K, vv + vrow * V, a + vrow * K,
+                              b[vrow], scale, bias, o + vrow * V, qh, kh, u);
+        }
+        if (final_slot[r] >= 0) store_state(&p, final_slot[r], h, S);
+        free(S);
+    }
+    (void)nthreads;
+    return bad ? -2 : 0;
+}
