@@ -232,7 +232,7 @@ def main():
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer measurement")
     ap.add_argument("--workload", choices=("decode_f32", "decode_f16"), default="decode_f32",
                     help="headline workload: the decode step on an fp32 pool (the metric's) or fp16 pool")
-    ap.add_argument("--case", choices=("verify_f16", "sweep"), default=None,
+    ap.add_argument("--case", choices=("verify_f16", "sweep", "prefill"), default=None,
                     help="time one secondary case alone and print its line (profiling runs)")
     ap.add_argument("--soak-seconds", type=float, default=1.0,
                     help="minimum untimed load before timing (clocks ramp; 0 under a profiler)")
@@ -373,6 +373,9 @@ def main():
     if args.case is not None:
         if args.case == "verify_f16":
             res = {"verify_f16": bench_verify(kda, workloads, torch, args, l2, peak)}
+        elif args.case == "prefill":
+            res = {f"prefill_{n}x{t}_fp16": bench_prefill(kda, workloads, torch, n, t) for n, t in
+                   ((1, 8192), (8, 1024), (64, 128))}
         else:
             res = {f"sweep_69_layers_n{n}_{nm}": bench_sweep(kda, workloads, torch, sd, n, peak)
                    for nm, sd in (("fp32", torch.float32), ("fp16", torch.float16))
@@ -413,6 +416,7 @@ def main():
         for sd_name, sd in (("fp32", torch.float32), ("fp16", torch.float16)):
             extra[f"sweep_69_layers_n128_{sd_name}"] = bench_sweep(kda, workloads, torch, sd, 128, peak)
         extra["ckpt_flush_fp32_n64"] = bench_ckpt(kda, workloads, torch, peak)
+        extra["prefill_8x1024_fp16"] = bench_prefill(kda, workloads, torch, 8, 1024)
 
     traffic = None
     tpath = os.path.join(REPO, "profiles", "decode_f32_n64_traffic.json")
@@ -509,6 +513,34 @@ def bench_sweep(kda, workloads, torch, state_dtype, n, peak, layers=69, replays=
             "us_per_forward": round(us_fwd, 2), "us_per_layer": round(us_fwd / layers, 3),
             "gbs": round(byt / (us_fwd * 1e-6) / 1e9, 1),
             "frac_of_peak": round(byt / (us_fwd * 1e-6) / 1e9 / peak, 4), "bytes_per_forward": byt}
+
+
+def bench_prefill(kda, workloads, torch, n, t, reps=5):
+    """Prefill of n fresh prompts of t tokens (HV=12, K=V=128, bf16 q/k/v,
+    fp16 pool), final states stored once; tokens per second."""
+    lib = kda.KdaLibrary(torch.float16)
+    inp = workloads.make_prefill(lens=[t] * n, state_dtype=torch.float16, num_slots=max(16, 2 * n), seed=7,
+                                 reset_p=1.0)
+    d = inp.to("cuda")
+    o = torch.empty(n * t, HV, V, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    call = lambda: lib.kda_prefill(d.pool, d.init_slot, d.final_slot, d.q, d.k, d.v, d.a, d.b, o, status,  # noqa
+                                   cu_seqlens=d.cu_seqlens, max_t=t, reset=d.reset)
+    call()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        call()
+    e1.record()
+    torch.cuda.synchronize()
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item())}")
+    ms = e0.elapsed_time(e1) / reps
+    flop = 6.0 * 2 * K * V * HV * n * t  # ~6 passes of 2 K V flop per token and head
+    return {"workload": f"prefill, {n} prompts x {t} tokens, HV=12, K=V=128, bf16 q/k/v, fp16 pool",
+            "ms_per_call": round(ms, 4), "tokens_per_s": round(n * t / (ms * 1e-3), 1),
+            "approx_tflops": round(flop / (ms * 1e-3) / 1e12, 3)}
 
 
 def bench_ckpt(kda, workloads, torch, peak, replays=200):

@@ -305,6 +305,47 @@ int kda_conv_step(const kda_conv_window* win, const kda_conv_args* args, int32_t
                   uint32_t flags, void* stream);
 
 /*
+ * Arguments of kda_prefill: the recurrence over packed prompts (the second
+ * workload of pull request 2130, What: prefill reads and writes the state
+ * through the destination's element type like every other path).  Request r
+ * owns tokens cu_seqlens[r] .. cu_seqlens[r+1] - 1 (or r * max_t .. with
+ * cu_seqlens NULL); its state starts from slot init_slot[r] (zero when
+ * reset[r] is nonzero: a fresh prompt; a negative init_slot is a padding
+ * request, nothing read or stored, outputs zero) and, after its last token,
+ * is stored to final_slot[r] (negative: not stored; it may equal init_slot[r]).
+ * No per-token state is stored.  A request with no tokens is left alone.
+ * Heads, gate and layouts as in kda_step_args; o gets every token's output.
+ */
+typedef struct kda_prefill_args {
+    int32_t n;                  /* requests */
+    int32_t total;              /* packed tokens */
+    int32_t max_t;              /* most tokens of any request */
+    int32_t h_qk;               /* q/k heads; hv % h_qk == 0 */
+    int32_t qkv_dtype;          /* KDA_F32, KDA_F16 or KDA_BF16 */
+    int32_t reserved;           /* 0 */
+    const int32_t* cu_seqlens;  /* [n + 1] or NULL */
+    const int32_t* init_slot;   /* [n] */
+    const int32_t* final_slot;  /* [n] */
+    const uint8_t* reset;       /* [n] or NULL */
+    const void* q;              /* [total][h_qk][k], 16-byte aligned */
+    const void* k;              /* [total][h_qk][k], 16-byte aligned */
+    const void* v;              /* [total][hv][v], 16-byte aligned */
+    const float* a;             /* [total][hv][k], 16-byte aligned */
+    const float* b;             /* [total][hv] */
+    const float* a_log;         /* [hv] or NULL */
+    const float* dt_bias;       /* [hv][k] or NULL */
+    float* o;                   /* [total][hv][v] (output) */
+} kda_prefill_args;
+
+/*
+ * Prefill (see kda_prefill_args).  Host checks as for kda_step (KDA_ERR_SHAPE
+ * for total != n * max_t without cu_seqlens); device: KDA_ERR_ARG for offsets
+ * outside 0 .. max_t or past total, KDA_ERR_SLOT_RANGE for a slot >= num_slots.
+ */
+int kda_prefill(const kda_pool* pool, const kda_prefill_args* args, int32_t* dev_status, uint32_t flags,
+                void* stream);
+
+/*
  * Checkpoint planes (ReplaySSM in pull request 2945, Changes: the checkpoint
  * load and the flush go through state_at; pull request 2130, What: the plane
  * shapes and the checkpoint layout id derive from the state dtype, so a build

@@ -35,7 +35,7 @@ KDA_LAUNCH_PDL, KDA_LAUNCH_PDL_EARLY_STATE = 1, 2
  KDA_ERR_SLOT_RANGE, KDA_ERR_ARG, KDA_ERR_TIMEOUT, KDA_ERR_LAYOUT) = range(12)
 
 EXPORTED_SYMBOLS = ("kda_build_state_dtype", "kda_pool_check", "kda_state_bytes",
-                    "kda_decode_step", "kda_spec_verify", "kda_step", "kda_conv_step",
+                    "kda_decode_step", "kda_spec_verify", "kda_step", "kda_prefill", "kda_conv_step",
                     "kda_layout_id", "kda_ckpt_flush", "kda_ckpt_load", "kda_strerror")
 
 
@@ -62,6 +62,16 @@ class StepArgs(ctypes.Structure):
                 ("k", ctypes.c_void_p), ("v", ctypes.c_void_p), ("a", ctypes.c_void_p),
                 ("b", ctypes.c_void_p), ("a_log", ctypes.c_void_p), ("dt_bias", ctypes.c_void_p),
                 ("o", ctypes.c_void_p)]
+
+
+class PrefillArgs(ctypes.Structure):
+    """Mirror of ``struct kda_prefill_args`` (include/kda.h)."""
+    _fields_ = [("n", ctypes.c_int32), ("total", ctypes.c_int32), ("max_t", ctypes.c_int32),
+                ("h_qk", ctypes.c_int32), ("qkv_dtype", ctypes.c_int32), ("reserved", ctypes.c_int32),
+                ("cu_seqlens", ctypes.c_void_p), ("init_slot", ctypes.c_void_p), ("final_slot", ctypes.c_void_p),
+                ("reset", ctypes.c_void_p), ("q", ctypes.c_void_p), ("k", ctypes.c_void_p), ("v", ctypes.c_void_p),
+                ("a", ctypes.c_void_p), ("b", ctypes.c_void_p), ("a_log", ctypes.c_void_p),
+                ("dt_bias", ctypes.c_void_p), ("o", ctypes.c_void_p)]
 
 
 class ConvWindowDesc(ctypes.Structure):
@@ -163,6 +173,8 @@ def _load(state16: bool) -> ctypes.CDLL:
         lib.kda_spec_verify.argtypes = [P, vp, vp, vp, i32, i32, vp, vp, vp, i32, vp, vp, vp, vp, u32, vp]
         lib.kda_step.restype = ctypes.c_int
         lib.kda_step.argtypes = [P, ctypes.POINTER(StepArgs), vp, u32, vp]
+        lib.kda_prefill.restype = ctypes.c_int
+        lib.kda_prefill.argtypes = [P, ctypes.POINTER(PrefillArgs), vp, u32, vp]
         lib.kda_conv_step.restype = ctypes.c_int
         lib.kda_conv_step.argtypes = [ctypes.POINTER(ConvWindowDesc), ctypes.POINTER(ConvArgs), vp, u32, vp]
         lib.kda_layout_id.restype = ctypes.c_uint32
@@ -383,4 +395,42 @@ class KdaLibrary:
         """pool[slots[i]] <- plane[entries[i]] (whole states, bit for bit)."""
         self._ckpt(self.lib.kda_ckpt_load, "kda_ckpt_load", pool, plane, slots, entries, status, layout_id,
                    stream, flags)
+
+    def kda_prefill_raw(self, desc: PoolDesc, args: PrefillArgs, status, stream, flags=0) -> int:
+        return self.lib.kda_prefill(ctypes.byref(desc), ctypes.byref(args), status, flags, stream)
+
+    def kda_prefill(self, pool, init_slot, final_slot, q, k, v, a, b, o, status, cu_seqlens=None, max_t=None,
+                    reset=None, a_log=None, dt_bias=None, stream=None, flags=0) -> None:
+        """Prefill over packed prompts (see kda_prefill_args in include/kda.h)."""
+        import torch
+        desc = pool_desc(pool)
+        hv, kd, vd = desc.hv, desc.k, desc.v
+        n = int(init_slot.shape[0])
+        total, h_qk = int(q.shape[0]), int(q.shape[1])
+        qkv_types = (torch.float32, torch.float16, torch.bfloat16)
+        _expect("init_slot", init_slot, (n,), (torch.int32,))
+        _expect("final_slot", final_slot, (n,), (torch.int32,))
+        _expect("q", q, (total, h_qk, kd), qkv_types)
+        _expect("k", k, (total, h_qk, kd), (q.dtype,))
+        _expect("v", v, (total, hv, vd), (q.dtype,))
+        _expect("a", a, (total, hv, kd), (torch.float32,))
+        _expect("b", b, (total, hv), (torch.float32,))
+        _expect("o", o, (total, hv, vd), (torch.float32,))
+        _expect("status", status, (1,), (torch.int32,))
+        if cu_seqlens is not None:
+            _expect("cu_seqlens", cu_seqlens, (n + 1,), (torch.int32,))
+            if max_t is None:
+                raise ValueError("max_t is required with cu_seqlens")
+        elif max_t is None:
+            max_t = total // n if n else 0
+        if reset is not None:
+            _expect("reset", reset, (n,), (torch.uint8,))
+        if a_log is not None:
+            _expect("a_log", a_log, (hv,), (torch.float32,))
+        if dt_bias is not None:
+            _expect("dt_bias", dt_bias, (hv, kd), (torch.float32,))
+        args = PrefillArgs(n, total, int(max_t), h_qk, _dtype_code(q.dtype), 0, _ptr(cu_seqlens), _ptr(init_slot),
+                           _ptr(final_slot), _ptr(reset), _ptr(q), _ptr(k), _ptr(v), _ptr(a), _ptr(b), _ptr(a_log),
+                           _ptr(dt_bias), _ptr(o))
+        self._check(self.kda_prefill_raw(desc, args, _ptr(status), self._stream(stream), flags), "kda_prefill")
 

@@ -307,6 +307,7 @@ kda::StepParams make_params(const kda_pool* pool, const int32_t* init_slot,
     prm.dt_bias = nullptr;
     prm.mode = 0;
     prm.total = n * t;
+    prm.final_slot = nullptr;
     return prm;
 }
 
@@ -404,6 +405,37 @@ int kda_step(const kda_pool* pool, const kda_step_args* args, int32_t* dev_statu
     prm.mode = kda::MODE_PADDING;
     const cudaStream_t st = static_cast<cudaStream_t>(stream);
     return g.in_place ? launch<false>(pool, prm, g.qkv_dtype, st) : launch<true>(pool, prm, g.qkv_dtype, st);
+}
+
+int kda_prefill(const kda_pool* pool, const kda_prefill_args* args, int32_t* dev_status, uint32_t flags,
+                void* stream) {
+    if (args == nullptr) return KDA_ERR_NULL;
+    const kda_prefill_args& g = *args;
+    int rc = check_pool_for_build(pool);
+    if (rc != KDA_OK) return rc;
+    if (g.n < 0 || g.total < 0 || g.max_t < 0 || g.reserved != 0) return KDA_ERR_ARG;
+    if (flags & ~(uint32_t)(KDA_LAUNCH_PDL | KDA_LAUNCH_PDL_EARLY_STATE)) return KDA_ERR_ARG;
+    if (elem_size(g.qkv_dtype) == 0) return KDA_ERR_DTYPE_UNSUPPORTED;
+    if (g.h_qk < 1 || pool->hv % g.h_qk != 0) return KDA_ERR_SHAPE;
+    if (g.cu_seqlens == nullptr && (int64_t)g.total != (int64_t)g.n * g.max_t) return KDA_ERR_SHAPE;
+    if (g.n == 0 || g.total == 0 || g.max_t == 0) return KDA_OK;
+    if (!g.init_slot || !g.final_slot || !g.q || !g.k || !g.v || !g.a || !g.b || !g.o || !dev_status)
+        return KDA_ERR_NULL;
+    if (!aligned(g.init_slot, 4) || !aligned(g.final_slot, 4) || !aligned(dev_status, 4) || !aligned(g.b, 4) ||
+        !aligned(g.o, 4) || !aligned(g.a, 16) || !aligned(g.q, 16) || !aligned(g.k, 16) || !aligned(g.v, 16) ||
+        (g.cu_seqlens && !aligned(g.cu_seqlens, 4)) || (g.a_log && !aligned(g.a_log, 4)) ||
+        (g.dt_bias && !aligned(g.dt_bias, 4)))
+        return KDA_ERR_ALIGN;
+    kda::StepParams prm = make_params(pool, g.init_slot, nullptr, g.reset, g.n, g.max_t, g.q, g.k, g.v, g.a, g.b,
+                                      g.o, dev_status, flags);
+    prm.hqk = g.h_qk;
+    prm.cu = g.cu_seqlens;
+    prm.total = g.total;
+    prm.a_log = g.a_log;
+    prm.dt_bias = g.dt_bias;
+    prm.mode = kda::MODE_PADDING;
+    prm.final_slot = g.final_slot;
+    return launch<true>(pool, prm, g.qkv_dtype, static_cast<cudaStream_t>(stream));
 }
 
 int kda_conv_step(const kda_conv_window* win, const kda_conv_args* args, int32_t* dev_status,

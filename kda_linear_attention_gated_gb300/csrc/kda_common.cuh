@@ -49,6 +49,8 @@ struct StepParams {
     const float* dt_bias;     // [hv][k] or nullptr: gate bias
     uint32_t mode;            // MODE_* bits
     int total;                // rows of the packed token arrays (bounds cu)
+    const int32_t* final_slot; // [n] or nullptr: prefill, only the state after the last token is
+                              // stored, to final_slot[n] (negative: not stored); no snapshots
 };
 
 // A negative initial slot marks a padding request (nothing read or stored,

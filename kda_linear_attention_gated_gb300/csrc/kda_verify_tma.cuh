@@ -221,13 +221,16 @@ kda_verify_kernel(const __grid_constant__ CUtensorMap tmap, const StepParams p) 
     if (p.accepted != nullptr) col = p.accepted[n] - 1;
     const bool arg_ok = range_ok && col >= 0 && col < p.num_cols;
     const int32_t slot = arg_ok ? p.init_slot[(int64_t)n * p.init_stride + col] : 0;
-    const int32_t snap0 = arg_ok && lane < Tn ? p.snap_slot[(int64_t)n * p.snap_stride + lane] : 0;
+    const bool final_mode = p.final_slot != nullptr;  // prefill: no snapshots, one final store
+    const int32_t snap0 = !final_mode && arg_ok && lane < Tn ? p.snap_slot[(int64_t)n * p.snap_stride + lane] : 0;
+    const int32_t fin = final_mode ? p.final_slot[n] : -1;
     const bool issued = arg_ok && Tn > 0;  // the first chunk's inputs are requested
     if (!early && warp == 0 && issued) issue_inputs(0, min(TC, Tn));
     const bool padding = (p.mode & MODE_PADDING) != 0;
     auto slot_bad = [&](int32_t s) { return s >= p.num_slots || (s < 0 && !padding); };
-    bool bad = !arg_ok || slot_bad(slot) || slot_bad(snap0);
-    for (int t = lane + 32; arg_ok && t < Tn; t += 32) bad |= slot_bad(p.snap_slot[(int64_t)n * p.snap_stride + t]);
+    bool bad = !arg_ok || slot_bad(slot) || slot_bad(snap0) || fin >= p.num_slots;
+    for (int t = lane + 32; !final_mode && arg_ok && t < Tn; t += 32)
+        bad |= slot_bad(p.snap_slot[(int64_t)n * p.snap_stride + t]);
     bad = __any_sync(0xffffffffu, bad);  // the same answer in every warp
     const bool pad = !bad && slot < 0;     // a padding request
     const bool rst = !bad && p.reset != nullptr && p.reset[n] != 0;
@@ -264,7 +267,7 @@ kda_verify_kernel(const __grid_constant__ CUtensorMap tmap, const StepParams p) 
         if (t0 > 0 && warp == 0) issue_inputs(t0, tc);
         if (tid < tc) {
             bsm[tid] = __ldg(p.b + ((int64_t)tb + t0 + tid) * p.hv + h);
-            snaps[tid] = p.snap_slot[(int64_t)n * p.snap_stride + t0 + tid];
+            snaps[tid] = final_mode ? -1 : p.snap_slot[(int64_t)n * p.snap_stride + t0 + tid];
         }
         const bool ok_in = mbar_wait(bar_in, in_phase);
         in_phase ^= 1;
@@ -423,8 +426,28 @@ kda_verify_kernel(const __grid_constant__ CUtensorMap tmap, const StepParams p) 
         __syncthreads();
 
         // (6) the snapshots: S_t = alpha_t S_(t-1) + (beta_t khat_t) d_t^T,
-        // staged rounded in a swizzled tile, then stored
-        for (int j = 0; j < tc; ++j) {
+        // staged rounded in a swizzled tile, then stored.  Prefill keeps
+        // only the carry: the same update, nothing staged or stored.
+        for (int j = 0; final_mode && j < tc; ++j) {
+            float d[VEC];
+#pragma unroll
+            for (int c = 0; c < VEC; c += 4) {
+                const float4 d4 = *reinterpret_cast<const float4*>(dsm + j * BV + chunk * VEC + c);
+                d[c] = d4.x; d[c + 1] = d4.y; d[c + 2] = d4.z; d[c + 3] = d4.w;
+            }
+            const uint32_t gb = gate_base + j * SH::G_TOK;
+#pragma unroll
+            for (int rr = 0; rr < ROWS; ++rr) {
+                const int row = lane + 32 * rr;
+                if (row < p.k) {
+                    const uint4 gq = lds128(gb + row * 16);
+                    const float al = __uint_as_float(gq.z), bkr = __uint_as_float(gq.w);
+#pragma unroll
+                    for (int c = 0; c < VEC; ++c) x[rr][c] = fmaf(al, x[rr][c], bkr * d[c]);
+                }
+            }
+        }
+        for (int j = 0; !final_mode && j < tc; ++j) {
             float d[VEC];
 #pragma unroll
             for (int c = 0; c < VEC; c += 4) {
@@ -474,7 +497,22 @@ kda_verify_kernel(const __grid_constant__ CUtensorMap tmap, const StepParams p) 
         fence_proxy_async_smem();
         __syncthreads();
     }
-    if (SH::TMA_STORE && tid == 0) bulk_wait<0>();  // the snapshot stores are complete
+    // prefill: the state after the last token, staged rounded in buffer 0 (free:
+    // no snapshot store used it) and stored as one box
+    if (final_mode && alive && state_in && fin >= 0) {
+#pragma unroll
+        for (int rr = 0; rr < ROWS; ++rr) {
+            const int row = lane + 32 * rr;
+            if (row < p.k) sts128(tile_base + swz<SH::ROWBYTES>(row, chunk), SV::narrow(x[rr]));
+        }
+        fence_proxy_async_smem();
+        __syncthreads();
+        if (tid == 0) {
+            tma_store_3d(&tmap, smem, cb * BV, h * p.k, fin);
+            bulk_commit();
+        }
+    }
+    if ((SH::TMA_STORE || final_mode) && tid == 0) bulk_wait<0>();  // the stores are complete
     if (!alive) {
         if (tid == 0) {
             atomicExch(p.status, STATUS_TIMEOUT);

@@ -1,0 +1,66 @@
+"""GPU prefill (kda_prefill) against the fp64 oracle: outputs of every token,
+the final state stored once (fp32 pool max-abs 1e-5, fp16 within one ulp of
+the oracle's single rounding), nothing else written."""
+import numpy as np
+import pytest
+import torch
+
+import kda_linear_attention_gated_gb300 as kda
+from kda_linear_attention_gated_gb300 import workloads
+
+import oracle
+from _harness import assert_out_match, assert_pool_match, lib_for, pool_np
+
+pytestmark = [pytest.mark.gpu, pytest.mark.usefixtures("built_libs", "oracle_mod")]
+SD = [torch.float32, torch.float16]
+
+
+def run(inp, flags=0):
+    d = inp.to("cuda")
+    total, hv, v = d.v.shape
+    o = torch.full((total, hv, v), float("nan"), device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    lib_for(inp.pool.dtype).kda_prefill(d.pool, d.init_slot, d.final_slot, d.q, d.k, d.v, d.a, d.b, o, status,
+                                        cu_seqlens=d.cu_seqlens, max_t=inp.max_t, reset=d.reset, a_log=d.a_log,
+                                        dt_bias=d.dt_bias, flags=flags)
+    torch.cuda.synchronize()
+    P = pool_np(inp.pool)
+    o_ref = oracle.prefill(P, inp.init_slot.numpy(), inp.final_slot.numpy(), inp.q, inp.k, inp.v, inp.a, inp.b,
+                           cu_seqlens=inp.cu_seqlens.numpy(), reset=inp.reset.numpy(), a_log=inp.a_log,
+                           dt_bias=inp.dt_bias, nthreads=8)
+    return d.pool.cpu(), o.cpu(), int(status.item()), P, o_ref
+
+
+def written(inp):
+    lens = inp.meta["lens"]
+    return [int(f) for f, i, t in zip(inp.final_slot, inp.init_slot, lens) if f >= 0 and i >= 0 and t > 0]
+
+
+@pytest.mark.parametrize("state_dtype", SD)
+def test_prefill_layer_shape(state_dtype):
+    """Prompts of 200 and 37 tokens (many chunks, ragged last chunk), HV=12, K=V=128, bf16 q/k/v."""
+    inp = workloads.make_prefill(lens=(200, 37), state_dtype=state_dtype, seed=90)
+    gp, o, st, P, o_ref = run(inp)
+    assert st == 0
+    assert_out_match(o, o_ref, state_dtype, "o")
+    assert_pool_match(gp, P, written(inp), "pool")
+
+
+@pytest.mark.parametrize("state_dtype", SD)
+def test_prefill_varlen_grouped_heads_gate_scale_padding(state_dtype):
+    inp = workloads.make_prefill(lens=(13, 0, 64, 1, 9), h_qk=4, state_dtype=state_dtype, num_slots=16,
+                                 qkv_dtype=torch.float32, seed=91, gate_scale=True, pad_p=0.3)
+    gp, o, st, P, o_ref = run(inp, flags=kda.KDA_LAUNCH_PDL)
+    assert st == 0
+    assert_out_match(o, o_ref, state_dtype, "o")
+    assert_pool_match(gp, P, written(inp), "pool")
+
+
+def test_prefill_long_prompt_sampled():
+    """One 2048-token prompt on an fp16 pool: final state and a sample of outputs."""
+    inp = workloads.make_prefill(lens=(2048,), state_dtype=torch.float16, num_slots=4, seed=92, reset_p=1.0)
+    gp, o, st, P, o_ref = run(inp)
+    assert st == 0
+    idx = np.r_[0:16, 1000:1016, 2032:2048]
+    assert_out_match(o[idx], o_ref[idx], torch.float16, "o")
+    assert_pool_match(gp, P, written(inp), "pool")

@@ -242,6 +242,27 @@ def test_ckpt_refusals_before_any_launch(libs):
     assert L32.lib.kda_ckpt_load(ctypes.byref(d32), None, P, P, 1, P, 0, None) == kda.KDA_ERR_NULL
 
 
+def test_prefill_refusals_before_any_launch(libs):
+    L32 = libs[torch.float32]
+    P = 0x7F0000100000
+
+    def args(**kw):
+        f = dict(n=2, total=64, max_t=32, h_qk=12, qkv_dtype=kda.KDA_BF16, reserved=0, cu_seqlens=None,
+                 init_slot=P, final_slot=P, reset=None, q=P, k=P, v=P, a=P, b=P, a_log=None, dt_bias=None, o=P)
+        f.update(kw)
+        return kda.PrefillArgs(**f)
+
+    call = lambda a, d=None: L32.kda_prefill_raw(d or desc(), a, P, None, 0)  # noqa: E731
+    assert L32.lib.kda_prefill(ctypes.byref(desc()), None, P, 0, None) == kda.KDA_ERR_NULL
+    assert call(args(), d=desc(kda.KDA_F16)) == kda.KDA_ERR_DTYPE_MISMATCH
+    assert call(args(h_qk=7)) == kda.KDA_ERR_SHAPE
+    assert call(args(total=63)) == kda.KDA_ERR_SHAPE
+    assert call(args(reserved=2)) == kda.KDA_ERR_ARG
+    assert call(args(final_slot=None)) == kda.KDA_ERR_NULL
+    assert call(args(k=P + 8)) == kda.KDA_ERR_ALIGN
+    assert call(args(n=0, total=0)) == kda.KDA_OK
+
+
 def test_strerror_covers_every_code(libs):
     L = libs[torch.float32]
     msgs = {c: L.kda_strerror(c) for c in range(12)}
