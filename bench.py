@@ -374,8 +374,8 @@ def main():
         if args.case == "verify_f16":
             res = {"verify_f16": bench_verify(kda, workloads, torch, args, l2, peak)}
         elif args.case == "prefill":
-            res = {f"prefill_{n}x{t}_fp16": bench_prefill(kda, workloads, torch, n, t) for n, t in
-                   ((1, 8192), (8, 1024), (64, 128))}
+            res = {f"prefill_{n}x{t}_fp16{'_chunked' if c else ''}": bench_prefill(kda, workloads, torch, n, t, c)
+                   for c in (False, True) for n, t in ((1, 8192), (8, 1024), (64, 128))}
         else:
             res = {f"sweep_69_layers_n{n}_{nm}": bench_sweep(kda, workloads, torch, sd, n, peak)
                    for nm, sd in (("fp32", torch.float32), ("fp16", torch.float16))
@@ -417,6 +417,7 @@ def main():
             extra[f"sweep_69_layers_n128_{sd_name}"] = bench_sweep(kda, workloads, torch, sd, 128, peak)
         extra["ckpt_flush_fp32_n64"] = bench_ckpt(kda, workloads, torch, peak)
         extra["prefill_8x1024_fp16"] = bench_prefill(kda, workloads, torch, 8, 1024)
+        extra["prefill_8x1024_fp16_chunked"] = bench_prefill(kda, workloads, torch, 8, 1024, True)
 
     traffic = None
     tpath = os.path.join(REPO, "profiles", "decode_f32_n64_traffic.json")
@@ -515,17 +516,23 @@ def bench_sweep(kda, workloads, torch, state_dtype, n, peak, layers=69, replays=
             "frac_of_peak": round(byt / (us_fwd * 1e-6) / 1e9 / peak, 4), "bytes_per_forward": byt}
 
 
-def bench_prefill(kda, workloads, torch, n, t, reps=5):
+def bench_prefill(kda, workloads, torch, n, t, chunked=False, reps=5):
     """Prefill of n fresh prompts of t tokens (HV=12, K=V=128, bf16 q/k/v,
-    fp16 pool), final states stored once; tokens per second."""
+    fp16 pool), final states stored once; tokens per second.  chunked: the
+    two-pass form, its workspace allocated before timing."""
     lib = kda.KdaLibrary(torch.float16)
     inp = workloads.make_prefill(lens=[t] * n, state_dtype=torch.float16, num_slots=max(16, 2 * n), seed=7,
                                  reset_p=1.0)
     d = inp.to("cuda")
     o = torch.empty(n * t, HV, V, device="cuda")
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
-    call = lambda: lib.kda_prefill(d.pool, d.init_slot, d.final_slot, d.q, d.k, d.v, d.a, d.b, o, status,  # noqa
-                                   cu_seqlens=d.cu_seqlens, max_t=t, reset=d.reset)
+    if chunked:
+        ws = torch.empty(lib.kda_prefill_workspace_bytes(d.pool, n, n * t), dtype=torch.uint8, device="cuda")
+        call = lambda: lib.kda_prefill_chunked(d.pool, d.init_slot, d.final_slot, d.q, d.k, d.v, d.a, d.b, o,  # noqa
+                                               status, workspace=ws, cu_seqlens=d.cu_seqlens, max_t=t, reset=d.reset)
+    else:
+        call = lambda: lib.kda_prefill(d.pool, d.init_slot, d.final_slot, d.q, d.k, d.v, d.a, d.b, o, status,  # noqa
+                                       cu_seqlens=d.cu_seqlens, max_t=t, reset=d.reset)
     call()
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -538,7 +545,8 @@ def bench_prefill(kda, workloads, torch, n, t, reps=5):
         raise RuntimeError(f"device status {int(status.item())}")
     ms = e0.elapsed_time(e1) / reps
     flop = 6.0 * 2 * K * V * HV * n * t  # ~6 passes of 2 K V flop per token and head
-    return {"workload": f"prefill, {n} prompts x {t} tokens, HV=12, K=V=128, bf16 q/k/v, fp16 pool",
+    return {"workload": f"prefill{' (two passes)' if chunked else ''}, {n} prompts x {t} tokens, HV=12, K=V=128, "
+                        "bf16 q/k/v, fp16 pool",
             "ms_per_call": round(ms, 4), "tokens_per_s": round(n * t / (ms * 1e-3), 1),
             "approx_tflops": round(flop / (ms * 1e-3) / 1e12, 3)}
 

@@ -346,6 +346,19 @@ int kda_prefill(const kda_pool* pool, const kda_prefill_args* args, int32_t* dev
                 void* stream);
 
 /*
+ * Prefill in two passes over chunks of 16 tokens: a pass over every (chunk,
+ * head) at once that depends on the inputs only, then a short sequential scan
+ * per (request, head, 32 value columns) that carries the state from chunk to
+ * chunk.  Same arguments and results as kda_prefill; the first pass's results
+ * go to a caller-provided device workspace of at least
+ * kda_prefill_workspace_bytes(...) bytes, 256-byte aligned (KDA_ERR_ARG when
+ * smaller, KDA_ERR_ALIGN when misaligned).  K and V at most 128, as everywhere.
+ */
+int kda_prefill_workspace_bytes(const kda_pool* pool, int32_t n, int32_t total, int64_t* bytes);
+int kda_prefill_chunked(const kda_pool* pool, const kda_prefill_args* args, void* workspace,
+                        int64_t workspace_bytes, int32_t* dev_status, uint32_t flags, void* stream);
+
+/*
  * Checkpoint planes (ReplaySSM in pull request 2945, Changes: the checkpoint
  * load and the flush go through state_at; pull request 2130, What: the plane
  * shapes and the checkpoint layout id derive from the state dtype, so a build

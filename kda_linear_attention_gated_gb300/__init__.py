@@ -35,7 +35,8 @@ KDA_LAUNCH_PDL, KDA_LAUNCH_PDL_EARLY_STATE = 1, 2
  KDA_ERR_SLOT_RANGE, KDA_ERR_ARG, KDA_ERR_TIMEOUT, KDA_ERR_LAYOUT) = range(12)
 
 EXPORTED_SYMBOLS = ("kda_build_state_dtype", "kda_pool_check", "kda_state_bytes",
-                    "kda_decode_step", "kda_spec_verify", "kda_step", "kda_prefill", "kda_conv_step",
+                    "kda_decode_step", "kda_spec_verify", "kda_step", "kda_prefill", "kda_prefill_workspace_bytes",
+                    "kda_prefill_chunked", "kda_conv_step",
                     "kda_layout_id", "kda_ckpt_flush", "kda_ckpt_load", "kda_strerror")
 
 
@@ -175,6 +176,10 @@ def _load(state16: bool) -> ctypes.CDLL:
         lib.kda_step.argtypes = [P, ctypes.POINTER(StepArgs), vp, u32, vp]
         lib.kda_prefill.restype = ctypes.c_int
         lib.kda_prefill.argtypes = [P, ctypes.POINTER(PrefillArgs), vp, u32, vp]
+        lib.kda_prefill_workspace_bytes.restype = ctypes.c_int
+        lib.kda_prefill_workspace_bytes.argtypes = [P, i32, i32, ctypes.POINTER(ctypes.c_int64)]
+        lib.kda_prefill_chunked.restype = ctypes.c_int
+        lib.kda_prefill_chunked.argtypes = [P, ctypes.POINTER(PrefillArgs), vp, ctypes.c_int64, vp, u32, vp]
         lib.kda_conv_step.restype = ctypes.c_int
         lib.kda_conv_step.argtypes = [ctypes.POINTER(ConvWindowDesc), ctypes.POINTER(ConvArgs), vp, u32, vp]
         lib.kda_layout_id.restype = ctypes.c_uint32
@@ -399,8 +404,27 @@ class KdaLibrary:
     def kda_prefill_raw(self, desc: PoolDesc, args: PrefillArgs, status, stream, flags=0) -> int:
         return self.lib.kda_prefill(ctypes.byref(desc), ctypes.byref(args), status, flags, stream)
 
+    def kda_prefill_workspace_bytes(self, pool, n: int, total: int) -> int:
+        out = ctypes.c_int64(0)
+        self._check(self.lib.kda_prefill_workspace_bytes(ctypes.byref(pool_desc(pool)), n, total, ctypes.byref(out)),
+                    "kda_prefill_workspace_bytes")
+        return out.value
+
+    def kda_prefill_chunked(self, pool, init_slot, final_slot, q, k, v, a, b, o, status, workspace=None,
+                            **kw) -> None:
+        """kda_prefill in two passes (see include/kda.h); ``workspace`` is a CUDA
+        tensor of at least kda_prefill_workspace_bytes bytes, made here when None."""
+        import torch
+        need = self.kda_prefill_workspace_bytes(pool, int(init_slot.shape[0]), int(q.shape[0]))
+        if workspace is None:
+            workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+        if not workspace.is_cuda or not workspace.is_contiguous():
+            raise ValueError("workspace must be a contiguous CUDA tensor")
+        self.kda_prefill(pool, init_slot, final_slot, q, k, v, a, b, o, status,
+                         _workspace=(workspace.data_ptr(), workspace.numel() * workspace.element_size()), **kw)
+
     def kda_prefill(self, pool, init_slot, final_slot, q, k, v, a, b, o, status, cu_seqlens=None, max_t=None,
-                    reset=None, a_log=None, dt_bias=None, stream=None, flags=0) -> None:
+                    reset=None, a_log=None, dt_bias=None, stream=None, flags=0, _workspace=None) -> None:
         """Prefill over packed prompts (see kda_prefill_args in include/kda.h)."""
         import torch
         desc = pool_desc(pool)
@@ -432,5 +456,10 @@ class KdaLibrary:
         args = PrefillArgs(n, total, int(max_t), h_qk, _dtype_code(q.dtype), 0, _ptr(cu_seqlens), _ptr(init_slot),
                            _ptr(final_slot), _ptr(reset), _ptr(q), _ptr(k), _ptr(v), _ptr(a), _ptr(b), _ptr(a_log),
                            _ptr(dt_bias), _ptr(o))
-        self._check(self.kda_prefill_raw(desc, args, _ptr(status), self._stream(stream), flags), "kda_prefill")
+        if _workspace is None:
+            self._check(self.kda_prefill_raw(desc, args, _ptr(status), self._stream(stream), flags), "kda_prefill")
+        else:
+            self._check(self.lib.kda_prefill_chunked(ctypes.byref(desc), ctypes.byref(args), _workspace[0],
+                                                     _workspace[1], _ptr(status), flags, self._stream(stream)),
+                        "kda_prefill_chunked")
 

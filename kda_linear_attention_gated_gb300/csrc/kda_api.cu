@@ -23,6 +23,7 @@
 #include "kda_verify_tma.cuh"
 #include "kda_conv.cuh"
 #include "kda_ckpt.cuh"
+#include "kda_prefill_chunk.cuh"
 
 #ifndef KDA_STATE16
 #error "build with -DKDA_STATE16=0 (fp32 pool) or -DKDA_STATE16=1 (fp16 pool)"
@@ -436,6 +437,82 @@ int kda_prefill(const kda_pool* pool, const kda_prefill_args* args, int32_t* dev
     prm.mode = kda::MODE_PADDING;
     prm.final_slot = g.final_slot;
     return launch<true>(pool, prm, g.qkv_dtype, static_cast<cudaStream_t>(stream));
+}
+
+int kda_prefill_workspace_bytes(const kda_pool* pool, int32_t n, int32_t total, int64_t* bytes) {
+    if (pool == nullptr || bytes == nullptr) return KDA_ERR_NULL;
+    if (n < 0 || total < 0) return KDA_ERR_ARG;
+    // one block per (chunk slot, head); chunk slots stay below total / 16 + n
+    *bytes = ((int64_t)total / kda::PCH + n) * pool->hv * (int64_t)kda::PCH_FLOATS * 4;
+    return KDA_OK;
+}
+
+int kda_prefill_chunked(const kda_pool* pool, const kda_prefill_args* args, void* workspace,
+                        int64_t workspace_bytes, int32_t* dev_status, uint32_t flags, void* stream) {
+    if (args == nullptr) return KDA_ERR_NULL;
+    const kda_prefill_args& g = *args;
+    int rc = check_pool_for_build(pool);
+    if (rc != KDA_OK) return rc;
+    if (g.n < 0 || g.total < 0 || g.max_t < 0 || g.reserved != 0) return KDA_ERR_ARG;
+    if (flags & ~(uint32_t)(KDA_LAUNCH_PDL | KDA_LAUNCH_PDL_EARLY_STATE)) return KDA_ERR_ARG;
+    if (elem_size(g.qkv_dtype) == 0) return KDA_ERR_DTYPE_UNSUPPORTED;
+    if (g.h_qk < 1 || pool->hv % g.h_qk != 0) return KDA_ERR_SHAPE;
+    if (g.cu_seqlens == nullptr && (int64_t)g.total != (int64_t)g.n * g.max_t) return KDA_ERR_SHAPE;
+    if (g.n == 0 || g.total == 0 || g.max_t == 0) return KDA_OK;
+    if (!g.init_slot || !g.final_slot || !g.q || !g.k || !g.v || !g.a || !g.b || !g.o || !dev_status ||
+        !workspace)
+        return KDA_ERR_NULL;
+    int64_t need = 0;
+    kda_prefill_workspace_bytes(pool, g.n, g.total, &need);
+    if (workspace_bytes < need) return KDA_ERR_ARG;
+    if (!aligned(workspace, 256) || !aligned(g.init_slot, 4) || !aligned(g.final_slot, 4) ||
+        !aligned(dev_status, 4) || !aligned(g.b, 4) || !aligned(g.o, 4) || !aligned(g.a, 4) ||
+        !aligned(g.q, 4) || !aligned(g.k, 4) || !aligned(g.v, 4) || (g.cu_seqlens && !aligned(g.cu_seqlens, 4)) ||
+        (g.a_log && !aligned(g.a_log, 4)) || (g.dt_bias && !aligned(g.dt_bias, 4)))
+        return KDA_ERR_ALIGN;
+    kda::StepParams prm = make_params(pool, g.init_slot, nullptr, g.reset, g.n, g.max_t, g.q, g.k, g.v, g.a, g.b,
+                                      g.o, dev_status, flags);
+    prm.hqk = g.h_qk;
+    prm.cu = g.cu_seqlens;
+    prm.total = g.total;
+    prm.a_log = g.a_log;
+    prm.dt_bias = g.dt_bias;
+    prm.mode = kda::MODE_PADDING;
+    prm.final_slot = g.final_slot;
+    const int max_chunks = (g.max_t + kda::PCH - 1) / kda::PCH;
+    const int vtiles = (pool->v + kda::PVT - 1) / kda::PVT;
+    if ((int64_t)g.n * max_chunks > 0x7fffffffLL || (int64_t)g.n * pool->hv * vtiles > 0x7fffffffLL ||
+        pool->hv > 65535)
+        return KDA_ERR_SHAPE;
+    const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    float* ws = static_cast<float*>(workspace);
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr;
+    cfg.gridDim = dim3((unsigned)(g.n * max_chunks), (unsigned)pool->hv, 1);
+    cfg.blockDim = dim3(kda::KMAX, 1, 1);
+    cfg.stream = st;
+    set_pdl(cfg, &attr, flags);
+    cudaError_t err;
+    switch (g.qkv_dtype) {
+        case KDA_F32: err = cudaLaunchKernelEx(&cfg, kda::kda_prefill_prep_kernel<float>, prm, ws, max_chunks); break;
+        case KDA_F16: err = cudaLaunchKernelEx(&cfg, kda::kda_prefill_prep_kernel<__half>, prm, ws, max_chunks); break;
+        default: err = cudaLaunchKernelEx(&cfg, kda::kda_prefill_prep_kernel<__nv_bfloat16>, prm, ws, max_chunks); break;
+    }
+    if (err != cudaSuccess) return KDA_ERR_LAUNCH;
+    constexpr size_t smem = kda::PrefillScanSmem<state_t>::BYTES;
+    auto scan = kda::kda_prefill_scan_kernel<state_t>;
+    int occ = 0, sms = 0;
+    rc = occupancy(reinterpret_cast<const void*>(scan), kda::PSCAN_WARPS * 32, smem, &occ, &sms);
+    if (rc != KDA_OK) return rc;
+    cudaLaunchConfig_t cfg2 = {};
+    cudaLaunchAttribute attr2;
+    cfg2.gridDim = dim3((unsigned)(g.n * pool->hv * vtiles), 1, 1);
+    cfg2.blockDim = dim3(kda::PSCAN_WARPS * 32, 1, 1);
+    cfg2.dynamicSmemBytes = smem;
+    cfg2.stream = st;
+    set_pdl(cfg2, &attr2, KDA_LAUNCH_PDL);  // the scan starts while the first pass drains
+    err = cudaLaunchKernelEx(&cfg2, scan, prm, static_cast<const float*>(ws));
+    return err == cudaSuccess ? KDA_OK : KDA_ERR_LAUNCH;
 }
 
 int kda_conv_step(const kda_conv_window* win, const kda_conv_args* args, int32_t* dev_status,

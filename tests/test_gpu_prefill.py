@@ -15,14 +15,15 @@ pytestmark = [pytest.mark.gpu, pytest.mark.usefixtures("built_libs", "oracle_mod
 SD = [torch.float32, torch.float16]
 
 
-def run(inp, flags=0):
+def run(inp, flags=0, chunked=False):
     d = inp.to("cuda")
     total, hv, v = d.v.shape
     o = torch.full((total, hv, v), float("nan"), device="cuda")
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
-    lib_for(inp.pool.dtype).kda_prefill(d.pool, d.init_slot, d.final_slot, d.q, d.k, d.v, d.a, d.b, o, status,
-                                        cu_seqlens=d.cu_seqlens, max_t=inp.max_t, reset=d.reset, a_log=d.a_log,
-                                        dt_bias=d.dt_bias, flags=flags)
+    lib = lib_for(inp.pool.dtype)
+    call = lib.kda_prefill_chunked if chunked else lib.kda_prefill
+    call(d.pool, d.init_slot, d.final_slot, d.q, d.k, d.v, d.a, d.b, o, status, cu_seqlens=d.cu_seqlens,
+         max_t=inp.max_t, reset=d.reset, a_log=d.a_log, dt_bias=d.dt_bias, flags=flags)
     torch.cuda.synchronize()
     P = pool_np(inp.pool)
     o_ref = oracle.prefill(P, inp.init_slot.numpy(), inp.final_slot.numpy(), inp.q, inp.k, inp.v, inp.a, inp.b,
@@ -36,31 +37,64 @@ def written(inp):
     return [int(f) for f, i, t in zip(inp.final_slot, inp.init_slot, lens) if f >= 0 and i >= 0 and t > 0]
 
 
+CHUNKED = [False, True]
+
+
+@pytest.mark.parametrize("chunked", CHUNKED)
 @pytest.mark.parametrize("state_dtype", SD)
-def test_prefill_layer_shape(state_dtype):
+def test_prefill_layer_shape(state_dtype, chunked):
     """Prompts of 200 and 37 tokens (many chunks, ragged last chunk), HV=12, K=V=128, bf16 q/k/v."""
     inp = workloads.make_prefill(lens=(200, 37), state_dtype=state_dtype, seed=90)
-    gp, o, st, P, o_ref = run(inp)
+    gp, o, st, P, o_ref = run(inp, chunked=chunked)
     assert st == 0
     assert_out_match(o, o_ref, state_dtype, "o")
     assert_pool_match(gp, P, written(inp), "pool")
 
 
+@pytest.mark.parametrize("chunked", CHUNKED)
 @pytest.mark.parametrize("state_dtype", SD)
-def test_prefill_varlen_grouped_heads_gate_scale_padding(state_dtype):
+def test_prefill_varlen_grouped_heads_gate_scale_padding(state_dtype, chunked):
     inp = workloads.make_prefill(lens=(13, 0, 64, 1, 9), h_qk=4, state_dtype=state_dtype, num_slots=16,
                                  qkv_dtype=torch.float32, seed=91, gate_scale=True, pad_p=0.3)
-    gp, o, st, P, o_ref = run(inp, flags=kda.KDA_LAUNCH_PDL)
+    gp, o, st, P, o_ref = run(inp, flags=kda.KDA_LAUNCH_PDL, chunked=chunked)
     assert st == 0
     assert_out_match(o, o_ref, state_dtype, "o")
     assert_pool_match(gp, P, written(inp), "pool")
 
 
-def test_prefill_long_prompt_sampled():
+@pytest.mark.parametrize("chunked", CHUNKED)
+def test_prefill_long_prompt_sampled(chunked):
     """One 2048-token prompt on an fp16 pool: final state and a sample of outputs."""
     inp = workloads.make_prefill(lens=(2048,), state_dtype=torch.float16, num_slots=4, seed=92, reset_p=1.0)
-    gp, o, st, P, o_ref = run(inp)
+    gp, o, st, P, o_ref = run(inp, chunked=chunked)
     assert st == 0
     idx = np.r_[0:16, 1000:1016, 2032:2048]
     assert_out_match(o[idx], o_ref[idx], torch.float16, "o")
     assert_pool_match(gp, P, written(inp), "pool")
+
+
+@pytest.mark.parametrize("state_dtype", SD)
+def test_chunked_prefill_ragged_shapes(state_dtype):
+    """K = 48, V = 80 (a partial 32-column tile), prompts shorter and longer than a chunk."""
+    inp = workloads.make_prefill(lens=(5, 16, 17, 40), hv=3, k=48, v=80, num_slots=12, state_dtype=state_dtype,
+                                 qkv_dtype=torch.float32, seed=93)
+    gp, o, st, P, o_ref = run(inp, chunked=True)
+    assert st == 0
+    assert_out_match(o, o_ref, state_dtype, "o")
+    assert_pool_match(gp, P, written(inp), "pool")
+
+
+def test_chunked_prefill_workspace_too_small_is_refused():
+    inp = workloads.make_prefill(lens=(20,), hv=2, k=16, v=16, num_slots=4, state_dtype=torch.float32,
+                                 qkv_dtype=torch.float32, seed=94)
+    d = inp.to("cuda")
+    lib = lib_for(torch.float32)
+    o = torch.empty(20, 2, 16, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    need = lib.kda_prefill_workspace_bytes(d.pool, 1, 20)
+    assert need == (20 // 16 + 1) * 2 * 10368 * 4
+    with pytest.raises(kda.KdaError) as e:
+        lib.kda_prefill_chunked(d.pool, d.init_slot, d.final_slot, d.q, d.k, d.v, d.a, d.b, o, status,
+                                workspace=torch.empty(need - 256, dtype=torch.uint8, device="cuda"),
+                                cu_seqlens=d.cu_seqlens, max_t=20, reset=d.reset)
+    assert e.value.code == kda.KDA_ERR_ARG
