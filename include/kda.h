@@ -359,6 +359,18 @@ int kda_prefill_chunked(const kda_pool* pool, const kda_prefill_args* args, void
                         int64_t workspace_bytes, int32_t* dev_status, uint32_t flags, void* stream);
 
 /*
+ * kda_prefill_chunked without a caller workspace, allocating nothing: the
+ * first pass's results go to a scratch buffer of KDA_PREFILL_SCRATCH_BYTES
+ * that the library holds in device memory for the life of the process (one
+ * per device).  KDA_ERR_SHAPE when kda_prefill_workspace_bytes(...) exceeds
+ * it.  Calls share that buffer, so they must be ordered (one stream, or
+ * streams synchronised between calls); otherwise as kda_prefill_chunked.
+ */
+#define KDA_PREFILL_SCRATCH_BYTES (128ll << 20)
+int kda_prefill_chunked_noalloc(const kda_pool* pool, const kda_prefill_args* args, int32_t* dev_status,
+                                uint32_t flags, void* stream);
+
+/*
  * Checkpoint planes (ReplaySSM in pull request 2945, Changes: the checkpoint
  * load and the flush go through state_at; pull request 2130, What: the plane
  * shapes and the checkpoint layout id derive from the state dtype, so a build

@@ -36,7 +36,7 @@ KDA_LAUNCH_PDL, KDA_LAUNCH_PDL_EARLY_STATE = 1, 2
 
 EXPORTED_SYMBOLS = ("kda_build_state_dtype", "kda_pool_check", "kda_state_bytes",
                     "kda_decode_step", "kda_spec_verify", "kda_step", "kda_prefill", "kda_prefill_workspace_bytes",
-                    "kda_prefill_chunked", "kda_conv_step",
+                    "kda_prefill_chunked", "kda_prefill_chunked_noalloc", "kda_conv_step",
                     "kda_layout_id", "kda_ckpt_flush", "kda_ckpt_load", "kda_strerror")
 
 
@@ -180,6 +180,8 @@ def _load(state16: bool) -> ctypes.CDLL:
         lib.kda_prefill_workspace_bytes.argtypes = [P, i32, i32, ctypes.POINTER(ctypes.c_int64)]
         lib.kda_prefill_chunked.restype = ctypes.c_int
         lib.kda_prefill_chunked.argtypes = [P, ctypes.POINTER(PrefillArgs), vp, ctypes.c_int64, vp, u32, vp]
+        lib.kda_prefill_chunked_noalloc.restype = ctypes.c_int
+        lib.kda_prefill_chunked_noalloc.argtypes = [P, ctypes.POINTER(PrefillArgs), vp, u32, vp]
         lib.kda_conv_step.restype = ctypes.c_int
         lib.kda_conv_step.argtypes = [ctypes.POINTER(ConvWindowDesc), ctypes.POINTER(ConvArgs), vp, u32, vp]
         lib.kda_layout_id.restype = ctypes.c_uint32
@@ -406,7 +408,8 @@ class KdaLibrary:
 
     def kda_prefill_workspace_bytes(self, pool, n: int, total: int) -> int:
         out = ctypes.c_int64(0)
-        self._check(self.lib.kda_prefill_workspace_bytes(ctypes.byref(pool_desc(pool)), n, total, ctypes.byref(out)),
+        desc = pool if isinstance(pool, PoolDesc) else pool_desc(pool)
+        self._check(self.lib.kda_prefill_workspace_bytes(ctypes.byref(desc), n, total, ctypes.byref(out)),
                     "kda_prefill_workspace_bytes")
         return out.value
 
@@ -423,8 +426,13 @@ class KdaLibrary:
         self.kda_prefill(pool, init_slot, final_slot, q, k, v, a, b, o, status,
                          _workspace=(workspace.data_ptr(), workspace.numel() * workspace.element_size()), **kw)
 
+    def kda_prefill_chunked_noalloc(self, pool, init_slot, final_slot, q, k, v, a, b, o, status, **kw) -> None:
+        """kda_prefill in two passes on the library's own scratch buffer: nothing is allocated."""
+        self.kda_prefill(pool, init_slot, final_slot, q, k, v, a, b, o, status, _noalloc=True, **kw)
+
     def kda_prefill(self, pool, init_slot, final_slot, q, k, v, a, b, o, status, cu_seqlens=None, max_t=None,
-                    reset=None, a_log=None, dt_bias=None, stream=None, flags=0, _workspace=None) -> None:
+                    reset=None, a_log=None, dt_bias=None, stream=None, flags=0, _workspace=None,
+                    _noalloc=False) -> None:
         """Prefill over packed prompts (see kda_prefill_args in include/kda.h)."""
         import torch
         desc = pool_desc(pool)
@@ -456,7 +464,11 @@ class KdaLibrary:
         args = PrefillArgs(n, total, int(max_t), h_qk, _dtype_code(q.dtype), 0, _ptr(cu_seqlens), _ptr(init_slot),
                            _ptr(final_slot), _ptr(reset), _ptr(q), _ptr(k), _ptr(v), _ptr(a), _ptr(b), _ptr(a_log),
                            _ptr(dt_bias), _ptr(o))
-        if _workspace is None:
+        if _noalloc:
+            self._check(self.lib.kda_prefill_chunked_noalloc(ctypes.byref(desc), ctypes.byref(args), _ptr(status),
+                                                             flags, self._stream(stream)),
+                        "kda_prefill_chunked_noalloc")
+        elif _workspace is None:
             self._check(self.kda_prefill_raw(desc, args, _ptr(status), self._stream(stream), flags), "kda_prefill")
         else:
             self._check(self.lib.kda_prefill_chunked(ctypes.byref(desc), ctypes.byref(args), _workspace[0],

@@ -169,6 +169,25 @@ int occupancy(const void* kernel, int threads, size_t smem, int* blocks_per_sm, 
     return KDA_OK;
 }
 
+// The scratch of kda_prefill_chunked_noalloc: a file-scope device array, so
+// that the call allocates nothing.  Its address is looked up once per device.
+static __device__ __align__(256) float g_prefill_scratch[KDA_PREFILL_SCRATCH_BYTES / 4];
+
+void* prefill_scratch() {
+    static std::mutex mu;
+    static std::map<int, void*> addr;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return nullptr;
+    std::lock_guard<std::mutex> lock(mu);
+    auto it = addr.find(dev);
+    if (it == addr.end()) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_prefill_scratch) != cudaSuccess) return nullptr;
+        it = addr.emplace(dev, p).first;
+    }
+    return it->second;
+}
+
 // Programmatic dependent launch attribute when the caller asked for it.
 void set_pdl(cudaLaunchConfig_t& cfg, cudaLaunchAttribute* attr, uint32_t flags) {
     if (flags & KDA_LAUNCH_PDL) {
@@ -513,6 +532,18 @@ int kda_prefill_chunked(const kda_pool* pool, const kda_prefill_args* args, void
     set_pdl(cfg2, &attr2, KDA_LAUNCH_PDL);  // the scan starts while the first pass drains
     err = cudaLaunchKernelEx(&cfg2, scan, prm, static_cast<const float*>(ws));
     return err == cudaSuccess ? KDA_OK : KDA_ERR_LAUNCH;
+}
+
+int kda_prefill_chunked_noalloc(const kda_pool* pool, const kda_prefill_args* args, int32_t* dev_status,
+                                uint32_t flags, void* stream) {
+    if (pool == nullptr || args == nullptr) return KDA_ERR_NULL;
+    int64_t need = 0;
+    const int rc = kda_prefill_workspace_bytes(pool, args->n, args->total, &need);
+    if (rc != KDA_OK) return rc;
+    if (need > KDA_PREFILL_SCRATCH_BYTES) return KDA_ERR_SHAPE;
+    void* ws = prefill_scratch();
+    if (ws == nullptr) return KDA_ERR_LAUNCH;
+    return kda_prefill_chunked(pool, args, ws, KDA_PREFILL_SCRATCH_BYTES, dev_status, flags, stream);
 }
 
 int kda_conv_step(const kda_conv_window* win, const kda_conv_args* args, int32_t* dev_status,
