@@ -28,7 +28,10 @@ namespace kda {
 constexpr int PCH = 16;                                   // tokens per chunk
 constexpr int PCH_FLOATS = 3 * KMAX * PCH + KMAX + 2 * KMAX * PCH;  // workspace floats per (chunk, head)
 constexpr int PVT = 32;                                   // value columns per scan CTA
-constexpr int PSCAN_WARPS = 8;                            // scan: warp w owns rows 16 w .. 16 w + 15
+#ifndef KDA_PSCAN_WARPS
+#define KDA_PSCAN_WARPS 8
+#endif
+constexpr int PSCAN_WARPS = KDA_PSCAN_WARPS;              // scan: warp w owns rows KMAX / PSCAN_WARPS * w ..
 constexpr int PSCAN_ROWS = KMAX / PSCAN_WARPS;
 
 // workspace offsets (floats) inside one (chunk, head) block
@@ -39,6 +42,7 @@ constexpr int PW_C = PW_KT + KMAX * PCH;        // c_(CH-1) [KMAX]
 constexpr int PW_U = PW_C + KMAX;               // U [KMAX / PVT][PCH][PVT]
 constexpr int PW_OI = PW_U + KMAX * PCH;        // O_intra [KMAX / PVT][PCH][PVT] (already / sqrt(K))
 static_assert(PW_OI + KMAX * PCH == PCH_FLOATS, "workspace layout");
+static_assert((2 * PCH) % PSCAN_WARPS == 0 && KMAX % PSCAN_WARPS == 0, "scan warps split the rows and vectors");
 
 // Chunk j of request r lives at slot floor(tb / PCH) + r + j, tb = the request's
 // first token: distinct for every (r, j) and below total / PCH + n.

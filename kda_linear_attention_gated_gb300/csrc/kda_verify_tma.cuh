@@ -8,10 +8,8 @@
 // token the state, rounded to the pool's dtype, is written to a swizzled
 // shared-memory staging tile and from there to that token's snapshot slot
 // snap_slot[n][t] (ROCm/ATOM pull request 2945, Changes: the state after each
-// token goes to the token's snapshot slot through state_at): either as one TMA
-// box store (KDA_VER_TMA_STORE, NSTAGE buffers in turn) or by every thread
-// reading back whole 16-byte row pieces and storing them coalesced (two
-// buffers in turn).
+// token goes to the token's snapshot slot through state_at) as one TMA box
+// store, three staging buffers in turn.
 //
 // The general step: request n owns tokens cu[n] .. cu[n+1] - 1 of packed
 // inputs (or n T .. n T + T - 1), reads its initial state from column
@@ -42,14 +40,8 @@
 
 #include "kda_common.cuh"
 
-#ifndef KDA_VER_TMA_STORE
-#define KDA_VER_TMA_STORE 1
-#endif
 #ifndef KDA_VER_MINB
 #define KDA_VER_MINB 3
-#endif
-#ifndef KDA_VER_NSTAGE
-#define KDA_VER_NSTAGE 3
 #endif
 
 namespace kda {
@@ -77,8 +69,7 @@ struct VerifyShape {
     // the gates overlay the inputs, which are all read into registers first
     static constexpr uint32_t WORK_BYTES = IN_BYTES > GATE_BYTES ? IN_BYTES : GATE_BYTES;
     // staging buffers for the snapshot stores (the state tile's area is the first)
-    static constexpr bool TMA_STORE = KDA_VER_TMA_STORE != 0;
-    static constexpr int NSTAGE = TMA_STORE ? KDA_VER_NSTAGE : 2;
+    static constexpr int NSTAGE = 3;
     // norms [TC][NW][2] and b [TC], scalars [TC] float4, A and B per warp
     // [NW][64] then summed [64], column sums [TC][2][BV], d [TC][BV], snapshot ids [TC]
     static constexpr uint32_t RED_NORM = 0, RED_B = RED_NORM + TC * NW * 8;
@@ -468,28 +459,14 @@ kda_verify_kernel(const __grid_constant__ CUtensorMap tmap, const StepParams p) 
                     sts128(stage + swz<SH::ROWBYTES>(row, chunk), SV::narrow(x[rr]));
                 }
             }
-            if constexpr (SH::TMA_STORE) {
-                fence_proxy_async_smem();
-                __syncthreads();
-                if (tid == 0 && snaps[j] >= 0) {  // a negative slot: this snapshot is not kept
-                    tma_store_3d(&tmap, smem + b * SH::TILE_BYTES, cb * BV, h * p.k, snaps[j]);
-                    bulk_commit();
-                    // the stores of the last NSTAGE - 2 tokens may still read their
-                    // buffers; the one token t + 1 rewrites is free
-                    bulk_wait_read<SH::NSTAGE - 2>();
-                }
-            } else {
-                // Every thread stores whole 16-byte pieces of rows, consecutive
-                // threads along a row: coalesced.  The barrier also frees the
-                // other buffer, which the next token writes.
-                __syncthreads();
-                ST* dst = static_cast<ST*>(p.pool) + state_at(p, snaps[j], h) + cb * BV;
-                for (int pc = tid; snaps[j] >= 0 && pc < p.k * NW; pc += SH::NT) {
-                    const int row = pc / NW, ch = pc - row * NW;
-                    if (ch * VEC < vcols)
-                        __stcs(reinterpret_cast<uint4*>(dst + (int64_t)row * p.v + ch * VEC),
-                               lds128(stage + swz<SH::ROWBYTES>(row, ch)));
-                }
+            fence_proxy_async_smem();
+            __syncthreads();
+            if (tid == 0 && snaps[j] >= 0) {  // a negative slot: this snapshot is not kept
+                tma_store_3d(&tmap, smem + b * SH::TILE_BYTES, cb * BV, h * p.k, snaps[j]);
+                bulk_commit();
+                // the store of token t - 1 may still read its buffer; the one
+                // token t + 1 rewrites is free
+                bulk_wait_read<SH::NSTAGE - 2>();
             }
         }
         // The next chunk's bulk copies (async proxy) overwrite this chunk's
@@ -512,7 +489,7 @@ kda_verify_kernel(const __grid_constant__ CUtensorMap tmap, const StepParams p) 
             bulk_commit();
         }
     }
-    if ((SH::TMA_STORE || final_mode) && tid == 0) bulk_wait<0>();  // the stores are complete
+    if (tid == 0) bulk_wait<0>();  // the stores are complete
     if (!alive) {
         if (tid == 0) {
             atomicExch(p.status, STATUS_TIMEOUT);
