@@ -328,43 +328,100 @@ def main():
                     pool_bytes=R * pools[0].numel() * es)
 
     def bench_e2e(steps):
-        """Through the C ABI with host buffers: H2D inputs, kernel, D2H output, per step."""
+        """Through the C ABI with host buffers, every step: one host-to-device
+        copy of the step's inputs (slot ids, q, k, v, a, b packed in one pinned
+        buffer), the decode kernel, one device-to-host copy of o.  Two sets of
+        device buffers alternate over three streams, so the copies of one step
+        overlap the kernels of its neighbours; events keep each buffer's
+        writer behind its last reader.  A group of steps is captured in one
+        CUDA graph (copies, calls and events included) and replayed, so the
+        host's per-call work does not pace the GPU; if capture is refused the
+        steps are issued one by one."""
         inp = workloads.make_decode(n=N, hv=HV, k=K, v=V, num_slots=SLOTS, state_dtype=torch.float32,
                                     qkv_dtype=torch.bfloat16, seed=0)
         R = max(4, math.ceil(4 * l2 / (N * HV * K * V * 4)) + 1)
         pools = make_pools(inp, R)
-        host = {n: getattr(inp, n).pin_memory() for n in ("init_slot", "q", "k", "v", "a", "b")}
-        dev = {n: torch.empty_like(t, device="cuda") for n, t in host.items()}
-        o = torch.empty(N, HV, V, device="cuda")
-        o_host = torch.empty(N, HV, V).pin_memory()
+        names = ("init_slot", "q", "k", "v", "a", "b")
+        srcs = [getattr(inp, n_).contiguous() for n_ in names]
+        sizes = [t.numel() * t.element_size() for t in srcs]
+        offs = [0]
+        for sz in sizes[:-1]:
+            offs.append(offs[-1] + (sz + 255) // 256 * 256)
+        h2d = offs[-1] + sizes[-1]
+        host = torch.empty(h2d, dtype=torch.uint8).pin_memory()
+        for t, off, sz in zip(srcs, offs, sizes):
+            host[off:off + sz].copy_(t.view(-1).view(torch.uint8))
+        dev_in = [torch.empty(h2d, dtype=torch.uint8, device="cuda") for _ in range(2)]
+        views = [[buf[off:off + sz].view(t.dtype).view(t.shape) for t, off, sz in zip(srcs, offs, sizes)]
+                 for buf in dev_in]
+        o = [torch.empty(N, HV, V, device="cuda") for _ in range(2)]
+        o_host = [torch.empty(N, HV, V).pin_memory() for _ in range(2)]
+        d2h = o[0].numel() * 4
         status = torch.zeros(1, dtype=torch.int32, device="cuda")
-        stream = torch.cuda.Stream()
-        h2d = sum(t.numel() * t.element_size() for t in host.values())
-        d2h = o.numel() * 4
+        s_in, s_k, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
+        ev_in = [torch.cuda.Event() for _ in range(2)]
+        ev_k = [torch.cuda.Event() for _ in range(2)]
+        ev_out = [torch.cuda.Event() for _ in range(2)]
 
-        def one(i):
-            for n_, t in host.items():
-                dev[n_].copy_(t, non_blocking=True)
-            lib32.kda_decode_step(pools[i % R], dev["init_slot"], dev["q"], dev["k"], dev["v"],
-                                  dev["a"], dev["b"], o, status, stream=stream)
-            o_host.copy_(o, non_blocking=True)
+        def one(i, first=False):
+            b_ = i & 1
+            if not first:
+                s_in.wait_event(ev_k[b_])    # the kernel two steps back has read these inputs
+            with torch.cuda.stream(s_in):
+                dev_in[b_].copy_(host, non_blocking=True)
+            ev_in[b_].record(s_in)
+            s_k.wait_event(ev_in[b_])
+            if not first:
+                s_k.wait_event(ev_out[b_])   # o[b] was read back two steps ago
+            sl, q_, k_, v_, a_, bb = views[b_]
+            lib32.kda_decode_step(pools[i % R], sl, q_, k_, v_, a_, bb, o[b_], status, stream=s_k)
+            ev_k[b_].record(s_k)
+            s_out.wait_event(ev_k[b_])
+            with torch.cuda.stream(s_out):
+                o_host[b_].copy_(o[b_], non_blocking=True)
+            ev_out[b_].record(s_out)
 
-        with torch.cuda.stream(stream):
-            for i in range(max(3, args.warmup // 10)):
-                one(i)
+        for i in range(max(3, args.warmup // 10)):
+            one(i)
         torch.cuda.synchronize()
+        group = 50
+        graph = None
+        try:
+            g_ = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g_, stream=s_in):
+                s_k.wait_stream(s_in)
+                s_out.wait_stream(s_in)
+                for i in range(group):
+                    one(i, first=i < 2)
+                s_in.wait_stream(s_k)
+                s_in.wait_stream(s_out)
+            for _ in range(3):
+                g_.replay()
+            torch.cuda.synchronize()
+            graph = g_
+        except Exception:
+            torch.cuda.synchronize()
         if dist is not None:
             dist.barrier()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        n_e2e = min(steps, 2000)
-        with torch.cuda.stream(stream):
-            e0.record(stream)
+        n_e2e = min(steps, 2000) // group * group or group
+        e0.record(s_in)
+        if graph is not None:
+            with torch.cuda.stream(s_in):
+                for _ in range(n_e2e // group):
+                    graph.replay()
+        else:
             for i in range(n_e2e):
                 one(i)
-            e1.record(stream)
+            s_in.wait_event(ev_out[0])
+            s_in.wait_event(ev_out[1])
+        e1.record(s_in)
         torch.cuda.synchronize()
+        if int(status.item()) != 0:
+            raise RuntimeError(f"device status {int(status.item())}")
         ms = e0.elapsed_time(e1)
-        return dict(us_per_step=ms * 1e3 / n_e2e, steps=n_e2e, h2d=h2d, d2h=d2h)
+        return dict(us_per_step=ms * 1e3 / n_e2e, steps=n_e2e, h2d=h2d, d2h=d2h,
+                    mode=f"CUDA graph of {group} steps" if graph is not None else "eager")
 
     def max_over_ranks(x):
         return reduce_max(x, dist, "cuda")
@@ -458,7 +515,10 @@ def main():
             "e2e": None if e2e is None else {
                 "value": round(e2e_gbs, 2), "unit": "GB/s", "us_per_step": round(e2e_us, 3),
                 "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"],
-                "steps": e2e["steps"]},
+                "steps": e2e["steps"],
+                "how": "every step one pinned H2D copy of its packed inputs, the C-ABI decode call, one D2H "
+                       "copy of o; two buffer sets over three streams overlap neighbouring steps; "
+                       + e2e["mode"]},
             "gpu_launches": args.steps,
             "clocks": head["clocks"],
             "extra": extra,
