@@ -28,6 +28,9 @@ namespace kda {
 constexpr int PCH = 16;                                   // tokens per chunk
 constexpr int PCH_FLOATS = 3 * KMAX * PCH + KMAX + 2 * KMAX * PCH;  // workspace floats per (chunk, head)
 constexpr int PVT = 32;                                   // value columns per scan CTA
+#ifndef KDA_PREP_MINB
+#define KDA_PREP_MINB 4   // resident prepare CTAs per SM the register budget must allow
+#endif
 #ifndef KDA_PSCAN_WARPS
 #define KDA_PSCAN_WARPS 8
 #endif
@@ -77,10 +80,11 @@ __device__ __forceinline__ void pab_terms(float (&out)[32], const float (&bk)[PC
 // Pass 1.  grid = (n * max_chunks, hv), 128 threads: thread i owns key
 // channel i (and value column i for the V-side solve).
 template <typename QT>
-__global__ void __launch_bounds__(KMAX) kda_prefill_prep_kernel(const StepParams p, float* __restrict__ ws,
+__global__ void __launch_bounds__(KMAX, KDA_PREP_MINB) kda_prefill_prep_kernel(const StepParams p, float* __restrict__ ws,
                                                                 int max_chunks) {
     __shared__ float vs[PCH][KMAX];        // v of the chunk's tokens
     __shared__ float wsm[PCH][KMAX];       // W, then W'
+    __shared__ float zsm[PCH][KMAX];       // Z = c qhat
     __shared__ float abw[KMAX / 32][256];  // per warp row sums
     __shared__ float ab[256];              // A then B
     __shared__ float nrm[KMAX / 32][32];
@@ -144,7 +148,7 @@ __global__ void __launch_bounds__(KMAX) kda_prefill_prep_kernel(const StepParams
 
     // (2) row tid: khat, qhat, W = c khat, Z = c qhat, Ke, c_(CH-1), and its
     // terms of the 256 row sums of A and B
-    float kh[PCH], qh[PCH], bk[PCH], z[PCH];
+    float kh[PCH], qh[PCH], bk[PCH];
     float c = 1.f;
 #pragma unroll
     for (int t = 0; t < PCH; ++t) {
@@ -153,7 +157,7 @@ __global__ void __launch_bounds__(KMAX) kda_prefill_prep_kernel(const StepParams
         bk[t] = sc[t][0] * kh[t];
         c *= al[t];
         wsm[t][tid] = c * kh[t];
-        z[t] = c * qh[t];
+        zsm[t][tid] = c * qh[t];
     }
     if (tid < p.k) {
         w[PW_C + tid] = c;
@@ -198,7 +202,7 @@ __global__ void __launch_bounds__(KMAX) kda_prefill_prep_kernel(const StepParams
     const int vt = tid / PVT, vc = tid - vt * PVT;
 #pragma unroll
     for (int t = 0; t < PCH; ++t) {
-        float qp = z[t], oi = 0.f;
+        float qp = zsm[t][tid], oi = 0.f;
 #pragma unroll
         for (int s = 0; s <= t; ++s) {
             const float bts = ab[pidx_b(t, s)];
