@@ -198,6 +198,25 @@ void set_pdl(cudaLaunchConfig_t& cfg, cudaLaunchAttribute* attr, uint32_t flags)
     }
 }
 
+// The prefill scan pass with NC value columns per CTA, launched with
+// programmatic dependent launch so that it starts while the first pass drains.
+template <int NC>
+int launch_scan(const kda::StepParams& prm, const float* ws, int64_t heads, int v, cudaStream_t st) {
+    constexpr size_t smem = kda::PrefillScanSmem<NC>::BYTES;
+    auto scan = kda::kda_prefill_scan_kernel<state_t, NC>;
+    int occ = 0, sms = 0;
+    const int rc = occupancy(reinterpret_cast<const void*>(scan), kda::PSCAN_WARPS * 32, smem, &occ, &sms);
+    if (rc != KDA_OK) return rc;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr;
+    cfg.gridDim = dim3((unsigned)(heads * ((v + NC - 1) / NC)), 1, 1);
+    cfg.blockDim = dim3(kda::PSCAN_WARPS * 32, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    set_pdl(cfg, &attr, KDA_LAUNCH_PDL);
+    return cudaLaunchKernelEx(&cfg, scan, prm, ws) == cudaSuccess ? KDA_OK : KDA_ERR_LAUNCH;
+}
+
 template <typename QT, bool FULLK>
 int launch_decode_k(const kda_pool* pool, const kda::StepParams& prm, cudaStream_t stream) {
     constexpr int BV = KDA_DEC_BV, NT = KDA_DEC_NT;
@@ -499,7 +518,7 @@ int kda_prefill_chunked(const kda_pool* pool, const kda_prefill_args* args, void
     prm.mode = kda::MODE_PADDING;
     prm.final_slot = g.final_slot;
     const int max_chunks = (g.max_t + kda::PCH - 1) / kda::PCH;
-    const int vtiles = (pool->v + kda::PVT - 1) / kda::PVT;
+    const int vtiles = (pool->v + 8 - 1) / 8;  // the narrowest scan tiling bounds the grid
     if ((int64_t)g.n * max_chunks > 0x7fffffffLL || (int64_t)g.n * pool->hv * vtiles > 0x7fffffffLL ||
         pool->hv > 65535)
         return KDA_ERR_SHAPE;
@@ -518,20 +537,19 @@ int kda_prefill_chunked(const kda_pool* pool, const kda_prefill_args* args, void
         default: err = cudaLaunchKernelEx(&cfg, kda::kda_prefill_prep_kernel<__nv_bfloat16>, prm, ws, max_chunks); break;
     }
     if (err != cudaSuccess) return KDA_ERR_LAUNCH;
-    constexpr size_t smem = kda::PrefillScanSmem<state_t>::BYTES;
-    auto scan = kda::kda_prefill_scan_kernel<state_t>;
-    int occ = 0, sms = 0;
-    rc = occupancy(reinterpret_cast<const void*>(scan), kda::PSCAN_WARPS * 32, smem, &occ, &sms);
-    if (rc != KDA_OK) return rc;
-    cudaLaunchConfig_t cfg2 = {};
-    cudaLaunchAttribute attr2;
-    cfg2.gridDim = dim3((unsigned)(g.n * pool->hv * vtiles), 1, 1);
-    cfg2.blockDim = dim3(kda::PSCAN_WARPS * 32, 1, 1);
-    cfg2.dynamicSmemBytes = smem;
-    cfg2.stream = st;
-    set_pdl(cfg2, &attr2, KDA_LAUNCH_PDL);  // the scan starts while the first pass drains
-    err = cudaLaunchKernelEx(&cfg2, scan, prm, static_cast<const float*>(ws));
-    return err == cudaSuccess ? KDA_OK : KDA_ERR_LAUNCH;
+    // the widest scan tiling (32, 16 or 8 value columns per CTA) whose grid
+    // still covers the SMs: few long prompts get narrower tiles and more CTAs
+    int sms = 0, dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return KDA_ERR_LAUNCH;
+    const int64_t heads = (int64_t)g.n * pool->hv;
+    const int nc = heads * ((pool->v + 31) / 32) >= sms ? 32 : heads * ((pool->v + 15) / 16) >= sms ? 16 : 8;
+    switch (nc) {
+        case 32: return launch_scan<32>(prm, ws, heads, pool->v, st);
+        case 16: return launch_scan<16>(prm, ws, heads, pool->v, st);
+        default: return launch_scan<8>(prm, ws, heads, pool->v, st);
+    }
 }
 
 int kda_prefill_chunked_noalloc(const kda_pool* pool, const kda_prefill_args* args, int32_t* dev_status,

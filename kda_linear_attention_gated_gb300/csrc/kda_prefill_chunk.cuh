@@ -220,32 +220,42 @@ __global__ void __launch_bounds__(KMAX, KDA_PREP_MINB) kda_prefill_prep_kernel(c
     }
 }
 
-// Pass 2.  grid = n * hv * ceil(v / 32) CTAs of 256 threads: warp w owns rows
-// 16 w .. 16 w + 15 of the state tile, lane l its value column.
-template <typename ST>
+// Pass 2.  grid = n * hv * ceil(v / NC) CTAs of PSCAN_WARPS warps, NC = 32, 16
+// or 8 value columns per CTA (narrower tiles when few requests leave SMs idle).
+// Warp w owns rows 16 w .. 16 w + 15 of the state tile; lane l = rq NC + cc
+// takes column cc and rows 16 w + rq RPT + i (i < RPT = 16 NC / 32).
+template <int NC>
 struct PrefillScanSmem {
     static constexpr uint32_t OPS = (3 * KMAX * PCH + KMAX + 2 * PCH * PVT) * 4;  // one chunk's operands
     static constexpr uint32_t BUF = (OPS + 127u) & ~127u;
-    static constexpr uint32_t RED = PSCAN_WARPS * 2 * PCH * 32 * 4;               // partial sums
-    static constexpr uint32_t BYTES = 2 * BUF + RED + 2 * PCH * 32 * 4 + 16;
+    static constexpr uint32_t RED = PSCAN_WARPS * 2 * PCH * NC * 4;               // partial sums
+    static constexpr uint32_t BYTES = 2 * BUF + RED + 2 * PCH * NC * 4 + 16;
 };
 
-template <typename ST>
+template <typename ST, int NC>
 __global__ void __launch_bounds__(PSCAN_WARPS * 32) kda_prefill_scan_kernel(const StepParams p,
                                                                            const float* __restrict__ ws) {
-    using SM = PrefillScanSmem<ST>;
-    extern __shared__ __align__(128) uint8_t smem[];
-    float* red = reinterpret_cast<float*>(smem + 2 * SM::BUF);  // [warp][32 vectors][32 lanes]
-    float* fin = red + PSCAN_WARPS * 2 * PCH * 32;               // [32 vectors][32 lanes]
-    uint64_t* bars = reinterpret_cast<uint64_t*>(fin + 2 * PCH * 32);  // two chunk-operand barriers
+    static_assert(NC == 32 || NC == 16 || NC == 8, "columns per scan CTA");
+    constexpr int NRQ = 32 / NC;                 // lanes sharing a column
+    constexpr int RPT = PSCAN_ROWS / NRQ;        // rows per thread
+    constexpr int KEEP = 2 * PCH / NRQ;          // partial sums a lane keeps after the reduce-scatter
+    static_assert(PSCAN_ROWS % NRQ == 0, "row split");
+    using SM = PrefillScanSmem<NC>;
+    extern __shared__ __align__(1024) uint8_t smem[];
+    float* red = reinterpret_cast<float*>(smem + 2 * SM::BUF);  // [warp][32 vectors][NC]
+    float* fin = red + PSCAN_WARPS * 2 * PCH * NC;               // [32 vectors][NC]
+    uint64_t* bars = reinterpret_cast<uint64_t*>(fin + 2 * PCH * NC);  // two chunk-operand barriers
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int vtiles = (p.v + PVT - 1) / PVT;
+    const int rq = lane / NC, cc = lane - rq * NC;
+    const int vtiles = (p.v + NC - 1) / NC;
     const int tile = (int)blockIdx.x;
     const int r = tile / (p.hv * vtiles);
     const int rem = tile - r * p.hv * vtiles;
     const int h = rem / vtiles, cb = rem - h * vtiles;
-    const int col = cb * PVT + lane;
+    const int col = cb * NC + cc;
+    const int c32 = (cb * NC) / PVT;             // the 32-column workspace tile holding this CTA's columns
+    const int cw = col - c32 * PVT;              // column inside it
     const bool col_ok = col < p.v;
     cudaTriggerProgrammaticLaunchCompletion();
     cudaGridDependencySynchronize();
@@ -263,23 +273,24 @@ __global__ void __launch_bounds__(PSCAN_WARPS * 32) kda_prefill_scan_kernel(cons
         return;
     }
     if (slot < 0) {  // padding: outputs zero, nothing read or stored
-        for (int e = tid; e < Tn * PVT; e += PSCAN_WARPS * 32) {
-            const int c2 = cb * PVT + (e % PVT);
-            if (c2 < p.v) p.o[((int64_t)(tb + e / PVT) * p.hv + h) * p.v + c2] = 0.f;
+        for (int e = tid; e < Tn * NC; e += PSCAN_WARPS * 32) {
+            const int c2 = cb * NC + (e % NC);
+            if (c2 < p.v) p.o[((int64_t)(tb + e / NC) * p.hv + h) * p.v + c2] = 0.f;
         }
         return;
     }
     if (Tn == 0) return;
     const int nch = (Tn + PCH - 1) / PCH;
+    const int row0 = warp * PSCAN_ROWS + rq * RPT;  // this thread's rows: row0 .. row0 + RPT - 1
 
-    // the state tile, fp32 in registers: rows 16 warp + rr, column col
-    float S[PSCAN_ROWS];
+    // the state tile, fp32 in registers
+    float S[RPT];
     const bool rst = p.reset != nullptr && p.reset[r] != 0;
     const ST* src = static_cast<const ST*>(p.pool) + state_at(p, slot, h);
 #pragma unroll
-    for (int rr = 0; rr < PSCAN_ROWS; ++rr) {
-        const int row = warp * PSCAN_ROWS + rr;
-        S[rr] = (!rst && col_ok && row < p.k) ? to_f32(src[(int64_t)row * p.v + col]) : 0.f;
+    for (int i = 0; i < RPT; ++i) {
+        const int row = row0 + i;
+        S[i] = (!rst && col_ok && row < p.k) ? to_f32(src[(int64_t)row * p.v + col]) : 0.f;
     }
 
     // chunk operands of chunk j -> buffer j % 2, one barrier per buffer
@@ -293,8 +304,8 @@ __global__ void __launch_bounds__(PSCAN_WARPS * 32) kda_prefill_scan_kernel(cons
         bulk_load(buf + KMAX * PCH * 4, w + PW_QT, kb, bar);
         bulk_load(buf + 2 * KMAX * PCH * 4, w + PW_KT, kb, bar);
         bulk_load(buf + 3 * KMAX * PCH * 4, w + PW_C, (uint32_t)p.k * 4, bar);
-        bulk_load(buf + (3 * KMAX * PCH + KMAX) * 4, w + PW_U + cb * PCH * PVT, tb2, bar);
-        bulk_load(buf + (3 * KMAX * PCH + KMAX + PCH * PVT) * 4, w + PW_OI + cb * PCH * PVT, tb2, bar);
+        bulk_load(buf + (3 * KMAX * PCH + KMAX) * 4, w + PW_U + c32 * PCH * PVT, tb2, bar);
+        bulk_load(buf + (3 * KMAX * PCH + KMAX + PCH * PVT) * 4, w + PW_OI + c32 * PCH * PVT, tb2, bar);
     };
     if (tid == 0) {
         mbar_init(bars, 1);
@@ -324,62 +335,73 @@ __global__ void __launch_bounds__(PSCAN_WARPS * 32) kda_prefill_scan_kernel(cons
         const float* U = CC + KMAX;
         const float* OI = U + PCH * PVT;
 
-        // partial sums over this warp's rows: pw_t = sum_i W'_ti S_i, pq_t = sum_i Q'_ti S_i
-        float pw[PCH], pq[PCH];
+        // partial sums over this thread's rows: v_t = sum_i W'_ti S_i (t < 16),
+        // v_(16+t) = sum_i Q'_ti S_i
+        float vals[2 * PCH];
 #pragma unroll
-        for (int t = 0; t < PCH; ++t) { pw[t] = 0.f; pq[t] = 0.f; }
+        for (int t = 0; t < 2 * PCH; ++t) vals[t] = 0.f;
 #pragma unroll
-        for (int rr = 0; rr < PSCAN_ROWS; ++rr) {
-            const int row = warp * PSCAN_ROWS + rr;
+        for (int i = 0; i < RPT; ++i) {
+            const int row = row0 + i;
             if (row < p.k) {
                 const float4* w4 = reinterpret_cast<const float4*>(WT + row * PCH);
                 const float4* q4 = reinterpret_cast<const float4*>(QT_ + row * PCH);
 #pragma unroll
                 for (int g = 0; g < PCH / 4; ++g) {
                     const float4 a = w4[g], b = q4[g];
-                    pw[4 * g] = fmaf(a.x, S[rr], pw[4 * g]);
-                    pw[4 * g + 1] = fmaf(a.y, S[rr], pw[4 * g + 1]);
-                    pw[4 * g + 2] = fmaf(a.z, S[rr], pw[4 * g + 2]);
-                    pw[4 * g + 3] = fmaf(a.w, S[rr], pw[4 * g + 3]);
-                    pq[4 * g] = fmaf(b.x, S[rr], pq[4 * g]);
-                    pq[4 * g + 1] = fmaf(b.y, S[rr], pq[4 * g + 1]);
-                    pq[4 * g + 2] = fmaf(b.z, S[rr], pq[4 * g + 2]);
-                    pq[4 * g + 3] = fmaf(b.w, S[rr], pq[4 * g + 3]);
+                    vals[4 * g] = fmaf(a.x, S[i], vals[4 * g]);
+                    vals[4 * g + 1] = fmaf(a.y, S[i], vals[4 * g + 1]);
+                    vals[4 * g + 2] = fmaf(a.z, S[i], vals[4 * g + 2]);
+                    vals[4 * g + 3] = fmaf(a.w, S[i], vals[4 * g + 3]);
+                    vals[PCH + 4 * g] = fmaf(b.x, S[i], vals[PCH + 4 * g]);
+                    vals[PCH + 4 * g + 1] = fmaf(b.y, S[i], vals[PCH + 4 * g + 1]);
+                    vals[PCH + 4 * g + 2] = fmaf(b.z, S[i], vals[PCH + 4 * g + 2]);
+                    vals[PCH + 4 * g + 3] = fmaf(b.w, S[i], vals[PCH + 4 * g + 3]);
                 }
             }
         }
+        // over the NRQ lanes sharing column cc: a reduce-scatter, each keeps KEEP sums
+        int kbase = 0;
 #pragma unroll
-        for (int t = 0; t < PCH; ++t) {
-            red[(warp * 2 * PCH + t) * 32 + lane] = pw[t];
-            red[(warp * 2 * PCH + PCH + t) * 32 + lane] = pq[t];
+        for (int m = 16, cnt = 2 * PCH; m >= NC; m >>= 1, cnt >>= 1) {
+            const bool upper = (lane & m) != 0;
+#pragma unroll
+            for (int e = 0; e < cnt / 2; ++e) {
+                const float send = upper ? vals[e] : vals[e + cnt / 2];
+                const float keep = upper ? vals[e + cnt / 2] : vals[e];
+                vals[e] = keep + __shfl_xor_sync(0xffffffffu, send, m);
+            }
+            kbase += upper ? cnt / 2 : 0;
         }
+#pragma unroll
+        for (int e = 0; e < KEEP; ++e) red[(warp * 2 * PCH + kbase + e) * NC + cc] = vals[e];
         __syncthreads();
-        // warp w finishes vectors 4 w .. 4 w + 3 of the 32 (16 W', 16 Q') for every column
+        // the sums over the warps: 32 vectors x NC columns
+        for (int e = tid; e < 2 * PCH * NC; e += PSCAN_WARPS * 32) {
+            float sum = 0.f;
 #pragma unroll
-        for (int e = 0; e < 2 * PCH / PSCAN_WARPS; ++e) {
-            const int vec = warp * (2 * PCH / PSCAN_WARPS) + e;
-            float s = 0.f;
-#pragma unroll
-            for (int w2 = 0; w2 < PSCAN_WARPS; ++w2) s += red[(w2 * 2 * PCH + vec) * 32 + lane];
-            fin[vec * 32 + lane] = s;
+            for (int w2 = 0; w2 < PSCAN_WARPS; ++w2) sum += red[w2 * 2 * PCH * NC + e];
+            fin[e] = sum;
         }
         __syncthreads();
         // d_t = U_t - (W' S)_t for this column; outputs O_t = (Q' S)_t + O_intra_t
         float d[PCH];
 #pragma unroll
-        for (int t = 0; t < PCH; ++t) d[t] = U[t * PVT + lane] - fin[t * 32 + lane];
+        for (int t = 0; t < PCH; ++t) d[t] = U[t * PVT + cw] - fin[t * NC + cc];
         const int cl = min(PCH, Tn - j * PCH);
-        if (warp == 0 && col_ok)
-            for (int t = 0; t < cl; ++t)
-                p.o[((int64_t)(tb + j * PCH + t) * p.hv + h) * p.v + col] = fin[(PCH + t) * 32 + lane] +
-                                                                           OI[t * PVT + lane];
+        for (int e = tid; e < cl * NC; e += PSCAN_WARPS * 32) {
+            const int t = e / NC, c2 = e - t * NC, gcol = cb * NC + c2;
+            if (gcol < p.v)
+                p.o[((int64_t)(tb + j * PCH + t) * p.hv + h) * p.v + gcol] =
+                    fin[(PCH + t) * NC + c2] + OI[t * PVT + gcol - c32 * PVT];
+        }
         // S <- c S + Ke^T D
 #pragma unroll
-        for (int rr = 0; rr < PSCAN_ROWS; ++rr) {
-            const int row = warp * PSCAN_ROWS + rr;
+        for (int i = 0; i < RPT; ++i) {
+            const int row = row0 + i;
             if (row < p.k) {
                 const float4* k4 = reinterpret_cast<const float4*>(KT + row * PCH);
-                float x = CC[row] * S[rr];
+                float x = CC[row] * S[i];
 #pragma unroll
                 for (int g = 0; g < PCH / 4; ++g) {
                     const float4 kk = k4[g];
@@ -388,7 +410,7 @@ __global__ void __launch_bounds__(PSCAN_WARPS * 32) kda_prefill_scan_kernel(cons
                     x = fmaf(kk.z, d[4 * g + 2], x);
                     x = fmaf(kk.w, d[4 * g + 3], x);
                 }
-                S[rr] = x;
+                S[i] = x;
             }
         }
         // every thread is done with this buffer and with red/fin before the
@@ -407,11 +429,11 @@ __global__ void __launch_bounds__(PSCAN_WARPS * 32) kda_prefill_scan_kernel(cons
     if (fin_slot >= 0 && col_ok) {
         ST* dst = static_cast<ST*>(p.pool) + state_at(p, fin_slot, h);
 #pragma unroll
-        for (int rr = 0; rr < PSCAN_ROWS; ++rr) {
-            const int row = warp * PSCAN_ROWS + rr;
+        for (int i = 0; i < RPT; ++i) {
+            const int row = row0 + i;
             if (row < p.k) {
-                if constexpr (sizeof(ST) == 4) dst[(int64_t)row * p.v + col] = S[rr];
-                else dst[(int64_t)row * p.v + col] = __float2half_rn(S[rr]);
+                if constexpr (sizeof(ST) == 4) dst[(int64_t)row * p.v + col] = S[i];
+                else dst[(int64_t)row * p.v + col] = __float2half_rn(S[i]);
             }
         }
     }
