@@ -62,11 +62,22 @@ __device__ __forceinline__ float softplus_f(float x) {
     return x > 0.f ? x + log1pf(expf(-x)) : log1pf(expf(x));
 }
 
+// sigmoid(-x) = 1 / (1 + e^x): the fast reciprocal refined by one
+// Newton-Raphson step, r <- r + r (1 - y r), which brings its error to about
+// half an ulp at a fraction of the cost of the correctly rounded reciprocal.
+// x is capped at 80 (1 + e^80 < 2^126, inside the fast reciprocal's range),
+// which changes the result by less than 2e-35; a NaN passes through.
+__device__ __forceinline__ float sigmoid_neg(float x) {
+    const float y = 1.0f + expf(x > 80.f ? 80.f : x);
+    const float r = __fdividef(1.0f, y);
+    return fmaf(r, fmaf(-y, r, 1.0f), r);
+}
+
 // The per-key-channel decay alpha_i of one row.  Plain gate: exp(-softplus(a))
 // = 1 / (1 + e^a) (one exponential, no logarithm).  Learned scale (the KDA
 // layer's A_log, dt_bias): exp(-exp(A_log) softplus(a + dt_bias)).
 __device__ __forceinline__ float gate_alpha(float a, bool scaled, float scale, float bias) {
-    return scaled ? expf(-scale * softplus_f(a + bias)) : __frcp_rn(1.0f + expf(a));
+    return scaled ? expf(-scale * softplus_f(a + bias)) : sigmoid_neg(a);
 }
 
 constexpr uint32_t LAUNCH_PDL = 1u;               // KDA_LAUNCH_PDL in kda.h

@@ -212,7 +212,7 @@ kda_decode_kernel(const __grid_constant__ CUtensorMap tmap, const StepParams p) 
     }
     const float rk = __frsqrt_rn(kk2 + L2_EPS);
     const float rq = __frsqrt_rn(qq2 + L2_EPS);
-    const float beta = __frcp_rn(1.0f + expf(-b));  // sigmoid(b)
+    const float beta = sigmoid_neg(-b);  // sigmoid(b)
     const float bqk = beta * (kq * rk * rq);         // beta (qhat . khat)
     // Per row: w = alpha khat and z = alpha qhat fold the decay into the two
     // reductions (u = sum_i S_ij w_i, p = sum_i S_ij z_i); alpha and beta khat

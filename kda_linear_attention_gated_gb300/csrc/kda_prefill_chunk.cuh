@@ -139,7 +139,7 @@ __global__ void __launch_bounds__(KMAX, KDA_PREP_MINB) kda_prefill_prep_kernel(c
             kk2 += nrm[w2][2 * tid];
             qq2 += nrm[w2][2 * tid + 1];
         }
-        const float beta = tid < cl ? __frcp_rn(1.0f + expf(-__ldg(p.b + (int64_t)(t0 + tid) * p.hv + h))) : 0.f;
+        const float beta = tid < cl ? sigmoid_neg(-__ldg(p.b + (int64_t)(t0 + tid) * p.hv + h)) : 0.f;
         sc[tid][0] = beta;
         sc[tid][1] = __frsqrt_rn(kk2 + L2_EPS);
         sc[tid][2] = __frsqrt_rn(qq2 + L2_EPS);

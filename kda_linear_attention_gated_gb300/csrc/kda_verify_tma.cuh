@@ -3,7 +3,8 @@
 // Tile: one (request n, value head h, block of BV state columns) with all K
 // rows; BV * sizeof(state) is 64 or 128 bytes, one warp per 16-byte column
 // chunk.  The state tile is TMA-loaded once from init_slot[n] (or taken as
-// zero on reset); lane l of warp w then carries rows l, l+32, l+64, l+96 of
+// zero on reset); the per-token inputs are plain coalesced loads, thread r
+// taking row r of q, k and a and column r of the v slice.  Lane l of warp w then carries rows l, l+32, l+64, l+96 of
 // chunk w in fp32 registers through the T tokens without rounding.  After each
 // token the state, rounded to the pool's dtype, is written to a swizzled
 // shared-memory staging tile and from there to that token's snapshot slot
@@ -31,6 +32,10 @@
 // reduction waits on the previous token), each column solves its T x T
 // lower-triangular system for d by forward substitution, and the snapshots
 // then need only S_t = alpha_t S_{t-1} + (beta_t khat_t) d_t^T per element.
+// Every sum is taken over the raw k and q: khat = k / |k| and the norms, like
+// beta, are per-token scalars, so they multiply the 64 sums A and B, the
+// column sums and d after the reductions.  The gates, the terms of A and B
+// and the squared norms then come from one pass over the rows.
 // It is the token-by-token recurrence with its sums taken in another order;
 // the products P are formed by multiplication, never division, so alpha = 0
 // stays exact.
@@ -60,14 +65,10 @@ struct VerifyShape {
     static constexpr int NA = TC * (TC - 1) / 2, NB = TC * (TC + 1) / 2;  // 28 + 36 = 64 sums
     static constexpr int G = 16 / VEC;        // tokens per group of column sums (2 G VEC = 32 values)
     static constexpr uint32_t TILE_BYTES = (KMAX * ROWBYTES + 1023u) & ~1023u;
-    // per token inputs: q row, k row (QES-byte elements), a row (fp32), v slice
-    static constexpr uint32_t IN_Q = 0, IN_K = KMAX * QES, IN_A = 2 * KMAX * QES;
-    static constexpr uint32_t IN_V = IN_A + KMAX * 4, IN_TOK = (IN_V + BV * QES + 15u) & ~15u;
-    // per token gates: float4 {c khat, c qhat, alpha, beta khat} per row, then v (fp32)
+    // per token gates: float4 {c k, c q, alpha, k} per row (raw k and q), then v (fp32)
     static constexpr uint32_t G_V = KMAX * 16, G_TOK = G_V + BV * 4;
-    static constexpr uint32_t IN_BYTES = TC * IN_TOK, GATE_BYTES = TC * G_TOK;
-    // the gates overlay the inputs, which are all read into registers first
-    static constexpr uint32_t WORK_BYTES = IN_BYTES > GATE_BYTES ? IN_BYTES : GATE_BYTES;
+    static constexpr uint32_t GATE_BYTES = TC * G_TOK;
+    static constexpr uint32_t WORK_BYTES = GATE_BYTES;
     // staging buffers for the snapshot stores (the state tile's area is the first)
     static constexpr int NSTAGE = 3;
     // norms [TC][NW][2] and b [TC], scalars [TC] float4, A and B per warp
@@ -82,7 +83,7 @@ struct VerifyShape {
     static_assert(NA + NB == 64 && 2 * G * VEC == 32 && TC % G == 0 && TC == 8, "chunk shape");
     static_assert(BV <= NT, "one thread per column in the solve");
     static_assert(NSTAGE >= 2, "staging buffers");
-    static_assert(IN_K % 16 == 0 && IN_A % 16 == 0 && IN_V % 16 == 0 && G_TOK % 16 == 0 &&
+    static_assert(G_TOK % 16 == 0 &&
                   WORK_BYTES % 16 == 0 && RED_RES % 16 == 0 && RED_D % 16 == 0, "layout");
 };
 
@@ -125,19 +126,17 @@ kda_verify_kernel(const __grid_constant__ CUtensorMap tmap, const StepParams p) 
     constexpr int VEC = SH::VEC, NW = SH::NW, ROWS = SH::ROWS, TC = SH::TC, G = SH::G;
 
     extern __shared__ __align__(1024) uint8_t smem[];
-    uint8_t* ins = smem + SH::NSTAGE * SH::TILE_BYTES;
-    uint8_t* gts = ins;  // overlays the inputs once they are in registers
-    uint8_t* redb = ins + SH::WORK_BYTES;
+    uint8_t* gts = smem + SH::NSTAGE * SH::TILE_BYTES;
+    uint8_t* redb = gts + SH::WORK_BYTES;
     float* nrm = reinterpret_cast<float*>(redb + SH::RED_NORM);    // [TC][NW][2]
     float* bsm = reinterpret_cast<float*>(redb + SH::RED_B);       // [TC]
-    float4* scal = reinterpret_cast<float4*>(redb + SH::RED_SCAL); // [TC] {beta, rk, rq, -}
+    float4* scal = reinterpret_cast<float4*>(redb + SH::RED_SCAL); // [TC] {beta, 1/|k|, 1/|q|, -}
     float* abw = reinterpret_cast<float*>(redb + SH::RED_ABW);     // [NW][64]
     float* ab = reinterpret_cast<float*>(redb + SH::RED_AB);       // [64]
     float* res = reinterpret_cast<float*>(redb + SH::RED_RES);     // [TC][2][BV]
     float* dsm = reinterpret_cast<float*>(redb + SH::RED_D);       // [TC][BV]
     int32_t* snaps = reinterpret_cast<int32_t*>(redb + SH::RED_SNAP);  // [TC]
     uint64_t* bar_st = reinterpret_cast<uint64_t*>(redb + SH::RED_BYTES);
-    uint64_t* bar_in = bar_st + 1;
     const uint32_t tile_base = smem_u32(smem);
     const uint32_t gate_base = smem_u32(gts);
 
@@ -150,7 +149,6 @@ kda_verify_kernel(const __grid_constant__ CUtensorMap tmap, const StepParams p) 
     const int n = r / p.hv;
     const int h = r - n * p.hv;
     const int T = p.t;  // most tokens a request may have
-    const int qes = (int)sizeof(QT);
     const int hq = h / (p.hv / p.hqk);  // q/k head of value head h
     const int vcols = min(BV, p.v - cb * BV);
     if ((tile_base & 1023u) != 0) {  // the swizzled tile needs a 1024-byte aligned base
@@ -158,43 +156,39 @@ kda_verify_kernel(const __grid_constant__ CUtensorMap tmap, const StepParams p) 
         return;
     }
 
-    const uint32_t qk_bytes = (uint32_t)p.k * qes;
-    const uint32_t v_bytes = (uint32_t)vcols * qes;
     int tb = n * T, Tn = T;  // request n's packed tokens tb .. tb + Tn - 1 (set below)
-    // inputs of tokens t0 .. t0 + tc - 1 into the work area: lane 0 of warp 0
-    // arms the barrier with the whole byte count, then warp 0 issues the 4 tc
-    // copies (none of them depends on a slot id)
-    auto issue_inputs = [&](int t0, int tc) {
-        if (lane == 0)
-            mbar_arrive_expect_tx(bar_in, (uint32_t)tc * (2 * qk_bytes + (uint32_t)p.k * 4 + v_bytes));
-        __syncwarp();
-        for (int c = lane; c < 4 * tc; c += 32) {
-            const int j = c >> 2, kind = c & 3;
-            const int64_t tok = (int64_t)tb + t0 + j;
-            const int64_t rt = tok * p.hv + h, rq = tok * p.hqk + hq;
-            uint8_t* in = ins + j * SH::IN_TOK;
-            if (kind == 0)
-                bulk_load(in + SH::IN_Q, static_cast<const char*>(p.q) + rq * qk_bytes, qk_bytes, bar_in);
-            else if (kind == 1)
-                bulk_load(in + SH::IN_K, static_cast<const char*>(p.kk) + rq * qk_bytes, qk_bytes, bar_in);
-            else if (kind == 2)
-                bulk_load(in + SH::IN_A, p.a + rt * p.k, (uint32_t)p.k * 4, bar_in);
-            else
-                bulk_load(in + SH::IN_V, static_cast<const char*>(p.vv) + (rt * p.v + (int64_t)cb * BV) * qes,
-                          v_bytes, bar_in);
+    // Row tid of k, q and a, and column tid of this tile's v slice, of tokens
+    // t0 .. t0 + tc - 1 (tc >= 1), straight into registers: coalesced loads,
+    // none of which depends on a slot id.  Every load is unconditional, from
+    // an address clamped into the request's last token, row 0 or column 0,
+    // so that all of them are in flight at once; the values past tc or the
+    // row or column count are zeroed where they are used.
+    QT kraw[TC], qraw[TC], vraw[TC];
+    float araw[TC];
+    auto load_inputs = [&](int t0, int tc) {
+        const QT* qp = static_cast<const QT*>(p.q);
+        const QT* kp = static_cast<const QT*>(p.kk);
+        const QT* vp = static_cast<const QT*>(p.vv);
+        const int row = tid < p.k ? tid : 0, col = tid < vcols ? tid : 0;
+#pragma unroll
+        for (int j = 0; j < TC; ++j) {
+            const int64_t tok = (int64_t)tb + t0 + min(j, tc - 1);
+            const int64_t rq = (tok * p.hqk + hq) * p.k + row, rt = tok * p.hv + h;
+            kraw[j] = kp[rq];
+            qraw[j] = qp[rq];
+            araw[j] = __ldg(p.a + rt * p.k + row);
+            vraw[j] = vp[rt * p.v + (int64_t)cb * BV + col];
         }
     };
 
     // Programmatic dependent launch: as in the decode kernel, only the slot ids
     // and the state may be read before the previous kernel completes, and only
     // when the caller vouches for it (KDA_LAUNCH_PDL_EARLY_STATE).  The first
-    // chunk's inputs are requested as soon as that allows, before the slot ids
-    // are even read.
+    // chunk's inputs are requested as soon as that allows.
     cudaTriggerProgrammaticLaunchCompletion();
     const bool early = (p.flags & LAUNCH_PDL_EARLY_STATE) != 0;
     if (tid == 0) {
         mbar_init(bar_st, 1);
-        mbar_init(bar_in, 1);
         fence_mbar_init();
     }
     if (!early) cudaGridDependencySynchronize();
@@ -216,7 +210,10 @@ kda_verify_kernel(const __grid_constant__ CUtensorMap tmap, const StepParams p) 
     const int32_t snap0 = !final_mode && arg_ok && lane < Tn ? p.snap_slot[(int64_t)n * p.snap_stride + lane] : 0;
     const int32_t fin = final_mode ? p.final_slot[n] : -1;
     const bool issued = arg_ok && Tn > 0;  // the first chunk's inputs are requested
-    if (!early && warp == 0 && issued) issue_inputs(0, min(TC, Tn));
+    // The first chunk's inputs: in the prologue, under the slot-id loads,
+    // when the registers allow it (128-thread tiles); else with the chunk.
+    constexpr bool PRO_INPUTS = SH::NT <= 128;
+    if (PRO_INPUTS && !early && issued) load_inputs(0, min(TC, Tn));
     const bool padding = (p.mode & MODE_PADDING) != 0;
     auto slot_bad = [&](int32_t s) { return s >= p.num_slots || (s < 0 && !padding); };
     bool bad = !arg_ok || slot_bad(slot) || slot_bad(snap0) || fin >= p.num_slots;
@@ -232,16 +229,13 @@ kda_verify_kernel(const __grid_constant__ CUtensorMap tmap, const StepParams p) 
     }
     if (early) {
         cudaGridDependencySynchronize();
-        if (warp == 0 && issued) issue_inputs(0, min(TC, Tn));
+        if (PRO_INPUTS && issued) load_inputs(0, min(TC, Tn));
     }
     if (bad || pad || Tn == 0) {
         if (pad)  // padding: this tile's outputs of every token are zero
             for (int e = tid; e < Tn * vcols; e += SH::NT)
                 p.o[((int64_t)(tb + e / vcols) * p.hv + h) * p.v + cb * BV + e % vcols] = 0.f;
-        if (tid == 0) {
-            if (bad) atomicCAS(p.status, 0, arg_ok ? STATUS_SLOT_RANGE : STATUS_ARG);
-            if (issued) mbar_wait(bar_in, 0);  // bounded: the input copies land before the CTA exits
-        }
+        if (tid == 0 && bad) atomicCAS(p.status, 0, arg_ok ? STATUS_SLOT_RANGE : STATUS_ARG);
         return;  // uniform; no state copy was issued
     }
     __syncthreads();  // barriers initialised
@@ -249,37 +243,52 @@ kda_verify_kernel(const __grid_constant__ CUtensorMap tmap, const StepParams p) 
     float x[ROWS][VEC];
     bool state_in = false;
     bool alive = true;
-    int in_phase = 0;
     const bool scaled = p.a_log != nullptr;
     const float gscale = scaled ? expf(__ldg(p.a_log + h)) : 1.f;
     const float gbias = p.dt_bias != nullptr && tid < p.k ? __ldg(p.dt_bias + (int64_t)h * p.k + tid) : 0.f;
     for (int t0 = 0; t0 < Tn; t0 += TC) {
         const int tc = min(TC, Tn - t0);
-        if (t0 > 0 && warp == 0) issue_inputs(t0, tc);
+        if (t0 > 0 || !PRO_INPUTS) load_inputs(t0, tc);
         if (tid < tc) {
             bsm[tid] = __ldg(p.b + ((int64_t)tb + t0 + tid) * p.hv + h);
             snaps[tid] = final_mode ? -1 : p.snap_slot[(int64_t)n * p.snap_stride + t0 + tid];
         }
-        const bool ok_in = mbar_wait(bar_in, in_phase);
-        in_phase ^= 1;
 
-        // (1) row tid of every token: k, q, alpha; the squared norms of k and q
-        // per warp (one reduce-scatter of 16 values: lane pair 2m holds value m)
-        float kt[TC], qt[TC], at[TC], vv[TC];
-#pragma unroll
-        for (int j = 0; j < TC; ++j) {
-            kt[j] = 0.f; qt[j] = 0.f; at[j] = 0.f; vv[j] = 0.f;
-            if (ok_in && j < tc) {
-                const uint8_t* in = ins + j * SH::IN_TOK;
-                if (tid < p.k) {
-                    kt[j] = to_f32(reinterpret_cast<const QT*>(in + SH::IN_K)[tid]);
-                    qt[j] = to_f32(reinterpret_cast<const QT*>(in + SH::IN_Q)[tid]);
-                    at[j] = gate_alpha(reinterpret_cast<const float*>(in + SH::IN_A)[tid], scaled, gscale, gbias);
-                }
-                if (tid < vcols) vv[j] = to_f32(reinterpret_cast<const QT*>(in + SH::IN_V)[tid]);
-            }
-        }
+        // (1) row tid of every token, in one pass: alpha; the gates
+        // {c k, c q, alpha, k} and v into shared memory; this row's terms of
+        // the 64 raw sums A and B and of the squared norms, summed over the
+        // warp's rows (reduce-scatters: lane pair 2m holds norm value m, lane
+        // L sum L of each half of A and B) and stored per warp
         {
+            float kt[TC], qt[TC], at[TC];
+#pragma unroll
+            for (int j = 0; j < TC; ++j) {
+                const bool in_row = j < tc && tid < p.k;
+                kt[j] = in_row ? to_f32(kraw[j]) : 0.f;
+                qt[j] = in_row ? to_f32(qraw[j]) : 0.f;
+                at[j] = in_row ? araw[j] : 0.f;
+            }
+            if (tid < BV)
+#pragma unroll
+                for (int j = 0; j < TC; ++j)
+                    if (j < tc)
+                        reinterpret_cast<float*>(gts + j * SH::G_TOK + SH::G_V)[tid] =
+                            tid < vcols ? to_f32(vraw[j]) : 0.f;
+            // the decay, one branch for all tokens
+            if (scaled) {
+#pragma unroll
+                for (int j = 0; j < TC; ++j) at[j] = j < tc && tid < p.k ? gate_alpha(at[j], true, gscale, gbias) : 0.f;
+            } else {
+#pragma unroll
+                for (int j = 0; j < TC; ++j) at[j] = j < tc && tid < p.k ? gate_alpha(at[j], false, gscale, gbias) : 0.f;
+            }
+            float cdec = 1.f;
+#pragma unroll
+            for (int j = 0; j < TC; ++j) {
+                cdec *= at[j];  // c_j: alpha of tokens 0 .. j
+                if (j < tc && tid < p.k)
+                    reinterpret_cast<float4*>(gts + j * SH::G_TOK)[tid] = make_float4(cdec * kt[j], cdec * qt[j], at[j], kt[j]);
+            }
             float sq[2 * TC];
 #pragma unroll
             for (int j = 0; j < TC; ++j) { sq[2 * j] = kt[j] * kt[j]; sq[2 * j + 1] = qt[j] * qt[j]; }
@@ -288,54 +297,21 @@ kda_verify_kernel(const __grid_constant__ CUtensorMap tmap, const StepParams p) 
                 const int m = lane >> 1;  // token m >> 1, k (even) or q (odd)
                 nrm[((m >> 1) * NW + warp) * 2 + (m & 1)] = s;
             }
-        }
-        if (__syncthreads_or(ok_in ? 0 : 1)) {
-            alive = false;
-            break;
-        }
-        // (2) per-token scalars, a lane per token
-        if (warp == 0 && lane < tc) {
-            float kk2 = 0.f, qq2 = 0.f;
-#pragma unroll
-            for (int w = 0; w < NW; ++w) {
-                kk2 += nrm[(lane * NW + w) * 2 + 0];
-                qq2 += nrm[(lane * NW + w) * 2 + 1];
-            }
-            const float beta = __frcp_rn(1.0f + expf(-bsm[lane]));  // sigmoid(b)
-            scal[lane] = make_float4(beta, __frsqrt_rn(kk2 + L2_EPS), __frsqrt_rn(qq2 + L2_EPS), 0.f);
-        }
-        __syncthreads();
-        // (3) row tid: the gates of every token, then this row's terms of the
-        // 64 sums A and B, summed over the warp's rows (two reduce-scatters of
-        // 32: lane L holds sum L of each half) and stored per warp
-        {
-            float kh[TC], qh[TC], bk[TC], cdec = 1.f;
-#pragma unroll
-            for (int j = 0; j < TC; ++j) {
-                const float4 sc = scal[j];
-                kh[j] = j < tc ? kt[j] * sc.y : 0.f;
-                qh[j] = j < tc ? qt[j] * sc.z : 0.f;
-                bk[j] = j < tc ? sc.x * kh[j] : 0.f;
-                cdec *= at[j];  // c_j: alpha of tokens 0 .. j
-                if (j < tc) {
-                    uint8_t* g = gts + j * SH::G_TOK;
-                    if (tid < p.k)
-                        reinterpret_cast<float4*>(g)[tid] = make_float4(cdec * kh[j], cdec * qh[j], at[j], bk[j]);
-                    if (tid < BV) reinterpret_cast<float*>(g + SH::G_V)[tid] = vv[j];
-                }
-            }
             float part[32];
-            ab_terms<0, TC>(part, bk, kh, qh, at);
+            ab_terms<0, TC>(part, kt, kt, qt, at);
             abw[warp * 64 + lane] = warp_reduce_scatter<32>(part, lane);
-            ab_terms<32, TC>(part, bk, kh, qh, at);
+            ab_terms<32, TC>(part, kt, kt, qt, at);
             abw[warp * 64 + 32 + lane] = warp_reduce_scatter<32>(part, lane);
         }
-        if (!state_in) {  // the initial state, once, while the gates are written
-            const bool ok_st = rst || mbar_wait(bar_st, 0);
-            if (__syncthreads_or(ok_st ? 0 : 1)) {
+        {  // the initial state arrives (first chunk) while the rows are summed
+            bool ok = true;
+            if (!state_in) ok = rst || mbar_wait(bar_st, 0);
+            if (__syncthreads_or(ok ? 0 : 1)) {
                 alive = false;
                 break;
             }
+        }
+        if (!state_in) {
 #pragma unroll
             for (int rr = 0; rr < ROWS; ++rr) {
                 const int row = lane + 32 * rr;
@@ -345,19 +321,51 @@ kda_verify_kernel(const __grid_constant__ CUtensorMap tmap, const StepParams p) 
                     for (int c = 0; c < VEC; ++c) x[rr][c] = 0.f;
             }
             state_in = true;
-        } else {
-            __syncthreads();
         }
+        // (2) the scalars, beside the column sums: thread e < 64 finishes sum e
+        // of A and B, scaled by beta_s / (|k_s| |k_t|) or beta_s / (|k_s| |q_t|);
+        // threads 64 .. 64 + tc - 1 keep {beta, 1/|k|, 1/|q|} of their token
         if (tid < 64) {
-            float s = 0.f;
+            const bool is_a = tid < 28;
+            int t = is_a ? 1 : 0, s = 0;
+            if (is_a) {
 #pragma unroll
-            for (int w = 0; w < NW; ++w) s += abw[w * 64 + tid];
-            ab[tid] = s;
+                for (int u = 2; u < TC; ++u) t += idx_a(u, 0) <= tid ? 1 : 0;
+                s = tid - idx_a(t, 0);
+            } else {
+#pragma unroll
+                for (int u = 1; u < TC; ++u) t += idx_b(u, 0) <= tid ? 1 : 0;
+                s = tid - idx_b(t, 0);
+            }
+            float v = 0.f;
+            if (t < tc) {
+                float ks = 0.f, rt = 0.f;
+#pragma unroll
+                for (int w = 0; w < NW; ++w) {
+                    v += abw[w * 64 + tid];
+                    ks += nrm[(s * NW + w) * 2 + 0];
+                    rt += nrm[(t * NW + w) * 2 + (is_a ? 0 : 1)];
+                }
+                const float beta = sigmoid_neg(-bsm[s]);  // sigmoid(b_s)
+                v *= beta * __frsqrt_rn(ks + L2_EPS) * __frsqrt_rn(rt + L2_EPS);
+            }
+            ab[tid] = v;
+        } else if (tid < 64 + tc) {
+            const int t = tid - 64;
+            float kk2 = 0.f, qq2 = 0.f;
+#pragma unroll
+            for (int w = 0; w < NW; ++w) {
+                kk2 += nrm[(t * NW + w) * 2 + 0];
+                qq2 += nrm[(t * NW + w) * 2 + 1];
+            }
+            scal[t] = make_float4(sigmoid_neg(-bsm[t]), __frsqrt_rn(kk2 + L2_EPS),
+                                  __frsqrt_rn(qq2 + L2_EPS), 0.f);
         }
 
-        // (4) the column sums of the chunk's initial state against c khat and
-        // c qhat of every token, G tokens (32 values per lane) at a time
-#pragma unroll
+        // (3) the column sums of the chunk's initial state against c k and
+        // c q of every token, G tokens (32 values per lane) at a time; the
+        // groups run as a loop (fewer instructions to fetch)
+#pragma unroll 1
         for (int g0 = 0; g0 < TC; g0 += G) {
             if (g0 < tc) {
                 float acc[2 * G * VEC];
@@ -389,8 +397,9 @@ kda_verify_kernel(const __grid_constant__ CUtensorMap tmap, const StepParams p) 
         }
         __syncthreads();
 
-        // (5) per column: forward substitution for d, and the outputs; the
-        // columns past V get d = 0
+        // (4) per column: forward substitution for d, and the outputs; d is
+        // kept scaled by beta_t / |k_t| for the snapshots, which add raw k_t
+        // times it; the columns past V get d = 0
         if (tid < BV) {
             const int j = tid;
             const bool col_ok = j < vcols;
@@ -399,24 +408,25 @@ kda_verify_kernel(const __grid_constant__ CUtensorMap tmap, const StepParams p) 
             for (int t = 0; t < TC; ++t) {
                 d[t] = 0.f;
                 if (t < tc) {
+                    const float4 sc = scal[t];
                     if (col_ok) {
                         const float* g = reinterpret_cast<const float*>(gts + t * SH::G_TOK + SH::G_V);
-                        float u = res[(t * 2 + 0) * BV + j];
+                        float u = sc.y * res[(t * 2 + 0) * BV + j];
 #pragma unroll
                         for (int s = 0; s < t; ++s) u = fmaf(ab[idx_a(t, s)], d[s], u);
                         d[t] = g[j] - u;  // d_t = v_t - (D_t S_(t-1))^T khat_t
-                        float o = res[(t * 2 + 1) * BV + j];
+                        float o = sc.z * res[(t * 2 + 1) * BV + j];
 #pragma unroll
                         for (int s = 0; s <= t; ++s) o = fmaf(ab[idx_b(t, s)], d[s], o);
                         p.o[(((int64_t)tb + t0 + t) * p.hv + h) * p.v + cb * BV + j] = o * p.inv_sqrt_k;
                     }
-                    dsm[t * BV + j] = d[t];
+                    dsm[t * BV + j] = d[t] * (sc.x * sc.y);
                 }
             }
         }
         __syncthreads();
 
-        // (6) the snapshots: S_t = alpha_t S_(t-1) + (beta_t khat_t) d_t^T,
+        // (5) the snapshots: S_t = alpha_t S_(t-1) + (beta_t khat_t) d_t^T,
         // staged rounded in a swizzled tile, then stored.  Prefill keeps
         // only the carry: the same update, nothing staged or stored.
         for (int j = 0; final_mode && j < tc; ++j) {
@@ -469,9 +479,7 @@ kda_verify_kernel(const __grid_constant__ CUtensorMap tmap, const StepParams p) 
                 bulk_wait_read<SH::NSTAGE - 2>();
             }
         }
-        // The next chunk's bulk copies (async proxy) overwrite this chunk's
-        // gates (generic proxy): fence, then the barrier before they are issued.
-        fence_proxy_async_smem();
+        // the next chunk rewrites the gates, d and the token scalars
         __syncthreads();
     }
     // prefill: the state after the last token, staged rounded in buffer 0 (free:
@@ -493,8 +501,7 @@ kda_verify_kernel(const __grid_constant__ CUtensorMap tmap, const StepParams p) 
     if (!alive) {
         if (tid == 0) {
             atomicExch(p.status, STATUS_TIMEOUT);
-            mbar_wait(bar_in, in_phase ^ 1);  // bounded: no copy may still target this CTA's memory
-            if (!rst) mbar_wait(bar_st, 0);
+            if (!rst) mbar_wait(bar_st, 0);  // bounded: no copy may still target this CTA's memory
         }
     }
 }

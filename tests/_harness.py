@@ -10,7 +10,14 @@ import kda_linear_attention_gated_gb300 as kda
 from kda_linear_attention_gated_gb300.workloads import StepInputs
 
 FP32_ATOL = 1e-5          # max-abs bound for an fp32 pool (states and outputs)
-F16_STATE_ULPS = 1        # stored fp16 states: within 1 ulp of the oracle's RNE value
+F16_STATE_ULPS = 1        # stored fp16 states: within 1 ulp of the oracle's RNE value ...
+# ... except in the bottom binades, |S| < 2^-13, where one fp16 step is 2^-24
+# (6.0e-8): that is below the rounding error of any fp32 carry through terms of
+# magnitude up to about 1 (an fp32 ulp there is 2^-23 .. 2^-24), so a second
+# step (1.2e-7 in all) is allowed there and nowhere else
+F16_LOW_BINADE = 2.0 ** -13
+F16_LOW_ULPS = 2
+F16_OFF_FRACTION = 1e-3   # and at most this share of the stored elements off by any ulp
 F16_OUT_RTOL = 2e-3       # outputs with an fp16 pool: relative
 F16_OUT_ATOL = 1e-6       # ... with an absolute floor for outputs near zero
 
@@ -89,7 +96,14 @@ def assert_pool_match(gpu_pool: torch.Tensor, ref: np.ndarray, touched_slots, wh
     assert g[~touched].tobytes() == ref[~touched].tobytes(), f"{what}: untouched slots changed"
     if g.dtype == np.uint16:
         dist = f16_ulp_distance(g[touched], ref[touched])
-        assert dist.max() <= F16_STATE_ULPS, f"{what}: fp16 state off by {dist.max()} ulp"
+        low = np.abs(ref[touched].view(np.float16).astype(np.float64)) < F16_LOW_BINADE
+        bound = np.where(low, F16_LOW_ULPS, F16_STATE_ULPS)
+        worst = int(np.argmax(dist - bound))
+        assert (dist <= bound).all(), (
+            f"{what}: fp16 state off by {dist.ravel()[worst]} ulp at reference value "
+            f"{ref[touched].view(np.float16).ravel()[worst]}")
+        off = float((dist > 0).mean())
+        assert off <= F16_OFF_FRACTION, f"{what}: {off:.2e} of the fp16 states are off by an ulp"
         return dist
     diff = np.abs(g[touched].astype(np.float64) - ref[touched].astype(np.float64))
     assert np.isfinite(g[touched]).all()

@@ -4,8 +4,9 @@ the same seeded inputs.
 Tolerances (the method's statement of the target): fp32 pool -- states and
 outputs within max-abs 1e-5; fp16 pool -- stored states within 1 fp16 ulp of
 the oracle's round-to-nearest-even value (the GPU rounds from fp32, the oracle
-from fp64, so a value near a rounding midpoint may land one step apart) and
-outputs within 2e-3 relative.  Slot placement is checked bit-exact: every slot
+from fp64, so a value near a rounding midpoint may land one step apart; in the
+bottom binades, |S| < 2^-13, where an fp16 step of 2^-24 is below the fp32
+carry's own rounding error, two steps) and outputs within 2e-3 relative.  Slot placement is checked bit-exact: every slot
 the call must not write is compared byte for byte.
 """
 import numpy as np
