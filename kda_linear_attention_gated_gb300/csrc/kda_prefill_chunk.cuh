@@ -107,23 +107,43 @@ __global__ void __launch_bounds__(KMAX, KDA_PREP_MINB) kda_prefill_prep_kernel(c
     const int hq = h / (p.hv / p.hqk);
     float* w = ws + (prefill_chunk_slot(tb, r, j) * p.hv + h) * PCH_FLOATS;
 
-    // (1) inputs: row tid of k, q, a for every token; value column tid of v
+    // (1) inputs: row tid of k, q, a for every token; value column tid of v.
+    // Half a chunk at a time, every load unconditional from an address
+    // clamped into the chunk's last token, row 0 or column 0, so that all of
+    // a half's loads are in flight at once; values out of range are zeroed.
     float kt[PCH], qt[PCH], al[PCH];
     const bool scaled = p.a_log != nullptr;
     const float gscale = scaled ? expf(__ldg(p.a_log + h)) : 1.f;
     const float gbias = p.dt_bias != nullptr && tid < p.k ? __ldg(p.dt_bias + (int64_t)h * p.k + tid) : 0.f;
+    {
+        const int row = tid < p.k ? tid : 0, col = tid < p.v ? tid : 0;
+        const QT* qp = static_cast<const QT*>(p.q);
+        const QT* kp = static_cast<const QT*>(p.kk);
+        const QT* vp = static_cast<const QT*>(p.vv);
+        constexpr int HALF = PCH / 2;
 #pragma unroll
-    for (int t = 0; t < PCH; ++t) {
-        kt[t] = 0.f; qt[t] = 0.f; al[t] = 1.f;
-        const bool live = t < cl;
-        if (live && tid < p.k) {
-            const int64_t rq = (int64_t)(t0 + t) * p.hqk + hq;
-            kt[t] = to_f32(static_cast<const QT*>(p.kk)[rq * p.k + tid]);
-            qt[t] = to_f32(static_cast<const QT*>(p.q)[rq * p.k + tid]);
-            al[t] = gate_alpha(__ldg(p.a + ((int64_t)(t0 + t) * p.hv + h) * p.k + tid), scaled, gscale, gbias);
+        for (int t1 = 0; t1 < PCH; t1 += HALF) {
+            QT kr[HALF], qr[HALF], vr[HALF];
+            float ar[HALF];
+#pragma unroll
+            for (int u = 0; u < HALF; ++u) {
+                const int64_t tok = (int64_t)t0 + min(t1 + u, cl - 1);
+                const int64_t rq = (tok * p.hqk + hq) * p.k + row, rt = tok * p.hv + h;
+                kr[u] = kp[rq];
+                qr[u] = qp[rq];
+                ar[u] = __ldg(p.a + rt * p.k + row);
+                vr[u] = vp[rt * p.v + col];
+            }
+#pragma unroll
+            for (int u = 0; u < HALF; ++u) {
+                const int t = t1 + u;
+                const bool in_row = t < cl && tid < p.k;
+                kt[t] = in_row ? to_f32(kr[u]) : 0.f;
+                qt[t] = in_row ? to_f32(qr[u]) : 0.f;
+                al[t] = in_row ? gate_alpha(ar[u], scaled, gscale, gbias) : 1.f;
+                vs[t][tid] = t < cl && tid < p.v ? to_f32(vr[u]) : 0.f;
+            }
         }
-        vs[t][tid] = live && tid < p.v ? to_f32(static_cast<const QT*>(p.vv)[((int64_t)(t0 + t) * p.hv + h) * p.v + tid])
-                                       : 0.f;
     }
     {
         float sq[2 * PCH];
