@@ -81,7 +81,7 @@ struct VerifyShape {
     static_assert(ROWBYTES == 128 || ROWBYTES == 64, "tile row bytes");
     static_assert(NT >= KMAX, "one thread per key row in the gate phase");
     static_assert(NA + NB == 64 && 2 * G * VEC == 32 && TC % G == 0 && TC == 8, "chunk shape");
-    static_assert(BV <= NT, "one thread per column in the solve");
+    static_assert(BV == 32 && TC % NW == 0, "the solve: a lane per column, whole token shares per warp");
     static_assert(NSTAGE >= 2, "staging buffers");
     static_assert(G_TOK % 16 == 0 &&
                   WORK_BYTES % 16 == 0 && RED_RES % 16 == 0 && RED_D % 16 == 0, "layout");
@@ -397,17 +397,21 @@ kda_verify_kernel(const __grid_constant__ CUtensorMap tmap, const StepParams p) 
         }
         __syncthreads();
 
-        // (4) per column: forward substitution for d, and the outputs; d is
-        // kept scaled by beta_t / |k_t| for the snapshots, which add raw k_t
-        // times it; the columns past V get d = 0
-        if (tid < BV) {
-            const int j = tid;
+        // (4) per column (lane j): forward substitution for d, and the
+        // outputs.  Warp w keeps tokens TPW w .. TPW w + TPW - 1: it solves
+        // up to its last token and writes only its own tokens' outputs and d,
+        // so no warp carries all the outputs and stores.  d is kept scaled by
+        // beta_t / |k_t| for the snapshots, which add raw k_t times it; the
+        // columns past V get d = 0.
+        {
+            constexpr int TPW = TC / NW;
+            const int j = lane, tlo = warp * TPW, thi = tlo + TPW;
             const bool col_ok = j < vcols;
             float d[TC];
 #pragma unroll
             for (int t = 0; t < TC; ++t) {
                 d[t] = 0.f;
-                if (t < tc) {
+                if (t < tc && t < thi) {
                     const float4 sc = scal[t];
                     if (col_ok) {
                         const float* g = reinterpret_cast<const float*>(gts + t * SH::G_TOK + SH::G_V);
@@ -415,12 +419,14 @@ kda_verify_kernel(const __grid_constant__ CUtensorMap tmap, const StepParams p) 
 #pragma unroll
                         for (int s = 0; s < t; ++s) u = fmaf(ab[idx_a(t, s)], d[s], u);
                         d[t] = g[j] - u;  // d_t = v_t - (D_t S_(t-1))^T khat_t
-                        float o = sc.z * res[(t * 2 + 1) * BV + j];
+                        if (t >= tlo) {
+                            float o = sc.z * res[(t * 2 + 1) * BV + j];
 #pragma unroll
-                        for (int s = 0; s <= t; ++s) o = fmaf(ab[idx_b(t, s)], d[s], o);
-                        p.o[(((int64_t)tb + t0 + t) * p.hv + h) * p.v + cb * BV + j] = o * p.inv_sqrt_k;
+                            for (int s = 0; s <= t; ++s) o = fmaf(ab[idx_b(t, s)], d[s], o);
+                            p.o[(((int64_t)tb + t0 + t) * p.hv + h) * p.v + cb * BV + j] = o * p.inv_sqrt_k;
+                        }
                     }
-                    dsm[t * BV + j] = d[t] * (sc.x * sc.y);
+                    if (t >= tlo) dsm[t * BV + j] = d[t] * (sc.x * sc.y);
                 }
             }
         }
