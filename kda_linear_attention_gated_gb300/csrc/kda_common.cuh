@@ -65,10 +65,12 @@ __device__ __forceinline__ float softplus_f(float x) {
 // sigmoid(-x) = 1 / (1 + e^x): the fast reciprocal refined by one
 // Newton-Raphson step, r <- r + r (1 - y r), which brings its error to about
 // half an ulp at a fraction of the cost of the correctly rounded reciprocal.
-// x is capped at 80 (1 + e^80 < 2^126, inside the fast reciprocal's range),
-// which changes the result by less than 2e-35; a NaN passes through.
+// Past x = 88 (e^x overflows) the result is exactly 0; between 87.3 and 88
+// (y > 2^126) the fast reciprocal gives 0, and the step keeps it: the true
+// value there is below 1.2e-38.  x = -inf gives exactly 1; a NaN passes through.
 __device__ __forceinline__ float sigmoid_neg(float x) {
-    const float y = 1.0f + expf(x > 80.f ? 80.f : x);
+    if (x > 88.f) return 0.f;
+    const float y = 1.0f + expf(x);
     const float r = __fdividef(1.0f, y);
     return fmaf(r, fmaf(-y, r, 1.0f), r);
 }

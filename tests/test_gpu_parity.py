@@ -183,6 +183,40 @@ def test_identity_step_is_bit_exact(state_dtype):
     assert_out_match(o, o_ref, state_dtype, "o")
 
 
+def _saturate_gates(inp):
+    """Rows of a at +inf, -inf, +100 and -100 (alpha = 0, 1, ~4e-44, ~1),
+    b per head at +inf, -inf, +100, -100, 0 in turn (beta = 1, 0, ~1, ~4e-44, 1/2)."""
+    k = inp.a.shape[-1]
+    for i, val in enumerate((float("inf"), -float("inf"), 100.0, -100.0)):
+        inp.a[..., i * k // 4:(i + 1) * k // 4] = val
+    vals = (float("inf"), -float("inf"), 100.0, -100.0, 0.0)
+    for h in range(inp.b.shape[-1]):
+        inp.b[..., h] = vals[h % len(vals)]
+    return inp
+
+
+@pytest.mark.parametrize("state_dtype", [torch.float32, torch.float16])
+def test_saturated_gates_match_oracle(state_dtype):
+    """The decay and the update gate at their limits: alpha exactly 0 and 1,
+    beta exactly 1 and 0, and values past the point where e^a overflows."""
+    dec = _saturate_gates(workloads.make_decode(n=8, hv=10, k=128, v=128, num_slots=16,
+                                                state_dtype=state_dtype, seed=57))
+    gpool, o, st = gpu_decode(dec)
+    assert st == 0
+    ref, o_ref = oracle_decode(dec)
+    assert np.isfinite(o.numpy()).all()
+    assert_out_match(o, o_ref, state_dtype, "decode o")
+    assert_pool_match(gpool, ref, dec.init_slot.numpy(), "decode pool")
+    ver = _saturate_gates(workloads.make_verify(n=4, t=5, hv=10, k=128, v=128, num_slots=32,
+                                                state_dtype=state_dtype, seed=58))
+    gpool, o, st = gpu_verify(ver)
+    assert st == 0
+    ref, o_ref = oracle_verify(ver)
+    assert np.isfinite(o.numpy()).all()
+    assert_out_match(o, o_ref, state_dtype, "verify o")
+    assert_pool_match(gpool, ref, ver.snap_slot.numpy(), "verify snapshots")
+
+
 def test_verify_equals_chained_decode_on_fp32_pool():
     """An fp32 pool stores the fp32 carry exactly, so T decode calls and one
     T-token verify agree up to the order of the fp32 sums over K (the two
