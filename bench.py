@@ -232,7 +232,7 @@ def main():
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer measurement")
     ap.add_argument("--workload", choices=("decode_f32", "decode_f16"), default="decode_f32",
                     help="headline workload: the decode step on an fp32 pool (the metric's) or fp16 pool")
-    ap.add_argument("--case", choices=("verify_f16", "sweep", "prefill"), default=None,
+    ap.add_argument("--case", choices=("verify_f16", "sweep", "prefill", "aux"), default=None,
                     help="time one secondary case alone and print its line (profiling runs)")
     ap.add_argument("--soak-seconds", type=float, default=1.0,
                     help="minimum untimed load before timing (clocks ramp; 0 under a profiler)")
@@ -430,6 +430,10 @@ def main():
     if args.case is not None:
         if args.case == "verify_f16":
             res = {"verify_f16": bench_verify(kda, workloads, torch, args, l2, peak)}
+        elif args.case == "aux":
+            res = {"ckpt_flush_fp32_n64": bench_ckpt(kda, workloads, torch, peak),
+                   "ckpt_load_fp32_n64": bench_ckpt(kda, workloads, torch, peak, load=True),
+                   "conv_step_n64_t5_bf16": bench_conv(kda, workloads, torch, peak)}
         elif args.case == "prefill":
             res = {f"prefill_{n}x{t}_fp16{'_chunked' if c else ''}": bench_prefill(kda, workloads, torch, n, t, c)
                    for c in (False, True) for n, t in ((1, 8192), (8, 1024), (64, 128))}
@@ -473,6 +477,8 @@ def main():
         for sd_name, sd in (("fp32", torch.float32), ("fp16", torch.float16)):
             extra[f"sweep_69_layers_n128_{sd_name}"] = bench_sweep(kda, workloads, torch, sd, 128, peak)
         extra["ckpt_flush_fp32_n64"] = bench_ckpt(kda, workloads, torch, peak)
+        extra["ckpt_load_fp32_n64"] = bench_ckpt(kda, workloads, torch, peak, load=True)
+        extra["conv_step_n64_t5_bf16"] = bench_conv(kda, workloads, torch, peak)
         extra["prefill_8x1024_fp16"] = bench_prefill(kda, workloads, torch, 8, 1024)
         extra["prefill_8x1024_fp16_chunked"] = bench_prefill(kda, workloads, torch, 8, 1024, True)
 
@@ -611,9 +617,10 @@ def bench_prefill(kda, workloads, torch, n, t, chunked=False, reps=5):
             "approx_tflops": round(flop / (ms * 1e-3) / 1e12, 3)}
 
 
-def bench_ckpt(kda, workloads, torch, peak, replays=200):
+def bench_ckpt(kda, workloads, torch, peak, replays=200, load=False):
     """Checkpoint flush of 64 fp32 states (12 x 128 x 128) from a 256-slot pool
-    to a 128-entry plane; 24 pool/plane pairs rotate (4.8 GB, far past L2)."""
+    to a 128-entry plane (load: the reverse copy); 24 pool/plane pairs rotate
+    (4.8 GB, far past L2)."""
     lib = kda.KdaLibrary(torch.float32)
     g = torch.Generator().manual_seed(9)
     R = 24
@@ -624,12 +631,13 @@ def bench_ckpt(kda, workloads, torch, peak, replays=200):
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
     stream = torch.cuda.Stream()
     g_ = torch.cuda.CUDAGraph()
+    call = lib.kda_ckpt_load if load else lib.kda_ckpt_flush
     with torch.cuda.stream(stream):
-        lib.kda_ckpt_flush(pools[0], planes[0], slots, entries, status)
+        call(pools[0], planes[0], slots, entries, status)
         stream.synchronize()
         with torch.cuda.graph(g_, stream=stream):
             for i in range(R):
-                lib.kda_ckpt_flush(pools[i], planes[i], slots, entries, status)
+                call(pools[i], planes[i], slots, entries, status)
         for _ in range(3):
             g_.replay()
     torch.cuda.synchronize()
@@ -647,9 +655,66 @@ def bench_ckpt(kda, workloads, torch, peak, replays=200):
     byt = 2 * 64 * HV * K * V * 4
     del pools, planes
     torch.cuda.empty_cache()
-    return {"workload": "checkpoint flush, 64 fp32 states [12,128,128], 256-slot pool -> 128-entry plane",
+    what = ("checkpoint load, 64 fp32 states [12,128,128], 128-entry plane -> 256-slot pool" if load else
+            "checkpoint flush, 64 fp32 states [12,128,128], 256-slot pool -> 128-entry plane")
+    return {"workload": what,
             "us_per_call": round(us, 3), "gbs": round(byt / (us * 1e-6) / 1e9, 1),
             "frac_of_peak": round(byt / (us * 1e-6) / 1e9 / peak, 4), "bytes_per_call": byt}
+
+
+def bench_conv(kda, workloads, torch, peak, replays=480):
+    """The causal short convolution in front of the recurrence at the layer
+    shape: N=64 requests x T=5 tokens (4 drafts + 1), C = 4608 channels (q, k,
+    v of 12 heads of 128), KW=4, a bf16 window of L = KW - 1 + 4 = 7 entries
+    per slot.  48 window/input/output sets rotate (about 0.5 GB, past L2),
+    launched with programmatic dependent launch (the kernel reads nothing
+    before the previous kernel completes).
+    Algorithmic bytes: per request and channel the KW - 1 history entries
+    read, the L window entries written, T inputs read and T outputs written,
+    plus the fp32 weights and bias once."""
+    lib = kda.KdaLibrary(torch.float32)
+    n, t, C, kw, spec = 64, 5, 4608, 4, 4
+    R = 48
+    sets = [workloads.make_conv(n=n, t=t, channels=C, kw=kw, num_spec=spec, num_slots=n,
+                                dtype=torch.bfloat16, seed=70 + i).to("cuda") for i in range(R)]
+    ys = [torch.empty_like(d.x) for d in sets]
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    stream = torch.cuda.Stream()
+    g_ = torch.cuda.CUDAGraph()
+
+    def call(i):
+        d = sets[i]
+        lib.kda_conv_step(d.window, d.conv_slot, d.x, d.weight, ys[i], status, bias=d.bias,
+                          cu_seqlens=d.cu_seqlens, max_t=t, accepted=d.accepted, reset=d.reset,
+                          flags=kda.KDA_LAUNCH_PDL)
+    with torch.cuda.stream(stream):
+        call(0)
+        stream.synchronize()
+        with torch.cuda.graph(g_, stream=stream):
+            for i in range(R):
+                call(i)
+        for _ in range(3):
+            g_.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    reps = max(1, replays // R)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(reps):
+            g_.replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item())}")
+    us = e0.elapsed_time(e1) * 1e3 / (reps * R)
+    L = kw - 1 + spec
+    byt = n * C * 2 * ((kw - 1) + L + 2 * t) + C * (kw + 1) * 4
+    del sets, ys
+    torch.cuda.empty_cache()
+    return {"workload": "conv window step, N=64 x T=5, C=4608, KW=4, bf16 window of 7 entries",
+            "us_per_call": round(us, 3), "gbs": round(byt / (us * 1e-6) / 1e9, 1),
+            "frac_of_peak": round(byt / (us * 1e-6) / 1e9 / peak, 4), "bytes_per_call": byt,
+            "launch": f"CUDA graph of {R} launches, replayed; flags KDA_LAUNCH_PDL"}
 
 
 def bench_verify(kda, workloads, torch, args, l2, peak):

@@ -585,7 +585,13 @@ int kda_conv_step(const kda_conv_window* win, const kda_conv_args* args, int32_t
         !aligned(g.weight, 4) || !aligned(dev_status, 4) || (g.bias && !aligned(g.bias, 4)) ||
         (g.cu_seqlens && !aligned(g.cu_seqlens, 4)) || (g.accepted && !aligned(g.accepted, 4)))
         return KDA_ERR_ALIGN;
-    const int64_t cblocks = (win->channels + kda::CONV_THREADS - 1) / kda::CONV_THREADS;
+    // four channels a thread when the kernel is at most 4 wide and the channel
+    // count and every address allow 4-element accesses, else one
+    const int64_t vb = 4LL * es;
+    const bool vec4 = g.kernel_width <= kda::CONV_VEC_KW_MAX && win->channels % 4 == 0 &&
+                      win->slot_stride % 4 == 0 && aligned(win->base, vb) && aligned(g.x, vb) && aligned(g.y, vb);
+    const int vc = vec4 ? 4 : 1, ct = vec4 ? kda::CONV_VEC_THREADS : kda::CONV_THREADS;
+    const int64_t cblocks = (win->channels / vc + ct - 1) / ct;
     if (cblocks * g.n > 0x7fffffffLL) return KDA_ERR_SHAPE;
     kda::ConvParams prm;
     prm.window = win->base;
@@ -609,16 +615,27 @@ int kda_conv_step(const kda_conv_window* win, const kda_conv_args* args, int32_t
     prm.status = dev_status;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(cblocks * g.n), 1, 1);
-    cfg.blockDim = dim3(kda::CONV_THREADS, 1, 1);
+    cfg.blockDim = dim3((unsigned)ct, 1, 1);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = static_cast<cudaStream_t>(stream);
     cudaLaunchAttribute attr;
     set_pdl(cfg, &attr, flags);
     cudaError_t err;
+    using namespace kda;
+    constexpr int C1 = CONV_THREADS, C4 = CONV_VEC_THREADS, K1 = CONV_KW_MAX, K4 = CONV_VEC_KW_MAX;
     switch (win->dtype) {
-        case KDA_F32: err = cudaLaunchKernelEx(&cfg, kda::kda_conv_kernel<float>, prm); break;
-        case KDA_F16: err = cudaLaunchKernelEx(&cfg, kda::kda_conv_kernel<__half>, prm); break;
-        default: err = cudaLaunchKernelEx(&cfg, kda::kda_conv_kernel<__nv_bfloat16>, prm); break;
+        case KDA_F32:
+            err = vec4 ? cudaLaunchKernelEx(&cfg, kda_conv_kernel<float, 4, C4, K4>, prm)
+                       : cudaLaunchKernelEx(&cfg, kda_conv_kernel<float, 1, C1, K1>, prm);
+            break;
+        case KDA_F16:
+            err = vec4 ? cudaLaunchKernelEx(&cfg, kda_conv_kernel<__half, 4, C4, K4>, prm)
+                       : cudaLaunchKernelEx(&cfg, kda_conv_kernel<__half, 1, C1, K1>, prm);
+            break;
+        default:
+            err = vec4 ? cudaLaunchKernelEx(&cfg, kda_conv_kernel<__nv_bfloat16, 4, C4, K4>, prm)
+                       : cudaLaunchKernelEx(&cfg, kda_conv_kernel<__nv_bfloat16, 1, C1, K1>, prm);
+            break;
     }
     return err == cudaSuccess ? KDA_OK : KDA_ERR_LAUNCH;
 }

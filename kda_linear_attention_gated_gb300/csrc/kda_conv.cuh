@@ -9,13 +9,13 @@
 // [slot][L][C], oldest entry first and the channel innermost, so that a warp's
 // 32 consecutive channels of one entry are one coalesced access.
 //
-// One thread per (request, channel).  With acc = accepted[r] - 1 (0 without),
+// One thread per (request, 1 or 4 channels).  With acc = accepted[r] - 1 (0 without),
 // m = acc + KW - 1 valid entries and kept = max(0, L - T) old ones:
 //   history h_i = W[acc + i] (i < KW - 1; zero on reset), z = h ++ x,
 //   y_t = act(bias + sum_i w_i z_{t+i})      (w_{KW-1} weighs the newest input)
 //   new window = W[m - kept .. m - 1] (zero on reset) ++ the last min(T, L) inputs.
 // Every read of the window happens before any write to it.  The arithmetic is
-// fp32; y is rounded to the window's dtype to nearest even.
+// fp32, SiLU as s sigmoid(s); y is rounded to the window's dtype to nearest even.
 #pragma once
 
 #include "kda_common.cuh"
@@ -24,7 +24,9 @@ namespace kda {
 
 constexpr int CONV_KW_MAX = 8;   // kernel widths 1 .. 8
 constexpr int CONV_L_MAX = 32;   // window entries up to 32
-constexpr int CONV_THREADS = 256;
+constexpr int CONV_THREADS = 256;      // threads per CTA, one channel each
+constexpr int CONV_VEC_THREADS = 128;  // threads per CTA, four channels each ...
+constexpr int CONV_VEC_KW_MAX = 4;     // ... for kernel widths up to 4
 
 struct ConvParams {
     void* window;
@@ -45,18 +47,51 @@ struct ConvParams {
     int32_t* status;
 };
 
-__device__ __forceinline__ float conv_ld(const float* p, int64_t i) { return p[i]; }
-__device__ __forceinline__ float conv_ld(const __half* p, int64_t i) { return __half2float(p[i]); }
-__device__ __forceinline__ float conv_ld(const __nv_bfloat16* p, int64_t i) { return __bfloat162float(p[i]); }
-__device__ __forceinline__ void conv_st(float* p, int64_t i, float v) { p[i] = v; }
-__device__ __forceinline__ void conv_st(__half* p, int64_t i, float v) { p[i] = __float2half_rn(v); }
-__device__ __forceinline__ void conv_st(__nv_bfloat16* p, int64_t i, float v) { p[i] = __float2bfloat16_rn(v); }
+__device__ __forceinline__ float conv_f32(float v) { return v; }
+__device__ __forceinline__ float conv_f32(__half v) { return __half2float(v); }
+__device__ __forceinline__ float conv_f32(__nv_bfloat16 v) { return __bfloat162float(v); }
+__device__ __forceinline__ void conv_round(float v, float& e) { e = v; }
+__device__ __forceinline__ void conv_round(float v, __half& e) { e = __float2half_rn(v); }
+__device__ __forceinline__ void conv_round(float v, __nv_bfloat16& e) { e = __float2bfloat16_rn(v); }
 
-template <typename ET>
-__global__ void __launch_bounds__(CONV_THREADS) kda_conv_kernel(const ConvParams p) {
-    const int cblocks = (p.C + CONV_THREADS - 1) / CONV_THREADS;
+// VC consecutive channels of one window entry or token row as one access.
+template <int BYTES> struct ConvRaw;
+template <> struct ConvRaw<2> { using T = unsigned short; };
+template <> struct ConvRaw<4> { using T = unsigned int; };
+template <> struct ConvRaw<8> { using T = uint2; };
+template <> struct ConvRaw<16> { using T = uint4; };
+
+template <typename ET, int VC>
+struct ConvIO {
+    using R = typename ConvRaw<VC * (int)sizeof(ET)>::T;
+    static __device__ __forceinline__ R ld(const ET* p) { return *reinterpret_cast<const R*>(p); }
+    static __device__ __forceinline__ void st(ET* p, R v) { *reinterpret_cast<R*>(p) = v; }
+    static __device__ __forceinline__ void widen(R r, float (&f)[VC]) {
+        ET e[VC];
+        memcpy(e, &r, sizeof(R));
+#pragma unroll
+        for (int v = 0; v < VC; ++v) f[v] = conv_f32(e[v]);
+    }
+    static __device__ __forceinline__ R narrow(const float (&f)[VC]) {  // to nearest even
+        ET e[VC];
+#pragma unroll
+        for (int v = 0; v < VC; ++v) conv_round(f[v], e[v]);
+        R r;
+        memcpy(&r, e, sizeof(R));
+        return r;
+    }
+};
+
+// VC channels per thread (1, or 4 when C and every address allow 4-channel
+// accesses), CT threads per CTA, kernel widths up to KWM; grid = requests x
+// ceil(C / (VC CT)).
+template <typename ET, int VC, int CT, int KWM>
+__global__ void __launch_bounds__(CT) kda_conv_kernel(const ConvParams p) {
+    using IO = ConvIO<ET, VC>;
+    using R = typename IO::R;
+    const int cblocks = (p.C / VC + CT - 1) / CT;
     const int r = (int)blockIdx.x / cblocks;
-    const int c = ((int)blockIdx.x - r * cblocks) * CONV_THREADS + (int)threadIdx.x;
+    const int c = (((int)blockIdx.x - r * cblocks) * CT + (int)threadIdx.x) * VC;  // first channel
     cudaTriggerProgrammaticLaunchCompletion();
     cudaGridDependencySynchronize();  // nothing here is read before the previous kernel is done
 
@@ -69,6 +104,16 @@ __global__ void __launch_bounds__(CONV_THREADS) kda_conv_kernel(const ConvParams
     const int acc = p.accepted != nullptr ? p.accepted[r] - 1 : 0;
     const int m = acc + p.KW - 1;
     const int kept = max(0, p.L - T);
+    constexpr int CB = 8;  // window entries or tokens per batch of loads
+    // The first CB inputs of this request go out before anything that waits
+    // for the slot id or the accepted index (rows clamped into the request,
+    // the channels into range; only read once the token range is checked).
+    const bool range_ok = tb >= 0 && T > 0 && T <= p.t && tb + T <= p.total;
+    const ET* x = static_cast<const ET*>(p.x) + (int64_t)tb * p.C + min(c, p.C - VC);  // token t at x[t C]
+    R x0[CB];
+    if (range_ok)
+#pragma unroll
+        for (int u = 0; u < CB; ++u) x0[u] = IO::ld(x + (int64_t)min(u, T - 1) * p.C);
     // uniform over the CTA: one request
     if (slot >= p.num_slots) {
         if (threadIdx.x == 0) atomicCAS(p.status, 0, STATUS_SLOT_RANGE);
@@ -79,51 +124,102 @@ __global__ void __launch_bounds__(CONV_THREADS) kda_conv_kernel(const ConvParams
         return;
     }
     if (c >= p.C) return;
-    ET* y = static_cast<ET*>(p.y);
+    ET* y = static_cast<ET*>(p.y) + (int64_t)tb * p.C + c;  // token t at y[t C]
+    const R zero = R{};    // +0 in every channel, for all three element types
     if (slot < 0) {  // padding: zero outputs, window untouched
-        for (int t = 0; t < T; ++t) conv_st(y, (int64_t)(tb + t) * p.C + c, 0.f);
+        for (int t = 0; t < T; ++t) IO::st(y + (int64_t)t * p.C, zero);
         return;
     }
     if (T == 0) return;
 
-    const ET* x = static_cast<const ET*>(p.x);
+    // Each thread owns its VC channels of the slot's window, so its own
+    // program order is the only order its reads and writes need.  Loads go
+    // out in batches of CB, unconditionally, from indices clamped into the
+    // window or the request's tokens, so that a batch is in flight at once;
+    // the values out of range are dropped where they are used.
     ET* W = static_cast<ET*>(p.window) + (int64_t)slot * p.slot_stride + c;
     const bool rst = p.reset != nullptr && p.reset[r] != 0;
+    const int nh = p.KW - 1;  // history entries
     // w[i] weighs history entry i (i < KW - 1); wlast weighs the current input
-    float w[CONV_KW_MAX], z[CONV_KW_MAX], old[CONV_L_MAX];
+    float w[KWM][VC], z[KWM][VC], wlast[VC], bias[VC];
 #pragma unroll
-    for (int i = 0; i < CONV_KW_MAX; ++i) {
-        w[i] = i < p.KW - 1 ? __ldg(p.w + (int64_t)c * p.KW + i) : 0.f;
-        z[i] = (i < p.KW - 1 && !rst) ? conv_ld(W, (int64_t)(acc + i) * p.C) : 0.f;
-    }
-    const float wlast = __ldg(p.w + (int64_t)c * p.KW + p.KW - 1);
+    for (int i = 0; i < KWM; ++i) {
+        const R hr = IO::ld(W + (int64_t)min(acc + i, p.L - 1) * p.C);
+        float hv[VC];
+        IO::widen(hr, hv);
 #pragma unroll
-    for (int e = 0; e < CONV_L_MAX; ++e)
-        old[e] = (e < kept && !rst) ? conv_ld(W, (int64_t)(m - kept + e) * p.C) : 0.f;
-    const float bias = p.bias != nullptr ? __ldg(p.bias + c) : 0.f;
-
-    for (int t = 0; t < T; ++t) {
-        const float xv = conv_ld(x, (int64_t)(tb + t) * p.C + c);
-        float s = bias;
-#pragma unroll
-        for (int i = 0; i < CONV_KW_MAX; ++i) s = fmaf(w[i], z[i], s);  // w is 0 past KW - 2
-        s = fmaf(wlast, xv, s);
-        const float out = p.silu ? s / (1.0f + expf(-s)) : s;
-        conv_st(y, (int64_t)(tb + t) * p.C + c, out);
-        // slide the history by one: z_i <- z_(i+1), the last history entry <- x_t
-#pragma unroll
-        for (int i = 0; i < CONV_KW_MAX; ++i) {
-            if (i < p.KW - 2) z[i] = z[i + 1 < CONV_KW_MAX ? i + 1 : i];
-            else if (i == p.KW - 2) z[i] = xv;
+        for (int v = 0; v < VC; ++v) {
+            w[i][v] = i < nh ? __ldg(p.w + (int64_t)(c + v) * p.KW + i) : 0.f;
+            z[i][v] = i < nh && !rst ? hv[v] : 0.f;
         }
     }
-    // the new window: kept old entries, then the last min(T, L) inputs (a copy)
 #pragma unroll
-    for (int e = 0; e < CONV_L_MAX; ++e)
-        if (e < kept) conv_st(W, (int64_t)e * p.C, old[e]);
+    for (int v = 0; v < VC; ++v) {
+        wlast[v] = __ldg(p.w + (int64_t)(c + v) * p.KW + p.KW - 1);
+        bias[v] = p.bias != nullptr ? __ldg(p.bias + c + v) : 0.f;
+    }
+
+    // the kept old entries W[m - kept + e] -> W[e] (zero on reset), ascending:
+    // a source never lies below its destination (m >= kept), so no batch reads
+    // what an earlier one wrote
+    for (int e0 = 0; e0 < kept; e0 += CB) {
+        R v[CB];
+#pragma unroll
+        for (int u = 0; u < CB; ++u) v[u] = IO::ld(W + (int64_t)min(m - kept + e0 + u, p.L - 1) * p.C);
+#pragma unroll
+        for (int u = 0; u < CB; ++u)
+            if (e0 + u < kept) IO::st(W + (int64_t)(e0 + u) * p.C, rst ? zero : v[u]);
+    }
+
+    for (int t0 = 0; t0 < T; t0 += CB) {
+        R xr[CB];
+        if (t0 == 0) {
+#pragma unroll
+            for (int u = 0; u < CB; ++u) xr[u] = x0[u];
+        } else {
+#pragma unroll
+            for (int u = 0; u < CB; ++u) xr[u] = IO::ld(x + (int64_t)min(t0 + u, T - 1) * p.C);
+        }
+#pragma unroll
+        for (int u = 0; u < CB; ++u) {
+            if (t0 + u < T) {
+                float xv[VC], out[VC];
+                IO::widen(xr[u], xv);
+#pragma unroll
+                for (int v = 0; v < VC; ++v) {
+                    float s = bias[v];
+#pragma unroll
+                    for (int i = 0; i < KWM; ++i) s = fmaf(w[i][v], z[i][v], s);  // w is 0 past KW - 2
+                    s = fmaf(wlast[v], xv[v], s);
+                    out[v] = p.silu ? s * sigmoid_neg(-s) : s;  // SiLU: s sigmoid(s)
+                    // slide the history by one: z_i <- z_(i+1), the last history entry <- x_t
+#pragma unroll
+                    for (int i = 0; i < KWM; ++i)
+                        z[i][v] = i < nh - 1 ? z[i + 1 < KWM ? i + 1 : i][v] : (i == nh - 1 ? xv[v] : z[i][v]);
+                }
+                IO::st(y + (int64_t)(t0 + u) * p.C, IO::narrow(out));
+            }
+        }
+    }
+
+    // then the last min(T, L) inputs, copied exactly: from the first batch's
+    // registers when they are all of them, else read again
     const int nin = min(T, p.L);
-    const ET* xs = x + (int64_t)(tb + T - nin) * p.C + c;
-    for (int e = 0; e < nin; ++e) W[(int64_t)(kept + e) * p.C] = xs[(int64_t)e * p.C];
+    if (T <= CB && T <= p.L) {
+#pragma unroll
+        for (int u = 0; u < CB; ++u)
+            if (u < T) IO::st(W + (int64_t)(kept + u) * p.C, x0[u]);
+        return;
+    }
+    const ET* xs = x + (int64_t)(T - nin) * p.C;
+    for (int e0 = 0; e0 < nin; e0 += CB) {
+        R v[CB];
+#pragma unroll
+        for (int u = 0; u < CB; ++u) v[u] = IO::ld(xs + (int64_t)min(e0 + u, nin - 1) * p.C);
+#pragma unroll
+        for (int u = 0; u < CB; ++u)
+            if (e0 + u < nin) IO::st(W + (int64_t)(kept + e0 + u) * p.C, v[u]);
+    }
 }
 
 }  // namespace kda

@@ -28,9 +28,19 @@ def storage(t):
     return t.contiguous().view(torch.int16).numpy().view(np.uint16).copy(), name
 
 
-def gpu_conv(inp, silu=True, flags=0):
+def offset_copy(t):
+    """The same values in a buffer whose base is one element past a 4-element boundary."""
+    buf = torch.empty(t.numel() + 4, dtype=t.dtype, device=t.device)
+    v = buf[1:1 + t.numel()].view(t.shape)
+    v.copy_(t)
+    return v
+
+
+def gpu_conv(inp, silu=True, flags=0, offset=False):
     d = inp.to("cuda")
     y = torch.full_like(d.x, float("nan"))
+    if offset:  # rules out 4-channel accesses
+        d.window, d.x, y = offset_copy(d.window), offset_copy(d.x), offset_copy(y)
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
     lib_for(torch.float32).kda_conv_step(d.window, d.conv_slot, d.x, d.weight, y, status, bias=d.bias,
                                          cu_seqlens=d.cu_seqlens, max_t=inp.max_t, accepted=d.accepted,
@@ -49,8 +59,8 @@ def oracle_conv(inp, silu=True):
     return W, y
 
 
-def compare(inp, silu=True, flags=0):
-    gw, gy, st = gpu_conv(inp, silu, flags)
+def compare(inp, silu=True, flags=0, offset=False):
+    gw, gy, st = gpu_conv(inp, silu, flags, offset)
     rw, ry = oracle_conv(inp, silu)
     assert st == 0, lib_for(torch.float32).kda_strerror(st)
     gws, _ = storage(gw)
@@ -75,6 +85,15 @@ def test_conv_variable_lengths(dtype):
     inp = workloads.make_conv(n=5, t_lens=[5, 0, 3, 5, 1], channels=300, dtype=dtype, seed=61)
     inp.accepted[:] = 5  # the whole window is history: every token count is valid
     compare(inp)
+
+
+@pytest.mark.parametrize("dtype", DT)
+def test_conv_one_channel_per_thread_path(dtype):
+    """Shapes and addresses that rule out 4-channel accesses -- 301 channels,
+    and a window, input and output one element past a 4-element boundary --
+    take the one-channel path, with the same results."""
+    compare(workloads.make_conv(n=5, t=5, channels=301, dtype=dtype, seed=65, reset_p=0.2))
+    compare(workloads.make_conv(n=4, t=5, channels=256, dtype=dtype, seed=66, reset_p=0.2), offset=True)
 
 
 @pytest.mark.parametrize("kw", [1, 2, 3, 4, 8])
