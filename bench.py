@@ -330,10 +330,13 @@ def main():
     def bench_e2e(steps):
         """Through the C ABI with host buffers, every step: one host-to-device
         copy of the step's inputs (slot ids, q, k, v, a, b packed in one pinned
-        buffer), the decode kernel, one device-to-host copy of o.  Two sets of
-        device buffers alternate over three streams, so the copies of one step
+        buffer), the decode kernel, one device-to-host copy of o.  NB sets of
+        device buffers rotate over three streams, so the copies of one step
         overlap the kernels of its neighbours; events keep each buffer's
-        writer behind its last reader.  A group of steps is captured in one
+        writer behind its last reader.  The kernels take the device value's
+        launch flags (PDL with early state): a step's slot ids arrive by the
+        copy its kernel waits for, and its pool was last written R steps
+        earlier.  A group of steps is captured in one
         CUDA graph (copies, calls and events included) and replayed, so the
         host's per-call work does not pace the GPU; if capture is refused the
         steps are issued one by one."""
@@ -351,30 +354,32 @@ def main():
         host = torch.empty(h2d, dtype=torch.uint8).pin_memory()
         for t, off, sz in zip(srcs, offs, sizes):
             host[off:off + sz].copy_(t.view(-1).view(torch.uint8))
-        dev_in = [torch.empty(h2d, dtype=torch.uint8, device="cuda") for _ in range(2)]
+        NB = 4
+        dev_in = [torch.empty(h2d, dtype=torch.uint8, device="cuda") for _ in range(NB)]
         views = [[buf[off:off + sz].view(t.dtype).view(t.shape) for t, off, sz in zip(srcs, offs, sizes)]
                  for buf in dev_in]
-        o = [torch.empty(N, HV, V, device="cuda") for _ in range(2)]
-        o_host = [torch.empty(N, HV, V).pin_memory() for _ in range(2)]
+        o = [torch.empty(N, HV, V, device="cuda") for _ in range(NB)]
+        o_host = [torch.empty(N, HV, V).pin_memory() for _ in range(NB)]
         d2h = o[0].numel() * 4
         status = torch.zeros(1, dtype=torch.int32, device="cuda")
         s_in, s_k, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
-        ev_in = [torch.cuda.Event() for _ in range(2)]
-        ev_k = [torch.cuda.Event() for _ in range(2)]
-        ev_out = [torch.cuda.Event() for _ in range(2)]
+        ev_in = [torch.cuda.Event() for _ in range(NB)]
+        ev_k = [torch.cuda.Event() for _ in range(NB)]
+        ev_out = [torch.cuda.Event() for _ in range(NB)]
+        flags = kda.KDA_LAUNCH_PDL | kda.KDA_LAUNCH_PDL_EARLY_STATE
 
         def one(i, first=False):
-            b_ = i & 1
+            b_ = i % NB
             if not first:
-                s_in.wait_event(ev_k[b_])    # the kernel two steps back has read these inputs
+                s_in.wait_event(ev_k[b_])    # the kernel NB steps back has read these inputs
             with torch.cuda.stream(s_in):
                 dev_in[b_].copy_(host, non_blocking=True)
             ev_in[b_].record(s_in)
             s_k.wait_event(ev_in[b_])
             if not first:
-                s_k.wait_event(ev_out[b_])   # o[b] was read back two steps ago
+                s_k.wait_event(ev_out[b_])   # o[b] was read back NB steps ago
             sl, q_, k_, v_, a_, bb = views[b_]
-            lib32.kda_decode_step(pools[i % R], sl, q_, k_, v_, a_, bb, o[b_], status, stream=s_k)
+            lib32.kda_decode_step(pools[i % R], sl, q_, k_, v_, a_, bb, o[b_], status, stream=s_k, flags=flags)
             ev_k[b_].record(s_k)
             s_out.wait_event(ev_k[b_])
             with torch.cuda.stream(s_out):
@@ -392,7 +397,7 @@ def main():
                 s_k.wait_stream(s_in)
                 s_out.wait_stream(s_in)
                 for i in range(group):
-                    one(i, first=i < 2)
+                    one(i, first=i < NB)
                 s_in.wait_stream(s_k)
                 s_in.wait_stream(s_out)
             for _ in range(3):
@@ -413,8 +418,8 @@ def main():
         else:
             for i in range(n_e2e):
                 one(i)
-            s_in.wait_event(ev_out[0])
-            s_in.wait_event(ev_out[1])
+            for ev in ev_out:
+                s_in.wait_event(ev)
         e1.record(s_in)
         torch.cuda.synchronize()
         if int(status.item()) != 0:
@@ -522,9 +527,9 @@ def main():
                 "value": round(e2e_gbs, 2), "unit": "GB/s", "us_per_step": round(e2e_us, 3),
                 "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"],
                 "steps": e2e["steps"],
-                "how": "every step one pinned H2D copy of its packed inputs, the C-ABI decode call, one D2H "
-                       "copy of o; two buffer sets over three streams overlap neighbouring steps; "
-                       + e2e["mode"]},
+                "how": "every step one pinned H2D copy of its packed inputs, the C-ABI decode call (flags "
+                       "KDA_LAUNCH_PDL|KDA_LAUNCH_PDL_EARLY_STATE), one D2H copy of o; four buffer sets over "
+                       "three streams overlap neighbouring steps; " + e2e["mode"]},
             "gpu_launches": args.steps,
             "clocks": head["clocks"],
             "extra": extra,
