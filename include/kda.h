@@ -90,6 +90,18 @@ typedef enum kda_status {
 #define KDA_LAUNCH_PDL_EARLY_STATE 2u
 
 /*
+ * KDA_LAUNCH_TEST_WITHHOLD_STATE: a test hook of kda_decode_step,
+ *   kda_spec_verify and kda_step, for the timeout path only; never for
+ *   production calls, and refused by every other entry point.  Each tile arms
+ *   its state tile's barrier but withholds the copy, so every wait on it gives
+ *   up at its 1 s bound: the call then reports KDA_ERR_TIMEOUT through
+ *   dev_status (after about 2 s: the wait, then a bounded drain), writes
+ *   neither those tiles' states nor their outputs, and the context stays
+ *   usable.  Requests that reset (no state read) are not affected.
+ */
+#define KDA_LAUNCH_TEST_WITHHOLD_STATE (1u << 30)
+
+/*
  * One layer's state pool: num_slots slots, each holding hv heads of a [k][v]
  * state (v innermost, row-major), all in device memory.
  *   state_at(slot, h) = base + (slot * slot_stride + h * k * v) elements.

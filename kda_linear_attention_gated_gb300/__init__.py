@@ -26,10 +26,11 @@ __all__ = ["KdaError", "KdaLibrary", "PoolDesc", "build", "lib_path",
            "KDA_ERR_DTYPE_MISMATCH", "KDA_ERR_DTYPE_UNSUPPORTED", "KDA_ERR_LAYERS_DISAGREE",
            "KDA_ERR_SHAPE", "KDA_ERR_ALIGN", "KDA_ERR_LAUNCH", "KDA_ERR_SLOT_RANGE",
            "KDA_ERR_ARG", "KDA_ERR_TIMEOUT", "KDA_ERR_LAYOUT", "KDA_LAUNCH_PDL", "KDA_LAUNCH_PDL_EARLY_STATE",
-           "EXPORTED_SYMBOLS"]
+           "KDA_LAUNCH_TEST_WITHHOLD_STATE", "EXPORTED_SYMBOLS"]
 
 KDA_F32, KDA_F16, KDA_BF16 = 0, 1, 2
 KDA_LAUNCH_PDL, KDA_LAUNCH_PDL_EARLY_STATE = 1, 2
+KDA_LAUNCH_TEST_WITHHOLD_STATE = 1 << 30  # test hook of the timeout path (include/kda.h)
 (KDA_OK, KDA_ERR_NULL, KDA_ERR_DTYPE_MISMATCH, KDA_ERR_DTYPE_UNSUPPORTED,
  KDA_ERR_LAYERS_DISAGREE, KDA_ERR_SHAPE, KDA_ERR_ALIGN, KDA_ERR_LAUNCH,
  KDA_ERR_SLOT_RANGE, KDA_ERR_ARG, KDA_ERR_TIMEOUT, KDA_ERR_LAYOUT) = range(12)

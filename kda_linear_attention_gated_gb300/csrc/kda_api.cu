@@ -296,7 +296,8 @@ int check_step_args(const kda_pool* pool, const int32_t* init_slot, int32_t n, i
     int rc = check_pool_for_build(pool);
     if (rc != KDA_OK) return rc;
     if (n < 0 || t < 0) return KDA_ERR_ARG;
-    if (flags & ~(uint32_t)(KDA_LAUNCH_PDL | KDA_LAUNCH_PDL_EARLY_STATE)) return KDA_ERR_ARG;
+    if (flags & ~(uint32_t)(KDA_LAUNCH_PDL | KDA_LAUNCH_PDL_EARLY_STATE | KDA_LAUNCH_TEST_WITHHOLD_STATE))
+        return KDA_ERR_ARG;
     const int qs = elem_size(qkv_dtype);
     if (qs == 0) return KDA_ERR_DTYPE_UNSUPPORTED;
     if (n == 0 || t == 0) return KDA_OK;  // nothing to do; empty buffers may be NULL
@@ -414,7 +415,8 @@ int kda_step(const kda_pool* pool, const kda_step_args* args, int32_t* dev_statu
     int rc = check_pool_for_build(pool);
     if (rc != KDA_OK) return rc;
     if (g.n < 0 || g.total < 0 || g.max_t < 0 || g.reserved != 0) return KDA_ERR_ARG;
-    if (flags & ~(uint32_t)(KDA_LAUNCH_PDL | KDA_LAUNCH_PDL_EARLY_STATE)) return KDA_ERR_ARG;
+    if (flags & ~(uint32_t)(KDA_LAUNCH_PDL | KDA_LAUNCH_PDL_EARLY_STATE | KDA_LAUNCH_TEST_WITHHOLD_STATE))
+        return KDA_ERR_ARG;
     if (elem_size(g.qkv_dtype) == 0) return KDA_ERR_DTYPE_UNSUPPORTED;
     if (g.h_qk < 1 || pool->hv % g.h_qk != 0 || g.num_cols < 1) return KDA_ERR_SHAPE;
     if (g.in_place) {

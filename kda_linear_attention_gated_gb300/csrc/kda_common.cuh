@@ -84,6 +84,7 @@ __device__ __forceinline__ float gate_alpha(float a, bool scaled, float scale, f
 
 constexpr uint32_t LAUNCH_PDL = 1u;               // KDA_LAUNCH_PDL in kda.h
 constexpr uint32_t LAUNCH_PDL_EARLY_STATE = 2u;   // KDA_LAUNCH_PDL_EARLY_STATE in kda.h
+constexpr uint32_t LAUNCH_TEST_WITHHOLD_STATE = 1u << 30;  // KDA_LAUNCH_TEST_WITHHOLD_STATE in kda.h
 
 __device__ __forceinline__ float to_f32(float x) { return x; }
 __device__ __forceinline__ float to_f32(__half x) { return __half2float(x); }

@@ -225,7 +225,8 @@ kda_verify_kernel(const __grid_constant__ CUtensorMap tmap, const StepParams p) 
     if (tid == 0 && !bad && !pad && !rst && Tn > 0) {
         prefetch_tmap(&tmap);
         mbar_arrive_expect_tx(bar_st, (uint32_t)p.k * SH::ROWBYTES);
-        tma_load_3d(smem, &tmap, bar_st, cb * BV, h * p.k, slot);
+        if (!(p.flags & LAUNCH_TEST_WITHHOLD_STATE))  // the test hook: the wait runs out
+            tma_load_3d(smem, &tmap, bar_st, cb * BV, h * p.k, slot);
     }
     if (early) {
         cudaGridDependencySynchronize();

@@ -134,6 +134,7 @@ def test_step_refusals_before_any_launch(libs):
     # unknown launch flags
     assert call(**args(desc(), flags=4)) == kda.KDA_ERR_ARG
     assert call(**args(desc(), n=0, flags=kda.KDA_LAUNCH_PDL | kda.KDA_LAUNCH_PDL_EARLY_STATE)) == kda.KDA_OK
+    assert call(**args(desc(), n=0, flags=kda.KDA_LAUNCH_TEST_WITHHOLD_STATE)) == kda.KDA_OK  # the test hook
 
 
 def test_general_step_refusals_before_any_launch(libs):
@@ -170,6 +171,7 @@ def test_general_step_refusals_before_any_launch(libs):
     assert call(args(dt_bias=P + 1)) == kda.KDA_ERR_ALIGN
     # nothing to do: succeeds without touching the GPU
     assert call(args(n=0, total=0)) == kda.KDA_OK
+    assert call(args(n=0, total=0), flags=kda.KDA_LAUNCH_TEST_WITHHOLD_STATE) == kda.KDA_OK  # the test hook
     assert call(args(total=0, cu_seqlens=P)) == kda.KDA_OK
 
 
@@ -202,6 +204,7 @@ def test_conv_step_refusals_before_any_launch(libs):
     assert call(win(), args(activation=2)) == kda.KDA_ERR_ARG
     assert call(win(reserved=1), args()) == kda.KDA_ERR_ARG
     assert call(win(), args(), flags=16) == kda.KDA_ERR_ARG
+    assert call(win(), args(), flags=kda.KDA_LAUNCH_TEST_WITHHOLD_STATE) == kda.KDA_ERR_ARG  # not a conv option
     assert call(win(), args(conv_slot=None)) == kda.KDA_ERR_NULL
     assert call(win(), args(x=P + 1)) == kda.KDA_ERR_ALIGN
     assert call(win(), args(weight=P + 2)) == kda.KDA_ERR_ALIGN
@@ -252,7 +255,7 @@ def test_prefill_refusals_before_any_launch(libs):
         f.update(kw)
         return kda.PrefillArgs(**f)
 
-    call = lambda a, d=None: L32.kda_prefill_raw(d or desc(), a, P, None, 0)  # noqa: E731
+    call = lambda a, d=None, flags=0: L32.kda_prefill_raw(d or desc(), a, P, None, flags)  # noqa: E731
     assert L32.lib.kda_prefill(ctypes.byref(desc()), None, P, 0, None) == kda.KDA_ERR_NULL
     assert call(args(), d=desc(kda.KDA_F16)) == kda.KDA_ERR_DTYPE_MISMATCH
     assert call(args(h_qk=7)) == kda.KDA_ERR_SHAPE
@@ -261,6 +264,7 @@ def test_prefill_refusals_before_any_launch(libs):
     assert call(args(final_slot=None)) == kda.KDA_ERR_NULL
     assert call(args(k=P + 8)) == kda.KDA_ERR_ALIGN
     assert call(args(n=0, total=0)) == kda.KDA_OK
+    assert call(args(), flags=kda.KDA_LAUNCH_TEST_WITHHOLD_STATE) == kda.KDA_ERR_ARG  # not a prefill option
 
 
 def test_strerror_covers_every_code(libs):
