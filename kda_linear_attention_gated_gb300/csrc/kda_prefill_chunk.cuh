@@ -179,13 +179,18 @@ __global__ void __launch_bounds__(KMAX, KDA_PREP_MINB) kda_prefill_prep_kernel(c
         wsm[t][tid] = c * kh[t];
         zsm[t][tid] = c * qh[t];
     }
+    // The workspace rows of W'^T, Q'^T and Ke^T are 64 bytes, one per thread:
+    // each is stored as four 16-byte vectors.
     if (tid < p.k) {
         w[PW_C + tid] = c;
         float e = 1.f;  // alpha_(s+1) ... alpha_(CH-1)
+        float4* kt4 = reinterpret_cast<float4*>(w + PW_KT + tid * PCH);
+        float kv[4];
 #pragma unroll
         for (int s = PCH - 1; s >= 0; --s) {
-            w[PW_KT + tid * PCH + s] = bk[s] * e;
+            kv[s & 3] = bk[s] * e;
             e *= al[s];
+            if ((s & 3) == 0) kt4[s >> 2] = make_float4(kv[0], kv[1], kv[2], kv[3]);
         }
     }
     {
@@ -220,6 +225,9 @@ __global__ void __launch_bounds__(KMAX, KDA_PREP_MINB) kda_prefill_prep_kernel(c
         u[t] = xu;
     }
     const int vt = tid / PVT, vc = tid - vt * PVT;
+    float4* wt4 = reinterpret_cast<float4*>(w + PW_WT + tid * PCH);
+    float4* qt4 = reinterpret_cast<float4*>(w + PW_QT + tid * PCH);
+    float qv[4];
 #pragma unroll
     for (int t = 0; t < PCH; ++t) {
         float qp = zsm[t][tid], oi = 0.f;
@@ -229,9 +237,10 @@ __global__ void __launch_bounds__(KMAX, KDA_PREP_MINB) kda_prefill_prep_kernel(c
             qp = fmaf(-bts, wp[s], qp);
             oi = fmaf(bts, u[s], oi);
         }
-        if (tid < p.k) {
-            w[PW_WT + tid * PCH + t] = wp[t];
-            w[PW_QT + tid * PCH + t] = qp * p.inv_sqrt_k;
+        qv[t & 3] = qp * p.inv_sqrt_k;
+        if ((t & 3) == 3 && tid < p.k) {
+            wt4[t >> 2] = make_float4(wp[t - 3], wp[t - 2], wp[t - 1], wp[t]);
+            qt4[t >> 2] = make_float4(qv[0], qv[1], qv[2], qv[3]);
         }
         if (tid < p.v) {
             w[PW_U + (vt * PCH + t) * PVT + vc] = u[t];
