@@ -217,6 +217,30 @@ def test_saturated_gates_match_oracle(state_dtype):
     assert_pool_match(gpool, ref, ver.snap_slot.numpy(), "verify snapshots")
 
 
+@pytest.mark.parametrize("state_dtype", [torch.float32, torch.float16])
+def test_zero_k_and_q_rows_match_oracle(state_dtype):
+    """All-zero k or q rows (the norm's epsilon keeps khat = 0 and qhat = 0, no
+    NaN): the update is the decay alone and the output is zero where q is."""
+    dec = workloads.make_decode(n=8, hv=4, k=128, v=128, num_slots=16, state_dtype=state_dtype, seed=59)
+    dec.k[::2, 1] = 0.0
+    dec.q[1::3, 2] = 0.0
+    gpool, o, st = gpu_decode(dec)
+    assert st == 0
+    ref, o_ref = oracle_decode(dec)
+    assert np.isfinite(o.numpy()).all()
+    assert_out_match(o, o_ref, state_dtype, "decode o")
+    assert_pool_match(gpool, ref, dec.init_slot.numpy(), "decode pool")
+    ver = workloads.make_verify(n=4, t=5, hv=4, k=128, v=128, num_slots=32, state_dtype=state_dtype, seed=60)
+    ver.k[:, 1::2, 1] = 0.0   # tokens 1 and 3 of head 1
+    ver.q[2, :, 3] = 0.0      # every token of request 2, head 3
+    gpool, o, st = gpu_verify(ver)
+    assert st == 0
+    ref, o_ref = oracle_verify(ver)
+    assert np.isfinite(o.numpy()).all()
+    assert_out_match(o, o_ref, state_dtype, "verify o")
+    assert_pool_match(gpool, ref, ver.snap_slot.numpy(), "verify snapshots")
+
+
 def test_verify_equals_chained_decode_on_fp32_pool():
     """An fp32 pool stores the fp32 carry exactly, so T decode calls and one
     T-token verify agree up to the order of the fp32 sums over K (the two
