@@ -4,8 +4,9 @@
 // rows; BV * sizeof(state) is 64 or 128 bytes, one warp per 16-byte column
 // chunk.  The state tile is TMA-loaded once from init_slot[n] (or taken as
 // zero on reset); the per-token inputs are plain coalesced loads, thread r
-// taking row r of q, k and a and column r of the v slice.  Lane l of warp w then carries rows l, l+32, l+64, l+96 of
-// chunk w in fp32 registers through the T tokens without rounding.  After each
+// taking row r of q, k and a and column r of the v slice.  Lane l of warp w
+// then carries rows l, l+32, l+64, l+96 of chunk w in fp32 registers through
+// the T tokens without rounding.  After each
 // token the state, rounded to the pool's dtype, is written to a swizzled
 // shared-memory staging tile and from there to that token's snapshot slot
 // snap_slot[n][t] (ROCm/ATOM pull request 2945, Changes: the state after each

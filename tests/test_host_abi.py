@@ -295,3 +295,20 @@ def test_library_missing_fails_loudly(monkeypatch, tmp_path):
     monkeypatch.setattr(pkg, "_libs", {})
     with pytest.raises(RuntimeError, match="no CPU fallback"):
         pkg.KdaLibrary(torch.float32)
+
+
+def test_source_hash_ignores_comments_and_layout_but_not_code(tmp_path, monkeypatch):
+    """The profile summaries' staleness check: comments and whitespace do not
+    change the hash, string literals and preprocessor line breaks are kept,
+    and any code change does."""
+    import kda_linear_attention_gated_gb300 as pkg
+    src = 'int a = 1; // note\n/* two\n lines */ const char* s = "x // y";\n#define X 1 /* t */\n'
+    assert pkg.code_text(src) == 'int a = 1;\nconst char* s = "x // y";\n#define X 1'
+    f = tmp_path / "k.cu"
+    f.write_text(src)
+    monkeypatch.setattr(pkg, "SOURCES", [str(f)])
+    h0 = pkg.source_hash()
+    f.write_text("  // a new comment\n\n" + src.replace("// note", "// edited   note").replace("int a", "int   a"))
+    assert pkg.source_hash() == h0  # comments, blank lines and runs of spaces
+    f.write_text(src.replace("int a = 1;", "int a = 2;"))
+    assert pkg.source_hash() != h0  # code
