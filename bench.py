@@ -625,7 +625,8 @@ def bench_prefill(kda, workloads, torch, n, t, chunked=False, reps=5):
 def bench_ckpt(kda, workloads, torch, peak, replays=200, load=False):
     """Checkpoint flush of 64 fp32 states (12 x 128 x 128) from a 256-slot pool
     to a 128-entry plane (load: the reverse copy); 24 pool/plane pairs rotate
-    (4.8 GB, far past L2)."""
+    (4.8 GB, far past L2), launched with programmatic dependent launch (the
+    kernel reads nothing before the previous kernel completes)."""
     lib = kda.KdaLibrary(torch.float32)
     g = torch.Generator().manual_seed(9)
     R = 24
@@ -642,7 +643,7 @@ def bench_ckpt(kda, workloads, torch, peak, replays=200, load=False):
         stream.synchronize()
         with torch.cuda.graph(g_, stream=stream):
             for i in range(R):
-                call(pools[i], planes[i], slots, entries, status)
+                call(pools[i], planes[i], slots, entries, status, flags=kda.KDA_LAUNCH_PDL)
         for _ in range(3):
             g_.replay()
     torch.cuda.synchronize()
@@ -662,7 +663,7 @@ def bench_ckpt(kda, workloads, torch, peak, replays=200, load=False):
     torch.cuda.empty_cache()
     what = ("checkpoint load, 64 fp32 states [12,128,128], 128-entry plane -> 256-slot pool" if load else
             "checkpoint flush, 64 fp32 states [12,128,128], 256-slot pool -> 128-entry plane")
-    return {"workload": what,
+    return {"workload": what, "launch": f"CUDA graph of {R} launches, replayed; flags KDA_LAUNCH_PDL",
             "us_per_call": round(us, 3), "gbs": round(byt / (us * 1e-6) / 1e9, 1),
             "frac_of_peak": round(byt / (us * 1e-6) / 1e9 / peak, 4), "bytes_per_call": byt}
 
