@@ -79,6 +79,13 @@ struct VerifyShape {
     static constexpr uint32_t RED_AB = RED_ABW + NW * 64 * 4, RED_RES = RED_AB + 64 * 4;
     static constexpr uint32_t RED_D = RED_RES + TC * 2 * BV * 4, RED_SNAP = RED_D + TC * BV * 4;
     static constexpr uint32_t RED_BYTES = (RED_SNAP + TC * 4 + 15u) & ~15u;
+    // tensor-core column sums (fp16 pool, first chunk, K = KMAX): the gates of
+    // the 2 TC token-kind rows in three fp16 parts, [3][2 TC][G16_STRIDE] halves;
+    // rows of 272 bytes keep the ldmatrix row reads free of bank conflicts
+    static constexpr bool MMA_CS = sizeof(ST) == 2 && 2 * TC == 16 && VEC == 8;
+    static constexpr int G16_STRIDE = KMAX + 8;
+    static constexpr uint32_t G16_ARRAY = 2 * TC * G16_STRIDE * 2;
+    static constexpr uint32_t G16_BYTES = MMA_CS ? 3 * G16_ARRAY : 0;
     static_assert(ROWBYTES == 128 || ROWBYTES == 64, "tile row bytes");
     static_assert(NT >= KMAX, "one thread per key row in the gate phase");
     static_assert(NA + NB == 64 && 2 * G * VEC == 32 && TC % G == 0 && TC == 8, "chunk shape");
@@ -91,7 +98,7 @@ struct VerifyShape {
 template <typename ST, int BV, int QES>
 constexpr size_t verify_smem_bytes() {
     using SH = VerifyShape<ST, BV, QES>;
-    return SH::NSTAGE * SH::TILE_BYTES + SH::WORK_BYTES + SH::RED_BYTES + 16;
+    return SH::NSTAGE * SH::TILE_BYTES + SH::WORK_BYTES + SH::RED_BYTES + SH::G16_BYTES + 16;
 }
 
 // Position of A_ts (s < t) and of B_ts (s <= t) among a chunk's 64 row sums.
@@ -137,7 +144,8 @@ kda_verify_kernel(const __grid_constant__ CUtensorMap tmap, const StepParams p) 
     float* res = reinterpret_cast<float*>(redb + SH::RED_RES);     // [TC][2][BV]
     float* dsm = reinterpret_cast<float*>(redb + SH::RED_D);       // [TC][BV]
     int32_t* snaps = reinterpret_cast<int32_t*>(redb + SH::RED_SNAP);  // [TC]
-    uint64_t* bar_st = reinterpret_cast<uint64_t*>(redb + SH::RED_BYTES);
+    __half* g16 = reinterpret_cast<__half*>(redb + SH::RED_BYTES);  // [3][2 TC][G16_STRIDE] (fp16 pool)
+    uint64_t* bar_st = reinterpret_cast<uint64_t*>(redb + SH::RED_BYTES + SH::G16_BYTES);
     const uint32_t tile_base = smem_u32(smem);
     const uint32_t gate_base = smem_u32(gts);
 
@@ -284,12 +292,33 @@ kda_verify_kernel(const __grid_constant__ CUtensorMap tmap, const StepParams p) 
 #pragma unroll
                 for (int j = 0; j < TC; ++j) at[j] = j < tc && tid < p.k ? gate_alpha(at[j], false, gscale, gbias) : 0.f;
             }
+            // the first chunk of an fp16 pool at K = KMAX takes its column sums
+            // on the tensor cores: rows 2 j (c k) and 2 j + 1 (c q) of the gate
+            // matrix, each value split into three fp16 parts g = h0 + h1 2^-11 +
+            // h2 2^-22 (exact differences; the rest is below 2^-33 |g|)
+            const bool mma_cs = SH::MMA_CS && t0 == 0 && !rst && p.k == KMAX;
+            auto g16_put = [&](int m, float g) {
+                const __half h0 = __float2half_rn(g);
+                const float r1 = (g - __half2float(h0)) * 2048.f;
+                const __half h1 = __float2half_rn(r1);
+                const __half h2 = __float2half_rn((r1 - __half2float(h1)) * 2048.f);
+                __half* row = g16 + m * SH::G16_STRIDE + tid;
+                row[0] = h0;
+                row[2 * TC * SH::G16_STRIDE] = h1;
+                row[4 * TC * SH::G16_STRIDE] = h2;
+            };
             float cdec = 1.f;
 #pragma unroll
             for (int j = 0; j < TC; ++j) {
                 cdec *= at[j];  // c_j: alpha of tokens 0 .. j
                 if (j < tc && tid < p.k)
                     reinterpret_cast<float4*>(gts + j * SH::G_TOK)[tid] = make_float4(cdec * kt[j], cdec * qt[j], at[j], kt[j]);
+                if constexpr (SH::MMA_CS) {
+                    if (mma_cs) {  // past tc the raw k and q are zero, so are these rows
+                        g16_put(2 * j, cdec * kt[j]);
+                        g16_put(2 * j + 1, cdec * qt[j]);
+                    }
+                }
             }
             float sq[2 * TC];
 #pragma unroll
@@ -365,10 +394,42 @@ kda_verify_kernel(const __grid_constant__ CUtensorMap tmap, const StepParams p) 
         }
 
         // (3) the column sums of the chunk's initial state against c k and
-        // c q of every token, G tokens (32 values per lane) at a time; the
-        // groups run as a loop (fewer instructions to fetch)
+        // c q of every token.  Tensor cores where the first chunk's state is
+        // the fp16 tile itself: warp w multiplies the 16 x 128 gate matrix by
+        // its 128 x 8 slice of the tile, once per fp16 part, and adds the
+        // parts' fp32 sums at their scales (rows and columns of the products:
+        // lane l holds rows l / 4 and l / 4 + 8, columns 2 (l % 4) and + 1)
+        if constexpr (SH::MMA_CS) {
+            if (t0 == 0 && !rst && p.k == KMAX) {
+                float acc[3][4] = {};
+                const uint32_t gb16 = smem_u32(g16) + ((lane & 15) * SH::G16_STRIDE + (lane >> 4) * 8) * 2;
+#pragma unroll
+                for (int kb = 0; kb < KMAX; kb += 16) {
+                    uint32_t b0, b1;  // rows kb .. kb + 15 of this warp's 8 columns
+                    ldsm_x2_trans(tile_base + swz<SH::ROWBYTES>(kb + (lane & 15), chunk), b0, b1);
+#pragma unroll
+                    for (int part = 0; part < 3; ++part) {
+                        uint32_t a0, a1, a2, a3;
+                        ldsm_x4(gb16 + part * SH::G16_ARRAY + kb * 2, a0, a1, a2, a3);
+                        mma_16816_f16(acc[part], a0, a1, a2, a3, b0, b1);
+                    }
+                }
+                const int m = lane >> 2, c = (lane & 3) * 2;
+                float* r0 = res + m * BV + chunk * VEC + c;
+                float* r8 = res + (m + 8) * BV + chunk * VEC + c;
+                constexpr float S1 = 1.f / 2048.f, S2 = 1.f / (2048.f * 2048.f);
+                r0[0] = fmaf(acc[2][0], S2, fmaf(acc[1][0], S1, acc[0][0]));
+                r0[1] = fmaf(acc[2][1], S2, fmaf(acc[1][1], S1, acc[0][1]));
+                r8[0] = fmaf(acc[2][2], S2, fmaf(acc[1][2], S1, acc[0][2]));
+                r8[1] = fmaf(acc[2][3], S2, fmaf(acc[1][3], S1, acc[0][3]));
+            }
+        }
+        // Otherwise on the CUDA cores from the fp32 carry, G tokens (32 values
+        // per lane) at a time; the groups run as a loop (fewer instructions to
+        // fetch)
+        const bool fma_cs = !(SH::MMA_CS && t0 == 0 && !rst && p.k == KMAX);
 #pragma unroll 1
-        for (int g0 = 0; g0 < TC; g0 += G) {
+        for (int g0 = 0; fma_cs && g0 < TC; g0 += G) {
             if (g0 < tc) {
                 float acc[2 * G * VEC];
 #pragma unroll
