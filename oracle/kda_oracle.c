@@ -552,7 +552,10 @@ int oracle_ckpt_transfer(void* pool_base, int64_t num_slots, int64_t slot_stride
  * init_slot[r] (zero when reset[r]; a negative init_slot is a padding request:
  * nothing read or stored, outputs zero) and only the state after its last
  * token is stored, to final_slot[r] (negative: not stored; may equal
- * init_slot[r]).  A request with no tokens is left alone (nothing stored).
+ * init_slot[r]).  A request with no tokens stores its initial state (zero
+ * when reset[r]) to final_slot[r]: the state after its last token is the state
+ * it started from, so splitting a prompt into an empty part and the rest
+ * changes nothing.
  * Heads, gate and layouts as in oracle_step.  Returns 0, -1 slot out of range,
  * -3 layout.
  */
@@ -602,7 +605,7 @@ int oracle_prefill(void* base, int dtype, int64_t num_slots, int hv, int k, int 
             recur_token_gated(K, V, S, q + qrow * K, kk + qrow * K, vv + vrow * V, a + vrow * K,
                               b[vrow], scale, bias, o + vrow * V, qh, kh, u);
         }
-        if (final_slot[r] >= 0 && tr > 0) store_state(&p, final_slot[r], h, S);
+        if (final_slot[r] >= 0) store_state(&p, final_slot[r], h, S);
         free(S);
     }
     (void)nthreads;

@@ -87,3 +87,55 @@ def test_padding_and_unstored_final():
     assert (o[:4] == 0).all() and (o[4:] != 0).any()
     changed = np.nonzero([not np.array_equal(pool[s], before[s]) for s in range(8)])[0].tolist()
     assert changed == [int(final[2])]
+
+
+@pytest.mark.parametrize("reset", [0, 1])
+@pytest.mark.parametrize("state_dtype", [torch.float32, torch.float16])
+def test_empty_first_part_split_equals_whole_prompt(state_dtype, reset):
+    """A prompt split as 0 | T, init and final slots distinct: the empty call
+    must leave the final slot holding the request's initial state (zero on a
+    reset), so that the second call, from the final slot, reproduces the whole
+    prompt bit for bit.  A rule that left an empty request alone would make
+    the second call start from whatever the final slot held before."""
+    T = 11
+    inp = workloads.make_prefill(lens=(T,), hv=2, k=16, v=32, num_slots=6, state_dtype=state_dtype,
+                                 qkv_dtype=torch.float32, seed=5, reset_p=float(reset), same_slot_p=0.0)
+    assert int(inp.init_slot[0]) != int(inp.final_slot[0])
+    rs = np.array([reset], np.uint8)
+    whole = pnp(inp.pool)
+    ow = oracle.prefill(whole, inp.init_slot, inp.final_slot, inp.q, inp.k, inp.v, inp.a, inp.b,
+                        cu_seqlens=inp.cu_seqlens, reset=rs)
+    part = pnp(inp.pool)
+    empty = lambda x: x[:0]  # noqa: E731
+    o1 = oracle.prefill(part, inp.init_slot, inp.final_slot, *(empty(x) for x in (inp.q, inp.k, inp.v, inp.a, inp.b)),
+                        cu_seqlens=np.array([0, 0], np.int32), reset=rs)
+    assert o1.shape == (0, 2, 32)
+    f, i = int(inp.final_slot[0]), int(inp.init_slot[0])
+    before = pnp(inp.pool)
+    if reset:
+        assert not part[f].any()
+    else:
+        assert part[f].tobytes() == before[i].tobytes()
+    others = [s for s in range(6) if s != f]
+    assert part[others].tobytes() == before[others].tobytes()
+    o2 = oracle.prefill(part, inp.final_slot, inp.final_slot, inp.q, inp.k, inp.v, inp.a, inp.b,
+                        cu_seqlens=inp.cu_seqlens)
+    assert np.array_equal(o2, ow)
+    assert part.tobytes() == whole.tobytes()
+
+
+def test_empty_middle_part_changes_nothing():
+    """T1 | 0 | T2 on one slot equals T1 | T2: an empty call from a slot to the
+    same slot rewrites its state with itself."""
+    inp = workloads.make_prefill(lens=(14,), hv=2, k=16, v=16, num_slots=4, state_dtype=torch.float16,
+                                 qkv_dtype=torch.float32, seed=6, reset_p=0.0, same_slot_p=1.0)
+    s = inp.init_slot
+    a = pnp(inp.pool)
+    oracle.prefill(a, s, s, inp.q[:5], inp.k[:5], inp.v[:5], inp.a[:5], inp.b[:5])
+    b = a.copy()
+    oracle.prefill(b, s, s, inp.q[:0], inp.k[:0], inp.v[:0], inp.a[:0], inp.b[:0],
+                   cu_seqlens=np.array([0, 0], np.int32))
+    assert a.tobytes() == b.tobytes()
+    oracle.prefill(a, s, s, inp.q[5:], inp.k[5:], inp.v[5:], inp.a[5:], inp.b[5:])
+    oracle.prefill(b, s, s, inp.q[5:], inp.k[5:], inp.v[5:], inp.a[5:], inp.b[5:])
+    assert a.tobytes() == b.tobytes()
