@@ -325,7 +325,10 @@ int kda_conv_step(const kda_conv_window* win, const kda_conv_args* args, int32_t
  * reset[r] is nonzero: a fresh prompt; a negative init_slot is a padding
  * request, nothing read or stored, outputs zero) and, after its last token,
  * is stored to final_slot[r] (negative: not stored; it may equal init_slot[r]).
- * No per-token state is stored.  A request with no tokens is left alone.
+ * No per-token state is stored.  A request with no tokens stores its initial
+ * state (zero on a reset) to final_slot[r] unchanged: the state after its last
+ * token is the one it started from, so a prompt split into an empty part and
+ * the rest gives the same final state as the whole prompt.
  * Heads, gate and layouts as in kda_step_args; o gets every token's output.
  */
 typedef struct kda_prefill_args {
@@ -353,6 +356,8 @@ typedef struct kda_prefill_args {
  * Prefill (see kda_prefill_args).  Host checks as for kda_step (KDA_ERR_SHAPE
  * for total != n * max_t without cu_seqlens); device: KDA_ERR_ARG for offsets
  * outside 0 .. max_t or past total, KDA_ERR_SLOT_RANGE for a slot >= num_slots.
+ * n == 0 is a no-op.  total == 0 with n > 0 still stores every request's
+ * initial state to its final slot; q, k, v, a, b and o may then be NULL.
  */
 int kda_prefill(const kda_pool* pool, const kda_prefill_args* args, int32_t* dev_status, uint32_t flags,
                 void* stream);

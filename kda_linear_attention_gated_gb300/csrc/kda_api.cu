@@ -459,9 +459,11 @@ int kda_prefill(const kda_pool* pool, const kda_prefill_args* args, int32_t* dev
     if (elem_size(g.qkv_dtype) == 0) return KDA_ERR_DTYPE_UNSUPPORTED;
     if (g.h_qk < 1 || pool->hv % g.h_qk != 0) return KDA_ERR_SHAPE;
     if (g.cu_seqlens == nullptr && (int64_t)g.total != (int64_t)g.n * g.max_t) return KDA_ERR_SHAPE;
-    if (g.n == 0 || g.total == 0 || g.max_t == 0) return KDA_OK;
-    if (!g.init_slot || !g.final_slot || !g.q || !g.k || !g.v || !g.a || !g.b || !g.o || !dev_status)
-        return KDA_ERR_NULL;
+    // with no tokens at all there is still work: each request's initial state
+    // goes to its final slot (the token buffers may then be NULL)
+    if (g.n == 0) return KDA_OK;
+    if (!g.init_slot || !g.final_slot || !dev_status) return KDA_ERR_NULL;
+    if (g.total > 0 && (!g.q || !g.k || !g.v || !g.a || !g.b || !g.o)) return KDA_ERR_NULL;
     if (!aligned(g.init_slot, 4) || !aligned(g.final_slot, 4) || !aligned(dev_status, 4) || !aligned(g.b, 4) ||
         !aligned(g.o, 4) || !aligned(g.a, 16) || !aligned(g.q, 16) || !aligned(g.k, 16) || !aligned(g.v, 16) ||
         (g.cu_seqlens && !aligned(g.cu_seqlens, 4)) || (g.a_log && !aligned(g.a_log, 4)) ||
@@ -498,10 +500,10 @@ int kda_prefill_chunked(const kda_pool* pool, const kda_prefill_args* args, void
     if (elem_size(g.qkv_dtype) == 0) return KDA_ERR_DTYPE_UNSUPPORTED;
     if (g.h_qk < 1 || pool->hv % g.h_qk != 0) return KDA_ERR_SHAPE;
     if (g.cu_seqlens == nullptr && (int64_t)g.total != (int64_t)g.n * g.max_t) return KDA_ERR_SHAPE;
-    if (g.n == 0 || g.total == 0 || g.max_t == 0) return KDA_OK;
-    if (!g.init_slot || !g.final_slot || !g.q || !g.k || !g.v || !g.a || !g.b || !g.o || !dev_status ||
-        !workspace)
-        return KDA_ERR_NULL;
+    // as in kda_prefill: with no tokens the scan pass alone stores the initial states
+    if (g.n == 0) return KDA_OK;
+    if (!g.init_slot || !g.final_slot || !dev_status || !workspace) return KDA_ERR_NULL;
+    if (g.total > 0 && (!g.q || !g.k || !g.v || !g.a || !g.b || !g.o)) return KDA_ERR_NULL;
     int64_t need = 0;
     kda_prefill_workspace_bytes(pool, g.n, g.total, &need);
     if (workspace_bytes < need) return KDA_ERR_ARG;
@@ -532,11 +534,13 @@ int kda_prefill_chunked(const kda_pool* pool, const kda_prefill_args* args, void
     cfg.blockDim = dim3(kda::KMAX, 1, 1);
     cfg.stream = st;
     set_pdl(cfg, &attr, flags);
-    cudaError_t err;
-    switch (g.qkv_dtype) {
-        case KDA_F32: err = cudaLaunchKernelEx(&cfg, kda::kda_prefill_prep_kernel<float>, prm, ws, max_chunks); break;
-        case KDA_F16: err = cudaLaunchKernelEx(&cfg, kda::kda_prefill_prep_kernel<__half>, prm, ws, max_chunks); break;
-        default: err = cudaLaunchKernelEx(&cfg, kda::kda_prefill_prep_kernel<__nv_bfloat16>, prm, ws, max_chunks); break;
+    cudaError_t err = cudaSuccess;
+    if (max_chunks > 0) {  // no chunk at all (max_t == 0): only the scan pass runs
+        switch (g.qkv_dtype) {
+            case KDA_F32: err = cudaLaunchKernelEx(&cfg, kda::kda_prefill_prep_kernel<float>, prm, ws, max_chunks); break;
+            case KDA_F16: err = cudaLaunchKernelEx(&cfg, kda::kda_prefill_prep_kernel<__half>, prm, ws, max_chunks); break;
+            default: err = cudaLaunchKernelEx(&cfg, kda::kda_prefill_prep_kernel<__nv_bfloat16>, prm, ws, max_chunks); break;
+        }
     }
     if (err != cudaSuccess) return KDA_ERR_LAUNCH;
     // the widest scan tiling (32, 16 or 8 value columns per CTA) whose grid

@@ -308,7 +308,9 @@ __global__ void __launch_bounds__(PSCAN_WARPS * 32) kda_prefill_scan_kernel(cons
         }
         return;
     }
-    if (Tn == 0) return;
+    // a request with no tokens stores its initial state (zero on a reset) to
+    // its final slot: the state after its last token
+    if (Tn == 0 && fin_slot < 0) return;
     const int nch = (Tn + PCH - 1) / PCH;
     const int row0 = warp * PSCAN_ROWS + rq * RPT;  // this thread's rows: row0 .. row0 + RPT - 1
 
@@ -340,12 +342,12 @@ __global__ void __launch_bounds__(PSCAN_WARPS * 32) kda_prefill_scan_kernel(cons
         mbar_init(bars, 1);
         mbar_init(bars + 1, 1);
         fence_mbar_init();
-        issue(0);
+        if (nch > 0) issue(0);
     }
     __syncthreads();
 
     // chunk j is buffer j % 2's (j / 2)-th use: barrier parity (j / 2) % 2
-    int jfail = -1, issued = 1;
+    int jfail = -1, issued = nch > 0 ? 1 : 0;
     for (int j = 0; j < nch; ++j) {
         if (j + 1 < nch) {  // its buffer's last reader was chunk j - 1
             if (tid == 0) issue(j + 1);

@@ -90,6 +90,9 @@ struct VerifyShape {
     static_assert(NT >= KMAX, "one thread per key row in the gate phase");
     static_assert(NA + NB == 64 && 2 * G * VEC == 32 && TC % G == 0 && TC == 8, "chunk shape");
     static_assert(BV == 32 && TC % NW == 0, "the solve: a lane per column, whole token shares per warp");
+    // the gate matrix of the tensor-core column sums has one column per key
+    // row, written by thread tid for row tid: exactly KMAX threads
+    static_assert(!MMA_CS || NT == KMAX, "tensor-core column sums need one thread per key row");
     static_assert(NSTAGE >= 2, "staging buffers");
     static_assert(G_TOK % 16 == 0 &&
                   WORK_BYTES % 16 == 0 && RED_RES % 16 == 0 && RED_D % 16 == 0, "layout");
@@ -231,7 +234,10 @@ kda_verify_kernel(const __grid_constant__ CUtensorMap tmap, const StepParams p) 
     bad = __any_sync(0xffffffffu, bad);  // the same answer in every warp
     const bool pad = !bad && slot < 0;     // a padding request
     const bool rst = !bad && p.reset != nullptr && p.reset[n] != 0;
-    if (tid == 0 && !bad && !pad && !rst && Tn > 0) {
+    // A prefill request with no tokens still stores its initial state (zero on
+    // a reset) to its final slot: the state after its last token.
+    const bool need_state = Tn > 0 || (final_mode && fin >= 0);
+    if (tid == 0 && !bad && !pad && !rst && need_state) {
         prefetch_tmap(&tmap);
         mbar_arrive_expect_tx(bar_st, (uint32_t)p.k * SH::ROWBYTES);
         if (!(p.flags & LAUNCH_TEST_WITHHOLD_STATE))  // the test hook: the wait runs out
@@ -241,7 +247,7 @@ kda_verify_kernel(const __grid_constant__ CUtensorMap tmap, const StepParams p) 
         cudaGridDependencySynchronize();
         if (PRO_INPUTS && issued) load_inputs(0, min(TC, Tn));
     }
-    if (bad || pad || Tn == 0) {
+    if (bad || pad || !need_state) {
         if (pad)  // padding: this tile's outputs of every token are zero
             for (int e = tid; e < Tn * vcols; e += SH::NT)
                 p.o[((int64_t)(tb + e / vcols) * p.hv + h) * p.v + cb * BV + e % vcols] = 0.f;
@@ -253,6 +259,23 @@ kda_verify_kernel(const __grid_constant__ CUtensorMap tmap, const StepParams p) 
     float x[ROWS][VEC];
     bool state_in = false;
     bool alive = true;
+    if (Tn == 0) {  // prefill, empty prompt: the loaded tile (or zeros) goes to the final slot as is
+        const bool ok = rst || mbar_wait(bar_st, 0);
+        if (__syncthreads_or(ok ? 0 : 1)) {
+            alive = false;
+        } else {
+            if (rst) {
+                for (int e = tid; e < p.k * (SH::ROWBYTES / 16); e += SH::NT)
+                    sts128(tile_base + e * 16, make_uint4(0u, 0u, 0u, 0u));
+                fence_proxy_async_smem();
+            }
+            __syncthreads();
+            if (tid == 0) {
+                tma_store_3d(&tmap, smem, cb * BV, h * p.k, fin);
+                bulk_commit();
+            }
+        }
+    }
     const bool scaled = p.a_log != nullptr;
     const float gscale = scaled ? expf(__ldg(p.a_log + h)) : 1.f;
     const float gbias = p.dt_bias != nullptr && tid < p.k ? __ldg(p.dt_bias + (int64_t)h * p.k + tid) : 0.f;

@@ -33,8 +33,9 @@ def run(inp, flags=0, chunked=False):
 
 
 def written(inp):
-    lens = inp.meta["lens"]
-    return [int(f) for f, i, t in zip(inp.final_slot, inp.init_slot, lens) if f >= 0 and i >= 0 and t > 0]
+    """Final slots a call writes: every non-padding request with a final slot,
+    an empty one included (it stores its initial state there)."""
+    return [int(f) for f, i in zip(inp.final_slot, inp.init_slot) if f >= 0 and i >= 0]
 
 
 CHUNKED = [False, True]
@@ -98,3 +99,36 @@ def test_chunked_prefill_workspace_too_small_is_refused():
                                 workspace=torch.empty(need - 256, dtype=torch.uint8, device="cuda"),
                                 cu_seqlens=d.cu_seqlens, max_t=20, reset=d.reset)
     assert e.value.code == kda.KDA_ERR_ARG
+
+
+@pytest.mark.parametrize("chunked", CHUNKED)
+@pytest.mark.parametrize("state_dtype", SD)
+def test_prefill_empty_prompts_store_their_initial_state(state_dtype, chunked):
+    """Requests with no tokens beside ones with tokens, init and final slots
+    distinct, with and without reset: an empty request's final slot gets its
+    initial state bit for bit (zeros on a reset), as the oracle says."""
+    inp = workloads.make_prefill(lens=(0, 7, 0, 0, 20), hv=12, k=128, v=128, num_slots=12, state_dtype=state_dtype,
+                                 qkv_dtype=torch.bfloat16, seed=95, reset_p=0.0, same_slot_p=0.0)
+    inp.reset[:] = torch.tensor([0, 0, 1, 0, 1], dtype=torch.uint8)
+    gp, o, st, P, o_ref = run(inp, chunked=chunked)
+    assert st == 0
+    before = pool_np(inp.pool)
+    for r, lr in enumerate(inp.meta["lens"]):
+        if lr == 0:
+            f, i = int(inp.final_slot[r]), int(inp.init_slot[r])
+            expect = np.zeros_like(before[i]) if int(inp.reset[r]) else before[i]
+            assert pool_np(gp)[f].tobytes() == expect.tobytes()
+    assert_out_match(o, o_ref, state_dtype, "o")
+    assert_pool_match(gp, P, written(inp), "pool")
+
+
+@pytest.mark.parametrize("chunked", CHUNKED)
+@pytest.mark.parametrize("state_dtype", SD)
+def test_prefill_call_without_tokens(state_dtype, chunked):
+    """total == 0 (every prompt empty, max_t 0, NULL token buffers): the call
+    still moves each request's initial state to its final slot."""
+    inp = workloads.make_prefill(lens=(0, 0, 0), hv=3, k=48, v=80, num_slots=8, state_dtype=state_dtype,
+                                 qkv_dtype=torch.float32, seed=96, reset_p=0.5, same_slot_p=0.0, pad_p=0.3)
+    gp, o, st, P, o_ref = run(inp, chunked=chunked)
+    assert st == 0 and o.shape[0] == 0
+    assert_pool_match(gp, P, written(inp), "pool")

@@ -33,27 +33,43 @@ def test_too_large_for_the_scratch_is_refused_before_any_launch(built_libs):
 @pytest.mark.gpu
 @pytest.mark.usefixtures("built_libs", "oracle_mod")
 @pytest.mark.parametrize("state_dtype", [torch.float32, torch.float16])
-def test_noalloc_prefill_matches_oracle_and_allocates_nothing(state_dtype):
-    inp = workloads.make_prefill(lens=(200, 37), state_dtype=state_dtype, seed=95)
+def test_noalloc_prefill_matches_workspace_entry_and_allocates_nothing(state_dtype):
+    """Two no-alloc calls in a row, each on a fresh copy of the pool, against
+    kda_prefill_chunked with a caller workspace (and against the oracle): the
+    same outputs and final states within the parity tolerances, and no device
+    memory allocated by the second call."""
+    inp = workloads.make_prefill(lens=(200, 0, 37), state_dtype=state_dtype, seed=95, same_slot_p=0.3)
     d = inp.to("cuda")
     total, hv, v = d.v.shape
-    o = torch.full((total, hv, v), float("nan"), device="cuda")
-    status = torch.zeros(1, dtype=torch.int32, device="cuda")
     lib = lib_for(state_dtype)
     kw = dict(cu_seqlens=d.cu_seqlens, max_t=inp.max_t, reset=d.reset)
-    # first call on a copy: loads the module and looks up the scratch address
-    lib.kda_prefill_chunked_noalloc(d.pool.clone(), d.init_slot, d.final_slot, d.q, d.k, d.v, d.a, d.b, o, status,
-                                    **kw)
+    args = (d.init_slot, d.final_slot, d.q, d.k, d.v, d.a, d.b)
+
+    def buffers():
+        return (d.pool.clone(), torch.full((total, hv, v), float("nan"), device="cuda"),
+                torch.zeros(1, dtype=torch.int32, device="cuda"))
+
+    pool_w, o_w, st_w = buffers()
+    ws = torch.empty(lib.kda_prefill_workspace_bytes(d.pool, len(inp.meta["lens"]), total), dtype=torch.uint8,
+                     device="cuda")
+    lib.kda_prefill_chunked(pool_w, *args, o_w, st_w, workspace=ws, **kw)
+    # first call: may load the module and look up the scratch address
+    pool_1, o_1, st_1 = buffers()
+    lib.kda_prefill_chunked_noalloc(pool_1, *args, o_1, st_1, **kw)
+    pool_2, o_2, st_2 = buffers()
     torch.cuda.synchronize()
     free0, alloc0 = torch.cuda.mem_get_info()[0], torch.cuda.memory_allocated()
-    lib.kda_prefill_chunked_noalloc(d.pool, d.init_slot, d.final_slot, d.q, d.k, d.v, d.a, d.b, o, status, **kw)
+    lib.kda_prefill_chunked_noalloc(pool_2, *args, o_2, st_2, **kw)
     torch.cuda.synchronize()
     assert torch.cuda.mem_get_info()[0] == free0 and torch.cuda.memory_allocated() == alloc0
-    assert int(status.item()) == 0
+    assert int(st_w.item()) == 0 and int(st_1.item()) == 0 and int(st_2.item()) == 0
+    written = [int(f) for f, i in zip(inp.final_slot, inp.init_slot) if f >= 0 and i >= 0]
+    ref_pool, ref_o = pool_np(pool_w), o_w.cpu().numpy().astype("float64")
+    for pool_x, o_x in ((pool_1, o_1), (pool_2, o_2)):
+        assert_out_match(o_x.cpu(), ref_o, state_dtype, "o vs workspace entry")
+        assert_pool_match(pool_x.cpu(), ref_pool, written, "pool vs workspace entry")
     P = pool_np(inp.pool)
     o_ref = oracle.prefill(P, inp.init_slot.numpy(), inp.final_slot.numpy(), inp.q, inp.k, inp.v, inp.a, inp.b,
                            cu_seqlens=inp.cu_seqlens.numpy(), reset=inp.reset.numpy(), nthreads=8)
-    assert_out_match(o.cpu(), o_ref, state_dtype, "o")
-    lens = inp.meta["lens"]
-    written = [int(f) for f, i, t in zip(inp.final_slot, inp.init_slot, lens) if f >= 0 and i >= 0 and t > 0]
-    assert_pool_match(d.pool.cpu(), P, written, "pool")
+    assert_out_match(o_2.cpu(), o_ref, state_dtype, "o vs oracle")
+    assert_pool_match(pool_2.cpu(), P, written, "pool vs oracle")
