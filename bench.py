@@ -48,6 +48,66 @@ WORKLOAD = {
 }
 
 
+_CODE_TOKENS = None
+
+# The sources that define the decode kernel and its launch shape: a recorded
+# traffic figure stays valid while their code (comments and layout removed)
+# is unchanged.
+DECODE_SOURCES = ("kda_common.cuh", "kda_decode_tma.cuh", "kda_api.cu")
+
+
+def code_text(src: str) -> str:
+    """C/C++/CUDA source with its comments removed and its whitespace collapsed:
+    what the compiler sees, so that an edit to a comment changes nothing."""
+    global _CODE_TOKENS
+    import re
+    if _CODE_TOKENS is None:  # string and character literals are kept whole
+        _CODE_TOKENS = re.compile(r"""//[^\n]*|/\*.*?\*/|"(?:\\.|[^"\\\n])*"|'(?:\\.|[^'\\\n])*'""", re.S)
+
+    def drop(m):
+        tok = m.group(0)
+        if tok[0] in "\"'":
+            return tok
+        return "\n" * tok.count("\n") if tok.startswith("/*") else ""  # lines stay lines (directives)
+    kept = _CODE_TOKENS.sub(drop, src)
+    lines = (" ".join(line.split()) for line in kept.splitlines())
+    return "\n".join(line for line in lines if line)
+
+
+def source_hash(paths=None) -> str:
+    """Short hash of CUDA sources' code (comments and layout removed; default:
+    the decode kernel's files): profile summaries record it, so a number
+    measured on an older kernel is recognised as stale, while an edited
+    comment leaves it valid."""
+    import hashlib
+    if paths is None:
+        csrc = os.path.join(REPO, "kda_linear_attention_gated_gb300", "csrc")
+        paths = [os.path.join(csrc, f) for f in DECODE_SOURCES]
+    h = hashlib.sha256()
+    for path in paths:
+        with open(path, encoding="utf-8") as f:
+            h.update(code_text(f.read()).encode())
+    return h.hexdigest()[:16]
+
+
+def timed_replays(graph, stream, reps):
+    """Milliseconds of `reps` replays of `graph` on `stream`, by CUDA events.
+    One untimed replay is queued first, so that the GPU is busy when the start
+    event is recorded and the timed replays are already queued behind it: the
+    window holds the replays themselves, not the host's graph launch latency."""
+    import torch
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        graph.replay()
+        e0.record(stream)
+        for _ in range(reps):
+            graph.replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1)
+
+
 def algorithmic_bytes(n, hv, k, v, t, state_bytes, qkv_bytes, reads=1, writes=1):
     """State read + written plus q, k, v (qkv_bytes each) and fp32 o."""
     state = (reads + writes * t) * n * hv * k * v * state_bytes
@@ -308,18 +368,10 @@ def main():
                     g.replay()
         if dist is not None:
             dist.barrier()
-        torch.cuda.synchronize()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        with torch.cuda.stream(stream):
-            e0.record(stream)
-            for _ in range(steps // chunk):
-                g.replay()
-            e1.record(stream)
-        torch.cuda.synchronize()
+        ms = timed_replays(g, stream, steps // chunk)
         if dist is not None:
             dist.barrier()
         clocks = sampler.stop() if sampler else None
-        ms = e0.elapsed_time(e1)
         st = int(status.item())
         if st != 0:
             raise RuntimeError(f"device status {st}: {lib.kda_strerror(st)}")
@@ -479,6 +531,7 @@ def main():
             "frac_of_peak": round(h16["bytes"] / (h16["us_per_step"] * 1e-6) / 1e9 / peak, 4),
             "bytes_per_step": h16["bytes"], "pools": h16["pools"]}
         extra["verify"] = bench_verify(kda, workloads, torch, args, l2, peak)
+        extra["verify_fp32_pool"] = bench_verify(kda, workloads, torch, args, l2, peak, torch.float32)
         for sd_name, sd in (("fp32", torch.float32), ("fp16", torch.float16)):
             extra[f"sweep_69_layers_n128_{sd_name}"] = bench_sweep(kda, workloads, torch, sd, 128, peak)
         extra["ckpt_flush_fp32_n64"] = bench_ckpt(kda, workloads, torch, peak)
@@ -492,7 +545,7 @@ def main():
     if os.path.exists(tpath):
         try:
             t = json.load(open(tpath))
-            if t.get("source_hash") == kda.source_hash():
+            if t.get("source_hash") == source_hash():
                 traffic = t["dram_bytes_per_launch"]
         except Exception:
             traffic = None
@@ -564,15 +617,7 @@ def bench_sweep(kda, workloads, torch, state_dtype, n, peak, layers=69, replays=
                                     reset=d.reset, flags=flags)
         for _ in range(3):
             g.replay()
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(stream):
-        e0.record(stream)
-        for _ in range(replays):
-            g.replay()
-        e1.record(stream)
-    torch.cuda.synchronize()
-    us_fwd = e0.elapsed_time(e1) * 1e3 / replays
+    us_fwd = timed_replays(g, stream, replays) * 1e3 / replays
     if int(status.item()) != 0:
         raise RuntimeError(f"device status {int(status.item())}")
     resets = sum(int(d.reset.sum().item()) for d in dev)
@@ -646,18 +691,10 @@ def bench_ckpt(kda, workloads, torch, peak, replays=200, load=False):
                 call(pools[i], planes[i], slots, entries, status, flags=kda.KDA_LAUNCH_PDL)
         for _ in range(3):
             g_.replay()
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     reps = max(1, replays // R)
-    with torch.cuda.stream(stream):
-        e0.record(stream)
-        for _ in range(reps):
-            g_.replay()
-        e1.record(stream)
-    torch.cuda.synchronize()
+    us = timed_replays(g_, stream, reps) * 1e3 / (reps * R)
     if int(status.item()) != 0:
         raise RuntimeError(f"device status {int(status.item())}")
-    us = e0.elapsed_time(e1) * 1e3 / (reps * R)
     byt = 2 * 64 * HV * K * V * 4
     del pools, planes
     torch.cuda.empty_cache()
@@ -701,18 +738,10 @@ def bench_conv(kda, workloads, torch, peak, replays=480):
                 call(i)
         for _ in range(3):
             g_.replay()
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     reps = max(1, replays // R)
-    with torch.cuda.stream(stream):
-        e0.record(stream)
-        for _ in range(reps):
-            g_.replay()
-        e1.record(stream)
-    torch.cuda.synchronize()
+    us = timed_replays(g_, stream, reps) * 1e3 / (reps * R)
     if int(status.item()) != 0:
         raise RuntimeError(f"device status {int(status.item())}")
-    us = e0.elapsed_time(e1) * 1e3 / (reps * R)
     L = kw - 1 + spec
     byt = n * C * 2 * ((kw - 1) + L + 2 * t) + C * (kw + 1) * 4
     del sets, ys
@@ -723,13 +752,16 @@ def bench_conv(kda, workloads, torch, peak, replays=480):
             "launch": f"CUDA graph of {R} launches, replayed; flags KDA_LAUNCH_PDL"}
 
 
-def bench_verify(kda, workloads, torch, args, l2, peak):
-    """Speculative verify, fp16 pool, N=8 x T=8, HV=12, K=V=128, fp32 inputs."""
-    lib = kda.KdaLibrary(torch.float16)
+def bench_verify(kda, workloads, torch, args, l2, peak, state_dtype=None):
+    """Speculative verify, N=8 x T=8, HV=12, K=V=128, fp32 inputs, on an fp16
+    pool (the verify workload's) or an fp32 pool."""
+    state_dtype = state_dtype or torch.float16
+    es = 2 if state_dtype == torch.float16 else 4
+    lib = kda.KdaLibrary(state_dtype)
     n, t = 8, 8
     inp = workloads.make_verify(n=n, t=t, hv=HV, k=K, v=V, num_slots=SLOTS,
-                                state_dtype=torch.float16, qkv_dtype=torch.float32, seed=2)
-    per = n * (1 + t) * HV * K * V * 2
+                                state_dtype=state_dtype, qkv_dtype=torch.float32, seed=2)
+    per = n * (1 + t) * HV * K * V * es
     R = max(4, math.ceil(4 * l2 / per) + 1)
     base = inp.pool.to("cuda")
     pools = [base] + [base.clone() for _ in range(R - 1)]
@@ -750,19 +782,11 @@ def bench_verify(kda, workloads, torch, args, l2, peak):
                                     flags=kda.KDA_LAUNCH_PDL | kda.KDA_LAUNCH_PDL_EARLY_STATE)
         for _ in range(max(1, args.warmup // chunk)):
             g.replay()
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(stream):
-        e0.record(stream)
-        for _ in range(steps // chunk):
-            g.replay()
-        e1.record(stream)
-    torch.cuda.synchronize()
-    us = e0.elapsed_time(e1) * 1e3 / steps
-    byt = algorithmic_bytes(n, HV, K, V, t, 2, 4)
+    us = timed_replays(g, stream, steps // chunk) * 1e3 / steps
+    byt = algorithmic_bytes(n, HV, K, V, t, es, 4)
     if int(status.item()) != 0:
         raise RuntimeError(f"device status {int(status.item())}")
-    return {"workload": "spec verify, fp16 pool, N=8 x T=8, HV=12, K=V=128, fp32 q/k/v",
+    return {"workload": f"spec verify, {'fp16' if es == 2 else 'fp32'} pool, N=8 x T=8, HV=12, K=V=128, fp32 q/k/v",
             "us_per_step": round(us, 3), "gbs": round(byt / (us * 1e-6) / 1e9, 1),
             "frac_of_peak": round(byt / (us * 1e-6) / 1e9 / peak, 4), "bytes_per_step": byt,
             "pools": R, "launch": f"CUDA graph of {chunk} launches, replayed; flags KDA_LAUNCH_PDL|KDA_LAUNCH_PDL_EARLY_STATE"}

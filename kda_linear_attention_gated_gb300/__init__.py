@@ -98,38 +98,6 @@ class CkptPlaneDesc(ctypes.Structure):
                 ("num_entries", ctypes.c_int64), ("entry_stride", ctypes.c_int64)]
 
 
-_CODE_TOKENS = None
-
-
-def code_text(src: str) -> str:
-    """C/C++/CUDA source with its comments removed and its whitespace collapsed:
-    what the compiler sees, so that an edit to a comment changes nothing."""
-    global _CODE_TOKENS
-    import re
-    if _CODE_TOKENS is None:  # string and character literals are kept whole
-        _CODE_TOKENS = re.compile(r"""//[^\n]*|/\*.*?\*/|"(?:\\.|[^"\\\n])*"|'(?:\\.|[^'\\\n])*'""", re.S)
-    def drop(m):
-        tok = m.group(0)
-        if tok[0] in "\"'":
-            return tok
-        return "\n" * tok.count("\n") if tok.startswith("/*") else ""  # lines stay lines (directives)
-    kept = _CODE_TOKENS.sub(drop, src)
-    lines = (" ".join(line.split()) for line in kept.splitlines())
-    return "\n".join(line for line in lines if line)
-
-
-def source_hash() -> str:
-    """Short hash of the CUDA sources' code (comments and layout removed):
-    profile summaries record it, so a number measured on an older kernel is
-    recognised as stale, while an edited comment leaves it valid."""
-    import hashlib
-    h = hashlib.sha256()
-    for path in SOURCES:
-        with open(path, encoding="utf-8") as f:
-            h.update(code_text(f.read()).encode())
-    return h.hexdigest()[:16]
-
-
 def _dtype_code(dt) -> int:
     import torch
     table = {torch.float32: KDA_F32, torch.float16: KDA_F16, torch.bfloat16: KDA_BF16}

@@ -297,18 +297,17 @@ def test_library_missing_fails_loudly(monkeypatch, tmp_path):
         pkg.KdaLibrary(torch.float32)
 
 
-def test_source_hash_ignores_comments_and_layout_but_not_code(tmp_path, monkeypatch):
-    """The profile summaries' staleness check: comments and whitespace do not
-    change the hash, string literals and preprocessor line breaks are kept,
-    and any code change does."""
-    import kda_linear_attention_gated_gb300 as pkg
+def test_source_hash_ignores_comments_and_layout_but_not_code(tmp_path):
+    """The profile summaries' staleness check (bench.py): comments and
+    whitespace do not change the hash, string literals and preprocessor line
+    breaks are kept, and any code change does."""
+    import bench
     src = 'int a = 1; // note\n/* two\n lines */ const char* s = "x // y";\n#define X 1 /* t */\n'
-    assert pkg.code_text(src) == 'int a = 1;\nconst char* s = "x // y";\n#define X 1'
+    assert bench.code_text(src) == 'int a = 1;\nconst char* s = "x // y";\n#define X 1'
     f = tmp_path / "k.cu"
     f.write_text(src)
-    monkeypatch.setattr(pkg, "SOURCES", [str(f)])
-    h0 = pkg.source_hash()
+    h0 = bench.source_hash([str(f)])
     f.write_text("  // a new comment\n\n" + src.replace("// note", "// edited   note").replace("int a", "int   a"))
-    assert pkg.source_hash() == h0  # comments, blank lines and runs of spaces
+    assert bench.source_hash([str(f)]) == h0  # comments, blank lines and runs of spaces
     f.write_text(src.replace("int a = 1;", "int a = 2;"))
-    assert pkg.source_hash() != h0  # code
+    assert bench.source_hash([str(f)]) != h0  # code
