@@ -2,7 +2,8 @@
 against the fp64 oracle.
 
 y: fp32 within max-abs 1e-5; fp16 / bf16 within one step of the oracle's
-value rounded once from fp64 (the GPU rounds from its fp32 sum).  The window
+value rounded once from fp64 (the GPU rounds from its fp32 sum), or within
+CONV_Y_ABS of it where that sum's fp32 error spans more steps (near zero).  The window
 holds copies of inputs and old entries, so it must match bit for bit, and
 windows of slots no request uses must not change.
 """
@@ -14,7 +15,7 @@ import kda_linear_attention_gated_gb300 as kda
 from kda_linear_attention_gated_gb300 import workloads
 
 import oracle
-from _harness import lib_for
+from _harness import CONV_Y_ABS, lib_for
 
 pytestmark = [pytest.mark.gpu, pytest.mark.usefixtures("built_libs", "oracle_mod")]
 
@@ -70,7 +71,20 @@ def compare(inp, silu=True, flags=0, offset=False):
         assert np.isfinite(gys).all()
         assert np.abs(gys.astype(np.float64) - ry.astype(np.float64)).max() <= 1e-5
     else:
-        assert np.abs(gys.astype(np.int32) - ry.astype(np.int32)).max() <= 1, "y more than one step off"
+        assert_y16_match(gys, ry, inp.x.dtype)
+
+
+def y16_values(bits, dtype):
+    return torch.from_numpy(bits.astype(np.uint16).view(np.int16)).view(dtype).double().numpy()
+
+
+def assert_y16_match(gys, ry, dtype):
+    """fp16 / bf16 y: within one step of the oracle's value, or within
+    CONV_Y_ABS of it (the fp32 sum's error, which is many steps near zero)."""
+    steps = np.abs(gys.astype(np.int32) - ry.astype(np.int32))
+    diff = np.abs(y16_values(gys, dtype) - y16_values(ry, dtype))
+    bad = (steps > 1) & (diff > CONV_Y_ABS)
+    assert not bad.any(), f"y off by {steps[bad].max()} steps, {diff[bad].max():.3e} absolute"
 
 
 @pytest.mark.parametrize("dtype", DT)
