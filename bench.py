@@ -710,8 +710,9 @@ def bench_conv(kda, workloads, torch, peak, replays=480):
     shape: N=64 requests x T=5 tokens (4 drafts + 1), C = 4608 channels (q, k,
     v of 12 heads of 128), KW=4, a bf16 window of L = KW - 1 + 4 = 7 entries
     per slot.  48 window/input/output sets rotate (about 0.5 GB, past L2),
-    launched with programmatic dependent launch (the kernel reads nothing
-    before the previous kernel completes).
+    launched with programmatic dependent launch and early reads (each launch
+    reads its window, slot ids and weights while the previous one drains;
+    the sets are distinct, so no launch reads what its predecessor writes).
     Algorithmic bytes: per request and channel the KW - 1 history entries
     read, the L window entries written, T inputs read and T outputs written,
     plus the fp32 weights and bias once."""
@@ -729,7 +730,7 @@ def bench_conv(kda, workloads, torch, peak, replays=480):
         d = sets[i]
         lib.kda_conv_step(d.window, d.conv_slot, d.x, d.weight, ys[i], status, bias=d.bias,
                           cu_seqlens=d.cu_seqlens, max_t=t, accepted=d.accepted, reset=d.reset,
-                          flags=kda.KDA_LAUNCH_PDL)
+                          flags=kda.KDA_LAUNCH_PDL | kda.KDA_LAUNCH_PDL_EARLY_STATE)
     with torch.cuda.stream(stream):
         call(0)
         stream.synchronize()
@@ -749,7 +750,7 @@ def bench_conv(kda, workloads, torch, peak, replays=480):
     return {"workload": "conv window step, N=64 x T=5, C=4608, KW=4, bf16 window of 7 entries",
             "us_per_call": round(us, 3), "gbs": round(byt / (us * 1e-6) / 1e9, 1),
             "frac_of_peak": round(byt / (us * 1e-6) / 1e9 / peak, 4), "bytes_per_call": byt,
-            "launch": f"CUDA graph of {R} launches, replayed; flags KDA_LAUNCH_PDL"}
+            "launch": f"CUDA graph of {R} launches, replayed; flags KDA_LAUNCH_PDL|KDA_LAUNCH_PDL_EARLY_STATE"}
 
 
 def bench_verify(kda, workloads, torch, args, l2, peak, state_dtype=None):

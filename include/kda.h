@@ -84,7 +84,10 @@ typedef enum kda_status {
  *   has completed, so the state stream overlaps that kernel's tail.  Only valid
  *   when the previous kernel on the stream writes none of those: e.g. it is a
  *   projection producing q/k/v/a/b, or a step on another layer's pool.  Two
- *   back-to-back calls on the same pool must not use it.
+ *   back-to-back calls on the same pool must not use it.  For kda_conv_step
+ *   the early reads are the token offsets, slot ids, accepted indices, reset
+ *   flags, weights, bias and the window entries; x is read, and y and the
+ *   window are written, only after the previous kernel has completed.
  */
 #define KDA_LAUNCH_PDL 1u
 #define KDA_LAUNCH_PDL_EARLY_STATE 2u

@@ -618,6 +618,7 @@ int kda_conv_step(const kda_conv_window* win, const kda_conv_args* args, int32_t
     prm.bias = g.bias;
     prm.y = g.y;
     prm.silu = g.activation;
+    prm.flags = flags;
     prm.status = dev_status;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(cblocks * g.n), 1, 1);

@@ -93,8 +93,19 @@ __device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162flo
 // A 16-byte vector of state elements <-> fp32 registers.
 template <typename ST> struct StateVec;
 
+// Float pairs for the packed fp32 FMA of sm_100 and later (one FFMA2 does two
+// fmaf with the same rounding each): widen2 / narrow2 move a 16-byte vector
+// as VEC / 2 pairs of adjacent elements.
 template <> struct StateVec<float> {
     static constexpr int VEC = 4;
+    static __device__ __forceinline__ void widen2(const uint4& r, float2 (&x)[VEC / 2]) {
+        x[0] = make_float2(__uint_as_float(r.x), __uint_as_float(r.y));
+        x[1] = make_float2(__uint_as_float(r.z), __uint_as_float(r.w));
+    }
+    static __device__ __forceinline__ uint4 narrow2(const float2 (&x)[VEC / 2]) {
+        return make_uint4(__float_as_uint(x[0].x), __float_as_uint(x[0].y),
+                          __float_as_uint(x[1].x), __float_as_uint(x[1].y));
+    }
     static __device__ __forceinline__ void widen(const uint4& r, float (&x)[VEC]) {
         x[0] = __uint_as_float(r.x); x[1] = __uint_as_float(r.y);
         x[2] = __uint_as_float(r.z); x[3] = __uint_as_float(r.w);
@@ -124,6 +135,12 @@ template <> struct StateVec<__half> {
     }
     static __device__ __forceinline__ uint4 narrow(const float (&x)[VEC]) {
         return make_uint4(n2(x[0], x[1]), n2(x[2], x[3]), n2(x[4], x[5]), n2(x[6], x[7]));
+    }
+    static __device__ __forceinline__ void widen2(const uint4& r, float2 (&x)[VEC / 2]) {
+        x[0] = w2(r.x); x[1] = w2(r.y); x[2] = w2(r.z); x[3] = w2(r.w);
+    }
+    static __device__ __forceinline__ uint4 narrow2(const float2 (&x)[VEC / 2]) {
+        return make_uint4(n2(x[0].x, x[0].y), n2(x[1].x, x[1].y), n2(x[2].x, x[2].y), n2(x[3].x, x[3].y));
     }
 };
 

@@ -44,6 +44,7 @@ struct ConvParams {
     const float* bias;            // [C] or nullptr
     void* y;                      // [total][C]
     int silu;
+    uint32_t flags;               // KDA_LAUNCH_* bits
     int32_t* status;
 };
 
@@ -85,6 +86,12 @@ struct ConvIO {
 // VC channels per thread (1, or 4 when C and every address allow 4-channel
 // accesses), CT threads per CTA, kernel widths up to KWM; grid = requests x
 // ceil(C / (VC CT)).
+//
+// With KDA_LAUNCH_PDL_EARLY_STATE the reads that do not depend on the previous
+// kernel on the stream -- token offsets, slot id, accepted index, reset flag,
+// weights, bias and the window entries -- go out before the wait for it, so
+// they overlap its tail; the inputs x are read, and everything is written,
+// after the wait.
 template <typename ET, int VC, int CT, int KWM>
 __global__ void __launch_bounds__(CT) kda_conv_kernel(const ConvParams p) {
     using IO = ConvIO<ET, VC>;
@@ -93,7 +100,8 @@ __global__ void __launch_bounds__(CT) kda_conv_kernel(const ConvParams p) {
     const int r = (int)blockIdx.x / cblocks;
     const int c = (((int)blockIdx.x - r * cblocks) * CT + (int)threadIdx.x) * VC;  // first channel
     cudaTriggerProgrammaticLaunchCompletion();
-    cudaGridDependencySynchronize();  // nothing here is read before the previous kernel is done
+    const bool early = (p.flags & LAUNCH_PDL_EARLY_STATE) != 0;
+    if (!early) cudaGridDependencySynchronize();  // nothing here is read before the previous kernel is done
 
     int tb = r * p.t, T = p.t;
     if (p.cu != nullptr) {
@@ -102,18 +110,22 @@ __global__ void __launch_bounds__(CT) kda_conv_kernel(const ConvParams p) {
     }
     const int32_t slot = p.conv_slot[r];
     const int acc = p.accepted != nullptr ? p.accepted[r] - 1 : 0;
+    const bool rst = p.reset != nullptr && p.reset[r] != 0;
     const int m = acc + p.KW - 1;
     const int kept = max(0, p.L - T);
     constexpr int CB = 8;  // window entries or tokens per batch of loads
+    const bool range_ok = tb >= 0 && T > 0 && T <= p.t && tb + T <= p.total;
+    const ET* x = static_cast<const ET*>(p.x) + (int64_t)tb * p.C + min(c, p.C - VC);  // token t at x[t C]
     // The first CB inputs of this request go out before anything that waits
     // for the slot id or the accepted index (rows clamped into the request,
     // the channels into range; only read once the token range is checked).
-    const bool range_ok = tb >= 0 && T > 0 && T <= p.t && tb + T <= p.total;
-    const ET* x = static_cast<const ET*>(p.x) + (int64_t)tb * p.C + min(c, p.C - VC);  // token t at x[t C]
     R x0[CB];
-    if (range_ok)
+    auto load_x0 = [&]() {
+        if (range_ok)
 #pragma unroll
-        for (int u = 0; u < CB; ++u) x0[u] = IO::ld(x + (int64_t)min(u, T - 1) * p.C);
+            for (int u = 0; u < CB; ++u) x0[u] = IO::ld(x + (int64_t)min(u, T - 1) * p.C);
+    };
+    if (!early) load_x0();
     // uniform over the CTA: one request
     if (slot >= p.num_slots) {
         if (threadIdx.x == 0) atomicCAS(p.status, 0, STATUS_SLOT_RANGE);
@@ -127,6 +139,7 @@ __global__ void __launch_bounds__(CT) kda_conv_kernel(const ConvParams p) {
     ET* y = static_cast<ET*>(p.y) + (int64_t)tb * p.C + c;  // token t at y[t C]
     const R zero = R{};    // +0 in every channel, for all three element types
     if (slot < 0) {  // padding: zero outputs, window untouched
+        if (early) cudaGridDependencySynchronize();
         for (int t = 0; t < T; ++t) IO::st(y + (int64_t)t * p.C, zero);
         return;
     }
@@ -138,31 +151,44 @@ __global__ void __launch_bounds__(CT) kda_conv_kernel(const ConvParams p) {
     // window or the request's tokens, so that a batch is in flight at once;
     // the values out of range are dropped where they are used.
     ET* W = static_cast<ET*>(p.window) + (int64_t)slot * p.slot_stride + c;
-    const bool rst = p.reset != nullptr && p.reset[r] != 0;
     const int nh = p.KW - 1;  // history entries
+    // the history entries and the first batch of kept old entries, read
+    // together (the kept entries W[m - kept + e] move to W[e])
+    R hr[KWM], kv[CB];
+#pragma unroll
+    for (int i = 0; i < KWM; ++i) hr[i] = IO::ld(W + (int64_t)min(acc + i, p.L - 1) * p.C);
+#pragma unroll
+    for (int u = 0; u < CB; ++u) kv[u] = IO::ld(W + (int64_t)min(m - kept + u, p.L - 1) * p.C);
     // w[i] weighs history entry i (i < KW - 1); wlast weighs the current input
     float w[KWM][VC], z[KWM][VC], wlast[VC], bias[VC];
 #pragma unroll
-    for (int i = 0; i < KWM; ++i) {
-        const R hr = IO::ld(W + (int64_t)min(acc + i, p.L - 1) * p.C);
-        float hv[VC];
-        IO::widen(hr, hv);
+    for (int i = 0; i < KWM; ++i)
 #pragma unroll
-        for (int v = 0; v < VC; ++v) {
-            w[i][v] = i < nh ? __ldg(p.w + (int64_t)(c + v) * p.KW + i) : 0.f;
-            z[i][v] = i < nh && !rst ? hv[v] : 0.f;
-        }
-    }
+        for (int v = 0; v < VC; ++v) w[i][v] = i < nh ? __ldg(p.w + (int64_t)(c + v) * p.KW + i) : 0.f;
 #pragma unroll
     for (int v = 0; v < VC; ++v) {
         wlast[v] = __ldg(p.w + (int64_t)(c + v) * p.KW + p.KW - 1);
         bias[v] = p.bias != nullptr ? __ldg(p.bias + c + v) : 0.f;
     }
+    if (early) {
+        cudaGridDependencySynchronize();
+        load_x0();
+    }
+#pragma unroll
+    for (int i = 0; i < KWM; ++i) {
+        float hv[VC];
+        IO::widen(hr[i], hv);
+#pragma unroll
+        for (int v = 0; v < VC; ++v) z[i][v] = i < nh && !rst ? hv[v] : 0.f;
+    }
 
     // the kept old entries W[m - kept + e] -> W[e] (zero on reset), ascending:
     // a source never lies below its destination (m >= kept), so no batch reads
     // what an earlier one wrote
-    for (int e0 = 0; e0 < kept; e0 += CB) {
+#pragma unroll
+    for (int u = 0; u < CB; ++u)
+        if (u < kept) IO::st(W + (int64_t)u * p.C, rst ? zero : kv[u]);
+    for (int e0 = CB; e0 < kept; e0 += CB) {
         R v[CB];
 #pragma unroll
         for (int u = 0; u < CB; ++u) v[u] = IO::ld(W + (int64_t)min(m - kept + e0 + u, p.L - 1) * p.C);
@@ -170,7 +196,6 @@ __global__ void __launch_bounds__(CT) kda_conv_kernel(const ConvParams p) {
         for (int u = 0; u < CB; ++u)
             if (e0 + u < kept) IO::st(W + (int64_t)(e0 + u) * p.C, rst ? zero : v[u]);
     }
-
     for (int t0 = 0; t0 < T; t0 += CB) {
         R xr[CB];
         if (t0 == 0) {

@@ -234,23 +234,27 @@ kda_decode_kernel(const __grid_constant__ CUtensorMap tmap, const StepParams p) 
     constexpr uint32_t SSTRIDE = RG * SH::ROWBYTES, GSTRIDE = RG * 16;
 
     // (2) the two partial sums over this thread's rows, once the tile is in.
+    // Adjacent columns travel as float pairs through the packed FMA (two
+    // fmaf per instruction, each rounded as fmaf rounds).
+    constexpr int VP = VEC / 2;
     const bool ok_st = rst || mbar_wait(bar_st, 0);
-    float u[VEC], pp[VEC];
-    float xs[KEEP ? ROWS : 1][VEC];
+    float2 u[VP], pp[VP];
+    float2 xs[KEEP ? ROWS : 1][VP];
 #pragma unroll
-    for (int c = 0; c < VEC; ++c) { u[c] = 0.f; pp[c] = 0.f; }
+    for (int c = 0; c < VP; ++c) { u[c] = make_float2(0.f, 0.f); pp[c] = make_float2(0.f, 0.f); }
     if (!rst && ok_st) {
 #pragma unroll
         for (int rr = 0; rr < ROWS; ++rr) {
             if (FULLK || rr < nrows) {
-                float x[VEC];
-                SV::widen(lds128(srow0 + rr * SSTRIDE), x);
+                float2 x[VP];
+                SV::widen2(lds128(srow0 + rr * SSTRIDE), x);
                 const uint4 g = lds128(grow0 + rr * GSTRIDE);
                 const float w = __uint_as_float(g.x), z = __uint_as_float(g.y);
+                const float2 w2 = make_float2(w, w), z2 = make_float2(z, z);
 #pragma unroll
-                for (int c = 0; c < VEC; ++c) {
-                    u[c] = fmaf(x[c], w, u[c]);
-                    pp[c] = fmaf(x[c], z, pp[c]);
+                for (int c = 0; c < VP; ++c) {
+                    u[c] = __ffma2_rn(x[c], w2, u[c]);
+                    pp[c] = __ffma2_rn(x[c], z2, pp[c]);
                     if (KEEP) xs[KEEP ? rr : 0][c] = x[c];
                 }
             }
@@ -262,7 +266,10 @@ kda_decode_kernel(const __grid_constant__ CUtensorMap tmap, const StepParams p) 
     // the 2 VEC values {u[0..VEC), p[0..VEC)} of chunk cl, at index kbase.
     float vals[2 * VEC];
 #pragma unroll
-    for (int c = 0; c < VEC; ++c) { vals[c] = u[c]; vals[VEC + c] = pp[c]; }
+    for (int c = 0; c < VP; ++c) {
+        vals[2 * c] = u[c].x; vals[2 * c + 1] = u[c].y;
+        vals[VEC + 2 * c] = pp[c].x; vals[VEC + 2 * c + 1] = pp[c].y;
+    }
     int kbase = 0;
 #pragma unroll
     for (int m = 16, cnt = 2 * VEC; m >= CL; m >>= 1, cnt >>= 1) {
@@ -305,35 +312,37 @@ kda_decode_kernel(const __grid_constant__ CUtensorMap tmap, const StepParams p) 
     }
     __syncthreads();
     if (col0 >= p.v) return;
-    float d[VEC];
+    float2 d[VP];
 #pragma unroll
-    for (int c = 0; c < VEC; c += 4) {
-        const float4 d4 = *reinterpret_cast<const float4*>(dsm + cl * VEC + c);
-        d[c] = d4.x; d[c + 1] = d4.y; d[c + 2] = d4.z; d[c + 3] = d4.w;
+    for (int c = 0; c < VP; c += 2) {
+        const float4 d4 = *reinterpret_cast<const float4*>(dsm + cl * VEC + 2 * c);
+        d[c] = make_float2(d4.x, d4.y); d[c + 1] = make_float2(d4.z, d4.w);
     }
 
-    // (3) the delta update S' = alpha S + (beta khat) d, stored in place with
-    // coalesced 16-byte stores.
+    // (3) the delta update S' = alpha S + (beta khat) d (per element
+    // fmaf(alpha, S, (beta khat) d), in pairs), stored in place with coalesced
+    // 16-byte stores.
     ST* dst = static_cast<ST*>(p.pool) + state_at(p, slot, h) + (int64_t)rg * p.v + col0;
     const int64_t gstride = (int64_t)RG * p.v;
 #pragma unroll
     for (int rr = 0; rr < ROWS; ++rr) {
         if (FULLK || rr < nrows) {
-            float x[VEC];
+            float2 x[VP];
             if (rst) {
 #pragma unroll
-                for (int c = 0; c < VEC; ++c) x[c] = 0.f;
+                for (int c = 0; c < VP; ++c) x[c] = make_float2(0.f, 0.f);
             } else if (KEEP) {
 #pragma unroll
-                for (int c = 0; c < VEC; ++c) x[c] = xs[KEEP ? rr : 0][c];
+                for (int c = 0; c < VP; ++c) x[c] = xs[KEEP ? rr : 0][c];
             } else {
-                SV::widen(lds128(srow0 + rr * SSTRIDE), x);
+                SV::widen2(lds128(srow0 + rr * SSTRIDE), x);
             }
             const uint4 g = lds128(grow0 + rr * GSTRIDE);
             const float al = __uint_as_float(g.z), bk = __uint_as_float(g.w);
+            const float2 al2 = make_float2(al, al), bk2 = make_float2(bk, bk);
 #pragma unroll
-            for (int c = 0; c < VEC; ++c) x[c] = fmaf(al, x[c], bk * d[c]);
-            __stcs(reinterpret_cast<uint4*>(dst + rr * gstride), SV::narrow(x));
+            for (int c = 0; c < VP; ++c) x[c] = __ffma2_rn(al2, x[c], __fmul2_rn(bk2, d[c]));
+            __stcs(reinterpret_cast<uint4*>(dst + rr * gstride), SV::narrow2(x));
         }
     }
 }

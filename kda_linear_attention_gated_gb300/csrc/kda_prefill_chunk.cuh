@@ -29,7 +29,7 @@ constexpr int PCH = 16;                                   // tokens per chunk
 constexpr int PCH_FLOATS = 3 * KMAX * PCH + KMAX + 2 * KMAX * PCH;  // workspace floats per (chunk, head)
 constexpr int PVT = 32;                                   // value columns per scan CTA
 #ifndef KDA_PREP_MINB
-#define KDA_PREP_MINB 4   // resident prepare CTAs per SM the register budget must allow
+#define KDA_PREP_MINB 3   // resident prepare CTAs per SM the register budget must allow (168 registers, no spill)
 #endif
 #ifndef KDA_PSCAN_WARPS
 #define KDA_PSCAN_WARPS 8
@@ -262,7 +262,7 @@ struct PrefillScanSmem {
 };
 
 template <typename ST, int NC>
-__global__ void __launch_bounds__(PSCAN_WARPS * 32) kda_prefill_scan_kernel(const StepParams p,
+__global__ void __launch_bounds__(PSCAN_WARPS * 32, 2) kda_prefill_scan_kernel(const StepParams p,
                                                                            const float* __restrict__ ws) {
     static_assert(NC == 32 || NC == 16 || NC == 8, "columns per scan CTA");
     constexpr int NRQ = 32 / NC;                 // lanes sharing a column

@@ -44,6 +44,8 @@
 // KDA_ERR_TIMEOUT, wait once more (bounded) for its copies, and exit.
 #pragma once
 
+#include <type_traits>
+
 #include "kda_common.cuh"
 
 #ifndef KDA_VER_MINB
@@ -175,7 +177,10 @@ kda_verify_kernel(const __grid_constant__ CUtensorMap tmap, const StepParams p) 
     // an address clamped into the request's last token, row 0 or column 0,
     // so that all of them are in flight at once; the values past tc or the
     // row or column count are zeroed where they are used.
-    QT kraw[TC], qraw[TC], vraw[TC];
+    // fp16 inputs of a 256-thread (fp32 pool) tile are held as fp32: as 16-bit
+    // values they need more registers than its 85-register budget allows
+    using RT = typename std::conditional<sizeof(ST) == 4 && std::is_same<QT, __half>::value, float, QT>::type;
+    RT kraw[TC], qraw[TC], vraw[TC];
     float araw[TC];
     auto load_inputs = [&](int t0, int tc) {
         const QT* qp = static_cast<const QT*>(p.q);
@@ -186,10 +191,10 @@ kda_verify_kernel(const __grid_constant__ CUtensorMap tmap, const StepParams p) 
         for (int j = 0; j < TC; ++j) {
             const int64_t tok = (int64_t)tb + t0 + min(j, tc - 1);
             const int64_t rq = (tok * p.hqk + hq) * p.k + row, rt = tok * p.hv + h;
-            kraw[j] = kp[rq];
-            qraw[j] = qp[rq];
+            kraw[j] = (RT)kp[rq];
+            qraw[j] = (RT)qp[rq];
             araw[j] = __ldg(p.a + rt * p.k + row);
-            vraw[j] = vp[rt * p.v + (int64_t)cb * BV + col];
+            vraw[j] = (RT)vp[rt * p.v + (int64_t)cb * BV + col];
         }
     };
 
