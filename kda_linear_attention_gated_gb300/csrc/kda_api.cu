@@ -198,19 +198,20 @@ void set_pdl(cudaLaunchConfig_t& cfg, cudaLaunchAttribute* attr, uint32_t flags)
     }
 }
 
-// The prefill scan pass with NC value columns per CTA, launched with
-// programmatic dependent launch so that it starts while the first pass drains.
-template <int NC>
-int launch_scan(const kda::StepParams& prm, const float* ws, int64_t heads, int v, cudaStream_t st) {
-    constexpr size_t smem = kda::PrefillScanSmem<NC>::BYTES;
-    auto scan = kda::kda_prefill_scan_kernel<state_t, NC>;
+// The prefill scan pass with WPC warps (16 value columns each) per CTA,
+// launched with programmatic dependent launch so that it starts while the
+// first pass drains.
+template <int WPC>
+int launch_scan(const kda::StepParams& prm, const uint8_t* ws, int64_t heads, int v, cudaStream_t st) {
+    constexpr size_t smem = kda::PrefillScanSmem<WPC>::BYTES;
+    auto scan = kda::kda_prefill_scan_kernel<state_t, WPC>;
     int occ = 0, sms = 0;
-    const int rc = occupancy(reinterpret_cast<const void*>(scan), kda::PSCAN_WARPS * 32, smem, &occ, &sms);
+    const int rc = occupancy(reinterpret_cast<const void*>(scan), WPC * 32, smem, &occ, &sms);
     if (rc != KDA_OK) return rc;
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr;
-    cfg.gridDim = dim3((unsigned)(heads * ((v + NC - 1) / NC)), 1, 1);
-    cfg.blockDim = dim3(kda::PSCAN_WARPS * 32, 1, 1);
+    cfg.gridDim = dim3((unsigned)(heads * ((v + 16 * WPC - 1) / (16 * WPC))), 1, 1);
+    cfg.blockDim = dim3(WPC * 32, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
     set_pdl(cfg, &attr, KDA_LAUNCH_PDL);
@@ -485,7 +486,7 @@ int kda_prefill_workspace_bytes(const kda_pool* pool, int32_t n, int32_t total, 
     if (pool == nullptr || bytes == nullptr) return KDA_ERR_NULL;
     if (n < 0 || total < 0) return KDA_ERR_ARG;
     // one block per (chunk slot, head); chunk slots stay below total / 16 + n
-    *bytes = ((int64_t)total / kda::PCH + n) * pool->hv * (int64_t)kda::PCH_FLOATS * 4;
+    *bytes = ((int64_t)total / kda::PCH + n) * pool->hv * (int64_t)kda::PCH_BYTES;
     return KDA_OK;
 }
 
@@ -522,12 +523,12 @@ int kda_prefill_chunked(const kda_pool* pool, const kda_prefill_args* args, void
     prm.mode = kda::MODE_PADDING;
     prm.final_slot = g.final_slot;
     const int max_chunks = (g.max_t + kda::PCH - 1) / kda::PCH;
-    const int vtiles = (pool->v + 8 - 1) / 8;  // the narrowest scan tiling bounds the grid
+    const int vtiles = (pool->v + 15) / 16;  // the narrowest scan tiling bounds the grid
     if ((int64_t)g.n * max_chunks > 0x7fffffffLL || (int64_t)g.n * pool->hv * vtiles > 0x7fffffffLL ||
         pool->hv > 65535)
         return KDA_ERR_SHAPE;
     const cudaStream_t st = static_cast<cudaStream_t>(stream);
-    float* ws = static_cast<float*>(workspace);
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr;
     cfg.gridDim = dim3((unsigned)(g.n * max_chunks), (unsigned)pool->hv, 1);
@@ -543,19 +544,18 @@ int kda_prefill_chunked(const kda_pool* pool, const kda_prefill_args* args, void
         }
     }
     if (err != cudaSuccess) return KDA_ERR_LAUNCH;
-    // the widest scan tiling (32, 16 or 8 value columns per CTA) whose grid
-    // still covers the SMs: few long prompts get narrower tiles and more CTAs
+    // the most warps per scan CTA (they share each chunk's operand copy) whose
+    // grid still covers the SMs: few long prompts get one-warp CTAs
     int sms = 0, dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
         return KDA_ERR_LAUNCH;
     const int64_t heads = (int64_t)g.n * pool->hv;
-    const int nc = heads * ((pool->v + 31) / 32) >= sms ? 32 : heads * ((pool->v + 15) / 16) >= sms ? 16 : 8;
-    switch (nc) {
-        case 32: return launch_scan<32>(prm, ws, heads, pool->v, st);
-        case 16: return launch_scan<16>(prm, ws, heads, pool->v, st);
-        default: return launch_scan<8>(prm, ws, heads, pool->v, st);
-    }
+    auto ctas = [&](int wpc) { return heads * ((pool->v + 16 * wpc - 1) / (16 * wpc)); };
+    if (ctas(8) >= sms) return launch_scan<8>(prm, ws, heads, pool->v, st);
+    if (ctas(4) >= sms) return launch_scan<4>(prm, ws, heads, pool->v, st);
+    if (ctas(2) >= sms) return launch_scan<2>(prm, ws, heads, pool->v, st);
+    return launch_scan<1>(prm, ws, heads, pool->v, st);
 }
 
 int kda_prefill_chunked_noalloc(const kda_pool* pool, const kda_prefill_args* args, int32_t* dev_status,

@@ -285,6 +285,37 @@ __device__ __forceinline__ void mma_16816_f16(float (&d)[4], uint32_t a0, uint32
                  : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(addr) : "memory");
+}
+// d += A B for a 16 x 16 bf16 A (row-major fragment) and a 16 x 8 bf16 B
+// (column fragment), fp32 accumulators.
+__device__ __forceinline__ void mma_16816_bf16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                               uint32_t b0, uint32_t b1) {
+    asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+                 "{%8, %9}, {%0, %1, %2, %3};"
+                 : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+                 : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// x = p0 + p1 + p2 exactly, each part a bf16 value (8 significant bits): p0
+// is x rounded to bf16, p1 the remainder rounded, p2 what is left (at most 8
+// significant bits, so exact).  Both differences are exact in fp32.  Two
+// values at a time, packed as the bf16x2 words an mma fragment takes (the
+// first value in the low half).
+__device__ __forceinline__ void split3_bf16x2(float x, float y, uint32_t& p0, uint32_t& p1, uint32_t& p2) {
+    const __nv_bfloat162 h0 = __floats2bfloat162_rn(x, y);
+    const float2 b0 = __bfloat1622float2(h0);
+    const float rx = x - b0.x, ry = y - b0.y;
+    const __nv_bfloat162 h1 = __floats2bfloat162_rn(rx, ry);
+    const float2 b1 = __bfloat1622float2(h1);
+    const __nv_bfloat162 h2 = __floats2bfloat162_rn(rx - b1.x, ry - b1.y);
+    p0 = *reinterpret_cast<const uint32_t*>(&h0);
+    p1 = *reinterpret_cast<const uint32_t*>(&h1);
+    p2 = *reinterpret_cast<const uint32_t*>(&h2);
+}
+
 __device__ __forceinline__ uint4 lds128(uint32_t addr) {
     uint4 r;
     asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"

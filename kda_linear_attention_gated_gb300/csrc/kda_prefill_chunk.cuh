@@ -11,12 +11,13 @@
 //   S_end = diag(c_(CH-1)) S_0 + Ke^T D,  Ke_s = beta_s khat_s P_(CH-1)s.
 // Everything but S_0 depends on the chunk's inputs only, so
 //   pass 1 (prepare): one CTA per (chunk, head), all chunks at once, writes
-//     W'^T, Q'^T, Ke^T ([K][CH] each), c_(CH-1) [K], U and O_intra ([V/32][CH][32])
-//     to a workspace;
-//   pass 2 (scan): one CTA per (request, head, 32 value columns) walks the
-//     request's chunks in order: D = U - W' S, O = Q' S + O_intra,
-//     S <- c S + Ke^T D, with each chunk's operands bulk-copied into shared
-//     memory one chunk ahead; the final state is stored once.
+//     W', Q' and Ke ([CH][K] each, as three bf16 parts), c_(CH-1) [K], U and
+//     O_intra ([CH][V], fp32) to a workspace;
+//   pass 2 (scan): per (request, head), warps of 16 value columns walk the
+//     request's chunks in order on the tensor cores: D = U - W' S,
+//     O = Q' S + O_intra, S <- c S + Ke^T D, with each chunk's operands
+//     bulk-copied into shared memory one chunk ahead; the final state is
+//     stored once.
 // The products P are formed by multiplication (no division), so alpha = 0 is
 // exact.  Tokens past a request's end are padded as alpha = 1, beta = 0, k = 0.
 #pragma once
@@ -26,26 +27,24 @@
 namespace kda {
 
 constexpr int PCH = 16;                                   // tokens per chunk
-constexpr int PCH_FLOATS = 3 * KMAX * PCH + KMAX + 2 * KMAX * PCH;  // workspace floats per (chunk, head)
-constexpr int PVT = 32;                                   // value columns per scan CTA
 #ifndef KDA_PREP_MINB
 #define KDA_PREP_MINB 3   // resident prepare CTAs per SM the register budget must allow (168 registers, no spill)
 #endif
-#ifndef KDA_PSCAN_WARPS
-#define KDA_PSCAN_WARPS 8
-#endif
-constexpr int PSCAN_WARPS = KDA_PSCAN_WARPS;              // scan: warp w owns rows KMAX / PSCAN_WARPS * w ..
-constexpr int PSCAN_ROWS = KMAX / PSCAN_WARPS;
 
-// workspace offsets (floats) inside one (chunk, head) block
-constexpr int PW_WT = 0;                        // W'^T [KMAX][PCH]
-constexpr int PW_QT = PW_WT + KMAX * PCH;       // Q'^T [KMAX][PCH] (already / sqrt(K))
-constexpr int PW_KT = PW_QT + KMAX * PCH;       // Ke^T [KMAX][PCH]
-constexpr int PW_C = PW_KT + KMAX * PCH;        // c_(CH-1) [KMAX]
-constexpr int PW_U = PW_C + KMAX;               // U [KMAX / PVT][PCH][PVT]
-constexpr int PW_OI = PW_U + KMAX * PCH;        // O_intra [KMAX / PVT][PCH][PVT] (already / sqrt(K))
-static_assert(PW_OI + KMAX * PCH == PCH_FLOATS, "workspace layout");
-static_assert((2 * PCH) % PSCAN_WARPS == 0 && KMAX % PSCAN_WARPS == 0, "scan warps split the rows and vectors");
+// Workspace block of one (chunk, head), in bytes.  W', Q' (already / sqrt(K))
+// and Ke are [PCH tokens][KMAX rows] matrices, each as three bf16 part
+// matrices (x = x0 + x1 + x2), rows padded to PT_ROW elements (272 bytes: the
+// 8 rows an ldmatrix reads fall in distinct banks); U and O_intra (already
+// / sqrt(K)) are [PCH tokens][KMAX columns] fp32, rows padded to PU_ROW.
+constexpr int PT_ROW = KMAX + 8;
+constexpr int PU_ROW = KMAX + 4;
+constexpr uint32_t PART_BYTES = PCH * PT_ROW * 2;
+constexpr uint32_t PB_W = 0, PB_Q = 3 * PART_BYTES, PB_K = 6 * PART_BYTES;
+constexpr uint32_t PB_C = 9 * PART_BYTES;                  // c_(CH-1) [KMAX] fp32
+constexpr uint32_t PB_U = PB_C + KMAX * 4;
+constexpr uint32_t PB_OI = PB_U + PCH * PU_ROW * 4;
+constexpr uint32_t PCH_BYTES = PB_OI + PCH * PU_ROW * 4;
+static_assert(PART_BYTES % 16 == 0 && PB_C % 16 == 0 && PB_U % 16 == 0 && PCH_BYTES % 256 == 0, "workspace layout");
 
 // Chunk j of request r lives at slot floor(tb / PCH) + r + j, tb = the request's
 // first token: distinct for every (r, j) and below total / PCH + n.
@@ -79,8 +78,20 @@ __device__ __forceinline__ void pab_terms(float (&out)[32], const float (&bk)[PC
 
 // Pass 1.  grid = (n * max_chunks, hv), 128 threads: thread i owns key
 // channel i (and value column i for the V-side solve).
+// x in three bf16 parts, element [t][i] of part matrices base, base + 1, base + 2
+__device__ __forceinline__ void put_parts(__nv_bfloat16* base, int t, int i, float x) {
+    const __nv_bfloat16 h0 = __float2bfloat16_rn(x);
+    const float r = x - __bfloat162float(h0);
+    const __nv_bfloat16 h1 = __float2bfloat16_rn(r);
+    const __nv_bfloat16 h2 = __float2bfloat16_rn(r - __bfloat162float(h1));
+    __nv_bfloat16* e = base + t * PT_ROW + i;
+    e[0] = h0;
+    e[PCH * PT_ROW] = h1;
+    e[2 * PCH * PT_ROW] = h2;
+}
+
 template <typename QT>
-__global__ void __launch_bounds__(KMAX, KDA_PREP_MINB) kda_prefill_prep_kernel(const StepParams p, float* __restrict__ ws,
+__global__ void __launch_bounds__(KMAX, KDA_PREP_MINB) kda_prefill_prep_kernel(const StepParams p, uint8_t* __restrict__ ws,
                                                                 int max_chunks) {
     __shared__ float vs[PCH][KMAX];        // v of the chunk's tokens
     __shared__ float wsm[PCH][KMAX];       // W, then W'
@@ -105,7 +116,12 @@ __global__ void __launch_bounds__(KMAX, KDA_PREP_MINB) kda_prefill_prep_kernel(c
     const int cl = min(PCH, Tn - j * PCH);
     const int t0 = tb + j * PCH;
     const int hq = h / (p.hv / p.hqk);
-    float* w = ws + (prefill_chunk_slot(tb, r, j) * p.hv + h) * PCH_FLOATS;
+    uint8_t* w = ws + (prefill_chunk_slot(tb, r, j) * p.hv + h) * (int64_t)PCH_BYTES;
+    __nv_bfloat16* wpart = reinterpret_cast<__nv_bfloat16*>(w + PB_W);
+    __nv_bfloat16* qpart = reinterpret_cast<__nv_bfloat16*>(w + PB_Q);
+    __nv_bfloat16* kpart = reinterpret_cast<__nv_bfloat16*>(w + PB_K);
+    float* wu = reinterpret_cast<float*>(w + PB_U);
+    float* woi = reinterpret_cast<float*>(w + PB_OI);
 
     // (1) inputs: row tid of k, q, a for every token; value column tid of v.
     // Half a chunk at a time, every load unconditional from an address
@@ -179,18 +195,14 @@ __global__ void __launch_bounds__(KMAX, KDA_PREP_MINB) kda_prefill_prep_kernel(c
         wsm[t][tid] = c * kh[t];
         zsm[t][tid] = c * qh[t];
     }
-    // The workspace rows of W'^T, Q'^T and Ke^T are 64 bytes, one per thread:
-    // each is stored as four 16-byte vectors.
-    if (tid < p.k) {
-        w[PW_C + tid] = c;
+    // Column tid of Ke and c_(CH-1); rows past K hold zeros (k = 0 there).
+    {
+        reinterpret_cast<float*>(w + PB_C)[tid] = c;
         float e = 1.f;  // alpha_(s+1) ... alpha_(CH-1)
-        float4* kt4 = reinterpret_cast<float4*>(w + PW_KT + tid * PCH);
-        float kv[4];
 #pragma unroll
         for (int s = PCH - 1; s >= 0; --s) {
-            kv[s & 3] = bk[s] * e;
+            put_parts(kpart, s, tid, bk[s] * e);
             e *= al[s];
-            if ((s & 3) == 0) kt4[s >> 2] = make_float4(kv[0], kv[1], kv[2], kv[3]);
         }
     }
     {
@@ -224,10 +236,7 @@ __global__ void __launch_bounds__(KMAX, KDA_PREP_MINB) kda_prefill_prep_kernel(c
         wp[t] = xw;
         u[t] = xu;
     }
-    const int vt = tid / PVT, vc = tid - vt * PVT;
-    float4* wt4 = reinterpret_cast<float4*>(w + PW_WT + tid * PCH);
-    float4* qt4 = reinterpret_cast<float4*>(w + PW_QT + tid * PCH);
-    float qv[4];
+    // row tid of W' and Q', column tid of U and O_intra (zeros past K and V)
 #pragma unroll
     for (int t = 0; t < PCH; ++t) {
         float qp = zsm[t][tid], oi = 0.f;
@@ -237,55 +246,50 @@ __global__ void __launch_bounds__(KMAX, KDA_PREP_MINB) kda_prefill_prep_kernel(c
             qp = fmaf(-bts, wp[s], qp);
             oi = fmaf(bts, u[s], oi);
         }
-        qv[t & 3] = qp * p.inv_sqrt_k;
-        if ((t & 3) == 3 && tid < p.k) {
-            wt4[t >> 2] = make_float4(wp[t - 3], wp[t - 2], wp[t - 1], wp[t]);
-            qt4[t >> 2] = make_float4(qv[0], qv[1], qv[2], qv[3]);
-        }
-        if (tid < p.v) {
-            w[PW_U + (vt * PCH + t) * PVT + vc] = u[t];
-            w[PW_OI + (vt * PCH + t) * PVT + vc] = oi * p.inv_sqrt_k;
-        }
+        put_parts(wpart, t, tid, wp[t]);
+        put_parts(qpart, t, tid, qp * p.inv_sqrt_k);
+        wu[t * PU_ROW + tid] = u[t];
+        woi[t * PU_ROW + tid] = oi * p.inv_sqrt_k;
     }
 }
 
-// Pass 2.  grid = n * hv * ceil(v / NC) CTAs of PSCAN_WARPS warps, NC = 32, 16
-// or 8 value columns per CTA (narrower tiles when few requests leave SMs idle).
-// Warp w owns rows 16 w .. 16 w + 15 of the state tile; lane l = rq NC + cc
-// takes column cc and rows 16 w + rq RPT + i (i < RPT = 16 NC / 32).
-template <int NC>
+// Pass 2 on the tensor cores.  grid = n * hv * ceil(v / (16 WPC)) CTAs of WPC
+// warps; warp w owns the 16 state columns c0 .. c0 + 15 (c0 = 16 (WPC cb + w))
+// with all K rows, held transposed, S^T (16 x K), in m16n8 accumulator
+// fragments: tile nt covers rows 8 nt .. 8 nt + 7 and lane (g, qd) = (lane / 4,
+// lane % 4) holds
+//   {S[8nt+2qd][c0+g], S[8nt+2qd+1][c0+g], S[8nt+2qd][c0+g+8], S[8nt+2qd+1][c0+g+8]}.
+// Two adjacent tiles are exactly the A fragment of a 16 x 16 block of S^T, so
+// every product takes the state straight from its accumulators:
+//   [X^T | Y^T] = S^T [W'^T | Q'^T]    (16 x K by K x 32: X = W' S, Y = Q' S)
+//   D^T = U^T - X^T,  O^T = Y^T + O_intra^T
+//   S^T <- S^T diag(c) + D^T Ke        (16 x 16 by 16 x K onto the scaled accumulators)
+// No sum crosses a warp.  mma.sync takes bf16 operands and accumulates in
+// fp32; fp32 accuracy comes from splitting each factor in three bf16 parts
+// (x = x0 + x1 + x2 exactly) and summing the six products x_i y_j with
+// i + j <= 2: the three left out are below 2^-23 |x y| together.
+template <int WPC>
 struct PrefillScanSmem {
-    static constexpr uint32_t OPS = (3 * KMAX * PCH + KMAX + 2 * PCH * PVT) * 4;  // one chunk's operands
-    static constexpr uint32_t BUF = (OPS + 127u) & ~127u;
-    static constexpr uint32_t RED = PSCAN_WARPS * 2 * PCH * NC * 4;               // partial sums
-    static constexpr uint32_t BYTES = 2 * BUF + RED + 2 * PCH * NC * 4 + 16;
+    static constexpr uint32_t BYTES = 2 * PCH_BYTES + 16;  // two chunk buffers, two barriers
 };
 
-template <typename ST, int NC>
-__global__ void __launch_bounds__(PSCAN_WARPS * 32, 2) kda_prefill_scan_kernel(const StepParams p,
-                                                                           const float* __restrict__ ws) {
-    static_assert(NC == 32 || NC == 16 || NC == 8, "columns per scan CTA");
-    constexpr int NRQ = 32 / NC;                 // lanes sharing a column
-    constexpr int RPT = PSCAN_ROWS / NRQ;        // rows per thread
-    constexpr int KEEP = 2 * PCH / NRQ;          // partial sums a lane keeps after the reduce-scatter
-    static_assert(PSCAN_ROWS % NRQ == 0, "row split");
-    using SM = PrefillScanSmem<NC>;
+template <typename ST, int WPC>
+__global__ void __launch_bounds__(WPC * 32, 1) kda_prefill_scan_kernel(const StepParams p,
+                                                                      const uint8_t* __restrict__ ws) {
+    static_assert(WPC == 1 || WPC == 2 || WPC == 4 || WPC == 8, "warps per scan CTA");
+    constexpr int NT = WPC * 32, NTILE = KMAX / 8;
     extern __shared__ __align__(1024) uint8_t smem[];
-    float* red = reinterpret_cast<float*>(smem + 2 * SM::BUF);  // [warp][32 vectors][NC]
-    float* fin = red + PSCAN_WARPS * 2 * PCH * NC;               // [32 vectors][NC]
-    uint64_t* bars = reinterpret_cast<uint64_t*>(fin + 2 * PCH * NC);  // two chunk-operand barriers
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + 2 * PCH_BYTES);  // two chunk-operand barriers
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int rq = lane / NC, cc = lane - rq * NC;
-    const int vtiles = (p.v + NC - 1) / NC;
+    const int g = lane >> 2, qd = lane & 3;
+    const int ctiles = (p.v + 16 * WPC - 1) / (16 * WPC);
     const int tile = (int)blockIdx.x;
-    const int r = tile / (p.hv * vtiles);
-    const int rem = tile - r * p.hv * vtiles;
-    const int h = rem / vtiles, cb = rem - h * vtiles;
-    const int col = cb * NC + cc;
-    const int c32 = (cb * NC) / PVT;             // the 32-column workspace tile holding this CTA's columns
-    const int cw = col - c32 * PVT;              // column inside it
-    const bool col_ok = col < p.v;
+    const int r = tile / (p.hv * ctiles);
+    const int rem = tile - r * p.hv * ctiles;
+    const int h = rem / ctiles, cb = rem - h * ctiles;
+    const int c0 = (cb * WPC + warp) * 16;
+    const bool wact = c0 < p.v;  // V is a multiple of 16: a warp's columns are all in or all out
     cudaTriggerProgrammaticLaunchCompletion();
     cudaGridDependencySynchronize();
 
@@ -302,9 +306,9 @@ __global__ void __launch_bounds__(PSCAN_WARPS * 32, 2) kda_prefill_scan_kernel(c
         return;
     }
     if (slot < 0) {  // padding: outputs zero, nothing read or stored
-        for (int e = tid; e < Tn * NC; e += PSCAN_WARPS * 32) {
-            const int c2 = cb * NC + (e % NC);
-            if (c2 < p.v) p.o[((int64_t)(tb + e / NC) * p.hv + h) * p.v + c2] = 0.f;
+        for (int e = tid; e < Tn * 16 * WPC; e += NT) {
+            const int c2 = cb * 16 * WPC + (e % (16 * WPC));
+            if (c2 < p.v) p.o[((int64_t)(tb + e / (16 * WPC)) * p.hv + h) * p.v + c2] = 0.f;
         }
         return;
     }
@@ -312,31 +316,26 @@ __global__ void __launch_bounds__(PSCAN_WARPS * 32, 2) kda_prefill_scan_kernel(c
     // its final slot: the state after its last token
     if (Tn == 0 && fin_slot < 0) return;
     const int nch = (Tn + PCH - 1) / PCH;
-    const int row0 = warp * PSCAN_ROWS + rq * RPT;  // this thread's rows: row0 .. row0 + RPT - 1
+    const int nkt = p.k / 8;  // row tiles in use (K is a multiple of 16)
 
-    // the state tile, fp32 in registers
-    float S[RPT];
+    // the state, transposed, in accumulator fragments
+    float acc[NTILE][4];
     const bool rst = p.reset != nullptr && p.reset[r] != 0;
     const ST* src = static_cast<const ST*>(p.pool) + state_at(p, slot, h);
 #pragma unroll
-    for (int i = 0; i < RPT; ++i) {
-        const int row = row0 + i;
-        S[i] = (!rst && col_ok && row < p.k) ? to_f32(src[(int64_t)row * p.v + col]) : 0.f;
-    }
+    for (int nt = 0; nt < NTILE; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int row = 8 * nt + 2 * qd + (e & 1), col = c0 + g + 8 * (e >> 1);
+            acc[nt][e] = (!rst && wact && nt < nkt) ? to_f32(src[(int64_t)row * p.v + col]) : 0.f;
+        }
 
-    // chunk operands of chunk j -> buffer j % 2, one barrier per buffer
+    // chunk j's operand block -> buffer j % 2, one barrier per buffer
     auto issue = [&](int j) {
-        const float* w = ws + (prefill_chunk_slot(tb, r, j) * p.hv + h) * PCH_FLOATS;
-        uint8_t* buf = smem + (j & 1) * SM::BUF;
+        const uint8_t* blk = ws + (prefill_chunk_slot(tb, r, j) * p.hv + h) * (int64_t)PCH_BYTES;
         uint64_t* bar = bars + (j & 1);
-        const uint32_t kb = (uint32_t)p.k * PCH * 4, tb2 = PCH * PVT * 4;
-        mbar_arrive_expect_tx(bar, 3 * kb + (uint32_t)p.k * 4 + 2 * tb2);
-        bulk_load(buf, w + PW_WT, kb, bar);
-        bulk_load(buf + KMAX * PCH * 4, w + PW_QT, kb, bar);
-        bulk_load(buf + 2 * KMAX * PCH * 4, w + PW_KT, kb, bar);
-        bulk_load(buf + 3 * KMAX * PCH * 4, w + PW_C, (uint32_t)p.k * 4, bar);
-        bulk_load(buf + (3 * KMAX * PCH + KMAX) * 4, w + PW_U + c32 * PCH * PVT, tb2, bar);
-        bulk_load(buf + (3 * KMAX * PCH + KMAX + PCH * PVT) * 4, w + PW_OI + c32 * PCH * PVT, tb2, bar);
+        mbar_arrive_expect_tx(bar, PCH_BYTES);
+        bulk_load(smem + (j & 1) * PCH_BYTES, blk, PCH_BYTES, bar);
     };
     if (tid == 0) {
         mbar_init(bars, 1);
@@ -346,10 +345,17 @@ __global__ void __launch_bounds__(PSCAN_WARPS * 32, 2) kda_prefill_scan_kernel(c
     }
     __syncthreads();
 
+    // ldmatrix lane addresses (bytes inside a part matrix): lane l reads row
+    // (l & 7) of 8 x 8 block l / 8.  W', Q' as B[k = row of S][n = token]:
+    // blocks (tokens 0-7 | 8-15) x (k 0-7 | 8-15); Ke as B[k = token][n = row
+    // of S], transposed: blocks (tokens 0-7 | 8-15) x (two row tiles)
+    const uint32_t lwq = ((lane & 7) + 8 * (lane >> 4)) * (PT_ROW * 2) + 16 * ((lane >> 3) & 1);
+    const uint32_t lke = ((lane & 7) + 8 * ((lane >> 3) & 1)) * (PT_ROW * 2) + 16 * (lane >> 4);
+
     // chunk j is buffer j % 2's (j / 2)-th use: barrier parity (j / 2) % 2
     int jfail = -1, issued = nch > 0 ? 1 : 0;
     for (int j = 0; j < nch; ++j) {
-        if (j + 1 < nch) {  // its buffer's last reader was chunk j - 1
+        if (j + 1 < nch) {  // its buffer's last readers were done with chunk j - 1
             if (tid == 0) issue(j + 1);
             ++issued;
         }
@@ -358,94 +364,94 @@ __global__ void __launch_bounds__(PSCAN_WARPS * 32, 2) kda_prefill_scan_kernel(c
             jfail = j;
             break;
         }
-        const float* buf = reinterpret_cast<const float*>(smem + (j & 1) * SM::BUF);
-        const float* WT = buf;
-        const float* QT_ = buf + KMAX * PCH;
-        const float* KT = buf + 2 * KMAX * PCH;
-        const float* CC = buf + 3 * KMAX * PCH;
-        const float* U = CC + KMAX;
-        const float* OI = U + PCH * PVT;
-
-        // partial sums over this thread's rows: v_t = sum_i W'_ti S_i (t < 16),
-        // v_(16+t) = sum_i Q'_ti S_i
-        float vals[2 * PCH];
+        const uint8_t* buf = smem + (j & 1) * PCH_BYTES;
+        const uint32_t bw = smem_u32(buf + PB_W), bq = smem_u32(buf + PB_Q), bke = smem_u32(buf + PB_K);
+        const float* cc = reinterpret_cast<const float*>(buf + PB_C);
+        const float* U = reinterpret_cast<const float*>(buf + PB_U);
+        const float* OI = reinterpret_cast<const float*>(buf + PB_OI);
+        if (wact) {
+            // X^T (tiles 0, 1: tokens 0-7, 8-15) and Y^T (tiles 2, 3): the
+            // leading product and the five small ones in separate sums
+            float xh[4][4], xl[4][4];
 #pragma unroll
-        for (int t = 0; t < 2 * PCH; ++t) vals[t] = 0.f;
+            for (int t = 0; t < 4; ++t)
 #pragma unroll
-        for (int i = 0; i < RPT; ++i) {
-            const int row = row0 + i;
-            if (row < p.k) {
-                const float4* w4 = reinterpret_cast<const float4*>(WT + row * PCH);
-                const float4* q4 = reinterpret_cast<const float4*>(QT_ + row * PCH);
+                for (int e = 0; e < 4; ++e) { xh[t][e] = 0.f; xl[t][e] = 0.f; }
 #pragma unroll
-                for (int g = 0; g < PCH / 4; ++g) {
-                    const float4 a = w4[g], b = q4[g];
-                    vals[4 * g] = fmaf(a.x, S[i], vals[4 * g]);
-                    vals[4 * g + 1] = fmaf(a.y, S[i], vals[4 * g + 1]);
-                    vals[4 * g + 2] = fmaf(a.z, S[i], vals[4 * g + 2]);
-                    vals[4 * g + 3] = fmaf(a.w, S[i], vals[4 * g + 3]);
-                    vals[PCH + 4 * g] = fmaf(b.x, S[i], vals[PCH + 4 * g]);
-                    vals[PCH + 4 * g + 1] = fmaf(b.y, S[i], vals[PCH + 4 * g + 1]);
-                    vals[PCH + 4 * g + 2] = fmaf(b.z, S[i], vals[PCH + 4 * g + 2]);
-                    vals[PCH + 4 * g + 3] = fmaf(b.w, S[i], vals[PCH + 4 * g + 3]);
+            for (int kk = 0; kk < NTILE / 2; ++kk) {
+                if (2 * kk >= nkt) break;  // (unrolled: the state's tiles keep register indices)
+                uint32_t a[3][4];
+                split3_bf16x2(acc[2 * kk][0], acc[2 * kk][1], a[0][0], a[1][0], a[2][0]);
+                split3_bf16x2(acc[2 * kk][2], acc[2 * kk][3], a[0][1], a[1][1], a[2][1]);
+                split3_bf16x2(acc[2 * kk + 1][0], acc[2 * kk + 1][1], a[0][2], a[1][2], a[2][2]);
+                split3_bf16x2(acc[2 * kk + 1][2], acc[2 * kk + 1][3], a[0][3], a[1][3], a[2][3]);
+#pragma unroll
+                for (int m = 0; m < 2; ++m) {
+                    uint32_t b[3][4];
+#pragma unroll
+                    for (int part = 0; part < 3; ++part)
+                        ldsm_x4((m ? bq : bw) + part * PART_BYTES + lwq + kk * 32, b[part][0], b[part][1], b[part][2],
+                                b[part][3]);
+#pragma unroll
+                    for (int nh = 0; nh < 2; ++nh) {
+                        float(&dh)[4] = xh[2 * m + nh];
+                        float(&dl)[4] = xl[2 * m + nh];
+                        const int i0 = 2 * nh, i1 = 2 * nh + 1;
+                        mma_16816_bf16(dh, a[0][0], a[0][1], a[0][2], a[0][3], b[0][i0], b[0][i1]);
+                        mma_16816_bf16(dl, a[0][0], a[0][1], a[0][2], a[0][3], b[1][i0], b[1][i1]);
+                        mma_16816_bf16(dl, a[1][0], a[1][1], a[1][2], a[1][3], b[0][i0], b[0][i1]);
+                        mma_16816_bf16(dl, a[0][0], a[0][1], a[0][2], a[0][3], b[2][i0], b[2][i1]);
+                        mma_16816_bf16(dl, a[1][0], a[1][1], a[1][2], a[1][3], b[1][i0], b[1][i1]);
+                        mma_16816_bf16(dl, a[2][0], a[2][1], a[2][2], a[2][3], b[0][i0], b[0][i1]);
+                    }
+                }
+            }
+            // D^T = U^T - X^T; O^T = Y^T + O_intra^T for the chunk's tokens
+            const int cl = min(PCH, Tn - j * PCH);
+            float dd[2][4];
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int tok = 8 * nt + 2 * qd + (e & 1), col = c0 + g + 8 * (e >> 1);
+                    dd[nt][e] = U[tok * PU_ROW + col] - (xh[nt][e] + xl[nt][e]);
+                    if (tok < cl)
+                        p.o[((int64_t)(tb + j * PCH + tok) * p.hv + h) * p.v + col] =
+                            (xh[2 + nt][e] + xl[2 + nt][e]) + OI[tok * PU_ROW + col];
+                }
+            // S^T <- S^T diag(c) + D^T Ke
+            uint32_t a[3][4];
+            split3_bf16x2(dd[0][0], dd[0][1], a[0][0], a[1][0], a[2][0]);
+            split3_bf16x2(dd[0][2], dd[0][3], a[0][1], a[1][1], a[2][1]);
+            split3_bf16x2(dd[1][0], dd[1][1], a[0][2], a[1][2], a[2][2]);
+            split3_bf16x2(dd[1][2], dd[1][3], a[0][3], a[1][3], a[2][3]);
+#pragma unroll
+            for (int np = 0; np < NTILE / 2; ++np) {
+                if (2 * np < nkt) {
+                    uint32_t b[3][4];
+#pragma unroll
+                    for (int part = 0; part < 3; ++part)
+                        ldsm_x4_trans(bke + part * PART_BYTES + lke + np * 32, b[part][0], b[part][1], b[part][2],
+                                      b[part][3]);
+#pragma unroll
+                    for (int nh = 0; nh < 2; ++nh) {
+                        float(&s4)[4] = acc[2 * np + nh];
+                        const int row = 8 * (2 * np + nh) + 2 * qd;
+                        const float c_lo = cc[row], c_hi = cc[row + 1];
+                        s4[0] *= c_lo; s4[1] *= c_hi; s4[2] *= c_lo; s4[3] *= c_hi;
+                        const int i0 = 2 * nh, i1 = 2 * nh + 1;
+                        mma_16816_bf16(s4, a[2][0], a[2][1], a[2][2], a[2][3], b[0][i0], b[0][i1]);
+                        mma_16816_bf16(s4, a[1][0], a[1][1], a[1][2], a[1][3], b[1][i0], b[1][i1]);
+                        mma_16816_bf16(s4, a[0][0], a[0][1], a[0][2], a[0][3], b[2][i0], b[2][i1]);
+                        mma_16816_bf16(s4, a[1][0], a[1][1], a[1][2], a[1][3], b[0][i0], b[0][i1]);
+                        mma_16816_bf16(s4, a[0][0], a[0][1], a[0][2], a[0][3], b[1][i0], b[1][i1]);
+                        mma_16816_bf16(s4, a[0][0], a[0][1], a[0][2], a[0][3], b[0][i0], b[0][i1]);
+                    }
                 }
             }
         }
-        // over the NRQ lanes sharing column cc: a reduce-scatter, each keeps KEEP sums
-        int kbase = 0;
-#pragma unroll
-        for (int m = 16, cnt = 2 * PCH; m >= NC; m >>= 1, cnt >>= 1) {
-            const bool upper = (lane & m) != 0;
-#pragma unroll
-            for (int e = 0; e < cnt / 2; ++e) {
-                const float send = upper ? vals[e] : vals[e + cnt / 2];
-                const float keep = upper ? vals[e + cnt / 2] : vals[e];
-                vals[e] = keep + __shfl_xor_sync(0xffffffffu, send, m);
-            }
-            kbase += upper ? cnt / 2 : 0;
-        }
-#pragma unroll
-        for (int e = 0; e < KEEP; ++e) red[(warp * 2 * PCH + kbase + e) * NC + cc] = vals[e];
-        __syncthreads();
-        // the sums over the warps: 32 vectors x NC columns
-        for (int e = tid; e < 2 * PCH * NC; e += PSCAN_WARPS * 32) {
-            float sum = 0.f;
-#pragma unroll
-            for (int w2 = 0; w2 < PSCAN_WARPS; ++w2) sum += red[w2 * 2 * PCH * NC + e];
-            fin[e] = sum;
-        }
-        __syncthreads();
-        // d_t = U_t - (W' S)_t for this column; outputs O_t = (Q' S)_t + O_intra_t
-        float d[PCH];
-#pragma unroll
-        for (int t = 0; t < PCH; ++t) d[t] = U[t * PVT + cw] - fin[t * NC + cc];
-        const int cl = min(PCH, Tn - j * PCH);
-        for (int e = tid; e < cl * NC; e += PSCAN_WARPS * 32) {
-            const int t = e / NC, c2 = e - t * NC, gcol = cb * NC + c2;
-            if (gcol < p.v)
-                p.o[((int64_t)(tb + j * PCH + t) * p.hv + h) * p.v + gcol] =
-                    fin[(PCH + t) * NC + c2] + OI[t * PVT + gcol - c32 * PVT];
-        }
-        // S <- c S + Ke^T D
-#pragma unroll
-        for (int i = 0; i < RPT; ++i) {
-            const int row = row0 + i;
-            if (row < p.k) {
-                const float4* k4 = reinterpret_cast<const float4*>(KT + row * PCH);
-                float x = CC[row] * S[i];
-#pragma unroll
-                for (int g = 0; g < PCH / 4; ++g) {
-                    const float4 kk = k4[g];
-                    x = fmaf(kk.x, d[4 * g], x);
-                    x = fmaf(kk.y, d[4 * g + 1], x);
-                    x = fmaf(kk.z, d[4 * g + 2], x);
-                    x = fmaf(kk.w, d[4 * g + 3], x);
-                }
-                S[i] = x;
-            }
-        }
-        // every thread is done with this buffer and with red/fin before the
-        // next issue (generic reads, then async writes: fence first)
+        // every thread is done with this buffer before the next issue
+        // (generic reads, then async writes: fence first)
         fence_proxy_async_smem();
         __syncthreads();
     }
@@ -457,16 +463,18 @@ __global__ void __launch_bounds__(PSCAN_WARPS * 32, 2) kda_prefill_scan_kernel(c
         }
         return;
     }
-    if (fin_slot >= 0 && col_ok) {
+    if (fin_slot >= 0 && wact) {
         ST* dst = static_cast<ST*>(p.pool) + state_at(p, fin_slot, h);
 #pragma unroll
-        for (int i = 0; i < RPT; ++i) {
-            const int row = row0 + i;
-            if (row < p.k) {
-                if constexpr (sizeof(ST) == 4) dst[(int64_t)row * p.v + col] = S[i];
-                else dst[(int64_t)row * p.v + col] = __float2half_rn(S[i]);
+        for (int nt = 0; nt < NTILE; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int row = 8 * nt + 2 * qd + (e & 1), col = c0 + g + 8 * (e >> 1);
+                if (nt < nkt) {
+                    if constexpr (sizeof(ST) == 4) dst[(int64_t)row * p.v + col] = acc[nt][e];
+                    else dst[(int64_t)row * p.v + col] = __float2half_rn(acc[nt][e]);
+                }
             }
-        }
     }
 }
 

@@ -93,7 +93,9 @@ def test_chunked_prefill_workspace_too_small_is_refused():
     o = torch.empty(20, 2, 16, device="cuda")
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
     need = lib.kda_prefill_workspace_bytes(d.pool, 1, 20)
-    assert need == (20 // 16 + 1) * 2 * 10368 * 4
+    # one 56,576-byte block per (16-token chunk slot, head): W', Q' and Ke as three
+    # bf16 parts of [16][136], c [128] fp32, U and O_intra [16][132] fp32
+    assert need == (20 // 16 + 1) * 2 * 56576
     with pytest.raises(kda.KdaError) as e:
         lib.kda_prefill_chunked(d.pool, d.init_slot, d.final_slot, d.q, d.k, d.v, d.a, d.b, o, status,
                                 workspace=torch.empty(need - 256, dtype=torch.uint8, device="cuda"),
