@@ -380,18 +380,18 @@ def main():
                     pool_bytes=R * pools[0].numel() * es)
 
     def bench_e2e(steps):
-        """Through the C ABI with host buffers, every step: one host-to-device
-        copy of the step's inputs (slot ids, q, k, v, a, b packed in one pinned
-        buffer), the decode kernel, one device-to-host copy of o.  NB sets of
-        device buffers rotate over three streams, so the copies of one step
-        overlap the kernels of its neighbours; events keep each buffer's
-        writer behind its last reader.  The kernels take the device value's
-        launch flags (PDL with early state): a step's slot ids arrive by the
-        copy its kernel waits for, and its pool was last written R steps
-        earlier.  A group of steps is captured in one
-        CUDA graph (copies, calls and events included) and replayed, so the
-        host's per-call work does not pace the GPU; if capture is refused the
-        steps are issued one by one."""
+        """Through the C ABI with host buffers.  Every step: one kda_stage_host
+        launch copies the step's packed inputs (slot ids, q, k, v, a, b) from
+        pinned host memory into one of NB device buffer sets (a kernel, one
+        thread per 16 bytes, loads over the host link: no copy-engine
+        transfer and its fixed cost), then kda_decode_step writes o straight
+        into pinned host memory.  Both on one stream with programmatic
+        dependent launch: the staging loads start while the previous decode
+        drains and store after it; the decode starts while the staging runs
+        and reads its inputs after it (no early state reads: its slot ids come
+        from the kernel just before it).  A group of steps is captured in one
+        CUDA graph and replayed, so the host's per-call work does not pace the
+        GPU."""
         inp = workloads.make_decode(n=N, hv=HV, k=K, v=V, num_slots=SLOTS, state_dtype=torch.float32,
                                     qkv_dtype=torch.bfloat16, seed=0)
         R = max(4, math.ceil(4 * l2 / (N * HV * K * V * 4)) + 1)
@@ -410,75 +410,45 @@ def main():
         dev_in = [torch.empty(h2d, dtype=torch.uint8, device="cuda") for _ in range(NB)]
         views = [[buf[off:off + sz].view(t.dtype).view(t.shape) for t, off, sz in zip(srcs, offs, sizes)]
                  for buf in dev_in]
-        o = [torch.empty(N, HV, V, device="cuda") for _ in range(NB)]
         o_host = [torch.empty(N, HV, V).pin_memory() for _ in range(NB)]
-        d2h = o[0].numel() * 4
+        d2h = o_host[0].numel() * 4
         status = torch.zeros(1, dtype=torch.int32, device="cuda")
-        s_in, s_k, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
-        ev_in = [torch.cuda.Event() for _ in range(NB)]
-        ev_k = [torch.cuda.Event() for _ in range(NB)]
-        ev_out = [torch.cuda.Event() for _ in range(NB)]
-        flags = kda.KDA_LAUNCH_PDL | kda.KDA_LAUNCH_PDL_EARLY_STATE
+        stream = torch.cuda.Stream()
+        pdl = kda.KDA_LAUNCH_PDL
+        st_ptr = status.data_ptr()
 
-        def one(i, first=False):
+        def one(i):
             b_ = i % NB
-            if not first:
-                s_in.wait_event(ev_k[b_])    # the kernel NB steps back has read these inputs
-            with torch.cuda.stream(s_in):
-                dev_in[b_].copy_(host, non_blocking=True)
-            ev_in[b_].record(s_in)
-            s_k.wait_event(ev_in[b_])
-            if not first:
-                s_k.wait_event(ev_out[b_])   # o[b] was read back NB steps ago
+            rc = lib32.kda_stage_host_raw([(dev_in[b_].data_ptr(), host.data_ptr(), h2d)], stream.cuda_stream, pdl)
+            if rc != 0:
+                raise RuntimeError(f"kda_stage_host: {lib32.kda_strerror(rc)}")
             sl, q_, k_, v_, a_, bb = views[b_]
-            lib32.kda_decode_step(pools[i % R], sl, q_, k_, v_, a_, bb, o[b_], status, stream=s_k, flags=flags)
-            ev_k[b_].record(s_k)
-            s_out.wait_event(ev_k[b_])
-            with torch.cuda.stream(s_out):
-                o_host[b_].copy_(o[b_], non_blocking=True)
-            ev_out[b_].record(s_out)
+            rc = lib32.kda_decode_step_raw(kda.pool_desc(pools[i % R]), sl.data_ptr(), None, N, q_.data_ptr(),
+                                           k_.data_ptr(), v_.data_ptr(), kda.KDA_BF16, a_.data_ptr(), bb.data_ptr(),
+                                           o_host[b_].data_ptr(), st_ptr, stream.cuda_stream, pdl)
+            if rc != 0:
+                raise RuntimeError(f"kda_decode_step: {lib32.kda_strerror(rc)}")
 
-        for i in range(max(3, args.warmup // 10)):
-            one(i)
+        with torch.cuda.stream(stream):
+            for i in range(max(3, args.warmup // 10)):
+                one(i)
         torch.cuda.synchronize()
         group = 50
-        graph = None
-        try:
-            g_ = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g_, stream=s_in):
-                s_k.wait_stream(s_in)
-                s_out.wait_stream(s_in)
-                for i in range(group):
-                    one(i, first=i < NB)
-                s_in.wait_stream(s_k)
-                s_in.wait_stream(s_out)
+        g_ = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g_, stream=stream):
+            for i in range(group):
+                one(i)
+        with torch.cuda.stream(stream):
             for _ in range(3):
                 g_.replay()
-            torch.cuda.synchronize()
-            graph = g_
-        except Exception:
-            torch.cuda.synchronize()
         if dist is not None:
             dist.barrier()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         n_e2e = min(steps, 2000) // group * group or group
-        e0.record(s_in)
-        if graph is not None:
-            with torch.cuda.stream(s_in):
-                for _ in range(n_e2e // group):
-                    graph.replay()
-        else:
-            for i in range(n_e2e):
-                one(i)
-            for ev in ev_out:
-                s_in.wait_event(ev)
-        e1.record(s_in)
-        torch.cuda.synchronize()
+        ms = timed_replays(g_, stream, n_e2e // group)
         if int(status.item()) != 0:
             raise RuntimeError(f"device status {int(status.item())}")
-        ms = e0.elapsed_time(e1)
         return dict(us_per_step=ms * 1e3 / n_e2e, steps=n_e2e, h2d=h2d, d2h=d2h,
-                    mode=f"CUDA graph of {group} steps" if graph is not None else "eager")
+                    mode=f"CUDA graph of {group} steps")
 
     def max_over_ranks(x):
         return reduce_max(x, dist, "cuda")
@@ -580,9 +550,10 @@ def main():
                 "value": round(e2e_gbs, 2), "unit": "GB/s", "us_per_step": round(e2e_us, 3),
                 "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"],
                 "steps": e2e["steps"],
-                "how": "every step one pinned H2D copy of its packed inputs, the C-ABI decode call (flags "
-                       "KDA_LAUNCH_PDL|KDA_LAUNCH_PDL_EARLY_STATE), one D2H copy of o; four buffer sets over "
-                       "three streams overlap neighbouring steps; " + e2e["mode"]},
+                "how": "every step one kda_stage_host launch copies its packed inputs from pinned host "
+                       "memory into one of four device buffer sets (a kernel over the host link), then the "
+                       "C-ABI decode call writes o into pinned host memory; one stream, flags KDA_LAUNCH_PDL "
+                       "on both; " + e2e["mode"]},
             "gpu_launches": args.steps,
             "clocks": head["clocks"],
             "extra": extra,
@@ -660,11 +631,24 @@ def bench_prefill(kda, workloads, torch, n, t, chunked=False, reps=5):
     if int(status.item()) != 0:
         raise RuntimeError(f"device status {int(status.item())}")
     ms = e0.elapsed_time(e1) / reps
-    flop = 6.0 * 2 * K * V * HV * n * t  # ~6 passes of 2 K V flop per token and head
-    return {"workload": f"prefill{' (two passes)' if chunked else ''}, {n} prompts x {t} tokens, HV=12, K=V=128, "
+    # the recurrence's own arithmetic: decay (K V), u = S^T k (2 K V), the
+    # rank-1 update (2 K V) and o = S^T q (2 K V) per token and head
+    flop = 7.0 * K * V * HV * n * t
+    line = {"workload": f"prefill{' (two passes)' if chunked else ''}, {n} prompts x {t} tokens, HV=12, K=V=128, "
                         "bf16 q/k/v, fp16 pool",
             "ms_per_call": round(ms, 4), "tokens_per_s": round(n * t / (ms * 1e-3), 1),
-            "approx_tflops": round(flop / (ms * 1e-3) / 1e12, 3)}
+            "recurrence_tflops": round(flop / (ms * 1e-3) / 1e12, 3)}
+    if chunked:
+        # the scan's tensor-core products as executed, per 16-token chunk and
+        # head: [X | Y] (V x 32 x K) and the state update (K x V x 16), six
+        # bf16 part products each, 2 flop per multiply-add
+        chunks = n * ((t + 15) // 16)
+        tc = chunks * HV * 6 * 2.0 * (V * 32 * K + K * V * 16)
+        sus = peaks()[2].get("bf16_tflops_sustained")
+        line["tensor_tflops"] = round(tc / (ms * 1e-3) / 1e12, 3)
+        if sus:
+            line["tensor_frac_of_bf16_sustained"] = round(tc / (ms * 1e-3) / 1e12 / float(sus), 5)
+    return line
 
 
 def bench_ckpt(kda, workloads, torch, peak, replays=200, load=False):

@@ -391,6 +391,31 @@ int kda_prefill_chunked_noalloc(const kda_pool* pool, const kda_prefill_args* ar
                                 uint32_t flags, void* stream);
 
 /*
+ * Staging of a step's inputs from host memory by a kernel.  copies[i] moves
+ * `bytes` bytes from `src`, pinned host memory mapped into the device's address
+ * space (cudaHostAlloc / cudaMallocHost memory; pageable memory is refused),
+ * to `dst`, device memory; both 16-byte aligned, bytes a multiple of 16.
+ * One thread per 16 bytes loads over the host link and stores to the device
+ * buffer, all copies in one launch: small per-step transfers then run on the
+ * SMs beside other kernels instead of paying the copy engine's fixed cost
+ * each.  With KDA_LAUNCH_PDL the loads start before the previous kernel on the
+ * stream completes and the stores wait for it.  copies: host array of
+ * n <= KDA_STAGE_MAX_COPIES entries.  Host checks: KDA_ERR_ARG (n out of
+ * range, bytes negative or not a multiple of 16, a source that is not
+ * device-mapped host memory or a destination that is not device memory,
+ * flags other than KDA_LAUNCH_PDL), KDA_ERR_NULL, KDA_ERR_ALIGN.  The pages
+ * have no counterpart: this serves the end-to-end measurement of a step fed
+ * from host buffers.
+ */
+#define KDA_STAGE_MAX_COPIES 8
+typedef struct kda_host_copy {
+    void* dst;          /* device */
+    const void* src;    /* pinned, device-mapped host memory */
+    int64_t bytes;
+} kda_host_copy;
+int kda_stage_host(const kda_host_copy* copies, int32_t n, uint32_t flags, void* stream);
+
+/*
  * Checkpoint planes (ReplaySSM in pull request 2945, Changes: the checkpoint
  * load and the flush go through state_at; pull request 2130, What: the plane
  * shapes and the checkpoint layout id derive from the state dtype, so a build

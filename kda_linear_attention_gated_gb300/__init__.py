@@ -38,7 +38,7 @@ KDA_LAUNCH_TEST_WITHHOLD_STATE = 1 << 30  # test hook of the timeout path (inclu
 EXPORTED_SYMBOLS = ("kda_build_state_dtype", "kda_pool_check", "kda_state_bytes",
                     "kda_decode_step", "kda_spec_verify", "kda_step", "kda_prefill", "kda_prefill_workspace_bytes",
                     "kda_prefill_chunked", "kda_prefill_chunked_noalloc", "kda_conv_step",
-                    "kda_layout_id", "kda_ckpt_flush", "kda_ckpt_load", "kda_strerror")
+                    "kda_layout_id", "kda_ckpt_flush", "kda_ckpt_load", "kda_stage_host", "kda_strerror")
 
 
 class KdaError(RuntimeError):
@@ -90,6 +90,11 @@ class ConvArgs(ctypes.Structure):
                 ("cu_seqlens", ctypes.c_void_p), ("conv_slot", ctypes.c_void_p), ("accepted", ctypes.c_void_p),
                 ("reset", ctypes.c_void_p), ("x", ctypes.c_void_p), ("weight", ctypes.c_void_p),
                 ("bias", ctypes.c_void_p), ("y", ctypes.c_void_p)]
+
+
+class HostCopy(ctypes.Structure):
+    """Mirror of ``struct kda_host_copy`` (include/kda.h)."""
+    _fields_ = [("dst", ctypes.c_void_p), ("src", ctypes.c_void_p), ("bytes", ctypes.c_int64)]
 
 
 class CkptPlaneDesc(ctypes.Structure):
@@ -179,6 +184,8 @@ def _load(state16: bool) -> ctypes.CDLL:
         for fn in (lib.kda_ckpt_flush, lib.kda_ckpt_load):
             fn.restype = ctypes.c_int
             fn.argtypes = [P, ctypes.POINTER(CkptPlaneDesc), vp, vp, i32, vp, u32, vp]
+        lib.kda_stage_host.restype = ctypes.c_int
+        lib.kda_stage_host.argtypes = [ctypes.POINTER(HostCopy), i32, u32, vp]
         lib.kda_strerror.restype = ctypes.c_char_p
         lib.kda_strerror.argtypes = [i32]
         _libs[state16] = lib
@@ -359,6 +366,25 @@ class KdaLibrary:
         args = ConvArgs(n, total, int(max_t), kw, int(bool(silu)), 0, _ptr(cu_seqlens), _ptr(conv_slot),
                         _ptr(accepted), _ptr(reset), _ptr(x), _ptr(weight), _ptr(bias), _ptr(y))
         self._check(self.kda_conv_step_raw(win, args, _ptr(status), self._stream(stream), flags), "kda_conv_step")
+
+    def kda_stage_host_raw(self, copies, stream, flags=0) -> int:
+        """copies: a list of (dst device address, src pinned host address, bytes)."""
+        arr = (HostCopy * max(1, len(copies)))(*[HostCopy(d, s_, b) for d, s_, b in copies])
+        return self.lib.kda_stage_host(arr, len(copies), flags, stream)
+
+    def kda_stage_host(self, pairs, stream=None, flags=0) -> None:
+        """Copy each (dst, src) pair -- dst a contiguous CUDA tensor, src a
+        contiguous pinned CPU tensor of the same byte size -- with one kernel
+        launch (see kda_stage_host in include/kda.h)."""
+        copies = []
+        for dst, src in pairs:
+            if not dst.is_cuda or src.is_cuda or not dst.is_contiguous() or not src.is_contiguous():
+                raise ValueError("kda_stage_host copies a contiguous pinned CPU tensor into a contiguous CUDA tensor")
+            nb = dst.numel() * dst.element_size()
+            if src.numel() * src.element_size() != nb:
+                raise ValueError("source and destination differ in size")
+            copies.append((dst.data_ptr(), src.data_ptr(), nb))
+        self._check(self.kda_stage_host_raw(copies, self._stream(stream), flags), "kda_stage_host")
 
     def kda_layout_id(self, pool) -> int:
         desc = pool if isinstance(pool, PoolDesc) else pool_desc(pool)

@@ -22,7 +22,7 @@ INCLUDE = os.path.join(REPO_DIR, "include")
 LIB_DIR = os.path.join(PKG_DIR, "lib")
 SOURCES = [os.path.join(CSRC, f) for f in ("kda_api.cu", "kda_common.cuh", "kda_decode_tma.cuh",
                                           "kda_verify_tma.cuh", "kda_conv.cuh", "kda_ckpt.cuh",
-                                          "kda_prefill_chunk.cuh")] + [os.path.join(INCLUDE, "kda.h")]
+                                          "kda_prefill_chunk.cuh", "kda_stage.cuh")] + [os.path.join(INCLUDE, "kda.h")]
 
 ARCH_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

@@ -24,6 +24,7 @@
 #include "kda_conv.cuh"
 #include "kda_ckpt.cuh"
 #include "kda_prefill_chunk.cuh"
+#include "kda_stage.cuh"
 
 #ifndef KDA_STATE16
 #error "build with -DKDA_STATE16=0 (fp32 pool) or -DKDA_STATE16=1 (fp16 pool)"
@@ -67,6 +68,15 @@ static constexpr int kBuildDtype = KDA_F32;
 #else
 #define KDA_DEC_MINB 11
 #endif
+#endif
+// Warps per 16-column block of the prefill scan: KDA_PSCAN_KS_MID when the
+// grid has a CTA per SM or more only with one or two blocks per CTA, and
+// KDA_PSCAN_KS_FEW when it has fewer CTAs than SMs (few long prompts).
+#ifndef KDA_PSCAN_KS_MID
+#define KDA_PSCAN_KS_MID 1
+#endif
+#ifndef KDA_PSCAN_KS_FEW
+#define KDA_PSCAN_KS_FEW 4
 #endif
 #ifndef KDA_DEC_KEEP
 #define KDA_DEC_KEEP 0
@@ -198,20 +208,20 @@ void set_pdl(cudaLaunchConfig_t& cfg, cudaLaunchAttribute* attr, uint32_t flags)
     }
 }
 
-// The prefill scan pass with WPC warps (16 value columns each) per CTA,
-// launched with programmatic dependent launch so that it starts while the
-// first pass drains.
-template <int WPC>
+// The prefill scan pass with WPC column blocks of 16 value columns per CTA,
+// KS warps per block, launched with programmatic dependent launch so that it
+// starts while the first pass drains.
+template <int WPC, int KS>
 int launch_scan(const kda::StepParams& prm, const uint8_t* ws, int64_t heads, int v, cudaStream_t st) {
-    constexpr size_t smem = kda::PrefillScanSmem<WPC>::BYTES;
-    auto scan = kda::kda_prefill_scan_kernel<state_t, WPC>;
+    constexpr size_t smem = kda::PrefillScanSmem<WPC, KS>::BYTES;
+    auto scan = kda::kda_prefill_scan_kernel<state_t, WPC, KS>;
     int occ = 0, sms = 0;
-    const int rc = occupancy(reinterpret_cast<const void*>(scan), WPC * 32, smem, &occ, &sms);
+    const int rc = occupancy(reinterpret_cast<const void*>(scan), WPC * KS * 32, smem, &occ, &sms);
     if (rc != KDA_OK) return rc;
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr;
     cfg.gridDim = dim3((unsigned)(heads * ((v + 16 * WPC - 1) / (16 * WPC))), 1, 1);
-    cfg.blockDim = dim3(WPC * 32, 1, 1);
+    cfg.blockDim = dim3(WPC * KS * 32, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
     set_pdl(cfg, &attr, KDA_LAUNCH_PDL);
@@ -544,18 +554,21 @@ int kda_prefill_chunked(const kda_pool* pool, const kda_prefill_args* args, void
         }
     }
     if (err != cudaSuccess) return KDA_ERR_LAUNCH;
-    // the most warps per scan CTA (they share each chunk's operand copy) whose
-    // grid still covers the SMs: few long prompts get one-warp CTAs
+    // The most column blocks per scan CTA (they share each chunk's operand
+    // copy) whose grid still covers the SMs.  When even one block per CTA
+    // leaves SMs idle (few long prompts), each block's rows are split over
+    // KS warps, which shortens every chunk step.
     int sms = 0, dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
         return KDA_ERR_LAUNCH;
     const int64_t heads = (int64_t)g.n * pool->hv;
     auto ctas = [&](int wpc) { return heads * ((pool->v + 16 * wpc - 1) / (16 * wpc)); };
-    if (ctas(8) >= sms) return launch_scan<8>(prm, ws, heads, pool->v, st);
-    if (ctas(4) >= sms) return launch_scan<4>(prm, ws, heads, pool->v, st);
-    if (ctas(2) >= sms) return launch_scan<2>(prm, ws, heads, pool->v, st);
-    return launch_scan<1>(prm, ws, heads, pool->v, st);
+    if (ctas(8) >= sms) return launch_scan<8, 1>(prm, ws, heads, pool->v, st);
+    if (ctas(4) >= sms) return launch_scan<4, 1>(prm, ws, heads, pool->v, st);
+    if (ctas(2) >= sms) return launch_scan<2, KDA_PSCAN_KS_MID>(prm, ws, heads, pool->v, st);
+    if (ctas(1) >= sms) return launch_scan<1, KDA_PSCAN_KS_MID>(prm, ws, heads, pool->v, st);
+    return launch_scan<1, KDA_PSCAN_KS_FEW>(prm, ws, heads, pool->v, st);
 }
 
 int kda_prefill_chunked_noalloc(const kda_pool* pool, const kda_prefill_args* args, int32_t* dev_status,
@@ -645,6 +658,56 @@ int kda_conv_step(const kda_conv_window* win, const kda_conv_args* args, int32_t
             break;
     }
     return err == cudaSuccess ? KDA_OK : KDA_ERR_LAUNCH;
+}
+
+static_assert(kda::STAGE_MAX_COPIES == KDA_STAGE_MAX_COPIES, "staging copies per launch");
+
+int kda_stage_host(const kda_host_copy* copies, int32_t n, uint32_t flags, void* stream) {
+    if (n < 0 || n > KDA_STAGE_MAX_COPIES) return KDA_ERR_ARG;
+    if (flags & ~(uint32_t)KDA_LAUNCH_PDL) return KDA_ERR_ARG;
+    if (n == 0) return KDA_OK;
+    if (copies == nullptr) return KDA_ERR_NULL;
+    kda::StageParams prm = {};
+    int64_t total = 0;
+    for (int32_t i = 0; i < n; ++i) {
+        const kda_host_copy& c = copies[i];
+        if (c.bytes < 0 || c.bytes % 16 != 0) return KDA_ERR_ARG;
+        if (c.bytes > 0 && (c.dst == nullptr || c.src == nullptr)) return KDA_ERR_NULL;
+        if (!aligned(c.dst, 16) || !aligned(c.src, 16)) return KDA_ERR_ALIGN;
+        const void* dev_src = c.src;
+        if (c.bytes > 0) {
+            // the source: pinned host memory the device can address; the
+            // destination: device memory
+            cudaPointerAttributes a;
+            if (cudaPointerGetAttributes(&a, c.src) != cudaSuccess || a.type != cudaMemoryTypeHost ||
+                a.devicePointer == nullptr) {
+                cudaGetLastError();  // clear the error an unregistered pointer may leave
+                return KDA_ERR_ARG;
+            }
+            dev_src = a.devicePointer;
+            if (cudaPointerGetAttributes(&a, c.dst) != cudaSuccess || a.type != cudaMemoryTypeDevice) {
+                cudaGetLastError();
+                return KDA_ERR_ARG;
+            }
+            if (!aligned(dev_src, 16)) return KDA_ERR_ALIGN;
+        }
+        prm.dst[i] = static_cast<uint4*>(c.dst);
+        prm.src[i] = static_cast<const uint4*>(dev_src);
+        total += c.bytes / 16;
+        prm.end[i] = total;
+    }
+    prm.n = n;
+    prm.flags = flags;
+    if (total == 0) return KDA_OK;
+    const int64_t blocks = (total + kda::STAGE_THREADS - 1) / kda::STAGE_THREADS;
+    if (blocks > 0x7fffffffLL) return KDA_ERR_SHAPE;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)blocks, 1, 1);
+    cfg.blockDim = dim3(kda::STAGE_THREADS, 1, 1);
+    cfg.stream = static_cast<cudaStream_t>(stream);
+    cudaLaunchAttribute attr;
+    set_pdl(cfg, &attr, flags);
+    return cudaLaunchKernelEx(&cfg, kda::kda_stage_kernel, prm) == cudaSuccess ? KDA_OK : KDA_ERR_LAUNCH;
 }
 
 uint32_t kda_layout_id(const kda_pool* pool) {

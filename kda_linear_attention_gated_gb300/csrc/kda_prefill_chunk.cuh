@@ -253,43 +253,53 @@ __global__ void __launch_bounds__(KMAX, KDA_PREP_MINB) kda_prefill_prep_kernel(c
     }
 }
 
-// Pass 2 on the tensor cores.  grid = n * hv * ceil(v / (16 WPC)) CTAs of WPC
-// warps; warp w owns the 16 state columns c0 .. c0 + 15 (c0 = 16 (WPC cb + w))
-// with all K rows, held transposed, S^T (16 x K), in m16n8 accumulator
-// fragments: tile nt covers rows 8 nt .. 8 nt + 7 and lane (g, qd) = (lane / 4,
-// lane % 4) holds
+// Pass 2 on the tensor cores.  A CTA holds WPC column blocks of 16 value
+// columns, each worked by KS warps that split its K rows (the warps of block
+// cbk = w / KS own rows 128 / KS * (w % KS) ..); grid = n * hv * ceil(v / (16
+// WPC)).  A warp holds its part of the block's state transposed, S^T (16
+// columns x its rows), in m16n8 accumulator fragments: tile nt covers rows
+// 8 nt .. 8 nt + 7 and lane (g, qd) = (lane / 4, lane % 4) holds
 //   {S[8nt+2qd][c0+g], S[8nt+2qd+1][c0+g], S[8nt+2qd][c0+g+8], S[8nt+2qd+1][c0+g+8]}.
 // Two adjacent tiles are exactly the A fragment of a 16 x 16 block of S^T, so
 // every product takes the state straight from its accumulators:
 //   [X^T | Y^T] = S^T [W'^T | Q'^T]    (16 x K by K x 32: X = W' S, Y = Q' S)
 //   D^T = U^T - X^T,  O^T = Y^T + O_intra^T
 //   S^T <- S^T diag(c) + D^T Ke        (16 x 16 by 16 x K onto the scaled accumulators)
-// No sum crosses a warp.  mma.sync takes bf16 operands and accumulates in
-// fp32; fp32 accuracy comes from splitting each factor in three bf16 parts
-// (x = x0 + x1 + x2 exactly) and summing the six products x_i y_j with
-// i + j <= 2: the three left out are below 2^-23 |x y| together.
-template <int WPC>
+// With KS > 1 each warp forms X^T and Y^T over its rows only; the KS partial
+// sums meet in shared memory and every warp of the block adds them in the same
+// order, so all of them hold the same D.  No other sum crosses a warp.
+// mma.sync takes bf16 operands and accumulates in fp32; fp32 accuracy comes
+// from splitting each factor in three bf16 parts (x = x0 + x1 + x2 exactly)
+// and summing the six products x_i y_j with i + j <= 2: the three left out
+// are below 2^-23 |x y| together.
+template <int WPC, int KS>
 struct PrefillScanSmem {
-    static constexpr uint32_t BYTES = 2 * PCH_BYTES + 16;  // two chunk buffers, two barriers
+    static constexpr uint32_t XCH = KS > 1 ? WPC * KS * 32 * 16 * 4 : 0;  // partial sums [block][ks][lane][16]
+    static constexpr uint32_t BYTES = 2 * PCH_BYTES + XCH + 16;          // two chunk buffers, two barriers
 };
 
-template <typename ST, int WPC>
-__global__ void __launch_bounds__(WPC * 32, 1) kda_prefill_scan_kernel(const StepParams p,
-                                                                      const uint8_t* __restrict__ ws) {
-    static_assert(WPC == 1 || WPC == 2 || WPC == 4 || WPC == 8, "warps per scan CTA");
-    constexpr int NT = WPC * 32, NTILE = KMAX / 8;
+template <typename ST, int WPC, int KS>
+__global__ void __launch_bounds__(WPC * KS * 32, 1) kda_prefill_scan_kernel(const StepParams p,
+                                                                           const uint8_t* __restrict__ ws) {
+    static_assert(WPC == 1 || WPC == 2 || WPC == 4 || WPC == 8, "column blocks per scan CTA");
+    static_assert(KS == 1 || KS == 2 || KS == 4, "warps per column block");
+    constexpr int NT = WPC * KS * 32, NTILE = KMAX / 8, MT = NTILE / KS;  // MT: row tiles per warp
+    using SM = PrefillScanSmem<WPC, KS>;
     extern __shared__ __align__(1024) uint8_t smem[];
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + 2 * PCH_BYTES);  // two chunk-operand barriers
+    float* xch = reinterpret_cast<float*>(smem + 2 * PCH_BYTES);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + 2 * PCH_BYTES + SM::XCH);  // two chunk-operand barriers
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int cbk = warp / KS, ks = warp - cbk * KS;
     const int g = lane >> 2, qd = lane & 3;
     const int ctiles = (p.v + 16 * WPC - 1) / (16 * WPC);
     const int tile = (int)blockIdx.x;
     const int r = tile / (p.hv * ctiles);
     const int rem = tile - r * p.hv * ctiles;
     const int h = rem / ctiles, cb = rem - h * ctiles;
-    const int c0 = (cb * WPC + warp) * 16;
-    const bool wact = c0 < p.v;  // V is a multiple of 16: a warp's columns are all in or all out
+    const int c0 = (cb * WPC + cbk) * 16;
+    const bool wact = c0 < p.v;  // V is a multiple of 16: a block's columns are all in or all out
+    const int t0 = ks * MT;      // this warp's first row tile
     cudaTriggerProgrammaticLaunchCompletion();
     cudaGridDependencySynchronize();
 
@@ -318,16 +328,16 @@ __global__ void __launch_bounds__(WPC * 32, 1) kda_prefill_scan_kernel(const Ste
     const int nch = (Tn + PCH - 1) / PCH;
     const int nkt = p.k / 8;  // row tiles in use (K is a multiple of 16)
 
-    // the state, transposed, in accumulator fragments
-    float acc[NTILE][4];
+    // this warp's rows of the state, transposed, in accumulator fragments
+    float acc[MT][4];
     const bool rst = p.reset != nullptr && p.reset[r] != 0;
     const ST* src = static_cast<const ST*>(p.pool) + state_at(p, slot, h);
 #pragma unroll
-    for (int nt = 0; nt < NTILE; ++nt)
+    for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-            const int row = 8 * nt + 2 * qd + (e & 1), col = c0 + g + 8 * (e >> 1);
-            acc[nt][e] = (!rst && wact && nt < nkt) ? to_f32(src[(int64_t)row * p.v + col]) : 0.f;
+            const int row = 8 * (t0 + mt) + 2 * qd + (e & 1), col = c0 + g + 8 * (e >> 1);
+            acc[mt][e] = (!rst && wact && t0 + mt < nkt) ? to_f32(src[(int64_t)row * p.v + col]) : 0.f;
         }
 
     // chunk j's operand block -> buffer j % 2, one barrier per buffer
@@ -369,33 +379,36 @@ __global__ void __launch_bounds__(WPC * 32, 1) kda_prefill_scan_kernel(const Ste
         const float* cc = reinterpret_cast<const float*>(buf + PB_C);
         const float* U = reinterpret_cast<const float*>(buf + PB_U);
         const float* OI = reinterpret_cast<const float*>(buf + PB_OI);
-        if (wact) {
-            // X^T (tiles 0, 1: tokens 0-7, 8-15) and Y^T (tiles 2, 3): the
-            // leading product and the five small ones in separate sums
-            float xh[4][4], xl[4][4];
+        // X^T (tiles 0, 1: tokens 0-7, 8-15) and Y^T (tiles 2, 3) over this
+        // warp's rows: the leading product and the five small ones in
+        // separate sums, each of those per k-step parity (shorter chains)
+        float xs[4][4];
+        {
+            float xh[4][4], xl[2][4][4];
 #pragma unroll
             for (int t = 0; t < 4; ++t)
 #pragma unroll
-                for (int e = 0; e < 4; ++e) { xh[t][e] = 0.f; xl[t][e] = 0.f; }
+                for (int e = 0; e < 4; ++e) { xh[t][e] = 0.f; xl[0][t][e] = 0.f; xl[1][t][e] = 0.f; }
 #pragma unroll
-            for (int kk = 0; kk < NTILE / 2; ++kk) {
-                if (2 * kk >= nkt) break;  // (unrolled: the state's tiles keep register indices)
+            for (int kk = 0; kk < MT / 2; ++kk) {
+                if (!wact || t0 + 2 * kk >= nkt) break;  // (unrolled: the state's tiles keep register indices)
                 uint32_t a[3][4];
                 split3_bf16x2(acc[2 * kk][0], acc[2 * kk][1], a[0][0], a[1][0], a[2][0]);
                 split3_bf16x2(acc[2 * kk][2], acc[2 * kk][3], a[0][1], a[1][1], a[2][1]);
                 split3_bf16x2(acc[2 * kk + 1][0], acc[2 * kk + 1][1], a[0][2], a[1][2], a[2][2]);
                 split3_bf16x2(acc[2 * kk + 1][2], acc[2 * kk + 1][3], a[0][3], a[1][3], a[2][3]);
+                const uint32_t kofs = (t0 / 2 + kk) * 32;
 #pragma unroll
                 for (int m = 0; m < 2; ++m) {
                     uint32_t b[3][4];
 #pragma unroll
                     for (int part = 0; part < 3; ++part)
-                        ldsm_x4((m ? bq : bw) + part * PART_BYTES + lwq + kk * 32, b[part][0], b[part][1], b[part][2],
+                        ldsm_x4((m ? bq : bw) + part * PART_BYTES + lwq + kofs, b[part][0], b[part][1], b[part][2],
                                 b[part][3]);
 #pragma unroll
                     for (int nh = 0; nh < 2; ++nh) {
                         float(&dh)[4] = xh[2 * m + nh];
-                        float(&dl)[4] = xl[2 * m + nh];
+                        float(&dl)[4] = xl[kk & 1][2 * m + nh];
                         const int i0 = 2 * nh, i1 = 2 * nh + 1;
                         mma_16816_bf16(dh, a[0][0], a[0][1], a[0][2], a[0][3], b[0][i0], b[0][i1]);
                         mma_16816_bf16(dl, a[0][0], a[0][1], a[0][2], a[0][3], b[1][i0], b[1][i1]);
@@ -406,6 +419,30 @@ __global__ void __launch_bounds__(WPC * 32, 1) kda_prefill_scan_kernel(const Ste
                     }
                 }
             }
+#pragma unroll
+            for (int t = 0; t < 4; ++t)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) xs[t][e] = xh[t][e] + (xl[0][t][e] + xl[1][t][e]);
+        }
+        if constexpr (KS > 1) {
+            // the block's KS partial sums, added in the same order by every
+            // warp of the block
+            float4* mine = reinterpret_cast<float4*>(xch + ((cbk * KS + ks) * 32 + lane) * 16);
+#pragma unroll
+            for (int t = 0; t < 4; ++t) mine[t] = make_float4(xs[t][0], xs[t][1], xs[t][2], xs[t][3]);
+            __syncthreads();
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+                float4 sum = reinterpret_cast<const float4*>(xch + ((cbk * KS) * 32 + lane) * 16)[t];
+#pragma unroll
+                for (int k2 = 1; k2 < KS; ++k2) {
+                    const float4 o4 = reinterpret_cast<const float4*>(xch + ((cbk * KS + k2) * 32 + lane) * 16)[t];
+                    sum.x += o4.x; sum.y += o4.y; sum.z += o4.z; sum.w += o4.w;
+                }
+                xs[t][0] = sum.x; xs[t][1] = sum.y; xs[t][2] = sum.z; xs[t][3] = sum.w;
+            }
+        }
+        if (wact) {
             // D^T = U^T - X^T; O^T = Y^T + O_intra^T for the chunk's tokens
             const int cl = min(PCH, Tn - j * PCH);
             float dd[2][4];
@@ -414,29 +451,28 @@ __global__ void __launch_bounds__(WPC * 32, 1) kda_prefill_scan_kernel(const Ste
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     const int tok = 8 * nt + 2 * qd + (e & 1), col = c0 + g + 8 * (e >> 1);
-                    dd[nt][e] = U[tok * PU_ROW + col] - (xh[nt][e] + xl[nt][e]);
-                    if (tok < cl)
-                        p.o[((int64_t)(tb + j * PCH + tok) * p.hv + h) * p.v + col] =
-                            (xh[2 + nt][e] + xl[2 + nt][e]) + OI[tok * PU_ROW + col];
+                    dd[nt][e] = U[tok * PU_ROW + col] - xs[nt][e];
+                    if (ks == 0 && tok < cl)
+                        p.o[((int64_t)(tb + j * PCH + tok) * p.hv + h) * p.v + col] = xs[2 + nt][e] + OI[tok * PU_ROW + col];
                 }
-            // S^T <- S^T diag(c) + D^T Ke
+            // S^T <- S^T diag(c) + D^T Ke on this warp's rows
             uint32_t a[3][4];
             split3_bf16x2(dd[0][0], dd[0][1], a[0][0], a[1][0], a[2][0]);
             split3_bf16x2(dd[0][2], dd[0][3], a[0][1], a[1][1], a[2][1]);
             split3_bf16x2(dd[1][0], dd[1][1], a[0][2], a[1][2], a[2][2]);
             split3_bf16x2(dd[1][2], dd[1][3], a[0][3], a[1][3], a[2][3]);
 #pragma unroll
-            for (int np = 0; np < NTILE / 2; ++np) {
-                if (2 * np < nkt) {
+            for (int np = 0; np < MT / 2; ++np) {
+                if (t0 + 2 * np < nkt) {
                     uint32_t b[3][4];
 #pragma unroll
                     for (int part = 0; part < 3; ++part)
-                        ldsm_x4_trans(bke + part * PART_BYTES + lke + np * 32, b[part][0], b[part][1], b[part][2],
-                                      b[part][3]);
+                        ldsm_x4_trans(bke + part * PART_BYTES + lke + (t0 / 2 + np) * 32, b[part][0], b[part][1],
+                                      b[part][2], b[part][3]);
 #pragma unroll
                     for (int nh = 0; nh < 2; ++nh) {
                         float(&s4)[4] = acc[2 * np + nh];
-                        const int row = 8 * (2 * np + nh) + 2 * qd;
+                        const int row = 8 * (t0 + 2 * np + nh) + 2 * qd;
                         const float c_lo = cc[row], c_hi = cc[row + 1];
                         s4[0] *= c_lo; s4[1] *= c_hi; s4[2] *= c_lo; s4[3] *= c_hi;
                         const int i0 = 2 * nh, i1 = 2 * nh + 1;
@@ -450,8 +486,8 @@ __global__ void __launch_bounds__(WPC * 32, 1) kda_prefill_scan_kernel(const Ste
                 }
             }
         }
-        // every thread is done with this buffer before the next issue
-        // (generic reads, then async writes: fence first)
+        // every thread is done with this buffer and the partial sums before
+        // the next issue (generic reads, then async writes: fence first)
         fence_proxy_async_smem();
         __syncthreads();
     }
@@ -466,13 +502,13 @@ __global__ void __launch_bounds__(WPC * 32, 1) kda_prefill_scan_kernel(const Ste
     if (fin_slot >= 0 && wact) {
         ST* dst = static_cast<ST*>(p.pool) + state_at(p, fin_slot, h);
 #pragma unroll
-        for (int nt = 0; nt < NTILE; ++nt)
+        for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-                const int row = 8 * nt + 2 * qd + (e & 1), col = c0 + g + 8 * (e >> 1);
-                if (nt < nkt) {
-                    if constexpr (sizeof(ST) == 4) dst[(int64_t)row * p.v + col] = acc[nt][e];
-                    else dst[(int64_t)row * p.v + col] = __float2half_rn(acc[nt][e]);
+                const int row = 8 * (t0 + mt) + 2 * qd + (e & 1), col = c0 + g + 8 * (e >> 1);
+                if (t0 + mt < nkt) {
+                    if constexpr (sizeof(ST) == 4) dst[(int64_t)row * p.v + col] = acc[mt][e];
+                    else dst[(int64_t)row * p.v + col] = __float2half_rn(acc[mt][e]);
                 }
             }
     }
