@@ -76,7 +76,7 @@ static constexpr int kBuildDtype = KDA_F32;
 #define KDA_PSCAN_KS_MID 1
 #endif
 #ifndef KDA_PSCAN_KS_FEW
-#define KDA_PSCAN_KS_FEW 4
+#define KDA_PSCAN_KS_FEW 2
 #endif
 #ifndef KDA_DEC_KEEP
 #define KDA_DEC_KEEP 0
