@@ -52,8 +52,10 @@ _CODE_TOKENS = None
 
 # The sources that define the decode kernel and its launch shape: a recorded
 # traffic figure stays valid while their code (comments and layout removed)
-# is unchanged.
+# is unchanged.  Of kda_api.cu only the lines of the decode tile shape
+# (the KDA_DEC_* settings and the decode launcher) count.
 DECODE_SOURCES = ("kda_common.cuh", "kda_decode_tma.cuh", "kda_api.cu")
+DECODE_API_MARKERS = ("KDA_DEC_", "launch_decode", "decode_smem_bytes", "kda_decode_kernel")
 
 
 def code_text(src: str) -> str:
@@ -80,10 +82,16 @@ def source_hash(paths=None) -> str:
     measured on an older kernel is recognised as stale, while an edited
     comment leaves it valid."""
     import hashlib
+    h = hashlib.sha256()
     if paths is None:
         csrc = os.path.join(REPO, "kda_linear_attention_gated_gb300", "csrc")
-        paths = [os.path.join(csrc, f) for f in DECODE_SOURCES]
-    h = hashlib.sha256()
+        for name in DECODE_SOURCES:
+            with open(os.path.join(csrc, name), encoding="utf-8") as f:
+                code = code_text(f.read())
+            if name == "kda_api.cu":
+                code = "\n".join(l for l in code.splitlines() if any(m in l for m in DECODE_API_MARKERS))
+            h.update(code.encode())
+        return h.hexdigest()[:16]
     for path in paths:
         with open(path, encoding="utf-8") as f:
             h.update(code_text(f.read()).encode())
