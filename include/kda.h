@@ -25,10 +25,17 @@
  * Conventions for every entry point:
  *  - Return value: KDA_OK (0) or a kda_status code; argument errors are
  *    detected on the host, synchronously, before anything is launched.
- *  - Memory: the caller owns every buffer and the stream; the library
- *    allocates nothing, keeps no state between calls and never synchronises.
- *    Pointers marked "device" must be device-accessible (cudaMalloc'd);
- *    pointers marked "host" are read on the host during the call.
+ *  - Memory: the caller owns every buffer and the stream; no call allocates
+ *    memory, keeps state between calls or synchronises.  One exception to
+ *    "the library holds no memory": each library build carries the
+ *    KDA_PREFILL_SCRATCH_BYTES (128 MB) scratch array of
+ *    kda_prefill_chunked_noalloc as a file-scope device array, resident on
+ *    every device where the library's module is loaded (by its first kernel
+ *    launch of any kind) for the life of the process, whether or not that
+ *    entry point is ever called; a process that loads both builds holds
+ *    256 MB per device.  Pointers marked "device" must be device-accessible
+ *    (cudaMalloc'd); pointers marked "host" are read on the host during the
+ *    call.
  *  - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
  *    stream) and runs asynchronously; outputs are valid once it completes.
  *  - Device-side errors do not trap.  A slot id outside [0, num_slots): the
@@ -379,12 +386,19 @@ int kda_prefill_chunked(const kda_pool* pool, const kda_prefill_args* args, void
                         int64_t workspace_bytes, int32_t* dev_status, uint32_t flags, void* stream);
 
 /*
- * kda_prefill_chunked without a caller workspace, allocating nothing: the
- * first pass's results go to a scratch buffer of KDA_PREFILL_SCRATCH_BYTES
- * that the library holds in device memory for the life of the process (one
- * per device).  KDA_ERR_SHAPE when kda_prefill_workspace_bytes(...) exceeds
- * it.  Calls share that buffer, so they must be ordered (one stream, or
- * streams synchronised between calls); otherwise as kda_prefill_chunked.
+ * kda_prefill_chunked without a caller workspace, allocating nothing, for
+ * callers that cannot call cudaMalloc (inside a stream capture whose
+ * allocation mode forbids it, or a runtime that hands out no device memory):
+ * the first pass's results go to a scratch buffer of KDA_PREFILL_SCRATCH_BYTES
+ * that each library build holds in device memory as a file-scope array,
+ * resident on every device where the library's module is loaded, for the life
+ * of the process.  The first call on a device looks up the array's device
+ * address (cudaGetSymbolAddress); make that first call before any stream
+ * capture.  KDA_ERR_SHAPE when kda_prefill_workspace_bytes(...) exceeds the
+ * buffer (at HV=12, K=V=128 it holds about 4K tokens).  Every call shares the
+ * buffer, and calls that overlap on the GPU race on it: order them (one
+ * stream, or streams synchronised between calls).  The pages have no
+ * counterpart; otherwise as kda_prefill_chunked.
  */
 #define KDA_PREFILL_SCRATCH_BYTES (128ll << 20)
 int kda_prefill_chunked_noalloc(const kda_pool* pool, const kda_prefill_args* args, int32_t* dev_status,
