@@ -134,3 +134,16 @@ def test_prefill_call_without_tokens(state_dtype, chunked):
     gp, o, st, P, o_ref = run(inp, chunked=chunked)
     assert st == 0 and o.shape[0] == 0
     assert_pool_match(gp, P, written(inp), "pool")
+
+
+@pytest.mark.parametrize("n_prompts", [8, 16])
+def test_chunked_prefill_wide_scan_tilings(n_prompts):
+    """8 prompts (96 heads: four 16-column blocks per scan CTA) and 16 prompts
+    (192 heads: eight blocks per CTA), ragged lengths, fp16 pool: the scan
+    shapes a batch takes, against the oracle."""
+    lens = tuple(17 + 9 * i for i in range(n_prompts))
+    inp = workloads.make_prefill(lens=lens, state_dtype=torch.float16, num_slots=2 * n_prompts + 2, seed=97)
+    gp, o, st, P, o_ref = run(inp, chunked=True)
+    assert st == 0
+    assert_out_match(o, o_ref, torch.float16, "o")
+    assert_pool_match(gp, P, written(inp), "pool")
