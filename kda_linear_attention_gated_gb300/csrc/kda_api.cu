@@ -214,7 +214,10 @@ void set_pdl(cudaLaunchConfig_t& cfg, cudaLaunchAttribute* attr, uint32_t flags)
 template <int WPC, int KS>
 int launch_scan(const kda::StepParams& prm, const uint8_t* ws, int64_t heads, int v, cudaStream_t st) {
     constexpr size_t smem = kda::PrefillScanSmem<WPC, KS>::BYTES;
-    auto scan = kda::kda_prefill_scan_kernel<state_t, WPC, KS>;
+    // K = 128 (the configured models' key dimension) gets a build whose row
+    // loops have compile-time bounds
+    auto scan = prm.k == kda::KMAX ? kda::kda_prefill_scan_kernel<state_t, WPC, KS, true>
+                                   : kda::kda_prefill_scan_kernel<state_t, WPC, KS, false>;
     int occ = 0, sms = 0;
     const int rc = occupancy(reinterpret_cast<const void*>(scan), WPC * KS * 32, smem, &occ, &sms);
     if (rc != KDA_OK) return rc;

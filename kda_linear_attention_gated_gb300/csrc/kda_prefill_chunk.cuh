@@ -278,7 +278,7 @@ struct PrefillScanSmem {
     static constexpr uint32_t BYTES = 2 * PCH_BYTES + XCH + 16;          // two chunk buffers, two barriers
 };
 
-template <typename ST, int WPC, int KS>
+template <typename ST, int WPC, int KS, bool FULLK>
 __global__ void __launch_bounds__(WPC * KS * 32, 1) kda_prefill_scan_kernel(const StepParams p,
                                                                            const uint8_t* __restrict__ ws) {
     static_assert(WPC == 1 || WPC == 2 || WPC == 4 || WPC == 8, "column blocks per scan CTA");
@@ -326,7 +326,7 @@ __global__ void __launch_bounds__(WPC * KS * 32, 1) kda_prefill_scan_kernel(cons
     // its final slot: the state after its last token
     if (Tn == 0 && fin_slot < 0) return;
     const int nch = (Tn + PCH - 1) / PCH;
-    const int nkt = p.k / 8;  // row tiles in use (K is a multiple of 16)
+    const int nkt = FULLK ? NTILE : p.k / 8;  // row tiles in use (K is a multiple of 16)
 
     // this warp's rows of the state, transposed, in accumulator fragments
     float acc[MT][4];
