@@ -268,7 +268,11 @@ int launch_verify(const kda_pool* pool, const kda::StepParams& prm, cudaStream_t
     constexpr int BV = KDA_VER_BV;
     using SH = kda::VerifyShape<state_t, BV, (int)sizeof(QT)>;
     constexpr size_t smem = kda::verify_smem_bytes<state_t, BV, (int)sizeof(QT)>();
-    auto kernel = kda::kda_verify_kernel<state_t, QT, BV>;
+    // an fp16 pool at K = 128 gets the build with compile-time row loops; an
+    // fp32 pool's 256-thread tiles have no register room for it (it spills)
+    constexpr bool kFullkOk = sizeof(state_t) == 2;
+    auto kernel = (kFullkOk && prm.k == kda::KMAX) ? kda::kda_verify_kernel<state_t, QT, BV, kFullkOk>
+                                                   : kda::kda_verify_kernel<state_t, QT, BV, false>;
     const int64_t tiles = (int64_t)prm.n * prm.hv * ((prm.v + BV - 1) / BV);
     if (tiles > 0x7fffffffLL) return KDA_ERR_SHAPE;
     CUtensorMap map;
@@ -648,16 +652,19 @@ int kda_conv_step(const kda_conv_window* win, const kda_conv_args* args, int32_t
     constexpr int C1 = CONV_THREADS, C4 = CONV_VEC_THREADS, K1 = CONV_KW_MAX, K4 = CONV_VEC_KW_MAX;
     switch (win->dtype) {
         case KDA_F32:
-            err = vec4 ? cudaLaunchKernelEx(&cfg, kda_conv_kernel<float, 4, C4, K4>, prm)
-                       : cudaLaunchKernelEx(&cfg, kda_conv_kernel<float, 1, C1, K1>, prm);
+            err = vec4 ? (g.kernel_width == 4 ? cudaLaunchKernelEx(&cfg, kda_conv_kernel<float, 4, C4, K4, 4>, prm)
+                                               : cudaLaunchKernelEx(&cfg, kda_conv_kernel<float, 4, C4, K4, 0>, prm))
+                       : cudaLaunchKernelEx(&cfg, kda_conv_kernel<float, 1, C1, K1, 0>, prm);
             break;
         case KDA_F16:
-            err = vec4 ? cudaLaunchKernelEx(&cfg, kda_conv_kernel<__half, 4, C4, K4>, prm)
-                       : cudaLaunchKernelEx(&cfg, kda_conv_kernel<__half, 1, C1, K1>, prm);
+            err = vec4 ? (g.kernel_width == 4 ? cudaLaunchKernelEx(&cfg, kda_conv_kernel<__half, 4, C4, K4, 4>, prm)
+                                               : cudaLaunchKernelEx(&cfg, kda_conv_kernel<__half, 4, C4, K4, 0>, prm))
+                       : cudaLaunchKernelEx(&cfg, kda_conv_kernel<__half, 1, C1, K1, 0>, prm);
             break;
         default:
-            err = vec4 ? cudaLaunchKernelEx(&cfg, kda_conv_kernel<__nv_bfloat16, 4, C4, K4>, prm)
-                       : cudaLaunchKernelEx(&cfg, kda_conv_kernel<__nv_bfloat16, 1, C1, K1>, prm);
+            err = vec4 ? (g.kernel_width == 4 ? cudaLaunchKernelEx(&cfg, kda_conv_kernel<__nv_bfloat16, 4, C4, K4, 4>, prm)
+                                               : cudaLaunchKernelEx(&cfg, kda_conv_kernel<__nv_bfloat16, 4, C4, K4, 0>, prm))
+                       : cudaLaunchKernelEx(&cfg, kda_conv_kernel<__nv_bfloat16, 1, C1, K1, 0>, prm);
             break;
     }
     return err == cudaSuccess ? KDA_OK : KDA_ERR_LAUNCH;

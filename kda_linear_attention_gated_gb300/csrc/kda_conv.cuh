@@ -92,8 +92,11 @@ struct ConvIO {
 // weights, bias and the window entries -- go out before the wait for it, so
 // they overlap its tail; the inputs x are read, and everything is written,
 // after the wait.
-template <typename ET, int VC, int CT, int KWM>
+// KWF: the kernel width fixed at compile time (0: read from the parameters).
+template <typename ET, int VC, int CT, int KWM, int KWF>
 __global__ void __launch_bounds__(CT) kda_conv_kernel(const ConvParams p) {
+    static_assert(KWF <= KWM, "fixed kernel width");
+#define KWR (KWF > 0 ? KWF : p.KW)
     using IO = ConvIO<ET, VC>;
     using R = typename IO::R;
     const int cblocks = (p.C / VC + CT - 1) / CT;
@@ -111,7 +114,7 @@ __global__ void __launch_bounds__(CT) kda_conv_kernel(const ConvParams p) {
     const int32_t slot = p.conv_slot[r];
     const int acc = p.accepted != nullptr ? p.accepted[r] - 1 : 0;
     const bool rst = p.reset != nullptr && p.reset[r] != 0;
-    const int m = acc + p.KW - 1;
+    const int m = acc + KWR - 1;
     const int kept = max(0, p.L - T);
     constexpr int CB = 8;  // window entries or tokens per batch of loads
     const bool range_ok = tb >= 0 && T > 0 && T <= p.t && tb + T <= p.total;
@@ -151,7 +154,7 @@ __global__ void __launch_bounds__(CT) kda_conv_kernel(const ConvParams p) {
     // window or the request's tokens, so that a batch is in flight at once;
     // the values out of range are dropped where they are used.
     ET* W = static_cast<ET*>(p.window) + (int64_t)slot * p.slot_stride + c;
-    const int nh = p.KW - 1;  // history entries
+    const int nh = KWR - 1;  // history entries
     // the history entries and the first batch of kept old entries, read
     // together (the kept entries W[m - kept + e] move to W[e])
     R hr[KWM], kv[CB];
@@ -164,10 +167,10 @@ __global__ void __launch_bounds__(CT) kda_conv_kernel(const ConvParams p) {
 #pragma unroll
     for (int i = 0; i < KWM; ++i)
 #pragma unroll
-        for (int v = 0; v < VC; ++v) w[i][v] = i < nh ? __ldg(p.w + (int64_t)(c + v) * p.KW + i) : 0.f;
+        for (int v = 0; v < VC; ++v) w[i][v] = i < nh ? __ldg(p.w + (int64_t)(c + v) * KWR + i) : 0.f;
 #pragma unroll
     for (int v = 0; v < VC; ++v) {
-        wlast[v] = __ldg(p.w + (int64_t)(c + v) * p.KW + p.KW - 1);
+        wlast[v] = __ldg(p.w + (int64_t)(c + v) * KWR + KWR - 1);
         bias[v] = p.bias != nullptr ? __ldg(p.bias + c + v) : 0.f;
     }
     if (early) {
@@ -246,5 +249,6 @@ __global__ void __launch_bounds__(CT) kda_conv_kernel(const ConvParams p) {
             if (e0 + u < nin) IO::st(W + (int64_t)(kept + e0 + u) * p.C, v[u]);
     }
 }
+#undef KWR
 
 }  // namespace kda

@@ -131,9 +131,12 @@ __device__ __forceinline__ void ab_terms(float (&out)[32], const float (&bk)[TC]
     }
 }
 
-template <typename ST, typename QT, int BV>
+// FULLK: K = KMAX, known at compile time (the row guards and loops fold away).
+template <typename ST, typename QT, int BV, bool FULLK>
 __global__ void __launch_bounds__(VerifyShape<ST, BV, (int)sizeof(QT)>::NT, VerifyShape<ST, BV, (int)sizeof(QT)>::MINB)
 kda_verify_kernel(const __grid_constant__ CUtensorMap tmap, const StepParams p) {
+// key rows: KMAX in the K = KMAX build, else read from the parameters where used
+#define KK (FULLK ? KMAX : p.k)
     using SH = VerifyShape<ST, BV, (int)sizeof(QT)>;
     using SV = StateVec<ST>;
     constexpr int VEC = SH::VEC, NW = SH::NW, ROWS = SH::ROWS, TC = SH::TC, G = SH::G;
@@ -186,14 +189,14 @@ kda_verify_kernel(const __grid_constant__ CUtensorMap tmap, const StepParams p) 
         const QT* qp = static_cast<const QT*>(p.q);
         const QT* kp = static_cast<const QT*>(p.kk);
         const QT* vp = static_cast<const QT*>(p.vv);
-        const int row = tid < p.k ? tid : 0, col = tid < vcols ? tid : 0;
+        const int row = tid < KK ? tid : 0, col = tid < vcols ? tid : 0;
 #pragma unroll
         for (int j = 0; j < TC; ++j) {
             const int64_t tok = (int64_t)tb + t0 + min(j, tc - 1);
-            const int64_t rq = (tok * p.hqk + hq) * p.k + row, rt = tok * p.hv + h;
+            const int64_t rq = (tok * p.hqk + hq) * KK + row, rt = tok * p.hv + h;
             kraw[j] = (RT)kp[rq];
             qraw[j] = (RT)qp[rq];
-            araw[j] = __ldg(p.a + rt * p.k + row);
+            araw[j] = __ldg(p.a + rt * KK + row);
             vraw[j] = (RT)vp[rt * p.v + (int64_t)cb * BV + col];
         }
     };
@@ -244,9 +247,9 @@ kda_verify_kernel(const __grid_constant__ CUtensorMap tmap, const StepParams p) 
     const bool need_state = Tn > 0 || (final_mode && fin >= 0);
     if (tid == 0 && !bad && !pad && !rst && need_state) {
         prefetch_tmap(&tmap);
-        mbar_arrive_expect_tx(bar_st, (uint32_t)p.k * SH::ROWBYTES);
+        mbar_arrive_expect_tx(bar_st, (uint32_t)KK * SH::ROWBYTES);
         if (!(p.flags & LAUNCH_TEST_WITHHOLD_STATE))  // the test hook: the wait runs out
-            tma_load_3d(smem, &tmap, bar_st, cb * BV, h * p.k, slot);
+            tma_load_3d(smem, &tmap, bar_st, cb * BV, h * KK, slot);
     }
     if (early) {
         cudaGridDependencySynchronize();
@@ -270,20 +273,20 @@ kda_verify_kernel(const __grid_constant__ CUtensorMap tmap, const StepParams p) 
             alive = false;
         } else {
             if (rst) {
-                for (int e = tid; e < p.k * (SH::ROWBYTES / 16); e += SH::NT)
+                for (int e = tid; e < KK * (SH::ROWBYTES / 16); e += SH::NT)
                     sts128(tile_base + e * 16, make_uint4(0u, 0u, 0u, 0u));
                 fence_proxy_async_smem();
             }
             __syncthreads();
             if (tid == 0) {
-                tma_store_3d(&tmap, smem, cb * BV, h * p.k, fin);
+                tma_store_3d(&tmap, smem, cb * BV, h * KK, fin);
                 bulk_commit();
             }
         }
     }
     const bool scaled = p.a_log != nullptr;
     const float gscale = scaled ? expf(__ldg(p.a_log + h)) : 1.f;
-    const float gbias = p.dt_bias != nullptr && tid < p.k ? __ldg(p.dt_bias + (int64_t)h * p.k + tid) : 0.f;
+    const float gbias = p.dt_bias != nullptr && tid < KK ? __ldg(p.dt_bias + (int64_t)h * KK + tid) : 0.f;
     for (int t0 = 0; t0 < Tn; t0 += TC) {
         const int tc = min(TC, Tn - t0);
         if (t0 > 0 || !PRO_INPUTS) load_inputs(t0, tc);
@@ -301,7 +304,7 @@ kda_verify_kernel(const __grid_constant__ CUtensorMap tmap, const StepParams p) 
             float kt[TC], qt[TC], at[TC];
 #pragma unroll
             for (int j = 0; j < TC; ++j) {
-                const bool in_row = j < tc && tid < p.k;
+                const bool in_row = j < tc && tid < KK;
                 kt[j] = in_row ? to_f32(kraw[j]) : 0.f;
                 qt[j] = in_row ? to_f32(qraw[j]) : 0.f;
                 at[j] = in_row ? araw[j] : 0.f;
@@ -315,16 +318,16 @@ kda_verify_kernel(const __grid_constant__ CUtensorMap tmap, const StepParams p) 
             // the decay, one branch for all tokens
             if (scaled) {
 #pragma unroll
-                for (int j = 0; j < TC; ++j) at[j] = j < tc && tid < p.k ? gate_alpha(at[j], true, gscale, gbias) : 0.f;
+                for (int j = 0; j < TC; ++j) at[j] = j < tc && tid < KK ? gate_alpha(at[j], true, gscale, gbias) : 0.f;
             } else {
 #pragma unroll
-                for (int j = 0; j < TC; ++j) at[j] = j < tc && tid < p.k ? gate_alpha(at[j], false, gscale, gbias) : 0.f;
+                for (int j = 0; j < TC; ++j) at[j] = j < tc && tid < KK ? gate_alpha(at[j], false, gscale, gbias) : 0.f;
             }
             // the first chunk of an fp16 pool at K = KMAX takes its column sums
             // on the tensor cores: rows 2 j (c k) and 2 j + 1 (c q) of the gate
             // matrix, each value split into three fp16 parts g = h0 + h1 2^-11 +
             // h2 2^-22 (exact differences; the rest is below 2^-33 |g|)
-            const bool mma_cs = SH::MMA_CS && t0 == 0 && !rst && p.k == KMAX;
+            const bool mma_cs = SH::MMA_CS && t0 == 0 && !rst && KK == KMAX;
             auto g16_put = [&](int m, float g) {
                 const __half h0 = __float2half_rn(g);
                 const float r1 = (g - __half2float(h0)) * 2048.f;
@@ -339,7 +342,7 @@ kda_verify_kernel(const __grid_constant__ CUtensorMap tmap, const StepParams p) 
 #pragma unroll
             for (int j = 0; j < TC; ++j) {
                 cdec *= at[j];  // c_j: alpha of tokens 0 .. j
-                if (j < tc && tid < p.k)
+                if (j < tc && tid < KK)
                     reinterpret_cast<float4*>(gts + j * SH::G_TOK)[tid] = make_float4(cdec * kt[j], cdec * qt[j], at[j], kt[j]);
                 if constexpr (SH::MMA_CS) {
                     if (mma_cs) {  // past tc the raw k and q are zero, so are these rows
@@ -374,7 +377,7 @@ kda_verify_kernel(const __grid_constant__ CUtensorMap tmap, const StepParams p) 
 #pragma unroll
             for (int rr = 0; rr < ROWS; ++rr) {
                 const int row = lane + 32 * rr;
-                if (!rst && row < p.k) SV::widen(lds128(tile_base + swz<SH::ROWBYTES>(row, chunk)), x[rr]);
+                if (!rst && row < KK) SV::widen(lds128(tile_base + swz<SH::ROWBYTES>(row, chunk)), x[rr]);
                 else
 #pragma unroll
                     for (int c = 0; c < VEC; ++c) x[rr][c] = 0.f;
@@ -428,7 +431,7 @@ kda_verify_kernel(const __grid_constant__ CUtensorMap tmap, const StepParams p) 
         // parts' fp32 sums at their scales (rows and columns of the products:
         // lane l holds rows l / 4 and l / 4 + 8, columns 2 (l % 4) and + 1)
         if constexpr (SH::MMA_CS) {
-            if (t0 == 0 && !rst && p.k == KMAX) {
+            if (t0 == 0 && !rst && KK == KMAX) {
                 float acc[3][4] = {};
                 const uint32_t gb16 = smem_u32(g16) + ((lane & 15) * SH::G16_STRIDE + (lane >> 4) * 8) * 2;
 #pragma unroll
@@ -455,7 +458,7 @@ kda_verify_kernel(const __grid_constant__ CUtensorMap tmap, const StepParams p) 
         // Otherwise on the CUDA cores from the fp32 carry, G tokens (32 values
         // per lane) at a time; the groups run as a loop (fewer instructions to
         // fetch)
-        const bool fma_cs = !(SH::MMA_CS && t0 == 0 && !rst && p.k == KMAX);
+        const bool fma_cs = !(SH::MMA_CS && t0 == 0 && !rst && KK == KMAX);
 #pragma unroll 1
         for (int g0 = 0; fma_cs && g0 < TC; g0 += G) {
             if (g0 < tc) {
@@ -469,7 +472,7 @@ kda_verify_kernel(const __grid_constant__ CUtensorMap tmap, const StepParams p) 
 #pragma unroll
                         for (int rr = 0; rr < ROWS; ++rr) {
                             const int row = lane + 32 * rr;
-                            if (row < p.k) {
+                            if (row < KK) {
                                 const uint4 gq = lds128(gb + row * 16);
                                 const float w = __uint_as_float(gq.x), z = __uint_as_float(gq.y);
 #pragma unroll
@@ -537,7 +540,7 @@ kda_verify_kernel(const __grid_constant__ CUtensorMap tmap, const StepParams p) 
 #pragma unroll
             for (int rr = 0; rr < ROWS; ++rr) {
                 const int row = lane + 32 * rr;
-                if (row < p.k) {
+                if (row < KK) {
                     const uint4 gq = lds128(gb + row * 16);
                     const float al = __uint_as_float(gq.z), bkr = __uint_as_float(gq.w);
 #pragma unroll
@@ -558,7 +561,7 @@ kda_verify_kernel(const __grid_constant__ CUtensorMap tmap, const StepParams p) 
 #pragma unroll
             for (int rr = 0; rr < ROWS; ++rr) {
                 const int row = lane + 32 * rr;
-                if (row < p.k) {
+                if (row < KK) {
                     const uint4 gq = lds128(gb + row * 16);
                     const float al = __uint_as_float(gq.z), bkr = __uint_as_float(gq.w);
 #pragma unroll
@@ -569,7 +572,7 @@ kda_verify_kernel(const __grid_constant__ CUtensorMap tmap, const StepParams p) 
             fence_proxy_async_smem();
             __syncthreads();
             if (tid == 0 && snaps[j] >= 0) {  // a negative slot: this snapshot is not kept
-                tma_store_3d(&tmap, smem + b * SH::TILE_BYTES, cb * BV, h * p.k, snaps[j]);
+                tma_store_3d(&tmap, smem + b * SH::TILE_BYTES, cb * BV, h * KK, snaps[j]);
                 bulk_commit();
                 // the store of token t - 1 may still read its buffer; the one
                 // token t + 1 rewrites is free
@@ -585,12 +588,12 @@ kda_verify_kernel(const __grid_constant__ CUtensorMap tmap, const StepParams p) 
 #pragma unroll
         for (int rr = 0; rr < ROWS; ++rr) {
             const int row = lane + 32 * rr;
-            if (row < p.k) sts128(tile_base + swz<SH::ROWBYTES>(row, chunk), SV::narrow(x[rr]));
+            if (row < KK) sts128(tile_base + swz<SH::ROWBYTES>(row, chunk), SV::narrow(x[rr]));
         }
         fence_proxy_async_smem();
         __syncthreads();
         if (tid == 0) {
-            tma_store_3d(&tmap, smem, cb * BV, h * p.k, fin);
+            tma_store_3d(&tmap, smem, cb * BV, h * KK, fin);
             bulk_commit();
         }
     }
@@ -602,5 +605,6 @@ kda_verify_kernel(const __grid_constant__ CUtensorMap tmap, const StepParams p) 
         }
     }
 }
+#undef KK
 
 }  // namespace kda
