@@ -464,7 +464,8 @@ def main():
     peak, peak_kind, _ = peaks()
     if args.case is not None:
         if args.case == "verify_f16":
-            res = {"verify_f16": bench_verify(kda, workloads, torch, args, l2, peak)}
+            res = {"verify_f16": bench_verify(kda, workloads, torch, args, l2, peak),
+                   "step_spec_n32_t8_fp16": bench_step(kda, workloads, torch, l2, peak)}
         elif args.case == "aux":
             res = {"ckpt_flush_fp32_n64": bench_ckpt(kda, workloads, torch, peak),
                    "ckpt_load_fp32_n64": bench_ckpt(kda, workloads, torch, peak, load=True),
@@ -510,6 +511,7 @@ def main():
             "bytes_per_step": h16["bytes"], "pools": h16["pools"]}
         extra["verify"] = bench_verify(kda, workloads, torch, args, l2, peak)
         extra["verify_fp32_pool"] = bench_verify(kda, workloads, torch, args, l2, peak, torch.float32)
+        extra["step_spec_n32_t8_fp16"] = bench_step(kda, workloads, torch, l2, peak)
         for sd_name, sd in (("fp32", torch.float32), ("fp16", torch.float16)):
             extra[f"sweep_69_layers_n128_{sd_name}"] = bench_sweep(kda, workloads, torch, sd, 128, peak)
         extra["ckpt_flush_fp32_n64"] = bench_ckpt(kda, workloads, torch, peak)
@@ -742,6 +744,50 @@ def bench_conv(kda, workloads, torch, peak, replays=480):
     return {"workload": "conv window step, N=64 x T=5, C=4608, KW=4, bf16 window of 7 entries",
             "us_per_call": round(us, 3), "gbs": round(byt / (us * 1e-6) / 1e9, 1),
             "frac_of_peak": round(byt / (us * 1e-6) / 1e9 / peak, 4), "bytes_per_call": byt,
+            "launch": f"CUDA graph of {R} launches, replayed; flags KDA_LAUNCH_PDL|KDA_LAUNCH_PDL_EARLY_STATE"}
+
+
+def bench_step(kda, workloads, torch, l2, peak, n=32, t=8, replays=400):
+    """The general step at serving scale: N=32 requests x T=8 tokens (one
+    accepted + seven drafts) on an fp16 pool, the initial state at each
+    request's accepted column of an [N][8] slot table, every token's state
+    stored to its column, the learned gate scale, bf16 q/k/v.  Pools rotate
+    past L2; programmatic dependent launch with early state reads."""
+    lib = kda.KdaLibrary(torch.float16)
+    inp = workloads.make_general(n=n, t=t, num_cols=t, h_qk=HV, state_dtype=torch.float16,
+                                 qkv_dtype=torch.bfloat16, num_slots=n * t, seed=10, gate_scale=True)
+    per = n * (1 + t) * HV * K * V * 2
+    R = max(2, math.ceil(4 * l2 / per) + 1)
+    base = inp.pool.to("cuda")
+    pools = [base] + [base.clone() for _ in range(R - 1)]
+    d = inp.to("cuda")
+    total = n * t
+    o = torch.empty(total, HV, V, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    stream = torch.cuda.Stream()
+    flags = kda.KDA_LAUNCH_PDL | kda.KDA_LAUNCH_PDL_EARLY_STATE
+
+    def call(pool, fl):
+        lib.kda_step(pool, d.slot_table, d.q, d.k, d.v, d.a, d.b, o, status, cu_seqlens=d.cu_seqlens, max_t=t,
+                     accepted=d.accepted, a_log=d.a_log, dt_bias=d.dt_bias, flags=fl)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        call(pools[0], 0)
+        stream.synchronize()
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(R):
+                call(pools[i], flags)
+        for _ in range(3):
+            g.replay()
+    reps = max(1, replays // R)
+    us = timed_replays(g, stream, reps) * 1e3 / (reps * R)
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item())}")
+    byt = n * HV * K * V * 2 * (1 + t) + total * (HV * (2 * K + V) * 2 + HV * K * 4 + HV * 4 + HV * V * 4)
+    return {"workload": f"general step (kda_step), N={n} x T={t} (1 accepted + {t - 1} drafts), fp16 pool, "
+                        "accepted columns of an [N][8] slot table, learned gate scale, bf16 q/k/v",
+            "us_per_step": round(us, 3), "gbs": round(byt / (us * 1e-6) / 1e9, 1),
+            "frac_of_peak": round(byt / (us * 1e-6) / 1e9 / peak, 4), "bytes_per_step": byt, "pools": R,
             "launch": f"CUDA graph of {R} launches, replayed; flags KDA_LAUNCH_PDL|KDA_LAUNCH_PDL_EARLY_STATE"}
 
 
