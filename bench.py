@@ -469,7 +469,8 @@ def main():
         elif args.case == "aux":
             res = {"ckpt_flush_fp32_n64": bench_ckpt(kda, workloads, torch, peak),
                    "ckpt_load_fp32_n64": bench_ckpt(kda, workloads, torch, peak, load=True),
-                   "conv_step_n64_t5_bf16": bench_conv(kda, workloads, torch, peak)}
+                   "conv_step_n64_t5_bf16": bench_conv(kda, workloads, torch, peak),
+                   "copy_floor": bench_copy_floor(kda, torch, l2, peak)}
         elif args.case == "prefill":
             res = {f"prefill_{n}x{t}_fp16{'_chunked' if c else ''}": bench_prefill(kda, workloads, torch, n, t, c)
                    for c in (False, True) for n, t in ((1, 8192), (8, 1024), (64, 128))}
@@ -517,6 +518,7 @@ def main():
         extra["ckpt_flush_fp32_n64"] = bench_ckpt(kda, workloads, torch, peak)
         extra["ckpt_load_fp32_n64"] = bench_ckpt(kda, workloads, torch, peak, load=True)
         extra["conv_step_n64_t5_bf16"] = bench_conv(kda, workloads, torch, peak)
+        extra["copy_floor"] = bench_copy_floor(kda, torch, l2, peak)
         extra["prefill_8x1024_fp16"] = bench_prefill(kda, workloads, torch, 8, 1024)
         extra["prefill_8x1024_fp16_chunked"] = bench_prefill(kda, workloads, torch, 8, 1024, True)
 
@@ -697,6 +699,49 @@ def bench_ckpt(kda, workloads, torch, peak, replays=200, load=False):
     return {"workload": what, "launch": f"CUDA graph of {R} launches, replayed; flags KDA_LAUNCH_PDL",
             "us_per_call": round(us, 3), "gbs": round(byt / (us * 1e-6) / 1e9, 1),
             "frac_of_peak": round(byt / (us * 1e-6) / 1e9 / peak, 4), "bytes_per_call": byt}
+
+
+def bench_copy_floor(kda, torch, l2, peak, states=(8, 19, 33, 64), replays=400):
+    """What a pure copy reaches at the byte counts of the paths above, launched
+    the same way (a CUDA graph of launches over rotating buffers, programmatic
+    dependent launch): the checkpoint flush of n fp32 states [12,128,128],
+    16-byte streaming loads and stores and no arithmetic, moves 2 n 786,432 B.
+    n = 8 is about the conv window step's bytes, 19 exactly the verify step's
+    (29,884,416 B), 33 about the fp16-pool decode's, 64 the fp32-pool
+    decode's.  A kernel launched this way pays a fixed cost per launch (the
+    ramp to full bandwidth and the drain), which this line measures."""
+    lib = kda.KdaLibrary(torch.float32)
+    st_b = HV * K * V * 4
+    out = {}
+    for n in states:
+        byt = 2 * n * st_b
+        R = max(8, math.ceil(4 * l2 / byt) + 1)
+        gen = torch.Generator(device="cuda").manual_seed(11)
+        pools = [torch.randn(n, HV, K, V, device="cuda", generator=gen) for _ in range(R)]
+        planes = [torch.empty(n, HV, K, V, device="cuda") for _ in range(R)]
+        ids = torch.arange(n, dtype=torch.int32, device="cuda")
+        status = torch.zeros(1, dtype=torch.int32, device="cuda")
+        stream = torch.cuda.Stream()
+        g_ = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            lib.kda_ckpt_flush(pools[0], planes[0], ids, ids, status)
+            stream.synchronize()
+            with torch.cuda.graph(g_, stream=stream):
+                for i in range(R):
+                    lib.kda_ckpt_flush(pools[i], planes[i], ids, ids, status, flags=kda.KDA_LAUNCH_PDL)
+            for _ in range(3):
+                g_.replay()
+        reps = max(2, replays // R)
+        us = timed_replays(g_, stream, reps) * 1e3 / (reps * R)
+        if int(status.item()) != 0:
+            raise RuntimeError(f"device status {int(status.item())}")
+        out[f"bytes_{byt}"] = {"us_per_call": round(us, 3), "gbs": round(byt / (us * 1e-6) / 1e9, 1),
+                               "frac_of_peak": round(byt / (us * 1e-6) / 1e9 / peak, 4)}
+        del pools, planes
+        torch.cuda.empty_cache()
+    out["what"] = ("checkpoint flush of n fp32 states (a pure copy), n in " + str(list(states)) +
+                   "; CUDA graph of launches over rotating buffers past L2, flags KDA_LAUNCH_PDL")
+    return out
 
 
 def bench_conv(kda, workloads, torch, peak, replays=480):

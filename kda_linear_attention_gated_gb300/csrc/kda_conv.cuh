@@ -55,6 +55,15 @@ __device__ __forceinline__ void conv_round(float v, float& e) { e = v; }
 __device__ __forceinline__ void conv_round(float v, __half& e) { e = __float2half_rn(v); }
 __device__ __forceinline__ void conv_round(float v, __nv_bfloat16& e) { e = __float2bfloat16_rn(v); }
 
+// SiLU, s sigmoid(s) = s / (1 + e^-s), with the fast exponential and division
+// intrinsics: a few instructions in place of the full-precision forms, which
+// made the token loop instruction-bound.  The error is relative to y, about
+// 1e-6 at the layer's pre-activation range (the exponential's documented bound
+// is 2 + floor(1.173 |x|) ulp, the division's 2 ulp), far below a 16-bit
+// output's step and below the fp32 sum's own error near y = 0.  For s below
+// about -87 the divisor passes 2^126 and the quotient is -0, the limit of y.
+__device__ __forceinline__ float silu_fast(float s) { return __fdividef(s, 1.0f + __expf(-s)); }
+
 // VC consecutive channels of one window entry or token row as one access.
 template <int BYTES> struct ConvRaw;
 template <> struct ConvRaw<2> { using T = unsigned short; };
@@ -162,17 +171,47 @@ __global__ void __launch_bounds__(CT) kda_conv_kernel(const ConvParams p) {
     for (int i = 0; i < KWM; ++i) hr[i] = IO::ld(W + (int64_t)min(acc + i, p.L - 1) * p.C);
 #pragma unroll
     for (int u = 0; u < CB; ++u) kv[u] = IO::ld(W + (int64_t)min(m - kept + u, p.L - 1) * p.C);
-    // w[i] weighs history entry i (i < KW - 1); wlast weighs the current input
+    // w[i] weighs history entry i (i < KW - 1); wlast weighs the current input.
+    // A channel's KW = 4 weights are one 16-byte row, and four channels' biases
+    // one 16-byte vector, read as such where the arrays are 16-byte aligned.
     float w[KWM][VC], z[KWM][VC], wlast[VC], bias[VC];
+    bool w_rows = false, b_vec = false;
+    if constexpr (VC == 4 && KWF == 4) w_rows = (reinterpret_cast<uintptr_t>(p.w) & 15u) == 0;
+    if constexpr (VC == 4) b_vec = p.bias != nullptr && (reinterpret_cast<uintptr_t>(p.bias) & 15u) == 0;
+    if constexpr (VC == 4 && KWF == 4) {
+        if (w_rows) {
 #pragma unroll
-    for (int i = 0; i < KWM; ++i)
+            for (int v = 0; v < VC; ++v) {
+                const float4 wr = __ldg(reinterpret_cast<const float4*>(p.w + (int64_t)(c + v) * 4));
+                w[0][v] = wr.x;
+                w[1][v] = wr.y;
+                w[2][v] = wr.z;
+                wlast[v] = wr.w;
 #pragma unroll
-        for (int v = 0; v < VC; ++v) w[i][v] = i < nh ? __ldg(p.w + (int64_t)(c + v) * KWR + i) : 0.f;
-#pragma unroll
-    for (int v = 0; v < VC; ++v) {
-        wlast[v] = __ldg(p.w + (int64_t)(c + v) * KWR + KWR - 1);
-        bias[v] = p.bias != nullptr ? __ldg(p.bias + c + v) : 0.f;
+                for (int i = 3; i < KWM; ++i) w[i][v] = 0.f;
+            }
+        }
     }
+    if (!w_rows) {
+#pragma unroll
+        for (int i = 0; i < KWM; ++i)
+#pragma unroll
+            for (int v = 0; v < VC; ++v) w[i][v] = i < nh ? __ldg(p.w + (int64_t)(c + v) * KWR + i) : 0.f;
+#pragma unroll
+        for (int v = 0; v < VC; ++v) wlast[v] = __ldg(p.w + (int64_t)(c + v) * KWR + KWR - 1);
+    }
+    if constexpr (VC == 4) {
+        if (b_vec) {
+            const float4 bv = __ldg(reinterpret_cast<const float4*>(p.bias + c));
+            bias[0] = bv.x;
+            bias[1] = bv.y;
+            bias[2] = bv.z;
+            bias[3] = bv.w;
+        }
+    }
+    if (!b_vec)
+#pragma unroll
+        for (int v = 0; v < VC; ++v) bias[v] = p.bias != nullptr ? __ldg(p.bias + c + v) : 0.f;
     if (early) {
         cudaGridDependencySynchronize();
         load_x0();
@@ -219,7 +258,7 @@ __global__ void __launch_bounds__(CT) kda_conv_kernel(const ConvParams p) {
 #pragma unroll
                     for (int i = 0; i < KWM; ++i) s = fmaf(w[i][v], z[i][v], s);  // w is 0 past KW - 2
                     s = fmaf(wlast[v], xv[v], s);
-                    out[v] = p.silu ? s * sigmoid_neg(-s) : s;  // SiLU: s sigmoid(s)
+                    out[v] = p.silu ? silu_fast(s) : s;
                     // slide the history by one: z_i <- z_(i+1), the last history entry <- x_t
 #pragma unroll
                     for (int i = 0; i < KWM; ++i)

@@ -36,11 +36,13 @@ def offset_copy(t):
     return v
 
 
-def gpu_conv(inp, silu=True, flags=0, offset=False):
+def gpu_conv(inp, silu=True, flags=0, offset=False, offset_wb=False):
     d = inp.to("cuda")
     y = torch.full_like(d.x, float("nan"))
     if offset:  # rules out 4-channel accesses
         d.window, d.x, y = offset_copy(d.window), offset_copy(d.x), offset_copy(y)
+    if offset_wb:  # rules out 16-byte weight rows and bias vectors
+        d.weight, d.bias = offset_copy(d.weight), offset_copy(d.bias)
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
     lib_for(torch.float32).kda_conv_step(d.window, d.conv_slot, d.x, d.weight, y, status, bias=d.bias,
                                          cu_seqlens=d.cu_seqlens, max_t=inp.max_t, accepted=d.accepted,
@@ -59,8 +61,10 @@ def oracle_conv(inp, silu=True):
     return W, y
 
 
-def compare(inp, silu=True, flags=0, offset=False):
-    gw, gy, st = gpu_conv(inp, silu, flags, offset)
+def compare(inp, silu=True, flags=0, offset=False, offset_wb=False, scale=1.0):
+    """scale: the inputs' magnitude against the generator's unit scale; the
+    fp32 sum's error grows with it, so both absolute bars are multiplied by it."""
+    gw, gy, st = gpu_conv(inp, silu, flags, offset, offset_wb)
     rw, ry = oracle_conv(inp, silu)
     assert st == 0, lib_for(torch.float32).kda_strerror(st)
     gws, _ = storage(gw)
@@ -68,21 +72,21 @@ def compare(inp, silu=True, flags=0, offset=False):
     gys, _ = storage(gy)
     if inp.x.dtype == torch.float32:
         assert np.isfinite(gys).all()
-        assert np.abs(gys.astype(np.float64) - ry.astype(np.float64)).max() <= 1e-5
+        assert np.abs(gys.astype(np.float64) - ry.astype(np.float64)).max() <= 1e-5 * scale
     else:
-        assert_y16_match(gys, ry, inp.x.dtype)
+        assert_y16_match(gys, ry, inp.x.dtype, CONV_Y_ABS * scale)
 
 
 def y16_values(bits, dtype):
     return torch.from_numpy(bits.astype(np.uint16).view(np.int16)).view(dtype).double().numpy()
 
 
-def assert_y16_match(gys, ry, dtype):
+def assert_y16_match(gys, ry, dtype, abs_floor=CONV_Y_ABS):
     """fp16 / bf16 y: within one step of the oracle's value, or within
     CONV_Y_ABS of it (the fp32 sum's error, which is many steps near zero)."""
     steps = np.abs(gys.astype(np.int32) - ry.astype(np.int32))
     diff = np.abs(y16_values(gys, dtype) - y16_values(ry, dtype))
-    bad = (steps > 1) & (diff > CONV_Y_ABS)
+    bad = (steps > 1) & (diff > abs_floor)
     assert not bad.any(), f"y off by {steps[bad].max()} steps, {diff[bad].max():.3e} absolute"
 
 
@@ -133,6 +137,28 @@ def test_conv_one_channel_per_thread_path(dtype):
     take the one-channel path, with the same results."""
     compare(workloads.make_conv(n=5, t=5, channels=301, dtype=dtype, seed=65, reset_p=0.2))
     compare(workloads.make_conv(n=4, t=5, channels=256, dtype=dtype, seed=66, reset_p=0.2), offset=True)
+
+
+@pytest.mark.parametrize("flags", [0, EARLY])
+@pytest.mark.parametrize("dtype", DT)
+def test_conv_unaligned_weights_and_bias(dtype, flags):
+    """Weights and bias one element past a 16-byte boundary, everything else
+    aligned: the 4-channel, kernel-width-4 path reads them element by element,
+    with the same results."""
+    compare(workloads.make_conv(n=6, t=5, dtype=dtype, seed=67, reset_p=0.2), flags=flags, offset_wb=True)
+
+
+@pytest.mark.parametrize("dtype", DT)
+def test_conv_silu_saturates(dtype):
+    """Inputs and window scaled by 64 (exact in every dtype here) put the
+    pre-activations at hundreds in both directions: SiLU's limits, y = s for
+    large s and y = -0 or a vanishing negative for very negative s.  Every
+    term of the fp32 sum is 64 times larger, so its error is, and the
+    absolute bars are scaled to match (one fp32 ulp at 256 is already 3e-5)."""
+    inp = workloads.make_conv(n=6, t=5, dtype=dtype, seed=68, reset_p=0.2)
+    inp.x = inp.x * 64
+    inp.window = inp.window * 64
+    compare(inp, scale=64.0)
 
 
 @pytest.mark.parametrize("kw", [1, 2, 3, 4, 8])
