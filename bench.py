@@ -514,7 +514,8 @@ def main():
         extra["verify_fp32_pool"] = bench_verify(kda, workloads, torch, args, l2, peak, torch.float32)
         extra["step_spec_n32_t8_fp16"] = bench_step(kda, workloads, torch, l2, peak)
         for sd_name, sd in (("fp32", torch.float32), ("fp16", torch.float16)):
-            extra[f"sweep_69_layers_n128_{sd_name}"] = bench_sweep(kda, workloads, torch, sd, 128, peak)
+            for n_sweep in (1, 16, 64, 128):
+                extra[f"sweep_69_layers_n{n_sweep}_{sd_name}"] = bench_sweep(kda, workloads, torch, sd, n_sweep, peak)
         extra["ckpt_flush_fp32_n64"] = bench_ckpt(kda, workloads, torch, peak)
         extra["ckpt_load_fp32_n64"] = bench_ckpt(kda, workloads, torch, peak, load=True)
         extra["conv_step_n64_t5_bf16"] = bench_conv(kda, workloads, torch, peak)

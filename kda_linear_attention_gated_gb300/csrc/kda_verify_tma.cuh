@@ -82,11 +82,13 @@ struct VerifyShape {
     static constexpr uint32_t RED_D = RED_RES + TC * 2 * BV * 4, RED_SNAP = RED_D + TC * BV * 4;
     static constexpr uint32_t RED_BYTES = (RED_SNAP + TC * 4 + 15u) & ~15u;
     // tensor-core column sums (fp16 pool, first chunk, K = KMAX): the gates of
-    // the 2 TC token-kind rows in three fp16 parts, [3][2 TC][G16_STRIDE] halves;
-    // rows of 272 bytes keep the ldmatrix row reads free of bank conflicts
+    // the 2 TC token-kind rows in three fp16 parts, stored key-major,
+    // [3][KMAX][G16_STRIDE] halves: key row i holds its 2 TC values (one
+    // thread's two 16-byte stores per part), and the 48-byte row stride keeps
+    // the transposing ldmatrix reads of 8 rows free of bank conflicts
     static constexpr bool MMA_CS = sizeof(ST) == 2 && 2 * TC == 16 && VEC == 8;
-    static constexpr int G16_STRIDE = KMAX + 8;
-    static constexpr uint32_t G16_ARRAY = 2 * TC * G16_STRIDE * 2;
+    static constexpr int G16_STRIDE = 2 * TC + 8;
+    static constexpr uint32_t G16_ARRAY = KMAX * G16_STRIDE * 2;
     static constexpr uint32_t G16_BYTES = MMA_CS ? 3 * G16_ARRAY : 0;
     static_assert(ROWBYTES == 128 || ROWBYTES == 64, "tile row bytes");
     static_assert(NT >= KMAX, "one thread per key row in the gate phase");
@@ -152,7 +154,7 @@ kda_verify_kernel(const __grid_constant__ CUtensorMap tmap, const StepParams p) 
     float* res = reinterpret_cast<float*>(redb + SH::RED_RES);     // [TC][2][BV]
     float* dsm = reinterpret_cast<float*>(redb + SH::RED_D);       // [TC][BV]
     int32_t* snaps = reinterpret_cast<int32_t*>(redb + SH::RED_SNAP);  // [TC]
-    __half* g16 = reinterpret_cast<__half*>(redb + SH::RED_BYTES);  // [3][2 TC][G16_STRIDE] (fp16 pool)
+    __half* g16 = reinterpret_cast<__half*>(redb + SH::RED_BYTES);  // [3][KMAX][G16_STRIDE] (fp16 pool)
     uint64_t* bar_st = reinterpret_cast<uint64_t*>(redb + SH::RED_BYTES + SH::G16_BYTES);
     const uint32_t tile_base = smem_u32(smem);
     const uint32_t gate_base = smem_u32(gts);
@@ -264,7 +266,10 @@ kda_verify_kernel(const __grid_constant__ CUtensorMap tmap, const StepParams p) 
     }
     __syncthreads();  // barriers initialised
 
-    float x[ROWS][VEC];
+    // the carry as pairs of adjacent columns: each pair's update is one packed
+    // fp32 FMA (two fmaf with their own rounding, the same results)
+    constexpr int VP = VEC / 2;
+    float2 x[ROWS][VP];
     bool state_in = false;
     bool alive = true;
     if (Tn == 0) {  // prefill, empty prompt: the loaded tile (or zeros) goes to the final slot as is
@@ -328,26 +333,38 @@ kda_verify_kernel(const __grid_constant__ CUtensorMap tmap, const StepParams p) 
             // matrix, each value split into three fp16 parts g = h0 + h1 2^-11 +
             // h2 2^-22 (exact differences; the rest is below 2^-33 |g|)
             const bool mma_cs = SH::MMA_CS && t0 == 0 && !rst && KK == KMAX;
-            auto g16_put = [&](int m, float g) {
-                const __half h0 = __float2half_rn(g);
-                const float r1 = (g - __half2float(h0)) * 2048.f;
-                const __half h1 = __float2half_rn(r1);
-                const __half h2 = __float2half_rn((r1 - __half2float(h1)) * 2048.f);
-                __half* row = g16 + m * SH::G16_STRIDE + tid;
-                row[0] = h0;
-                row[2 * TC * SH::G16_STRIDE] = h1;
-                row[4 * TC * SH::G16_STRIDE] = h2;
-            };
+            float2 gpair[TC];  // {c k, c q} of token j: gate-matrix rows 2 j and 2 j + 1
             float cdec = 1.f;
 #pragma unroll
             for (int j = 0; j < TC; ++j) {
                 cdec *= at[j];  // c_j: alpha of tokens 0 .. j
+                gpair[j] = make_float2(cdec * kt[j], cdec * qt[j]);
                 if (j < tc && tid < KK)
-                    reinterpret_cast<float4*>(gts + j * SH::G_TOK)[tid] = make_float4(cdec * kt[j], cdec * qt[j], at[j], kt[j]);
-                if constexpr (SH::MMA_CS) {
-                    if (mma_cs) {  // past tc the raw k and q are zero, so are these rows
-                        g16_put(2 * j, cdec * kt[j]);
-                        g16_put(2 * j + 1, cdec * qt[j]);
+                    reinterpret_cast<float4*>(gts + j * SH::G_TOK)[tid] = make_float4(gpair[j].x, gpair[j].y, at[j], kt[j]);
+            }
+            if constexpr (SH::MMA_CS) {
+                // past tc the raw k and q are zero, so are those rows; thread
+                // tid < KMAX = NT writes key row tid of each part
+                if (mma_cs) {
+                    uint32_t part[3][TC];
+#pragma unroll
+                    for (int j = 0; j < TC; ++j) {
+                        const float2 g = gpair[j];
+                        const __half2 h0 = __float22half2_rn(g);
+                        const float2 f0 = __half22float2(h0);
+                        const float2 r1 = make_float2((g.x - f0.x) * 2048.f, (g.y - f0.y) * 2048.f);
+                        const __half2 h1 = __float22half2_rn(r1);
+                        const float2 f1 = __half22float2(h1);
+                        const __half2 h2 = __float22half2_rn(make_float2((r1.x - f1.x) * 2048.f, (r1.y - f1.y) * 2048.f));
+                        part[0][j] = *reinterpret_cast<const uint32_t*>(&h0);
+                        part[1][j] = *reinterpret_cast<const uint32_t*>(&h1);
+                        part[2][j] = *reinterpret_cast<const uint32_t*>(&h2);
+                    }
+                    const uint32_t row = smem_u32(g16) + tid * SH::G16_STRIDE * 2;
+#pragma unroll
+                    for (int q = 0; q < 3; ++q) {
+                        sts128(row + q * SH::G16_ARRAY, make_uint4(part[q][0], part[q][1], part[q][2], part[q][3]));
+                        sts128(row + q * SH::G16_ARRAY + 16, make_uint4(part[q][4], part[q][5], part[q][6], part[q][7]));
                     }
                 }
             }
@@ -377,10 +394,10 @@ kda_verify_kernel(const __grid_constant__ CUtensorMap tmap, const StepParams p) 
 #pragma unroll
             for (int rr = 0; rr < ROWS; ++rr) {
                 const int row = lane + 32 * rr;
-                if (!rst && row < KK) SV::widen(lds128(tile_base + swz<SH::ROWBYTES>(row, chunk)), x[rr]);
+                if (!rst && row < KK) SV::widen2(lds128(tile_base + swz<SH::ROWBYTES>(row, chunk)), x[rr]);
                 else
 #pragma unroll
-                    for (int c = 0; c < VEC; ++c) x[rr][c] = 0.f;
+                    for (int c = 0; c < VP; ++c) x[rr][c] = make_float2(0.f, 0.f);
             }
             state_in = true;
         }
@@ -433,7 +450,11 @@ kda_verify_kernel(const __grid_constant__ CUtensorMap tmap, const StepParams p) 
         if constexpr (SH::MMA_CS) {
             if (t0 == 0 && !rst && KK == KMAX) {
                 float acc[3][4] = {};
-                const uint32_t gb16 = smem_u32(g16) + ((lane & 15) * SH::G16_STRIDE + (lane >> 4) * 8) * 2;
+                // lane l addresses row r = l % 8 of 8 x 8 block l / 8 of the A
+                // fragment (m 0-7 | 8-15 by l / 8 odd, k 0-7 | 8-15 by l / 16),
+                // stored k-major: key row kb + (l / 16) 8 + r, gate rows from (l / 8 % 2) 8
+                const uint32_t gb16 = smem_u32(g16) +
+                                      (((lane >> 4) * 8 + (lane & 7)) * SH::G16_STRIDE + ((lane >> 3) & 1) * 8) * 2;
 #pragma unroll
                 for (int kb = 0; kb < KMAX; kb += 16) {
                     uint32_t b0, b1;  // rows kb .. kb + 15 of this warp's 8 columns
@@ -441,7 +462,7 @@ kda_verify_kernel(const __grid_constant__ CUtensorMap tmap, const StepParams p) 
 #pragma unroll
                     for (int part = 0; part < 3; ++part) {
                         uint32_t a0, a1, a2, a3;
-                        ldsm_x4(gb16 + part * SH::G16_ARRAY + kb * 2, a0, a1, a2, a3);
+                        ldsm_x4_trans(gb16 + part * SH::G16_ARRAY + kb * SH::G16_STRIDE * 2, a0, a1, a2, a3);
                         mma_16816_f16(acc[part], a0, a1, a2, a3, b0, b1);
                     }
                 }
@@ -462,9 +483,9 @@ kda_verify_kernel(const __grid_constant__ CUtensorMap tmap, const StepParams p) 
 #pragma unroll 1
         for (int g0 = 0; fma_cs && g0 < TC; g0 += G) {
             if (g0 < tc) {
-                float acc[2 * G * VEC];
+                float2 acc2[G * VEC];  // token jj: pairs jj VEC .. (c k), jj VEC + VP .. (c q)
 #pragma unroll
-                for (int i = 0; i < 2 * G * VEC; ++i) acc[i] = 0.f;
+                for (int i = 0; i < G * VEC; ++i) acc2[i] = make_float2(0.f, 0.f);
 #pragma unroll
                 for (int jj = 0; jj < G; ++jj) {
                     if (g0 + jj < tc) {
@@ -475,14 +496,21 @@ kda_verify_kernel(const __grid_constant__ CUtensorMap tmap, const StepParams p) 
                             if (row < KK) {
                                 const uint4 gq = lds128(gb + row * 16);
                                 const float w = __uint_as_float(gq.x), z = __uint_as_float(gq.y);
+                                const float2 w2 = make_float2(w, w), z2 = make_float2(z, z);
 #pragma unroll
-                                for (int c = 0; c < VEC; ++c) {
-                                    acc[jj * 2 * VEC + c] = fmaf(x[rr][c], w, acc[jj * 2 * VEC + c]);
-                                    acc[jj * 2 * VEC + VEC + c] = fmaf(x[rr][c], z, acc[jj * 2 * VEC + VEC + c]);
+                                for (int c = 0; c < VP; ++c) {
+                                    acc2[jj * VEC + c] = __ffma2_rn(x[rr][c], w2, acc2[jj * VEC + c]);
+                                    acc2[jj * VEC + VP + c] = __ffma2_rn(x[rr][c], z2, acc2[jj * VEC + VP + c]);
                                 }
                             }
                         }
                     }
+                }
+                float acc[2 * G * VEC];
+#pragma unroll
+                for (int i = 0; i < G * VEC; ++i) {
+                    acc[2 * i] = acc2[i].x;
+                    acc[2 * i + 1] = acc2[i].y;
                 }
                 const float sum = warp_reduce_scatter<2 * G * VEC>(acc, lane);  // entry `lane`
                 const int jj = lane / (2 * VEC), kind = (lane / VEC) & 1, c = lane % VEC;
@@ -530,11 +558,12 @@ kda_verify_kernel(const __grid_constant__ CUtensorMap tmap, const StepParams p) 
         // staged rounded in a swizzled tile, then stored.  Prefill keeps
         // only the carry: the same update, nothing staged or stored.
         for (int j = 0; final_mode && j < tc; ++j) {
-            float d[VEC];
+            float2 d[VP];
 #pragma unroll
-            for (int c = 0; c < VEC; c += 4) {
-                const float4 d4 = *reinterpret_cast<const float4*>(dsm + j * BV + chunk * VEC + c);
-                d[c] = d4.x; d[c + 1] = d4.y; d[c + 2] = d4.z; d[c + 3] = d4.w;
+            for (int c = 0; c < VP; c += 2) {
+                const float4 d4 = *reinterpret_cast<const float4*>(dsm + j * BV + chunk * VEC + 2 * c);
+                d[c] = make_float2(d4.x, d4.y);
+                d[c + 1] = make_float2(d4.z, d4.w);
             }
             const uint32_t gb = gate_base + j * SH::G_TOK;
 #pragma unroll
@@ -542,18 +571,20 @@ kda_verify_kernel(const __grid_constant__ CUtensorMap tmap, const StepParams p) 
                 const int row = lane + 32 * rr;
                 if (row < KK) {
                     const uint4 gq = lds128(gb + row * 16);
-                    const float al = __uint_as_float(gq.z), bkr = __uint_as_float(gq.w);
+                    const float2 al2 = make_float2(__uint_as_float(gq.z), __uint_as_float(gq.z));
+                    const float2 bk2 = make_float2(__uint_as_float(gq.w), __uint_as_float(gq.w));
 #pragma unroll
-                    for (int c = 0; c < VEC; ++c) x[rr][c] = fmaf(al, x[rr][c], bkr * d[c]);
+                    for (int c = 0; c < VP; ++c) x[rr][c] = __ffma2_rn(al2, x[rr][c], __fmul2_rn(bk2, d[c]));
                 }
             }
         }
         for (int j = 0; !final_mode && j < tc; ++j) {
-            float d[VEC];
+            float2 d[VP];
 #pragma unroll
-            for (int c = 0; c < VEC; c += 4) {
-                const float4 d4 = *reinterpret_cast<const float4*>(dsm + j * BV + chunk * VEC + c);
-                d[c] = d4.x; d[c + 1] = d4.y; d[c + 2] = d4.z; d[c + 3] = d4.w;
+            for (int c = 0; c < VP; c += 2) {
+                const float4 d4 = *reinterpret_cast<const float4*>(dsm + j * BV + chunk * VEC + 2 * c);
+                d[c] = make_float2(d4.x, d4.y);
+                d[c + 1] = make_float2(d4.z, d4.w);
             }
             const uint32_t gb = gate_base + j * SH::G_TOK;
             const int b = (t0 + j) % SH::NSTAGE;
@@ -563,10 +594,11 @@ kda_verify_kernel(const __grid_constant__ CUtensorMap tmap, const StepParams p) 
                 const int row = lane + 32 * rr;
                 if (row < KK) {
                     const uint4 gq = lds128(gb + row * 16);
-                    const float al = __uint_as_float(gq.z), bkr = __uint_as_float(gq.w);
+                    const float2 al2 = make_float2(__uint_as_float(gq.z), __uint_as_float(gq.z));
+                    const float2 bk2 = make_float2(__uint_as_float(gq.w), __uint_as_float(gq.w));
 #pragma unroll
-                    for (int c = 0; c < VEC; ++c) x[rr][c] = fmaf(al, x[rr][c], bkr * d[c]);
-                    sts128(stage + swz<SH::ROWBYTES>(row, chunk), SV::narrow(x[rr]));
+                    for (int c = 0; c < VP; ++c) x[rr][c] = __ffma2_rn(al2, x[rr][c], __fmul2_rn(bk2, d[c]));
+                    sts128(stage + swz<SH::ROWBYTES>(row, chunk), SV::narrow2(x[rr]));
                 }
             }
             fence_proxy_async_smem();
@@ -588,7 +620,7 @@ kda_verify_kernel(const __grid_constant__ CUtensorMap tmap, const StepParams p) 
 #pragma unroll
         for (int rr = 0; rr < ROWS; ++rr) {
             const int row = lane + 32 * rr;
-            if (row < KK) sts128(tile_base + swz<SH::ROWBYTES>(row, chunk), SV::narrow(x[rr]));
+            if (row < KK) sts128(tile_base + swz<SH::ROWBYTES>(row, chunk), SV::narrow2(x[rr]));
         }
         fence_proxy_async_smem();
         __syncthreads();
