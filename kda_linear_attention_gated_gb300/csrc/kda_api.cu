@@ -263,18 +263,16 @@ int launch_decode(const kda_pool* pool, const kda::StepParams& prm, cudaStream_t
                               : launch_decode_k<QT, false>(pool, prm, stream);
 }
 
-template <typename QT>
-int launch_verify(const kda_pool* pool, const kda::StepParams& prm, cudaStream_t stream) {
+template <typename QT, bool WIDE>
+int launch_verify_shape(const kda_pool* pool, const kda::StepParams& prm, cudaStream_t stream, int64_t tiles) {
     constexpr int BV = KDA_VER_BV;
-    using SH = kda::VerifyShape<state_t, BV, (int)sizeof(QT)>;
-    constexpr size_t smem = kda::verify_smem_bytes<state_t, BV, (int)sizeof(QT)>();
+    using SH = kda::VerifyShape<state_t, BV, (int)sizeof(QT), WIDE>;
+    constexpr size_t smem = kda::verify_smem_bytes<state_t, BV, (int)sizeof(QT), WIDE>();
     // an fp16 pool at K = 128 gets the build with compile-time row loops; an
     // fp32 pool's 256-thread tiles have no register room for it (it spills)
     constexpr bool kFullkOk = sizeof(state_t) == 2;
-    auto kernel = (kFullkOk && prm.k == kda::KMAX) ? kda::kda_verify_kernel<state_t, QT, BV, kFullkOk>
-                                                   : kda::kda_verify_kernel<state_t, QT, BV, false>;
-    const int64_t tiles = (int64_t)prm.n * prm.hv * ((prm.v + BV - 1) / BV);
-    if (tiles > 0x7fffffffLL) return KDA_ERR_SHAPE;
+    auto kernel = (kFullkOk && prm.k == kda::KMAX) ? kda::kda_verify_kernel<state_t, QT, BV, kFullkOk, WIDE>
+                                                   : kda::kda_verify_kernel<state_t, QT, BV, false, WIDE>;
     CUtensorMap map;
     int rc = make_pool_map(pool, BV, &map);
     if (rc != KDA_OK) return rc;
@@ -290,6 +288,26 @@ int launch_verify(const kda_pool* pool, const kda::StepParams& prm, cudaStream_t
     set_pdl(cfg, &attr, prm.flags);
     const cudaError_t err = cudaLaunchKernelEx(&cfg, kernel, map, prm);
     return err == cudaSuccess ? KDA_OK : KDA_ERR_LAUNCH;
+}
+
+// A launch that fits in one wave of the default shape runs it; a larger one,
+// on an fp16 pool with 16-bit inputs, runs the wide shape (4 CTAs per SM).
+template <typename QT>
+int launch_verify(const kda_pool* pool, const kda::StepParams& prm, cudaStream_t stream) {
+    constexpr int BV = KDA_VER_BV;
+    const int64_t tiles = (int64_t)prm.n * prm.hv * ((prm.v + BV - 1) / BV);
+    if (tiles > 0x7fffffffLL) return KDA_ERR_SHAPE;
+    constexpr bool kWideOk = sizeof(state_t) == 2 && sizeof(QT) == 2;
+    if constexpr (kWideOk) {
+        using SH = kda::VerifyShape<state_t, BV, (int)sizeof(QT)>;
+        constexpr size_t smem = kda::verify_smem_bytes<state_t, BV, (int)sizeof(QT)>();
+        int occ = 0, sms = 0;
+        const int rc = occupancy(reinterpret_cast<const void*>(kda::kda_verify_kernel<state_t, QT, BV, false>),
+                                 SH::NT, smem, &occ, &sms);
+        if (rc != KDA_OK) return rc;
+        if (tiles > (int64_t)occ * sms) return launch_verify_shape<QT, kWideOk>(pool, prm, stream, tiles);
+    }
+    return launch_verify_shape<QT, false>(pool, prm, stream, tiles);
 }
 
 template <bool VERIFY>

@@ -54,7 +54,11 @@
 
 namespace kda {
 
-template <typename ST, int BV, int QES>
+// WIDE: the shape for launches of more than one wave at 3 CTAs per SM (an
+// fp16 pool with 16-bit inputs): 4 resident CTAs per SM, from a 128-register
+// cap and two staging buffers instead of three.  A one-wave launch runs the
+// default shape, whose extra registers and buffer shorten each CTA.
+template <typename ST, int BV, int QES, bool WIDE = false>
 struct VerifyShape {
     static constexpr int VEC = StateVec<ST>::VEC;
     static constexpr int ROWBYTES = BV * (int)sizeof(ST);
@@ -62,7 +66,7 @@ struct VerifyShape {
     static constexpr int NT = 32 * NW;
     // resident CTAs per SM the register budget must allow: at the configured
     // shapes a launch is about 2.5 CTAs per SM, so 3 keep it in one wave
-    static constexpr int MINB = KDA_VER_MINB;
+    static constexpr int MINB = WIDE ? 4 : KDA_VER_MINB;
     static constexpr int ROWS = KMAX / 32;    // rows per lane
     static constexpr int TC = 8;              // tokens per chunk
     static constexpr int NA = TC * (TC - 1) / 2, NB = TC * (TC + 1) / 2;  // 28 + 36 = 64 sums
@@ -73,7 +77,7 @@ struct VerifyShape {
     static constexpr uint32_t GATE_BYTES = TC * G_TOK;
     static constexpr uint32_t WORK_BYTES = GATE_BYTES;
     // staging buffers for the snapshot stores (the state tile's area is the first)
-    static constexpr int NSTAGE = 3;
+    static constexpr int NSTAGE = WIDE ? 2 : 3;
     // norms [TC][NW][2] and b [TC], scalars [TC] float4, A and B per warp
     // [NW][64] then summed [64], column sums [TC][2][BV], d [TC][BV], snapshot ids [TC]
     static constexpr uint32_t RED_NORM = 0, RED_B = RED_NORM + TC * NW * 8;
@@ -83,13 +87,16 @@ struct VerifyShape {
     static constexpr uint32_t RED_BYTES = (RED_SNAP + TC * 4 + 15u) & ~15u;
     // tensor-core column sums (fp16 pool, first chunk, K = KMAX): the gates of
     // the 2 TC token-kind rows in three fp16 parts, stored key-major,
-    // [3][KMAX][G16_STRIDE] halves: key row i holds its 2 TC values (one
-    // thread's two 16-byte stores per part), and the 48-byte row stride keeps
-    // the transposing ldmatrix reads of 8 rows free of bank conflicts
+    // [3][KMAX][G16_STRIDE] halves: key row i holds its 2 TC values as two
+    // 16-byte halves (gate rows 0-7 and 8-15; one thread's two stores per
+    // part), the halves swapped in rows with bit 2 set (g16_half), so that
+    // the 8 rows a transposing ldmatrix reads, and 8 threads' stores, fall in
+    // distinct banks
     static constexpr bool MMA_CS = sizeof(ST) == 2 && 2 * TC == 16 && VEC == 8;
-    static constexpr int G16_STRIDE = 2 * TC + 8;
+    static constexpr int G16_STRIDE = 2 * TC;
     static constexpr uint32_t G16_ARRAY = KMAX * G16_STRIDE * 2;
     static constexpr uint32_t G16_BYTES = MMA_CS ? 3 * G16_ARRAY : 0;
+    static_assert(G16_STRIDE * 2 == 32, "g16_half: 32-byte key rows");
     static_assert(ROWBYTES == 128 || ROWBYTES == 64, "tile row bytes");
     static_assert(NT >= KMAX, "one thread per key row in the gate phase");
     static_assert(NA + NB == 64 && 2 * G * VEC == 32 && TC % G == 0 && TC == 8, "chunk shape");
@@ -98,14 +105,21 @@ struct VerifyShape {
     // row, written by thread tid for row tid: exactly KMAX threads
     static_assert(!MMA_CS || NT == KMAX, "tensor-core column sums need one thread per key row");
     static_assert(NSTAGE >= 2, "staging buffers");
+    static_assert(!WIDE || (sizeof(ST) == 2 && QES == 2), "the wide shape: fp16 pool, 16-bit inputs");
     static_assert(G_TOK % 16 == 0 &&
                   WORK_BYTES % 16 == 0 && RED_RES % 16 == 0 && RED_D % 16 == 0, "layout");
 };
 
-template <typename ST, int BV, int QES>
+template <typename ST, int BV, int QES, bool WIDE = false>
 constexpr size_t verify_smem_bytes() {
-    using SH = VerifyShape<ST, BV, QES>;
+    using SH = VerifyShape<ST, BV, QES, WIDE>;
     return SH::NSTAGE * SH::TILE_BYTES + SH::WORK_BYTES + SH::RED_BYTES + SH::G16_BYTES + 16;
+}
+
+// Byte offset of 16-byte half h (gate rows 8 h .. 8 h + 7) of key row k in one
+// part of the gate matrix.
+__device__ __forceinline__ uint32_t g16_half(int k, int h) {
+    return (uint32_t)(k * 32 + ((h ^ ((k >> 2) & 1)) << 4));
 }
 
 // Position of A_ts (s < t) and of B_ts (s <= t) among a chunk's 64 row sums.
@@ -134,12 +148,13 @@ __device__ __forceinline__ void ab_terms(float (&out)[32], const float (&bk)[TC]
 }
 
 // FULLK: K = KMAX, known at compile time (the row guards and loops fold away).
-template <typename ST, typename QT, int BV, bool FULLK>
-__global__ void __launch_bounds__(VerifyShape<ST, BV, (int)sizeof(QT)>::NT, VerifyShape<ST, BV, (int)sizeof(QT)>::MINB)
+template <typename ST, typename QT, int BV, bool FULLK, bool WIDE = false>
+__global__ void __launch_bounds__(VerifyShape<ST, BV, (int)sizeof(QT), WIDE>::NT,
+                                  VerifyShape<ST, BV, (int)sizeof(QT), WIDE>::MINB)
 kda_verify_kernel(const __grid_constant__ CUtensorMap tmap, const StepParams p) {
 // key rows: KMAX in the K = KMAX build, else read from the parameters where used
 #define KK (FULLK ? KMAX : p.k)
-    using SH = VerifyShape<ST, BV, (int)sizeof(QT)>;
+    using SH = VerifyShape<ST, BV, (int)sizeof(QT), WIDE>;
     using SV = StateVec<ST>;
     constexpr int VEC = SH::VEC, NW = SH::NW, ROWS = SH::ROWS, TC = SH::TC, G = SH::G;
 
@@ -360,11 +375,11 @@ kda_verify_kernel(const __grid_constant__ CUtensorMap tmap, const StepParams p) 
                         part[1][j] = *reinterpret_cast<const uint32_t*>(&h1);
                         part[2][j] = *reinterpret_cast<const uint32_t*>(&h2);
                     }
-                    const uint32_t row = smem_u32(g16) + tid * SH::G16_STRIDE * 2;
+                    const uint32_t lo = smem_u32(g16) + g16_half(tid, 0), hi = smem_u32(g16) + g16_half(tid, 1);
 #pragma unroll
                     for (int q = 0; q < 3; ++q) {
-                        sts128(row + q * SH::G16_ARRAY, make_uint4(part[q][0], part[q][1], part[q][2], part[q][3]));
-                        sts128(row + q * SH::G16_ARRAY + 16, make_uint4(part[q][4], part[q][5], part[q][6], part[q][7]));
+                        sts128(lo + q * SH::G16_ARRAY, make_uint4(part[q][0], part[q][1], part[q][2], part[q][3]));
+                        sts128(hi + q * SH::G16_ARRAY, make_uint4(part[q][4], part[q][5], part[q][6], part[q][7]));
                     }
                 }
             }
@@ -452,9 +467,10 @@ kda_verify_kernel(const __grid_constant__ CUtensorMap tmap, const StepParams p) 
                 float acc[3][4] = {};
                 // lane l addresses row r = l % 8 of 8 x 8 block l / 8 of the A
                 // fragment (m 0-7 | 8-15 by l / 8 odd, k 0-7 | 8-15 by l / 16),
-                // stored k-major: key row kb + (l / 16) 8 + r, gate rows from (l / 8 % 2) 8
-                const uint32_t gb16 = smem_u32(g16) +
-                                      (((lane >> 4) * 8 + (lane & 7)) * SH::G16_STRIDE + ((lane >> 3) & 1) * 8) * 2;
+                // stored k-major: key row kb + (l / 16) 8 + r, half (l / 8) % 2.
+                // kb is a multiple of 16, so the swap of the halves depends on
+                // r alone and row kb adds kb * 32 bytes
+                const uint32_t gb16 = smem_u32(g16) + g16_half((lane >> 4) * 8 + (lane & 7), (lane >> 3) & 1);
 #pragma unroll
                 for (int kb = 0; kb < KMAX; kb += 16) {
                     uint32_t b0, b1;  // rows kb .. kb + 15 of this warp's 8 columns
@@ -462,7 +478,7 @@ kda_verify_kernel(const __grid_constant__ CUtensorMap tmap, const StepParams p) 
 #pragma unroll
                     for (int part = 0; part < 3; ++part) {
                         uint32_t a0, a1, a2, a3;
-                        ldsm_x4_trans(gb16 + part * SH::G16_ARRAY + kb * SH::G16_STRIDE * 2, a0, a1, a2, a3);
+                        ldsm_x4_trans(gb16 + part * SH::G16_ARRAY + kb * 32, a0, a1, a2, a3);
                         mma_16816_f16(acc[part], a0, a1, a2, a3, b0, b1);
                     }
                 }

@@ -170,3 +170,46 @@ def _without(inp, r):
     acc[r] = 1
     return workloads.GeneralInputs(inp.pool, table, inp.q, inp.k, inp.v, inp.a, inp.b, inp.cu_seqlens, acc,
                                    inp.reset, inp.a_log, inp.dt_bias, inp.in_place, inp.max_t, dict(inp.meta))
+
+
+# Launches of more than one wave of the default verify shape (3 CTAs per SM;
+# 456 CTAs on 152 SMs) run the wide shape on an fp16 pool with 16-bit inputs:
+# 4 CTAs per SM, two staging buffers.  N=32 requests x 12 heads x 4 column
+# tiles is 1536 CTAs.
+
+@pytest.mark.parametrize("qkv_dtype", [torch.bfloat16, torch.float16])
+@pytest.mark.parametrize("flags", [0, kda.KDA_LAUNCH_PDL | kda.KDA_LAUNCH_PDL_EARLY_STATE])
+def test_serving_scale_step_wide_launch(qkv_dtype, flags):
+    """The general step at serving scale, N=32 x 8 tokens on an fp16 pool:
+    accepted columns, learned gate scale, resets and padding."""
+    check(workloads.make_general(n=32, t=8, num_cols=8, hv=12, num_slots=256, state_dtype=torch.float16,
+                                 qkv_dtype=qkv_dtype, seed=52, reset_p=0.1, pad_p=0.05, gate_scale=True),
+          flags)
+
+
+@pytest.mark.parametrize("qkv_dtype", [torch.bfloat16, torch.float16])
+def test_wide_launch_equals_one_wave_launches_bits(qkv_dtype):
+    """Requests are independent, so one launch of 32 requests (the wide shape)
+    must give the same bits as four launches of 8 (the default shape)."""
+    n, t, part = 32, 8, 8
+    inp = workloads.make_verify(n=n, t=t, hv=12, k=128, v=128, num_slots=n * (t + 1), state_dtype=torch.float16,
+                                qkv_dtype=qkv_dtype, seed=53, reset_p=0.2)
+    lib = lib_for(torch.float16)
+    d = inp.to("cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    pool_wide = d.pool.clone()
+    o_wide = torch.empty(n, t, 12, 128, device="cuda")
+    lib.kda_spec_verify(pool_wide, d.init_slot, d.snap_slot, d.q, d.k, d.v, d.a, d.b, o_wide, st, reset=d.reset)
+    pool_parts = d.pool.clone()
+    o_parts = torch.empty(n, t, 12, 128, device="cuda")
+    for r0 in range(0, n, part):
+        sl = slice(r0, r0 + part)
+        o_sl = torch.empty(part, t, 12, 128, device="cuda")
+        lib.kda_spec_verify(pool_parts, d.init_slot[sl].contiguous(), d.snap_slot[sl].contiguous(),
+                            d.q[sl].contiguous(), d.k[sl].contiguous(), d.v[sl].contiguous(),
+                            d.a[sl].contiguous(), d.b[sl].contiguous(), o_sl, st, reset=d.reset[sl].contiguous())
+        o_parts[sl] = o_sl
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    assert torch.equal(pool_wide, pool_parts)
+    assert torch.equal(o_wide, o_parts)
