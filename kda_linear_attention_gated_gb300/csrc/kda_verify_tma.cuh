@@ -11,7 +11,7 @@
 // shared-memory staging tile and from there to that token's snapshot slot
 // snap_slot[n][t] (ROCm/ATOM pull request 2945, Changes: the state after each
 // token goes to the token's snapshot slot through state_at) as one TMA box
-// store, three staging buffers in turn.
+// store, three staging buffers in turn (two in the wide shape).
 //
 // The general step: request n owns tokens cu[n] .. cu[n+1] - 1 of packed
 // inputs (or n T .. n T + T - 1), reads its initial state from column
