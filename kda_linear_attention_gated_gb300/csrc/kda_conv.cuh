@@ -249,14 +249,22 @@ __global__ void __launch_bounds__(CT) kda_conv_kernel(const ConvParams p) {
         }
 #pragma unroll
         for (int u = 0; u < CB; ++u) {
-            if (t0 + u < T) {
+            // past the last token, leave: the history slide below then runs
+            // unconditionally and compiles to register renaming, where a
+            // guard around it would keep every history register live through
+            // selects
+            if (t0 + u >= T) break;
+            {
                 float xv[VC], out[VC];
                 IO::widen(xr[u], xv);
 #pragma unroll
                 for (int v = 0; v < VC; ++v) {
                     float s = bias[v];
 #pragma unroll
-                    for (int i = 0; i < KWM; ++i) s = fmaf(w[i][v], z[i][v], s);  // w is 0 past KW - 2
+                    // w is 0 past KW - 2; with the width fixed at compile time those
+                    // terms (0 times a zero history slot) are left out
+                    for (int i = 0; i < KWM; ++i)
+                        if (KWF == 0 || i < KWF - 1) s = fmaf(w[i][v], z[i][v], s);
                     s = fmaf(wlast[v], xv[v], s);
                     out[v] = p.silu ? silu_fast(s) : s;
                     // slide the history by one: z_i <- z_(i+1), the last history entry <- x_t
