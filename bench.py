@@ -98,6 +98,19 @@ def source_hash(paths=None) -> str:
     return h.hexdigest()[:16]
 
 
+IN_GRAPH_PREFIX = 3  # untimed launches ahead of e0 when the events are recorded inside the graph
+
+
+def in_graph_events(torch):
+    """Two timing events that record as nodes of a captured graph, or None
+    where this torch cannot make them (the caller then times whole replays)."""
+    try:
+        return (torch.cuda.Event(enable_timing=True, external=True),
+                torch.cuda.Event(enable_timing=True, external=True))
+    except TypeError:
+        return None
+
+
 def timed_replays(graph, stream, reps):
     """Milliseconds of `reps` replays of `graph` on `stream`, by CUDA events.
     One untimed replay is queued first, so that the GPU is busy when the start
@@ -350,15 +363,30 @@ def main():
         status = torch.zeros(1, dtype=torch.int32, device="cuda")
         stream = torch.cuda.Stream()
         chunk = chunk_size(steps)
+        # A run that fits in one graph is timed by events recorded inside it
+        # (in_graph_events): PREFIX untimed launches run first, e0 is recorded
+        # on a side stream once the last of them completes, and e1 once the
+        # last timed launch completes.  The window holds exactly the `steps`
+        # launches, each behind its predecessor as in a long stream, and
+        # neither the host's graph launch nor a first launch on an idle GPU.
+        events = in_graph_events(torch) if chunk == steps else None
+        prefix = IN_GRAPH_PREFIX if events else 0
         g = torch.cuda.CUDAGraph()
         with torch.cuda.stream(stream):
             # eager warm-up launch (module load) before capture
             lib.kda_decode_step(pools[0], d.init_slot, d.q, d.k, d.v, d.a, d.b, o, status)
             stream.synchronize()
+            side = torch.cuda.Stream() if events else None
             with torch.cuda.graph(g, stream=stream):
-                for i in range(chunk):
+                for i in range(prefix + chunk):
+                    if events and i == prefix:
+                        side.wait_stream(stream)
+                        events[0].record(side)
                     lib.kda_decode_step(pools[i % R], d.init_slot, d.q, d.k, d.v, d.a, d.b, o, status,
                                         flags=flags)
+                if events:
+                    events[1].record(stream)
+                    stream.wait_stream(side)
         # warm-up: at least `warmup` steps and at least ~1 s of load
         t_w = time.perf_counter()
         done = 0
@@ -376,14 +404,21 @@ def main():
                     g.replay()
         if dist is not None:
             dist.barrier()
-        ms = timed_replays(g, stream, steps // chunk)
+        if events:
+            torch.cuda.synchronize()
+            with torch.cuda.stream(stream):
+                g.replay()
+            torch.cuda.synchronize()
+            ms = events[0].elapsed_time(events[1])
+        else:
+            ms = timed_replays(g, stream, steps // chunk)
         if dist is not None:
             dist.barrier()
         clocks = sampler.stop() if sampler else None
         st = int(status.item())
         if st != 0:
             raise RuntimeError(f"device status {st}: {lib.kda_strerror(st)}")
-        return dict(ms_total=ms, us_per_step=ms * 1e3 / steps, pools=R, chunk=chunk,
+        return dict(ms_total=ms, us_per_step=ms * 1e3 / steps, pools=R, chunk=chunk, prefix=prefix,
                     bytes=algorithmic_bytes(N, HV, K, V, 1, es, 2), clocks=clocks,
                     pool_bytes=R * pools[0].numel() * es)
 
@@ -553,7 +588,11 @@ def main():
                        "l2": f"inputs larger than L2: {head['pools']} rotating pools, "
                              f"{head['pool_bytes'] / 1e9:.2f} GB > 4 x {l2 / 2**20:.0f} MiB L2",
                        "launch": f"CUDA graph of {head['chunk']} launches, replayed; "
-                      "flags KDA_LAUNCH_PDL|KDA_LAUNCH_PDL_EARLY_STATE"},
+                      "flags KDA_LAUNCH_PDL|KDA_LAUNCH_PDL_EARLY_STATE",
+                       "timing": (f"events inside the graph: {head['prefix']} untimed launches, then e0 "
+                                  f"(recorded once the last of them completes), the {head['chunk']} timed "
+                                  "launches, e1 (once the last completes)") if head["prefix"] else
+                                 "events around the timed graph replays, one untimed replay queued ahead"},
             "roofline": {"bound": "hbm", "achieved": round(gbs_per_gpu, 1), "peak": peak,
                          "unit": "GB/s", "frac": round(gbs_per_gpu / peak, 4),
                          "traffic": traffic, "peak_kind": peak_kind,
