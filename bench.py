@@ -129,6 +129,44 @@ def timed_replays(graph, stream, reps):
     return e0.elapsed_time(e1)
 
 
+def graph_timed(torch, stream, launch, n, warm=3):
+    """Milliseconds of n launches, launch(i) for i = IN_GRAPH_PREFIX .. +n-1,
+    timed by events inside one CUDA graph behind IN_GRAPH_PREFIX untimed
+    launches (as for the headline: the window runs from the completion of
+    the launch before the first timed one to the completion of the last).
+    Where the events cannot be made, the graph holds the n launches alone and
+    is timed as a whole replay with one untimed replay queued ahead.  The
+    caller has made one eager launch first (module load)."""
+    events = in_graph_events(torch)
+    prefix = IN_GRAPH_PREFIX if events else 0
+    g = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream() if events else None
+    with torch.cuda.stream(stream):
+        stream.synchronize()
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(prefix + n):
+                if events and i == prefix:
+                    side.wait_stream(stream)
+                    events[0].record(side)
+                launch(i)
+            if events:
+                events[1].record(stream)
+                stream.wait_stream(side)
+        for _ in range(warm):
+            g.replay()
+    if not events:
+        return timed_replays(g, stream, 1)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        g.replay()
+    torch.cuda.synchronize()
+    return events[0].elapsed_time(events[1])
+
+
+GRAPH_TIMED = ("one CUDA graph: 3 untimed launches, then the timed ones between events recorded inside "
+               "the graph")
+
+
 def algorithmic_bytes(n, hv, k, v, t, state_bytes, qkv_bytes, reads=1, writes=1):
     """State read + written plus q, k, v (qkv_bytes each) and fp32 o."""
     state = (reads + writes * t) * n * hv * k * v * state_bytes
@@ -640,6 +678,8 @@ def bench_sweep(kda, workloads, torch, state_dtype, n, peak, layers=69, replays=
                                     reset=d.reset, flags=flags)
         for _ in range(3):
             g.replay()
+    # one replay is one forward pass over the layers, as a model launches it:
+    # whole replays are timed, the boundary between forwards included
     us_fwd = timed_replays(g, stream, replays) * 1e3 / replays
     if int(status.item()) != 0:
         raise RuntimeError(f"device status {int(status.item())}")
@@ -717,18 +757,12 @@ def bench_ckpt(kda, workloads, torch, peak, replays=200, load=False):
     entries = torch.randperm(128, generator=g)[:64].to(torch.int32).to("cuda")
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
     stream = torch.cuda.Stream()
-    g_ = torch.cuda.CUDAGraph()
     call = lib.kda_ckpt_load if load else lib.kda_ckpt_flush
     with torch.cuda.stream(stream):
         call(pools[0], planes[0], slots, entries, status)
-        stream.synchronize()
-        with torch.cuda.graph(g_, stream=stream):
-            for i in range(R):
-                call(pools[i], planes[i], slots, entries, status, flags=kda.KDA_LAUNCH_PDL)
-        for _ in range(3):
-            g_.replay()
-    reps = max(1, replays // R)
-    us = timed_replays(g_, stream, reps) * 1e3 / (reps * R)
+    n_timed = R * max(1, replays // R)
+    us = graph_timed(torch, stream, lambda i: call(pools[i % R], planes[i % R], slots, entries, status,
+                                                   flags=kda.KDA_LAUNCH_PDL), n_timed) * 1e3 / n_timed
     if int(status.item()) != 0:
         raise RuntimeError(f"device status {int(status.item())}")
     byt = 2 * 64 * HV * K * V * 4
@@ -736,7 +770,8 @@ def bench_ckpt(kda, workloads, torch, peak, replays=200, load=False):
     torch.cuda.empty_cache()
     what = ("checkpoint load, 64 fp32 states [12,128,128], 128-entry plane -> 256-slot pool" if load else
             "checkpoint flush, 64 fp32 states [12,128,128], 256-slot pool -> 128-entry plane")
-    return {"workload": what, "launch": f"CUDA graph of {R} launches, replayed; flags KDA_LAUNCH_PDL",
+    return {"workload": what, "launch": f"{GRAPH_TIMED} ({n_timed}, over {R} pool/plane pairs); "
+                                        "flags KDA_LAUNCH_PDL",
             "us_per_call": round(us, 3), "gbs": round(byt / (us * 1e-6) / 1e9, 1),
             "frac_of_peak": round(byt / (us * 1e-6) / 1e9 / peak, 4), "bytes_per_call": byt}
 
@@ -762,17 +797,12 @@ def bench_copy_floor(kda, torch, l2, peak, states=(8, 19, 33, 64), replays=400):
         ids = torch.arange(n, dtype=torch.int32, device="cuda")
         status = torch.zeros(1, dtype=torch.int32, device="cuda")
         stream = torch.cuda.Stream()
-        g_ = torch.cuda.CUDAGraph()
         with torch.cuda.stream(stream):
             lib.kda_ckpt_flush(pools[0], planes[0], ids, ids, status)
-            stream.synchronize()
-            with torch.cuda.graph(g_, stream=stream):
-                for i in range(R):
-                    lib.kda_ckpt_flush(pools[i], planes[i], ids, ids, status, flags=kda.KDA_LAUNCH_PDL)
-            for _ in range(3):
-                g_.replay()
-        reps = max(2, replays // R)
-        us = timed_replays(g_, stream, reps) * 1e3 / (reps * R)
+        n_timed = R * max(2, replays // R)
+        us = graph_timed(torch, stream, lambda i: lib.kda_ckpt_flush(pools[i % R], planes[i % R], ids, ids, status,
+                                                                     flags=kda.KDA_LAUNCH_PDL),
+                         n_timed) * 1e3 / n_timed
         if int(status.item()) != 0:
             raise RuntimeError(f"device status {int(status.item())}")
         out[f"bytes_{byt}"] = {"us_per_call": round(us, 3), "gbs": round(byt / (us * 1e-6) / 1e9, 1),
@@ -780,7 +810,7 @@ def bench_copy_floor(kda, torch, l2, peak, states=(8, 19, 33, 64), replays=400):
         del pools, planes
         torch.cuda.empty_cache()
     out["what"] = ("checkpoint flush of n fp32 states (a pure copy), n in " + str(list(states)) +
-                   "; CUDA graph of launches over rotating buffers past L2, flags KDA_LAUNCH_PDL")
+                   f"; {GRAPH_TIMED}, over rotating buffers past L2, flags KDA_LAUNCH_PDL")
     return out
 
 
@@ -803,7 +833,6 @@ def bench_conv(kda, workloads, torch, peak, replays=480):
     ys = [torch.empty_like(d.x) for d in sets]
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
     stream = torch.cuda.Stream()
-    g_ = torch.cuda.CUDAGraph()
 
     def call(i):
         d = sets[i]
@@ -812,14 +841,8 @@ def bench_conv(kda, workloads, torch, peak, replays=480):
                           flags=kda.KDA_LAUNCH_PDL | kda.KDA_LAUNCH_PDL_EARLY_STATE)
     with torch.cuda.stream(stream):
         call(0)
-        stream.synchronize()
-        with torch.cuda.graph(g_, stream=stream):
-            for i in range(R):
-                call(i)
-        for _ in range(3):
-            g_.replay()
-    reps = max(1, replays // R)
-    us = timed_replays(g_, stream, reps) * 1e3 / (reps * R)
+    n_timed = R * max(1, replays // R)
+    us = graph_timed(torch, stream, lambda i: call(i % R), n_timed) * 1e3 / n_timed
     if int(status.item()) != 0:
         raise RuntimeError(f"device status {int(status.item())}")
     L = kw - 1 + spec
@@ -829,7 +852,7 @@ def bench_conv(kda, workloads, torch, peak, replays=480):
     return {"workload": "conv window step, N=64 x T=5, C=4608, KW=4, bf16 window of 7 entries",
             "us_per_call": round(us, 3), "gbs": round(byt / (us * 1e-6) / 1e9, 1),
             "frac_of_peak": round(byt / (us * 1e-6) / 1e9 / peak, 4), "bytes_per_call": byt,
-            "launch": f"CUDA graph of {R} launches, replayed; flags KDA_LAUNCH_PDL|KDA_LAUNCH_PDL_EARLY_STATE"}
+            "launch": f"{GRAPH_TIMED} ({n_timed}, over {R} sets); flags KDA_LAUNCH_PDL|KDA_LAUNCH_PDL_EARLY_STATE"}
 
 
 def bench_step(kda, workloads, torch, l2, peak, n=32, t=8, replays=400):
@@ -855,17 +878,10 @@ def bench_step(kda, workloads, torch, l2, peak, n=32, t=8, replays=400):
     def call(pool, fl):
         lib.kda_step(pool, d.slot_table, d.q, d.k, d.v, d.a, d.b, o, status, cu_seqlens=d.cu_seqlens, max_t=t,
                      accepted=d.accepted, a_log=d.a_log, dt_bias=d.dt_bias, flags=fl)
-    g = torch.cuda.CUDAGraph()
     with torch.cuda.stream(stream):
         call(pools[0], 0)
-        stream.synchronize()
-        with torch.cuda.graph(g, stream=stream):
-            for i in range(R):
-                call(pools[i], flags)
-        for _ in range(3):
-            g.replay()
-    reps = max(1, replays // R)
-    us = timed_replays(g, stream, reps) * 1e3 / (reps * R)
+    n_timed = R * max(1, replays // R)
+    us = graph_timed(torch, stream, lambda i: call(pools[i % R], flags), n_timed) * 1e3 / n_timed
     if int(status.item()) != 0:
         raise RuntimeError(f"device status {int(status.item())}")
     byt = n * HV * K * V * 2 * (1 + t) + total * (HV * (2 * K + V) * 2 + HV * K * 4 + HV * 4 + HV * V * 4)
@@ -873,10 +889,10 @@ def bench_step(kda, workloads, torch, l2, peak, n=32, t=8, replays=400):
                         "accepted columns of an [N][8] slot table, learned gate scale, bf16 q/k/v",
             "us_per_step": round(us, 3), "gbs": round(byt / (us * 1e-6) / 1e9, 1),
             "frac_of_peak": round(byt / (us * 1e-6) / 1e9 / peak, 4), "bytes_per_step": byt, "pools": R,
-            "launch": f"CUDA graph of {R} launches, replayed; flags KDA_LAUNCH_PDL|KDA_LAUNCH_PDL_EARLY_STATE"}
+            "launch": f"{GRAPH_TIMED} ({n_timed}, over {R} pools); flags KDA_LAUNCH_PDL|KDA_LAUNCH_PDL_EARLY_STATE"}
 
 
-def bench_verify(kda, workloads, torch, args, l2, peak, state_dtype=None):
+def bench_verify(kda, workloads, torch, args, l2, peak, state_dtype=None, replays=400):
     """Speculative verify, N=8 x T=8, HV=12, K=V=128, fp32 inputs, on an fp16
     pool (the verify workload's) or an fp32 pool."""
     state_dtype = state_dtype or torch.float16
@@ -893,27 +909,22 @@ def bench_verify(kda, workloads, torch, args, l2, peak, state_dtype=None):
     o = torch.empty(n, t, HV, V, device="cuda")
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
     stream = torch.cuda.Stream()
-    steps = min(args.steps, 10000)
-    chunk = chunk_size(steps)
-    g = torch.cuda.CUDAGraph()
     with torch.cuda.stream(stream):
         lib.kda_spec_verify(pools[0], d.init_slot, d.snap_slot, d.q, d.k, d.v, d.a, d.b, o, status)
-        stream.synchronize()
-        with torch.cuda.graph(g, stream=stream):
-            for i in range(chunk):
-                lib.kda_spec_verify(pools[i % R], d.init_slot, d.snap_slot, d.q, d.k, d.v, d.a,
-                                    d.b, o, status,
-                                    flags=kda.KDA_LAUNCH_PDL | kda.KDA_LAUNCH_PDL_EARLY_STATE)
-        for _ in range(max(1, args.warmup // chunk)):
-            g.replay()
-    us = timed_replays(g, stream, steps // chunk) * 1e3 / steps
+    n_timed = R * max(1, replays // R)
+    us = graph_timed(torch, stream,
+                     lambda i: lib.kda_spec_verify(pools[i % R], d.init_slot, d.snap_slot, d.q, d.k, d.v, d.a,
+                                                   d.b, o, status,
+                                                   flags=kda.KDA_LAUNCH_PDL | kda.KDA_LAUNCH_PDL_EARLY_STATE),
+                     n_timed) * 1e3 / n_timed
     byt = algorithmic_bytes(n, HV, K, V, t, es, 4)
     if int(status.item()) != 0:
         raise RuntimeError(f"device status {int(status.item())}")
     return {"workload": f"spec verify, {'fp16' if es == 2 else 'fp32'} pool, N=8 x T=8, HV=12, K=V=128, fp32 q/k/v",
             "us_per_step": round(us, 3), "gbs": round(byt / (us * 1e-6) / 1e9, 1),
             "frac_of_peak": round(byt / (us * 1e-6) / 1e9 / peak, 4), "bytes_per_step": byt,
-            "pools": R, "launch": f"CUDA graph of {chunk} launches, replayed; flags KDA_LAUNCH_PDL|KDA_LAUNCH_PDL_EARLY_STATE"}
+            "pools": R, "launch": f"{GRAPH_TIMED} ({n_timed}, over {R} pools); "
+                                  "flags KDA_LAUNCH_PDL|KDA_LAUNCH_PDL_EARLY_STATE"}
 
 
 if __name__ == "__main__":
