@@ -139,6 +139,21 @@ def test_conv_one_channel_per_thread_path(dtype):
     compare(workloads.make_conv(n=4, t=5, channels=256, dtype=dtype, seed=66, reset_p=0.2), offset=True)
 
 
+@pytest.mark.parametrize("channels", [4608, 301])
+@pytest.mark.parametrize("flags", [0, EARLY])
+@pytest.mark.parametrize("dtype", DT)
+def test_conv_long_requests_and_window(dtype, flags, channels):
+    """Requests of 13, 20, 9 and 1 tokens on a 22-entry window (19 drafts):
+    the inputs and the kept old entries run past one batch of 8 registers, so
+    the history carries from batch to batch, the kept entries (9 to 21 of
+    them) move in the loop, and the last inputs are read again for the window;
+    4-channel and 1-channel paths."""
+    inp = workloads.make_conv(n=4, t_lens=[13, 20, 9, 1], channels=channels, num_spec=19, dtype=dtype,
+                              seed=69, reset_p=0.25)
+    inp.accepted[:] = 20  # the whole window is history: every token count is valid
+    compare(inp, flags=flags)
+
+
 @pytest.mark.parametrize("flags", [0, EARLY])
 @pytest.mark.parametrize("dtype", DT)
 def test_conv_unaligned_weights_and_bias(dtype, flags):

@@ -187,6 +187,16 @@ def test_serving_scale_step_wide_launch(qkv_dtype, flags):
           flags)
 
 
+def test_wide_launch_variable_lengths_past_one_chunk():
+    """A wide launch (40 requests: 1920 CTAs) of packed requests of 13, 1, 8,
+    16, 0 and 9 tokens: two chunks of 8 for some, the two staging buffers
+    reused across the chunk boundary, empty requests beside them."""
+    lens = [13, 1, 8, 16, 0, 9] * 6 + [13, 16, 9, 5]
+    check(workloads.make_general(n=40, t_lens=lens, num_cols=16, hv=12, num_slots=40 * 16 + 8,
+                                 state_dtype=torch.float16, qkv_dtype=torch.bfloat16, seed=54, reset_p=0.1,
+                                 gate_scale=True))
+
+
 @pytest.mark.parametrize("qkv_dtype", [torch.bfloat16, torch.float16])
 def test_wide_launch_equals_one_wave_launches_bits(qkv_dtype):
     """Requests are independent, so one launch of 32 requests (the wide shape)
