@@ -69,6 +69,16 @@ static constexpr int kBuildDtype = KDA_F32;
 #define KDA_DEC_MINB 11
 #endif
 #endif
+// Decode tiles per CTA: an fp16 pool's two 64-column tiles of a head share one
+// CTA (768 CTAs at N = 64, all resident), an fp32 pool's stay one per CTA (two
+// would leave 6 CTAs per SM for 3072 tiles).
+#ifndef KDA_DEC_TPC
+#if KDA_STATE16
+#define KDA_DEC_TPC 2
+#else
+#define KDA_DEC_TPC 1
+#endif
+#endif
 // Warps per 16-column block of the prefill scan: KDA_PSCAN_KS_MID when the
 // grid has a CTA per SM or more only with one or two blocks per CTA, and
 // KDA_PSCAN_KS_FEW when it has fewer CTAs than SMs (few long prompts).
@@ -233,10 +243,11 @@ int launch_scan(const kda::StepParams& prm, const uint8_t* ws, int64_t heads, in
 
 template <typename QT, bool FULLK>
 int launch_decode_k(const kda_pool* pool, const kda::StepParams& prm, cudaStream_t stream) {
-    constexpr int BV = KDA_DEC_BV, NT = KDA_DEC_NT;
-    constexpr size_t smem = kda::decode_smem_bytes<state_t, BV, NT, (int)sizeof(QT)>();
-    auto kernel = kda::kda_decode_kernel<state_t, QT, BV, NT, KDA_DEC_MINB, KDA_DEC_KEEP != 0, FULLK>;
-    const int64_t tiles = (int64_t)prm.n * prm.hv * ((prm.v + BV - 1) / BV);
+    constexpr int BV = KDA_DEC_BV, NT = KDA_DEC_NT, TPC = KDA_DEC_TPC;
+    constexpr size_t smem = kda::decode_smem_bytes<state_t, BV, NT, (int)sizeof(QT), TPC>();
+    auto kernel = kda::kda_decode_kernel<state_t, QT, BV, NT, KDA_DEC_MINB, KDA_DEC_KEEP != 0, FULLK, TPC>;
+    // CTAs: TPC column blocks each
+    const int64_t tiles = (int64_t)prm.n * prm.hv * (((prm.v + BV - 1) / BV + TPC - 1) / TPC);
     if (tiles > 0x7fffffffLL) return KDA_ERR_SHAPE;
     CUtensorMap map;
     int rc = make_pool_map(pool, BV, &map);

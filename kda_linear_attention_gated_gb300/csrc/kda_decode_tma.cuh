@@ -1,17 +1,21 @@
-// KDA decode step, one CTA per tile, the tile staged by TMA (sm_103a).
+// KDA decode step, one CTA per one or two tiles, staged by TMA (sm_103a).
 //
 // Work unit ("tile"): one (request n, value head h, block of BV state columns)
 // with all K rows.  Columns are independent in this recurrence, so a tile needs
 // nothing from other tiles.  BV * sizeof(state) is 128, 64 or 32 bytes: one
 // TMA box row, one swizzle span.
 //
-// A CTA owns one tile.  Thread 0 starts one 3-D tensor-map load of the state
-// tile and 1-D bulk copies of the q, k and a rows and the tile's slice of v
-// into shared memory, all completing on one barrier.  Because the bytes land in
-// shared memory rather than registers, a CTA is small in registers and many
-// CTAs stay resident per SM, so the SM keeps a deep queue of state bytes in
-// flight while the hardware scheduler overlaps loading CTAs with computing
-// ones.  Then all threads work the tile:
+// A CTA owns TPC adjacent tiles of one (request, head): one for an fp32 pool,
+// two for an fp16 pool, so that an fp16 launch at N = 64 is 768 CTAs, all
+// resident at once (6 per SM by shared memory), where one tile per CTA made
+// 1.26 waves of 1536.  Thread 0 starts one 3-D tensor-map load per state tile,
+// each on its own barrier, and 1-D bulk copies of the q, k and a rows and the
+// tiles' slices of v into shared memory, completing on one more barrier.
+// Because the bytes land in shared memory rather than registers, a CTA is
+// small in registers and many CTAs stay resident per SM, so the SM keeps a
+// deep queue of state bytes in flight while the hardware scheduler overlaps
+// loading CTAs with computing ones.  The gates are worked out once for the
+// CTA's tiles; then all threads work each tile in turn:
 //   (1) gates: thread i < K turns row i's inputs into khat_i, qhat_i, alpha_i
 //       (the norms of k and q are a block reduction);
 //   (2) thread (row group rg, 16-byte column chunk cl) reads rows rg, rg + RG,
@@ -44,7 +48,10 @@
 
 namespace kda {
 
-template <typename ST, int BV, int NT, int QES>
+// TPC: tiles per CTA, adjacent column blocks of one (request, value head).
+// They share the inputs and the gates, and their state boxes are all in flight
+// from the start.
+template <typename ST, int BV, int NT, int QES, int TPC = 1>
 struct DecodeShape {
     static constexpr int VEC = StateVec<ST>::VEC;
     static constexpr int ROWBYTES = BV * (int)sizeof(ST);
@@ -55,10 +62,10 @@ struct DecodeShape {
     static constexpr uint32_t TILE_BYTES = (KMAX * ROWBYTES + 1023u) & ~1023u;
     // input area: q row, k row (QES-byte elements), a row (fp32), v slice
     static constexpr uint32_t IN_Q = 0, IN_K = KMAX * QES, IN_A = 2 * KMAX * QES;
-    static constexpr uint32_t IN_V = IN_A + KMAX * 4, IN_END = IN_V + BV * QES;
+    static constexpr uint32_t IN_V = IN_A + KMAX * 4, IN_END = IN_V + TPC * BV * QES;
     // gates: float4 {alpha khat, alpha qhat, alpha, beta khat} per row, then v
     // (fp32); they overlay the input area, which is read into registers first
-    static constexpr uint32_t GATE_BYTES = KMAX * 16 + BV * 4;
+    static constexpr uint32_t GATE_BYTES = KMAX * 16 + TPC * BV * 4;
     static constexpr uint32_t WORK_BYTES = ((IN_END > GATE_BYTES ? IN_END : GATE_BYTES) + 15u) & ~15u;
     // lanes of a warp that share a column chunk, and the values each keeps
     // after the in-warp reduce-scatter of its 2 VEC partial sums
@@ -76,47 +83,47 @@ struct DecodeShape {
     static_assert((RG * ROWBYTES) % 1024 == 0, "row stride must span whole swizzle periods");
 };
 
-template <typename ST, int BV, int NT, int QES>
+template <typename ST, int BV, int NT, int QES, int TPC = 1>
 constexpr size_t decode_smem_bytes() {
-    using SH = DecodeShape<ST, BV, NT, QES>;
+    using SH = DecodeShape<ST, BV, NT, QES, TPC>;
     // the tile, inputs/gates, reductions, two barriers (no alignment slack: the
     // dynamic shared memory base is 1024-byte aligned, which the kernel checks)
-    return SH::TILE_BYTES + SH::WORK_BYTES + SH::RED_BYTES + 16;
+    return TPC * SH::TILE_BYTES + SH::WORK_BYTES + SH::RED_BYTES + 8 * (TPC + 1);
 }
 
-template <typename ST, typename QT, int BV, int NT, int MINB, bool KEEP, bool FULLK>
+template <typename ST, typename QT, int BV, int NT, int MINB, bool KEEP, bool FULLK, int TPC = 1>
 __global__ void __launch_bounds__(NT, MINB)
 kda_decode_kernel(const __grid_constant__ CUtensorMap tmap, const StepParams p) {
-    using SH = DecodeShape<ST, BV, NT, (int)sizeof(QT)>;
+    using SH = DecodeShape<ST, BV, NT, (int)sizeof(QT), TPC>;
     using SV = StateVec<ST>;
     constexpr int VEC = SH::VEC, CL = SH::CL, RG = SH::RG, ROWS = SH::ROWS, NWARP = SH::NWARP;
     constexpr int KEEPV = SH::KEEPV;
 
     extern __shared__ __align__(1024) uint8_t smem[];
-    uint8_t* in = smem + SH::TILE_BYTES;
+    uint8_t* in = smem + TPC * SH::TILE_BYTES;
     float4* gates = reinterpret_cast<float4*>(in);  // overlays the inputs once they are read
     float* gv = reinterpret_cast<float*>(gates + KMAX);
     float* red = reinterpret_cast<float*>(in + SH::WORK_BYTES);  // [NWARP][4]
     float* red2 = red + NWARP * 4;                               // [NWARP][CL][2 VEC]
     float* dsm = red2 + NWARP * CL * 2 * VEC;                    // [BV]: d = v - u
     uint64_t* bar_st = reinterpret_cast<uint64_t*>(dsm + BV);    // state tile landed
-    uint64_t* bar_in = bar_st + 1;                                                 // inputs landed
-    const uint32_t tile_base = smem_u32(smem);
+    uint64_t* bar_in = bar_st + TPC;                                           // inputs landed
+    const uint32_t tile_base0 = smem_u32(smem);
     const uint32_t gate_base = smem_u32(gates);
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int cl = tid % CL, rg = tid / CL;
     // 32-bit index arithmetic: the host guarantees n * hv * ceil(v / BV) < 2^31
     const int vt = (p.v + BV - 1) / BV;
+    const int ct = (vt + TPC - 1) / TPC;  // CTAs per (request, head)
     const int tile = (int)blockIdx.x;
-    const int r = tile / vt;  // n * hv + h
-    const int cb = tile - r * vt;
+    const int r = tile / ct;  // n * hv + h
+    const int cb0 = (tile - r * ct) * TPC;  // first column block of this CTA
     const int n = r / p.hv;
     const int h = r - n * p.hv;
-    const int col0 = cb * BV + cl * VEC;
     const int qes = (int)sizeof(QT);
     // The swizzled tile needs a 1024-byte aligned base; report, never guess.
-    if ((tile_base & 1023u) != 0) {
+    if ((tile_base0 & 1023u) != 0) {
         if (tid == 0) atomicCAS(p.status, 0, STATUS_SMEM_ALIGN);
         return;
     }
@@ -139,20 +146,21 @@ kda_decode_kernel(const __grid_constant__ CUtensorMap tmap, const StepParams p) 
     const bool valid = col_ok && slot >= 0 && slot < p.num_slots;
     const bool rst = valid && p.reset != nullptr && p.reset[n] != 0;
     if (tid == 0) {
-        mbar_init(bar_st, 1);
-        mbar_init(bar_in, 1);
+        for (int j = 0; j <= TPC; ++j) mbar_init(bar_st + j, 1);
         fence_mbar_init();
         if (valid && !rst) {
             prefetch_tmap(&tmap);
-            mbar_arrive_expect_tx(bar_st, (uint32_t)p.k * SH::ROWBYTES);
-            if (!(p.flags & LAUNCH_TEST_WITHHOLD_STATE))  // the test hook: the wait runs out
-                tma_load_3d(smem, &tmap, bar_st, cb * BV, h * p.k, slot);
+            for (int j = 0; j < TPC && (TPC == 1 || cb0 + j < vt); ++j) {
+                mbar_arrive_expect_tx(bar_st + j, (uint32_t)p.k * SH::ROWBYTES);
+                if (!(p.flags & LAUNCH_TEST_WITHHOLD_STATE))  // the test hook: the wait runs out
+                    tma_load_3d(smem + j * SH::TILE_BYTES, &tmap, bar_st + j, (cb0 + j) * BV, h * p.k, slot);
+            }
         }
     }
     if (early) cudaGridDependencySynchronize();
     if (!valid) {
-        if (pad) {  // padding: this tile's outputs are zero
-            if (tid < min(BV, p.v - cb * BV)) p.o[(int64_t)r * p.v + cb * BV + tid] = 0.f;
+        if (pad) {  // padding: this CTA's outputs are zero
+            for (int e = tid; e < min(TPC * BV, p.v - cb0 * BV); e += NT) p.o[(int64_t)r * p.v + cb0 * BV + e] = 0.f;
         } else if (tid == 0) {
             atomicCAS(p.status, 0, col_ok ? STATUS_SLOT_RANGE : STATUS_ARG);
         }
@@ -160,14 +168,14 @@ kda_decode_kernel(const __grid_constant__ CUtensorMap tmap, const StepParams p) 
     }
     if (tid == 0) {
         const uint32_t qk_bytes = (uint32_t)p.k * qes;
-        const uint32_t v_bytes = (uint32_t)min(BV, p.v - cb * BV) * qes;
+        const uint32_t v_bytes = (uint32_t)min(TPC * BV, p.v - cb0 * BV) * qes;
         mbar_arrive_expect_tx(bar_in, 2 * qk_bytes + (uint32_t)p.k * 4 + v_bytes);
         const int64_t r64 = r;
         const int64_t rqk = (int64_t)n * p.hqk + h / (p.hv / p.hqk);  // grouped q/k heads
         bulk_load(in + SH::IN_Q, static_cast<const char*>(p.q) + rqk * qk_bytes, qk_bytes, bar_in);
         bulk_load(in + SH::IN_K, static_cast<const char*>(p.kk) + rqk * qk_bytes, qk_bytes, bar_in);
         bulk_load(in + SH::IN_A, p.a + r64 * p.k, (uint32_t)p.k * 4, bar_in);
-        bulk_load(in + SH::IN_V, static_cast<const char*>(p.vv) + (r64 * p.v + (int64_t)cb * BV) * qes,
+        bulk_load(in + SH::IN_V, static_cast<const char*>(p.vv) + (r64 * p.v + (int64_t)cb0 * BV) * qes,
                   v_bytes, bar_in);
     }
     const float b = __ldg(p.b + r);
@@ -178,8 +186,12 @@ kda_decode_kernel(const __grid_constant__ CUtensorMap tmap, const StepParams p) 
 
     // (1) gates: thread tid < K owns row tid.
     float kt = 0.f, qt = 0.f, alpha = 0.f, vt_ = 0.f;
-    if (ok && tid < BV && tid < min(BV, p.v - cb * BV))
-        vt_ = to_f32(reinterpret_cast<const QT*>(in + SH::IN_V)[tid]);
+    float vts[(TPC * BV + NT - 1) / NT];
+#pragma unroll
+    for (int e = 0; e < (TPC * BV + NT - 1) / NT; ++e) {
+        const int c = tid + e * NT;
+        vts[e] = ok && c < TPC * BV && c < p.v - cb0 * BV ? to_f32(reinterpret_cast<const QT*>(in + SH::IN_V)[c]) : 0.f;
+    }
     if (ok && tid < p.k) {
         kt = to_f32(reinterpret_cast<const QT*>(in + SH::IN_K)[tid]);
         qt = to_f32(reinterpret_cast<const QT*>(in + SH::IN_Q)[tid]);
@@ -198,7 +210,8 @@ kda_decode_kernel(const __grid_constant__ CUtensorMap tmap, const StepParams p) 
         if (tid == 0) {
             atomicExch(p.status, STATUS_TIMEOUT);
             mbar_wait(bar_in, 0);  // bounded: no copy may still target this CTA's memory
-            if (!rst) mbar_wait(bar_st, 0);
+            if (!rst)
+                for (int j = 0; j < TPC && (TPC == 1 || cb0 + j < vt); ++j) mbar_wait(bar_st + j, 0);
         }
         return;
     }
@@ -222,127 +235,141 @@ kda_decode_kernel(const __grid_constant__ CUtensorMap tmap, const StepParams p) 
         const float kh = kt * rk, qh = qt * rq;
         gates[tid] = make_float4(alpha * kh, alpha * qh, alpha, beta * kh);
     }
-    if (tid < BV) gv[tid] = vt_;
+#pragma unroll
+    for (int e = 0; e < (TPC * BV + NT - 1) / NT; ++e)
+        if (tid + e * NT < TPC * BV) gv[tid + e * NT] = vts[e];
     __syncthreads();
 
-    // This thread's rows are rg + RG * rr.  RG rows span whole swizzle periods,
-    // so the XOR term of every row equals that of row rg: one base address,
-    // then a constant stride.
-    const int nrows = FULLK ? ROWS : min(ROWS, (p.k - rg + RG - 1) / RG);
-    const uint32_t srow0 = tile_base + swz<SH::ROWBYTES>(rg, cl);
-    const uint32_t grow0 = gate_base + rg * 16;
-    constexpr uint32_t SSTRIDE = RG * SH::ROWBYTES, GSTRIDE = RG * 16;
+    for (int jt = 0; jt < TPC; ++jt) {
+        // tile jt of this CTA: column block cb (past the last block when V
+        // is not a multiple of TPC BV: then only the barriers are kept)
+        const int cb = cb0 + jt;
+        const bool tile_in = TPC == 1 || cb < vt;  // one tile a CTA: the grid covers exactly vt
+        const int col0 = cb * BV + cl * VEC;
+        const uint32_t tile_base = tile_base0 + jt * SH::TILE_BYTES;
+        // This thread's rows are rg + RG * rr.  RG rows span whole swizzle periods,
+        // so the XOR term of every row equals that of row rg: one base address,
+        // then a constant stride.
+        const int nrows = FULLK ? ROWS : min(ROWS, (p.k - rg + RG - 1) / RG);
+        const uint32_t srow0 = tile_base + swz<SH::ROWBYTES>(rg, cl);
+        const uint32_t grow0 = gate_base + rg * 16;
+        constexpr uint32_t SSTRIDE = RG * SH::ROWBYTES, GSTRIDE = RG * 16;
 
-    // (2) the two partial sums over this thread's rows, once the tile is in.
-    // Adjacent columns travel as float pairs through the packed FMA (two
-    // fmaf per instruction, each rounded as fmaf rounds).
-    constexpr int VP = VEC / 2;
-    const bool ok_st = rst || mbar_wait(bar_st, 0);
-    float2 u[VP], pp[VP];
-    float2 xs[KEEP ? ROWS : 1][VP];
+        // (2) the two partial sums over this thread's rows, once the tile is in.
+        // Adjacent columns travel as float pairs through the packed FMA (two
+        // fmaf per instruction, each rounded as fmaf rounds).
+        constexpr int VP = VEC / 2;
+        const bool ok_st = rst || !tile_in || mbar_wait(bar_st + jt, 0);
+        float2 u[VP], pp[VP];
+        float2 xs[KEEP ? ROWS : 1][VP];
 #pragma unroll
-    for (int c = 0; c < VP; ++c) { u[c] = make_float2(0.f, 0.f); pp[c] = make_float2(0.f, 0.f); }
-    if (!rst && ok_st) {
+        for (int c = 0; c < VP; ++c) { u[c] = make_float2(0.f, 0.f); pp[c] = make_float2(0.f, 0.f); }
+        if (!rst && ok_st && tile_in) {
 #pragma unroll
-        for (int rr = 0; rr < ROWS; ++rr) {
-            if (FULLK || rr < nrows) {
-                float2 x[VP];
-                SV::widen2(lds128(srow0 + rr * SSTRIDE), x);
-                const uint4 g = lds128(grow0 + rr * GSTRIDE);
-                const float w = __uint_as_float(g.x), z = __uint_as_float(g.y);
-                const float2 w2 = make_float2(w, w), z2 = make_float2(z, z);
+            for (int rr = 0; rr < ROWS; ++rr) {
+                if (FULLK || rr < nrows) {
+                    float2 x[VP];
+                    SV::widen2(lds128(srow0 + rr * SSTRIDE), x);
+                    const uint4 g = lds128(grow0 + rr * GSTRIDE);
+                    const float w = __uint_as_float(g.x), z = __uint_as_float(g.y);
+                    const float2 w2 = make_float2(w, w), z2 = make_float2(z, z);
 #pragma unroll
-                for (int c = 0; c < VP; ++c) {
-                    u[c] = __ffma2_rn(x[c], w2, u[c]);
-                    pp[c] = __ffma2_rn(x[c], z2, pp[c]);
-                    if (KEEP) xs[KEEP ? rr : 0][c] = x[c];
+                    for (int c = 0; c < VP; ++c) {
+                        u[c] = __ffma2_rn(x[c], w2, u[c]);
+                        pp[c] = __ffma2_rn(x[c], z2, pp[c]);
+                        if (KEEP) xs[KEEP ? rr : 0][c] = x[c];
+                    }
                 }
             }
         }
-    }
-    // Sum over the row groups of this warp (the lanes that share cl) as a
-    // reduce-scatter: each step hands the partner lane the half of the values
-    // this lane will not keep, so the lane ends with KEEPV finished sums of
-    // the 2 VEC values {u[0..VEC), p[0..VEC)} of chunk cl, at index kbase.
-    float vals[2 * VEC];
+        // Sum over the row groups of this warp (the lanes that share cl) as a
+        // reduce-scatter: each step hands the partner lane the half of the values
+        // this lane will not keep, so the lane ends with KEEPV finished sums of
+        // the 2 VEC values {u[0..VEC), p[0..VEC)} of chunk cl, at index kbase.
+        float vals[2 * VEC];
 #pragma unroll
-    for (int c = 0; c < VP; ++c) {
-        vals[2 * c] = u[c].x; vals[2 * c + 1] = u[c].y;
-        vals[VEC + 2 * c] = pp[c].x; vals[VEC + 2 * c + 1] = pp[c].y;
-    }
-    int kbase = 0;
-#pragma unroll
-    for (int m = 16, cnt = 2 * VEC; m >= CL; m >>= 1, cnt >>= 1) {
-        const bool upper = (lane & m) != 0;
-#pragma unroll
-        for (int j = 0; j < cnt / 2; ++j) {
-            const float send = upper ? vals[j] : vals[j + cnt / 2];
-            const float keep = upper ? vals[j + cnt / 2] : vals[j];
-            vals[j] = keep + __shfl_xor_sync(0xffffffffu, send, m);
+        for (int c = 0; c < VP; ++c) {
+            vals[2 * c] = u[c].x; vals[2 * c + 1] = u[c].y;
+            vals[VEC + 2 * c] = pp[c].x; vals[VEC + 2 * c + 1] = pp[c].y;
         }
-        kbase += upper ? cnt / 2 : 0;
-    }
-    {
-        float* dst = red2 + (warp * CL + cl) * 2 * VEC + kbase;
-        if (KEEPV == 4) *reinterpret_cast<float4*>(dst) = make_float4(vals[0], vals[1], vals[2], vals[3]);
-        else if (KEEPV == 2) *reinterpret_cast<float2*>(dst) = make_float2(vals[0], vals[1]);
-        else dst[0] = vals[0];
-    }
-    if (__syncthreads_or(ok_st ? 0 : 1)) {  // the state tile did not land in time
-        if (tid == 0) {
-            atomicExch(p.status, STATUS_TIMEOUT);
-            mbar_wait(bar_st, 0);  // bounded, as above
-        }
-        return;
-    }
-    // ... then over the warps: thread j < BV finishes column j, writes its
-    // output and leaves d_j = v_j - u_j for the update.
-    const int ncols = min(BV, p.v - cb * BV);
-    if (tid < ncols) {
-        const int jc = tid / VEC, jv = tid - jc * VEC;
-        float su = 0.f, sp = 0.f;
+        int kbase = 0;
 #pragma unroll
-        for (int w = 0; w < NWARP; ++w) {
-            su += red2[(w * CL + jc) * 2 * VEC + jv];
-            sp += red2[(w * CL + jc) * 2 * VEC + VEC + jv];
-        }
-        const float dj = gv[tid] - su;
-        dsm[tid] = dj;
-        p.o[(int64_t)r * p.v + cb * BV + tid] = fmaf(bqk, dj, sp) * p.inv_sqrt_k;
-    }
-    __syncthreads();
-    if (col0 >= p.v) return;
-    float2 d[VP];
+        for (int m = 16, cnt = 2 * VEC; m >= CL; m >>= 1, cnt >>= 1) {
+            const bool upper = (lane & m) != 0;
 #pragma unroll
-    for (int c = 0; c < VP; c += 2) {
-        const float4 d4 = *reinterpret_cast<const float4*>(dsm + cl * VEC + 2 * c);
-        d[c] = make_float2(d4.x, d4.y); d[c + 1] = make_float2(d4.z, d4.w);
-    }
-
-    // (3) the delta update S' = alpha S + (beta khat) d (per element
-    // fmaf(alpha, S, (beta khat) d), in pairs), stored in place with coalesced
-    // 16-byte stores.
-    ST* dst = static_cast<ST*>(p.pool) + state_at(p, slot, h) + (int64_t)rg * p.v + col0;
-    const int64_t gstride = (int64_t)RG * p.v;
-#pragma unroll
-    for (int rr = 0; rr < ROWS; ++rr) {
-        if (FULLK || rr < nrows) {
-            float2 x[VP];
-            if (rst) {
-#pragma unroll
-                for (int c = 0; c < VP; ++c) x[c] = make_float2(0.f, 0.f);
-            } else if (KEEP) {
-#pragma unroll
-                for (int c = 0; c < VP; ++c) x[c] = xs[KEEP ? rr : 0][c];
-            } else {
-                SV::widen2(lds128(srow0 + rr * SSTRIDE), x);
+            for (int j = 0; j < cnt / 2; ++j) {
+                const float send = upper ? vals[j] : vals[j + cnt / 2];
+                const float keep = upper ? vals[j + cnt / 2] : vals[j];
+                vals[j] = keep + __shfl_xor_sync(0xffffffffu, send, m);
             }
-            const uint4 g = lds128(grow0 + rr * GSTRIDE);
-            const float al = __uint_as_float(g.z), bk = __uint_as_float(g.w);
-            const float2 al2 = make_float2(al, al), bk2 = make_float2(bk, bk);
+            kbase += upper ? cnt / 2 : 0;
+        }
+        {
+            float* dst = red2 + (warp * CL + cl) * 2 * VEC + kbase;
+            if (KEEPV == 4) *reinterpret_cast<float4*>(dst) = make_float4(vals[0], vals[1], vals[2], vals[3]);
+            else if (KEEPV == 2) *reinterpret_cast<float2*>(dst) = make_float2(vals[0], vals[1]);
+            else dst[0] = vals[0];
+        }
+        if (__syncthreads_or(ok_st ? 0 : 1)) {  // the state tile did not land in time
+            if (tid == 0) {
+                atomicExch(p.status, STATUS_TIMEOUT);
+                for (int j = jt; j < TPC && (TPC == 1 || cb0 + j < vt); ++j) mbar_wait(bar_st + j, 0);  // bounded, as above
+            }
+            return;
+        }
+        // ... then over the warps: thread j < BV finishes column j, writes its
+        // output and leaves d_j = v_j - u_j for the update.
+        const int ncols = min(BV, p.v - cb * BV);  // <= 0 past the last column block
+        if (tid < ncols) {
+            const int jc = tid / VEC, jv = tid - jc * VEC;
+            float su = 0.f, sp = 0.f;
 #pragma unroll
-            for (int c = 0; c < VP; ++c) x[c] = __ffma2_rn(al2, x[c], __fmul2_rn(bk2, d[c]));
-            __stcs(reinterpret_cast<uint4*>(dst + rr * gstride), SV::narrow2(x));
+            for (int w = 0; w < NWARP; ++w) {
+                su += red2[(w * CL + jc) * 2 * VEC + jv];
+                sp += red2[(w * CL + jc) * 2 * VEC + VEC + jv];
+            }
+            const float dj = gv[jt * BV + tid] - su;
+            dsm[tid] = dj;
+            p.o[(int64_t)r * p.v + cb * BV + tid] = fmaf(bqk, dj, sp) * p.inv_sqrt_k;
+        }
+        __syncthreads();
+        if constexpr (TPC == 1) {
+            if (col0 >= p.v) return;  // one tile a CTA: nothing follows
+        }
+        if (TPC == 1 || col0 < p.v) {  // the tile holds columns: the update and the stores
+            float2 d[VP];
+#pragma unroll
+            for (int c = 0; c < VP; c += 2) {
+                const float4 d4 = *reinterpret_cast<const float4*>(dsm + cl * VEC + 2 * c);
+                d[c] = make_float2(d4.x, d4.y); d[c + 1] = make_float2(d4.z, d4.w);
+            }
+
+            // (3) the delta update S' = alpha S + (beta khat) d (per element
+            // fmaf(alpha, S, (beta khat) d), in pairs), stored in place with coalesced
+            // 16-byte stores.
+            ST* dst = static_cast<ST*>(p.pool) + state_at(p, slot, h) + (int64_t)rg * p.v + col0;
+            const int64_t gstride = (int64_t)RG * p.v;
+#pragma unroll
+            for (int rr = 0; rr < ROWS; ++rr) {
+                if (FULLK || rr < nrows) {
+                    float2 x[VP];
+                    if (rst) {
+#pragma unroll
+                        for (int c = 0; c < VP; ++c) x[c] = make_float2(0.f, 0.f);
+                    } else if (KEEP) {
+#pragma unroll
+                        for (int c = 0; c < VP; ++c) x[c] = xs[KEEP ? rr : 0][c];
+                    } else {
+                        SV::widen2(lds128(srow0 + rr * SSTRIDE), x);
+                    }
+                    const uint4 g = lds128(grow0 + rr * GSTRIDE);
+                    const float al = __uint_as_float(g.z), bk = __uint_as_float(g.w);
+                    const float2 al2 = make_float2(al, al), bk2 = make_float2(bk, bk);
+#pragma unroll
+                    for (int c = 0; c < VP; ++c) x[c] = __ffma2_rn(al2, x[c], __fmul2_rn(bk2, d[c]));
+                    __stcs(reinterpret_cast<uint4*>(dst + rr * gstride), SV::narrow2(x));
+                }
+            }
         }
     }
 }
