@@ -69,9 +69,11 @@ static constexpr int kBuildDtype = KDA_F32;
 #define KDA_DEC_MINB 11
 #endif
 #endif
-// Decode tiles per CTA: an fp16 pool's two 64-column tiles of a head share one
-// CTA (768 CTAs at N = 64, all resident), an fp32 pool's stay one per CTA (two
-// would leave 6 CTAs per SM for 3072 tiles).
+// Decode tiles per CTA for launches past one wave: an fp16 pool's two
+// 64-column tiles of a head then share one CTA (768 CTAs at N = 64, all
+// resident); an fp32 pool's stay one per CTA (two would leave 6 CTAs per SM
+// for 3072 tiles).  Launches within one wave keep one tile per CTA, for the
+// parallelism.
 #ifndef KDA_DEC_TPC
 #if KDA_STATE16
 #define KDA_DEC_TPC 2
@@ -241,9 +243,9 @@ int launch_scan(const kda::StepParams& prm, const uint8_t* ws, int64_t heads, in
     return cudaLaunchKernelEx(&cfg, scan, prm, ws) == cudaSuccess ? KDA_OK : KDA_ERR_LAUNCH;
 }
 
-template <typename QT, bool FULLK>
+template <typename QT, bool FULLK, int TPC>
 int launch_decode_k(const kda_pool* pool, const kda::StepParams& prm, cudaStream_t stream) {
-    constexpr int BV = KDA_DEC_BV, NT = KDA_DEC_NT, TPC = KDA_DEC_TPC;
+    constexpr int BV = KDA_DEC_BV, NT = KDA_DEC_NT;
     constexpr size_t smem = kda::decode_smem_bytes<state_t, BV, NT, (int)sizeof(QT), TPC>();
     auto kernel = kda::kda_decode_kernel<state_t, QT, BV, NT, KDA_DEC_MINB, KDA_DEC_KEEP != 0, FULLK, TPC>;
     // CTAs: TPC column blocks each
@@ -268,10 +270,29 @@ int launch_decode_k(const kda_pool* pool, const kda::StepParams& prm, cudaStream
 
 // K = 128 (the configured models' key dimension) gets a build without the
 // per-row bound checks.
+template <typename QT, int TPC>
+int launch_decode_t(const kda_pool* pool, const kda::StepParams& prm, cudaStream_t stream) {
+    return prm.k == kda::KMAX ? launch_decode_k<QT, true, TPC>(pool, prm, stream)
+                              : launch_decode_k<QT, false, TPC>(pool, prm, stream);
+}
+
+// KDA_DEC_TPC tiles per CTA when the one-tile grid is more than one wave of
+// the one-tile kernel, else one.
 template <typename QT>
 int launch_decode(const kda_pool* pool, const kda::StepParams& prm, cudaStream_t stream) {
-    return prm.k == kda::KMAX ? launch_decode_k<QT, true>(pool, prm, stream)
-                              : launch_decode_k<QT, false>(pool, prm, stream);
+    constexpr int TPC = KDA_DEC_TPC;
+    if constexpr (TPC > 1) {
+        constexpr int BV = KDA_DEC_BV, NT = KDA_DEC_NT;
+        constexpr size_t smem = kda::decode_smem_bytes<state_t, BV, NT, (int)sizeof(QT)>();
+        const int64_t tiles = (int64_t)prm.n * prm.hv * ((prm.v + BV - 1) / BV);
+        int occ = 0, sms = 0;
+        const int rc = occupancy(reinterpret_cast<const void*>(
+                                     kda::kda_decode_kernel<state_t, QT, BV, NT, KDA_DEC_MINB, KDA_DEC_KEEP != 0, true>),
+                                 NT, smem, &occ, &sms);
+        if (rc != KDA_OK) return rc;
+        if (tiles > (int64_t)occ * sms) return launch_decode_t<QT, TPC>(pool, prm, stream);
+    }
+    return launch_decode_t<QT, 1>(pool, prm, stream);
 }
 
 template <typename QT, bool WIDE>

@@ -85,6 +85,20 @@ def test_decode_ragged_shapes_and_input_types(state_dtype, qkv_dtype, K, V):
     assert_pool_match(gpool, ref, inp.init_slot.numpy(), "pool")
 
 
+# An fp16-pool decode whose one-tile grid exceeds one wave (8 CTAs per SM: 1216
+# on 152 SMs) runs two 64-column tiles per CTA.  V = 80 gives each head a full
+# and a 16-column tile; V = 48 gives one tile, the CTA's second slot empty.
+@pytest.mark.parametrize("n,hv,K,V", [(64, 12, 128, 80), (128, 12, 64, 48)])
+def test_fp16_decode_two_tiles_a_cta_ragged(n, hv, K, V):
+    inp = workloads.make_decode(n=n, hv=hv, k=K, v=V, num_slots=n + 7, state_dtype=torch.float16,
+                                qkv_dtype=torch.bfloat16, seed=K * 1000 + V + 7, reset_p=0.2)
+    gpool, o, st = gpu_decode(inp)
+    ref, o_ref = oracle_decode(inp)
+    assert st == 0
+    assert_out_match(o, o_ref, torch.float16, "o")
+    assert_pool_match(gpool, ref, inp.init_slot.numpy(), "pool")
+
+
 @pytest.mark.parametrize("state_dtype", [torch.float32, torch.float16])
 @pytest.mark.parametrize("T", [1, 3, 8, 13])
 def test_verify_token_counts_and_resets(state_dtype, T):
