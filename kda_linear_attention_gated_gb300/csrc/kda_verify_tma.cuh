@@ -68,6 +68,11 @@ struct VerifyShape {
     // shapes a launch is about 2.5 CTAs per SM, so 3 keep it in one wave
     static constexpr int MINB = WIDE ? 4 : KDA_VER_MINB;
     static constexpr int ROWS = KMAX / 32;    // rows per lane
+    // the row pass: thread r < KMAX takes key row r; with 2 KMAX threads (an
+    // fp32 pool's 128-byte rows) thread KMAX + r takes row r as well and the
+    // two split its terms of the sums A and B.  RW warps cover the rows once.
+    static constexpr bool SPLIT = NT >= 2 * KMAX;
+    static constexpr int RW = KMAX / 32;
     static constexpr int TC = 8;              // tokens per chunk
     static constexpr int NA = TC * (TC - 1) / 2, NB = TC * (TC + 1) / 2;  // 28 + 36 = 64 sums
     static constexpr int G = 16 / VEC;        // tokens per group of column sums (2 G VEC = 32 values)
@@ -176,6 +181,8 @@ kda_verify_kernel(const __grid_constant__ CUtensorMap tmap, const StepParams p) 
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int chunk = warp;
+    const int rowt = SH::SPLIT ? (tid & (KMAX - 1)) : tid;  // this thread's key row in the row pass
+    const int half = SH::SPLIT ? tid / KMAX : 0;             // which half of the terms (uniform per warp)
     const int vt = (p.v + BV - 1) / BV;
     const int tile = (int)blockIdx.x;
     const int r = tile / vt;  // n * hv + h
@@ -206,7 +213,7 @@ kda_verify_kernel(const __grid_constant__ CUtensorMap tmap, const StepParams p) 
         const QT* qp = static_cast<const QT*>(p.q);
         const QT* kp = static_cast<const QT*>(p.kk);
         const QT* vp = static_cast<const QT*>(p.vv);
-        const int row = tid < KK ? tid : 0, col = tid < vcols ? tid : 0;
+        const int row = rowt < KK ? rowt : 0, col = tid < vcols ? tid : 0;
 #pragma unroll
         for (int j = 0; j < TC; ++j) {
             const int64_t tok = (int64_t)tb + t0 + min(j, tc - 1);
@@ -306,7 +313,7 @@ kda_verify_kernel(const __grid_constant__ CUtensorMap tmap, const StepParams p) 
     }
     const bool scaled = p.a_log != nullptr;
     const float gscale = scaled ? expf(__ldg(p.a_log + h)) : 1.f;
-    const float gbias = p.dt_bias != nullptr && tid < KK ? __ldg(p.dt_bias + (int64_t)h * KK + tid) : 0.f;
+    const float gbias = p.dt_bias != nullptr && rowt < KK ? __ldg(p.dt_bias + (int64_t)h * KK + rowt) : 0.f;
     for (int t0 = 0; t0 < Tn; t0 += TC) {
         const int tc = min(TC, Tn - t0);
         if (t0 > 0 || !PRO_INPUTS) load_inputs(t0, tc);
@@ -324,7 +331,7 @@ kda_verify_kernel(const __grid_constant__ CUtensorMap tmap, const StepParams p) 
             float kt[TC], qt[TC], at[TC];
 #pragma unroll
             for (int j = 0; j < TC; ++j) {
-                const bool in_row = j < tc && tid < KK;
+                const bool in_row = j < tc && rowt < KK;
                 kt[j] = in_row ? to_f32(kraw[j]) : 0.f;
                 qt[j] = in_row ? to_f32(qraw[j]) : 0.f;
                 at[j] = in_row ? araw[j] : 0.f;
@@ -338,10 +345,10 @@ kda_verify_kernel(const __grid_constant__ CUtensorMap tmap, const StepParams p) 
             // the decay, one branch for all tokens
             if (scaled) {
 #pragma unroll
-                for (int j = 0; j < TC; ++j) at[j] = j < tc && tid < KK ? gate_alpha(at[j], true, gscale, gbias) : 0.f;
+                for (int j = 0; j < TC; ++j) at[j] = j < tc && rowt < KK ? gate_alpha(at[j], true, gscale, gbias) : 0.f;
             } else {
 #pragma unroll
-                for (int j = 0; j < TC; ++j) at[j] = j < tc && tid < KK ? gate_alpha(at[j], false, gscale, gbias) : 0.f;
+                for (int j = 0; j < TC; ++j) at[j] = j < tc && rowt < KK ? gate_alpha(at[j], false, gscale, gbias) : 0.f;
             }
             // the first chunk of an fp16 pool at K = KMAX takes its column sums
             // on the tensor cores: rows 2 j (c k) and 2 j + 1 (c q) of the gate
@@ -383,19 +390,25 @@ kda_verify_kernel(const __grid_constant__ CUtensorMap tmap, const StepParams p) 
                     }
                 }
             }
-            float sq[2 * TC];
+            if (half == 0) {  // the first RW warps: the squared norms
+                float sq[2 * TC];
 #pragma unroll
-            for (int j = 0; j < TC; ++j) { sq[2 * j] = kt[j] * kt[j]; sq[2 * j + 1] = qt[j] * qt[j]; }
-            const float s = warp_reduce_scatter<2 * TC>(sq, lane);
-            if ((lane & 1) == 0) {
-                const int m = lane >> 1;  // token m >> 1, k (even) or q (odd)
-                nrm[((m >> 1) * NW + warp) * 2 + (m & 1)] = s;
+                for (int j = 0; j < TC; ++j) { sq[2 * j] = kt[j] * kt[j]; sq[2 * j + 1] = qt[j] * qt[j]; }
+                const float s = warp_reduce_scatter<2 * TC>(sq, lane);
+                if ((lane & 1) == 0) {
+                    const int m = lane >> 1;  // token m >> 1, k (even) or q (odd)
+                    nrm[((m >> 1) * SH::RW + warp) * 2 + (m & 1)] = s;
+                }
             }
             float part[32];
-            ab_terms<0, TC>(part, kt, kt, qt, at);
-            abw[warp * 64 + lane] = warp_reduce_scatter<32>(part, lane);
-            ab_terms<32, TC>(part, kt, kt, qt, at);
-            abw[warp * 64 + 32 + lane] = warp_reduce_scatter<32>(part, lane);
+            if (!SH::SPLIT || half == 0) {
+                ab_terms<0, TC>(part, kt, kt, qt, at);
+                abw[(warp % SH::RW) * 64 + lane] = warp_reduce_scatter<32>(part, lane);
+            }
+            if (!SH::SPLIT || half == 1) {
+                ab_terms<32, TC>(part, kt, kt, qt, at);
+                abw[(warp % SH::RW) * 64 + 32 + lane] = warp_reduce_scatter<32>(part, lane);
+            }
         }
         {  // the initial state arrives (first chunk) while the rows are summed
             bool ok = true;
@@ -435,10 +448,10 @@ kda_verify_kernel(const __grid_constant__ CUtensorMap tmap, const StepParams p) 
             if (t < tc) {
                 float ks = 0.f, rt = 0.f;
 #pragma unroll
-                for (int w = 0; w < NW; ++w) {
+                for (int w = 0; w < SH::RW; ++w) {
                     v += abw[w * 64 + tid];
-                    ks += nrm[(s * NW + w) * 2 + 0];
-                    rt += nrm[(t * NW + w) * 2 + (is_a ? 0 : 1)];
+                    ks += nrm[(s * SH::RW + w) * 2 + 0];
+                    rt += nrm[(t * SH::RW + w) * 2 + (is_a ? 0 : 1)];
                 }
                 const float beta = sigmoid_neg(-bsm[s]);  // sigmoid(b_s)
                 v *= beta * __frsqrt_rn(ks + L2_EPS) * __frsqrt_rn(rt + L2_EPS);
@@ -448,9 +461,9 @@ kda_verify_kernel(const __grid_constant__ CUtensorMap tmap, const StepParams p) 
             const int t = tid - 64;
             float kk2 = 0.f, qq2 = 0.f;
 #pragma unroll
-            for (int w = 0; w < NW; ++w) {
-                kk2 += nrm[(t * NW + w) * 2 + 0];
-                qq2 += nrm[(t * NW + w) * 2 + 1];
+            for (int w = 0; w < SH::RW; ++w) {
+                kk2 += nrm[(t * SH::RW + w) * 2 + 0];
+                qq2 += nrm[(t * SH::RW + w) * 2 + 1];
             }
             scal[t] = make_float4(sigmoid_neg(-bsm[t]), __frsqrt_rn(kk2 + L2_EPS),
                                   __frsqrt_rn(qq2 + L2_EPS), 0.f);
