@@ -49,6 +49,33 @@ def test_withheld_state_copy_times_out_and_writes_nothing(state_dtype):
     assert_pool_match(gpool, ref, inp.init_slot.numpy(), "pool after the timeout")
 
 
+def test_withheld_state_copy_times_out_two_tiles_a_cta():
+    """An fp16-pool launch past one wave (N=64 x HV=12 x 2 column tiles) runs
+    two tiles a CTA: with both state copies withheld, each CTA's first wait
+    runs out, it waits (bounded) on both tiles' barriers, and the call reports
+    the timeout with nothing written; the context stays usable."""
+    lib = lib_for(torch.float16)
+    inp = workloads.make_decode(n=64, hv=12, k=64, v=128, num_slots=72, state_dtype=torch.float16, seed=84)
+    d = inp.to("cuda")
+    before = pool_np(d.pool.cpu())
+    o = torch.full((64, 12, 128), float("nan"), device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    t0 = time.monotonic()
+    lib.kda_decode_step(d.pool, d.init_slot, d.q, d.k, d.v, d.a, d.b, o, status,
+                        flags=kda.KDA_LAUNCH_TEST_WITHHOLD_STATE)
+    torch.cuda.synchronize()
+    elapsed = time.monotonic() - t0
+    assert int(status.item()) == kda.KDA_ERR_TIMEOUT
+    assert 0.9 <= elapsed < 30.0, f"the bounded waits took {elapsed:.2f} s"
+    assert pool_np(d.pool.cpu()).tobytes() == before.tobytes()
+    assert torch.isnan(o).all()
+    gpool, o2, st = gpu_decode(inp)
+    assert st == 0
+    ref, o_ref = oracle_decode(inp)
+    assert_out_match(o2, o_ref, torch.float16, "o after the timeout")
+    assert_pool_match(gpool, ref, inp.init_slot.numpy(), "pool after the timeout")
+
+
 @pytest.mark.parametrize("state_dtype", SD)
 def test_withheld_state_copy_times_out_in_verify(state_dtype):
     lib = lib_for(state_dtype)
