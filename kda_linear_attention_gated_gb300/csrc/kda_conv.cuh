@@ -126,6 +126,9 @@ __global__ void __launch_bounds__(CT) kda_conv_kernel(const ConvParams p) {
     const int m = acc + KWR - 1;
     const int kept = max(0, p.L - T);
     constexpr int CB = 8;  // window entries or tokens per batch of loads
+    // kept old entries per batch: a full-length step (T = L - KW + 2) keeps
+    // KW - 2 of them, so one batch of KWM - 2 covers it; more go through the loop
+    constexpr int CBK = KWM > 2 ? KWM - 2 : 1;
     const bool range_ok = tb >= 0 && T > 0 && T <= p.t && tb + T <= p.total;
     const ET* x = static_cast<const ET*>(p.x) + (int64_t)tb * p.C + min(c, p.C - VC);  // token t at x[t C]
     // The first CB inputs of this request go out before anything that waits
@@ -166,11 +169,11 @@ __global__ void __launch_bounds__(CT) kda_conv_kernel(const ConvParams p) {
     const int nh = KWR - 1;  // history entries
     // the history entries and the first batch of kept old entries, read
     // together (the kept entries W[m - kept + e] move to W[e])
-    R hr[KWM], kv[CB];
+    R hr[KWM], kv[CBK];
 #pragma unroll
     for (int i = 0; i < KWM; ++i) hr[i] = IO::ld(W + (int64_t)min(acc + i, p.L - 1) * p.C);
 #pragma unroll
-    for (int u = 0; u < CB; ++u) kv[u] = IO::ld(W + (int64_t)min(m - kept + u, p.L - 1) * p.C);
+    for (int u = 0; u < CBK; ++u) kv[u] = IO::ld(W + (int64_t)min(m - kept + u, p.L - 1) * p.C);
     // w[i] weighs history entry i (i < KW - 1); wlast weighs the current input.
     // A channel's KW = 4 weights are one 16-byte row, and four channels' biases
     // one 16-byte vector, read as such where the arrays are 16-byte aligned.
@@ -228,9 +231,9 @@ __global__ void __launch_bounds__(CT) kda_conv_kernel(const ConvParams p) {
     // a source never lies below its destination (m >= kept), so no batch reads
     // what an earlier one wrote
 #pragma unroll
-    for (int u = 0; u < CB; ++u)
+    for (int u = 0; u < CBK; ++u)
         if (u < kept) IO::st(W + (int64_t)u * p.C, rst ? zero : kv[u]);
-    for (int e0 = CB; e0 < kept; e0 += CB) {
+    for (int e0 = CBK; e0 < kept; e0 += CB) {
         R v[CB];
 #pragma unroll
         for (int u = 0; u < CB; ++u) v[u] = IO::ld(W + (int64_t)min(m - kept + e0 + u, p.L - 1) * p.C);
