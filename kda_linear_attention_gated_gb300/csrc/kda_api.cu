@@ -93,6 +93,24 @@ static constexpr int kBuildDtype = KDA_F32;
 #ifndef KDA_DEC_KEEP
 #define KDA_DEC_KEEP 0
 #endif
+// The same two settings for the kernel with more than one tile per CTA.  Its
+// shared memory (two state tiles) allows 6 CTAs per SM, so 6 sets the register
+// cap (80), and the fp16 rows' raw 16-byte words from the sums pass stay in
+// registers for the update pass (32 registers) instead of being read again.
+#ifndef KDA_DEC_KEEP2
+#if KDA_STATE16
+#define KDA_DEC_KEEP2 1
+#else
+#define KDA_DEC_KEEP2 KDA_DEC_KEEP
+#endif
+#endif
+#ifndef KDA_DEC_MINB2
+#if KDA_STATE16
+#define KDA_DEC_MINB2 6
+#else
+#define KDA_DEC_MINB2 KDA_DEC_MINB
+#endif
+#endif
 
 namespace {
 
@@ -247,7 +265,9 @@ template <typename QT, bool FULLK, int TPC>
 int launch_decode_k(const kda_pool* pool, const kda::StepParams& prm, cudaStream_t stream) {
     constexpr int BV = KDA_DEC_BV, NT = KDA_DEC_NT;
     constexpr size_t smem = kda::decode_smem_bytes<state_t, BV, NT, (int)sizeof(QT), TPC>();
-    auto kernel = kda::kda_decode_kernel<state_t, QT, BV, NT, KDA_DEC_MINB, KDA_DEC_KEEP != 0, FULLK, TPC>;
+    constexpr int MINB = TPC > 1 ? KDA_DEC_MINB2 : KDA_DEC_MINB;
+    constexpr bool KEEP = (TPC > 1 ? KDA_DEC_KEEP2 : KDA_DEC_KEEP) != 0;
+    auto kernel = kda::kda_decode_kernel<state_t, QT, BV, NT, MINB, KEEP, FULLK, TPC>;
     // CTAs: TPC column blocks each
     const int64_t tiles = (int64_t)prm.n * prm.hv * (((prm.v + BV - 1) / BV + TPC - 1) / TPC);
     if (tiles > 0x7fffffffLL) return KDA_ERR_SHAPE;

@@ -22,9 +22,11 @@
 //       ... of its chunk from shared memory and accumulates u = S^T (alpha khat)
 //       and p = S^T (alpha qhat) (the decay folded into the gates); warp
 //       shuffles and one shared-memory pass finish the sums over K;
-//   (3) it reads its rows again (or keeps them in registers), applies the
-//       delta update and writes them back to the slot with coalesced 16-byte
-//       stores.
+//   (3) it reads its rows from shared memory again (one tile a CTA) or takes
+//       their raw 16-byte words, kept in registers since (2) (two fp16 tiles a
+//       CTA, where shared memory caps residency at 6 CTAs per SM and so leaves
+//       room for them), applies the delta update and writes the rows back to
+//       the slot with coalesced 16-byte stores.
 // The inputs and the state tile complete on separate barriers, so the gates
 // are computed while the state is still in flight.  Each barrier wait is
 // bounded (1 s); a wait that runs out makes the whole CTA record
@@ -261,7 +263,7 @@ kda_decode_kernel(const __grid_constant__ CUtensorMap tmap, const StepParams p) 
         constexpr int VP = VEC / 2;
         const bool ok_st = rst || !tile_in || mbar_wait(bar_st + jt, 0);
         float2 u[VP], pp[VP];
-        float2 xs[KEEP ? ROWS : 1][VP];
+        uint4 xs[KEEP ? ROWS : 1];  // KEEP: the rows' raw 16-byte words, for pass (3)
 #pragma unroll
         for (int c = 0; c < VP; ++c) { u[c] = make_float2(0.f, 0.f); pp[c] = make_float2(0.f, 0.f); }
         if (!rst && ok_st && tile_in) {
@@ -269,7 +271,9 @@ kda_decode_kernel(const __grid_constant__ CUtensorMap tmap, const StepParams p) 
             for (int rr = 0; rr < ROWS; ++rr) {
                 if (FULLK || rr < nrows) {
                     float2 x[VP];
-                    SV::widen2(lds128(srow0 + rr * SSTRIDE), x);
+                    const uint4 raw = lds128(srow0 + rr * SSTRIDE);
+                    if (KEEP) xs[KEEP ? rr : 0] = raw;
+                    SV::widen2(raw, x);
                     const uint4 g = lds128(grow0 + rr * GSTRIDE);
                     const float w = __uint_as_float(g.x), z = __uint_as_float(g.y);
                     const float2 w2 = make_float2(w, w), z2 = make_float2(z, z);
@@ -277,7 +281,6 @@ kda_decode_kernel(const __grid_constant__ CUtensorMap tmap, const StepParams p) 
                     for (int c = 0; c < VP; ++c) {
                         u[c] = __ffma2_rn(x[c], w2, u[c]);
                         pp[c] = __ffma2_rn(x[c], z2, pp[c]);
-                        if (KEEP) xs[KEEP ? rr : 0][c] = x[c];
                     }
                 }
             }
@@ -357,8 +360,7 @@ kda_decode_kernel(const __grid_constant__ CUtensorMap tmap, const StepParams p) 
 #pragma unroll
                         for (int c = 0; c < VP; ++c) x[c] = make_float2(0.f, 0.f);
                     } else if (KEEP) {
-#pragma unroll
-                        for (int c = 0; c < VP; ++c) x[c] = xs[KEEP ? rr : 0][c];
+                        SV::widen2(xs[KEEP ? rr : 0], x);
                     } else {
                         SV::widen2(lds128(srow0 + rr * SSTRIDE), x);
                     }
