@@ -327,6 +327,70 @@ int kda_conv_step(const kda_conv_window* win, const kda_conv_args* args, int32_t
                   uint32_t flags, void* stream);
 
 /*
+ * Arguments of kda_decode_conv_step: one decode token per request with the
+ * short convolution in front of the recurrence done in the same kernel (pull
+ * request 2894, review thread on the conv window: the conv runs on the
+ * inputs right before the recurrence; pull request 2130, What: the decode
+ * step).  x holds each request's pre-convolution inputs of the three streams
+ * side by side, channels = 2 * h_qk * k + hv * v (pool's hv, k, v):
+ *   q channels  [0, h_qk k)            head g, row i at g k + i
+ *   k channels  [h_qk k, 2 h_qk k)     head g, row i at h_qk k + g k + i
+ *   v channels  [2 h_qk k, channels)   head h, column j at 2 h_qk k + h v + j
+ * Per request r the call is, bit for bit, kda_conv_step with one token
+ * (conv_slot[r], no accepted index, the same reset flag) followed by
+ * kda_decode_step on slot_ids[r] whose q, k, v are that step's y, read as
+ * the window's dtype; value head h reads q/k head h / (hv / h_qk).  The
+ * window must hold kernel_width - 1 or kernel_width entries (a one-token step
+ * keeps state_len - 1 old ones, which must lie within the history it reads).
+ *   slot_ids, conv_slot  device int32 [n]: the state slot and the window slot.
+ *   reset     device uint8 [n] or NULL: zero state and zero history.
+ *   x         device [n][channels] of the window's dtype.
+ *   weight    device fp32 [channels][kernel_width];  bias device fp32 [channels] or NULL.
+ *   a, b, o   as for kda_decode_step: fp32 [n][hv][k] (16-byte aligned), [n][hv], [n][hv][v].
+ *   y         device [n][channels] of the window's dtype, or NULL: the
+ *             convolution's outputs, when the caller wants them as well.
+ *   counters  device int32 [n][h_qk], all zero on entry (allocate once and
+ *             zero once); the call leaves them zero.  Several CTAs read one
+ *             q/k channel's window, so the last of them to finish reading
+ *             writes the new entries; each counts its read here.
+ */
+typedef struct kda_decode_conv_args {
+    int32_t n;                  /* requests */
+    int32_t h_qk;               /* q/k heads: divides the pool's hv */
+    int32_t kernel_width;       /* 1 .. 4 */
+    int32_t activation;         /* 0 none, 1 SiLU */
+    const int32_t* slot_ids;    /* [n] */
+    const int32_t* conv_slot;   /* [n] */
+    const uint8_t* reset;       /* [n] or NULL */
+    const void* x;              /* [n][channels] */
+    const float* weight;        /* [channels][kernel_width] */
+    const float* bias;          /* [channels] or NULL */
+    const float* a;             /* [n][hv][k] */
+    const float* b;             /* [n][hv] */
+    float* o;                   /* [n][hv][v] (output) */
+    void* y;                    /* [n][channels] (output) or NULL */
+    int32_t* counters;          /* [n][h_qk] */
+} kda_decode_conv_args;
+
+/*
+ * One fused conv + decode step (see kda_decode_conv_args); pool, win and args
+ * are host pointers.  Host checks: those of kda_decode_step for the pool,
+ * KDA_ERR_NULL, _DTYPE_UNSUPPORTED (window dtype), _SHAPE (channels other
+ * than 2 h_qk k + hv v, h_qk not dividing hv, kernel_width outside 1 .. 4,
+ * state_len outside kernel_width - 1 .. kernel_width, slot_stride too small),
+ * _ALIGN (x, y, window base to their element size, a to 16 bytes, the rest to
+ * 4), _ARG (negative n, activation not 0/1, flags other than the PDL bits).
+ * Device checks (in *dev_status, the request skipped whole, its counters left
+ * alone): KDA_ERR_SLOT_RANGE for a slot id or window slot outside the pool.
+ * KDA_LAUNCH_PDL_EARLY_STATE lets the kernel read the slot ids, reset flags and
+ * state tiles early, as for kda_decode_step; x, the window and the counters
+ * are read only after the previous kernel has completed.
+ * n == 0 is a no-op after the host checks.
+ */
+int kda_decode_conv_step(const kda_pool* pool, const kda_conv_window* win, const kda_decode_conv_args* args,
+                         int32_t* dev_status, uint32_t flags, void* stream);
+
+/*
  * Arguments of kda_prefill: the recurrence over packed prompts (the second
  * workload of pull request 2130, What: prefill reads and writes the state
  * through the destination's element type like every other path).  Request r

@@ -37,7 +37,7 @@ KDA_LAUNCH_TEST_WITHHOLD_STATE = 1 << 30  # test hook of the timeout path (inclu
 
 EXPORTED_SYMBOLS = ("kda_build_state_dtype", "kda_pool_check", "kda_state_bytes",
                     "kda_decode_step", "kda_spec_verify", "kda_step", "kda_prefill", "kda_prefill_workspace_bytes",
-                    "kda_prefill_chunked", "kda_prefill_chunked_noalloc", "kda_conv_step",
+                    "kda_prefill_chunked", "kda_prefill_chunked_noalloc", "kda_conv_step", "kda_decode_conv_step",
                     "kda_layout_id", "kda_ckpt_flush", "kda_ckpt_load", "kda_stage_host", "kda_strerror")
 
 
@@ -90,6 +90,15 @@ class ConvArgs(ctypes.Structure):
                 ("cu_seqlens", ctypes.c_void_p), ("conv_slot", ctypes.c_void_p), ("accepted", ctypes.c_void_p),
                 ("reset", ctypes.c_void_p), ("x", ctypes.c_void_p), ("weight", ctypes.c_void_p),
                 ("bias", ctypes.c_void_p), ("y", ctypes.c_void_p)]
+
+
+class DecodeConvArgs(ctypes.Structure):
+    """Mirror of ``struct kda_decode_conv_args`` (include/kda.h)."""
+    _fields_ = [("n", ctypes.c_int32), ("h_qk", ctypes.c_int32), ("kernel_width", ctypes.c_int32),
+                ("activation", ctypes.c_int32), ("slot_ids", ctypes.c_void_p), ("conv_slot", ctypes.c_void_p),
+                ("reset", ctypes.c_void_p), ("x", ctypes.c_void_p), ("weight", ctypes.c_void_p),
+                ("bias", ctypes.c_void_p), ("a", ctypes.c_void_p), ("b", ctypes.c_void_p), ("o", ctypes.c_void_p),
+                ("y", ctypes.c_void_p), ("counters", ctypes.c_void_p)]
 
 
 class HostCopy(ctypes.Structure):
@@ -179,6 +188,9 @@ def _load(state16: bool) -> ctypes.CDLL:
         lib.kda_prefill_chunked_noalloc.argtypes = [P, ctypes.POINTER(PrefillArgs), vp, u32, vp]
         lib.kda_conv_step.restype = ctypes.c_int
         lib.kda_conv_step.argtypes = [ctypes.POINTER(ConvWindowDesc), ctypes.POINTER(ConvArgs), vp, u32, vp]
+        lib.kda_decode_conv_step.restype = ctypes.c_int
+        lib.kda_decode_conv_step.argtypes = [P, ctypes.POINTER(ConvWindowDesc), ctypes.POINTER(DecodeConvArgs),
+                                             vp, u32, vp]
         lib.kda_layout_id.restype = ctypes.c_uint32
         lib.kda_layout_id.argtypes = [P]
         for fn in (lib.kda_ckpt_flush, lib.kda_ckpt_load):
@@ -366,6 +378,47 @@ class KdaLibrary:
         args = ConvArgs(n, total, int(max_t), kw, int(bool(silu)), 0, _ptr(cu_seqlens), _ptr(conv_slot),
                         _ptr(accepted), _ptr(reset), _ptr(x), _ptr(weight), _ptr(bias), _ptr(y))
         self._check(self.kda_conv_step_raw(win, args, _ptr(status), self._stream(stream), flags), "kda_conv_step")
+
+    def kda_decode_conv_step_raw(self, desc: PoolDesc, win: ConvWindowDesc, args: DecodeConvArgs, status, stream,
+                                 flags=0) -> int:
+        return self.lib.kda_decode_conv_step(ctypes.byref(desc), ctypes.byref(win), ctypes.byref(args), status,
+                                             flags, stream)
+
+    def kda_decode_conv_step(self, pool, window, slot_ids, conv_slot, x, weight, a, b, o, status, counters,
+                             bias=None, y=None, reset=None, h_qk=None, silu=True, stream=None, flags=0) -> None:
+        """One decode token per request with the short convolution fused in
+        front of the recurrence (see kda_decode_conv_args in include/kda.h):
+        x [n, C] of the window's dtype with C = 2 h_qk K + HV V (q | k | v
+        channels), window [num_slots, L, C], weight fp32 [C, KW], counters
+        int32 [n, h_qk] (zero; left zero)."""
+        import torch
+        desc = pool_desc(pool)
+        if window.dim() != 3 or window.stride(2) != 1 or window.stride(1) != window.shape[2]:
+            raise ValueError("a conv window pool is a [num_slots, L, C] tensor, dense in [L, C]")
+        ns, L, C = window.shape
+        n, kw = int(slot_ids.shape[0]), int(weight.shape[1])
+        hv, kd, vd = desc.hv, desc.k, desc.v
+        h_qk = hv if h_qk is None else int(h_qk)
+        _expect("slot_ids", slot_ids, (n,), (torch.int32,))
+        _expect("conv_slot", conv_slot, (n,), (torch.int32,))
+        _expect("x", x, (n, C), (window.dtype,))
+        _expect("weight", weight, (C, kw), (torch.float32,))
+        _expect("a", a, (n, hv, kd), (torch.float32,))
+        _expect("b", b, (n, hv), (torch.float32,))
+        _expect("o", o, (n, hv, vd), (torch.float32,))
+        _expect("counters", counters, (n, h_qk), (torch.int32,))
+        _expect("status", status, (1,), (torch.int32,))
+        if bias is not None:
+            _expect("bias", bias, (C,), (torch.float32,))
+        if y is not None:
+            _expect("y", y, (n, C), (window.dtype,))
+        if reset is not None:
+            _expect("reset", reset, (n,), (torch.uint8,))
+        win = ConvWindowDesc(window.data_ptr(), _dtype_code(window.dtype), C, L, 0, ns, window.stride(0))
+        args = DecodeConvArgs(n, h_qk, kw, int(bool(silu)), _ptr(slot_ids), _ptr(conv_slot), _ptr(reset), _ptr(x),
+                              _ptr(weight), _ptr(bias), _ptr(a), _ptr(b), _ptr(o), _ptr(y), _ptr(counters))
+        self._check(self.kda_decode_conv_step_raw(desc, win, args, _ptr(status), self._stream(stream), flags),
+                    "kda_decode_conv_step")
 
     def kda_stage_host_raw(self, copies, stream, flags=0) -> int:
         """copies: a list of (dst device address, src pinned host address, bytes)."""

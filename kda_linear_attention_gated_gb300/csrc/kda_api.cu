@@ -261,13 +261,15 @@ int launch_scan(const kda::StepParams& prm, const uint8_t* ws, int64_t heads, in
     return cudaLaunchKernelEx(&cfg, scan, prm, ws) == cudaSuccess ? KDA_OK : KDA_ERR_LAUNCH;
 }
 
-template <typename QT, bool FULLK, int TPC>
+template <typename QT, bool FULLK, int TPC, bool CONV>
 int launch_decode_k(const kda_pool* pool, const kda::StepParams& prm, cudaStream_t stream) {
     constexpr int BV = KDA_DEC_BV, NT = KDA_DEC_NT;
     constexpr size_t smem = kda::decode_smem_bytes<state_t, BV, NT, (int)sizeof(QT), TPC>();
     constexpr int MINB = TPC > 1 ? KDA_DEC_MINB2 : KDA_DEC_MINB;
-    constexpr bool KEEP = (TPC > 1 ? KDA_DEC_KEEP2 : KDA_DEC_KEEP) != 0;
-    auto kernel = kda::kda_decode_kernel<state_t, QT, BV, NT, MINB, KEEP, FULLK, TPC>;
+    // the fused convolution's two-tile kernel has no room for the kept words
+    // under the 6-CTA cap (80 registers): it reads the rows twice
+    constexpr bool KEEP = (TPC > 1 ? KDA_DEC_KEEP2 : KDA_DEC_KEEP) != 0 && !CONV;
+    auto kernel = kda::kda_decode_kernel<state_t, QT, BV, NT, MINB, KEEP, FULLK, TPC, CONV>;
     // CTAs: TPC column blocks each
     const int64_t tiles = (int64_t)prm.n * prm.hv * (((prm.v + BV - 1) / BV + TPC - 1) / TPC);
     if (tiles > 0x7fffffffLL) return KDA_ERR_SHAPE;
@@ -290,15 +292,15 @@ int launch_decode_k(const kda_pool* pool, const kda::StepParams& prm, cudaStream
 
 // K = 128 (the configured models' key dimension) gets a build without the
 // per-row bound checks.
-template <typename QT, int TPC>
+template <typename QT, int TPC, bool CONV>
 int launch_decode_t(const kda_pool* pool, const kda::StepParams& prm, cudaStream_t stream) {
-    return prm.k == kda::KMAX ? launch_decode_k<QT, true, TPC>(pool, prm, stream)
-                              : launch_decode_k<QT, false, TPC>(pool, prm, stream);
+    return prm.k == kda::KMAX ? launch_decode_k<QT, true, TPC, CONV>(pool, prm, stream)
+                              : launch_decode_k<QT, false, TPC, CONV>(pool, prm, stream);
 }
 
 // KDA_DEC_TPC tiles per CTA when the one-tile grid is more than one wave of
-// the one-tile kernel, else one.
-template <typename QT>
+// the one-tile kernel, else one.  CONV: the decode with the fused convolution.
+template <typename QT, bool CONV = false>
 int launch_decode(const kda_pool* pool, const kda::StepParams& prm, cudaStream_t stream) {
     constexpr int TPC = KDA_DEC_TPC;
     if constexpr (TPC > 1) {
@@ -310,9 +312,9 @@ int launch_decode(const kda_pool* pool, const kda::StepParams& prm, cudaStream_t
                                      kda::kda_decode_kernel<state_t, QT, BV, NT, KDA_DEC_MINB, KDA_DEC_KEEP != 0, true>),
                                  NT, smem, &occ, &sms);
         if (rc != KDA_OK) return rc;
-        if (tiles > (int64_t)occ * sms) return launch_decode_t<QT, TPC>(pool, prm, stream);
+        if (tiles > (int64_t)occ * sms) return launch_decode_t<QT, TPC, CONV>(pool, prm, stream);
     }
-    return launch_decode_t<QT, 1>(pool, prm, stream);
+    return launch_decode_t<QT, 1, CONV>(pool, prm, stream);
 }
 
 template <typename QT, bool WIDE>
@@ -436,6 +438,7 @@ kda::StepParams make_params(const kda_pool* pool, const int32_t* init_slot,
     prm.mode = 0;
     prm.total = n * t;
     prm.final_slot = nullptr;
+    prm.conv = kda::StepParams::Conv{};
     return prm;
 }
 
@@ -738,6 +741,56 @@ int kda_conv_step(const kda_conv_window* win, const kda_conv_args* args, int32_t
             break;
     }
     return err == cudaSuccess ? KDA_OK : KDA_ERR_LAUNCH;
+}
+
+int kda_decode_conv_step(const kda_pool* pool, const kda_conv_window* win, const kda_decode_conv_args* args,
+                         int32_t* dev_status, uint32_t flags, void* stream) {
+    if (win == nullptr || args == nullptr) return KDA_ERR_NULL;
+    const kda_decode_conv_args& g = *args;
+    int rc = check_pool_for_build(pool);
+    if (rc != KDA_OK) return rc;
+    const int es = elem_size(win->dtype);
+    if (es == 0) return KDA_ERR_DTYPE_UNSUPPORTED;
+    if (win->reserved != 0 || g.n < 0 || (g.activation != 0 && g.activation != 1)) return KDA_ERR_ARG;
+    if (flags & ~(uint32_t)(KDA_LAUNCH_PDL | KDA_LAUNCH_PDL_EARLY_STATE)) return KDA_ERR_ARG;
+    // one token a request keeps state_len - 1 old entries, all within the
+    // kernel_width - 1 history it reads
+    if (g.h_qk < 1 || pool->hv % g.h_qk != 0 || g.kernel_width < 1 || g.kernel_width > kda::DCONV_KW_MAX ||
+        win->state_len < g.kernel_width - 1 || win->state_len > g.kernel_width || win->num_slots < 1 ||
+        (int64_t)win->channels != 2LL * g.h_qk * pool->k + (int64_t)pool->hv * pool->v ||
+        win->slot_stride < (int64_t)win->state_len * win->channels)
+        return KDA_ERR_SHAPE;
+    if (g.n == 0) return KDA_OK;
+    if (!win->base || !g.slot_ids || !g.conv_slot || !g.x || !g.weight || !g.a || !g.b || !g.o ||
+        !g.counters || !dev_status)
+        return KDA_ERR_NULL;
+    if (!aligned(win->base, es) || !aligned(g.x, es) || (g.y && !aligned(g.y, es)) || !aligned(g.slot_ids, 4) ||
+        !aligned(g.conv_slot, 4) || !aligned(g.weight, 4) || (g.bias && !aligned(g.bias, 4)) ||
+        !aligned(g.a, 16) || !aligned(g.b, 4) || !aligned(g.o, 4) || !aligned(g.counters, 4) ||
+        !aligned(dev_status, 4))
+        return KDA_ERR_ALIGN;
+    kda::StepParams prm = make_params(pool, g.slot_ids, nullptr, g.reset, g.n, 1, nullptr, nullptr, nullptr,
+                                      g.a, g.b, g.o, dev_status, flags);
+    prm.hqk = g.h_qk;
+    prm.conv.window = win->base;
+    prm.conv.num_slots = win->num_slots;
+    prm.conv.slot_stride = win->slot_stride;
+    prm.conv.C = win->channels;
+    prm.conv.L = win->state_len;
+    prm.conv.KW = g.kernel_width;
+    prm.conv.silu = g.activation;
+    prm.conv.slot = g.conv_slot;
+    prm.conv.x = g.x;
+    prm.conv.w = g.weight;
+    prm.conv.bias = g.bias;
+    prm.conv.y = g.y;
+    prm.conv.counters = g.counters;
+    const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    switch (win->dtype) {
+        case KDA_F32: return launch_decode<float, true>(pool, prm, st);
+        case KDA_F16: return launch_decode<__half, true>(pool, prm, st);
+        default: return launch_decode<__nv_bfloat16, true>(pool, prm, st);
+    }
 }
 
 static_assert(kda::STAGE_MAX_COPIES == KDA_STAGE_MAX_COPIES, "staging copies per launch");

@@ -51,6 +51,21 @@ struct StepParams {
     int total;                // rows of the packed token arrays (bounds cu)
     const int32_t* final_slot; // [n] or nullptr: prefill, only the state after the last token is
                               // stored, to final_slot[n] (negative: not stored); no snapshots
+    // The fused short convolution of a decode step (the conv-decode kernel only):
+    // q, k and v are its outputs y, of QT, computed from x and the window.
+    struct Conv {
+        void* window;             // [num_slots] x [L][C] of QT, slot_stride apart
+        int64_t num_slots;
+        int64_t slot_stride;      // elements
+        int C, L, KW;             // channels, window entries, kernel width
+        int silu;
+        const int32_t* slot;      // [n]: window slot of request n
+        const void* x;            // [n][C] of QT
+        const float* w;           // [C][KW]
+        const float* bias;        // [C] or nullptr
+        void* y;                  // [n][C] of QT or nullptr
+        int32_t* counters;        // [n][hqk]: reads of a q/k head's window so far
+    } conv;
 };
 
 // A negative initial slot marks a padding request (nothing read or stored,

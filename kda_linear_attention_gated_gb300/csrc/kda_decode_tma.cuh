@@ -47,8 +47,51 @@
 #pragma once
 
 #include "kda_common.cuh"
+#include "kda_conv.cuh"
 
 namespace kda {
+
+// Kernel widths of the decode step's fused convolution: 1 .. 4 (a history of
+// up to three entries, held in registers).
+constexpr int DCONV_KW_MAX = 4;
+constexpr int DCONV_H = DCONV_KW_MAX - 1;
+
+// The fused short convolution of a decode step (CONV), one channel: history
+// entries h_0 .. h_(KW-2) of the window at W[i C] (zero on reset) and the
+// token's input xr, weighed by w[0 .. KW-1] (w[KW-1] the input), plus the
+// bias; SiLU when silu; y rounded to QT.  The same fmaf chain as the conv
+// kernel, so y is bit-identical to kda_conv_step's.
+template <typename QT>
+__device__ __forceinline__ QT conv_channel(const QT* W, int C, int KW, bool rst, QT xr, const float* w,
+                                           float bias, int silu) {
+    float h[DCONV_H];
+#pragma unroll
+    for (int i = 0; i < DCONV_H; ++i) h[i] = !rst && i < KW - 1 ? to_f32(W[(int64_t)i * C]) : 0.f;
+    float s = bias;
+#pragma unroll
+    for (int i = 0; i < DCONV_H; ++i)
+        if (i < KW - 1) s = fmaf(__ldg(w + i), h[i], s);
+    s = fmaf(__ldg(w + KW - 1), to_f32(xr), s);
+    QT out;
+    conv_round(silu ? silu_fast(s) : s, out);
+    return out;
+}
+
+// The window of one channel after a one-token step: its last L - 1 history
+// entries (h_(KW-L+e) -> entry e; L is KW - 1 or KW; zero on reset) followed
+// by the input.  Entries move down in ascending order, so each is read before
+// it is overwritten; only the channel's one writer runs this, after every
+// reader of the old entries has read them.
+template <typename QT>
+__device__ __forceinline__ void conv_window_store(QT* W, int C, int L, int KW, bool rst, QT xr) {
+    const int shift = KW - L;  // 1, or 0 when L == KW (entry e keeps h_e)
+    QT zero;
+    conv_round(0.f, zero);
+#pragma unroll
+    for (int e = 0; e < DCONV_H; ++e)
+        if (e < L - 1) W[(int64_t)e * C] = rst ? zero : W[(int64_t)(e + shift) * C];
+    if (L >= 1) W[(int64_t)(L - 1) * C] = xr;
+}
 
 // TPC: tiles per CTA, adjacent column blocks of one (request, value head).
 // They share the inputs and the gates, and their state boxes are all in flight
@@ -93,7 +136,7 @@ constexpr size_t decode_smem_bytes() {
     return TPC * SH::TILE_BYTES + SH::WORK_BYTES + SH::RED_BYTES + 8 * (TPC + 1);
 }
 
-template <typename ST, typename QT, int BV, int NT, int MINB, bool KEEP, bool FULLK, int TPC = 1>
+template <typename ST, typename QT, int BV, int NT, int MINB, bool KEEP, bool FULLK, int TPC = 1, bool CONV = false>
 __global__ void __launch_bounds__(NT, MINB)
 kda_decode_kernel(const __grid_constant__ CUtensorMap tmap, const StepParams p) {
     using SH = DecodeShape<ST, BV, NT, (int)sizeof(QT), TPC>;
@@ -145,7 +188,9 @@ kda_decode_kernel(const __grid_constant__ CUtensorMap tmap, const StepParams p) 
     const bool col_ok = col >= 0 && col < p.num_cols;
     const int32_t slot = col_ok ? p.init_slot[(int64_t)n * p.init_stride + col] : -1;
     const bool pad = col_ok && slot < 0 && (p.mode & MODE_PADDING) != 0;
-    const bool valid = col_ok && slot >= 0 && slot < p.num_slots;
+    int32_t cslot = 0;  // the fused convolution's window slot
+    if constexpr (CONV) cslot = p.conv.slot[n];
+    const bool valid = col_ok && slot >= 0 && slot < p.num_slots && (!CONV || (cslot >= 0 && cslot < p.conv.num_slots));
     const bool rst = valid && p.reset != nullptr && p.reset[n] != 0;
     if (tid == 0) {
         for (int j = 0; j <= TPC; ++j) mbar_init(bar_st + j, 1);
@@ -171,32 +216,106 @@ kda_decode_kernel(const __grid_constant__ CUtensorMap tmap, const StepParams p) 
     if (tid == 0) {
         const uint32_t qk_bytes = (uint32_t)p.k * qes;
         const uint32_t v_bytes = (uint32_t)min(TPC * BV, p.v - cb0 * BV) * qes;
-        mbar_arrive_expect_tx(bar_in, 2 * qk_bytes + (uint32_t)p.k * 4 + v_bytes);
         const int64_t r64 = r;
-        const int64_t rqk = (int64_t)n * p.hqk + h / (p.hv / p.hqk);  // grouped q/k heads
-        bulk_load(in + SH::IN_Q, static_cast<const char*>(p.q) + rqk * qk_bytes, qk_bytes, bar_in);
-        bulk_load(in + SH::IN_K, static_cast<const char*>(p.kk) + rqk * qk_bytes, qk_bytes, bar_in);
+        if constexpr (CONV) {  // q, k and v come from the convolution below
+            mbar_arrive_expect_tx(bar_in, (uint32_t)p.k * 4);
+        } else {
+            mbar_arrive_expect_tx(bar_in, 2 * qk_bytes + (uint32_t)p.k * 4 + v_bytes);
+            const int64_t rqk = (int64_t)n * p.hqk + h / (p.hv / p.hqk);  // grouped q/k heads
+            bulk_load(in + SH::IN_Q, static_cast<const char*>(p.q) + rqk * qk_bytes, qk_bytes, bar_in);
+            bulk_load(in + SH::IN_K, static_cast<const char*>(p.kk) + rqk * qk_bytes, qk_bytes, bar_in);
+            bulk_load(in + SH::IN_V, static_cast<const char*>(p.vv) + (r64 * p.v + (int64_t)cb0 * BV) * qes,
+                      v_bytes, bar_in);
+        }
         bulk_load(in + SH::IN_A, p.a + r64 * p.k, (uint32_t)p.k * 4, bar_in);
-        bulk_load(in + SH::IN_V, static_cast<const char*>(p.vv) + (r64 * p.v + (int64_t)cb0 * BV) * qes,
-                  v_bytes, bar_in);
     }
     const float b = __ldg(p.b + r);
+
+    // The fused short convolution (CONV): thread i < K computes q and k of key
+    // row i, thread e < TPC BV value column e of the CTA's tiles, each from its
+    // channel's window and input (all read after the previous kernel is done).
+    // A value column's window belongs to this CTA alone, which rewrites it.  A
+    // q/k channel's window is read by every CTA of the request's value heads
+    // that share the q/k head: each counts its read (once all its threads hold
+    // the values they read) and the one that makes the count complete writes
+    // the new entries and puts the count back to zero.  No CTA waits for
+    // another.
+    constexpr int NVE = (TPC * BV + NT - 1) / NT;  // value columns per thread
+    float cq = 0.f, ck = 0.f, cvv[NVE];
+#pragma unroll
+    for (int e = 0; e < NVE; ++e) cvv[e] = 0.f;
+    if constexpr (CONV) {
+        const auto& cp = p.conv;
+        const int grp = p.hv / p.hqk, hq = h / grp;
+        const bool row = tid < p.k;
+        const int chq = hq * p.k + tid, chk = (p.hqk + hq) * p.k + tid;  // this row's q and k channels
+        // the window and input of channel c (pointers rebuilt from the
+        // parameters where needed, so that none stays live in a register)
+        auto win = [&](int c) { return static_cast<QT*>(cp.window) + (int64_t)cslot * cp.slot_stride + c; };
+        auto xin = [&](int c) { return static_cast<const QT*>(cp.x)[(int64_t)n * cp.C + c]; };
+        auto conv_y = [&](int c) {
+            return conv_channel(win(c), cp.C, cp.KW, rst, xin(c), cp.w + (int64_t)c * cp.KW,
+                                cp.bias != nullptr ? __ldg(cp.bias + c) : 0.f, cp.silu);
+        };
+        if (row) {
+            const QT yq = conv_y(chq), yk = conv_y(chk);
+            cq = to_f32(yq);
+            ck = to_f32(yk);
+            if (cp.y != nullptr && h % grp == 0 && cb0 == 0) {  // one writer of y per q/k channel
+                static_cast<QT*>(cp.y)[(int64_t)n * cp.C + chq] = yq;
+                static_cast<QT*>(cp.y)[(int64_t)n * cp.C + chk] = yk;
+            }
+        }
+#pragma unroll
+        for (int e = 0; e < NVE; ++e) {
+            const int c = tid + e * NT, col = cb0 * BV + c;
+            if (c < TPC * BV && col < p.v) {
+                const int chv = 2 * p.hqk * p.k + h * p.v + col;
+                const QT yv = conv_y(chv);
+                cvv[e] = to_f32(yv);
+                if (cp.y != nullptr) static_cast<QT*>(cp.y)[(int64_t)n * cp.C + chv] = yv;
+                conv_window_store(win(chv), cp.C, cp.L, cp.KW, rst, xin(chv));
+            }
+        }
+        const int readers = grp * ct;
+        bool last = true;
+        if (readers > 1) {
+            // The predicate uses the values read, so every thread's reads of
+            // the window have returned before thread 0 counts this CTA's.
+            const bool never = row && (__float_as_uint(cq) ^ __float_as_uint(ck)) == 0x7fc00001u;
+            __syncthreads_or(never ? 1 : 0);
+            int* flag = reinterpret_cast<int*>(red) + 3;  // unused word of the norm area
+            if (tid == 0) {
+                int* cnt = cp.counters + (int64_t)n * p.hqk + hq;
+                const bool done = atomicAdd(cnt, 1) == readers - 1;
+                if (done) atomicExch(cnt, 0);
+                *flag = done ? 1 : 0;
+            }
+            __syncthreads();
+            last = *flag != 0;
+        }
+        if (row && last) {
+            conv_window_store(win(chq), cp.C, cp.L, cp.KW, rst, xin(chq));
+            conv_window_store(win(chk), cp.C, cp.L, cp.KW, rst, xin(chk));
+        }
+    }
     __syncthreads();  // the barriers are initialised before anyone waits on them
     // The gates need only the small inputs, so they are worked out while the
     // state tile is still in flight.
     const bool ok = mbar_wait(bar_in, 0);
 
     // (1) gates: thread tid < K owns row tid.
-    float kt = 0.f, qt = 0.f, alpha = 0.f, vt_ = 0.f;
+    float kt = 0.f, qt = 0.f, alpha = 0.f;
     float vts[(TPC * BV + NT - 1) / NT];
 #pragma unroll
     for (int e = 0; e < (TPC * BV + NT - 1) / NT; ++e) {
         const int c = tid + e * NT;
-        vts[e] = ok && c < TPC * BV && c < p.v - cb0 * BV ? to_f32(reinterpret_cast<const QT*>(in + SH::IN_V)[c]) : 0.f;
+        vts[e] = ok && c < TPC * BV && c < p.v - cb0 * BV
+                     ? (CONV ? cvv[e] : to_f32(reinterpret_cast<const QT*>(in + SH::IN_V)[c])) : 0.f;
     }
     if (ok && tid < p.k) {
-        kt = to_f32(reinterpret_cast<const QT*>(in + SH::IN_K)[tid]);
-        qt = to_f32(reinterpret_cast<const QT*>(in + SH::IN_Q)[tid]);
+        kt = CONV ? ck : to_f32(reinterpret_cast<const QT*>(in + SH::IN_K)[tid]);
+        qt = CONV ? cq : to_f32(reinterpret_cast<const QT*>(in + SH::IN_Q)[tid]);
         const bool scaled = p.a_log != nullptr;
         alpha = gate_alpha(reinterpret_cast<const float*>(in + SH::IN_A)[tid], scaled,
                            scaled ? expf(__ldg(p.a_log + h)) : 1.f,

@@ -271,6 +271,53 @@ def make_conv(n=8, t=5, t_lens=None, channels=4608, kw=4, num_spec=4, num_slots=
 
 
 @dataclass
+class DecodeConvInputs:
+    """CPU tensors of one decode step with the short convolution fused in front."""
+    pool: torch.Tensor                 # [num_slots, HV, K, V] fp32 or fp16
+    slot_ids: torch.Tensor             # int32 [N]
+    window: torch.Tensor               # [num_wslots, L, C] fp32, fp16 or bf16
+    conv_slot: torch.Tensor            # int32 [N]
+    x: torch.Tensor                    # [N, C] of the window's dtype: q | k | v channels
+    weight: torch.Tensor               # fp32 [C, KW]
+    bias: torch.Tensor | None          # fp32 [C]
+    a: torch.Tensor                    # fp32 [N, HV, K]
+    b: torch.Tensor                    # fp32 [N, HV]
+    reset: torch.Tensor | None = None  # uint8 [N]
+    h_qk: int = 12
+    meta: dict = field(default_factory=dict)
+
+    def to(self, device) -> "DecodeConvInputs":
+        mv = lambda t: None if t is None else t.to(device)  # noqa: E731
+        return DecodeConvInputs(mv(self.pool), mv(self.slot_ids), mv(self.window), mv(self.conv_slot), mv(self.x),
+                                mv(self.weight), mv(self.bias), mv(self.a), mv(self.b), mv(self.reset), self.h_qk,
+                                dict(self.meta))
+
+
+def make_decode_conv(n=64, hv=12, h_qk=12, k=128, v=128, kw=4, L=3, num_slots=256, num_wslots=256,
+                     state_dtype=torch.float32, dtype=torch.bfloat16, seed=11, reset_p=0.0,
+                     bias=True) -> DecodeConvInputs:
+    """One decode token for n requests with the short convolution in front:
+    channels C = 2 h_qk k + hv v; the state pool as in make_decode; the window
+    (L entries) and x ~ N(0, 1) in dtype, weight ~ N(0, 1 / kw), bias ~
+    N(0, 0.1^2), as in make_conv; a, b ~ N(0, 1); n distinct state slots and
+    n distinct window slots."""
+    g = torch.Generator().manual_seed(seed)
+    C = 2 * h_qk * k + hv * v
+    P = make_pool(g, num_slots, hv, k, v, state_dtype)
+    slots = torch.randperm(num_slots, generator=g)[:n].to(torch.int32)
+    W = _randn(g, (num_wslots, L, C), dtype)
+    cslots = torch.randperm(num_wslots, generator=g)[:n].to(torch.int32)
+    x = _randn(g, (n, C), dtype)
+    w = _randn(g, (C, kw), std=1.0 / kw ** 0.5)
+    bv = _randn(g, (C,), std=0.1) if bias else None
+    a = _randn(g, (n, hv, k))
+    b = _randn(g, (n, hv))
+    reset = (torch.rand((n,), generator=g) < reset_p).to(torch.uint8) if reset_p > 0 else None
+    return DecodeConvInputs(P, slots, W, cslots, x, w, bv, a, b, reset, h_qk,
+                            dict(kind="decode_conv", n=n, hv=hv, h_qk=h_qk, k=k, v=v, kw=kw, L=L, seed=seed))
+
+
+@dataclass
 class PrefillInputs:
     """CPU tensors of one prefill call over packed prompts."""
     pool: torch.Tensor

@@ -211,6 +211,50 @@ def test_conv_step_refusals_before_any_launch(libs):
     assert call(win(), args(n=0, total=0)) == kda.KDA_OK
 
 
+def test_decode_conv_step_refusals_before_any_launch(libs):
+    """kda_decode_conv_step's host checks (include/kda.h, kda_decode_conv_args):
+    the pool's, the window's, and the channel count tying the two together."""
+    L = libs[torch.float32]
+    P = 0x7F0000100000
+    C = 2 * 12 * 128 + 12 * 128  # q | k | v channels of hv = h_qk = 12, K = V = 128
+
+    def win(**kw):
+        f = dict(base=P, dtype=kda.KDA_BF16, channels=C, state_len=3, reserved=0, num_slots=64, slot_stride=3 * C)
+        f.update(kw)
+        return kda.ConvWindowDesc(**f)
+
+    def args(**kw):
+        f = dict(n=8, h_qk=12, kernel_width=4, activation=1, slot_ids=P, conv_slot=P, reset=None, x=P, weight=P,
+                 bias=None, a=P, b=P, o=P, y=None, counters=P)
+        f.update(kw)
+        return kda.DecodeConvArgs(**f)
+
+    call = lambda w, a, d=None, status=P, flags=0: L.kda_decode_conv_step_raw(  # noqa: E731
+        d or desc(), w, a, status, None, flags)
+    assert L.lib.kda_decode_conv_step(ctypes.byref(desc()), None, ctypes.byref(args()), P, 0, None) == kda.KDA_ERR_NULL
+    assert call(win(), args(), d=desc(kda.KDA_F16)) == kda.KDA_ERR_DTYPE_MISMATCH  # the fp32 build
+    assert call(win(dtype=7), args()) == kda.KDA_ERR_DTYPE_UNSUPPORTED
+    assert call(win(channels=C - 1), args()) == kda.KDA_ERR_SHAPE                   # not q | k | v
+    assert call(win(channels=2 * 4 * 128 + 12 * 128), args()) == kda.KDA_ERR_SHAPE  # h_qk = 4 laid out, 12 given
+    assert call(win(channels=2 * 4 * 128 + 12 * 128), args(h_qk=4, n=0)) == kda.KDA_OK  # grouped: accepted
+    assert call(win(), args(h_qk=5)) == kda.KDA_ERR_SHAPE                          # does not divide hv
+    assert call(win(), args(kernel_width=5)) == kda.KDA_ERR_SHAPE                  # widths 1 .. 4
+    assert call(win(state_len=2), args()) == kda.KDA_ERR_SHAPE                      # fewer than kernel - 1
+    assert call(win(state_len=5, slot_stride=5 * C), args()) == kda.KDA_ERR_SHAPE   # more than one step keeps
+    assert call(win(slot_stride=3 * C - 1), args()) == kda.KDA_ERR_SHAPE
+    assert call(win(), args(activation=2)) == kda.KDA_ERR_ARG
+    assert call(win(reserved=1), args()) == kda.KDA_ERR_ARG
+    assert call(win(), args(n=-1)) == kda.KDA_ERR_ARG
+    assert call(win(), args(), flags=kda.KDA_LAUNCH_TEST_WITHHOLD_STATE) == kda.KDA_ERR_ARG
+    for name in ("slot_ids", "conv_slot", "x", "weight", "a", "b", "o", "counters"):
+        assert call(win(), args(**{name: None})) == kda.KDA_ERR_NULL, name
+    assert call(win(), args(a=P + 4)) == kda.KDA_ERR_ALIGN    # a moves by 16-byte bulk copy
+    assert call(win(), args(x=P + 1)) == kda.KDA_ERR_ALIGN
+    assert call(win(), args(y=P + 1)) == kda.KDA_ERR_ALIGN
+    assert call(win(), args(counters=P + 2)) == kda.KDA_ERR_ALIGN
+    assert call(win(), args(n=0)) == kda.KDA_OK               # nothing to do: no launch
+
+
 def test_layout_id_names_dtype_and_shape(libs):
     """Pull request 2130, What: the checkpoint layout id names the dtype, so an
     fp16 build cannot read an fp32 build's checkpoint images."""
