@@ -351,7 +351,7 @@ def main():
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer measurement")
     ap.add_argument("--workload", choices=("decode_f32", "decode_f16"), default="decode_f32",
                     help="headline workload: the decode step on an fp32 pool (the metric's) or fp16 pool")
-    ap.add_argument("--case", choices=("verify_f16", "sweep", "prefill", "aux"), default=None,
+    ap.add_argument("--case", choices=("verify_f16", "sweep", "prefill", "aux", "conv_decode"), default=None,
                     help="time one secondary case alone and print its line (profiling runs)")
     ap.add_argument("--soak-seconds", type=float, default=1.0,
                     help="minimum untimed load before timing (clocks ramp; 0 under a profiler)")
@@ -544,6 +544,9 @@ def main():
                    "ckpt_load_fp32_n64": bench_ckpt(kda, workloads, torch, peak, load=True),
                    "conv_step_n64_t5_bf16": bench_conv(kda, workloads, torch, peak),
                    "copy_floor": bench_copy_floor(kda, torch, l2, peak)}
+        elif args.case == "conv_decode":
+            res = {f"decode_conv_{nm}_n64": bench_decode_conv(kda, workloads, torch, l2, peak, sd)
+                   for nm, sd in (("fp32", torch.float32), ("fp16", torch.float16))}
         elif args.case == "prefill":
             res = {f"prefill_{n}x{t}_fp16{'_chunked' if c else ''}": bench_prefill(kda, workloads, torch, n, t, c)
                    for c in (False, True) for n, t in ((1, 8192), (8, 1024), (64, 128))}
@@ -592,6 +595,8 @@ def main():
         extra["ckpt_flush_fp32_n64"] = bench_ckpt(kda, workloads, torch, peak)
         extra["ckpt_load_fp32_n64"] = bench_ckpt(kda, workloads, torch, peak, load=True)
         extra["conv_step_n64_t5_bf16"] = bench_conv(kda, workloads, torch, peak)
+        for sd_name, sd in (("fp32", torch.float32), ("fp16", torch.float16)):
+            extra[f"decode_conv_{sd_name}_n64"] = bench_decode_conv(kda, workloads, torch, l2, peak, sd)
         extra["copy_floor"] = bench_copy_floor(kda, torch, l2, peak)
         extra["prefill_8x1024_fp16"] = bench_prefill(kda, workloads, torch, 8, 1024)
         extra["prefill_8x1024_fp16_chunked"] = bench_prefill(kda, workloads, torch, 8, 1024, True)
@@ -853,6 +858,69 @@ def bench_conv(kda, workloads, torch, peak, replays=480):
             "us_per_call": round(us, 3), "gbs": round(byt / (us * 1e-6) / 1e9, 1),
             "frac_of_peak": round(byt / (us * 1e-6) / 1e9 / peak, 4), "bytes_per_call": byt,
             "launch": f"{GRAPH_TIMED} ({n_timed}, over {R} sets); flags KDA_LAUNCH_PDL|KDA_LAUNCH_PDL_EARLY_STATE"}
+
+
+def bench_decode_conv(kda, workloads, torch, l2, peak, state_dtype, replays=400):
+    """The decode step with the short convolution fused in front
+    (kda_decode_conv_step) at the headline shape: N=64 x HV=12, K=V=128, q/k/v
+    from a bf16 conv of width 4 over a 3-entry window (C = 4608 channels).
+    Beside it, the same work as two launches: kda_conv_step (one token a
+    request) then kda_decode_step, both with PDL and early reads.  That
+    decode reads q/k/v buffers of the decode's own layout; turning the conv's
+    [N][C] outputs into them would cost a copy or three conv launches, which
+    is not counted, so the two-launch figure is a lower bound.  Rotating
+    state pools past L2.  Algorithmic bytes: the state read and written, x
+    read (the q/k/v bytes), the window's history read and new entries
+    written, o written (a, b, weights not counted, as for the decode)."""
+    lib = kda.KdaLibrary(state_dtype)
+    n, hv, K, V, kw, L = 64, 12, 128, 128, 4, 3
+    es = 4 if state_dtype == torch.float32 else 2
+    pool_bytes = n * hv * K * V * es
+    R = max(4, math.ceil(4 * l2 / pool_bytes) + 1)
+    sets = [workloads.make_decode_conv(n=n, num_slots=n, num_wslots=n, state_dtype=state_dtype, seed=90 + i)
+            .to("cuda") for i in range(R)]
+    C = sets[0].x.shape[1]
+    os_ = [torch.empty(n, hv, V, device="cuda") for _ in range(R)]
+    ys = [torch.empty_like(d.x) for d in sets]
+    qkv = [(torch.empty(n, hv, K, dtype=torch.bfloat16, device="cuda").normal_(),
+            torch.empty(n, hv, K, dtype=torch.bfloat16, device="cuda").normal_(),
+            torch.empty(n, hv, V, dtype=torch.bfloat16, device="cuda").normal_()) for _ in range(R)]
+    counters = torch.zeros(n, hv, dtype=torch.int32, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    stream = torch.cuda.Stream()
+    flags = kda.KDA_LAUNCH_PDL | kda.KDA_LAUNCH_PDL_EARLY_STATE
+
+    def fused(i):
+        d = sets[i % R]
+        lib.kda_decode_conv_step(d.pool, d.window, d.slot_ids, d.conv_slot, d.x, d.weight, d.a, d.b, os_[i % R],
+                                 status, counters, bias=d.bias, flags=flags)
+
+    def two(i):
+        d, (q, k, v) = sets[i % R], qkv[i % R]
+        lib.kda_conv_step(d.window, d.conv_slot, d.x, d.weight, ys[i % R], status, bias=d.bias, max_t=1,
+                          flags=flags)
+        lib.kda_decode_step(d.pool, d.slot_ids, q, k, v, d.a, d.b, os_[i % R], status, flags=flags)
+    with torch.cuda.stream(stream):
+        fused(0)
+        two(0)
+    n_timed = R * max(1, replays // R)
+    us = graph_timed(torch, stream, fused, n_timed) * 1e3 / n_timed
+    us2 = graph_timed(torch, stream, two, n_timed) * 1e3 / n_timed
+    if int(status.item()) != 0 or int(counters.abs().sum().item()) != 0:
+        raise RuntimeError(f"device status {int(status.item())}")
+    byt = 2 * pool_bytes + n * C * 2 * (1 + (kw - 1) + L) + n * hv * V * 4
+    del sets, ys, qkv, os_
+    torch.cuda.empty_cache()
+    sd = "fp32" if state_dtype == torch.float32 else "fp16"
+    return {"workload": f"decode step with the conv fused in front, N=64 x HV=12, K=V=128, {sd} pool, "
+                        f"bf16 conv window of 3 entries, width 4, C=4608",
+            "us_per_step": round(us, 3), "gbs": round(byt / (us * 1e-6) / 1e9, 1),
+            "frac_of_peak": round(byt / (us * 1e-6) / 1e9 / peak, 4), "bytes_per_step": byt,
+            "two_launches_us": round(us2, 3),
+            "two_launches": "kda_conv_step then kda_decode_step, each PDL with early reads (y's relayout into "
+                            "the decode's q/k/v not counted)",
+            "launch": f"{GRAPH_TIMED} ({n_timed} steps, over {R} pool/window sets); flags "
+                      "KDA_LAUNCH_PDL|KDA_LAUNCH_PDL_EARLY_STATE"}
 
 
 def bench_step(kda, workloads, torch, l2, peak, n=32, t=8, replays=400):

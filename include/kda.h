@@ -382,9 +382,12 @@ typedef struct kda_decode_conv_args {
  * 4), _ARG (negative n, activation not 0/1, flags other than the PDL bits).
  * Device checks (in *dev_status, the request skipped whole, its counters left
  * alone): KDA_ERR_SLOT_RANGE for a slot id or window slot outside the pool.
- * KDA_LAUNCH_PDL_EARLY_STATE lets the kernel read the slot ids, reset flags and
- * state tiles early, as for kda_decode_step; x, the window and the counters
- * are read only after the previous kernel has completed.
+ * KDA_LAUNCH_PDL_EARLY_STATE lets the kernel read the slot ids, reset flags,
+ * state tiles, weights, bias and the window's history entries before the
+ * previous kernel has completed (which must then step neither this pool nor
+ * this window); x is read, and the window, counters, y and o are written,
+ * only after it has completed.  The window is rewritten at the end of each
+ * CTA's work, off the recurrence's path.
  * n == 0 is a no-op after the host checks.
  */
 int kda_decode_conv_step(const kda_pool* pool, const kda_conv_window* win, const kda_decode_conv_args* args,

@@ -56,22 +56,42 @@ namespace kda {
 constexpr int DCONV_KW_MAX = 4;
 constexpr int DCONV_H = DCONV_KW_MAX - 1;
 
-// The fused short convolution of a decode step (CONV), one channel: history
-// entries h_0 .. h_(KW-2) of the window at W[i C] (zero on reset) and the
-// token's input xr, weighed by w[0 .. KW-1] (w[KW-1] the input), plus the
-// bias; SiLU when silu; y rounded to QT.  The same fmaf chain as the conv
-// kernel, so y is bit-identical to kda_conv_step's.
+// The fused short convolution of a decode step (CONV), one channel, in
+// stages.  conv_load: the history entries h_0 .. h_(KW-2) of the window at
+// W[i C] (zero on reset), the weights and the bias, into registers.
+// conv_apply: bias + sum_i w_i h_i + w_(KW-1) x, SiLU when silu, rounded to
+// QT: the same fmaf chain in the same order as the conv kernel, so y is
+// bit-identical to kda_conv_step's.  The loads can go out before the input
+// exists and the input's load before any of them returns.
 template <typename QT>
-__device__ __forceinline__ QT conv_channel(const QT* W, int C, int KW, bool rst, QT xr, const float* w,
-                                           float bias, int silu) {
-    float h[DCONV_H];
+__device__ __forceinline__ void conv_load(QT (&h)[DCONV_H], float (&w)[DCONV_H], float& wl, float& b, const QT* W,
+                                          int C, int KW, bool rst, const float* wp, bool w4, const float* bias) {
+    QT zero;
+    conv_round(0.f, zero);
 #pragma unroll
-    for (int i = 0; i < DCONV_H; ++i) h[i] = !rst && i < KW - 1 ? to_f32(W[(int64_t)i * C]) : 0.f;
-    float s = bias;
+    for (int i = 0; i < DCONV_H; ++i) h[i] = !rst && i < KW - 1 ? W[(int64_t)i * C] : zero;
+    if (w4) {  // KW = 4: the channel's weights are one 16-byte row
+        const float4 v = __ldg(reinterpret_cast<const float4*>(wp));
+        w[0] = v.x;
+        w[1] = v.y;
+        w[2] = v.z;
+        wl = v.w;
+    } else {
+#pragma unroll
+        for (int i = 0; i < DCONV_H; ++i) w[i] = i < KW - 1 ? __ldg(wp + i) : 0.f;
+        wl = __ldg(wp + KW - 1);  // the input's weight
+    }
+    b = bias != nullptr ? __ldg(bias) : 0.f;
+}
+
+template <typename QT>
+__device__ __forceinline__ QT conv_apply(const QT (&h)[DCONV_H], const float (&w)[DCONV_H], float wl, float b,
+                                         int KW, QT xr, int silu) {
+    float s = b;
 #pragma unroll
     for (int i = 0; i < DCONV_H; ++i)
-        if (i < KW - 1) s = fmaf(__ldg(w + i), h[i], s);
-    s = fmaf(__ldg(w + KW - 1), to_f32(xr), s);
+        if (i < KW - 1) s = fmaf(w[i], to_f32(h[i]), s);
+    s = fmaf(wl, to_f32(xr), s);
     QT out;
     conv_round(silu ? silu_fast(s) : s, out);
     return out;
@@ -79,17 +99,29 @@ __device__ __forceinline__ QT conv_channel(const QT* W, int C, int KW, bool rst,
 
 // The window of one channel after a one-token step: its last L - 1 history
 // entries (h_(KW-L+e) -> entry e; L is KW - 1 or KW; zero on reset) followed
-// by the input.  Entries move down in ascending order, so each is read before
-// it is overwritten; only the channel's one writer runs this, after every
-// reader of the old entries has read them.
+// by the input.  All kept entries are read before any is written; only the
+// channel's one writer runs this, after every reader of the old entries has
+// read them.
+template <typename QT>
+__device__ __forceinline__ void conv_window_store_kept(QT* W, int C, int L, int KW, const QT (&hraw)[DCONV_H], QT xr) {
+    const bool shift = KW - L == 1;  // else L == KW: entry e keeps h_e (hraw is zero on reset)
+#pragma unroll
+    for (int e = 0; e < DCONV_H; ++e)
+        if (e < L - 1) W[(int64_t)e * C] = shift ? hraw[e + 1 < DCONV_H ? e + 1 : e] : hraw[e];
+    if (L >= 1) W[(int64_t)(L - 1) * C] = xr;
+}
+
 template <typename QT>
 __device__ __forceinline__ void conv_window_store(QT* W, int C, int L, int KW, bool rst, QT xr) {
     const int shift = KW - L;  // 1, or 0 when L == KW (entry e keeps h_e)
     QT zero;
     conv_round(0.f, zero);
+    QT keep[DCONV_H];
+#pragma unroll
+    for (int e = 0; e < DCONV_H; ++e) keep[e] = !rst && e < L - 1 ? W[(int64_t)(e + shift) * C] : zero;
 #pragma unroll
     for (int e = 0; e < DCONV_H; ++e)
-        if (e < L - 1) W[(int64_t)e * C] = rst ? zero : W[(int64_t)(e + shift) * C];
+        if (e < L - 1) W[(int64_t)e * C] = keep[e];
     if (L >= 1) W[(int64_t)(L - 1) * C] = xr;
 }
 
@@ -166,6 +198,10 @@ kda_decode_kernel(const __grid_constant__ CUtensorMap tmap, const StepParams p) 
     const int cb0 = (tile - r * ct) * TPC;  // first column block of this CTA
     const int n = r / p.hv;
     const int h = r - n * p.hv;
+    // the fused convolution's q/k head and the CTAs that read its window
+    // (value heads sharing it times CTAs per head); formed once
+    const int cgrp = CONV ? p.hv / p.hqk : 1;
+    const int chq = CONV ? h / cgrp : 0;
     const int qes = (int)sizeof(QT);
     // The swizzled tile needs a 1024-byte aligned base; report, never guess.
     if ((tile_base0 & 1023u) != 0) {
@@ -204,6 +240,37 @@ kda_decode_kernel(const __grid_constant__ CUtensorMap tmap, const StepParams p) 
             }
         }
     }
+    // (0) the fused convolution (CONV): thread i < K takes the q and k
+    // channels of key row i, thread e < TPC BV value column e of the CTA's
+    // tiles.  Its history terms need only the window, weights and bias, so
+    // with early reads they are formed while the previous kernel drains.
+    constexpr int NVE = (TPC * BV + NT - 1) / NT;  // value columns per thread
+    // a value column's history also rewrites its window (this CTA's alone)
+    QT hq_[DCONV_H], hk_[DCONV_H], hv_[NVE][DCONV_H];
+    float wq_[DCONV_H], wk_[DCONV_H], wv_[NVE][DCONV_H], lq_ = 0.f, lk_ = 0.f, lv_[NVE], bq_ = 0.f, bk_ = 0.f, bv_[NVE];
+    if constexpr (CONV) {
+        if (valid) {
+            const auto& cp = p.conv;
+            const QT* W = static_cast<const QT*>(cp.window) + (int64_t)cslot * cp.slot_stride;
+            const bool w4 = cp.KW == 4 && (reinterpret_cast<uintptr_t>(cp.w) & 15u) == 0;
+            if (tid < p.k) {
+                const int qc = chq * p.k + tid, kc = (p.hqk + chq) * p.k + tid;
+                conv_load(hq_, wq_, lq_, bq_, W + qc, cp.C, cp.KW, rst, cp.w + (int64_t)qc * cp.KW, w4,
+                          cp.bias != nullptr ? cp.bias + qc : nullptr);
+                conv_load(hk_, wk_, lk_, bk_, W + kc, cp.C, cp.KW, rst, cp.w + (int64_t)kc * cp.KW, w4,
+                          cp.bias != nullptr ? cp.bias + kc : nullptr);
+            }
+#pragma unroll
+            for (int e = 0; e < NVE; ++e) {
+                const int c = tid + e * NT, col = cb0 * BV + c;
+                if (c < TPC * BV && col < p.v) {
+                    const int vc = 2 * p.hqk * p.k + h * p.v + col;
+                    conv_load(hv_[e], wv_[e], lv_[e], bv_[e], W + vc, cp.C, cp.KW, rst, cp.w + (int64_t)vc * cp.KW, w4,
+                              cp.bias != nullptr ? cp.bias + vc : nullptr);
+                }
+            }
+        }
+    }
     if (early) cudaGridDependencySynchronize();
     if (!valid) {
         if (pad) {  // padding: this CTA's outputs are zero
@@ -231,39 +298,34 @@ kda_decode_kernel(const __grid_constant__ CUtensorMap tmap, const StepParams p) 
     }
     const float b = __ldg(p.b + r);
 
-    // The fused short convolution (CONV): thread i < K computes q and k of key
-    // row i, thread e < TPC BV value column e of the CTA's tiles, each from its
-    // channel's window and input (all read after the previous kernel is done).
-    // A value column's window belongs to this CTA alone, which rewrites it.  A
-    // q/k channel's window is read by every CTA of the request's value heads
-    // that share the q/k head: each counts its read (once all its threads hold
-    // the values they read) and the one that makes the count complete writes
-    // the new entries and puts the count back to zero.  No CTA waits for
-    // another.
-    constexpr int NVE = (TPC * BV + NT - 1) / NT;  // value columns per thread
+    // The input terms, once the previous kernel is done: y, and q, k and v
+    // for the decode.
     float cq = 0.f, ck = 0.f, cvv[NVE];
 #pragma unroll
     for (int e = 0; e < NVE; ++e) cvv[e] = 0.f;
     if constexpr (CONV) {
         const auto& cp = p.conv;
-        const int grp = p.hv / p.hqk, hq = h / grp;
-        const bool row = tid < p.k;
-        const int chq = hq * p.k + tid, chk = (p.hqk + hq) * p.k + tid;  // this row's q and k channels
-        // the window and input of channel c (pointers rebuilt from the
-        // parameters where needed, so that none stays live in a register)
-        auto win = [&](int c) { return static_cast<QT*>(cp.window) + (int64_t)cslot * cp.slot_stride + c; };
-        auto xin = [&](int c) { return static_cast<const QT*>(cp.x)[(int64_t)n * cp.C + c]; };
-        auto conv_y = [&](int c) {
-            return conv_channel(win(c), cp.C, cp.KW, rst, xin(c), cp.w + (int64_t)c * cp.KW,
-                                cp.bias != nullptr ? __ldg(cp.bias + c) : 0.f, cp.silu);
-        };
-        if (row) {
-            const QT yq = conv_y(chq), yk = conv_y(chk);
+        const QT* X = static_cast<const QT*>(cp.x) + (int64_t)n * cp.C;
+        QT* Y = cp.y != nullptr ? static_cast<QT*>(cp.y) + (int64_t)n * cp.C : nullptr;
+        const int qc = chq * p.k + tid, kc = (p.hqk + chq) * p.k + tid;  // this row's q and k channels
+        QT xq, xk, xv[NVE];
+        if (tid < p.k) {
+            xq = X[qc];
+            xk = X[kc];
+        }
+#pragma unroll
+        for (int e = 0; e < NVE; ++e) {
+            const int c = tid + e * NT, col = cb0 * BV + c;
+            if (c < TPC * BV && col < p.v) xv[e] = X[2 * p.hqk * p.k + h * p.v + col];
+        }
+        if (tid < p.k) {
+            const QT yq = conv_apply(hq_, wq_, lq_, bq_, cp.KW, xq, cp.silu);
+            const QT yk = conv_apply(hk_, wk_, lk_, bk_, cp.KW, xk, cp.silu);
             cq = to_f32(yq);
             ck = to_f32(yk);
-            if (cp.y != nullptr && h % grp == 0 && cb0 == 0) {  // one writer of y per q/k channel
-                static_cast<QT*>(cp.y)[(int64_t)n * cp.C + chq] = yq;
-                static_cast<QT*>(cp.y)[(int64_t)n * cp.C + chk] = yk;
+            if (Y != nullptr && h % cgrp == 0 && cb0 == 0) {  // one writer of y per q/k channel
+                Y[qc] = yq;
+                Y[kc] = yk;
             }
         }
 #pragma unroll
@@ -271,32 +333,59 @@ kda_decode_kernel(const __grid_constant__ CUtensorMap tmap, const StepParams p) 
             const int c = tid + e * NT, col = cb0 * BV + c;
             if (c < TPC * BV && col < p.v) {
                 const int chv = 2 * p.hqk * p.k + h * p.v + col;
-                const QT yv = conv_y(chv);
+                const QT yv = conv_apply(hv_[e], wv_[e], lv_[e], bv_[e], cp.KW, xv[e], cp.silu);
                 cvv[e] = to_f32(yv);
-                if (cp.y != nullptr) static_cast<QT*>(cp.y)[(int64_t)n * cp.C + chv] = yv;
-                conv_window_store(win(chv), cp.C, cp.L, cp.KW, rst, xin(chv));
+                if (Y != nullptr) Y[chv] = yv;
+                conv_window_store_kept(static_cast<QT*>(cp.window) + (int64_t)cslot * cp.slot_stride + chv, cp.C,
+                                       cp.L, cp.KW, hv_[e], xv[e]);
             }
         }
-        const int readers = grp * ct;
-        bool last = true;
-        if (readers > 1) {
-            // The predicate uses the values read, so every thread's reads of
-            // the window have returned before thread 0 counts this CTA's.
-            const bool never = row && (__float_as_uint(cq) ^ __float_as_uint(ck)) == 0x7fc00001u;
-            __syncthreads_or(never ? 1 : 0);
-            int* flag = reinterpret_cast<int*>(red) + 3;  // unused word of the norm area
-            if (tid == 0) {
-                int* cnt = cp.counters + (int64_t)n * p.hqk + hq;
-                const bool done = atomicAdd(cnt, 1) == readers - 1;
-                if (done) atomicExch(cnt, 0);
-                *flag = done ? 1 : 0;
+    }
+    // (4) the fused convolution's q/k window update, the last thing the CTA
+    // does (all threads together).  A q/k channel's window is read by every
+    // CTA of the request's value heads that share the q/k head: each counts
+    // its read once its threads have used the values (they fed the gates,
+    // before a barrier; thread 0 counts right after it and keeps the old
+    // count, prev, for here), and the one that makes the count complete
+    // writes the new entries and puts the count back to zero.  No CTA waits
+    // for another.  prev < 0: not counted yet (a timeout before the gates).
+    auto conv_window_update = [&](int prev) {
+        if constexpr (CONV) {
+            const auto& cp = p.conv;
+            // the request and q/k head and the reader count, kept by thread 0
+            // in spare words of the norm area (no register holds them through
+            // the tile loop)
+            const int* meta = reinterpret_cast<const int*>(red);
+            const int n = meta[7], hq = meta[11], readers = meta[15];
+            bool last = true;
+            if (readers > 1) {
+                int* flag = reinterpret_cast<int*>(red) + 3;  // unused word of the norm area
+                if (tid == 0) {
+                    int* cnt = cp.counters + (int64_t)n * p.hqk + hq;
+                    const bool done = (prev >= 0 ? prev : atomicAdd(cnt, 1)) == readers - 1;
+                    if (done) atomicExch(cnt, 0);
+                    *flag = done ? 1 : 0;
+                }
+                __syncthreads();
+                last = *flag != 0;
             }
-            __syncthreads();
-            last = *flag != 0;
+            if (last && tid < p.k) {
+                const bool rst = p.reset != nullptr && p.reset[n] != 0;
+                QT* W = static_cast<QT*>(cp.window) + (int64_t)cp.slot[n] * cp.slot_stride;
+                const QT* X = static_cast<const QT*>(cp.x) + (int64_t)n * cp.C;
+                const int chq = hq * p.k + tid, chk = (p.hqk + hq) * p.k + tid;
+                conv_window_store(W + chq, cp.C, cp.L, cp.KW, rst, X[chq]);
+                conv_window_store(W + chk, cp.C, cp.L, cp.KW, rst, X[chk]);
+            }
         }
-        if (row && last) {
-            conv_window_store(win(chq), cp.C, cp.L, cp.KW, rst, xin(chq));
-            conv_window_store(win(chk), cp.C, cp.L, cp.KW, rst, xin(chk));
+    };
+    if constexpr (CONV) {  // for the window update at the end (spare words of the norm area)
+        static_assert(NWARP >= 4, "the norm area's spare words 3, 7, 11, 15");
+        if (tid == 0) {
+            int* meta = reinterpret_cast<int*>(red);
+            meta[7] = n;
+            meta[11] = chq;
+            meta[15] = cgrp * ct;
         }
     }
     __syncthreads();  // the barriers are initialised before anyone waits on them
@@ -334,6 +423,7 @@ kda_decode_kernel(const __grid_constant__ CUtensorMap tmap, const StepParams p) 
             if (!rst)
                 for (int j = 0; j < TPC && (TPC == 1 || cb0 + j < vt); ++j) mbar_wait(bar_st + j, 0);
         }
+        conv_window_update(-1);
         return;
     }
     kk2 = 0.f;
@@ -360,6 +450,14 @@ kda_decode_kernel(const __grid_constant__ CUtensorMap tmap, const StepParams p) 
     for (int e = 0; e < (TPC * BV + NT - 1) / NT; ++e)
         if (tid + e * NT < TPC * BV) gv[tid + e * NT] = vts[e];
     __syncthreads();
+    // the fused convolution: every thread of this CTA has used the window
+    // values it read (they fed the gates above), so thread 0 counts the
+    // CTA's read now; the result is needed only at the end
+    int conv_prev = 0;
+    if constexpr (CONV) {
+        const int* meta = reinterpret_cast<const int*>(red);  // request, q/k head, readers
+        if (tid == 0 && meta[15] > 1) conv_prev = atomicAdd(p.conv.counters + (int64_t)meta[7] * p.hqk + meta[11], 1);
+    }
 
     for (int jt = 0; jt < TPC; ++jt) {
         // tile jt of this CTA: column block cb (past the last block when V
@@ -437,6 +535,7 @@ kda_decode_kernel(const __grid_constant__ CUtensorMap tmap, const StepParams p) 
                 atomicExch(p.status, STATUS_TIMEOUT);
                 for (int j = jt; j < TPC && (TPC == 1 || cb0 + j < vt); ++j) mbar_wait(bar_st + j, 0);  // bounded, as above
             }
+            conv_window_update(conv_prev);
             return;
         }
         // ... then over the warps: thread j < BV finishes column j, writes its
@@ -455,10 +554,10 @@ kda_decode_kernel(const __grid_constant__ CUtensorMap tmap, const StepParams p) 
             p.o[(int64_t)r * p.v + cb * BV + tid] = fmaf(bqk, dj, sp) * p.inv_sqrt_k;
         }
         __syncthreads();
-        if constexpr (TPC == 1) {
+        if constexpr (TPC == 1 && !CONV) {
             if (col0 >= p.v) return;  // one tile a CTA: nothing follows
         }
-        if (TPC == 1 || col0 < p.v) {  // the tile holds columns: the update and the stores
+        if ((TPC == 1 && !CONV) || col0 < p.v) {  // the tile holds columns: the update and the stores
             float2 d[VP];
 #pragma unroll
             for (int c = 0; c < VP; c += 2) {
@@ -493,6 +592,7 @@ kda_decode_kernel(const __grid_constant__ CUtensorMap tmap, const StepParams p) 
             }
         }
     }
+    conv_window_update(conv_prev);
 }
 
 }  // namespace kda
