@@ -95,21 +95,13 @@ static constexpr int kBuildDtype = KDA_F32;
 #endif
 // The same two settings for the kernel with more than one tile per CTA.  Its
 // shared memory (two state tiles) allows 6 CTAs per SM, so 6 sets the register
-// cap (80), and the fp16 rows' raw 16-byte words from the sums pass stay in
+// cap (80), and the rows' raw 16-byte words from the sums pass stay in
 // registers for the update pass (32 registers) instead of being read again.
 #ifndef KDA_DEC_KEEP2
-#if KDA_STATE16
 #define KDA_DEC_KEEP2 1
-#else
-#define KDA_DEC_KEEP2 KDA_DEC_KEEP
-#endif
 #endif
 #ifndef KDA_DEC_MINB2
-#if KDA_STATE16
 #define KDA_DEC_MINB2 6
-#else
-#define KDA_DEC_MINB2 KDA_DEC_MINB
-#endif
 #endif
 
 namespace {
@@ -266,9 +258,7 @@ int launch_decode_k(const kda_pool* pool, const kda::StepParams& prm, cudaStream
     constexpr int BV = KDA_DEC_BV, NT = KDA_DEC_NT;
     constexpr size_t smem = kda::decode_smem_bytes<state_t, BV, NT, (int)sizeof(QT), TPC>();
     constexpr int MINB = TPC > 1 ? KDA_DEC_MINB2 : KDA_DEC_MINB;
-    // the fused convolution's two-tile kernel has no room for the kept words
-    // under the 6-CTA cap (80 registers): it reads the rows twice
-    constexpr bool KEEP = (TPC > 1 ? KDA_DEC_KEEP2 : KDA_DEC_KEEP) != 0 && !CONV;
+    constexpr bool KEEP = (TPC > 1 ? KDA_DEC_KEEP2 : KDA_DEC_KEEP) != 0;
     auto kernel = kda::kda_decode_kernel<state_t, QT, BV, NT, MINB, KEEP, FULLK, TPC, CONV>;
     // CTAs: TPC column blocks each
     const int64_t tiles = (int64_t)prm.n * prm.hv * (((prm.v + BV - 1) / BV + TPC - 1) / TPC);
@@ -299,10 +289,13 @@ int launch_decode_t(const kda_pool* pool, const kda::StepParams& prm, cudaStream
 }
 
 // KDA_DEC_TPC tiles per CTA when the one-tile grid is more than one wave of
-// the one-tile kernel, else one.  CONV: the decode with the fused convolution.
+// the one-tile kernel, else one.  CONV: the decode with the fused
+// convolution, two tiles a CTA on either pool past one wave: each CTA forms
+// its q/k head's 2 K conv outputs, so fewer CTAs a head form them fewer times
+// and share each q/k window among fewer readers.
 template <typename QT, bool CONV = false>
 int launch_decode(const kda_pool* pool, const kda::StepParams& prm, cudaStream_t stream) {
-    constexpr int TPC = KDA_DEC_TPC;
+    constexpr int TPC = CONV ? 2 : KDA_DEC_TPC;
     if constexpr (TPC > 1) {
         constexpr int BV = KDA_DEC_BV, NT = KDA_DEC_NT;
         constexpr size_t smem = kda::decode_smem_bytes<state_t, BV, NT, (int)sizeof(QT)>();
