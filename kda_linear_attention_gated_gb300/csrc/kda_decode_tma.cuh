@@ -6,9 +6,9 @@
 // TMA box row, one swizzle span.
 //
 // A CTA owns TPC adjacent tiles of one (request, head): one for an fp32 pool,
-// two for an fp16 pool, so that an fp16 launch at N = 64 is 768 CTAs, all
-// resident at once (6 per SM by shared memory), where one tile per CTA made
-// 1.26 waves of 1536.  Thread 0 starts one 3-D tensor-map load per state tile,
+// two for an fp16 pool (and for the fused-convolution build on either pool),
+// so that an fp16 launch at N = 64 is 768 CTAs, all resident at once (6 per SM
+// by shared memory), where one tile per CTA made 1.26 waves of 1536.  Thread 0 starts one 3-D tensor-map load per state tile,
 // each on its own barrier, and 1-D bulk copies of the q, k and a rows and the
 // tiles' slices of v into shared memory, completing on one more barrier.
 // Because the bytes land in shared memory rather than registers, a CTA is
@@ -23,10 +23,15 @@
 //       and p = S^T (alpha qhat) (the decay folded into the gates); warp
 //       shuffles and one shared-memory pass finish the sums over K;
 //   (3) it reads its rows from shared memory again (one tile a CTA) or takes
-//       their raw 16-byte words, kept in registers since (2) (two fp16 tiles a
-//       CTA, where shared memory caps residency at 6 CTAs per SM and so leaves
-//       room for them), applies the delta update and writes the rows back to
-//       the slot with coalesced 16-byte stores.
+//       their raw 16-byte words, kept in registers since (2) (two tiles a CTA,
+//       where shared memory caps residency at 6 CTAs per SM and so leaves room
+//       for them), applies the delta update and writes the rows back to the
+//       slot with coalesced 16-byte stores.
+// The CONV build puts the layer's short convolution in front: q, k and v are
+// not copied in but formed from the conv window and the pre-activations x
+// (thread i < K: the q and k channels of key row i; thread e < TPC BV: value
+// column e), and the window is rewritten; see the conv helpers below and
+// step (4) in the kernel.
 // The inputs and the state tile complete on separate barriers, so the gates
 // are computed while the state is still in flight.  Each barrier wait is
 // bounded (1 s); a wait that runs out makes the whole CTA record
@@ -242,8 +247,9 @@ kda_decode_kernel(const __grid_constant__ CUtensorMap tmap, const StepParams p) 
     }
     // (0) the fused convolution (CONV): thread i < K takes the q and k
     // channels of key row i, thread e < TPC BV value column e of the CTA's
-    // tiles.  Its history terms need only the window, weights and bias, so
-    // with early reads they are formed while the previous kernel drains.
+    // tiles.  The history entries, weights and bias are nothing the previous
+    // kernel writes, so with early reads they are loaded while it drains; the
+    // sums are formed once the inputs' loads are out, after the wait.
     constexpr int NVE = (TPC * BV + NT - 1) / NT;  // value columns per thread
     // a value column's history also rewrites its window (this CTA's alone)
     QT hq_[DCONV_H], hk_[DCONV_H], hv_[NVE][DCONV_H];
