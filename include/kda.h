@@ -349,6 +349,9 @@ int kda_conv_step(const kda_conv_window* win, const kda_conv_args* args, int32_t
  *   a, b, o   as for kda_decode_step: fp32 [n][hv][k] (16-byte aligned), [n][hv], [n][hv][v].
  *   y         device [n][channels] of the window's dtype, or NULL: the
  *             convolution's outputs, when the caller wants them as well.
+ *   a_log, dt_bias  device fp32 [hv] and [hv][k], or NULL: the layer's learned
+ *             gate scale and bias, alpha = exp(-exp(a_log[h]) softplus(a + dt_bias[h])),
+ *             as for kda_step (which the call then matches in place of kda_decode_step).
  *   counters  device int32 [n][h_qk], all zero on entry (allocate once and
  *             zero once); the call leaves them zero.  Several CTAs read one
  *             q/k channel's window, so the last of them to finish reading
@@ -370,6 +373,8 @@ typedef struct kda_decode_conv_args {
     float* o;                   /* [n][hv][v] (output) */
     void* y;                    /* [n][channels] (output) or NULL */
     int32_t* counters;          /* [n][h_qk] */
+    const float* a_log;         /* [hv] or NULL: the learned gate scale, as in kda_step */
+    const float* dt_bias;       /* [hv][k] or NULL: the gate bias, as in kda_step */
 } kda_decode_conv_args;
 
 /*

@@ -98,7 +98,8 @@ class DecodeConvArgs(ctypes.Structure):
                 ("activation", ctypes.c_int32), ("slot_ids", ctypes.c_void_p), ("conv_slot", ctypes.c_void_p),
                 ("reset", ctypes.c_void_p), ("x", ctypes.c_void_p), ("weight", ctypes.c_void_p),
                 ("bias", ctypes.c_void_p), ("a", ctypes.c_void_p), ("b", ctypes.c_void_p), ("o", ctypes.c_void_p),
-                ("y", ctypes.c_void_p), ("counters", ctypes.c_void_p)]
+                ("y", ctypes.c_void_p), ("counters", ctypes.c_void_p), ("a_log", ctypes.c_void_p),
+                ("dt_bias", ctypes.c_void_p)]
 
 
 class HostCopy(ctypes.Structure):
@@ -385,7 +386,8 @@ class KdaLibrary:
                                              flags, stream)
 
     def kda_decode_conv_step(self, pool, window, slot_ids, conv_slot, x, weight, a, b, o, status, counters,
-                             bias=None, y=None, reset=None, h_qk=None, silu=True, stream=None, flags=0) -> None:
+                             bias=None, y=None, reset=None, h_qk=None, silu=True, a_log=None, dt_bias=None,
+                             stream=None, flags=0) -> None:
         """One decode token per request with the short convolution fused in
         front of the recurrence (see kda_decode_conv_args in include/kda.h):
         x [n, C] of the window's dtype with C = 2 h_qk K + HV V (q | k | v
@@ -414,9 +416,14 @@ class KdaLibrary:
             _expect("y", y, (n, C), (window.dtype,))
         if reset is not None:
             _expect("reset", reset, (n,), (torch.uint8,))
+        if a_log is not None:
+            _expect("a_log", a_log, (hv,), (torch.float32,))
+        if dt_bias is not None:
+            _expect("dt_bias", dt_bias, (hv, kd), (torch.float32,))
         win = ConvWindowDesc(window.data_ptr(), _dtype_code(window.dtype), C, L, 0, ns, window.stride(0))
         args = DecodeConvArgs(n, h_qk, kw, int(bool(silu)), _ptr(slot_ids), _ptr(conv_slot), _ptr(reset), _ptr(x),
-                              _ptr(weight), _ptr(bias), _ptr(a), _ptr(b), _ptr(o), _ptr(y), _ptr(counters))
+                              _ptr(weight), _ptr(bias), _ptr(a), _ptr(b), _ptr(o), _ptr(y), _ptr(counters),
+                              _ptr(a_log), _ptr(dt_bias))
         self._check(self.kda_decode_conv_step_raw(desc, win, args, _ptr(status), self._stream(stream), flags),
                     "kda_decode_conv_step")
 

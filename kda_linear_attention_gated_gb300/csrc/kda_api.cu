@@ -760,11 +760,13 @@ int kda_decode_conv_step(const kda_pool* pool, const kda_conv_window* win, const
     if (!aligned(win->base, es) || !aligned(g.x, es) || (g.y && !aligned(g.y, es)) || !aligned(g.slot_ids, 4) ||
         !aligned(g.conv_slot, 4) || !aligned(g.weight, 4) || (g.bias && !aligned(g.bias, 4)) ||
         !aligned(g.a, 16) || !aligned(g.b, 4) || !aligned(g.o, 4) || !aligned(g.counters, 4) ||
-        !aligned(dev_status, 4))
+        !aligned(dev_status, 4) || (g.a_log && !aligned(g.a_log, 4)) || (g.dt_bias && !aligned(g.dt_bias, 4)))
         return KDA_ERR_ALIGN;
     kda::StepParams prm = make_params(pool, g.slot_ids, nullptr, g.reset, g.n, 1, nullptr, nullptr, nullptr,
                                       g.a, g.b, g.o, dev_status, flags);
     prm.hqk = g.h_qk;
+    prm.a_log = g.a_log;
+    prm.dt_bias = g.dt_bias;
     prm.conv.window = win->base;
     prm.conv.num_slots = win->num_slots;
     prm.conv.slot_stride = win->slot_stride;

@@ -56,6 +56,16 @@ def _randn(g, shape, dtype=torch.float32, std=1.0):
     return x.to(dtype)
 
 
+def _gate_scale(g, hv, k):
+    """A layer's learned gate scale and bias: A_log = log U(1, 16) per value
+    head; dt_bias = log(expm1(dt)) with dt = exp U(log 1e-3, log 1e-1) per
+    (head, key channel)."""
+    a_log = torch.log(1.0 + 15.0 * torch.rand((hv,), generator=g))
+    lo, hi = torch.log(torch.tensor(1e-3)), torch.log(torch.tensor(1e-1))
+    dt = torch.exp(lo + (hi - lo) * torch.rand((hv, k), generator=g))
+    return a_log, torch.log(torch.expm1(dt))
+
+
 def make_pool(g, num_slots, hv, k, v, state_dtype, std=0.1):
     """fp32 N(0, std^2), then (fp16 pool) rounded to nearest even by the dtype cast."""
     return _randn(g, (num_slots, hv, k, v), std=std).to(state_dtype)
@@ -206,12 +216,7 @@ def make_general(n=8, t_lens=None, t=8, num_cols=None, h_qk=None, hv=12, k=128, 
     reset = None
     if reset_p > 0:
         reset = (torch.rand((n,), generator=g) < reset_p).to(torch.uint8)
-    a_log = dt_bias = None
-    if gate_scale:
-        a_log = torch.log(1.0 + 15.0 * torch.rand((hv,), generator=g))
-        lo, hi = torch.log(torch.tensor(1e-3)), torch.log(torch.tensor(1e-1))
-        dt = torch.exp(lo + (hi - lo) * torch.rand((hv, k), generator=g))
-        dt_bias = torch.log(torch.expm1(dt))
+    a_log, dt_bias = _gate_scale(g, hv, k) if gate_scale else (None, None)
     cu = None
     if t_lens is not None:
         cu = torch.zeros(n + 1, dtype=torch.int32)
@@ -285,22 +290,25 @@ class DecodeConvInputs:
     reset: torch.Tensor | None = None  # uint8 [N]
     h_qk: int = 12
     meta: dict = field(default_factory=dict)
+    a_log: torch.Tensor | None = None    # fp32 [HV]
+    dt_bias: torch.Tensor | None = None  # fp32 [HV, K]
 
     def to(self, device) -> "DecodeConvInputs":
         mv = lambda t: None if t is None else t.to(device)  # noqa: E731
         return DecodeConvInputs(mv(self.pool), mv(self.slot_ids), mv(self.window), mv(self.conv_slot), mv(self.x),
                                 mv(self.weight), mv(self.bias), mv(self.a), mv(self.b), mv(self.reset), self.h_qk,
-                                dict(self.meta))
+                                dict(self.meta), mv(self.a_log), mv(self.dt_bias))
 
 
 def make_decode_conv(n=64, hv=12, h_qk=12, k=128, v=128, kw=4, L=3, num_slots=256, num_wslots=256,
                      state_dtype=torch.float32, dtype=torch.bfloat16, seed=11, reset_p=0.0,
-                     bias=True) -> DecodeConvInputs:
+                     bias=True, gate_scale=False) -> DecodeConvInputs:
     """One decode token for n requests with the short convolution in front:
     channels C = 2 h_qk k + hv v; the state pool as in make_decode; the window
     (L entries) and x ~ N(0, 1) in dtype, weight ~ N(0, 1 / kw), bias ~
     N(0, 0.1^2), as in make_conv; a, b ~ N(0, 1); n distinct state slots and
-    n distinct window slots."""
+    n distinct window slots; gate_scale: the learned gate scale and bias as in
+    make_general."""
     g = torch.Generator().manual_seed(seed)
     C = 2 * h_qk * k + hv * v
     P = make_pool(g, num_slots, hv, k, v, state_dtype)
@@ -313,8 +321,10 @@ def make_decode_conv(n=64, hv=12, h_qk=12, k=128, v=128, kw=4, L=3, num_slots=25
     a = _randn(g, (n, hv, k))
     b = _randn(g, (n, hv))
     reset = (torch.rand((n,), generator=g) < reset_p).to(torch.uint8) if reset_p > 0 else None
+    a_log, dt_bias = _gate_scale(g, hv, k) if gate_scale else (None, None)
     return DecodeConvInputs(P, slots, W, cslots, x, w, bv, a, b, reset, h_qk,
-                            dict(kind="decode_conv", n=n, hv=hv, h_qk=h_qk, k=k, v=v, kw=kw, L=L, seed=seed))
+                            dict(kind="decode_conv", n=n, hv=hv, h_qk=h_qk, k=k, v=v, kw=kw, L=L, seed=seed),
+                            a_log, dt_bias)
 
 
 @dataclass

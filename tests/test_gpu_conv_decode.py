@@ -45,11 +45,11 @@ def two_kernels(d, inp, pool, W, silu=True, flags=0):
                       flags=flags)
     q, k, v = split_y(y, inp)
     o = torch.full((n, hv, V), float("nan"), device="cuda")
-    if inp.h_qk == hv:
+    if inp.h_qk == hv and d.a_log is None:
         lib.kda_decode_step(pool, d.slot_ids, q, k, v, d.a, d.b, o, st, reset=d.reset, flags=flags)
     else:
         lib.kda_step(pool, d.slot_ids.view(n, 1).contiguous(), q, k, v, d.a, d.b, o, st, reset=d.reset,
-                     in_place=True, flags=flags)
+                     a_log=d.a_log, dt_bias=d.dt_bias, in_place=True, flags=flags)
     return o, y, st
 
 
@@ -60,7 +60,8 @@ def fused(d, inp, pool, W, counters, silu=True, flags=0, with_y=True):
     y = torch.full_like(d.x, float("nan")) if with_y else None
     o = torch.full((n, hv, V), float("nan"), device="cuda")
     lib.kda_decode_conv_step(pool, W, d.slot_ids, d.conv_slot, d.x, d.weight, d.a, d.b, o, st, counters,
-                             bias=d.bias, y=y, reset=d.reset, h_qk=inp.h_qk, silu=silu, flags=flags)
+                             bias=d.bias, y=y, reset=d.reset, h_qk=inp.h_qk, silu=silu, a_log=d.a_log,
+                             dt_bias=d.dt_bias, flags=flags)
     return o, y, st
 
 
@@ -100,8 +101,8 @@ def assert_fused_equals_two_kernels(inp, silu=True, flags=0, steps=1):
 @pytest.mark.parametrize("state_dtype", [torch.float32, torch.float16])
 def test_fused_layer_shape_equals_conv_then_decode(state_dtype, wdt):
     """N = 64, HV = 12, K = V = 128, kernel 4, a 3-entry window, resets: the
-    fp16 launch has one CTA per head (no shared q/k window), the fp32 one four
-    (the read counters decide the writer)."""
+    fp16 launch has one CTA per head (no shared q/k window), the fp32 one two
+    (two 32-column tiles each; the read counters decide the writer)."""
     inp = workloads.make_decode_conv(n=64, state_dtype=state_dtype, dtype=wdt, seed=11, reset_p=0.1)
     assert_fused_equals_two_kernels(inp)
 
@@ -109,8 +110,8 @@ def test_fused_layer_shape_equals_conv_then_decode(state_dtype, wdt):
 @pytest.mark.parametrize("n,h_qk", [(64, 4), (64, 1), (5, 12), (5, 3)])
 @pytest.mark.parametrize("state_dtype", [torch.float32, torch.float16])
 def test_fused_grouped_heads_and_small_launches(state_dtype, n, h_qk):
-    """Grouped q/k heads (up to 12 value heads x 4 column CTAs reading one q/k
-    window) and launches within one wave (fp16: one tile a CTA)."""
+    """Grouped q/k heads (up to 12 value heads x 2 CTAs, or x 4 and x 8 one-tile
+    CTAs within one wave, reading one q/k window) and launches within one wave."""
     inp = workloads.make_decode_conv(n=n, h_qk=h_qk, state_dtype=state_dtype, seed=12 + h_qk, reset_p=0.2)
     assert_fused_equals_two_kernels(inp)
 
@@ -133,6 +134,17 @@ def test_fused_ragged_key_and_value_sizes(state_dtype, K, V):
     tile (a partial second fp16 tile at V = 80, none at V = 48)."""
     inp = workloads.make_decode_conv(n=64, hv=6, h_qk=3, k=K, v=V, state_dtype=state_dtype, seed=30 + K + V)
     assert_fused_equals_two_kernels(inp)
+
+
+@pytest.mark.parametrize("h_qk", [12, 4])
+@pytest.mark.parametrize("state_dtype", [torch.float32, torch.float16])
+def test_fused_learned_gate_scale(state_dtype, h_qk):
+    """The layer's learned gate scale and bias (a_log, dt_bias): against the
+    conv step then the in-place kda_step with the same gate arguments, over
+    a 2-step chain."""
+    inp = workloads.make_decode_conv(n=64, h_qk=h_qk, state_dtype=state_dtype, seed=45 + h_qk, reset_p=0.1,
+                                     gate_scale=True)
+    assert_fused_equals_two_kernels(inp, steps=2)
 
 
 @pytest.mark.parametrize("flags", [0, PDL])
@@ -211,17 +223,18 @@ def test_fused_bad_window_slot_skips_the_request(state_dtype):
 # ---------------------------------------------------------------------------
 # against the fp64 oracle
 # ---------------------------------------------------------------------------
-@pytest.mark.parametrize("wdt", [torch.bfloat16, torch.float32])
+@pytest.mark.parametrize("wdt,gate_scale", [(torch.bfloat16, False), (torch.float32, False), (torch.bfloat16, True)])
 @pytest.mark.parametrize("kw,L", [(4, 3), (4, 4)])
 @pytest.mark.parametrize("state_dtype", [torch.float32, torch.float16])
-def test_fused_against_oracle(state_dtype, kw, L, wdt):
+def test_fused_against_oracle(state_dtype, kw, L, wdt, gate_scale):
     """n = 5, HV = 4 value heads on 2 q/k heads, K = V = 32, resets.  The
     oracle's convolution gives the window (exact) and y (the conv bar); its
     recurrence, fed the kernel's own q/k/v values, gives the pool and o
     (the decode bars), so a 16-bit y one step from the oracle's cannot
     masquerade as a recurrence error."""
     inp = workloads.make_decode_conv(n=5, hv=4, h_qk=2, k=32, v=32, kw=kw, L=L, num_slots=12, num_wslots=9,
-                                     state_dtype=state_dtype, dtype=wdt, seed=50 + L, reset_p=0.4)
+                                     state_dtype=state_dtype, dtype=wdt, seed=50 + L, reset_p=0.4,
+                                     gate_scale=gate_scale)
     d = inp.to("cuda")
     pool, W = d.pool.clone(), d.window.clone()
     c = torch.zeros(5, 2, dtype=torch.int32, device="cuda")
@@ -245,6 +258,8 @@ def test_fused_against_oracle(state_dtype, kw, L, wdt):
     ref = pool_np(inp.pool)
     o_ref = oracle.step(ref, inp.slot_ids.numpy().reshape(5, 1), q.double().numpy(), k.double().numpy(),
                         v.double().numpy(), inp.a.numpy(), inp.b.numpy(),
-                        reset=None if inp.reset is None else inp.reset.numpy(), in_place=True)
+                        reset=None if inp.reset is None else inp.reset.numpy(),
+                        a_log=None if inp.a_log is None else inp.a_log.numpy(),
+                        dt_bias=None if inp.dt_bias is None else inp.dt_bias.numpy(), in_place=True)
     assert_pool_match(pool.cpu(), ref, inp.slot_ids.numpy(), "pool")
     assert_out_match(o.cpu(), o_ref, state_dtype, "o")

@@ -252,6 +252,8 @@ def test_decode_conv_step_refusals_before_any_launch(libs):
     assert call(win(), args(x=P + 1)) == kda.KDA_ERR_ALIGN
     assert call(win(), args(y=P + 1)) == kda.KDA_ERR_ALIGN
     assert call(win(), args(counters=P + 2)) == kda.KDA_ERR_ALIGN
+    assert call(win(), args(a_log=P + 2)) == kda.KDA_ERR_ALIGN
+    assert call(win(), args(dt_bias=P + 1)) == kda.KDA_ERR_ALIGN
     assert call(win(), args(n=0)) == kda.KDA_OK               # nothing to do: no launch
 
 
