@@ -399,6 +399,57 @@ int kda_decode_conv_step(const kda_pool* pool, const kda_conv_window* win, const
                          int32_t* dev_status, uint32_t flags, void* stream);
 
 /*
+ * The convolution half of kda_step_conv: the general speculative step with the
+ * short convolution done in the same kernel (pull request 2894, review thread
+ * on the conv window: the window keeps kernel - 1 + num_spec inputs, a step
+ * reads its history at the accepted index and writes back the kept old
+ * entries followed by its inputs).  x holds each token's pre-convolution
+ * q | k | v inputs, channels = 2 * h_qk * k + hv * v, laid out as for
+ * kda_decode_conv_args.  Per call the result is, bit for bit, kda_conv_step
+ * over the same requests (cu_seqlens, accepted, reset; conv_slot[r]; a padding
+ * request's window left alone and its y rows zero) followed by kda_step with
+ * q, k, v taken from that y, read as the window's dtype.
+ *   conv_slot  device int32 [n]: the window slot of request r (ignored for a
+ *              padding request).
+ *   x          device [total][channels] of the window's dtype.
+ *   weight     device fp32 [channels][kernel_width];  bias device fp32 [channels] or NULL.
+ *   y          device [total][channels] of the window's dtype, or NULL.
+ *   counters   device int32 [n][h_qk], zero on entry; the call leaves them zero
+ *              (as for kda_decode_conv_args).
+ */
+typedef struct kda_step_conv_args {
+    int32_t kernel_width;       /* 1 .. 4 */
+    int32_t activation;         /* 0 none, 1 SiLU */
+    const int32_t* conv_slot;   /* [n] */
+    const void* x;              /* [total][channels] */
+    const float* weight;        /* [channels][kernel_width] */
+    const float* bias;          /* [channels] or NULL */
+    void* y;                    /* [total][channels] (output) or NULL */
+    int32_t* counters;          /* [n][h_qk] */
+} kda_step_conv_args;
+
+/*
+ * One speculative step with the convolution fused in front (see
+ * kda_step_conv_args); pool, step, win and conv are host pointers.  step is as
+ * for kda_step with in_place = 0, max_t <= 8 (one chunk of tokens a request),
+ * q, k and v NULL (the convolution makes them) and qkv_dtype the window's
+ * dtype.  Host checks: those of kda_step, then KDA_ERR_ARG (in_place set, q/k/v
+ * given, qkv_dtype not the window's, activation not 0/1, flags other than the
+ * PDL bits), KDA_ERR_SHAPE (max_t above 8, channels other than
+ * 2 h_qk k + hv v, kernel_width outside 1 .. 4, state_len outside
+ * kernel_width - 1 .. 32, slot_stride too small), _ALIGN, _NULL.  Device
+ * checks (the request skipped whole, its counters left alone): a window slot
+ * outside the pool, KDA_ERR_SLOT_RANGE; acc + kernel_width - 1 > state_len
+ * or more kept entries than that (acc = accepted[r] - 1), KDA_ERR_ARG.
+ * KDA_LAUNCH_PDL_EARLY_STATE also lets the kernel read the window slots,
+ * weights, bias and history entries early; x is read, and the window,
+ * counters, y and outputs are written, only after the previous kernel has
+ * completed.  n == 0 or total == 0 is a no-op after the host checks.
+ */
+int kda_step_conv(const kda_pool* pool, const kda_step_args* step, const kda_conv_window* win,
+                  const kda_step_conv_args* conv, int32_t* dev_status, uint32_t flags, void* stream);
+
+/*
  * Arguments of kda_prefill: the recurrence over packed prompts (the second
  * workload of pull request 2130, What: prefill reads and writes the state
  * through the destination's element type like every other path).  Request r

@@ -38,6 +38,7 @@ KDA_LAUNCH_TEST_WITHHOLD_STATE = 1 << 30  # test hook of the timeout path (inclu
 EXPORTED_SYMBOLS = ("kda_build_state_dtype", "kda_pool_check", "kda_state_bytes",
                     "kda_decode_step", "kda_spec_verify", "kda_step", "kda_prefill", "kda_prefill_workspace_bytes",
                     "kda_prefill_chunked", "kda_prefill_chunked_noalloc", "kda_conv_step", "kda_decode_conv_step",
+                    "kda_step_conv",
                     "kda_layout_id", "kda_ckpt_flush", "kda_ckpt_load", "kda_stage_host", "kda_strerror")
 
 
@@ -100,6 +101,13 @@ class DecodeConvArgs(ctypes.Structure):
                 ("bias", ctypes.c_void_p), ("a", ctypes.c_void_p), ("b", ctypes.c_void_p), ("o", ctypes.c_void_p),
                 ("y", ctypes.c_void_p), ("counters", ctypes.c_void_p), ("a_log", ctypes.c_void_p),
                 ("dt_bias", ctypes.c_void_p)]
+
+
+class StepConvArgs(ctypes.Structure):
+    """Mirror of ``struct kda_step_conv_args`` (include/kda.h)."""
+    _fields_ = [("kernel_width", ctypes.c_int32), ("activation", ctypes.c_int32), ("conv_slot", ctypes.c_void_p),
+                ("x", ctypes.c_void_p), ("weight", ctypes.c_void_p), ("bias", ctypes.c_void_p), ("y", ctypes.c_void_p),
+                ("counters", ctypes.c_void_p)]
 
 
 class HostCopy(ctypes.Structure):
@@ -189,6 +197,9 @@ def _load(state16: bool) -> ctypes.CDLL:
         lib.kda_prefill_chunked_noalloc.argtypes = [P, ctypes.POINTER(PrefillArgs), vp, u32, vp]
         lib.kda_conv_step.restype = ctypes.c_int
         lib.kda_conv_step.argtypes = [ctypes.POINTER(ConvWindowDesc), ctypes.POINTER(ConvArgs), vp, u32, vp]
+        lib.kda_step_conv.restype = ctypes.c_int
+        lib.kda_step_conv.argtypes = [P, ctypes.POINTER(StepArgs), ctypes.POINTER(ConvWindowDesc),
+                                      ctypes.POINTER(StepConvArgs), vp, u32, vp]
         lib.kda_decode_conv_step.restype = ctypes.c_int
         lib.kda_decode_conv_step.argtypes = [P, ctypes.POINTER(ConvWindowDesc), ctypes.POINTER(DecodeConvArgs),
                                              vp, u32, vp]
@@ -426,6 +437,62 @@ class KdaLibrary:
                               _ptr(a_log), _ptr(dt_bias))
         self._check(self.kda_decode_conv_step_raw(desc, win, args, _ptr(status), self._stream(stream), flags),
                     "kda_decode_conv_step")
+
+    def kda_step_conv_raw(self, desc: PoolDesc, args: StepArgs, win: ConvWindowDesc, cargs: StepConvArgs, status,
+                          stream, flags=0) -> int:
+        return self.lib.kda_step_conv(ctypes.byref(desc), ctypes.byref(args), ctypes.byref(win), ctypes.byref(cargs),
+                                      status, flags, stream)
+
+    def kda_step_conv(self, pool, window, slot_table, conv_slot, x, weight, a, b, o, status, counters,
+                      cu_seqlens=None, max_t=None, accepted=None, reset=None, a_log=None, dt_bias=None, bias=None,
+                      y=None, h_qk=None, silu=True, stream=None, flags=0) -> None:
+        """The general speculative step with the short convolution fused in
+        front (see kda_step_conv_args in include/kda.h): packed tokens x
+        [total, C] of the window's dtype (q | k | v channels, C = 2 h_qk K +
+        HV V), a [total, HV, K], b [total, HV], o [total, HV, V]; slot_table
+        [N, num_cols]; window [num_slots, L, C]; counters int32 [N, h_qk]."""
+        import torch
+        desc = pool_desc(pool)
+        hv, kd, vd = desc.hv, desc.k, desc.v
+        if window.dim() != 3 or window.stride(2) != 1 or window.stride(1) != window.shape[2]:
+            raise ValueError("a conv window pool is a [num_slots, L, C] tensor, dense in [L, C]")
+        ns, L, C = window.shape
+        n, ncols = int(slot_table.shape[0]), int(slot_table.shape[1])
+        total, kw = int(x.shape[0]), int(weight.shape[1])
+        h_qk = hv if h_qk is None else int(h_qk)
+        _expect("slot_table", slot_table, (n, ncols), (torch.int32,))
+        _expect("conv_slot", conv_slot, (n,), (torch.int32,))
+        _expect("x", x, (total, C), (window.dtype,))
+        _expect("weight", weight, (C, kw), (torch.float32,))
+        _expect("a", a, (total, hv, kd), (torch.float32,))
+        _expect("b", b, (total, hv), (torch.float32,))
+        _expect("o", o, (total, hv, vd), (torch.float32,))
+        _expect("counters", counters, (n, h_qk), (torch.int32,))
+        _expect("status", status, (1,), (torch.int32,))
+        for name, t, shape in (("bias", bias, (C,)), ("a_log", a_log, (hv,)), ("dt_bias", dt_bias, (hv, kd))):
+            if t is not None:
+                _expect(name, t, shape, (torch.float32,))
+        if y is not None:
+            _expect("y", y, (total, C), (window.dtype,))
+        if cu_seqlens is not None:
+            _expect("cu_seqlens", cu_seqlens, (n + 1,), (torch.int32,))
+            if max_t is None:
+                raise ValueError("max_t is required with cu_seqlens")
+        elif max_t is None:
+            max_t = total // n if n else 0
+        if accepted is not None:
+            _expect("accepted", accepted, (n,), (torch.int32,))
+        if reset is not None:
+            _expect("reset", reset, (n,), (torch.uint8,))
+        wd = _dtype_code(window.dtype)
+        args = StepArgs(n, total, int(max_t), h_qk, ncols, 0, wd, 0, _ptr(cu_seqlens), _ptr(slot_table),
+                        _ptr(accepted), _ptr(reset), None, None, None, _ptr(a), _ptr(b), _ptr(a_log), _ptr(dt_bias),
+                        _ptr(o))
+        win = ConvWindowDesc(window.data_ptr(), wd, C, L, 0, ns, window.stride(0))
+        cargs = StepConvArgs(kw, int(bool(silu)), _ptr(conv_slot), _ptr(x), _ptr(weight), _ptr(bias), _ptr(y),
+                             _ptr(counters))
+        self._check(self.kda_step_conv_raw(desc, args, win, cargs, _ptr(status), self._stream(stream), flags),
+                    "kda_step_conv")
 
     def kda_stage_host_raw(self, copies, stream, flags=0) -> int:
         """copies: a list of (dst device address, src pinned host address, bytes)."""

@@ -310,7 +310,7 @@ int launch_decode(const kda_pool* pool, const kda::StepParams& prm, cudaStream_t
     return launch_decode_t<QT, 1, CONV>(pool, prm, stream);
 }
 
-template <typename QT, bool WIDE>
+template <typename QT, bool WIDE, bool CONV>
 int launch_verify_shape(const kda_pool* pool, const kda::StepParams& prm, cudaStream_t stream, int64_t tiles) {
     constexpr int BV = KDA_VER_BV;
     using SH = kda::VerifyShape<state_t, BV, (int)sizeof(QT), WIDE>;
@@ -318,8 +318,8 @@ int launch_verify_shape(const kda_pool* pool, const kda::StepParams& prm, cudaSt
     // an fp16 pool at K = 128 gets the build with compile-time row loops; an
     // fp32 pool's 256-thread tiles have no register room for it (it spills)
     constexpr bool kFullkOk = sizeof(state_t) == 2;
-    auto kernel = (kFullkOk && prm.k == kda::KMAX) ? kda::kda_verify_kernel<state_t, QT, BV, kFullkOk, WIDE>
-                                                   : kda::kda_verify_kernel<state_t, QT, BV, false, WIDE>;
+    auto kernel = (kFullkOk && prm.k == kda::KMAX) ? kda::kda_verify_kernel<state_t, QT, BV, kFullkOk, WIDE, CONV>
+                                                   : kda::kda_verify_kernel<state_t, QT, BV, false, WIDE, CONV>;
     CUtensorMap map;
     int rc = make_pool_map(pool, BV, &map);
     if (rc != KDA_OK) return rc;
@@ -339,7 +339,8 @@ int launch_verify_shape(const kda_pool* pool, const kda::StepParams& prm, cudaSt
 
 // A launch that fits in one wave of the default shape runs it; a larger one,
 // on an fp16 pool with 16-bit inputs, runs the wide shape (4 CTAs per SM).
-template <typename QT>
+// CONV: the step with the short convolution fused in front.
+template <typename QT, bool CONV = false>
 int launch_verify(const kda_pool* pool, const kda::StepParams& prm, cudaStream_t stream) {
     constexpr int BV = KDA_VER_BV;
     const int64_t tiles = (int64_t)prm.n * prm.hv * ((prm.v + BV - 1) / BV);
@@ -352,9 +353,9 @@ int launch_verify(const kda_pool* pool, const kda::StepParams& prm, cudaStream_t
         const int rc = occupancy(reinterpret_cast<const void*>(kda::kda_verify_kernel<state_t, QT, BV, false>),
                                  SH::NT, smem, &occ, &sms);
         if (rc != KDA_OK) return rc;
-        if (tiles > (int64_t)occ * sms) return launch_verify_shape<QT, kWideOk>(pool, prm, stream, tiles);
+        if (tiles > (int64_t)occ * sms) return launch_verify_shape<QT, kWideOk, CONV>(pool, prm, stream, tiles);
     }
-    return launch_verify_shape<QT, false>(pool, prm, stream, tiles);
+    return launch_verify_shape<QT, false, CONV>(pool, prm, stream, tiles);
 }
 
 template <bool VERIFY>
@@ -785,6 +786,71 @@ int kda_decode_conv_step(const kda_pool* pool, const kda_conv_window* win, const
         case KDA_F32: return launch_decode<float, true>(pool, prm, st);
         case KDA_F16: return launch_decode<__half, true>(pool, prm, st);
         default: return launch_decode<__nv_bfloat16, true>(pool, prm, st);
+    }
+}
+
+int kda_step_conv(const kda_pool* pool, const kda_step_args* args, const kda_conv_window* win,
+                  const kda_step_conv_args* cv, int32_t* dev_status, uint32_t flags, void* stream) {
+    if (args == nullptr || win == nullptr || cv == nullptr) return KDA_ERR_NULL;
+    const kda_step_args& g = *args;
+    int rc = check_pool_for_build(pool);
+    if (rc != KDA_OK) return rc;
+    const int es = elem_size(win->dtype);
+    if (es == 0) return KDA_ERR_DTYPE_UNSUPPORTED;
+    if (g.n < 0 || g.total < 0 || g.max_t < 0 || g.reserved != 0 || win->reserved != 0 || g.in_place != 0 ||
+        g.q != nullptr || g.k != nullptr || g.v != nullptr || g.qkv_dtype != win->dtype ||
+        (cv->activation != 0 && cv->activation != 1))
+        return KDA_ERR_ARG;
+    if (flags & ~(uint32_t)(KDA_LAUNCH_PDL | KDA_LAUNCH_PDL_EARLY_STATE)) return KDA_ERR_ARG;
+    if (g.h_qk < 1 || pool->hv % g.h_qk != 0 || g.num_cols < 1 || g.max_t > g.num_cols ||
+        g.max_t > kda::VerifyShape<state_t, KDA_VER_BV, 2>::TC)
+        return KDA_ERR_SHAPE;
+    if (g.cu_seqlens == nullptr && (int64_t)g.total != (int64_t)g.n * g.max_t) return KDA_ERR_SHAPE;
+    if (cv->kernel_width < 1 || cv->kernel_width > kda::DCONV_KW_MAX || win->state_len < cv->kernel_width - 1 ||
+        win->state_len > kda::CONV_L_MAX || win->num_slots < 1 ||
+        (int64_t)win->channels != 2LL * g.h_qk * pool->k + (int64_t)pool->hv * pool->v ||
+        win->slot_stride < (int64_t)win->state_len * win->channels)
+        return KDA_ERR_SHAPE;
+    if (g.n == 0 || g.total == 0 || g.max_t == 0) return KDA_OK;
+    if (!g.slot_table || !g.a || !g.b || !g.o || !dev_status || !win->base || !cv->conv_slot || !cv->x ||
+        !cv->weight || !cv->counters)
+        return KDA_ERR_NULL;
+    if (!aligned(g.slot_table, 4) || !aligned(dev_status, 4) || !aligned(g.a, 4) || !aligned(g.b, 4) ||
+        !aligned(g.o, 4) || (g.cu_seqlens && !aligned(g.cu_seqlens, 4)) || (g.accepted && !aligned(g.accepted, 4)) ||
+        (g.a_log && !aligned(g.a_log, 4)) || (g.dt_bias && !aligned(g.dt_bias, 4)) || !aligned(win->base, es) ||
+        !aligned(cv->x, es) || (cv->y && !aligned(cv->y, es)) || !aligned(cv->conv_slot, 4) ||
+        !aligned(cv->weight, 4) || (cv->bias && !aligned(cv->bias, 4)) || !aligned(cv->counters, 4))
+        return KDA_ERR_ALIGN;
+    kda::StepParams prm = make_params(pool, g.slot_table, g.slot_table, g.reset, g.n, g.max_t, nullptr, nullptr,
+                                      nullptr, g.a, g.b, g.o, dev_status, flags);
+    prm.hqk = g.h_qk;
+    prm.init_stride = g.num_cols;
+    prm.snap_stride = g.num_cols;
+    prm.num_cols = g.num_cols;
+    prm.accepted = g.accepted;
+    prm.cu = g.cu_seqlens;
+    prm.total = g.total;
+    prm.a_log = g.a_log;
+    prm.dt_bias = g.dt_bias;
+    prm.mode = kda::MODE_PADDING;
+    prm.conv.window = win->base;
+    prm.conv.num_slots = win->num_slots;
+    prm.conv.slot_stride = win->slot_stride;
+    prm.conv.C = win->channels;
+    prm.conv.L = win->state_len;
+    prm.conv.KW = cv->kernel_width;
+    prm.conv.silu = cv->activation;
+    prm.conv.slot = cv->conv_slot;
+    prm.conv.x = cv->x;
+    prm.conv.w = cv->weight;
+    prm.conv.bias = cv->bias;
+    prm.conv.y = cv->y;
+    prm.conv.counters = cv->counters;
+    const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    switch (win->dtype) {
+        case KDA_F32: return launch_verify<float, true>(pool, prm, st);
+        case KDA_F16: return launch_verify<__half, true>(pool, prm, st);
+        default: return launch_verify<__nv_bfloat16, true>(pool, prm, st);
     }
 }
 

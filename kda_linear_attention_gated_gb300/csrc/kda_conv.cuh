@@ -23,6 +23,10 @@
 namespace kda {
 
 constexpr int CONV_KW_MAX = 8;   // kernel widths 1 .. 8
+// Kernel widths of the convolution fused into the recurrence kernels: 1 .. 4
+// (a history of up to three entries, held in registers).
+constexpr int DCONV_KW_MAX = 4;
+constexpr int DCONV_H = DCONV_KW_MAX - 1;
 constexpr int CONV_L_MAX = 32;   // window entries up to 32
 constexpr int CONV_THREADS = 256;      // threads per CTA, one channel each
 constexpr int CONV_VEC_THREADS = 128;  // threads per CTA, four channels each ...

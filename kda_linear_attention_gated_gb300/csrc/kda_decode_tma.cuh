@@ -56,11 +56,6 @@
 
 namespace kda {
 
-// Kernel widths of the decode step's fused convolution: 1 .. 4 (a history of
-// up to three entries, held in registers).
-constexpr int DCONV_KW_MAX = 4;
-constexpr int DCONV_H = DCONV_KW_MAX - 1;
-
 // The fused short convolution of a decode step (CONV), one channel, in
 // stages.  conv_load: the history entries h_0 .. h_(KW-2) of the window at
 // W[i C] (zero on reset), the weights and the bias, into registers.

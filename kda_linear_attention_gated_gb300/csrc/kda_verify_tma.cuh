@@ -47,6 +47,7 @@
 #include <type_traits>
 
 #include "kda_common.cuh"
+#include "kda_conv.cuh"
 
 #ifndef KDA_VER_MINB
 #define KDA_VER_MINB 3
@@ -152,10 +153,74 @@ __device__ __forceinline__ void ab_terms(float (&out)[32], const float (&bk)[TC]
     }
 }
 
+// The convolution fused in front of a speculative step (CONV), one channel:
+// its history right-aligned in DCONV_H slots and its weights left-padded to
+// match (slot i holds history entry i - (DCONV_H - (KW - 1)) and the weight
+// that multiplies it; the slots before are zero and skipped), so that token
+// j's taps are slots j .. DCONV_H - 1 of the history followed by the chunk's
+// inputs, every index known at compile time.  The fmaf chain runs the real
+// taps in ascending order and the input last, as the conv kernel does, so y
+// is bit-identical to kda_conv_step's.
+template <typename QT>
+__device__ __forceinline__ void sconv_load(QT (&z)[DCONV_H], float (&w)[DCONV_H], float& wl, float& b, const QT* W,
+                                           int C, int KW, int acc, bool rst, const float* wp, const float* bias) {
+    QT zero;
+    conv_round(0.f, zero);
+    const int pad = DCONV_H - (KW - 1);
+#pragma unroll
+    for (int i = 0; i < DCONV_H; ++i) {
+        z[i] = !rst && i >= pad ? W[(int64_t)(acc + i - pad) * C] : zero;
+        w[i] = i >= pad ? __ldg(wp + i - pad) : 0.f;
+    }
+    wl = __ldg(wp + KW - 1);
+    b = bias != nullptr ? __ldg(bias) : 0.f;
+}
+
+template <typename QT, int TC>
+__device__ __forceinline__ QT sconv_token(const QT (&z)[DCONV_H], const float (&w)[DCONV_H], float wl, float b,
+                                          const QT (&xs)[TC], int KW, int silu, int j) {
+    float s = b;
+#pragma unroll
+    for (int i = 0; i < DCONV_H; ++i)
+        if (i >= DCONV_H - (KW - 1)) s = fmaf(w[i], to_f32(j + i < DCONV_H ? z[(j + i) % DCONV_H] : xs[(j + i + TC - DCONV_H) % TC]), s);
+    s = fmaf(wl, to_f32(xs[j]), s);
+    QT out;
+    conv_round(silu ? silu_fast(s) : s, out);
+    return out;
+}
+
+// The window of one channel after a step of Tn tokens: entries e < kept take
+// the old entries m - kept + e (zero on reset), the rest the last nin inputs
+// (xc: the channel's input of the request's first token, rows C apart).
+// Sources lie at or above their destinations, and each batch is read whole
+// before it is written, so no entry is overwritten before it is read.
+template <typename QT>
+__device__ __forceinline__ void sconv_window_store(QT* W, const QT* xc, int C, int L, int m, int kept, int Tn,
+                                                   bool rst) {
+    QT zero;
+    conv_round(0.f, zero);
+    const int nin = min(Tn, L);
+    for (int e0 = 0; e0 < L; e0 += 8) {
+        QT v[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int e = e0 + u;
+            v[u] = e >= L ? zero
+                 : e < kept ? (rst ? zero : W[(int64_t)(m - kept + e) * C])
+                            : xc[(int64_t)(Tn - nin + e - kept) * C];
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+            if (e0 + u < L) W[(int64_t)(e0 + u) * C] = v[u];
+    }
+}
+
 // FULLK: K = KMAX, known at compile time (the row guards and loops fold away).
-template <typename ST, typename QT, int BV, bool FULLK, bool WIDE = false>
+// CONV on an fp32 pool: 2 CTAs per SM (128 registers), the 256-thread tile
+// having no room for the convolution's inputs under the 3-CTA cap of 80.
+template <typename ST, typename QT, int BV, bool FULLK, bool WIDE = false, bool CONV = false>
 __global__ void __launch_bounds__(VerifyShape<ST, BV, (int)sizeof(QT), WIDE>::NT,
-                                  VerifyShape<ST, BV, (int)sizeof(QT), WIDE>::MINB)
+                                  CONV && sizeof(ST) == 4 ? 2 : VerifyShape<ST, BV, (int)sizeof(QT), WIDE>::MINB)
 kda_verify_kernel(const __grid_constant__ CUtensorMap tmap, const StepParams p) {
 // key rows: KMAX in the K = KMAX build, else read from the parameters where used
 #define KK (FULLK ? KMAX : p.k)
@@ -209,19 +274,59 @@ kda_verify_kernel(const __grid_constant__ CUtensorMap tmap, const StepParams p) 
     using RT = typename std::conditional<sizeof(ST) == 4 && std::is_same<QT, __half>::value, float, QT>::type;
     RT kraw[TC], qraw[TC], vraw[TC];
     float araw[TC];
+    // CONV: the fused convolution makes q, k and v: thread r the q and k
+    // channels of key row r, thread j < vcols the tile's value column j, one
+    // channel at a time (its history at the accepted index, weights, bias and
+    // the chunk's inputs, then the chunk's y), so few registers are live at
+    // once; one chunk (the host refuses longer requests).  The window slot,
+    // accepted index and checks are set in the prologue before the first call.
+    int32_t cslot = 0;
+    int cacc = 0;
+    bool conv_ok = false;
     auto load_inputs = [&](int t0, int tc) {
-        const QT* qp = static_cast<const QT*>(p.q);
-        const QT* kp = static_cast<const QT*>(p.kk);
-        const QT* vp = static_cast<const QT*>(p.vv);
         const int row = rowt < KK ? rowt : 0, col = tid < vcols ? tid : 0;
+        if constexpr (CONV) {
+            const auto& cp = p.conv;
+            const QT* X = static_cast<const QT*>(cp.x);
+            const QT* W = static_cast<const QT*>(cp.window) + (int64_t)(conv_ok ? cslot : 0) * cp.slot_stride;
+            const bool rs = !conv_ok || (p.reset != nullptr && p.reset[n] != 0);  // no window read unless valid
+            QT* Y = static_cast<QT*>(cp.y);
+            auto chan = [&](int c, RT (&out)[TC], bool ywrite) {
+                QT z[DCONV_H], xs[TC];
+                float w[DCONV_H], wl, b;
+                sconv_load(z, w, wl, b, W + c, cp.C, cp.KW, cacc, rs, cp.w + (int64_t)c * cp.KW,
+                           cp.bias != nullptr ? cp.bias + c : nullptr);
 #pragma unroll
-        for (int j = 0; j < TC; ++j) {
-            const int64_t tok = (int64_t)tb + t0 + min(j, tc - 1);
-            const int64_t rq = (tok * p.hqk + hq) * KK + row, rt = tok * p.hv + h;
-            kraw[j] = (RT)kp[rq];
-            qraw[j] = (RT)qp[rq];
-            araw[j] = __ldg(p.a + rt * KK + row);
-            vraw[j] = (RT)vp[rt * p.v + (int64_t)cb * BV + col];
+                for (int j = 0; j < TC; ++j) xs[j] = X[((int64_t)tb + t0 + min(j, tc - 1)) * cp.C + c];
+#pragma unroll
+                for (int j = 0; j < TC; ++j) {
+                    const QT y = sconv_token(z, w, wl, b, xs, cp.KW, cp.silu, j);
+                    out[j] = (RT)y;
+                    if (ywrite && j < tc) Y[((int64_t)tb + t0 + j) * cp.C + c] = y;  // one writer of each y
+                }
+            };
+            // y only for a request whose window is valid (a padding request's
+            // rows are zeroed where it leaves; a bad one is left alone)
+            const bool yqk = Y != nullptr && conv_ok && h % (p.hv / p.hqk) == 0 && cb == 0 && rowt < KK && half == 0;
+            chan(hq * KK + row, qraw, yqk);
+            chan((p.hqk + hq) * KK + row, kraw, yqk);
+            chan(2 * p.hqk * KK + h * p.v + cb * BV + col, vraw, Y != nullptr && conv_ok && tid < vcols);
+#pragma unroll
+            for (int j = 0; j < TC; ++j)
+                araw[j] = __ldg(p.a + (((int64_t)tb + t0 + min(j, tc - 1)) * p.hv + h) * KK + row);
+        } else {
+            const QT* qp = static_cast<const QT*>(p.q);
+            const QT* kp = static_cast<const QT*>(p.kk);
+            const QT* vp = static_cast<const QT*>(p.vv);
+#pragma unroll
+            for (int j = 0; j < TC; ++j) {
+                const int64_t tok = (int64_t)tb + t0 + min(j, tc - 1);
+                const int64_t rq = (tok * p.hqk + hq) * KK + row, rt = tok * p.hv + h;
+                kraw[j] = (RT)kp[rq];
+                qraw[j] = (RT)qp[rq];
+                araw[j] = __ldg(p.a + rt * KK + row);
+                vraw[j] = (RT)vp[rt * p.v + (int64_t)cb * BV + col];
+            }
         }
     };
 
@@ -254,6 +359,19 @@ kda_verify_kernel(const __grid_constant__ CUtensorMap tmap, const StepParams p) 
     const int32_t snap0 = !final_mode && arg_ok && lane < Tn ? p.snap_slot[(int64_t)n * p.snap_stride + lane] : 0;
     const int32_t fin = final_mode ? p.final_slot[n] : -1;
     const bool issued = arg_ok && Tn > 0;  // the first chunk's inputs are requested
+    // CONV: the window slot and the geometry of its update (history at the
+    // accepted index acc = col; m = acc + KW - 1 entries before the inputs,
+    // kept = max(0, L - Tn) of them kept)
+    bool conv_geom = true, conv_slot_ok = true;
+    if constexpr (CONV) {
+        const auto& cp = p.conv;
+        cslot = arg_ok ? cp.slot[n] : 0;
+        cacc = col;
+        const int m = col + cp.KW - 1, kept = max(0, cp.L - Tn);
+        conv_geom = m <= cp.L && kept <= m;
+        conv_slot_ok = cslot >= 0 && cslot < cp.num_slots;
+        conv_ok = arg_ok && conv_geom && conv_slot_ok;
+    }
     // The first chunk's inputs: in the prologue, under the slot-id loads,
     // when the registers allow it (128-thread tiles); else with the chunk.
     constexpr bool PRO_INPUTS = SH::NT <= 128;
@@ -261,6 +379,8 @@ kda_verify_kernel(const __grid_constant__ CUtensorMap tmap, const StepParams p) 
     const bool padding = (p.mode & MODE_PADDING) != 0;
     auto slot_bad = [&](int32_t s) { return s >= p.num_slots || (s < 0 && !padding); };
     bool bad = !arg_ok || slot_bad(slot) || slot_bad(snap0) || fin >= p.num_slots;
+    const bool conv_bad = CONV && arg_ok && Tn > 0 && !(slot < 0 && padding) && !(conv_geom && conv_slot_ok);
+    bad |= conv_bad;
     for (int t = lane + 32; !final_mode && arg_ok && t < Tn; t += 32)
         bad |= slot_bad(p.snap_slot[(int64_t)n * p.snap_stride + t]);
     bad = __any_sync(0xffffffffu, bad);  // the same answer in every warp
@@ -283,7 +403,24 @@ kda_verify_kernel(const __grid_constant__ CUtensorMap tmap, const StepParams p) 
         if (pad)  // padding: this tile's outputs of every token are zero
             for (int e = tid; e < Tn * vcols; e += SH::NT)
                 p.o[((int64_t)(tb + e / vcols) * p.hv + h) * p.v + cb * BV + e % vcols] = 0.f;
-        if (tid == 0 && bad) atomicCAS(p.status, 0, arg_ok ? STATUS_SLOT_RANGE : STATUS_ARG);
+        if constexpr (CONV) {  // ... and so are its conv outputs (its window is left alone)
+            if (pad && p.conv.y != nullptr) {
+                const auto& cp = p.conv;
+                QT* Y = static_cast<QT*>(cp.y);
+                QT zero;
+                conv_round(0.f, zero);
+                const int qc = hq * KK + rowt, kc = (p.hqk + hq) * KK + rowt, vc = 2 * p.hqk * KK + h * p.v + cb * BV + tid;
+                for (int j = 0; j < Tn; ++j) {
+                    const int64_t row0 = ((int64_t)tb + j) * cp.C;
+                    if (h % (p.hv / p.hqk) == 0 && cb == 0 && rowt < KK && half == 0) {
+                        Y[row0 + qc] = zero;
+                        Y[row0 + kc] = zero;
+                    }
+                    if (tid < vcols) Y[row0 + vc] = zero;
+                }
+            }
+        }
+        if (tid == 0 && bad) atomicCAS(p.status, 0, arg_ok && conv_geom ? STATUS_SLOT_RANGE : STATUS_ARG);
         return;  // uniform; no state copy was issued
     }
     __syncthreads();  // barriers initialised
@@ -294,6 +431,7 @@ kda_verify_kernel(const __grid_constant__ CUtensorMap tmap, const StepParams p) 
     float2 x[ROWS][VP];
     bool state_in = false;
     bool alive = true;
+    int conv_prev = -1;  // CONV: this CTA's read count before its own, once counted
     if (Tn == 0) {  // prefill, empty prompt: the loaded tile (or zeros) goes to the final slot as is
         const bool ok = rst || mbar_wait(bar_st, 0);
         if (__syncthreads_or(ok ? 0 : 1)) {
@@ -316,7 +454,9 @@ kda_verify_kernel(const __grid_constant__ CUtensorMap tmap, const StepParams p) 
     const float gbias = p.dt_bias != nullptr && rowt < KK ? __ldg(p.dt_bias + (int64_t)h * KK + rowt) : 0.f;
     for (int t0 = 0; t0 < Tn; t0 += TC) {
         const int tc = min(TC, Tn - t0);
-        if (t0 > 0 || !PRO_INPUTS) load_inputs(t0, tc);
+        // CONV: one chunk (the host refuses longer requests), so the conv's
+        // history and weights die with the first call
+        if (CONV ? (t0 == 0 && !PRO_INPUTS) : (t0 > 0 || !PRO_INPUTS)) load_inputs(t0, tc);
         if (tid < tc) {
             bsm[tid] = __ldg(p.b + ((int64_t)tb + t0 + tid) * p.hv + h);
             snaps[tid] = final_mode ? -1 : p.snap_slot[(int64_t)n * p.snap_stride + t0 + tid];
@@ -417,6 +557,13 @@ kda_verify_kernel(const __grid_constant__ CUtensorMap tmap, const StepParams p) 
                 alive = false;
                 break;
             }
+        }
+        if constexpr (CONV) {
+            // every thread has used the window values it read (they fed the
+            // row pass, before the barrier above): thread 0 counts the CTA's
+            // read of its q/k windows; the result is needed only at the end
+            if (tid == 0 && t0 == 0 && (p.hv / p.hqk) * vt > 1)
+                conv_prev = atomicAdd(p.conv.counters + (int64_t)n * p.hqk + hq, 1);
         }
         if (!state_in) {
 #pragma unroll
@@ -642,6 +789,40 @@ kda_verify_kernel(const __grid_constant__ CUtensorMap tmap, const StepParams p) 
         }
         // the next chunk rewrites the gates, d and the token scalars
         __syncthreads();
+    }
+    // CONV: the windows' update, all threads together.  A value column's
+    // window belongs to this CTA; a q/k channel's is read by every CTA of the
+    // request's value heads sharing the q/k head, and the one whose count
+    // completes it writes the new entries and puts the count back to zero.
+    // No CTA waits for another.  conv_prev < 0: not counted yet (a wait that
+    // ran out before the count).
+    if constexpr (CONV) {
+        const auto& cp = p.conv;
+        const int m = col + cp.KW - 1, kept = max(0, cp.L - Tn), readers = (p.hv / p.hqk) * vt;
+        QT* W = static_cast<QT*>(cp.window) + (int64_t)cslot * cp.slot_stride;
+        const QT* X = static_cast<const QT*>(cp.x) + (int64_t)tb * cp.C;
+        if (tid < vcols) {
+            const int vc = 2 * p.hqk * KK + h * p.v + cb * BV + tid;
+            sconv_window_store(W + vc, X + vc, cp.C, cp.L, m, kept, Tn, rst);
+        }
+        bool last = true;
+        if (readers > 1) {
+            int* flag = snaps + TC - 1;  // the last token's snapshot id is no longer needed
+            __syncthreads();
+            if (tid == 0) {
+                int* cnt = cp.counters + (int64_t)n * p.hqk + hq;
+                const bool done = (conv_prev >= 0 ? conv_prev : atomicAdd(cnt, 1)) == readers - 1;
+                if (done) atomicExch(cnt, 0);
+                *flag = done ? 1 : 0;
+            }
+            __syncthreads();
+            last = *flag != 0;
+        }
+        if (last && rowt < KK && half == 0) {
+            const int qc = hq * KK + rowt, kc = (p.hqk + hq) * KK + rowt;
+            sconv_window_store(W + qc, X + qc, cp.C, cp.L, m, kept, Tn, rst);
+            sconv_window_store(W + kc, X + kc, cp.C, cp.L, m, kept, Tn, rst);
+        }
     }
     // prefill: the state after the last token, staged rounded in buffer 0 (free:
     // no snapshot store used it) and stored as one box

@@ -328,6 +328,80 @@ def make_decode_conv(n=64, hv=12, h_qk=12, k=128, v=128, kw=4, L=3, num_slots=25
 
 
 @dataclass
+class StepConvInputs:
+    """CPU tensors of one speculative step with the short convolution fused in front."""
+    pool: torch.Tensor                 # [num_slots, HV, K, V]
+    slot_table: torch.Tensor           # int32 [N, num_cols] (a padding request's row is -1)
+    accepted: torch.Tensor             # int32 [N]
+    cu_seqlens: torch.Tensor | None    # int32 [N + 1] or None
+    max_t: int
+    window: torch.Tensor               # [num_wslots, L, C]
+    conv_slot: torch.Tensor            # int32 [N] (-1 for a padding request)
+    x: torch.Tensor                    # [total, C]: q | k | v channels
+    weight: torch.Tensor               # fp32 [C, KW]
+    bias: torch.Tensor | None
+    a: torch.Tensor                    # fp32 [total, HV, K]
+    b: torch.Tensor                    # fp32 [total, HV]
+    reset: torch.Tensor | None = None
+    a_log: torch.Tensor | None = None
+    dt_bias: torch.Tensor | None = None
+    h_qk: int = 12
+    meta: dict = field(default_factory=dict)
+
+    def to(self, device) -> "StepConvInputs":
+        mv = lambda t: None if t is None else t.to(device)  # noqa: E731
+        return StepConvInputs(mv(self.pool), mv(self.slot_table), mv(self.accepted), mv(self.cu_seqlens), self.max_t,
+                              mv(self.window), mv(self.conv_slot), mv(self.x), mv(self.weight), mv(self.bias),
+                              mv(self.a), mv(self.b), mv(self.reset), mv(self.a_log), mv(self.dt_bias), self.h_qk,
+                              dict(self.meta))
+
+
+def make_step_conv(n=8, num_spec=4, t_lens=None, h_qk=12, hv=12, k=128, v=128, kw=4, num_slots=256, num_wslots=64,
+                   state_dtype=torch.float16, dtype=torch.bfloat16, seed=60, reset_p=0.0, pad_p=0.0,
+                   gate_scale=False, bias=True) -> StepConvInputs:
+    """A speculative step of n requests (num_spec + 1 tokens each, or t_lens)
+    with the conv window in front: L = kw - 1 + num_spec entries, a slot table
+    of num_spec + 1 distinct slots per request; accepted[r] drawn uniformly
+    among the values a request of T_r tokens admits (the window keeps
+    L - T_r old entries, which must lie below acc + kw - 1): max(1, num_spec -
+    T_r + 1) .. num_spec + 1.  Window, x ~ N(0, 1) in dtype, weight ~
+    N(0, 1 / kw), bias ~ N(0, 0.1^2) as in make_conv; the pool, a, b as in
+    make_general; padding requests (probability pad_p) have a slot-table row
+    and a window slot of -1."""
+    g = torch.Generator().manual_seed(seed)
+    L = kw - 1 + num_spec
+    ncols = num_spec + 1
+    lens = [ncols] * n if t_lens is None else list(t_lens)
+    if max(lens) > ncols:
+        raise ValueError("a request has more tokens than num_spec + 1")
+    total = sum(lens)
+    C = 2 * h_qk * k + hv * v
+    P = make_pool(g, num_slots, hv, k, v, state_dtype)
+    table = torch.randperm(num_slots, generator=g)[:n * ncols].to(torch.int32).reshape(n, ncols).clone()
+    acc = torch.tensor([int(torch.randint(max(1, num_spec - t + 1), ncols + 1, (1,), generator=g)) for t in lens],
+                       dtype=torch.int32)
+    W = _randn(g, (num_wslots, L, C), dtype)
+    cslots = torch.randperm(num_wslots, generator=g)[:n].to(torch.int32)
+    x = _randn(g, (total, C), dtype)
+    w = _randn(g, (C, kw), std=1.0 / kw ** 0.5)
+    bv = _randn(g, (C,), std=0.1) if bias else None
+    a = _randn(g, (total, hv, k))
+    b = _randn(g, (total, hv))
+    reset = (torch.rand((n,), generator=g) < reset_p).to(torch.uint8) if reset_p > 0 else None
+    if pad_p > 0:
+        pad = torch.rand((n,), generator=g) < pad_p
+        table[pad] = -1
+        cslots[pad] = -1
+    a_log, dt_bias = _gate_scale(g, hv, k) if gate_scale else (None, None)
+    cu = None
+    if t_lens is not None:
+        cu = torch.zeros(n + 1, dtype=torch.int32)
+        cu[1:] = torch.cumsum(torch.tensor(lens, dtype=torch.int64), 0).to(torch.int32)
+    return StepConvInputs(P, table, acc, cu, max(lens), W, cslots, x, w, bv, a, b, reset, a_log, dt_bias, h_qk,
+                          dict(kind="step_conv", n=n, num_spec=num_spec, lens=lens, kw=kw, L=L, seed=seed))
+
+
+@dataclass
 class PrefillInputs:
     """CPU tensors of one prefill call over packed prompts."""
     pool: torch.Tensor

@@ -257,6 +257,60 @@ def test_decode_conv_step_refusals_before_any_launch(libs):
     assert call(win(), args(n=0)) == kda.KDA_OK               # nothing to do: no launch
 
 
+def test_step_conv_refusals_before_any_launch(libs):
+    """kda_step_conv's host checks (include/kda.h, kda_step_conv_args): those of
+    kda_step, the window's, and the fused form's own (speculative, at most 8
+    tokens a request, q/k/v left to the convolution)."""
+    L = libs[torch.float16]
+    P = 0x7F0000100000
+    C = 2 * 12 * 128 + 12 * 128
+
+    def win(**kw):
+        f = dict(base=P, dtype=kda.KDA_BF16, channels=C, state_len=7, reserved=0, num_slots=64, slot_stride=7 * C)
+        f.update(kw)
+        return kda.ConvWindowDesc(**f)
+
+    def step(**kw):
+        f = dict(n=8, total=64, max_t=8, h_qk=12, num_cols=8, in_place=0, qkv_dtype=kda.KDA_BF16, reserved=0,
+                 cu_seqlens=None, slot_table=P, accepted=None, reset=None, q=None, k=None, v=None, a=P, b=P,
+                 a_log=None, dt_bias=None, o=P)
+        f.update(kw)
+        return kda.StepArgs(**f)
+
+    def conv(**kw):
+        f = dict(kernel_width=4, activation=1, conv_slot=P, x=P, weight=P, bias=None, y=None, counters=P)
+        f.update(kw)
+        return kda.StepConvArgs(**f)
+
+    def call(st=None, w=None, cv=None, d=None, flags=0):
+        return L.kda_step_conv_raw(d or desc(kda.KDA_F16), st or step(), w or win(), cv or conv(), P, None, flags)
+
+    assert L.lib.kda_step_conv(ctypes.byref(desc(kda.KDA_F16)), None, ctypes.byref(win()), ctypes.byref(conv()),
+                               P, 0, None) == kda.KDA_ERR_NULL
+    assert call(d=desc(kda.KDA_F32)) == kda.KDA_ERR_DTYPE_MISMATCH
+    assert call(w=win(dtype=7)) == kda.KDA_ERR_DTYPE_UNSUPPORTED
+    assert call(st=step(in_place=1)) == kda.KDA_ERR_ARG                      # the decode form is elsewhere
+    assert call(st=step(q=P)) == kda.KDA_ERR_ARG                             # the convolution makes q/k/v
+    assert call(st=step(qkv_dtype=kda.KDA_F16)) == kda.KDA_ERR_ARG           # not the window's dtype
+    assert call(cv=conv(activation=2)) == kda.KDA_ERR_ARG
+    assert call(flags=kda.KDA_LAUNCH_TEST_WITHHOLD_STATE) == kda.KDA_ERR_ARG
+    assert call(st=step(max_t=9, num_cols=9, total=72)) == kda.KDA_ERR_SHAPE  # one chunk of 8 at most
+    assert call(w=win(channels=C - 1)) == kda.KDA_ERR_SHAPE
+    assert call(st=step(h_qk=5)) == kda.KDA_ERR_SHAPE
+    assert call(st=step(total=63)) == kda.KDA_ERR_SHAPE
+    assert call(cv=conv(kernel_width=5)) == kda.KDA_ERR_SHAPE
+    assert call(w=win(state_len=2)) == kda.KDA_ERR_SHAPE
+    assert call(w=win(state_len=33, slot_stride=33 * C)) == kda.KDA_ERR_SHAPE
+    assert call(w=win(slot_stride=7 * C - 1)) == kda.KDA_ERR_SHAPE
+    for name in ("conv_slot", "x", "weight", "counters"):
+        assert call(cv=conv(**{name: None})) == kda.KDA_ERR_NULL, name
+    assert call(st=step(slot_table=None)) == kda.KDA_ERR_NULL
+    assert call(cv=conv(x=P + 1)) == kda.KDA_ERR_ALIGN
+    assert call(cv=conv(counters=P + 2)) == kda.KDA_ERR_ALIGN
+    assert call(st=step(a=P + 2)) == kda.KDA_ERR_ALIGN
+    assert call(st=step(n=0, total=0)) == kda.KDA_OK  # nothing to do: no launch
+
+
 def test_layout_id_names_dtype_and_shape(libs):
     """Pull request 2130, What: the checkpoint layout id names the dtype, so an
     fp16 build cannot read an fp32 build's checkpoint images."""
