@@ -547,6 +547,8 @@ def main():
         elif args.case == "conv_decode":
             res = {f"decode_conv_{nm}_n64": bench_decode_conv(kda, workloads, torch, l2, peak, sd)
                    for nm, sd in (("fp32", torch.float32), ("fp16", torch.float16))}
+            res.update({f"step_conv_n{n_sc}_t8_fp16": bench_step_conv(kda, workloads, torch, l2, peak, n_sc)
+                        for n_sc in (8, 32)})
         elif args.case == "prefill":
             res = {f"prefill_{n}x{t}_fp16{'_chunked' if c else ''}": bench_prefill(kda, workloads, torch, n, t, c)
                    for c in (False, True) for n, t in ((1, 8192), (8, 1024), (64, 128))}
@@ -597,6 +599,8 @@ def main():
         extra["conv_step_n64_t5_bf16"] = bench_conv(kda, workloads, torch, peak)
         for sd_name, sd in (("fp32", torch.float32), ("fp16", torch.float16)):
             extra[f"decode_conv_{sd_name}_n64"] = bench_decode_conv(kda, workloads, torch, l2, peak, sd)
+        for n_sc in (8, 32):
+            extra[f"step_conv_n{n_sc}_t8_fp16"] = bench_step_conv(kda, workloads, torch, l2, peak, n_sc)
         extra["copy_floor"] = bench_copy_floor(kda, torch, l2, peak)
         extra["prefill_8x1024_fp16"] = bench_prefill(kda, workloads, torch, 8, 1024)
         extra["prefill_8x1024_fp16_chunked"] = bench_prefill(kda, workloads, torch, 8, 1024, True)
@@ -958,6 +962,72 @@ def bench_step(kda, workloads, torch, l2, peak, n=32, t=8, replays=400):
             "us_per_step": round(us, 3), "gbs": round(byt / (us * 1e-6) / 1e9, 1),
             "frac_of_peak": round(byt / (us * 1e-6) / 1e9 / peak, 4), "bytes_per_step": byt, "pools": R,
             "launch": f"{GRAPH_TIMED} ({n_timed}, over {R} pools); flags KDA_LAUNCH_PDL|KDA_LAUNCH_PDL_EARLY_STATE"}
+
+
+def bench_step_conv(kda, workloads, torch, l2, peak, n, t=8, replays=400):
+    """The speculative step with the short convolution fused in front
+    (kda_step_conv): N requests x T=8 tokens (one accepted + seven drafts) on
+    an fp16 pool, each request's accepted column of an [N][8] slot table, the
+    learned gate scale; q/k/v from a bf16 conv of width 4 over a window of
+    kernel - 1 + 7 = 10 entries (C = 4608).  Beside it, the same work as two
+    launches: kda_conv_step then kda_step, both with PDL and early reads; that
+    step reads q/k/v buffers of its own layout (the conv's [total][C] y would
+    need a copy to become them, not counted).  Pool/window sets rotate past
+    L2.  Algorithmic bytes: the initial state read and T snapshots written, x,
+    a, b read, o written, the window's history read and its L entries
+    written."""
+    lib = kda.KdaLibrary(torch.float16)
+    kw, spec = 4, t - 1
+    L = kw - 1 + spec
+    per = n * (1 + t) * HV * K * V * 2
+    R = max(2, math.ceil(4 * l2 / per) + 1)
+    sets = [workloads.make_step_conv(n=n, num_spec=spec, kw=kw, num_slots=n * t, num_wslots=n,
+                                     state_dtype=torch.float16, seed=100 + i, gate_scale=True).to("cuda")
+            for i in range(R)]
+    C, total = sets[0].x.shape[1], n * t
+    o = torch.empty(total, HV, V, device="cuda")
+    ys = [torch.empty_like(d.x) for d in sets]
+    qkv = [(torch.empty(total, HV, K, dtype=torch.bfloat16, device="cuda").normal_(),
+            torch.empty(total, HV, K, dtype=torch.bfloat16, device="cuda").normal_(),
+            torch.empty(total, HV, V, dtype=torch.bfloat16, device="cuda").normal_()) for _ in range(R)]
+    counters = torch.zeros(n, HV, dtype=torch.int32, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    stream = torch.cuda.Stream()
+    flags = kda.KDA_LAUNCH_PDL | kda.KDA_LAUNCH_PDL_EARLY_STATE
+
+    def fused(i):
+        d = sets[i % R]
+        lib.kda_step_conv(d.pool, d.window, d.slot_table, d.conv_slot, d.x, d.weight, d.a, d.b, o, status, counters,
+                          max_t=t, accepted=d.accepted, a_log=d.a_log, dt_bias=d.dt_bias, bias=d.bias, flags=flags)
+
+    def two(i):
+        d, (q, k, v) = sets[i % R], qkv[i % R]
+        lib.kda_conv_step(d.window, d.conv_slot, d.x, d.weight, ys[i % R], status, bias=d.bias, max_t=t,
+                          accepted=d.accepted, flags=flags)
+        lib.kda_step(d.pool, d.slot_table, q, k, v, d.a, d.b, o, status, max_t=t, accepted=d.accepted,
+                     a_log=d.a_log, dt_bias=d.dt_bias, flags=flags)
+    with torch.cuda.stream(stream):
+        fused(0)
+        two(0)
+    n_timed = R * max(1, replays // R)
+    us = graph_timed(torch, stream, fused, n_timed) * 1e3 / n_timed
+    us2 = graph_timed(torch, stream, two, n_timed) * 1e3 / n_timed
+    if int(status.item()) != 0 or int(counters.abs().sum().item()) != 0:
+        raise RuntimeError(f"device status {int(status.item())}")
+    byt = (n * HV * K * V * 2 * (1 + t) + total * (C * 2 + HV * K * 4 + HV * 4 + HV * V * 4)
+           + n * C * 2 * ((kw - 1) + L))
+    del sets, ys, qkv
+    torch.cuda.empty_cache()
+    return {"workload": f"speculative step with the conv fused in front (kda_step_conv), N={n} x T={t} "
+                        f"(1 accepted + {t - 1} drafts), fp16 pool, bf16 conv window of {L} entries, width {kw}, "
+                        "C=4608, learned gate scale",
+            "us_per_step": round(us, 3), "gbs": round(byt / (us * 1e-6) / 1e9, 1),
+            "frac_of_peak": round(byt / (us * 1e-6) / 1e9 / peak, 4), "bytes_per_step": byt,
+            "two_launches_us": round(us2, 3),
+            "two_launches": "kda_conv_step then kda_step, each PDL with early reads (y's relayout into the step's "
+                            "q/k/v not counted)",
+            "launch": f"{GRAPH_TIMED} ({n_timed} steps, over {R} pool/window sets); flags "
+                      "KDA_LAUNCH_PDL|KDA_LAUNCH_PDL_EARLY_STATE"}
 
 
 def bench_verify(kda, workloads, torch, args, l2, peak, state_dtype=None, replays=400):

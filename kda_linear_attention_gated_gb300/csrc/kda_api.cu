@@ -317,9 +317,11 @@ int launch_verify_shape(const kda_pool* pool, const kda::StepParams& prm, cudaSt
     constexpr size_t smem = kda::verify_smem_bytes<state_t, BV, (int)sizeof(QT), WIDE>();
     // an fp16 pool at K = 128 gets the build with compile-time row loops; an
     // fp32 pool's 256-thread tiles have no register room for it (it spills)
+    // (the fused convolution's wide shape exists for K = 128 only: see launch_verify)
     constexpr bool kFullkOk = sizeof(state_t) == 2;
-    auto kernel = (kFullkOk && prm.k == kda::KMAX) ? kda::kda_verify_kernel<state_t, QT, BV, kFullkOk, WIDE, CONV>
-                                                   : kda::kda_verify_kernel<state_t, QT, BV, false, WIDE, CONV>;
+    auto kernel = (kFullkOk && prm.k == kda::KMAX) || (CONV && WIDE)
+                      ? kda::kda_verify_kernel<state_t, QT, BV, kFullkOk, WIDE, CONV>
+                      : kda::kda_verify_kernel<state_t, QT, BV, false, WIDE && !CONV, CONV>;
     CUtensorMap map;
     int rc = make_pool_map(pool, BV, &map);
     if (rc != KDA_OK) return rc;
@@ -353,7 +355,10 @@ int launch_verify(const kda_pool* pool, const kda::StepParams& prm, cudaStream_t
         const int rc = occupancy(reinterpret_cast<const void*>(kda::kda_verify_kernel<state_t, QT, BV, false>),
                                  SH::NT, smem, &occ, &sms);
         if (rc != KDA_OK) return rc;
-        if (tiles > (int64_t)occ * sms) return launch_verify_shape<QT, kWideOk, CONV>(pool, prm, stream, tiles);
+        // the fused convolution's wide build at K < 128 has no register room:
+        // those launches keep the default shape, in more waves
+        if (tiles > (int64_t)occ * sms && (!CONV || prm.k == kda::KMAX))
+            return launch_verify_shape<QT, kWideOk, CONV>(pool, prm, stream, tiles);
     }
     return launch_verify_shape<QT, false, CONV>(pool, prm, stream, tiles);
 }

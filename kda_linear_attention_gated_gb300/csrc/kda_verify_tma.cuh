@@ -157,10 +157,10 @@ __device__ __forceinline__ void ab_terms(float (&out)[32], const float (&bk)[TC]
 // its history right-aligned in DCONV_H slots and its weights left-padded to
 // match (slot i holds history entry i - (DCONV_H - (KW - 1)) and the weight
 // that multiplies it; the slots before are zero and skipped), so that token
-// j's taps are slots j .. DCONV_H - 1 of the history followed by the chunk's
-// inputs, every index known at compile time.  The fmaf chain runs the real
-// taps in ascending order and the input last, as the conv kernel does, so y
-// is bit-identical to kda_conv_step's.
+// j's taps are slots j .. j + DCONV_H - 1 of (history ++ the chunk's inputs)
+// and then the input itself.  The fmaf chain runs the real taps in ascending
+// order and the input last, as the conv kernel does, so y is bit-identical to
+// kda_conv_step's.
 template <typename QT>
 __device__ __forceinline__ void sconv_load(QT (&z)[DCONV_H], float (&w)[DCONV_H], float& wl, float& b, const QT* W,
                                            int C, int KW, int acc, bool rst, const float* wp, const float* bias) {
@@ -189,29 +189,70 @@ __device__ __forceinline__ QT sconv_token(const QT (&z)[DCONV_H], const float (&
     return out;
 }
 
-// The window of one channel after a step of Tn tokens: entries e < kept take
-// the old entries m - kept + e (zero on reset), the rest the last nin inputs
-// (xc: the channel's input of the request's first token, rows C apart).
-// Sources lie at or above their destinations, and each batch is read whole
-// before it is written, so no entry is overwritten before it is read.
-template <typename QT>
-__device__ __forceinline__ void sconv_window_store(QT* W, const QT* xc, int C, int L, int m, int kept, int Tn,
-                                                   bool rst) {
+// The window of a channel after a step of Tn tokens is the last L entries of
+// S = (old entries W[0 .. m-1]) ++ (the inputs x_0 .. x_(Tn-1)), m = acc +
+// KW - 1 (old entries zero on reset).  From registers: z holds S[m - DCONV_H
+// + i] in its real slots (the history) and xs[j] = S[m + j]; each register's
+// destination is computed, no register index is.  Older kept entries (below
+// the history) are read again first, in batches read whole before they are
+// written: their sources lie at or above their destinations and may be
+// register destinations too, so they move before those are written.
+template <typename QT, int TC>
+__device__ __forceinline__ void sconv_window_store_regs(QT* W, int C, int L, int KW, int m, int Tn, bool rst,
+                                                        const QT (&z)[DCONV_H], const QT (&xs)[TC]) {
     QT zero;
     conv_round(0.f, zero);
-    const int nin = min(Tn, L);
-    for (int e0 = 0; e0 < L; e0 += 8) {
+    const int first = m + Tn - L;     // S index of new entry 0 (>= 0: kept <= m)
+    const int lo = m - (KW - 1);      // the lowest S index the registers hold
+    for (int e0 = 0; first + e0 < lo && e0 < L; e0 += 8) {
         QT v[8];
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
             const int e = e0 + u;
-            v[u] = e >= L ? zero
-                 : e < kept ? (rst ? zero : W[(int64_t)(m - kept + e) * C])
-                            : xc[(int64_t)(Tn - nin + e - kept) * C];
+            v[u] = first + e < lo && e < L && !rst ? W[(int64_t)(first + e) * C] : zero;
         }
 #pragma unroll
         for (int u = 0; u < 8; ++u)
-            if (e0 + u < L) W[(int64_t)(e0 + u) * C] = v[u];
+            if (first + e0 + u < lo && e0 + u < L) W[(int64_t)(e0 + u) * C] = v[u];
+    }
+#pragma unroll
+    for (int i = 0; i < DCONV_H; ++i) {
+        const int e = m - DCONV_H + i - first;
+        if (i >= DCONV_H - (KW - 1) && e >= 0 && e < L) W[(int64_t)e * C] = z[i];
+    }
+#pragma unroll
+    for (int j = 0; j < TC; ++j) {
+        const int e = m + j - first;
+        if (j < Tn && e >= 0 && e < L) W[(int64_t)e * C] = xs[j];
+    }
+}
+
+// The same window update for two channels c0, c1 from memory (the q/k
+// windows, written by their last reader at the end): all of a batch of 16
+// entries of both channels are read before any is written, so a window of up
+// to 16 entries costs one round trip.
+template <typename QT>
+__device__ __forceinline__ void sconv_window_store2(QT* W, const QT* X, int c0, int c1, int C, int L, int m, int Tn,
+                                                    bool rst) {
+    QT zero;
+    conv_round(0.f, zero);
+    const int kept = max(0, L - Tn), nin = min(Tn, L);
+    for (int e0 = 0; e0 < L; e0 += 16) {
+        QT v0[16], v1[16];
+#pragma unroll
+        for (int u = 0; u < 16; ++u) {
+            const int e = e0 + u;
+            const bool old = e < kept;
+            const int64_t src = old ? (int64_t)(m - kept + e) * C : (int64_t)(Tn - nin + e - kept) * C;
+            v0[u] = e >= L || (old && rst) ? zero : (old ? W[src + c0] : X[src + c0]);
+            v1[u] = e >= L || (old && rst) ? zero : (old ? W[src + c1] : X[src + c1]);
+        }
+#pragma unroll
+        for (int u = 0; u < 16; ++u)
+            if (e0 + u < L) {
+                W[(int64_t)(e0 + u) * C + c0] = v0[u];
+                W[(int64_t)(e0 + u) * C + c1] = v1[u];
+            }
     }
 }
 
@@ -275,45 +316,54 @@ kda_verify_kernel(const __grid_constant__ CUtensorMap tmap, const StepParams p) 
     RT kraw[TC], qraw[TC], vraw[TC];
     float araw[TC];
     // CONV: the fused convolution makes q, k and v: thread r the q and k
-    // channels of key row r, thread j < vcols the tile's value column j, one
-    // channel at a time (its history at the accepted index, weights, bias and
-    // the chunk's inputs, then the chunk's y), so few registers are live at
-    // once; one chunk (the host refuses longer requests).  The window slot,
-    // accepted index and checks are set in the prologue before the first call.
+    // channels of key row r, thread j < vcols the tile's value column j.  The
+    // window slot, accepted index and checks are set in the prologue, which
+    // also loads each channel's history (at the accepted index), weights and
+    // bias (early with KDA_LAUNCH_PDL_EARLY_STATE); load_inputs then issues
+    // every input of the chunk before the first sum.  One chunk: the host
+    // refuses longer requests.  The value column's inputs stay for its window.
     int32_t cslot = 0;
     int cacc = 0;
     bool conv_ok = false;
+    QT zq[DCONV_H], zk[DCONV_H], zv[DCONV_H], xv[TC];
+    float wq[DCONV_H], wk[DCONV_H], wv[DCONV_H], lq = 0.f, lk = 0.f, lv = 0.f, bq = 0.f, bk = 0.f, bv = 0.f;
     auto load_inputs = [&](int t0, int tc) {
         const int row = rowt < KK ? rowt : 0, col = tid < vcols ? tid : 0;
         if constexpr (CONV) {
             const auto& cp = p.conv;
             const QT* X = static_cast<const QT*>(cp.x);
-            const QT* W = static_cast<const QT*>(cp.window) + (int64_t)(conv_ok ? cslot : 0) * cp.slot_stride;
-            const bool rs = !conv_ok || (p.reset != nullptr && p.reset[n] != 0);  // no window read unless valid
-            QT* Y = static_cast<QT*>(cp.y);
-            auto chan = [&](int c, RT (&out)[TC], bool ywrite) {
-                QT z[DCONV_H], xs[TC];
-                float w[DCONV_H], wl, b;
-                sconv_load(z, w, wl, b, W + c, cp.C, cp.KW, cacc, rs, cp.w + (int64_t)c * cp.KW,
-                           cp.bias != nullptr ? cp.bias + c : nullptr);
+            const int qc = hq * KK + row, kc = (p.hqk + hq) * KK + row, vc = 2 * p.hqk * KK + h * p.v + cb * BV + col;
+            QT xq[TC], xk[TC];
 #pragma unroll
-                for (int j = 0; j < TC; ++j) xs[j] = X[((int64_t)tb + t0 + min(j, tc - 1)) * cp.C + c];
-#pragma unroll
-                for (int j = 0; j < TC; ++j) {
-                    const QT y = sconv_token(z, w, wl, b, xs, cp.KW, cp.silu, j);
-                    out[j] = (RT)y;
-                    if (ywrite && j < tc) Y[((int64_t)tb + t0 + j) * cp.C + c] = y;  // one writer of each y
-                }
-            };
+            for (int j = 0; j < TC; ++j) {
+                const int64_t tok = (int64_t)tb + t0 + min(j, tc - 1);
+                xq[j] = X[tok * cp.C + qc];
+                xk[j] = X[tok * cp.C + kc];
+                xv[j] = X[tok * cp.C + vc];
+                araw[j] = __ldg(p.a + (tok * p.hv + h) * KK + row);
+            }
             // y only for a request whose window is valid (a padding request's
             // rows are zeroed where it leaves; a bad one is left alone)
+            QT* Y = static_cast<QT*>(cp.y);
             const bool yqk = Y != nullptr && conv_ok && h % (p.hv / p.hqk) == 0 && cb == 0 && rowt < KK && half == 0;
-            chan(hq * KK + row, qraw, yqk);
-            chan((p.hqk + hq) * KK + row, kraw, yqk);
-            chan(2 * p.hqk * KK + h * p.v + cb * BV + col, vraw, Y != nullptr && conv_ok && tid < vcols);
+            const bool yvv = Y != nullptr && conv_ok && tid < vcols;
 #pragma unroll
-            for (int j = 0; j < TC; ++j)
-                araw[j] = __ldg(p.a + (((int64_t)tb + t0 + min(j, tc - 1)) * p.hv + h) * KK + row);
+            for (int j = 0; j < TC; ++j) {
+                const QT yq = sconv_token(zq, wq, lq, bq, xq, cp.KW, cp.silu, j);
+                const QT yk = sconv_token(zk, wk, lk, bk, xk, cp.KW, cp.silu, j);
+                const QT yw = sconv_token(zv, wv, lv, bv, xv, cp.KW, cp.silu, j);
+                qraw[j] = (RT)yq;
+                kraw[j] = (RT)yk;
+                vraw[j] = (RT)yw;
+                if (j < tc) {  // one writer of each y
+                    const int64_t tok = (int64_t)tb + t0 + j;
+                    if (yqk) {
+                        Y[tok * cp.C + qc] = yq;
+                        Y[tok * cp.C + kc] = yk;
+                    }
+                    if (yvv) Y[tok * cp.C + vc] = yw;
+                }
+            }
         } else {
             const QT* qp = static_cast<const QT*>(p.q);
             const QT* kp = static_cast<const QT*>(p.kk);
@@ -371,6 +421,18 @@ kda_verify_kernel(const __grid_constant__ CUtensorMap tmap, const StepParams p) 
         conv_geom = m <= cp.L && kept <= m;
         conv_slot_ok = cslot >= 0 && cslot < cp.num_slots;
         conv_ok = arg_ok && conv_geom && conv_slot_ok;
+        if (issued) {  // no window read unless valid (zero history otherwise)
+            const bool rs = !conv_ok || (p.reset != nullptr && p.reset[n] != 0);
+            const QT* W = static_cast<const QT*>(cp.window) + (int64_t)(conv_ok ? cslot : 0) * cp.slot_stride;
+            const int row = rowt < KK ? rowt : 0, vcol = tid < vcols ? tid : 0;
+            const int qc = hq * KK + row, kc = (p.hqk + hq) * KK + row, vc = 2 * p.hqk * KK + h * p.v + cb * BV + vcol;
+            sconv_load(zq, wq, lq, bq, W + qc, cp.C, cp.KW, cacc, rs, cp.w + (int64_t)qc * cp.KW,
+                       cp.bias != nullptr ? cp.bias + qc : nullptr);
+            sconv_load(zk, wk, lk, bk, W + kc, cp.C, cp.KW, cacc, rs, cp.w + (int64_t)kc * cp.KW,
+                       cp.bias != nullptr ? cp.bias + kc : nullptr);
+            sconv_load(zv, wv, lv, bv, W + vc, cp.C, cp.KW, cacc, rs, cp.w + (int64_t)vc * cp.KW,
+                       cp.bias != nullptr ? cp.bias + vc : nullptr);
+        }
     }
     // The first chunk's inputs: in the prologue, under the slot-id loads,
     // when the registers allow it (128-thread tiles); else with the chunk.
@@ -424,6 +486,21 @@ kda_verify_kernel(const __grid_constant__ CUtensorMap tmap, const StepParams p) 
         return;  // uniform; no state copy was issued
     }
     __syncthreads();  // barriers initialised
+    // CONV: a value column's window belongs to this CTA alone: rewrite it from
+    // the registers, once the request is known valid (the inputs' registers
+    // hold it from here: 128-thread tiles load the first chunk in the
+    // prologue; the 256-thread ones do so in the loop, and rewrite it there)
+    auto conv_v_store = [&]() {
+        if constexpr (CONV) {
+            if (tid < vcols) {
+                const auto& cp = p.conv;
+                const int vc = 2 * p.hqk * KK + h * p.v + cb * BV + tid;
+                sconv_window_store_regs(static_cast<QT*>(cp.window) + (int64_t)cslot * cp.slot_stride + vc, cp.C,
+                                        cp.L, cp.KW, cacc + cp.KW - 1, Tn, rst, zv, xv);
+            }
+        }
+    };
+    if constexpr (PRO_INPUTS) conv_v_store();
 
     // the carry as pairs of adjacent columns: each pair's update is one packed
     // fp32 FMA (two fmaf with their own rounding, the same results)
@@ -457,6 +534,9 @@ kda_verify_kernel(const __grid_constant__ CUtensorMap tmap, const StepParams p) 
         // CONV: one chunk (the host refuses longer requests), so the conv's
         // history and weights die with the first call
         if (CONV ? (t0 == 0 && !PRO_INPUTS) : (t0 > 0 || !PRO_INPUTS)) load_inputs(t0, tc);
+        if constexpr (!PRO_INPUTS) {
+            if (t0 == 0) conv_v_store();
+        }
         if (tid < tc) {
             bsm[tid] = __ldg(p.b + ((int64_t)tb + t0 + tid) * p.hv + h);
             snaps[tid] = final_mode ? -1 : p.snap_slot[(int64_t)n * p.snap_stride + t0 + tid];
@@ -790,21 +870,17 @@ kda_verify_kernel(const __grid_constant__ CUtensorMap tmap, const StepParams p) 
         // the next chunk rewrites the gates, d and the token scalars
         __syncthreads();
     }
-    // CONV: the windows' update, all threads together.  A value column's
-    // window belongs to this CTA; a q/k channel's is read by every CTA of the
-    // request's value heads sharing the q/k head, and the one whose count
-    // completes it writes the new entries and puts the count back to zero.
-    // No CTA waits for another.  conv_prev < 0: not counted yet (a wait that
-    // ran out before the count).
+    // CONV: the q/k windows' update, all threads together (the value
+    // columns' were rewritten after the prologue).  A q/k channel's window is
+    // read by every CTA of the request's value heads sharing the q/k head, and
+    // the one whose count completes it writes the new entries and puts the
+    // count back to zero.  No CTA waits for another.  conv_prev < 0: not
+    // counted yet (a wait that ran out before the count).
     if constexpr (CONV) {
         const auto& cp = p.conv;
-        const int m = col + cp.KW - 1, kept = max(0, cp.L - Tn), readers = (p.hv / p.hqk) * vt;
+        const int m = col + cp.KW - 1, readers = (p.hv / p.hqk) * vt;
         QT* W = static_cast<QT*>(cp.window) + (int64_t)cslot * cp.slot_stride;
         const QT* X = static_cast<const QT*>(cp.x) + (int64_t)tb * cp.C;
-        if (tid < vcols) {
-            const int vc = 2 * p.hqk * KK + h * p.v + cb * BV + tid;
-            sconv_window_store(W + vc, X + vc, cp.C, cp.L, m, kept, Tn, rst);
-        }
         bool last = true;
         if (readers > 1) {
             int* flag = snaps + TC - 1;  // the last token's snapshot id is no longer needed
@@ -818,11 +894,8 @@ kda_verify_kernel(const __grid_constant__ CUtensorMap tmap, const StepParams p) 
             __syncthreads();
             last = *flag != 0;
         }
-        if (last && rowt < KK && half == 0) {
-            const int qc = hq * KK + rowt, kc = (p.hqk + hq) * KK + rowt;
-            sconv_window_store(W + qc, X + qc, cp.C, cp.L, m, kept, Tn, rst);
-            sconv_window_store(W + kc, X + kc, cp.C, cp.L, m, kept, Tn, rst);
-        }
+        if (last && rowt < KK && half == 0)
+            sconv_window_store2(W, X, hq * KK + rowt, (p.hqk + hq) * KK + rowt, cp.C, cp.L, m, Tn, rst);
     }
     // prefill: the state after the last token, staged rounded in buffer 0 (free:
     // no snapshot store used it) and stored as one box
