@@ -170,3 +170,33 @@ def test_window_layout_errors():
     with pytest.raises(ValueError):   # history past the window: accepted index 5 of a 7-entry window
         oracle.conv_step(W, name, inp.conv_slot, inp.x.numpy(), inp.weight, inp.bias,
                          accepted=np.array([6], np.int32))
+
+
+@pytest.mark.parametrize("seed,lens,kw,spec", [(90, [5, 1, 3, 0, 5, 8, 2, 7], 4, 7), (91, [1, 1, 4], 3, 3),
+                                               (92, None, 2, 4), (93, [2, 0, 5], 4, 4)])
+def test_fused_step_inputs_obey_the_window_rule(seed, lens, kw, spec):
+    """The speculative fused-step inputs (make_step_conv) draw each request's
+    accepted index among the values its length admits: the kept old entries,
+    max(0, L - T_r), lie below acc + kw - 1.  The oracle's conv_step checks
+    that rule (it raises on a violation) and leaves padding requests' windows
+    alone, so it runs cleanly over the generated step and moves only the
+    windows of requests with tokens."""
+    inp = workloads.make_step_conv(n=len(lens) if lens else 6, num_spec=spec, t_lens=lens, kw=kw, h_qk=2, hv=4,
+                                   k=16, v=16, num_slots=80, num_wslots=12, seed=seed, pad_p=0.3)
+    L = kw - 1 + spec
+    t = [inp.max_t] * inp.slot_table.shape[0] if lens is None else lens
+    for r, tr in enumerate(t):
+        acc = int(inp.accepted[r]) - 1
+        assert 0 <= acc <= spec and max(0, L - tr) <= acc + kw - 1
+        pad = bool((inp.slot_table[r] < 0).all())
+        assert pad == (int(inp.conv_slot[r]) < 0)
+    W, name = storage(inp.window)
+    before = W.copy()
+    xs, _ = storage(inp.x)
+    oracle.conv_step(W, name, inp.conv_slot.numpy(), xs, inp.weight, inp.bias,
+                     cu_seqlens=None if inp.cu_seqlens is None else inp.cu_seqlens.numpy(),
+                     accepted=inp.accepted.numpy(), silu=True)
+    moved = {int(inp.conv_slot[r]) for r, tr in enumerate(t) if tr > 0 and int(inp.conv_slot[r]) >= 0}
+    for s in range(W.shape[0]):
+        if s not in moved:
+            assert np.array_equal(W[s], before[s]), f"window {s} changed"
