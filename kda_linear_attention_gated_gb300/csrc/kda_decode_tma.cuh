@@ -328,6 +328,16 @@ kda_decode_kernel(const __grid_constant__ CUtensorMap tmap, const StepParams p) 
                 Y[qc] = yq;
                 Y[kc] = yk;
             }
+            // the only reader of its q/k windows (one CTA a head, one value
+            // head a q/k head): rewrite them now, from the registers, as the
+            // value columns' are below; no count, no re-read at the end (two
+            // tiles a CTA only: the one-tile kernels have no registers to
+            // spare and do it at the end)
+            if (TPC > 1 && cgrp * ct == 1) {
+                QT* W = static_cast<QT*>(cp.window) + (int64_t)cslot * cp.slot_stride;
+                conv_window_store_kept(W + qc, cp.C, cp.L, cp.KW, hq_, xq);
+                conv_window_store_kept(W + kc, cp.C, cp.L, cp.KW, hk_, xk);
+            }
         }
 #pragma unroll
         for (int e = 0; e < NVE; ++e) {
@@ -358,6 +368,7 @@ kda_decode_kernel(const __grid_constant__ CUtensorMap tmap, const StepParams p) 
             // the tile loop)
             const int* meta = reinterpret_cast<const int*>(red);
             const int n = meta[7], hq = meta[11], readers = meta[15];
+            if (TPC > 1 && readers == 1) return;  // rewritten with the value columns'
             bool last = true;
             if (readers > 1) {
                 int* flag = reinterpret_cast<int*>(red) + 3;  // unused word of the norm area
